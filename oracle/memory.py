@@ -1,0 +1,209 @@
+"""Batch sanitising, ubatch splitting, KV cells, slot finding, masks and the context parameters.
+
+[P1] Крок 10 (llama_batch_allocr::init), Крок 12 (llama_kv_cache::init_batch), Крок 13а (apply);
+[P4] バッチパイプライン, KVキャッシュの詳細 (llama_kv_cells: pos, seq bitset, seq_pos), エラーリカバリ.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+from enum import IntEnum
+from typing import List, Optional, Sequence
+
+import numpy as np
+
+LLAMA_MAX_SEQ = 256   # reading: the pages name the limit LLAMA_MAX_SEQ without its value
+N_CTX_PAD = 256       # [P2] Example 9: n_ctx is rounded up to a multiple of 256 (GGML_PAD)
+
+
+class DecodeStatus(IntEnum):
+    """llama_decode return values ([P1] Крок 11; [P4] エラーリカバリ)."""
+    OK = 0
+    NO_KV_SLOT = 1        # no room in the cache for the batch: warning, state unchanged
+    ABORTED = 2           # the abort callback stopped the computation
+    INVALID_BATCH = -1
+    ALLOC_FAILED = -2     # also: internal error / no memory context
+    COMPUTE_FAILED = -3
+
+
+def derive_cparams(n_ctx: int, n_batch: int, n_ubatch: int, n_seq_max: int, causal: bool = True):
+    """Context sizes ([P1] Крок 9-10 context constructor; [P2] Example 9):
+    n_ctx rounded up to a multiple of 256; n_batch = min(n_ctx, n_batch) for a causal model;
+    n_ubatch = min(n_batch, n_ubatch). Returns (n_ctx, n_batch, n_ubatch) or None if invalid."""
+    if n_ctx <= 0 or n_batch <= 0 or n_ubatch <= 0 or not (1 <= n_seq_max <= LLAMA_MAX_SEQ):
+        return None
+    n_ctx = (n_ctx + N_CTX_PAD - 1) // N_CTX_PAD * N_CTX_PAD
+    if causal:
+        n_batch = min(n_ctx, n_batch)
+    n_ubatch = min(n_batch, n_ubatch)
+    return n_ctx, n_batch, n_ubatch
+
+
+@dataclass
+class Batch:
+    """A sanitised batch: every field filled in ([P1] Крок 10 llama_batch)."""
+    token: np.ndarray            # int32 [n]
+    pos: np.ndarray              # int32 [n]
+    seq_id: List[List[int]]      # per token, one or more sequence ids
+    output: np.ndarray           # bool [n]
+
+    @property
+    def n_tokens(self) -> int:
+        return len(self.token)
+
+
+class Cells:
+    """KV cells ([P4] KVキャッシュの詳細, llama_kv_cells): per cell a position (-1 = empty) and the
+    set of sequences using it (a cell can be shared)."""
+
+    def __init__(self, n_ctx: int):
+        self.pos = np.full(n_ctx, -1, dtype=np.int64)
+        self.seq: List[set] = [set() for _ in range(n_ctx)]
+
+    @property
+    def size(self) -> int:
+        return len(self.pos)
+
+    def copy(self) -> "Cells":
+        c = Cells(self.size)
+        c.pos = self.pos.copy()
+        c.seq = [set(s) for s in self.seq]
+        return c
+
+    def is_empty(self, c: int) -> bool:
+        return self.pos[c] < 0
+
+    def seq_pos_max(self, s: int) -> int:
+        """Largest position held for sequence s, -1 if none ([P1] KV-cache section)."""
+        ps = [int(self.pos[c]) for c in range(self.size) if s in self.seq[c]]
+        return max(ps) if ps else -1
+
+    def seq_pos_min(self, s: int) -> int:
+        ps = [int(self.pos[c]) for c in range(self.size) if s in self.seq[c]]
+        return min(ps) if ps else -1
+
+    def seq_rm(self, s: int, p0: int, p1: int) -> bool:
+        """Remove sequence s from the cells with p0 <= pos < p1 ([P4] エラーリカバリ, seq_rm).
+
+        reading: p0 < 0 means 0 and p1 < 0 means no upper bound (the rollback calls
+        seq_rm(s, pos_min, -1) to drop everything from pos_min on); s < 0 means every sequence.
+        A cell whose sequence set becomes empty is freed (pos = -1)."""
+        if p0 < 0:
+            p0 = 0
+        if p1 < 0:
+            p1 = np.iinfo(np.int64).max
+        for c in range(self.size):
+            if self.pos[c] < 0 or not (p0 <= self.pos[c] < p1):
+                continue
+            if s < 0:
+                self.seq[c].clear()
+            else:
+                self.seq[c].discard(s)
+            if not self.seq[c]:
+                self.pos[c] = -1
+        return True
+
+    def find_slots(self, n: int) -> Optional[List[int]]:
+        """reading ("contiguous, or at least available" cells, [P4] KVキャッシュの詳細): the n
+        lowest-index empty cells, in ascending order; None if fewer than n are empty."""
+        free = [c for c in range(self.size) if self.pos[c] < 0]
+        return free[:n] if len(free) >= n else None
+
+    def apply(self, slots: Sequence[int], pos: Sequence[int], seq_ids: Sequence[Sequence[int]]):
+        """mctx->apply(): write each token's position and sequence ids into its cell
+        ([P1] Крок 13а; [P4] process_ubatch: the only point where memory changes)."""
+        for c, p, ss in zip(slots, pos, seq_ids):
+            assert self.pos[c] < 0, "slot must be empty"
+            self.pos[c] = int(p)
+            self.seq[c] = set(int(s) for s in ss)
+
+    def n_kv(self) -> int:
+        """Cells the attention reads: highest used cell + 1 (reading of the 'recount' in apply)."""
+        used = np.nonzero(self.pos >= 0)[0]
+        return int(used[-1]) + 1 if len(used) else 0
+
+    def mask(self, pos: Sequence[int], seq_ids: Sequence[Sequence[int]], n_kv: int) -> np.ndarray:
+        """The KQ mask as booleans [T, n_kv] (True = visible).
+
+        reading: token t may see cell c iff c holds a position, c shares a sequence with t, and
+        c.pos <= pos(t) (causal); cells written by the same ubatch are included, because apply()
+        and the K/V writes come before the attention ([P1] KV-cache section: K and V are appended
+        first, then Q is multiplied by every key in the cache, including the current one)."""
+        T = len(pos)
+        m = np.zeros((T, n_kv), dtype=bool)
+        for t in range(T):
+            st = set(int(s) for s in seq_ids[t])
+            for c in range(n_kv):
+                if self.pos[c] >= 0 and (self.seq[c] & st) and self.pos[c] <= pos[t]:
+                    m[t, c] = True
+        return m
+
+
+def sanitize_batch(token, pos, n_seq_id, seq_id, logits, *, n_vocab: int, n_seq_max: int,
+                   n_batch: int, cells: Optional[Cells], output_all: bool = False) -> Optional[Batch]:
+    """llama_batch_allocr::init ([P1] Крок 10): validate, then fill the fields left as None.
+
+    Invalid (returns None, which llama_decode turns into -1): no tokens; more than n_batch tokens;
+    a token id outside [0, n_vocab); a sequence id outside [0, n_seq_max); a token with no
+    sequence id.
+    Defaults: seq_id None -> every token in sequence 0; pos None -> each sequence continues from
+    seq_pos_max(s) + 1 in batch order (0 if there is no memory), and a token moves every one of its
+    sequences past its position; logits None -> only the last token (all tokens if output_all).
+    reading (the elided consistency checks): for each sequence, its positions in the batch must be
+    consecutive in batch order and start at seq_pos_max(s) + 1; otherwise the batch is invalid.
+    """
+    n = 0 if token is None else len(token)
+    if n <= 0 or n > n_batch:
+        return None
+    token = np.asarray(token, dtype=np.int64)
+    if np.any(token < 0) or np.any(token >= n_vocab):
+        return None
+    if seq_id is None:
+        sids = [[0] for _ in range(n)]
+    else:
+        sids = []
+        for i in range(n):
+            k = 1 if n_seq_id is None else int(n_seq_id[i])
+            if k < 1:
+                return None
+            ss = [int(s) for s in seq_id[i][:k]]
+            if any(s < 0 or s >= n_seq_max for s in ss):
+                return None
+            sids.append(ss)
+    p0 = {}
+    if pos is None:
+        out_pos = np.zeros(n, dtype=np.int64)
+        nxt = [0 if cells is None else cells.seq_pos_max(s) + 1 for s in range(n_seq_max)]
+        for i in range(n):
+            out_pos[i] = nxt[sids[i][0]]
+            for s in sids[i]:
+                nxt[s] = out_pos[i] + 1
+    else:
+        out_pos = np.asarray(pos, dtype=np.int64).copy()
+    # consistency: per sequence, consecutive positions continuing the memory
+    last = {}
+    for i in range(n):
+        for s in sids[i]:
+            if s not in last:
+                start = 0 if cells is None else cells.seq_pos_max(s) + 1
+                if out_pos[i] != start:
+                    return None
+            elif out_pos[i] != last[s] + 1:
+                return None
+            last[s] = out_pos[i]
+    if logits is None:
+        out = np.zeros(n, dtype=bool)
+        if output_all:
+            out[:] = True
+        else:
+            out[-1] = True
+    else:
+        out = np.asarray(logits).astype(bool).copy()
+        if output_all:
+            out[:] = True
+    return Batch(token.astype(np.int32), out_pos.astype(np.int32), sids, out)
+
+
+def split_simple(n_tokens: int, n_ubatch: int) -> List[range]:
+    """split_simple ([P1] Крок 12): the next at most n_ubatch unused tokens of the batch, in batch
+    order, until the batch is used up. Returns the token ranges of the ubatches."""
+    return [range(i, min(i + n_ubatch, n_tokens)) for i in range(0, n_tokens, n_ubatch)]
