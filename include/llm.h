@@ -1,0 +1,257 @@
+/*
+ * llm.h - C ABI of a single-GPU (sm_103a) decode library for Llama-architecture GQA transformers
+ * with a KV cache: llama_decode's processing of a batch, split into ubatches, through token
+ * embedding, per-layer RMSNorm / Q,K,V projections / RoPE / K,V append into the cache /
+ * grouped-query attention over the cache / output projection / SwiGLU FFN, then the final norm,
+ * logits for the flagged positions and a greedy pick.
+ *
+ * Sources (page title, section):
+ *   [P1] "llama.cpp AI LLM Engine - Як це працює": Крок 10 (llama_batch, batch_allocr::init),
+ *        Крок 11 (llama_decode and its return values), Крок 12 (init_batch: split and slot search),
+ *        Крок 13а-13в (process_ubatch: apply, graph, set_inputs, compute), Крок 14
+ *        (llama_get_logits_ith), KV-cache section (seq_pos_max, K/V appended before attention).
+ *   [P2] "llama.cpp Architecture": Example 2 (ggml shapes {ne0 = row length, ne1 = rows}, Q8_0
+ *        blocks), Example 4 (tensor names and shapes of one decode step), Example 8-10 (hparams,
+ *        context parameters, n_ctx padded to 256, KV sizes).
+ *   [P4] "デコードループ：バッチ処理、KVキャッシュ、メモリ管理": バッチパイプライン, KVキャッシュの詳細
+ *        (cells, slot_info), エラーリカバリとステートロールバック (apply/rollback, return codes).
+ *
+ * Conventions for every call:
+ *   - Pointers named "host" are CPU memory; "device" pointers are CUDA device memory of the GPU the
+ *     context was created on. Where either is accepted this is stated.
+ *   - The library never keeps a pointer the caller passed in after the call returns, except the
+ *     CUDA stream given to llm_ctx_init.
+ *   - Errors are reported by return value and never abort the process. llm_last_error() gives a
+ *     one-line description of the most recent failure of a context.
+ *   - A context is not thread-safe: calls on one context must not overlap.
+ */
+#ifndef LLM_H
+#define LLM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Storage types of weights and cache rows ([P2] Example 2). Q8_0: blocks of 32 values stored as
+ * a 2-byte little-endian fp16 scale d followed by 32 int8 quants q (34 bytes); value = d * q; a
+ * row holds a whole number of blocks. BF16: the top 16 bits of an IEEE float32. */
+typedef enum {
+    LLM_TYPE_F32  = 0,
+    LLM_TYPE_F16  = 1,
+    LLM_TYPE_BF16 = 2,
+    LLM_TYPE_Q8_0 = 8
+} llm_type;
+
+/* Model hyper-parameters ([P2] Example 8, print_info). head_dim * n_head is the width of the Q
+ * projection; n_head must be a multiple of n_head_kv (n_gqa = n_head / n_head_kv query heads
+ * share one KV head: query head h reads KV head h / n_gqa). rope_type 0 is the "normal" layout
+ * (adjacent element pairs); it is the only one supported. */
+typedef struct llm_hparams {
+    int32_t n_layer;
+    int32_t n_embd;
+    int32_t n_head;
+    int32_t n_head_kv;
+    int32_t head_dim;
+    int32_t n_ff;
+    int32_t n_vocab;
+    float   rope_freq_base;
+    float   rms_eps;
+    int32_t rope_type;
+} llm_hparams;
+
+/* Context flags. */
+enum {
+    /* Book-keeping only: batches are sanitised, split, given KV slots and committed, but no device
+     * memory is allocated and no kernel runs; llm_get_logits_ith returns NULL. Lets the host
+     * control plane be tested on a machine without a GPU. */
+    LLM_CTX_HOST_ONLY = 1u << 0,
+};
+
+/* Context parameters ([P1] Крок 9-10 context constructor; [P2] Example 9; [P4] コンテキストの構築).
+ * n_ctx is rounded up to a multiple of 256; n_batch becomes min(n_ctx, n_batch) and n_ubatch
+ * min(n_batch, n_ubatch). type_k / type_v: LLM_TYPE_F32 or LLM_TYPE_F16. stream: a cudaStream_t
+ * the library launches all its work on (NULL = the library creates its own non-blocking stream).
+ * The KV cache is unified: one set of n_ctx cells shared by all n_seq_max sequences. */
+typedef struct llm_cparams {
+    uint32_t n_ctx;
+    uint32_t n_seq_max;      /* 1 .. 256 */
+    uint32_t n_batch;
+    uint32_t n_ubatch;
+    int32_t  type_k;
+    int32_t  type_v;
+    void    *stream;
+    uint32_t flags;
+} llm_cparams;
+
+/* A batch ([P1] Крок 10, llama_batch). Arrays have n_tokens entries and are host memory owned by
+ * the caller; llm_decode copies what it needs before returning. Fields may be NULL:
+ *   pos NULL      -> each sequence continues from llm_seq_pos_max(s) + 1, in batch order;
+ *   seq_id NULL   -> every token belongs to sequence 0 (n_seq_id is then ignored);
+ *   n_seq_id NULL -> one sequence id per token (seq_id[i][0]);
+ *   logits NULL   -> logits only for the last token.
+ * logits[i] != 0 requests the logits row of token i. */
+typedef struct llm_batch {
+    int32_t               n_tokens;
+    const int32_t        *token;
+    const int32_t        *pos;
+    const int32_t        *n_seq_id;
+    const int32_t *const *seq_id;
+    const int8_t         *logits;
+} llm_batch;
+
+typedef struct llm_ctx llm_ctx;
+
+/* Defaults: n_ctx 4096, n_seq_max 1, n_batch 2048, n_ubatch 512, F16 K and V, own stream. */
+llm_cparams llm_cparams_default(void);
+
+/* Create a context: validates hp and cp, allocates the device weight store, the KV cache
+ * ([P1] KV-cache section: per layer one K and one V buffer for all n_ctx cells), every scratch
+ * buffer a ubatch of n_ubatch tokens needs and the output buffers, so llm_decode allocates
+ * nothing in the common case. Returns NULL on invalid parameters or failed allocation
+ * (llm_last_error(NULL) then describes the failure). */
+llm_ctx *llm_ctx_init(const llm_hparams *hp, const llm_cparams *cp);
+
+/* Release every resource of the context (waits for its stream first). NULL is a no-op. */
+void llm_ctx_free(llm_ctx *ctx);
+
+/* Copy one named tensor into the device weight store ([P2] Example 4 names and shapes):
+ *   token_embd.weight {n_embd, n_vocab}, output_norm.weight {n_embd},
+ *   output.weight {n_embd, n_vocab} (optional: absent = tied to token_embd),
+ *   blk.N.attn_norm.weight {n_embd}, blk.N.attn_q.weight {n_embd, n_head*head_dim},
+ *   blk.N.attn_k.weight / attn_v.weight {n_embd, n_head_kv*head_dim},
+ *   blk.N.attn_output.weight {n_head*head_dim, n_embd}, blk.N.ffn_norm.weight {n_embd},
+ *   blk.N.ffn_gate.weight / ffn_up.weight {n_embd, n_ff}, blk.N.ffn_down.weight {n_ff, n_embd}.
+ * ne[0] is the row length and ne[1] the number of rows (1 for vectors), ggml order. data holds
+ * the rows in storage type `type`, nbytes long; it may be host or device memory (any pointer
+ * CUDA's unified addressing resolves). Norm gains must be F32; linear weights F32, F16, BF16 or
+ * Q8_0 (Q8_0 needs ne[0] % 32 == 0); the three of attn_q/k/v of one layer must share a type,
+ * and so must ffn_gate/ffn_up. Returns 0 on success, -1 for an unknown name, a wrong shape, an
+ * unsupported type, a size mismatch or a second load of the same name, -2 on a CUDA failure.
+ * The call synchronises the device before reading data, so data written by earlier work on any
+ * stream is complete. */
+int llm_load_weights(llm_ctx *ctx, const char *name, int32_t type, const int64_t ne[2],
+                     const void *data, size_t nbytes);
+
+/* 0 if every required tensor is loaded, else -1 (llm_last_error names the first missing one). */
+int llm_weights_ready(llm_ctx *ctx);
+
+/* Decode a batch ([P1] Крок 11-13; [P4] process_ubatch). Steps: sanitise and fill defaults; split
+ * into ubatches of at most n_ubatch tokens in batch order; find KV cells for every ubatch before
+ * committing any (each ubatch takes the lowest-index empty cells, ascending); then per ubatch:
+ * commit its cells, run the forward pass on the device (K/V of the ubatch are written to the cache
+ * before the attention reads it) and append the flagged tokens' logits rows in batch order.
+ * Returns:
+ *    0  success
+ *    1  no KV slot for the batch: nothing was changed
+ *    2  aborted by the abort callback (checked before each ubatch's compute); the current ubatch
+ *       is rolled back, earlier ubatches stay in the cache
+ *   -1  invalid batch (no tokens, more than n_batch tokens, a token id outside [0, n_vocab), a
+ *       sequence id outside [0, n_seq_max), positions of a sequence that are not consecutive or
+ *       do not continue from llm_seq_pos_max + 1), or weights not ready
+ *   -2  internal / allocation failure
+ *   -3  the device computation failed (a CUDA error or a kernel's own bounds check); the current
+ *       ubatch is rolled back: seq_rm(s, pos_min(s), -1) for each of its sequences
+ * After a non-zero return no logits are readable. The call returns when the device work has
+ * finished. */
+int32_t llm_decode(llm_ctx *ctx, llm_batch batch);
+
+/* Logits row of the last llm_decode ([P1] Крок 14): i >= 0 is a token index of that batch, i < 0
+ * counts from the last output row (-1 = last). Returns a host pointer to n_vocab floats owned by
+ * the context and valid until the next llm_decode or llm_ctx_free; NULL if i names a token whose
+ * logits were not requested, is out of range, or the context is host-only. The first call after a
+ * decode copies the output rows from the device. */
+float *llm_get_logits_ith(llm_ctx *ctx, int32_t i);
+
+/* Greedy pick of the same row, computed on the device (the largest logit; the lowest index among
+ * equal maxima). -1 where llm_get_logits_ith would return NULL. Does not copy logits rows. */
+int32_t llm_get_argmax_ith(llm_ctx *ctx, int32_t i);
+
+/* Number of output rows of the last successful llm_decode. */
+int32_t llm_n_outputs(llm_ctx *ctx);
+
+/* Remove sequence seq from the cells holding positions p0 <= pos < p1 ([P4] llama_memory_i::seq_rm,
+ * エラーリカバリ); p0 < 0 means 0, p1 < 0 means no upper bound, seq < 0 means every sequence.
+ * Cells left with no sequence become empty and are reused by later batches. Returns 1. */
+int llm_seq_rm(llm_ctx *ctx, int32_t seq, int32_t p0, int32_t p1);
+
+/* Largest / smallest position held for a sequence, -1 if it holds none ([P1] KV-cache section). */
+int32_t llm_seq_pos_max(llm_ctx *ctx, int32_t seq);
+int32_t llm_seq_pos_min(llm_ctx *ctx, int32_t seq);
+
+/* Abort callback ([P1] Крок 11, return value 2): called before each ubatch's computation; a
+ * non-zero return aborts the decode with 2. NULL removes it. */
+void llm_set_abort_callback(llm_ctx *ctx, int (*cb)(void *user), void *user);
+
+/* Effective context sizes after rounding / clamping. */
+uint32_t llm_n_ctx(llm_ctx *ctx);
+uint32_t llm_n_batch(llm_ctx *ctx);
+uint32_t llm_n_ubatch(llm_ctx *ctx);
+
+/* Number of cells holding a position. */
+int32_t llm_kv_used_cells(llm_ctx *ctx);
+
+/* One-line description of the last failure of ctx (or of the last failed llm_ctx_init when ctx is
+ * NULL). The string is owned by the library. */
+const char *llm_last_error(llm_ctx *ctx);
+
+/* Timing counters ([P2] Example 11-12, llama_perf_context_print): decode calls, tokens, ubatches,
+ * CUDA-graph replays, and host milliseconds spent inside llm_decode. */
+typedef struct llm_perf_data {
+    int64_t n_decode_calls;
+    int64_t n_tokens;
+    int64_t n_ubatches;
+    int64_t n_graph_replays;
+    double  t_decode_ms;
+} llm_perf_data;
+void llm_perf(llm_ctx *ctx, llm_perf_data *out);
+
+/* ---- test and debugging hooks ---------------------------------------------------------------
+ * They expose intermediate state so tests can compare it with an independent implementation
+ * (the eval-callback idea of [P2] Example 4). */
+
+/* KV cell index of every token of the last llm_decode (slot_info, [P4] KVキャッシュの詳細), in batch
+ * order. Writes min(cap, n) values to out (host) and returns n. */
+int32_t llm_debug_last_slots(llm_ctx *ctx, int32_t *out, int32_t cap);
+
+/* Attention visibility of ubatch `ub` of the last llm_decode as the library computed it, expanded
+ * to a dense [n_tokens][n_kv] row-major byte matrix (1 = token may attend to the cell) on the host.
+ * n_kv is the highest used cell + 1 after that ubatch's commit. Returns n_tokens * n_kv (0 if ub
+ * is out of range); writes at most cap bytes. *n_kv_out receives n_kv. */
+int64_t llm_debug_ubatch_mask(llm_ctx *ctx, int32_t ub, uint8_t *out, int64_t cap,
+                              int32_t *n_kv_out);
+
+/* Keep copies of per-layer intermediates of the last ubatch (enable != 0) on the device. */
+int llm_debug_capture(llm_ctx *ctx, int enable);
+
+/* Copy a captured intermediate of the last ubatch to host memory as float32, row-major
+ * [n_tokens][width]. name: "embd" (layer ignored), "l_out" (residual stream after layer `layer`),
+ * "attn_out" (attention output of layer `layer`, before the output projection), "kq_in" (the Q
+ * rows after RoPE of layer `layer`), "result_norm" (final-normed output rows). Returns the number
+ * of floats available (0 if none), writes at most cap. */
+int64_t llm_debug_get_tensor(llm_ctx *ctx, const char *name, int32_t layer, float *out,
+                             int64_t cap);
+
+/* Per-kernel-class device timing. enable != 0 resets the counters and brackets every later launch
+ * with CUDA events on the context's stream (small overhead); 0 stops. */
+int llm_debug_kernel_timing(llm_ctx *ctx, int enable);
+
+/* Counters of kernel class i (0 <= i < the returned count): its name (NUL-terminated, at most
+ * name_cap bytes), launches, summed device milliseconds, and the summed algorithmic bytes moved
+ * and FLOPs of those launches (the minimum a launch must read and write, and its arithmetic).
+ * Any output pointer may be NULL. Returns the number of classes. */
+int32_t llm_debug_kernel_stats(llm_ctx *ctx, int32_t i, char *name, int32_t name_cap,
+                               int64_t *launches, double *ms, double *bytes, double *flops);
+
+/* Fault injection: kind 1 makes ubatch `ub` of the next llm_decode hand the K/V append kernel a
+ * cell index past the cache; the kernel's bounds check skips the write and reports the error
+ * word, so llm_decode returns -3 and rolls that ubatch back. kind 0 clears it. */
+int llm_debug_inject_fault(llm_ctx *ctx, int32_t kind, int32_t ub);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LLM_H */

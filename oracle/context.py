@@ -108,8 +108,9 @@ def output_logits(w: OracleWeights, hp, x_rows: np.ndarray) -> np.ndarray:
 class OracleContext:
     """A llama context: a unified KV cache of n_ctx cells, the batch allocator and the outputs."""
 
-    def __init__(self, hp, weights: OracleWeights, n_ctx: int, n_seq_max: int = 1,
-                 type_k: int = F16, type_v: int = F16, n_batch: int = 2048, n_ubatch: int = 512):
+    def __init__(self, hp, weights: Optional[OracleWeights], n_ctx: int, n_seq_max: int = 1,
+                 type_k: int = F16, type_v: int = F16, n_batch: int = 2048, n_ubatch: int = 512,
+                 compute: bool = True):
         cp = derive_cparams(n_ctx, n_batch, n_ubatch, n_seq_max)
         if cp is None:
             raise ValueError("invalid context parameters")
@@ -118,9 +119,11 @@ class OracleContext:
         self.n_seq_max = n_seq_max
         self.type_k, self.type_v = type_k, type_v
         self.cells = Cells(self.n_ctx)
+        self.compute = compute      # False: batch / cell bookkeeping only, no forward pass
         kvd = (hp.n_head_kv, hp.head_dim)
-        self.K = [np.zeros((self.n_ctx,) + kvd) for _ in range(hp.n_layer)]
-        self.V = [np.zeros((self.n_ctx,) + kvd) for _ in range(hp.n_layer)]
+        n_k = hp.n_layer if compute else 0
+        self.K = [np.zeros((self.n_ctx,) + kvd) for _ in range(n_k)]
+        self.V = [np.zeros((self.n_ctx,) + kvd) for _ in range(n_k)]
         self.abort_callback: Optional[Callable[[], bool]] = None
         self.fail_at_ubatch: Optional[int] = None      # test hook: ubatch whose compute fails
         self.output_all = False
@@ -220,6 +223,8 @@ class OracleContext:
         visible = self.cells.mask(upos, useq, n_kv)
         self.last_ubatches.append({"slots": list(slots), "n_kv": n_kv, "mask": visible,
                                    "out_rows": list(out_rows), "pos": list(upos)})
+        if not self.compute:
+            return np.zeros((len(out_rows), hp.n_vocab))
         x = self.w.rows("token_embd.weight", tokens)                        # GET_ROWS
         slots = np.asarray(slots)
 

@@ -130,11 +130,13 @@ class Cells:
         first, then Q is multiplied by every key in the cache, including the current one)."""
         T = len(pos)
         m = np.zeros((T, n_kv), dtype=bool)
+        cpos = self.pos[:n_kv]
+        shares = {}                      # sequence set -> cells sharing one of its sequences
         for t in range(T):
-            st = set(int(s) for s in seq_ids[t])
-            for c in range(n_kv):
-                if self.pos[c] >= 0 and (self.seq[c] & st) and self.pos[c] <= pos[t]:
-                    m[t, c] = True
+            key = frozenset(int(s) for s in seq_ids[t])
+            if key not in shares:
+                shares[key] = np.array([bool(self.seq[c] & key) for c in range(n_kv)], dtype=bool)
+            m[t] = shares[key] & (cpos >= 0) & (cpos <= pos[t])
         return m
 
 

@@ -1,0 +1,140 @@
+"""GPU parity of the decode path on the tiny-model workloads, through the C ABI, against the oracle.
+
+Bar: logits within a max relative error of 1e-4 per row (F32 weights; the F16 KV cache is rounded
+identically on both sides); greedy tokens equal wherever the oracle's top-2 gap exceeds 1e-3;
+KV slot indices and attention masks bit-exact."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synthetic as S
+from oracle.context import forward_layers
+from oracle.formats import round_to_type
+from tests import gpu_common as G
+
+pytestmark = pytest.mark.gpu
+TOL = 1e-4
+
+
+def test_generator_is_device_independent():
+    for name, shape, wt in (("blk.0.attn_q.weight", (256, 256), S.BF16),
+                            ("blk.1.ffn_gate.weight", (256, 704), S.Q8_0),
+                            ("output.weight", (256, 4096), S.F32)):
+        a = S.weight_bytes(77, name, shape, wt, "cpu")
+        b = S.weight_bytes(77, name, shape, wt, "cuda").cpu()
+        assert torch.equal(a.view(torch.uint8), b.view(torch.uint8)), name
+    assert torch.equal(S.prompt_tokens(5, 999, 151936, "cpu"), S.prompt_tokens(5, 999, 151936, "cuda").cpu())
+
+
+def test_tiny_1seq_prompt_and_32_greedy_steps():
+    key = "tiny_f32_1seq"
+    w = S.WORKLOADS[key]
+    ctx, ora = G.library_ctx(key), G.oracle_ctx(key)
+    toks = G.prompts(key)[0]
+    assert ctx.decode(toks) == 0, ctx.last_error()
+    assert ora.decode(toks) == 0
+    assert ctx.last_slots().tolist() == list(range(w.n_prompt))
+    rep = G.greedy_compare(ctx, ora, 1, [w.n_prompt - 1], w.n_decode, TOL, {})
+    assert rep["tokens_checked"] >= w.n_decode // 2
+    assert ctx.seq_pos_max(0) == w.n_prompt + w.n_decode - 1
+    ctx.free()
+
+
+def test_tiny_8seq_batched_prompt_and_greedy_steps():
+    key = "tiny_f32_8seq"
+    w = S.WORKLOADS[key]
+    ctx, ora = G.library_ctx(key), G.oracle_ctx(key)
+    ctx.debug_capture(True)
+    toks, seqs, flags = G.prompt_batch(key)
+    assert ctx.decode(toks, seq_ids=seqs, logits=flags) == 0, ctx.last_error()
+    assert ora.decode(toks, seq_id=seqs, n_seq_id=[1] * len(toks), logits=flags) == 0
+    assert ctx.n_outputs == w.n_seq
+    slots = [s for u in ora.last_ubatches for s in u["slots"]]
+    assert ctx.last_slots().tolist() == slots
+    for k, u in enumerate(ora.last_ubatches):
+        assert np.array_equal(ctx.ubatch_mask(k), u["mask"]), k
+    rows = [(s + 1) * w.n_prompt - 1 for s in range(w.n_seq)]
+    rep = G.greedy_compare(ctx, ora, w.n_seq, rows, 32, TOL, {})
+    assert rep["tokens_checked"] >= 100
+    ctx.free()
+
+
+def test_tiny_layer_outputs_match_oracle_layer_by_layer():
+    key = "tiny_f32_1seq"
+    w = S.WORKLOADS[key]
+    hp = w.hp
+    ctx = G.library_ctx(key)
+    ctx.debug_capture(True)
+    toks = G.prompts(key)[0][:20]
+    assert ctx.decode(toks, logits=[1] * 20) == 0
+    ow = G.oracle_weights(key)
+    pos = np.arange(20)
+    causal = np.tril(np.ones((20, 20), dtype=bool))
+    x = ow.rows("token_embd.weight", toks)
+    got = ctx.debug_tensor("embd").reshape(20, hp.n_embd)
+    assert np.max(np.abs(got - x)) == 0.0
+    for il in range(hp.n_layer):
+        store = {}
+
+        def kv_write(_il, k, v):
+            store["kv"] = (round_to_type(k, w.type_kv), round_to_type(v, w.type_kv))
+
+        def kv_read(_il):
+            return store["kv"][0], store["kv"][1], causal
+        x = forward_layers(ow, hp, x, pos, kv_write, kv_read, layers=[il])
+        got = ctx.debug_tensor("l_out", il).reshape(20, hp.n_embd)
+        e = np.max(np.abs(got - x)) / np.max(np.abs(x))
+        assert e < 1e-5, (il, e)
+    ctx.free()
+
+
+def test_ubatch_split_and_sequence_isolation_on_gpu():
+    key = "tiny_f32_8seq"
+    w = S.WORKLOADS[key]
+    toks, seqs, flags = G.prompt_batch(key)
+    n = 2 * w.n_prompt
+    ref = None
+    for nub in (128, 37, 5):
+        ctx = G.library_ctx(key, n_ubatch=nub)
+        assert ctx.decode(toks[:n], seq_ids=seqs[:n], logits=[1] * n) == 0
+        out = np.stack([ctx.get_logits_ith(i) for i in range(n)])
+        if ref is None:
+            ref = out
+        else:
+            assert np.max(np.abs(out - ref)) / np.max(np.abs(ref)) < 1e-5, nub
+        ctx.free()
+    # sequence 1 alone gives the same logits as inside the batch
+    ctx = G.library_ctx(key)
+    p1 = G.prompts(key)[1]
+    assert ctx.decode(p1, logits=[1] * w.n_prompt) == 0
+    alone = np.stack([ctx.get_logits_ith(i) for i in range(w.n_prompt)])
+    assert np.max(np.abs(alone - ref[w.n_prompt:])) / np.max(np.abs(ref)) < 1e-5
+    ctx.free()
+
+
+def test_error_paths_on_gpu():
+    key = "tiny_f32_1seq"
+    ctx = G.library_ctx(key, n_ctx=256, n_batch=256, n_ubatch=16)
+    toks = G.prompts(key)[0]
+    # a bad cell index planted for ubatch 1: the kernel's bounds check reports it, -3, rollback
+    ctx.inject_fault(1, 1)
+    assert ctx.decode(toks) == -3
+    assert ctx.seq_pos_max(0) == 15 and ctx.kv_used_cells() == 16
+    assert ctx.get_logits_ith(-1) is None
+    # the cache still works and continues from the kept ubatch
+    assert ctx.decode(toks[16:]) == 0, ctx.last_error()
+    ref = G.library_ctx(key, n_ctx=256, n_batch=256, n_ubatch=16)
+    assert ref.decode(toks) == 0
+    assert G.rel_err(ctx.get_logits_ith(-1), ref.get_logits_ith(-1).astype(np.float64)) < 1e-6
+    # abort before the second ubatch
+    calls = []
+    ref.set_abort_callback(lambda: (calls.append(1), len(calls) == 2)[1])
+    assert ref.decode(toks[:20]) == 2
+    assert ref.seq_pos_max(0) == 31 + 16
+    ref.set_abort_callback(None)
+    # a full cache returns 1 and changes nothing
+    used = ref.kv_used_cells()
+    assert ref.decode(np.zeros(256 - used + 1, dtype=np.int32)) in (1, -1)
+    assert ref.kv_used_cells() == used
+    ctx.free(); ref.free()

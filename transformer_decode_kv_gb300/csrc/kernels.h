@@ -1,0 +1,95 @@
+// Launchers of the decode path's CUDA kernels (sm_103a). All pointers are device pointers; every
+// launcher enqueues on `st` and returns immediately.
+#pragma once
+
+#include <cstdint>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+namespace llm {
+
+enum WType : int32_t { W_F32 = 0, W_F16 = 1, W_BF16 = 2, W_Q8_0 = 8 };
+
+// A weight matrix in the device store: `rows` rows of `cols` values, row-major. Q8_0 is kept as
+// int8 quants [rows][cols] plus fp16 scales [rows][cols / 32] (the same bytes as the file's
+// 34-byte blocks, split so each part can be read with aligned vector loads).
+struct DevMat {
+    int32_t type = -1;
+    int64_t rows = 0, cols = 0;
+    void* data = nullptr;
+    __half* scales = nullptr;
+};
+
+// Device error word bits, set by kernels' own bounds checks.
+enum : uint32_t { ERR_SLOT_RANGE = 1u, ERR_TOKEN_RANGE = 2u, ERR_ROW_RANGE = 4u };
+
+// ---- elementwise / small kernels (kernels_misc.cu) --------------------------------------------
+// x[t] = row tok[t] of the embedding table, as float32 ([P2] Example 4, GET_ROWS).
+void launch_embed(const DevMat& E, const int32_t* tok, int32_t T, float* x, uint32_t* err,
+                  cudaStream_t st);
+// y[r] = x[rows ? rows[r] : r] / sqrt(mean(x^2) + eps) * g, r < R, width d (RMS_NORM + MUL).
+void launch_rmsnorm(const float* x, const int32_t* rows, int32_t R, int32_t d, const float* g,
+                    float eps, float* y, cudaStream_t st);
+// cos/sin of pos[t] * base^(-2i/hd) for i < hd/2, computed in double: cs[t][i] = {cos, sin}.
+void launch_rope_table(const int32_t* pos, int32_t T, int32_t hd, float base, float2* cs,
+                       cudaStream_t st);
+// RoPE (adjacent pairs) on the q and k parts of qkv [T][(H + 2 Hkv) hd] (q in place), then K and
+// V rows written to their cache cells slot[t] ([P2] Example 4, ROPE + SET_ROWS). Cache layout:
+// [Hkv][n_ctx][hd], element type kv_type (F32 or F16). A slot outside [0, n_ctx) skips the write
+// and sets ERR_SLOT_RANGE.
+void launch_rope_kv_append(float* qkv, int32_t T, int32_t H, int32_t Hkv, int32_t hd,
+                           const float2* cs, const int32_t* slot, void* kc, void* vc,
+                           int32_t n_ctx, int32_t kv_type, uint32_t* err, cudaStream_t st);
+// u[t][j] = silu(g[t][j]) * up[t][j] with gu = [T][2F] (gate then up) -> u [T][F].
+void launch_swiglu(const float* gu, int32_t T, int32_t F, float* u, cudaStream_t st);
+// idx[r] = argmax of logits row r (lowest index among equal maxima).
+void launch_argmax(const float* logits, int32_t R, int32_t V, int32_t* idx, cudaStream_t st);
+// Split Q8_0 blocks (34 bytes: fp16 d, 32 int8 q) into quants [rows][cols] and scales.
+void launch_q8_0_unpack(const uint8_t* blocks, int64_t rows, int64_t cols, int8_t* q,
+                        __half* d, cudaStream_t st);
+
+// ---- linear layers (kernels_linear.cu) --------------------------------------------------------
+enum Epi : int32_t { EPI_STORE = 0, EPI_ADD = 1 };
+// y[t][m] (op)= sum_k W[row0 + m][k] x[t][k], m < M, t < T ([P2] Example 4, MUL_MAT; ADD for the
+// residual). x row stride ldx, y row stride ldy.
+void launch_linear(const DevMat& W, int64_t row0, int64_t M, const float* x, int32_t ldx,
+                   int32_t T, float* y, int32_t ldy, Epi epi, cudaStream_t st);
+// u[t][j] = silu(sum_k G[j][k] x[t][k]) * sum_k U[j][k] x[t][k] for the gate rows [0, F) and up
+// rows [F, 2F) of W ([P2] Example 4, ffn_gate, ffn_up, SWIGLU). tmp: [T][2F] scratch used when
+// the batched path computes the two projections before the product.
+void launch_linear_swiglu(const DevMat& W, int32_t F, const float* x, int32_t ldx, int32_t T,
+                          float* u, int32_t ldu, float* tmp, cudaStream_t st);
+// Largest T the GEMV path serves; larger T go through the tiled GEMM.
+int32_t gemv_max_tokens();
+
+// ---- attention (kernels_attention.cu) ---------------------------------------------------------
+constexpr int kAttnTileQ = 16;           // query tokens per attention tile
+// Shapes the attention kernels are built for.
+inline bool attention_supported(int hd, int n_gqa) {
+    return n_gqa == 4 && (hd == 32 || hd == 64 || hd == 128);
+}
+struct AttnArgs {
+    const float* q;          // qkv buffer; q of token t, head h at q[t * ldq + h * hd]
+    int32_t ldq;
+    const void* kc;          // this layer's K cache [Hkv][n_ctx][hd]
+    const void* vc;
+    int32_t n_ctx, kv_type, H, Hkv, hd;
+    const int32_t* tok_pos;  // [T]
+    const int32_t* list_off; const int32_t* list_cells; const int32_t* list_pos;
+    const int32_t* perm;     // [T] tokens grouped by list
+    const int32_t* tile_list; const int32_t* tile_start; const int32_t* tile_nq;
+    const int32_t* tile_wi_off;
+    const int32_t* wi_tile; const int32_t* wi_c0; const int32_t* wi_c1; const int32_t* wi_row_off;
+    float* part_o;           // [rows][Hkv][hd] unnormalised partial outputs
+    float* part_m;           // [rows][Hkv] running max (log2 domain)
+    float* part_l;           // [rows][Hkv] running sum
+    float* out;              // [T][H * hd]
+    int32_t ldo;
+    int32_t n_work, n_tiles, max_nq;
+};
+// Grouped-query attention of every token over the cells of its list with cell.pos <= token.pos:
+// split-K partial softmax per work item, then a combine per tile ([P2] Example 4 FLASH_ATTN_EXT;
+// Example 11 for the unfused meaning). Scale 1/sqrt(hd).
+bool launch_attention(const AttnArgs& a, cudaStream_t st);
+
+}  // namespace llm

@@ -1,0 +1,229 @@
+// Small kernels of the decode path: embedding gather, RMSNorm, RoPE table, RoPE + K/V append,
+// SwiGLU, greedy argmax and the Q8_0 block split.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include <cfloat>
+#include <climits>
+
+#include "kernels.h"
+
+namespace llm {
+
+namespace {
+
+__device__ __forceinline__ float load_elem(const DevMat& m, int64_t row, int64_t col) {
+    const int64_t i = row * m.cols + col;
+    switch (m.type) {
+        case W_F32: return static_cast<const float*>(m.data)[i];
+        case W_F16: return __half2float(static_cast<const __half*>(m.data)[i]);
+        case W_BF16: return __bfloat162float(static_cast<const __nv_bfloat16*>(m.data)[i]);
+        default: {
+            const float d = __half2float(m.scales[row * (m.cols / 32) + col / 32]);
+            return d * (float)static_cast<const int8_t*>(m.data)[i];
+        }
+    }
+}
+
+__device__ __forceinline__ float block_sum(float v, float* red) {
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+    if (l == 0) red[w] = v;
+    __syncthreads();
+    const int nw = (blockDim.x + 31) >> 5;
+    v = (threadIdx.x < nw) ? red[threadIdx.x] : 0.f;
+    if (w == 0)
+        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    if (threadIdx.x == 0) red[0] = v;
+    __syncthreads();
+    v = red[0];
+    __syncthreads();
+    return v;
+}
+
+__global__ void embed_kernel(DevMat E, const int32_t* __restrict__ tok, float* __restrict__ x,
+                             uint32_t* err) {
+    const int t = blockIdx.x;
+    const int32_t id = tok[t];
+    const bool ok = id >= 0 && id < E.rows;
+    if (!ok && threadIdx.x == 0) atomicOr(err, ERR_TOKEN_RANGE);
+    for (int64_t j = threadIdx.x; j < E.cols; j += blockDim.x)
+        x[(int64_t)t * E.cols + j] = ok ? load_elem(E, id, j) : 0.f;
+}
+
+__global__ void rmsnorm_kernel(const float* __restrict__ x, const int32_t* __restrict__ rows,
+                               int d, const float* __restrict__ g, float eps,
+                               float* __restrict__ y) {
+    __shared__ float red[32];
+    const int r = blockIdx.x;
+    const int src = rows ? rows[r] : r;
+    const float* xr = x + (int64_t)src * d;
+    float ss = 0.f;
+    for (int j = threadIdx.x; j < d; j += blockDim.x) ss += xr[j] * xr[j];
+    ss = block_sum(ss, red);
+    const float inv = 1.0f / sqrtf(ss / (float)d + eps);
+    for (int j = threadIdx.x; j < d; j += blockDim.x) y[(int64_t)r * d + j] = xr[j] * inv * g[j];
+}
+
+__global__ void rope_table_kernel(const int32_t* __restrict__ pos, int T, int half, double base,
+                                  float2* __restrict__ cs) {
+    const int idx = blockIdx.x * blockDim.x + threadIdx.x;
+    if (idx >= T * half) return;
+    const int t = idx / half, i = idx % half;
+    const double theta = pow(base, -2.0 * (double)i / (double)(2 * half));
+    double s, c;
+    sincos((double)pos[t] * theta, &s, &c);
+    cs[idx] = make_float2((float)c, (float)s);
+}
+
+template <typename KT>
+__device__ __forceinline__ KT to_kv(float v);
+template <>
+__device__ __forceinline__ float to_kv<float>(float v) { return v; }
+template <>
+__device__ __forceinline__ __half to_kv<__half>(float v) { return __float2half_rn(v); }
+
+template <typename KT>
+__global__ void rope_kv_append_kernel(float* __restrict__ qkv, int H, int Hkv, int hd,
+                                      const float2* __restrict__ cs,
+                                      const int32_t* __restrict__ slot, KT* __restrict__ kc,
+                                      KT* __restrict__ vc, int n_ctx, uint32_t* err) {
+    const int t = blockIdx.x;
+    const int half = hd / 2;
+    const int width = (H + 2 * Hkv) * hd;
+    float* row = qkv + (int64_t)t * width;
+    const int32_t c = slot[t];
+    const bool ok = c >= 0 && c < n_ctx;
+    if (!ok && threadIdx.x == 0) atomicOr(err, ERR_SLOT_RANGE);
+    const float2* cst = cs + (int64_t)t * half;
+    const int npairs = (H + Hkv) * half;
+    for (int j = threadIdx.x; j < npairs; j += blockDim.x) {
+        const int head = j / half, i = j % half;
+        float* p = row + head * hd + 2 * i;
+        const float x0 = p[0], x1 = p[1];
+        const float2 e = cst[i];
+        const float y0 = x0 * e.x - x1 * e.y;
+        const float y1 = x0 * e.y + x1 * e.x;
+        if (head < H) {
+            p[0] = y0;
+            p[1] = y1;
+        } else if (ok) {
+            KT* dst = kc + ((int64_t)(head - H) * n_ctx + c) * hd + 2 * i;
+            dst[0] = to_kv<KT>(y0);
+            dst[1] = to_kv<KT>(y1);
+        }
+    }
+    if (!ok) return;
+    const float* v = row + (H + Hkv) * hd;
+    for (int j = threadIdx.x; j < Hkv * hd; j += blockDim.x) {
+        const int g = j / hd, d = j % hd;
+        vc[((int64_t)g * n_ctx + c) * hd + d] = to_kv<KT>(v[j]);
+    }
+}
+
+__global__ void swiglu_kernel(const float* __restrict__ gu, int64_t T, int F,
+                              float* __restrict__ u) {
+    const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (idx >= T * F) return;
+    const int64_t t = idx / F, j = idx % F;
+    const float g = gu[t * 2 * F + j];
+    const float up = gu[t * 2 * F + F + j];
+    u[idx] = g / (1.0f + expf(-g)) * up;
+}
+
+__global__ void argmax_kernel(const float* __restrict__ logits, int V, int32_t* __restrict__ out) {
+    __shared__ float sv[32];
+    __shared__ int si[32];
+    const float* row = logits + (int64_t)blockIdx.x * V;
+    float best = -INFINITY;
+    int bi = INT_MAX;
+    for (int j = threadIdx.x; j < V; j += blockDim.x) {
+        const float v = row[j];
+        if (v > best || (v == best && j < bi)) { best = v; bi = j; }
+    }
+    for (int o = 16; o > 0; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, best, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+        if (ov > best || (ov == best && oi < bi)) { best = ov; bi = oi; }
+    }
+    const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+    if (l == 0) { sv[w] = best; si[w] = bi; }
+    __syncthreads();
+    if (w == 0) {
+        const int nw = blockDim.x >> 5;
+        best = l < nw ? sv[l] : -INFINITY;
+        bi = l < nw ? si[l] : INT_MAX;
+        for (int o = 16; o > 0; o >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, best, o);
+            const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+            if (ov > best || (ov == best && oi < bi)) { best = ov; bi = oi; }
+        }
+        if (l == 0) out[blockIdx.x] = bi == INT_MAX ? -1 : bi;
+    }
+}
+
+__global__ void q8_0_unpack_kernel(const uint8_t* __restrict__ blocks, int64_t nblocks,
+                                   int64_t bpr, int8_t* __restrict__ q, __half* __restrict__ d) {
+    const int64_t b = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (b >= nblocks) return;
+    const uint8_t* src = blocks + b * 34;
+    const uint16_t bits = (uint16_t)src[0] | ((uint16_t)src[1] << 8);
+    d[b] = __ushort_as_half(bits);
+    const int64_t row = b / bpr, kb = b % bpr;
+    int8_t* dst = q + row * bpr * 32 + kb * 32;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) dst[i] = (int8_t)src[2 + i];
+}
+
+}  // namespace
+
+void launch_embed(const DevMat& E, const int32_t* tok, int32_t T, float* x, uint32_t* err,
+                  cudaStream_t st) {
+    if (T <= 0) return;
+    embed_kernel<<<T, 256, 0, st>>>(E, tok, x, err);
+}
+
+void launch_rmsnorm(const float* x, const int32_t* rows, int32_t R, int32_t d, const float* g,
+                    float eps, float* y, cudaStream_t st) {
+    if (R <= 0) return;
+    rmsnorm_kernel<<<R, d >= 1024 ? 512 : 256, 0, st>>>(x, rows, d, g, eps, y);
+}
+
+void launch_rope_table(const int32_t* pos, int32_t T, int32_t hd, float base, float2* cs,
+                       cudaStream_t st) {
+    const int n = T * (hd / 2);
+    if (n <= 0) return;
+    rope_table_kernel<<<(n + 255) / 256, 256, 0, st>>>(pos, T, hd / 2, (double)base, cs);
+}
+
+void launch_rope_kv_append(float* qkv, int32_t T, int32_t H, int32_t Hkv, int32_t hd,
+                           const float2* cs, const int32_t* slot, void* kc, void* vc,
+                           int32_t n_ctx, int32_t kv_type, uint32_t* err, cudaStream_t st) {
+    if (T <= 0) return;
+    if (kv_type == W_F32)
+        rope_kv_append_kernel<float><<<T, 256, 0, st>>>(qkv, H, Hkv, hd, cs, slot, (float*)kc,
+                                                       (float*)vc, n_ctx, err);
+    else
+        rope_kv_append_kernel<__half><<<T, 256, 0, st>>>(qkv, H, Hkv, hd, cs, slot, (__half*)kc,
+                                                        (__half*)vc, n_ctx, err);
+}
+
+void launch_swiglu(const float* gu, int32_t T, int32_t F, float* u, cudaStream_t st) {
+    const int64_t n = (int64_t)T * F;
+    if (n <= 0) return;
+    swiglu_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(gu, T, F, u);
+}
+
+void launch_argmax(const float* logits, int32_t R, int32_t V, int32_t* idx, cudaStream_t st) {
+    if (R <= 0) return;
+    argmax_kernel<<<R, 1024, 0, st>>>(logits, V, idx);
+}
+
+void launch_q8_0_unpack(const uint8_t* blocks, int64_t rows, int64_t cols, int8_t* q, __half* d,
+                        cudaStream_t st) {
+    const int64_t nb = rows * (cols / 32);
+    if (nb <= 0) return;
+    q8_0_unpack_kernel<<<(unsigned)((nb + 255) / 256), 256, 0, st>>>(blocks, nb, cols / 32, q, d);
+}
+
+}  // namespace llm

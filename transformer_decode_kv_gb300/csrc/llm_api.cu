@@ -1,0 +1,919 @@
+// The C ABI of include/llm.h: context, device weight store, KV cache, the decode loop and the
+// per-ubatch launch sequence.
+//
+// Decode follows [P1] "llama.cpp AI LLM Engine - Як це працює", Крок 11-14 and [P4] "デコードループ"
+// (process_ubatch, エラーリカバリ): sanitise -> split -> slots for every ubatch before any commit ->
+// per ubatch: commit (apply), abort check, inputs upload (set_inputs), the device forward pass,
+// error check with rollback -> output rows in batch order.
+#include "../../include/llm.h"
+
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <chrono>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "host_plan.h"
+#include "kernels.h"
+
+using namespace llm;
+
+namespace {
+
+thread_local std::string g_init_error;
+
+size_t type_size(int32_t t) { return t == LLM_TYPE_F32 ? 4 : 2; }
+
+int64_t row_bytes(int32_t t, int64_t cols) {
+    switch (t) {
+        case LLM_TYPE_F32: return cols * 4;
+        case LLM_TYPE_F16:
+        case LLM_TYPE_BF16: return cols * 2;
+        case LLM_TYPE_Q8_0: return cols / 32 * 34;
+    }
+    return -1;
+}
+
+enum LayerBit : uint32_t {
+    B_ATTN_NORM = 1, B_Q = 2, B_K = 4, B_V = 8, B_O = 16, B_FFN_NORM = 32, B_GATE = 64, B_UP = 128,
+    B_DOWN = 256, B_ALL = 511
+};
+
+struct Layer {
+    DevMat qkv, wo, gu, down;
+    float* attn_norm = nullptr;
+    float* ffn_norm = nullptr;
+    uint32_t loaded = 0;
+};
+
+// Kernel classes timed by llm_debug_kernel_timing.
+enum KClass : int32_t {
+    KC_EMBED, KC_ROPE_TABLE, KC_RMSNORM, KC_LINEAR_GEMV, KC_LINEAR_GEMM, KC_ROPE_KV, KC_ATTENTION,
+    KC_LM_HEAD, KC_ARGMAX, KC_COUNT
+};
+const char* const kKClassNames[KC_COUNT] = {"embed", "rope_table", "rmsnorm", "linear_gemv",
+                                            "linear_gemm", "rope_kv_append", "attention",
+                                            "lm_head", "argmax"};
+struct KStat { int64_t launches = 0; double ms = 0, bytes = 0, flops = 0; };
+struct KPending { int32_t cls; cudaEvent_t a, b; double bytes, flops; };
+
+// Record of one ubatch for the debug hooks.
+struct UbDebug {
+    int32_t n_kv = 0;
+    std::vector<int32_t> pos, tok_list, list_off, list_cells, list_pos;
+};
+
+}  // namespace
+
+struct llm_ctx {
+    llm_hparams hp{};
+    int32_t n_ctx = 0, n_seq_max = 1, n_batch = 0, n_ubatch = 0, type_k = 1, type_v = 1;
+    bool host_only = false;
+    int device = 0, n_sm = 148;
+    cudaStream_t st = nullptr;
+    bool own_stream = false;
+    std::string err;
+
+    // weights
+    std::vector<Layer> layers;
+    DevMat embd, out;
+    float* out_norm = nullptr;
+    bool embd_loaded = false, out_loaded = false, out_norm_loaded = false, ready = false;
+    std::vector<void*> allocs;
+
+    // KV cache: K and V each [n_layer][Hkv][n_ctx][hd]
+    void* kv_k = nullptr;
+    void* kv_v = nullptr;
+    KvCells cells;
+
+    // scratch for one ubatch
+    float *x = nullptr, *h = nullptr, *qkv = nullptr, *attn = nullptr, *u = nullptr, *tmp = nullptr;
+    float *hout = nullptr;
+    float2* rope_cs = nullptr;
+    float *part_o = nullptr, *part_m = nullptr, *part_l = nullptr;
+    int32_t max_rows = 0;
+    int32_t* d_in = nullptr;
+    int32_t* h_in = nullptr;
+    size_t in_cap = 0;
+    uint32_t* d_err = nullptr;
+    uint32_t* h_err = nullptr;
+
+    // outputs of the last decode
+    float* d_logits = nullptr;
+    int32_t* d_argmax = nullptr;
+    int32_t out_cap = 0;
+    std::vector<float> h_logits;
+    std::vector<int32_t> h_argmax;
+    bool h_logits_valid = false, h_argmax_valid = false;
+    std::vector<int32_t> output_ids;
+    int32_t n_outputs = 0;
+
+    // control, debug
+    int (*abort_cb)(void*) = nullptr;
+    void* abort_ud = nullptr;
+    std::vector<int32_t> last_slots;
+    bool debug = false;
+    std::vector<UbDebug> dbg_ub;
+    float *dbg_embd = nullptr, *dbg_lout = nullptr, *dbg_attn = nullptr, *dbg_q = nullptr;
+    float* dbg_rnorm = nullptr;
+    int32_t dbg_T = 0, dbg_O = 0;
+    int32_t fault_kind = 0, fault_ub = -1;
+    llm_perf_data perf{};
+    bool ktime = false;
+    std::vector<cudaEvent_t> ev_pool;
+    size_t ev_used = 0;
+    std::vector<KPending> kpend;
+    KStat kstat[KC_COUNT];
+
+    SanBatch batch;
+    AttnPlan plan;
+
+    int32_t qkv_width() const { return (hp.n_head + 2 * hp.n_head_kv) * hp.head_dim; }
+    int32_t q_width() const { return hp.n_head * hp.head_dim; }
+    size_t kv_layer_elems() const { return (size_t)hp.n_head_kv * n_ctx * hp.head_dim; }
+};
+
+namespace {
+
+bool cuda_ok(llm_ctx* c, cudaError_t e, const char* what) {
+    if (e == cudaSuccess) return true;
+    c->err = std::string(what) + ": " + cudaGetErrorString(e);
+    return false;
+}
+
+template <typename T>
+bool dalloc(llm_ctx* c, T** p, size_t n) {
+    *p = nullptr;
+    if (n == 0) n = 1;
+    void* q = nullptr;
+    if (!cuda_ok(c, cudaMalloc(&q, n * sizeof(T)), "cudaMalloc")) return false;
+    c->allocs.push_back(q);
+    *p = static_cast<T*>(q);
+    return true;
+}
+
+void dfree(llm_ctx* c, void* p) {
+    if (!p) return;
+    cudaFree(p);
+    c->allocs.erase(std::remove(c->allocs.begin(), c->allocs.end(), p), c->allocs.end());
+}
+
+bool alloc_mat(llm_ctx* c, DevMat& m, int32_t type, int64_t rows, int64_t cols) {
+    m.type = type;
+    m.rows = rows;
+    m.cols = cols;
+    if (type == LLM_TYPE_Q8_0) {
+        int8_t* q = nullptr;
+        if (!dalloc(c, &q, (size_t)(rows * cols))) return false;
+        if (!dalloc(c, &m.scales, (size_t)(rows * cols / 32))) return false;
+        m.data = q;
+        return true;
+    }
+    uint8_t* p = nullptr;
+    if (!dalloc(c, &p, (size_t)(rows * cols) * type_size(type))) return false;
+    m.data = p;
+    return true;
+}
+
+// Copy rows (storage format `type`) into rows [row0, row0 + rows) of m.
+bool fill_rows(llm_ctx* c, DevMat& m, int64_t row0, int64_t rows, const void* data, size_t nbytes) {
+    if (m.type == LLM_TYPE_Q8_0) {
+        uint8_t* tmpb = nullptr;
+        if (!cuda_ok(c, cudaMalloc(&tmpb, nbytes), "cudaMalloc")) return false;
+        bool ok = cuda_ok(c, cudaMemcpyAsync(tmpb, data, nbytes, cudaMemcpyDefault, c->st), "copy");
+        if (ok) {
+            launch_q8_0_unpack(tmpb, rows, m.cols,
+                               static_cast<int8_t*>(m.data) + row0 * m.cols,
+                               m.scales + row0 * (m.cols / 32), c->st);
+            ok = cuda_ok(c, cudaGetLastError(), "q8_0 unpack") &&
+                 cuda_ok(c, cudaStreamSynchronize(c->st), "sync");
+        }
+        cudaFree(tmpb);
+        return ok;
+    }
+    uint8_t* dst = static_cast<uint8_t*>(m.data) + (size_t)row0 * m.cols * type_size(m.type);
+    return cuda_ok(c, cudaMemcpyAsync(dst, data, nbytes, cudaMemcpyDefault, c->st), "copy") &&
+           cuda_ok(c, cudaStreamSynchronize(c->st), "sync");
+}
+
+bool ensure_inputs(llm_ctx* c, size_t n_ints) {
+    if (n_ints <= c->in_cap) return true;
+    size_t cap = std::max(n_ints, c->in_cap * 2);
+    if (c->h_in) cudaFreeHost(c->h_in);
+    dfree(c, c->d_in);
+    c->h_in = nullptr;
+    c->d_in = nullptr;
+    c->in_cap = 0;
+    if (!cuda_ok(c, cudaMallocHost(&c->h_in, cap * sizeof(int32_t)), "cudaMallocHost")) return false;
+    if (!dalloc(c, &c->d_in, cap)) return false;
+    c->in_cap = cap;
+    return true;
+}
+
+bool ensure_outputs(llm_ctx* c, int32_t n) {
+    if (n <= c->out_cap) return true;
+    dfree(c, c->d_logits);
+    dfree(c, c->d_argmax);
+    c->d_logits = nullptr;
+    c->d_argmax = nullptr;
+    c->out_cap = 0;
+    if (!dalloc(c, &c->d_logits, (size_t)n * c->hp.n_vocab)) return false;
+    if (!dalloc(c, &c->d_argmax, (size_t)n)) return false;
+    c->out_cap = n;
+    return true;
+}
+
+void rollback(llm_ctx* c, int32_t i0, int32_t T) {
+    // [P4] エラーリカバリ: per sequence the smallest position of the ubatch, then seq_rm(s, pos_min, -1)
+    std::vector<int32_t> pmin(c->n_seq_max, INT32_MAX);
+    const SanBatch& b = c->batch;
+    for (int32_t i = i0; i < i0 + T; ++i)
+        for (int32_t s = 0; s < c->n_seq_max; ++s)
+            if (b.seqs[i].test(s)) pmin[s] = std::min(pmin[s], b.pos[i]);
+    for (int32_t s = 0; s < c->n_seq_max; ++s)
+        if (pmin[s] != INT32_MAX) c->cells.seq_rm(s, pmin[s], -1);
+}
+
+// ---- kernel timing --------------------------------------------------------------------------
+int kt_begin(llm_ctx* c) {
+    if (!c->ktime) return -1;
+    while (c->ev_pool.size() < c->ev_used + 2) {
+        cudaEvent_t e;
+        if (cudaEventCreate(&e) != cudaSuccess) return -1;
+        c->ev_pool.push_back(e);
+    }
+    const int i = (int)c->ev_used;
+    c->ev_used += 2;
+    cudaEventRecord(c->ev_pool[i], c->st);
+    return i;
+}
+
+void kt_end(llm_ctx* c, int i, int32_t cls, double bytes, double flops) {
+    if (i < 0) return;
+    cudaEventRecord(c->ev_pool[i + 1], c->st);
+    c->kpend.push_back({cls, c->ev_pool[i], c->ev_pool[i + 1], bytes, flops});
+}
+
+// After the stream is synchronised: fold the pending event pairs into the counters.
+void kt_collect(llm_ctx* c) {
+    for (const KPending& p : c->kpend) {
+        float ms = 0.f;
+        if (cudaEventElapsedTime(&ms, p.a, p.b) == cudaSuccess) {
+            KStat& s = c->kstat[p.cls];
+            s.launches += 1;
+            s.ms += ms;
+            s.bytes += p.bytes;
+            s.flops += p.flops;
+        }
+    }
+    c->kpend.clear();
+    c->ev_used = 0;
+}
+
+double wbytes(const DevMat& W, int64_t rows) { return (double)rows * (double)row_bytes(W.type, W.cols); }
+
+struct InOffsets {
+    size_t tok, pos, slot, out_rows, list_off, list_cells, list_pos, perm, tile_list, tile_start,
+        tile_nq, tile_wi_off, wi_tile, wi_c0, wi_c1, wi_row_off, total;
+};
+
+InOffsets layout_inputs(int32_t T, int32_t O, const AttnPlan& p) {
+    InOffsets o{};
+    size_t at = 0;
+    auto take = [&](size_t n) { size_t r = at; at += (n + 3) / 4 * 4; return r; };
+    o.tok = take(T);
+    o.pos = take(T);
+    o.slot = take(T);
+    o.out_rows = take(std::max(O, 1));
+    o.list_off = take(p.list_off.size());
+    o.list_cells = take(p.list_cells.size());
+    o.list_pos = take(p.list_pos.size());
+    o.perm = take(p.perm.size());
+    o.tile_list = take(p.tile_list.size());
+    o.tile_start = take(p.tile_start.size());
+    o.tile_nq = take(p.tile_nq.size());
+    o.tile_wi_off = take(p.tile_wi_off.size());
+    o.wi_tile = take(p.wi_tile.size());
+    o.wi_c0 = take(p.wi_c0.size());
+    o.wi_c1 = take(p.wi_c1.size());
+    o.wi_row_off = take(p.wi_row_off.size());
+    o.total = at;
+    return o;
+}
+
+void put(int32_t* base, size_t off, const std::vector<int32_t>& v) {
+    if (!v.empty()) std::memcpy(base + off, v.data(), v.size() * sizeof(int32_t));
+}
+
+// Enqueue the forward pass of one ubatch ([P2] Example 4 op chain; [P1] Крок 13б layer scheme).
+bool forward_ubatch(llm_ctx* c, int32_t T, int32_t O, int32_t out_row0, const InOffsets& io) {
+    const llm_hparams& hp = c->hp;
+    cudaStream_t st = c->st;
+    const int32_t d = hp.n_embd, H = hp.n_head, Hkv = hp.n_head_kv, hd = hp.head_dim, F = hp.n_ff;
+    const int32_t* din = c->d_in;
+    const int32_t *tok = din + io.tok, *pos = din + io.pos, *slot = din + io.slot;
+    const size_t kv_es = type_size(c->type_k);
+    const bool gemv = T <= gemv_max_tokens();
+    const int32_t lin_cls = gemv ? KC_LINEAR_GEMV : KC_LINEAR_GEMM;
+    const double Td = T, Od = O;
+    const int qw = c->q_width(), qkvw = c->qkv_width();
+
+    // algorithmic bytes / FLOPs of the attention of this ubatch (only needed when timing)
+    double att_bytes = 0, att_flops = 0;
+    if (c->ktime) {
+        const AttnPlan& p = c->plan;
+        for (int32_t t = 0; t < p.n_tiles(); ++t) {
+            const int32_t l = p.tile_list[t];
+            att_bytes += (double)(p.list_off[l + 1] - p.list_off[l]) * 2.0 * Hkv * hd * kv_es;
+        }
+        att_bytes += Td * qw * 4.0 * 2.0;
+        const SanBatch& b = c->batch;
+        (void)b;
+        for (int32_t t = 0; t < T; ++t) {
+            const int32_t l = p.tok_list[t];
+            int64_t vis = 0;
+            for (int32_t k = p.list_off[l]; k < p.list_off[l + 1]; ++k)
+                vis += p.list_pos[k] <= c->h_in[io.pos + t];
+            att_flops += 4.0 * (double)vis * H * hd;
+        }
+    }
+
+    int k;
+    k = kt_begin(c);
+    launch_embed(c->embd, tok, T, c->x, c->d_err, st);
+    kt_end(c, k, KC_EMBED, Td * d * (4.0 + type_size(c->embd.type == LLM_TYPE_Q8_0 ? 1 : c->embd.type)), 0);
+    k = kt_begin(c);
+    launch_rope_table(pos, T, hd, hp.rope_freq_base, c->rope_cs, st);
+    kt_end(c, k, KC_ROPE_TABLE, Td * hd * 4.0, 0);
+    if (c->debug) cudaMemcpyAsync(c->dbg_embd, c->x, sizeof(float) * T * d, cudaMemcpyDeviceToDevice, st);
+
+    AttnArgs a{};
+    a.ldq = qkvw;
+    a.q = c->qkv;
+    a.n_ctx = c->n_ctx;
+    a.kv_type = c->type_k;
+    a.H = H; a.Hkv = Hkv; a.hd = hd;
+    a.tok_pos = pos;
+    a.list_off = din + io.list_off; a.list_cells = din + io.list_cells; a.list_pos = din + io.list_pos;
+    a.perm = din + io.perm;
+    a.tile_list = din + io.tile_list; a.tile_start = din + io.tile_start; a.tile_nq = din + io.tile_nq;
+    a.tile_wi_off = din + io.tile_wi_off;
+    a.wi_tile = din + io.wi_tile; a.wi_c0 = din + io.wi_c0; a.wi_c1 = din + io.wi_c1;
+    a.wi_row_off = din + io.wi_row_off;
+    a.part_o = c->part_o; a.part_m = c->part_m; a.part_l = c->part_l;
+    a.out = c->attn;
+    a.ldo = qw;
+    a.n_work = c->plan.n_work();
+    a.n_tiles = c->plan.n_tiles();
+    a.max_nq = c->plan.max_nq;
+
+    const double norm_bytes = Td * d * 8.0 + d * 4.0;
+    for (int32_t il = 0; il < hp.n_layer; ++il) {
+        Layer& L = c->layers[il];
+        void* kc = static_cast<uint8_t*>(c->kv_k) + (size_t)il * c->kv_layer_elems() * kv_es;
+        void* vc = static_cast<uint8_t*>(c->kv_v) + (size_t)il * c->kv_layer_elems() * kv_es;
+        k = kt_begin(c);
+        launch_rmsnorm(c->x, nullptr, T, d, L.attn_norm, hp.rms_eps, c->h, st);
+        kt_end(c, k, KC_RMSNORM, norm_bytes, 0);
+        k = kt_begin(c);
+        launch_linear(L.qkv, 0, qkvw, c->h, d, T, c->qkv, qkvw, EPI_STORE, st);
+        kt_end(c, k, lin_cls, wbytes(L.qkv, qkvw) + Td * (d + qkvw) * 4.0, 2.0 * Td * qkvw * d);
+        k = kt_begin(c);
+        launch_rope_kv_append(c->qkv, T, H, Hkv, hd, c->rope_cs, slot, kc, vc, c->n_ctx,
+                              c->type_k, c->d_err, st);
+        kt_end(c, k, KC_ROPE_KV, Td * ((double)qkvw * 4.0 + qw * 4.0 + 2.0 * Hkv * hd * kv_es), 0);
+        a.kc = kc;
+        a.vc = vc;
+        k = kt_begin(c);
+        if (!launch_attention(a, st)) { c->err = "attention shape not supported"; return false; }
+        kt_end(c, k, KC_ATTENTION, att_bytes, att_flops);
+        if (c->debug) {
+            cudaMemcpy2DAsync(c->dbg_q + (size_t)il * T * qw, sizeof(float) * qw, c->qkv,
+                              sizeof(float) * qkvw, sizeof(float) * qw, T, cudaMemcpyDeviceToDevice, st);
+            cudaMemcpyAsync(c->dbg_attn + (size_t)il * T * qw, c->attn, sizeof(float) * T * qw,
+                            cudaMemcpyDeviceToDevice, st);
+        }
+        k = kt_begin(c);
+        launch_linear(L.wo, 0, d, c->attn, qw, T, c->x, d, EPI_ADD, st);
+        kt_end(c, k, lin_cls, wbytes(L.wo, d) + Td * (qw + 2.0 * d) * 4.0, 2.0 * Td * d * qw);
+        k = kt_begin(c);
+        launch_rmsnorm(c->x, nullptr, T, d, L.ffn_norm, hp.rms_eps, c->h, st);
+        kt_end(c, k, KC_RMSNORM, norm_bytes, 0);
+        k = kt_begin(c);
+        launch_linear_swiglu(L.gu, F, c->h, d, T, c->u, F, c->tmp, st);
+        kt_end(c, k, lin_cls, wbytes(L.gu, 2 * (int64_t)F) + Td * (d + F) * 4.0, 4.0 * Td * F * d);
+        k = kt_begin(c);
+        launch_linear(L.down, 0, d, c->u, F, T, c->x, d, EPI_ADD, st);
+        kt_end(c, k, lin_cls, wbytes(L.down, d) + Td * (F + 2.0 * d) * 4.0, 2.0 * Td * d * F);
+        if (c->debug)
+            cudaMemcpyAsync(c->dbg_lout + (size_t)il * T * d, c->x, sizeof(float) * T * d,
+                            cudaMemcpyDeviceToDevice, st);
+    }
+    if (O > 0) {
+        // keep only the requested rows, final norm, output matrix, greedy pick
+        k = kt_begin(c);
+        launch_rmsnorm(c->x, din + io.out_rows, O, d, c->out_norm, hp.rms_eps, c->hout, st);
+        kt_end(c, k, KC_RMSNORM, Od * d * 8.0 + d * 4.0, 0);
+        if (c->debug)
+            cudaMemcpyAsync(c->dbg_rnorm, c->hout, sizeof(float) * O * d, cudaMemcpyDeviceToDevice, st);
+        float* lg = c->d_logits + (size_t)out_row0 * hp.n_vocab;
+        k = kt_begin(c);
+        launch_linear(c->out, 0, hp.n_vocab, c->hout, d, O, lg, hp.n_vocab, EPI_STORE, st);
+        kt_end(c, k, KC_LM_HEAD, wbytes(c->out, hp.n_vocab) + Od * (d + (double)hp.n_vocab) * 4.0,
+               2.0 * Od * hp.n_vocab * d);
+        k = kt_begin(c);
+        launch_argmax(lg, O, hp.n_vocab, c->d_argmax + out_row0, st);
+        kt_end(c, k, KC_ARGMAX, Od * hp.n_vocab * 4.0, 0);
+    }
+    c->dbg_T = T;
+    c->dbg_O = O;
+    return cuda_ok(c, cudaGetLastError(), "kernel launch");
+}
+
+bool parse_layer_name(const char* name, int32_t* il, std::string* part) {
+    if (std::strncmp(name, "blk.", 4) != 0) return false;
+    const char* p = name + 4;
+    char* end = nullptr;
+    const long v = std::strtol(p, &end, 10);
+    if (end == p || *end != '.' || v < 0 || v > 100000) return false;
+    std::string rest(end + 1);
+    const std::string suffix = ".weight";
+    if (rest.size() <= suffix.size() || rest.compare(rest.size() - suffix.size(), suffix.size(), suffix) != 0)
+        return false;
+    *il = (int32_t)v;
+    *part = rest.substr(0, rest.size() - suffix.size());
+    return true;
+}
+
+}  // namespace
+
+// =============================================================================================
+extern "C" {
+
+llm_cparams llm_cparams_default(void) {
+    llm_cparams p{};
+    p.n_ctx = 4096;
+    p.n_seq_max = 1;
+    p.n_batch = 2048;
+    p.n_ubatch = 512;
+    p.type_k = LLM_TYPE_F16;
+    p.type_v = LLM_TYPE_F16;
+    p.stream = nullptr;
+    p.flags = 0;
+    return p;
+}
+
+llm_ctx* llm_ctx_init(const llm_hparams* hp, const llm_cparams* cp) {
+    g_init_error.clear();
+    auto fail = [](const std::string& m) -> llm_ctx* { g_init_error = m; return nullptr; };
+    if (!hp || !cp) return fail("NULL parameters");
+    const llm_hparams& h = *hp;
+    if (h.n_layer <= 0 || h.n_embd <= 0 || h.n_head <= 0 || h.n_head_kv <= 0 || h.head_dim <= 0 ||
+        h.n_ff <= 0 || h.n_vocab <= 0)
+        return fail("hyper-parameters must be positive");
+    if (h.n_head % h.n_head_kv != 0) return fail("n_head must be a multiple of n_head_kv");
+    if (h.rope_type != 0) return fail("only rope type 0 (normal) is supported");
+    if (h.n_embd % 32 != 0 || h.n_ff % 32 != 0) return fail("n_embd and n_ff must be multiples of 32");
+    if (!attention_supported(h.head_dim, h.n_head / h.n_head_kv))
+        return fail("attention kernels support head_dim 32/64/128 with n_head/n_head_kv = 4");
+    if (!(h.rms_eps >= 0.f) || !(h.rope_freq_base > 0.f)) return fail("bad rms_eps / rope_freq_base");
+    if (cp->n_ctx == 0 || cp->n_batch == 0 || cp->n_ubatch == 0) return fail("zero context size");
+    if (cp->n_seq_max < 1 || cp->n_seq_max > (uint32_t)kMaxSeq) return fail("n_seq_max out of range");
+    if ((cp->type_k != LLM_TYPE_F32 && cp->type_k != LLM_TYPE_F16) || cp->type_v != cp->type_k)
+        return fail("type_k/type_v must both be F32 or both F16");
+    if (cp->n_ctx > (1u << 24)) return fail("n_ctx too large");
+
+    auto* c = new llm_ctx();
+    c->hp = h;
+    c->n_ctx = (int32_t)((cp->n_ctx + 255) / 256 * 256);          // GGML_PAD(n_ctx, 256)
+    c->n_batch = (int32_t)std::min<uint32_t>(cp->n_batch, (uint32_t)c->n_ctx);
+    c->n_ubatch = (int32_t)std::min<uint32_t>(cp->n_ubatch, (uint32_t)c->n_batch);
+    c->n_seq_max = (int32_t)cp->n_seq_max;
+    c->type_k = cp->type_k;
+    c->type_v = cp->type_v;
+    c->host_only = (cp->flags & LLM_CTX_HOST_ONLY) != 0;
+    c->cells = KvCells(c->n_ctx, c->n_seq_max);
+    c->layers.resize(h.n_layer);
+    if (c->host_only) return c;
+
+    auto die = [&](const std::string& m) -> llm_ctx* {
+        g_init_error = m.empty() ? c->err : m;
+        llm_ctx_free(c);
+        return nullptr;
+    };
+    if (!cuda_ok(c, cudaGetDevice(&c->device), "cudaGetDevice")) return die("");
+    cudaDeviceGetAttribute(&c->n_sm, cudaDevAttrMultiProcessorCount, c->device);
+    if (cp->stream) {
+        c->st = static_cast<cudaStream_t>(cp->stream);
+    } else {
+        if (!cuda_ok(c, cudaStreamCreateWithFlags(&c->st, cudaStreamNonBlocking), "stream")) return die("");
+        c->own_stream = true;
+    }
+    const int64_t U = c->n_ubatch, d = h.n_embd;
+    const int G = h.n_head / h.n_head_kv;
+    const size_t kv_elems = (size_t)h.n_layer * c->kv_layer_elems();
+    bool ok = dalloc(c, reinterpret_cast<uint8_t**>(&c->kv_k), kv_elems * type_size(c->type_k)) &&
+              dalloc(c, reinterpret_cast<uint8_t**>(&c->kv_v), kv_elems * type_size(c->type_v)) &&
+              dalloc(c, &c->x, U * d) && dalloc(c, &c->h, U * d) &&
+              dalloc(c, &c->qkv, U * c->qkv_width()) && dalloc(c, &c->attn, U * c->q_width()) &&
+              dalloc(c, &c->u, U * h.n_ff) && dalloc(c, &c->tmp, U * 2 * (int64_t)h.n_ff) &&
+              dalloc(c, &c->hout, U * d) && dalloc(c, &c->rope_cs, U * (h.head_dim / 2)) &&
+              dalloc(c, &c->d_err, 1) &&
+              cuda_ok(c, cudaMallocHost(&c->h_err, sizeof(uint32_t)), "cudaMallocHost");
+    if (!ok) return die("");
+    c->max_rows = (int32_t)std::max<int64_t>(2 * U * G, 8192);
+    ok = dalloc(c, &c->part_o, (size_t)c->max_rows * h.n_head_kv * h.head_dim) &&
+         dalloc(c, &c->part_m, (size_t)c->max_rows * h.n_head_kv) &&
+         dalloc(c, &c->part_l, (size_t)c->max_rows * h.n_head_kv) &&
+         ensure_outputs(c, std::max<int32_t>(c->n_seq_max, (int32_t)std::min<int64_t>(U, 64))) &&
+         ensure_inputs(c, (size_t)8 * U + 2 * (size_t)c->n_ctx + 65536);
+    if (!ok) return die("");
+    // KV cells start zeroed so an unwritten cell never holds NaN bit patterns
+    ok = cuda_ok(c, cudaMemsetAsync(c->kv_k, 0, kv_elems * type_size(c->type_k), c->st), "memset") &&
+         cuda_ok(c, cudaMemsetAsync(c->kv_v, 0, kv_elems * type_size(c->type_v), c->st), "memset") &&
+         cuda_ok(c, cudaStreamSynchronize(c->st), "sync");
+    if (!ok) return die("");
+    return c;
+}
+
+void llm_ctx_free(llm_ctx* c) {
+    if (!c) return;
+    if (c->st) cudaStreamSynchronize(c->st);
+    for (void* p : c->allocs) cudaFree(p);
+    c->allocs.clear();
+    if (c->h_in) cudaFreeHost(c->h_in);
+    if (c->h_err) cudaFreeHost(c->h_err);
+    for (cudaEvent_t e : c->ev_pool) cudaEventDestroy(e);
+    if (c->own_stream && c->st) cudaStreamDestroy(c->st);
+    delete c;
+}
+
+int llm_load_weights(llm_ctx* c, const char* name, int32_t type, const int64_t ne[2],
+                     const void* data, size_t nbytes) {
+    if (!c || !name || !ne) return -1;
+    const llm_hparams& h = c->hp;
+    auto bad = [&](const std::string& m) { c->err = std::string(name) + ": " + m; return -1; };
+    if (type != LLM_TYPE_F32 && type != LLM_TYPE_F16 && type != LLM_TYPE_BF16 && type != LLM_TYPE_Q8_0)
+        return bad("unsupported type");
+    const int64_t cols = ne[0], rows = ne[1] <= 0 ? 1 : ne[1];
+    if (cols <= 0) return bad("bad shape");
+    if (type == LLM_TYPE_Q8_0 && cols % 32 != 0) return bad("Q8_0 rows must hold whole 32-value blocks");
+    if ((int64_t)nbytes != rows * row_bytes(type, cols)) return bad("byte size does not match shape and type");
+    if (!data) return bad("NULL data");
+    const int64_t d = h.n_embd, qd = (int64_t)h.n_head * h.head_dim, kvd = (int64_t)h.n_head_kv * h.head_dim;
+    const std::string n(name);
+    // data may have been produced by work on another stream of this device: wait for it
+    if (!c->host_only && !cuda_ok(c, cudaDeviceSynchronize(), "device synchronize")) return -2;
+    auto want_shape = [&](int64_t c0, int64_t r0) { return cols == c0 && rows == r0; };
+
+    if (n == "token_embd.weight" || n == "output.weight") {
+        if (!want_shape(d, h.n_vocab)) return bad("shape must be {n_embd, n_vocab}");
+        bool& flag = n == "token_embd.weight" ? c->embd_loaded : c->out_loaded;
+        DevMat& m = n == "token_embd.weight" ? c->embd : c->out;
+        if (flag) return bad("loaded twice");
+        if (c->host_only) { flag = true; return 0; }
+        if (!alloc_mat(c, m, type, rows, cols) || !fill_rows(c, m, 0, rows, data, nbytes)) return -2;
+        flag = true;
+        return 0;
+    }
+    if (n == "output_norm.weight") {
+        if (type != LLM_TYPE_F32 || !want_shape(d, 1)) return bad("norm gains must be F32 {n_embd}");
+        if (c->out_norm_loaded) return bad("loaded twice");
+        if (!c->host_only) {
+            if (!dalloc(c, &c->out_norm, d)) return -2;
+            if (!cuda_ok(c, cudaMemcpy(c->out_norm, data, nbytes, cudaMemcpyDefault), "copy")) return -2;
+        }
+        c->out_norm_loaded = true;
+        return 0;
+    }
+    int32_t il = -1;
+    std::string part;
+    if (!parse_layer_name(name, &il, &part) || il >= h.n_layer) return bad("unknown tensor name");
+    Layer& L = c->layers[il];
+    struct Spec { const char* part; uint32_t bit; int64_t c, r; };
+    const Spec specs[] = {
+        {"attn_norm", B_ATTN_NORM, d, 1}, {"attn_q", B_Q, d, qd}, {"attn_k", B_K, d, kvd},
+        {"attn_v", B_V, d, kvd}, {"attn_output", B_O, qd, d}, {"ffn_norm", B_FFN_NORM, d, 1},
+        {"ffn_gate", B_GATE, d, h.n_ff}, {"ffn_up", B_UP, d, h.n_ff}, {"ffn_down", B_DOWN, h.n_ff, d}};
+    const Spec* sp = nullptr;
+    for (const Spec& s : specs) if (part == s.part) sp = &s;
+    if (!sp) return bad("unknown tensor name");
+    if (!want_shape(sp->c, sp->r)) return bad("wrong shape");
+    if (L.loaded & sp->bit) return bad("loaded twice");
+    if (sp->bit == B_ATTN_NORM || sp->bit == B_FFN_NORM) {
+        if (type != LLM_TYPE_F32) return bad("norm gains must be F32");
+        if (!c->host_only) {
+            float*& g = sp->bit == B_ATTN_NORM ? L.attn_norm : L.ffn_norm;
+            if (!dalloc(c, &g, d)) return -2;
+            if (!cuda_ok(c, cudaMemcpy(g, data, nbytes, cudaMemcpyDefault), "copy")) return -2;
+        }
+        L.loaded |= sp->bit;
+        return 0;
+    }
+    // fused stores: Q, K, V rows stacked in one matrix; gate rows then up rows in another
+    DevMat* m = nullptr;
+    int64_t row0 = 0, total_rows = 0;
+    uint32_t group = 0;
+    switch (sp->bit) {
+        case B_Q: m = &L.qkv; row0 = 0; total_rows = qd + 2 * kvd; group = B_Q | B_K | B_V; break;
+        case B_K: m = &L.qkv; row0 = qd; total_rows = qd + 2 * kvd; group = B_Q | B_K | B_V; break;
+        case B_V: m = &L.qkv; row0 = qd + kvd; total_rows = qd + 2 * kvd; group = B_Q | B_K | B_V; break;
+        case B_O: m = &L.wo; row0 = 0; total_rows = d; group = B_O; break;
+        case B_GATE: m = &L.gu; row0 = 0; total_rows = 2 * (int64_t)h.n_ff; group = B_GATE | B_UP; break;
+        case B_UP: m = &L.gu; row0 = h.n_ff; total_rows = 2 * (int64_t)h.n_ff; group = B_GATE | B_UP; break;
+        default: m = &L.down; row0 = 0; total_rows = d; group = B_DOWN; break;
+    }
+    if (L.loaded & group) {
+        if (m->type != type) return bad("all tensors of a fused group must share a type");
+    } else if (!c->host_only) {
+        if (!alloc_mat(c, *m, type, total_rows, cols)) return -2;
+    } else {
+        m->type = type;
+    }
+    if (!c->host_only && !fill_rows(c, *m, row0, rows, data, nbytes)) return -2;
+    L.loaded |= sp->bit;
+    return 0;
+}
+
+int llm_weights_ready(llm_ctx* c) {
+    if (!c) return -1;
+    if (!c->embd_loaded) { c->err = "missing token_embd.weight"; return -1; }
+    if (!c->out_norm_loaded) { c->err = "missing output_norm.weight"; return -1; }
+    for (int32_t il = 0; il < c->hp.n_layer; ++il) {
+        if (c->layers[il].loaded != B_ALL) {
+            c->err = "missing weights of layer " + std::to_string(il);
+            return -1;
+        }
+    }
+    if (!c->out_loaded) c->out = c->embd;   // tied output
+    c->ready = true;
+    return 0;
+}
+
+int32_t llm_decode(llm_ctx* c, llm_batch bt) {
+    if (!c) return -2;
+    const auto t0 = std::chrono::steady_clock::now();
+    struct Timer {
+        llm_ctx* c;
+        std::chrono::steady_clock::time_point t0;
+        ~Timer() {
+            c->perf.t_decode_ms += std::chrono::duration<double, std::milli>(
+                                       std::chrono::steady_clock::now() - t0).count();
+        }
+    } timer{c, t0};
+    c->n_outputs = 0;
+    c->output_ids.clear();
+    c->h_logits_valid = c->h_argmax_valid = false;
+    if (!c->host_only && !c->ready && llm_weights_ready(c) != 0) return -1;
+    if (!c->host_only) cudaSetDevice(c->device);
+    SanBatch& b = c->batch;
+    std::string why;
+    if (!sanitize_batch(bt.n_tokens, bt.token, bt.pos, bt.n_seq_id, bt.seq_id, bt.logits,
+                        c->hp.n_vocab, c->n_seq_max, c->n_batch, c->cells, b, &why)) {
+        c->err = "invalid batch: " + why;
+        return -1;
+    }
+    // all slots before any commit ([P1] Крок 12): ubatch k takes the next lowest empty cells
+    std::vector<int32_t> slots;
+    if (!c->cells.find_free(b.n, slots)) {
+        c->err = "no KV slot for the batch";
+        return 1;
+    }
+    if (!c->host_only && !ensure_outputs(c, b.n_outputs)) return -2;
+    c->last_slots = slots;
+    c->dbg_ub.clear();
+    c->perf.n_decode_calls += 1;
+    const int32_t G = c->hp.n_head / c->hp.n_head_kv;
+    int32_t n_out = 0;
+    int32_t ub = 0;
+    for (int32_t i0 = 0; i0 < b.n; i0 += c->n_ubatch, ++ub) {
+        const int32_t T = std::min(c->n_ubatch, b.n - i0);
+        std::vector<int32_t> us(slots.begin() + i0, slots.begin() + i0 + T);
+        c->cells.apply(us, b.pos.data() + i0, b.seqs.data() + i0, T);       // mctx->apply()
+        if (c->abort_cb && c->abort_cb(c->abort_ud)) {
+            rollback(c, i0, T);
+            c->err = "aborted";
+            return 2;
+        }
+        build_attn_plan(c->cells, b, i0, T, kAttnTileQ, c->hp.n_head_kv, G, 4 * c->n_sm,
+                        c->max_rows, c->plan);
+        if (c->debug) {
+            UbDebug u;
+            u.n_kv = c->cells.n_kv();
+            u.pos.assign(b.pos.begin() + i0, b.pos.begin() + i0 + T);
+            u.tok_list = c->plan.tok_list;
+            u.list_off = c->plan.list_off;
+            u.list_cells = c->plan.list_cells;
+            u.list_pos = c->plan.list_pos;
+            c->dbg_ub.push_back(std::move(u));
+        }
+        std::vector<int32_t> out_rows;
+        for (int32_t t = 0; t < T; ++t)
+            if (b.output[i0 + t]) out_rows.push_back(t);
+        const int32_t O = (int32_t)out_rows.size();
+        c->perf.n_ubatches += 1;
+        c->perf.n_tokens += T;
+        if (c->host_only) { n_out += O; continue; }
+
+        const InOffsets io = layout_inputs(T, O, c->plan);
+        if (!ensure_inputs(c, io.total)) { rollback(c, i0, T); return -2; }
+        int32_t* hi = c->h_in;
+        std::memcpy(hi + io.tok, b.token.data() + i0, T * sizeof(int32_t));
+        std::memcpy(hi + io.pos, b.pos.data() + i0, T * sizeof(int32_t));
+        std::memcpy(hi + io.slot, us.data(), T * sizeof(int32_t));
+        if (c->fault_kind == 1 && c->fault_ub == ub) hi[io.slot] = c->n_ctx + 7;
+        put(hi, io.out_rows, out_rows);
+        const AttnPlan& p = c->plan;
+        put(hi, io.list_off, p.list_off); put(hi, io.list_cells, p.list_cells);
+        put(hi, io.list_pos, p.list_pos); put(hi, io.perm, p.perm);
+        put(hi, io.tile_list, p.tile_list); put(hi, io.tile_start, p.tile_start);
+        put(hi, io.tile_nq, p.tile_nq); put(hi, io.tile_wi_off, p.tile_wi_off);
+        put(hi, io.wi_tile, p.wi_tile); put(hi, io.wi_c0, p.wi_c0); put(hi, io.wi_c1, p.wi_c1);
+        put(hi, io.wi_row_off, p.wi_row_off);
+        bool ok = cuda_ok(c, cudaMemcpyAsync(c->d_in, hi, io.total * sizeof(int32_t),
+                                             cudaMemcpyHostToDevice, c->st), "inputs upload") &&
+                  cuda_ok(c, cudaMemsetAsync(c->d_err, 0, sizeof(uint32_t), c->st), "memset");
+        ok = ok && forward_ubatch(c, T, O, n_out, io);
+        ok = ok && cuda_ok(c, cudaMemcpyAsync(c->h_err, c->d_err, sizeof(uint32_t),
+                                              cudaMemcpyDeviceToHost, c->st), "error word") &&
+             cuda_ok(c, cudaStreamSynchronize(c->st), "device computation");
+        kt_collect(c);
+        if (ok && *c->h_err != 0) {
+            c->err = "device bounds check failed (error word " + std::to_string(*c->h_err) + ")";
+            ok = false;
+        }
+        if (!ok) {
+            rollback(c, i0, T);
+            c->fault_kind = 0;
+            return -3;
+        }
+        n_out += O;
+    }
+    c->fault_kind = 0;
+    c->n_outputs = n_out;
+    c->output_ids.assign(b.n, -1);
+    int32_t k = 0;
+    for (int32_t i = 0; i < b.n; ++i)
+        if (b.output[i]) c->output_ids[i] = k++;
+    return 0;
+}
+
+static int32_t resolve_row(llm_ctx* c, int32_t i) {
+    if (i < 0) {
+        const int32_t j = c->n_outputs + i;
+        return j >= 0 ? j : -1;
+    }
+    if (i >= (int32_t)c->output_ids.size()) return -1;
+    return c->output_ids[i];
+}
+
+float* llm_get_logits_ith(llm_ctx* c, int32_t i) {
+    if (!c || c->host_only) return nullptr;
+    const int32_t j = resolve_row(c, i);
+    if (j < 0) return nullptr;
+    if (!c->h_logits_valid) {
+        c->h_logits.resize((size_t)c->n_outputs * c->hp.n_vocab);
+        if (!cuda_ok(c, cudaMemcpyAsync(c->h_logits.data(), c->d_logits,
+                                        c->h_logits.size() * sizeof(float), cudaMemcpyDeviceToHost,
+                                        c->st), "logits copy") ||
+            !cuda_ok(c, cudaStreamSynchronize(c->st), "sync"))
+            return nullptr;
+        c->h_logits_valid = true;
+    }
+    return c->h_logits.data() + (size_t)j * c->hp.n_vocab;
+}
+
+int32_t llm_get_argmax_ith(llm_ctx* c, int32_t i) {
+    if (!c || c->host_only) return -1;
+    const int32_t j = resolve_row(c, i);
+    if (j < 0) return -1;
+    if (!c->h_argmax_valid) {
+        c->h_argmax.resize(c->n_outputs);
+        if (!cuda_ok(c, cudaMemcpyAsync(c->h_argmax.data(), c->d_argmax, c->n_outputs * sizeof(int32_t),
+                                        cudaMemcpyDeviceToHost, c->st), "argmax copy") ||
+            !cuda_ok(c, cudaStreamSynchronize(c->st), "sync"))
+            return -1;
+        c->h_argmax_valid = true;
+    }
+    return c->h_argmax[j];
+}
+
+int32_t llm_n_outputs(llm_ctx* c) { return c ? c->n_outputs : 0; }
+
+int llm_seq_rm(llm_ctx* c, int32_t seq, int32_t p0, int32_t p1) {
+    if (!c) return 0;
+    if (seq >= c->n_seq_max) return 1;
+    c->cells.seq_rm(seq, p0, p1);
+    return 1;
+}
+
+int32_t llm_seq_pos_max(llm_ctx* c, int32_t s) { return c ? c->cells.seq_pos_max(s) : -1; }
+int32_t llm_seq_pos_min(llm_ctx* c, int32_t s) { return c ? c->cells.seq_pos_min(s) : -1; }
+
+void llm_set_abort_callback(llm_ctx* c, int (*cb)(void*), void* ud) {
+    if (!c) return;
+    c->abort_cb = cb;
+    c->abort_ud = ud;
+}
+
+uint32_t llm_n_ctx(llm_ctx* c) { return c ? (uint32_t)c->n_ctx : 0; }
+uint32_t llm_n_batch(llm_ctx* c) { return c ? (uint32_t)c->n_batch : 0; }
+uint32_t llm_n_ubatch(llm_ctx* c) { return c ? (uint32_t)c->n_ubatch : 0; }
+int32_t llm_kv_used_cells(llm_ctx* c) { return c ? c->cells.used() : 0; }
+
+const char* llm_last_error(llm_ctx* c) { return c ? c->err.c_str() : g_init_error.c_str(); }
+
+void llm_perf(llm_ctx* c, llm_perf_data* out) {
+    if (c && out) *out = c->perf;
+}
+
+int32_t llm_debug_last_slots(llm_ctx* c, int32_t* out, int32_t cap) {
+    if (!c) return 0;
+    const int32_t n = (int32_t)c->last_slots.size();
+    if (out) std::memcpy(out, c->last_slots.data(), sizeof(int32_t) * std::max(0, std::min(n, cap)));
+    return n;
+}
+
+int64_t llm_debug_ubatch_mask(llm_ctx* c, int32_t ub, uint8_t* out, int64_t cap, int32_t* n_kv_out) {
+    if (!c || ub < 0 || ub >= (int32_t)c->dbg_ub.size()) return 0;
+    const UbDebug& u = c->dbg_ub[ub];
+    const int64_t T = (int64_t)u.pos.size(), nkv = u.n_kv, n = T * nkv;
+    if (n_kv_out) *n_kv_out = (int32_t)nkv;
+    if (!out) return n;
+    std::vector<uint8_t> m((size_t)n, 0);
+    for (int64_t t = 0; t < T; ++t) {
+        const int32_t l = u.tok_list[t];
+        for (int32_t k = u.list_off[l]; k < u.list_off[l + 1]; ++k)
+            if (u.list_pos[k] <= u.pos[t] && u.list_cells[k] < nkv) m[t * nkv + u.list_cells[k]] = 1;
+    }
+    std::memcpy(out, m.data(), (size_t)std::min(n, cap));
+    return n;
+}
+
+int llm_debug_capture(llm_ctx* c, int enable) {
+    if (!c) return -1;
+    c->debug = enable != 0;
+    if (!c->debug || c->host_only || c->dbg_lout) return 0;
+    const int64_t U = c->n_ubatch, d = c->hp.n_embd, L = c->hp.n_layer, qw = c->q_width();
+    const bool ok = dalloc(c, &c->dbg_embd, U * d) && dalloc(c, &c->dbg_lout, L * U * d) &&
+                    dalloc(c, &c->dbg_attn, L * U * qw) && dalloc(c, &c->dbg_q, L * U * qw) &&
+                    dalloc(c, &c->dbg_rnorm, U * d);
+    return ok ? 0 : -2;
+}
+
+int64_t llm_debug_get_tensor(llm_ctx* c, const char* name, int32_t layer, float* out, int64_t cap) {
+    if (!c || !name || c->host_only || !c->dbg_lout) return 0;
+    const std::string n(name);
+    const int64_t T = c->dbg_T, d = c->hp.n_embd, qw = c->q_width();
+    const float* src = nullptr;
+    int64_t cnt = 0;
+    if (n == "embd") { src = c->dbg_embd; cnt = T * d; }
+    else if (n == "result_norm") { src = c->dbg_rnorm; cnt = (int64_t)c->dbg_O * d; }
+    else if (layer >= 0 && layer < c->hp.n_layer) {
+        if (n == "l_out") { src = c->dbg_lout + layer * T * d; cnt = T * d; }
+        else if (n == "attn_out") { src = c->dbg_attn + layer * T * qw; cnt = T * qw; }
+        else if (n == "kq_in") { src = c->dbg_q + layer * T * qw; cnt = T * qw; }
+    }
+    if (!src) return 0;
+    if (out && cap > 0) {
+        cudaStreamSynchronize(c->st);
+        cudaMemcpy(out, src, sizeof(float) * std::min(cnt, cap), cudaMemcpyDeviceToHost);
+    }
+    return cnt;
+}
+
+int llm_debug_kernel_timing(llm_ctx* c, int enable) {
+    if (!c) return -1;
+    c->ktime = enable != 0 && !c->host_only;
+    if (c->ktime)
+        for (KStat& s : c->kstat) s = KStat();
+    return 0;
+}
+
+int32_t llm_debug_kernel_stats(llm_ctx* c, int32_t i, char* name, int32_t name_cap,
+                               int64_t* launches, double* ms, double* bytes, double* flops) {
+    if (!c) return 0;
+    if (i >= 0 && i < KC_COUNT) {
+        if (name && name_cap > 0) {
+            std::strncpy(name, kKClassNames[i], (size_t)name_cap - 1);
+            name[name_cap - 1] = 0;
+        }
+        if (launches) *launches = c->kstat[i].launches;
+        if (ms) *ms = c->kstat[i].ms;
+        if (bytes) *bytes = c->kstat[i].bytes;
+        if (flops) *flops = c->kstat[i].flops;
+    }
+    return KC_COUNT;
+}
+
+int llm_debug_inject_fault(llm_ctx* c, int32_t kind, int32_t ub) {
+    if (!c) return -1;
+    c->fault_kind = kind;
+    c->fault_ub = ub;
+    return 0;
+}
+
+}  // extern "C"
