@@ -245,6 +245,15 @@ int llm_debug_kernel_timing(llm_ctx *ctx, int enable);
 int32_t llm_debug_kernel_stats(llm_ctx *ctx, int32_t i, char *name, int32_t name_cap,
                                int64_t *launches, double *ms, double *bytes, double *flops);
 
+/* One launch of the tensor-core (tcgen05) GEMM on device buffers, synchronous: W bf16 row-major
+ * [rows][K], X bf16 row-major [T][K], K % 64 == 0. epi 0: Y[t][m] = sum_k W[m][k] X[t][k] as
+ * float32 (rows = M, M % 128 == 0); epi 1: the same added into Y; epi 2: Y[t][j] (bf16) =
+ * silu(gate_j) * up_j with gate rows [0, F) and up rows [F, 2F) of W (F % 64 == 0). ldy is Y's
+ * row stride in elements. Returns 0, -1 for an unsupported shape, -3 if the launch failed or the
+ * kernel reported an error (its waits are time-bounded). */
+int llm_debug_gemm_bf16(int32_t epi, const void *W, int64_t M, int64_t K, const void *X, int32_t T,
+                        void *Y, int32_t ldy, int32_t F);
+
 /* Fault injection: kind 1 makes ubatch `ub` of the next llm_decode hand the K/V append kernel a
  * cell index past the cache; the kernel's bounds check skips the write and reports the error
  * word, so llm_decode returns -3 and rolls that ubatch back. kind 0 clears it. */

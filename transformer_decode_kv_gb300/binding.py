@@ -75,6 +75,8 @@ SIGNATURES = {
                                          C.POINTER(C.c_float), C.c_int64]),
     "llm_debug_inject_fault": (C.c_int, [C.c_void_p, C.c_int32, C.c_int32]),
     "llm_debug_kernel_timing": (C.c_int, [C.c_void_p, C.c_int]),
+    "llm_debug_gemm_bf16": (C.c_int, [C.c_int32, C.c_void_p, C.c_int64, C.c_int64, C.c_void_p,
+                                      C.c_int32, C.c_void_p, C.c_int32, C.c_int32]),
     "llm_debug_kernel_stats": (C.c_int32, [C.c_void_p, C.c_int32, C.c_char_p, C.c_int32,
                                            C.POINTER(C.c_int64), C.POINTER(C.c_double),
                                            C.POINTER(C.c_double), C.POINTER(C.c_double)]),
@@ -109,6 +111,13 @@ def _ptr(a: np.ndarray, ct):
 
 class LlmError(RuntimeError):
     pass
+
+
+def debug_gemm_bf16(epi: int, W, X, Y, F: int = 0) -> int:
+    """One tensor-core GEMM launch on torch CUDA tensors (W [rows][K] bf16, X [T][K] bf16)."""
+    return lib().llm_debug_gemm_bf16(epi, C.c_void_p(W.data_ptr()), W.shape[0], W.shape[1],
+                                     C.c_void_p(X.data_ptr()), X.shape[0], C.c_void_p(Y.data_ptr()),
+                                     Y.stride(0), F)
 
 
 class Context:

@@ -1,0 +1,363 @@
+// Tensor-core GEMM for prefill ubatches on sm_103a: tcgen05.mma (BF16 x BF16 -> F32 in TMEM),
+// operands staged in shared memory by TMA (cp.async.bulk.tensor, 128-byte swizzle), an mbarrier
+// ring of pipeline stages, and fused epilogues read back with tcgen05.ld.
+//
+// Y[t][m] (op)= sum_k W[m][k] X[t][k] ([P2] "llama.cpp Architecture", Example 4: MUL_MAT of a
+// {K, M} weight by the ubatch's activations; ADD for the residual; SWIGLU(ffn_gate, ffn_up)).
+//
+// The MMA's A operand is a 128-row tile of the weight matrix and its B operand a BN-token tile
+// of the activations, both K-major; the accumulator D[128 weight rows][BN tokens] lives in
+// TMEM with one weight row per lane, so the epilogue's warp-wide stores write 32 consecutive
+// output features of one token (coalesced). SwiGLU: the A tile holds 64 gate rows then the 64
+// matching up rows; warps 2-3 pass their up values to warps 0-1 through shared memory.
+//
+// Roles (128 threads): thread 0 issues TMA loads, thread 32 issues MMAs, all four warps run the
+// epilogue. Every mbarrier wait is bounded by a wall-clock limit; a timeout sets ERR_TIMEOUT in
+// the error word, skips the remaining work, drains the copies it issued and frees TMEM.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cudaTypedefs.h>
+
+#include <cstdint>
+
+#include "gemm_tc.h"
+#include "kernels.h"
+
+namespace llm {
+
+namespace {
+
+constexpr int kBM = 128;          // weight rows per tile (MMA M)
+constexpr int kBK = 64;           // K per stage: 64 bf16 = one 128-byte swizzle row
+constexpr uint64_t kWaitNs = 2000000000ull;    // 2 s bound on any wait
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Wait for the phase of `parity` to complete; false after the time limit.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+    if (mbar_try(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    while (!mbar_try(bar, parity))
+        if (global_ns() - t0 > kWaitNs) return false;
+    return true;
+}
+
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar,
+                                            int x, int y) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y)
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor of a K-major tile with the 128-byte swizzle: 8-row groups of
+// 128-byte rows, 1024 bytes apart.
+__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);      // start address
+    d |= (uint64_t)1 << 16;                         // leading byte offset (unused for SW128 K-major)
+    d |= (uint64_t)(1024 >> 4) << 32;               // stride byte offset
+    d |= (uint64_t)1 << 46;                         // descriptor version
+    d |= (uint64_t)2 << 61;                         // 128-byte swizzle
+    return d;
+}
+
+// Instruction descriptor of kind::f16 with BF16 A/B, F32 D, both K-major.
+__host__ __device__ constexpr uint32_t idesc_bf16(int m, int n) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) |
+           ((uint32_t)(m >> 4) << 24);
+}
+
+__device__ __forceinline__ void umma_bf16(uint32_t dtmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                          uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(dtmem),
+        "l"(a), "l"(b), "r"(idesc), "r"(accumulate));
+}
+
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+            smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+        "%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+template <int BN>
+struct TcCfg {
+    static constexpr int kStages = BN == 256 ? 4 : 6;
+    static constexpr uint32_t kA = kBM * kBK * 2;          // 16 KB
+    static constexpr uint32_t kB = BN * kBK * 2;
+    static constexpr size_t kSmem = 1024 + (size_t)kStages * (kA + kB) + 256;
+};
+
+template <int BN, int EPI>
+__global__ void __launch_bounds__(128, 1)
+gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+               int K, int M, int T, int F, void* __restrict__ Y, int ldy,
+               uint32_t* __restrict__ err) {
+    using C = TcCfg<BN>;
+    constexpr int S = C::kStages;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    uint8_t* sA = smem;
+    uint8_t* sB = smem + S * C::kA;
+    uint64_t* full = reinterpret_cast<uint64_t*>(sB + S * C::kB);
+    uint64_t* empty = full + S;
+    uint64_t* accf = empty + S;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accf + 1);
+    int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nk = K / kBK;
+    const int row0 = blockIdx.x * (EPI == GEMM_EPI_SWIGLU ? 64 : kBM);
+    const int t0 = blockIdx.y * BN;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        mbar_init(accf, 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmA)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmB)) : "memory");
+    }
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(tmem_slot)),
+                     "r"((uint32_t)BN));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (threadIdx.x == 0) {
+        // ---- TMA producer
+        int issued = 0;
+        for (int kb = 0; kb < nk; ++kb) {
+            const int s = kb % S;
+            const uint32_t ph = (uint32_t)(kb / S) & 1u;
+            if (kb >= S && !mbar_wait(&empty[s], ph ^ 1u)) { atomicOr(err, ERR_TIMEOUT); *(volatile int*)abort_flag = 1; break; }
+            if (*(volatile int*)abort_flag) break;
+            mbar_expect_tx(&full[s], C::kA + C::kB);
+            if (EPI == GEMM_EPI_SWIGLU) {
+                tma_load_2d(sA + s * C::kA, &tmA, &full[s], kb * kBK, row0);
+                tma_load_2d(sA + s * C::kA + C::kA / 2, &tmA, &full[s], kb * kBK, F + row0);
+            } else {
+                tma_load_2d(sA + s * C::kA, &tmA, &full[s], kb * kBK, row0);
+            }
+            tma_load_2d(sB + s * C::kB, &tmB, &full[s], kb * kBK, t0);
+            issued = kb + 1;
+        }
+        // drain: every copy this thread issued has landed before the block can exit
+        for (int kb = (issued > S ? issued - S : 0); kb < issued; ++kb)
+            mbar_wait(&full[kb % S], (uint32_t)(kb / S) & 1u);
+    } else if (threadIdx.x == 32) {
+        // ---- MMA issuer
+        constexpr uint32_t idesc = idesc_bf16(kBM, BN);
+        bool ok = true;
+        for (int kb = 0; kb < nk; ++kb) {
+            const int s = kb % S;
+            const uint32_t ph = (uint32_t)(kb / S) & 1u;
+            if (!mbar_wait(&full[s], ph)) { ok = false; break; }
+            tc_fence_after();
+            const uint64_t ad = sdesc_sw128(smem_u32(sA + s * C::kA));
+            const uint64_t bd = sdesc_sw128(smem_u32(sB + s * C::kB));
+#pragma unroll
+            for (int kk = 0; kk < kBK / 16; ++kk)
+                umma_bf16(tmem, ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2), idesc,
+                          (kb | kk) != 0 ? 1u : 0u);
+            umma_commit(&empty[s]);
+        }
+        if (!ok) { atomicOr(err, ERR_TIMEOUT); *(volatile int*)abort_flag = 1; }
+        umma_commit(accf);
+    }
+    __syncwarp();
+
+    // ---- epilogue: TMEM -> registers -> global
+    const bool have = mbar_wait(accf, 0);
+    tc_fence_after();
+    if (!have) atomicOr(err, ERR_TIMEOUT);
+    const bool live = have && !*(volatile int*)abort_flag;
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    if (EPI != GEMM_EPI_SWIGLU) {
+        const int m = row0 + warp * 32 + lane;
+#pragma unroll 1
+        for (int c0 = 0; c0 < BN; c0 += 16) {
+            float v[16];
+            tmem_ld16(tmem + lane_base + (uint32_t)c0, v);
+            if (!live || m >= M) continue;
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                const int t = t0 + c0 + j;
+                if (t >= T) break;
+                float* dst = static_cast<float*>(Y) + (int64_t)t * ldy + m;
+                if (EPI == GEMM_EPI_ADD) *dst += v[j];
+                else *dst = v[j];
+            }
+        }
+    } else {
+        // warps 2-3 (up rows) hand their values to warps 0-1 (gate rows) through shared memory;
+        // the pipeline stages are free once the accumulator is complete
+        float* xu = reinterpret_cast<float*>(smem);          // [64 rows][16 columns]
+#pragma unroll 1
+        for (int c0 = 0; c0 < BN; c0 += 16) {
+            float v[16];
+            tmem_ld16(tmem + lane_base + (uint32_t)c0, v);
+            if (warp >= 2) {
+#pragma unroll
+                for (int j = 0; j < 16; ++j) xu[((warp - 2) * 32 + lane) * 17 + j] = v[j];
+            }
+            __syncthreads();
+            if (warp < 2 && live) {
+                const int jrow = row0 + warp * 32 + lane;
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const int t = t0 + c0 + j;
+                    if (t >= T) break;
+                    const float g = v[j];
+                    const float u = xu[(warp * 32 + lane) * 17 + j];
+                    const float o = g / (1.0f + expf(-g)) * u;
+                    static_cast<__nv_bfloat16*>(Y)[(int64_t)t * ldy + jrow] = __float2bfloat16_rn(o);
+                }
+            }
+            __syncthreads();
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                     "r"((uint32_t)BN));
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        cudaDriverEntryPointQueryResult q;
+        void* p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+template <int BN, int EPI>
+bool launch_tc(const CUtensorMap& a, const CUtensorMap& b, int K, int M, int T, int F, void* Y,
+               int ldy, uint32_t* err, cudaStream_t st) {
+    using C = TcCfg<BN>;
+    auto k = gemm_tc_kernel<BN, EPI>;
+    static bool attr = false;
+    if (!attr) {
+        if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem) != cudaSuccess)
+            return false;
+        attr = true;
+    }
+    const int rows_per_tile = EPI == GEMM_EPI_SWIGLU ? 64 : kBM;
+    const int mtiles = (EPI == GEMM_EPI_SWIGLU ? F : M) / rows_per_tile;
+    dim3 grid(mtiles, (T + BN - 1) / BN);
+    k<<<grid, 128, C::kSmem, st>>>(a, b, K, M, T, F, Y, ldy, err);
+    return cudaGetLastError() == cudaSuccess;
+}
+
+}  // namespace
+
+bool tc_make_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int box_rows) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    if (cols % kBK != 0 || (reinterpret_cast<uintptr_t>(base) & 15) != 0) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+    const cuuint32_t box[2] = {(cuuint32_t)kBK, (cuuint32_t)box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
+                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+int tc_token_tile(int T) { return T > 128 ? 256 : 128; }
+
+bool tc_shape_ok(int64_t M, int64_t K, int epi, int64_t F) {
+    if (K % kBK != 0 || K < kBK) return false;
+    if (epi == GEMM_EPI_SWIGLU) return F % 64 == 0 && F > 0;
+    return M % kBM == 0 && M > 0;
+}
+
+bool launch_gemm_tc(const CUtensorMap& wmap, const CUtensorMap& xmap, int epi, int K, int M,
+                    int T, int F, void* Y, int ldy, uint32_t* err, cudaStream_t st) {
+    if (T <= 0) return true;
+    const int bn = tc_token_tile(T);
+    switch (epi) {
+        case GEMM_EPI_STORE:
+            return bn == 256 ? launch_tc<256, GEMM_EPI_STORE>(wmap, xmap, K, M, T, F, Y, ldy, err, st)
+                             : launch_tc<128, GEMM_EPI_STORE>(wmap, xmap, K, M, T, F, Y, ldy, err, st);
+        case GEMM_EPI_ADD:
+            return bn == 256 ? launch_tc<256, GEMM_EPI_ADD>(wmap, xmap, K, M, T, F, Y, ldy, err, st)
+                             : launch_tc<128, GEMM_EPI_ADD>(wmap, xmap, K, M, T, F, Y, ldy, err, st);
+        case GEMM_EPI_SWIGLU:
+            return bn == 256 ? launch_tc<256, GEMM_EPI_SWIGLU>(wmap, xmap, K, M, T, F, Y, ldy, err, st)
+                             : launch_tc<128, GEMM_EPI_SWIGLU>(wmap, xmap, K, M, T, F, Y, ldy, err, st);
+    }
+    return false;
+}
+
+}  // namespace llm

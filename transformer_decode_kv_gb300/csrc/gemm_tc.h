@@ -1,0 +1,32 @@
+// Tensor-core (tcgen05 + TMA + TMEM) BF16 GEMM for prefill ubatches. See gemm_tc.cu.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+namespace llm {
+
+enum GemmEpi : int32_t {
+    GEMM_EPI_STORE = 0,    // Y[t][m] = acc (float32)
+    GEMM_EPI_ADD = 1,      // Y[t][m] += acc (float32, the residual add)
+    GEMM_EPI_SWIGLU = 2,   // Y[t][j] = silu(gate_j) * up_j (bf16); W rows [0,F) gate, [F,2F) up
+};
+
+// TMA map of a row-major bf16 matrix [rows][cols] (cols % 64 == 0, base 16-byte aligned), loaded
+// in boxes of 64 columns x box_rows rows with the 128-byte swizzle.
+bool tc_make_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int box_rows);
+
+// Token tile the launcher uses for T tokens (the activation map's box height must match).
+int tc_token_tile(int T);
+
+// Whether the tensor-core path supports a weight of M rows (or F gate/up rows) by K columns.
+bool tc_shape_ok(int64_t M, int64_t K, int epi, int64_t F);
+
+// Y (op)= X W^T for T tokens: wmap over W [rows][K] (box 128 rows, or 64 for SWIGLU), xmap over
+// X [>= T rows][K] bf16 (box rows = tc_token_tile(T)). Returns false on a launch failure.
+bool launch_gemm_tc(const CUtensorMap& wmap, const CUtensorMap& xmap, int epi, int K, int M,
+                    int T, int F, void* Y, int ldy, uint32_t* err, cudaStream_t st);
+
+}  // namespace llm

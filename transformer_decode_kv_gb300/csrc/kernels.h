@@ -21,7 +21,7 @@ struct DevMat {
 };
 
 // Device error word bits, set by kernels' own bounds checks.
-enum : uint32_t { ERR_SLOT_RANGE = 1u, ERR_TOKEN_RANGE = 2u, ERR_ROW_RANGE = 4u };
+enum : uint32_t { ERR_SLOT_RANGE = 1u, ERR_TOKEN_RANGE = 2u, ERR_ROW_RANGE = 4u, ERR_TIMEOUT = 8u };
 
 // ---- elementwise / small kernels (kernels_misc.cu) --------------------------------------------
 // x[t] = row tok[t] of the embedding table, as float32 ([P2] Example 4, GET_ROWS).

@@ -16,6 +16,7 @@
 #include <string>
 #include <vector>
 
+#include "gemm_tc.h"
 #include "host_plan.h"
 #include "kernels.h"
 
@@ -907,6 +908,26 @@ int32_t llm_debug_kernel_stats(llm_ctx* c, int32_t i, char* name, int32_t name_c
         if (flops) *flops = c->kstat[i].flops;
     }
     return KC_COUNT;
+}
+
+int llm_debug_gemm_bf16(int32_t epi, const void* W, int64_t M, int64_t K, const void* X, int32_t T,
+                        void* Y, int32_t ldy, int32_t F) {
+    if (!W || !X || !Y || T <= 0 || epi < 0 || epi > 2) return -1;
+    if (!tc_shape_ok(M, K, epi, F)) return -1;
+    const int64_t wrows = epi == GEMM_EPI_SWIGLU ? 2 * (int64_t)F : M;
+    CUtensorMap wm, xm;
+    if (!tc_make_map(&wm, W, wrows, K, epi == GEMM_EPI_SWIGLU ? 64 : 128) ||
+        !tc_make_map(&xm, X, T, K, tc_token_tile(T)))
+        return -1;
+    uint32_t* err = nullptr;
+    if (cudaMalloc(&err, sizeof(uint32_t)) != cudaSuccess) return -3;
+    cudaMemset(err, 0, sizeof(uint32_t));
+    bool ok = launch_gemm_tc(wm, xm, epi, (int)K, (int)M, T, F, Y, ldy, err, 0);
+    uint32_t h = 0;
+    ok = ok && cudaDeviceSynchronize() == cudaSuccess &&
+         cudaMemcpy(&h, err, sizeof(uint32_t), cudaMemcpyDeviceToHost) == cudaSuccess;
+    cudaFree(err);
+    return ok && h == 0 ? 0 : -3;
 }
 
 int llm_debug_inject_fault(llm_ctx* c, int32_t kind, int32_t ub) {
