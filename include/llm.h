@@ -254,6 +254,20 @@ int32_t llm_debug_kernel_stats(llm_ctx *ctx, int32_t i, char *name, int32_t name
 int llm_debug_gemm_bf16(int32_t epi, const void *W, int64_t M, int64_t K, const void *X, int32_t T,
                         void *Y, int32_t ldy, int32_t F);
 
+/* The same GEMM as llm_debug_gemm_bf16, for callers that cannot allocate device memory (for
+ * example engines that reserve all GPU memory up front for their own pools, or code that must
+ * not trigger the device-wide synchronisation cudaFree performs). The pages have no counterpart:
+ * this is an interface of this library only. The call allocates nothing: its scratch (the
+ * kernel's error word) is a fixed 256-byte array inside the library that every GPU which loads
+ * the library holds until the process exits. The first call on a device looks that array's
+ * device address up (cudaGetSymbolAddress) with the device current; make that first call before
+ * starting any stream capture. Every call shares the array, so calls whose GPU work overlaps
+ * (from several host threads or streams) race on it. Arguments, limits and results are those of
+ * llm_debug_gemm_bf16: -1 for an unsupported shape, -3 if the launch failed or the kernel
+ * reported an error. Synchronous (legacy default stream). */
+int llm_gemm_bf16_noalloc(int32_t epi, const void *W, int64_t M, int64_t K, const void *X,
+                          int32_t T, void *Y, int32_t ldy, int32_t F);
+
 /* Fault injection: kind 1 makes ubatch `ub` of the next llm_decode hand the K/V append kernel a
  * cell index past the cache; the kernel's bounds check skips the write and reports the error
  * word, so llm_decode returns -3 and rolls that ubatch back. kind 0 clears it. */

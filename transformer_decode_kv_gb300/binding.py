@@ -75,6 +75,8 @@ SIGNATURES = {
                                          C.POINTER(C.c_float), C.c_int64]),
     "llm_debug_inject_fault": (C.c_int, [C.c_void_p, C.c_int32, C.c_int32]),
     "llm_debug_kernel_timing": (C.c_int, [C.c_void_p, C.c_int]),
+    "llm_gemm_bf16_noalloc": (C.c_int, [C.c_int32, C.c_void_p, C.c_int64, C.c_int64, C.c_void_p,
+                                        C.c_int32, C.c_void_p, C.c_int32, C.c_int32]),
     "llm_debug_gemm_bf16": (C.c_int, [C.c_int32, C.c_void_p, C.c_int64, C.c_int64, C.c_void_p,
                                       C.c_int32, C.c_void_p, C.c_int32, C.c_int32]),
     "llm_debug_kernel_stats": (C.c_int32, [C.c_void_p, C.c_int32, C.c_char_p, C.c_int32,
@@ -118,6 +120,13 @@ def debug_gemm_bf16(epi: int, W, X, Y, F: int = 0) -> int:
     return lib().llm_debug_gemm_bf16(epi, C.c_void_p(W.data_ptr()), W.shape[0], W.shape[1],
                                      C.c_void_p(X.data_ptr()), X.shape[0], C.c_void_p(Y.data_ptr()),
                                      Y.stride(0), F)
+
+
+def gemm_bf16_noalloc(epi: int, W, X, Y, F: int = 0) -> int:
+    """The same GEMM through the entry point that allocates no device memory."""
+    return lib().llm_gemm_bf16_noalloc(epi, C.c_void_p(W.data_ptr()), W.shape[0], W.shape[1],
+                                       C.c_void_p(X.data_ptr()), X.shape[0],
+                                       C.c_void_p(Y.data_ptr()), Y.stride(0), F)
 
 
 class Context:
