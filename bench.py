@@ -270,17 +270,26 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--workload", default="llama8b_bf16_1seq")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="profiling aid: run the workload's shape with only this many layers "
+                         "(a small case for ncu captures; not a bench number)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     rank, world = _env_int("RANK", 0), _env_int("WORLD_SIZE", 1)
     local_rank = _env_int("LOCAL_RANK", 0)
+    import dataclasses
     import synthetic as S
     w = S.WORKLOADS[args.workload]
+    if args.layers:
+        w = dataclasses.replace(w, hp=dataclasses.replace(w.hp, n_layer=args.layers))
+        S.WORKLOADS[args.workload] = w
     config = {"workload": args.workload, "description": w.description,
               "prompt_tokens": w.n_prompt, "decode_steps_timed": args.steps,
               "n_ctx": w.n_ctx, "kv_cache": "f16" if w.type_kv == 1 else "f32",
               "l2": "inputs larger than L2: every decode step streams all weights (no flush)",
               "parallelism": "replicas" if args.gpus > 1 else "single"}
+    if args.layers:
+        config["profiling_case_layers"] = args.layers
 
     if args.impl == "reference":
         if rank != 0:

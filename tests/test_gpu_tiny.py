@@ -127,6 +127,12 @@ def test_error_paths_on_gpu():
     ref = G.library_ctx(key, n_ctx=256, n_batch=256, n_ubatch=16)
     assert ref.decode(toks) == 0
     assert G.rel_err(ctx.get_logits_ith(-1), ref.get_logits_ith(-1).astype(np.float64)) < 1e-6
+    # the same bounds check inside the fused decode-step kernels
+    p = ctx.seq_pos_max(0)
+    ctx.inject_fault(1, 0)
+    assert ctx.decode([7]) == -3
+    assert ctx.seq_pos_max(0) == p
+    assert ctx.decode([7]) == 0 and ctx.seq_pos_max(0) == p + 1
     # abort before the second ubatch
     calls = []
     ref.set_abort_callback(lambda: (calls.append(1), len(calls) == 2)[1])

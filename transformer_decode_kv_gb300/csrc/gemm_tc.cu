@@ -134,26 +134,29 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-template <int BN>
+// SPLIT: the activations come as two bf16 terms (hi + lo, about 16 significant bits); both are
+// multiplied into the same accumulator, so the product keeps float32-like activation precision.
+template <int BN, bool SPLIT = false>
 struct TcCfg {
-    static constexpr int kStages = BN == 256 ? 4 : 6;
     static constexpr uint32_t kA = kBM * kBK * 2;          // 16 KB
     static constexpr uint32_t kB = BN * kBK * 2;
-    static constexpr size_t kSmem = 1024 + (size_t)kStages * (kA + kB) + 256;
+    static constexpr uint32_t kStageB = SPLIT ? 2 * kB : kB;
+    static constexpr int kStages = (int)((196608u) / (kA + kStageB));
+    static constexpr size_t kSmem = 1024 + (size_t)kStages * (kA + kStageB) + 256;
 };
 
-template <int BN, int EPI>
+template <int BN, int EPI, bool SPLIT>
 __global__ void __launch_bounds__(128, 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-               int K, int M, int T, int F, void* __restrict__ Y, int ldy,
-               uint32_t* __restrict__ err) {
-    using C = TcCfg<BN>;
+               const __grid_constant__ CUtensorMap tmB2, int K, int M, int T, int F,
+               void* __restrict__ Y, void* __restrict__ Y2, int ldy, uint32_t* __restrict__ err) {
+    using C = TcCfg<BN, SPLIT>;
     constexpr int S = C::kStages;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     uint8_t* sA = smem;
     uint8_t* sB = smem + S * C::kA;
-    uint64_t* full = reinterpret_cast<uint64_t*>(sB + S * C::kB);
+    uint64_t* full = reinterpret_cast<uint64_t*>(sB + S * C::kStageB);
     uint64_t* empty = full + S;
     uint64_t* accf = empty + S;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accf + 1);
@@ -174,6 +177,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmA)) : "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmB)) : "memory");
+        if (SPLIT)
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmB2)) : "memory");
     }
     if (warp == 0) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -194,14 +199,15 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             const uint32_t ph = (uint32_t)(kb / S) & 1u;
             if (kb >= S && !mbar_wait(&empty[s], ph ^ 1u)) { atomicOr(err, ERR_TIMEOUT); *(volatile int*)abort_flag = 1; break; }
             if (*(volatile int*)abort_flag) break;
-            mbar_expect_tx(&full[s], C::kA + C::kB);
+            mbar_expect_tx(&full[s], C::kA + C::kStageB);
             if (EPI == GEMM_EPI_SWIGLU) {
                 tma_load_2d(sA + s * C::kA, &tmA, &full[s], kb * kBK, row0);
                 tma_load_2d(sA + s * C::kA + C::kA / 2, &tmA, &full[s], kb * kBK, F + row0);
             } else {
                 tma_load_2d(sA + s * C::kA, &tmA, &full[s], kb * kBK, row0);
             }
-            tma_load_2d(sB + s * C::kB, &tmB, &full[s], kb * kBK, t0);
+            tma_load_2d(sB + s * C::kStageB, &tmB, &full[s], kb * kBK, t0);
+            if (SPLIT) tma_load_2d(sB + s * C::kStageB + C::kB, &tmB2, &full[s], kb * kBK, t0);
             issued = kb + 1;
         }
         // drain: every copy this thread issued has landed before the block can exit
@@ -217,11 +223,17 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             if (!mbar_wait(&full[s], ph)) { ok = false; break; }
             tc_fence_after();
             const uint64_t ad = sdesc_sw128(smem_u32(sA + s * C::kA));
-            const uint64_t bd = sdesc_sw128(smem_u32(sB + s * C::kB));
+            const uint64_t bd = sdesc_sw128(smem_u32(sB + s * C::kStageB));
 #pragma unroll
             for (int kk = 0; kk < kBK / 16; ++kk)
                 umma_bf16(tmem, ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2), idesc,
                           (kb | kk) != 0 ? 1u : 0u);
+            if (SPLIT) {
+                const uint64_t bd2 = sdesc_sw128(smem_u32(sB + s * C::kStageB + C::kB));
+#pragma unroll
+                for (int kk = 0; kk < kBK / 16; ++kk)
+                    umma_bf16(tmem, ad + (uint64_t)(kk * 2), bd2 + (uint64_t)(kk * 2), idesc, 1u);
+            }
             umma_commit(&empty[s]);
         }
         if (!ok) { atomicOr(err, ERR_TIMEOUT); *(volatile int*)abort_flag = 1; }
@@ -273,7 +285,11 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     const float g = v[j];
                     const float u = xu[(warp * 32 + lane) * 17 + j];
                     const float o = g / (1.0f + expf(-g)) * u;
-                    static_cast<__nv_bfloat16*>(Y)[(int64_t)t * ldy + jrow] = __float2bfloat16_rn(o);
+                    const __nv_bfloat16 hi = __float2bfloat16_rn(o);
+                    static_cast<__nv_bfloat16*>(Y)[(int64_t)t * ldy + jrow] = hi;
+                    if (Y2)      // low term of the split output (the next GEMM's second operand)
+                        static_cast<__nv_bfloat16*>(Y2)[(int64_t)t * ldy + jrow] =
+                            __float2bfloat16_rn(o - __bfloat162float(hi));
                 }
             }
             __syncthreads();
@@ -299,11 +315,11 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-template <int BN, int EPI>
-bool launch_tc(const CUtensorMap& a, const CUtensorMap& b, int K, int M, int T, int F, void* Y,
-               int ldy, uint32_t* err, cudaStream_t st) {
-    using C = TcCfg<BN>;
-    auto k = gemm_tc_kernel<BN, EPI>;
+template <int BN, int EPI, bool SPLIT>
+bool launch_tc(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& b2, int K, int M,
+               int T, int F, void* Y, void* Y2, int ldy, uint32_t* err, cudaStream_t st) {
+    using C = TcCfg<BN, SPLIT>;
+    auto k = gemm_tc_kernel<BN, EPI, SPLIT>;
     static bool attr = false;
     if (!attr) {
         if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem) != cudaSuccess)
@@ -313,8 +329,19 @@ bool launch_tc(const CUtensorMap& a, const CUtensorMap& b, int K, int M, int T, 
     const int rows_per_tile = EPI == GEMM_EPI_SWIGLU ? 64 : kBM;
     const int mtiles = (EPI == GEMM_EPI_SWIGLU ? F : M) / rows_per_tile;
     dim3 grid(mtiles, (T + BN - 1) / BN);
-    k<<<grid, 128, C::kSmem, st>>>(a, b, K, M, T, F, Y, ldy, err);
+    k<<<grid, 128, C::kSmem, st>>>(a, b, b2, K, M, T, F, Y, Y2, ldy, err);
     return cudaGetLastError() == cudaSuccess;
+}
+
+template <int EPI>
+bool launch_epi(const CUtensorMap& wmap, const CUtensorMap& xmap, const CUtensorMap* xmap_lo,
+                int K, int M, int T, int F, void* Y, void* Y2, int ldy, uint32_t* err,
+                cudaStream_t st) {
+    if (xmap_lo)
+        return launch_tc<128, EPI, true>(wmap, xmap, *xmap_lo, K, M, T, F, Y, Y2, ldy, err, st);
+    if (tc_token_tile(T) == 256)
+        return launch_tc<256, EPI, false>(wmap, xmap, xmap, K, M, T, F, Y, Y2, ldy, err, st);
+    return launch_tc<128, EPI, false>(wmap, xmap, xmap, K, M, T, F, Y, Y2, ldy, err, st);
 }
 
 }  // namespace
@@ -343,19 +370,16 @@ bool tc_shape_ok(int64_t M, int64_t K, int epi, int64_t F) {
 }
 
 bool launch_gemm_tc(const CUtensorMap& wmap, const CUtensorMap& xmap, int epi, int K, int M,
-                    int T, int F, void* Y, int ldy, uint32_t* err, cudaStream_t st) {
+                    int T, int F, void* Y, int ldy, uint32_t* err, cudaStream_t st,
+                    const CUtensorMap* xmap_lo, void* Y2) {
     if (T <= 0) return true;
-    const int bn = tc_token_tile(T);
     switch (epi) {
         case GEMM_EPI_STORE:
-            return bn == 256 ? launch_tc<256, GEMM_EPI_STORE>(wmap, xmap, K, M, T, F, Y, ldy, err, st)
-                             : launch_tc<128, GEMM_EPI_STORE>(wmap, xmap, K, M, T, F, Y, ldy, err, st);
+            return launch_epi<GEMM_EPI_STORE>(wmap, xmap, xmap_lo, K, M, T, F, Y, Y2, ldy, err, st);
         case GEMM_EPI_ADD:
-            return bn == 256 ? launch_tc<256, GEMM_EPI_ADD>(wmap, xmap, K, M, T, F, Y, ldy, err, st)
-                             : launch_tc<128, GEMM_EPI_ADD>(wmap, xmap, K, M, T, F, Y, ldy, err, st);
+            return launch_epi<GEMM_EPI_ADD>(wmap, xmap, xmap_lo, K, M, T, F, Y, Y2, ldy, err, st);
         case GEMM_EPI_SWIGLU:
-            return bn == 256 ? launch_tc<256, GEMM_EPI_SWIGLU>(wmap, xmap, K, M, T, F, Y, ldy, err, st)
-                             : launch_tc<128, GEMM_EPI_SWIGLU>(wmap, xmap, K, M, T, F, Y, ldy, err, st);
+            return launch_epi<GEMM_EPI_SWIGLU>(wmap, xmap, xmap_lo, K, M, T, F, Y, Y2, ldy, err, st);
     }
     return false;
 }

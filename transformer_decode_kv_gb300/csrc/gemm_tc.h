@@ -25,8 +25,11 @@ int tc_token_tile(int T);
 bool tc_shape_ok(int64_t M, int64_t K, int epi, int64_t F);
 
 // Y (op)= X W^T for T tokens: wmap over W [rows][K] (box 128 rows, or 64 for SWIGLU), xmap over
-// X [>= T rows][K] bf16 (box rows = tc_token_tile(T)). Returns false on a launch failure.
+// X [>= T rows][K] bf16 (box rows = tc_token_tile(T)). With xmap_lo (box rows 128) the activations
+// are X = hi + lo, two bf16 terms both multiplied into the accumulator; SWIGLU then also writes
+// the low term of its bf16 output to Y2. Returns false on a launch failure.
 bool launch_gemm_tc(const CUtensorMap& wmap, const CUtensorMap& xmap, int epi, int K, int M,
-                    int T, int F, void* Y, int ldy, uint32_t* err, cudaStream_t st);
+                    int T, int F, void* Y, int ldy, uint32_t* err, cudaStream_t st,
+                    const CUtensorMap* xmap_lo = nullptr, void* Y2 = nullptr);
 
 }  // namespace llm

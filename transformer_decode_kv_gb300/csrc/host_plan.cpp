@@ -156,7 +156,7 @@ void KvCells::seq_rm(int32_t s, int32_t p0, int32_t p1) {
 // ---------------------------------------------------------------------------------------------
 void build_attn_plan(const KvCells& cells, const SanBatch& b, int32_t i0, int32_t T, int32_t tile_q,
                      int32_t n_head_kv, int32_t n_gqa, int32_t target_items, int32_t max_rows,
-                     AttnPlan& p) {
+                     int32_t max_work, AttnPlan& p, int32_t min_chunk) {
     p.list_off.assign(1, 0);
     p.list_cells.clear();
     p.list_pos.clear();
@@ -232,7 +232,7 @@ void build_attn_plan(const KvCells& cells, const SanBatch& b, int32_t i0, int32_
             const int32_t l = p.tile_list[t];
             const int32_t L = p.list_off[l + 1] - p.list_off[l];
             int32_t chunk = (L + want - 1) / want;
-            chunk = std::max(32, (chunk + 31) / 32 * 32);
+            chunk = std::max(min_chunk, (chunk + 31) / 32 * 32);
             for (int32_t c0 = 0; c0 < std::max(L, 1); c0 += chunk) {
                 p.wi_tile.push_back(t);
                 p.wi_c0.push_back(c0);
@@ -241,7 +241,8 @@ void build_attn_plan(const KvCells& cells, const SanBatch& b, int32_t i0, int32_
             }
             p.tile_wi_off.push_back((int32_t)p.wi_tile.size());
         }
-        if (p.wi_row_off.back() <= max_rows || want == 1) break;
+        if ((p.wi_row_off.back() <= max_rows && (int32_t)p.wi_tile.size() <= max_work) || want == 1)
+            break;
         want = std::max(1, want / 2);
     }
 }

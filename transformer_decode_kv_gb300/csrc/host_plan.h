@@ -104,10 +104,10 @@ struct AttnPlan {
 // Build the plan for ubatch tokens [i0, i0 + T) of a sanitised batch. target_items is the number
 // of (work item x KV head) blocks the split aims for; chunk sizes are multiples of 32 cells. A work
 // item of a tile with nq tokens produces nq * n_gqa partial rows; the split is coarsened until
-// the rows of all work items fit in max_rows (one item per tile always fits when
-// max_rows >= T * n_gqa).
+// the rows of all work items fit in max_rows and the items in max_work (one item per tile
+// always fits when max_rows >= T * n_gqa and max_work >= T).
 void build_attn_plan(const KvCells& cells, const SanBatch& b, int32_t i0, int32_t T,
                      int32_t tile_q, int32_t n_head_kv, int32_t n_gqa, int32_t target_items,
-                     int32_t max_rows, AttnPlan& plan);
+                     int32_t max_rows, int32_t max_work, AttnPlan& plan, int32_t min_chunk = 32);
 
 }  // namespace llm

@@ -24,15 +24,13 @@ struct DevMat {
 enum : uint32_t { ERR_SLOT_RANGE = 1u, ERR_TOKEN_RANGE = 2u, ERR_ROW_RANGE = 4u, ERR_TIMEOUT = 8u };
 
 // ---- elementwise / small kernels (kernels_misc.cu) --------------------------------------------
-// x[t] = row tok[t] of the embedding table, as float32 ([P2] Example 4, GET_ROWS).
-void launch_embed(const DevMat& E, const int32_t* tok, int32_t T, float* x, uint32_t* err,
-                  cudaStream_t st);
 // y[r] = x[rows ? rows[r] : r] / sqrt(mean(x^2) + eps) * g, r < R, width d (RMS_NORM + MUL).
 void launch_rmsnorm(const float* x, const int32_t* rows, int32_t R, int32_t d, const float* g,
                     float eps, float* y, cudaStream_t st);
-// cos/sin of pos[t] * base^(-2i/hd) for i < hd/2, computed in double: cs[t][i] = {cos, sin}.
-void launch_rope_table(const int32_t* pos, int32_t T, int32_t hd, float base, float2* cs,
-                       cudaStream_t st);
+// The same with a bf16 output (the A/B operand of a tensor-core GEMM).
+// yb_lo (optional) receives the low bf16 term: y = yb + yb_lo to about 16 bits.
+void launch_rmsnorm_bf16(const float* x, const int32_t* rows, int32_t R, int32_t d,
+                         const float* g, float eps, void* yb, void* yb_lo, cudaStream_t st);
 // RoPE (adjacent pairs) on the q and k parts of qkv [T][(H + 2 Hkv) hd] (q in place), then K and
 // V rows written to their cache cells slot[t] ([P2] Example 4, ROPE + SET_ROWS). Cache layout:
 // [Hkv][n_ctx][hd], element type kv_type (F32 or F16). A slot outside [0, n_ctx) skips the write
@@ -42,8 +40,20 @@ void launch_rope_kv_append(float* qkv, int32_t T, int32_t H, int32_t Hkv, int32_
                            int32_t n_ctx, int32_t kv_type, uint32_t* err, cudaStream_t st);
 // u[t][j] = silu(g[t][j]) * up[t][j] with gu = [T][2F] (gate then up) -> u [T][F].
 void launch_swiglu(const float* gu, int32_t T, int32_t F, float* u, cudaStream_t st);
-// idx[r] = argmax of logits row r (lowest index among equal maxima).
-void launch_argmax(const float* logits, int32_t R, int32_t V, int32_t* idx, cudaStream_t st);
+// amax[r] = the largest logit of row r packed with its index (value in the high word in an
+// order-preserving encoding, 0xFFFFFFFF - index in the low word: the lowest index wins ties).
+void launch_argmax(const float* logits, int32_t R, int32_t V, unsigned long long* amax,
+                   cudaStream_t st);
+// Decode a packed argmax (-1 if none).
+inline int32_t unpack_argmax(unsigned long long p) {
+    return p == 0 ? -1 : (int32_t)(0xFFFFFFFFu - (uint32_t)(p & 0xFFFFFFFFull));
+}
+// Per token: x[t] = embedding row tok[t]; cs[t][i] = (cos, sin) of pos[t] * theta[i] with
+// theta[i] = base^(-2i/hd) (a double table), the angle reduced in double before a float
+// sincos; amax[0..n_amax) reset to 0.
+void launch_embed_rope(const DevMat& E, const int32_t* tok, const int32_t* pos, int32_t T,
+                       int32_t hd, const double* theta, float* x, float2* cs,
+                       unsigned long long* amax, int32_t n_amax, uint32_t* err, cudaStream_t st);
 // Split Q8_0 blocks (34 bytes: fp16 d, 32 int8 q) into quants [rows][cols] and scales.
 void launch_q8_0_unpack(const uint8_t* blocks, int64_t rows, int64_t cols, int8_t* q,
                         __half* d, cudaStream_t st);
@@ -75,17 +85,24 @@ struct AttnArgs {
     const void* vc;
     int32_t n_ctx, kv_type, H, Hkv, hd;
     const int32_t* tok_pos;  // [T]
-    const int32_t* list_off; const int32_t* list_cells; const int32_t* list_pos;
+    const int32_t* list_cells; const int32_t* list_pos;   // concatenated cell lists
     const int32_t* perm;     // [T] tokens grouped by list
-    const int32_t* tile_list; const int32_t* tile_start; const int32_t* tile_nq;
-    const int32_t* tile_wi_off;
-    const int32_t* wi_tile; const int32_t* wi_c0; const int32_t* wi_c1; const int32_t* wi_row_off;
+    const int4* tile_desc;   // per tile, 2 x int4: {list, first token, tokens, first item},
+                             //                     {end item, list start, list length, 0}
+    const int4* wi_desc;     // per work item: {tile, first cell, end cell, first partial row}
+    int32_t* tickets;        // [tiles][Hkv] zero between launches (blocks done per tile)
     float* part_o;           // [rows][Hkv][hd] unnormalised partial outputs
     float* part_m;           // [rows][Hkv] running max (log2 domain)
     float* part_l;           // [rows][Hkv] running sum
     float* out;              // [T][H * hd]
+    void* out_b;             // if set: bf16 output [T][H * hd] instead of out
+    void* out_b_lo;          // with out_b: the low bf16 term of the output
     int32_t ldo;
-    int32_t n_work, n_tiles, max_nq;
+    const int32_t* hdr;      // device: [0] work items of this ubatch
+    int32_t n_work, max_nq;  // grid size (an upper bound of the device count), tile shape
+    bool pdl;                // programmatic dependent launch after the previous kernel
+    const int32_t* slot;     // decode steps: the cells this ubatch writes (n_tok of them)
+    int32_t n_tok;
 };
 // Grouped-query attention of every token over the cells of its list with cell.pos <= token.pos:
 // split-K partial softmax per work item, then a combine per tile ([P2] Example 4 FLASH_ATTN_EXT;

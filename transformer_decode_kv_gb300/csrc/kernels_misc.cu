@@ -1,4 +1,4 @@
-// Small kernels of the decode path: embedding gather, RMSNorm, RoPE table, RoPE + K/V append,
+// Small kernels of the decode path: embedding gather with the RoPE table, RMSNorm, RoPE + K/V append,
 // SwiGLU, greedy argmax and the Q8_0 block split.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -41,19 +41,15 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
     return v;
 }
 
-__global__ void embed_kernel(DevMat E, const int32_t* __restrict__ tok, float* __restrict__ x,
-                             uint32_t* err) {
-    const int t = blockIdx.x;
-    const int32_t id = tok[t];
-    const bool ok = id >= 0 && id < E.rows;
-    if (!ok && threadIdx.x == 0) atomicOr(err, ERR_TOKEN_RANGE);
-    for (int64_t j = threadIdx.x; j < E.cols; j += blockDim.x)
-        x[(int64_t)t * E.cols + j] = ok ? load_elem(E, id, j) : 0.f;
+__device__ __forceinline__ void store_out(float* y, int64_t i, float v) { y[i] = v; }
+__device__ __forceinline__ void store_out(__nv_bfloat16* y, int64_t i, float v) {
+    y[i] = __float2bfloat16_rn(v);
 }
 
+template <typename OT>
 __global__ void rmsnorm_kernel(const float* __restrict__ x, const int32_t* __restrict__ rows,
                                int d, const float* __restrict__ g, float eps,
-                               float* __restrict__ y) {
+                               OT* __restrict__ y, __nv_bfloat16* __restrict__ ylo) {
     __shared__ float red[32];
     const int r = blockIdx.x;
     const int src = rows ? rows[r] : r;
@@ -62,18 +58,14 @@ __global__ void rmsnorm_kernel(const float* __restrict__ x, const int32_t* __res
     for (int j = threadIdx.x; j < d; j += blockDim.x) ss += xr[j] * xr[j];
     ss = block_sum(ss, red);
     const float inv = 1.0f / sqrtf(ss / (float)d + eps);
-    for (int j = threadIdx.x; j < d; j += blockDim.x) y[(int64_t)r * d + j] = xr[j] * inv * g[j];
-}
-
-__global__ void rope_table_kernel(const int32_t* __restrict__ pos, int T, int half, double base,
-                                  float2* __restrict__ cs) {
-    const int idx = blockIdx.x * blockDim.x + threadIdx.x;
-    if (idx >= T * half) return;
-    const int t = idx / half, i = idx % half;
-    const double theta = pow(base, -2.0 * (double)i / (double)(2 * half));
-    double s, c;
-    sincos((double)pos[t] * theta, &s, &c);
-    cs[idx] = make_float2((float)c, (float)s);
+    for (int j = threadIdx.x; j < d; j += blockDim.x) {
+        const float v = xr[j] * inv * g[j];
+        store_out(y, (int64_t)r * d + j, v);
+        if (ylo) {
+            const float hi = __bfloat162float(__float2bfloat16_rn(v));
+            ylo[(int64_t)r * d + j] = __float2bfloat16_rn(v - hi);
+        }
+    }
 }
 
 template <typename KT>
@@ -131,7 +123,37 @@ __global__ void swiglu_kernel(const float* __restrict__ gu, int64_t T, int F,
     u[idx] = g / (1.0f + expf(-g)) * up;
 }
 
-__global__ void argmax_kernel(const float* __restrict__ logits, int V, int32_t* __restrict__ out) {
+__device__ __forceinline__ unsigned long long pack_max(float v, int idx) {
+    uint32_t u = __float_as_uint(v);
+    u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+    return ((unsigned long long)u << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)idx);
+}
+
+__global__ void embed_rope_kernel(DevMat E, const int32_t* __restrict__ tok,
+                                  const int32_t* __restrict__ pos, int half,
+                                  const double* __restrict__ theta, float* __restrict__ x,
+                                  float2* __restrict__ cs, unsigned long long* __restrict__ amax,
+                                  int n_amax, uint32_t* err) {
+    const int t = blockIdx.x;
+    const int32_t id = tok[t];
+    const bool ok = id >= 0 && id < E.rows;
+    if (!ok && threadIdx.x == 0) atomicOr(err, ERR_TOKEN_RANGE);
+    for (int64_t j = threadIdx.x; j < E.cols; j += blockDim.x)
+        x[(int64_t)t * E.cols + j] = ok ? load_elem(E, id, j) : 0.f;
+    for (int i = threadIdx.x; i < half; i += blockDim.x) {
+        // the angle pos * theta_i in double, reduced to [-pi, pi] in double, then float sincos
+        const double ang = (double)pos[t] * theta[i];
+        const double r = ang - rint(ang * 0.15915494309189535) * 6.283185307179586;
+        float s, c;
+        sincosf((float)r, &s, &c);
+        cs[(int64_t)t * half + i] = make_float2(c, s);
+    }
+    if (t == 0)
+        for (int i = threadIdx.x; i < n_amax; i += blockDim.x) amax[i] = 0ull;
+}
+
+__global__ void argmax_kernel(const float* __restrict__ logits, int V,
+                              unsigned long long* __restrict__ out) {
     __shared__ float sv[32];
     __shared__ int si[32];
     const float* row = logits + (int64_t)blockIdx.x * V;
@@ -158,7 +180,7 @@ __global__ void argmax_kernel(const float* __restrict__ logits, int V, int32_t* 
             const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
             if (ov > best || (ov == best && oi < bi)) { best = ov; bi = oi; }
         }
-        if (l == 0) out[blockIdx.x] = bi == INT_MAX ? -1 : bi;
+        if (l == 0) out[blockIdx.x] = bi == INT_MAX ? 0ull : pack_max(best, bi);
     }
 }
 
@@ -177,23 +199,17 @@ __global__ void q8_0_unpack_kernel(const uint8_t* __restrict__ blocks, int64_t n
 
 }  // namespace
 
-void launch_embed(const DevMat& E, const int32_t* tok, int32_t T, float* x, uint32_t* err,
-                  cudaStream_t st) {
-    if (T <= 0) return;
-    embed_kernel<<<T, 256, 0, st>>>(E, tok, x, err);
-}
-
 void launch_rmsnorm(const float* x, const int32_t* rows, int32_t R, int32_t d, const float* g,
                     float eps, float* y, cudaStream_t st) {
     if (R <= 0) return;
-    rmsnorm_kernel<<<R, d >= 1024 ? 512 : 256, 0, st>>>(x, rows, d, g, eps, y);
+    rmsnorm_kernel<float><<<R, d >= 1024 ? 512 : 256, 0, st>>>(x, rows, d, g, eps, y, nullptr);
 }
 
-void launch_rope_table(const int32_t* pos, int32_t T, int32_t hd, float base, float2* cs,
-                       cudaStream_t st) {
-    const int n = T * (hd / 2);
-    if (n <= 0) return;
-    rope_table_kernel<<<(n + 255) / 256, 256, 0, st>>>(pos, T, hd / 2, (double)base, cs);
+void launch_rmsnorm_bf16(const float* x, const int32_t* rows, int32_t R, int32_t d,
+                         const float* g, float eps, void* yb, void* yb_lo, cudaStream_t st) {
+    if (R <= 0) return;
+    rmsnorm_kernel<__nv_bfloat16><<<R, d >= 1024 ? 512 : 256, 0, st>>>(
+        x, rows, d, g, eps, static_cast<__nv_bfloat16*>(yb), static_cast<__nv_bfloat16*>(yb_lo));
 }
 
 void launch_rope_kv_append(float* qkv, int32_t T, int32_t H, int32_t Hkv, int32_t hd,
@@ -214,9 +230,17 @@ void launch_swiglu(const float* gu, int32_t T, int32_t F, float* u, cudaStream_t
     swiglu_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(gu, T, F, u);
 }
 
-void launch_argmax(const float* logits, int32_t R, int32_t V, int32_t* idx, cudaStream_t st) {
+void launch_argmax(const float* logits, int32_t R, int32_t V, unsigned long long* amax,
+                   cudaStream_t st) {
     if (R <= 0) return;
-    argmax_kernel<<<R, 1024, 0, st>>>(logits, V, idx);
+    argmax_kernel<<<R, 1024, 0, st>>>(logits, V, amax);
+}
+
+void launch_embed_rope(const DevMat& E, const int32_t* tok, const int32_t* pos, int32_t T,
+                       int32_t hd, const double* theta, float* x, float2* cs,
+                       unsigned long long* amax, int32_t n_amax, uint32_t* err, cudaStream_t st) {
+    if (T <= 0) return;
+    embed_rope_kernel<<<T, 256, 0, st>>>(E, tok, pos, hd / 2, theta, x, cs, amax, n_amax, err);
 }
 
 void launch_q8_0_unpack(const uint8_t* blocks, int64_t rows, int64_t cols, int8_t* q, __half* d,

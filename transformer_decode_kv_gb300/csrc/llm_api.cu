@@ -11,12 +11,15 @@
 
 #include <algorithm>
 #include <chrono>
+#include <cmath>
 #include <cstdio>
 #include <cstring>
+#include <map>
 #include <string>
 #include <vector>
 
 #include "gemm_tc.h"
+#include "gemv_bulk.h"
 #include "host_plan.h"
 #include "kernels.h"
 
@@ -48,18 +51,36 @@ struct Layer {
     float* attn_norm = nullptr;
     float* ffn_norm = nullptr;
     uint32_t loaded = 0;
+    // TMA maps of the BF16 weights for the tensor-core prefill GEMM
+    CUtensorMap mq, mo, mgu, md;
 };
 
 // Kernel classes timed by llm_debug_kernel_timing.
 enum KClass : int32_t {
     KC_EMBED, KC_ROPE_TABLE, KC_RMSNORM, KC_LINEAR_GEMV, KC_LINEAR_GEMM, KC_ROPE_KV, KC_ATTENTION,
-    KC_LM_HEAD, KC_ARGMAX, KC_COUNT
+    KC_LM_HEAD, KC_ARGMAX, KC_LINEAR_TC, KC_COUNT
 };
 const char* const kKClassNames[KC_COUNT] = {"embed", "rope_table", "rmsnorm", "linear_gemv",
                                             "linear_gemm", "rope_kv_append", "attention",
-                                            "lm_head", "argmax"};
+                                            "lm_head", "argmax", "linear_tcgen05"};
 struct KStat { int64_t launches = 0; double ms = 0, bytes = 0, flops = 0; };
 struct KPending { int32_t cls; cudaEvent_t a, b; double bytes, flops; };
+
+// A captured decode step: the forward pass of one ubatch shape, replayed with new inputs.
+struct StepGraph {
+    cudaGraphExec_t exec = nullptr;
+    std::vector<KPending> timing;   // event pairs recorded inside the graph (timing graphs)
+    std::vector<cudaEvent_t> events;
+};
+
+// Fixed layout (int32 offsets) of the per-ubatch upload buffer, so captured graphs can keep
+// pointers into it: a header, the per-token / per-tile / per-work-item arrays at capacity, then
+// the cell lists.
+struct InLayout {
+    size_t hdr, tok, pos, slot, out_rows, perm, tile_desc, wi_desc, fixed_end, list_cells, list_pos,
+        total;
+    size_t lcap = 0;
+};
 
 // Record of one ubatch for the debug hooks.
 struct UbDebug {
@@ -94,20 +115,30 @@ struct llm_ctx {
     float *x = nullptr, *h = nullptr, *qkv = nullptr, *attn = nullptr, *u = nullptr, *tmp = nullptr;
     float *hout = nullptr;
     float2* rope_cs = nullptr;
+    double* d_theta = nullptr;                 // RoPE frequencies base^(-2i/hd), i < hd/2
+    // bf16 activations feeding the tensor-core GEMM, and their TMA maps (token box 128 / 256)
+    void *hb = nullptr, *attnb = nullptr, *ub = nullptr, *hob = nullptr;
+    void *hb_lo = nullptr, *attnb_lo = nullptr, *ub_lo = nullptr, *hob_lo = nullptr;
+    CUtensorMap m_hb[2], m_attnb[2], m_ub[2], m_hob[2], m_lm;
+    CUtensorMap m_hb_lo, m_attnb_lo, m_ub_lo, m_hob_lo;        // low terms (token box 128)
+    bool tc_ok = false;
     float *part_o = nullptr, *part_m = nullptr, *part_l = nullptr;
+    int32_t* tickets = nullptr;
     int32_t max_rows = 0;
     int32_t* d_in = nullptr;
     int32_t* h_in = nullptr;
     size_t in_cap = 0;
+    InLayout io{};
+    int32_t max_work = 0;
     uint32_t* d_err = nullptr;
     uint32_t* h_err = nullptr;
 
     // outputs of the last decode
     float* d_logits = nullptr;
-    int32_t* d_argmax = nullptr;
+    unsigned long long* d_amax = nullptr;
     int32_t out_cap = 0;
     std::vector<float> h_logits;
-    std::vector<int32_t> h_argmax;
+    std::vector<unsigned long long> h_amax;
     bool h_logits_valid = false, h_argmax_valid = false;
     std::vector<int32_t> output_ids;
     int32_t n_outputs = 0;
@@ -127,7 +158,14 @@ struct llm_ctx {
     std::vector<cudaEvent_t> ev_pool;
     size_t ev_used = 0;
     std::vector<KPending> kpend;
+    std::vector<KPending>* kcap = nullptr;     // set while capturing a timing graph
+    std::vector<cudaEvent_t>* kcap_events = nullptr;
     KStat kstat[KC_COUNT];
+    double att_bytes_now = 0, att_flops_now = 0;
+
+    // decode-step graphs, per (tokens, outputs, output row, tile shape, timing) key
+    bool use_graphs = true, use_pdl = true, use_bulk = true;
+    std::map<uint64_t, StepGraph> graphs;
 
     SanBatch batch;
     AttnPlan plan;
@@ -200,29 +238,58 @@ bool fill_rows(llm_ctx* c, DevMat& m, int64_t row0, int64_t rows, const void* da
            cuda_ok(c, cudaStreamSynchronize(c->st), "sync");
 }
 
-bool ensure_inputs(llm_ctx* c, size_t n_ints) {
-    if (n_ints <= c->in_cap) return true;
-    size_t cap = std::max(n_ints, c->in_cap * 2);
+void drop_graphs(llm_ctx* c) {
+    for (auto& kv : c->graphs) {
+        if (kv.second.exec) cudaGraphExecDestroy(kv.second.exec);
+        for (cudaEvent_t e : kv.second.events) cudaEventDestroy(e);
+    }
+    c->graphs.clear();
+}
+
+InLayout make_layout(size_t U, size_t W, size_t L) {
+    InLayout o{};
+    size_t at = 0;
+    auto take = [&](size_t n) { size_t r = at; at += (n + 31) / 32 * 32; return r; };
+    o.hdr = take(8);
+    o.tok = take(U); o.pos = take(U); o.slot = take(U); o.out_rows = take(U); o.perm = take(U);
+    o.tile_desc = take(8 * U);
+    o.wi_desc = take(4 * W);
+    o.fixed_end = at;
+    o.list_cells = take(L); o.list_pos = take(L);
+    o.total = at;
+    o.lcap = L;
+    return o;
+}
+
+// Make room for `list_len` list entries in the upload buffer (reallocation drops the graphs,
+// whose kernels hold pointers into it).
+bool ensure_inputs(llm_ctx* c, size_t list_len) {
+    if (c->d_in && list_len <= c->io.lcap) return true;
+    const size_t L = std::max(list_len, c->io.lcap * 2);
+    const InLayout io = make_layout((size_t)c->n_ubatch, (size_t)c->max_work, L);
+    drop_graphs(c);
     if (c->h_in) cudaFreeHost(c->h_in);
     dfree(c, c->d_in);
     c->h_in = nullptr;
     c->d_in = nullptr;
-    c->in_cap = 0;
-    if (!cuda_ok(c, cudaMallocHost(&c->h_in, cap * sizeof(int32_t)), "cudaMallocHost")) return false;
-    if (!dalloc(c, &c->d_in, cap)) return false;
-    c->in_cap = cap;
+    c->io = InLayout{};
+    if (!cuda_ok(c, cudaMallocHost(&c->h_in, io.total * sizeof(int32_t)), "cudaMallocHost")) return false;
+    if (!dalloc(c, &c->d_in, io.total)) return false;
+    std::memset(c->h_in, 0, io.total * sizeof(int32_t));
+    c->io = io;
     return true;
 }
 
 bool ensure_outputs(llm_ctx* c, int32_t n) {
     if (n <= c->out_cap) return true;
+    drop_graphs(c);
     dfree(c, c->d_logits);
-    dfree(c, c->d_argmax);
+    dfree(c, c->d_amax);
     c->d_logits = nullptr;
-    c->d_argmax = nullptr;
+    c->d_amax = nullptr;
     c->out_cap = 0;
     if (!dalloc(c, &c->d_logits, (size_t)n * c->hp.n_vocab)) return false;
-    if (!dalloc(c, &c->d_argmax, (size_t)n)) return false;
+    if (!dalloc(c, &c->d_amax, (size_t)n)) return false;
     c->out_cap = n;
     return true;
 }
@@ -241,6 +308,16 @@ void rollback(llm_ctx* c, int32_t i0, int32_t T) {
 // ---- kernel timing --------------------------------------------------------------------------
 int kt_begin(llm_ctx* c) {
     if (!c->ktime) return -1;
+    if (c->kcap) {                                   // capturing a timing graph
+        cudaEvent_t a, b;
+        if (cudaEventCreate(&a) != cudaSuccess) return -1;
+        if (cudaEventCreate(&b) != cudaSuccess) { cudaEventDestroy(a); return -1; }
+        c->kcap_events->push_back(a);
+        c->kcap_events->push_back(b);
+        cudaEventRecordWithFlags(a, c->st, cudaEventRecordExternal);
+        c->kcap->push_back({-1, a, b, 0, 0});
+        return (int)c->kcap->size() - 1;
+    }
     while (c->ev_pool.size() < c->ev_used + 2) {
         cudaEvent_t e;
         if (cudaEventCreate(&e) != cudaSuccess) return -1;
@@ -252,103 +329,124 @@ int kt_begin(llm_ctx* c) {
     return i;
 }
 
+// bytes < 0 marks the attention, whose bytes depend on the step's context (taken at collection)
 void kt_end(llm_ctx* c, int i, int32_t cls, double bytes, double flops) {
     if (i < 0) return;
+    if (c->kcap) {
+        KPending& p = (*c->kcap)[i];
+        cudaEventRecordWithFlags(p.b, c->st, cudaEventRecordExternal);
+        p.cls = cls;
+        p.bytes = bytes;
+        p.flops = flops;
+        return;
+    }
     cudaEventRecord(c->ev_pool[i + 1], c->st);
     c->kpend.push_back({cls, c->ev_pool[i], c->ev_pool[i + 1], bytes, flops});
 }
 
-// After the stream is synchronised: fold the pending event pairs into the counters.
-void kt_collect(llm_ctx* c) {
-    for (const KPending& p : c->kpend) {
+void kt_fold(llm_ctx* c, const std::vector<KPending>& v) {
+    for (const KPending& p : v) {
         float ms = 0.f;
-        if (cudaEventElapsedTime(&ms, p.a, p.b) == cudaSuccess) {
-            KStat& s = c->kstat[p.cls];
-            s.launches += 1;
-            s.ms += ms;
-            s.bytes += p.bytes;
-            s.flops += p.flops;
-        }
+        if (p.cls < 0 || cudaEventElapsedTime(&ms, p.a, p.b) != cudaSuccess) continue;
+        KStat& s = c->kstat[p.cls];
+        s.launches += 1;
+        s.ms += ms;
+        s.bytes += p.bytes < 0 ? c->att_bytes_now : p.bytes;
+        s.flops += p.bytes < 0 ? c->att_flops_now : p.flops;
     }
+}
+
+// After the stream is synchronised: fold the pending event pairs into the counters.
+void kt_collect(llm_ctx* c, const StepGraph* g) {
+    if (g) kt_fold(c, g->timing);
+    kt_fold(c, c->kpend);
     c->kpend.clear();
     c->ev_used = 0;
 }
 
 double wbytes(const DevMat& W, int64_t rows) { return (double)rows * (double)row_bytes(W.type, W.cols); }
 
-struct InOffsets {
-    size_t tok, pos, slot, out_rows, list_off, list_cells, list_pos, perm, tile_list, tile_start,
-        tile_nq, tile_wi_off, wi_tile, wi_c0, wi_c1, wi_row_off, total;
-};
-
-InOffsets layout_inputs(int32_t T, int32_t O, const AttnPlan& p) {
-    InOffsets o{};
-    size_t at = 0;
-    auto take = [&](size_t n) { size_t r = at; at += (n + 3) / 4 * 4; return r; };
-    o.tok = take(T);
-    o.pos = take(T);
-    o.slot = take(T);
-    o.out_rows = take(std::max(O, 1));
-    o.list_off = take(p.list_off.size());
-    o.list_cells = take(p.list_cells.size());
-    o.list_pos = take(p.list_pos.size());
-    o.perm = take(p.perm.size());
-    o.tile_list = take(p.tile_list.size());
-    o.tile_start = take(p.tile_start.size());
-    o.tile_nq = take(p.tile_nq.size());
-    o.tile_wi_off = take(p.tile_wi_off.size());
-    o.wi_tile = take(p.wi_tile.size());
-    o.wi_c0 = take(p.wi_c0.size());
-    o.wi_c1 = take(p.wi_c1.size());
-    o.wi_row_off = take(p.wi_row_off.size());
-    o.total = at;
-    return o;
-}
-
 void put(int32_t* base, size_t off, const std::vector<int32_t>& v) {
     if (!v.empty()) std::memcpy(base + off, v.data(), v.size() * sizeof(int32_t));
 }
 
+// Algorithmic bytes / FLOPs of the attention of the current plan (for the kernel counters).
+void attention_work(llm_ctx* c, const int32_t* pos) {
+    const AttnPlan& p = c->plan;
+    const llm_hparams& hp = c->hp;
+    const double kv_es = (double)type_size(c->type_k);
+    double by = 0, fl = 0;
+    for (int32_t t = 0; t < p.n_tiles(); ++t) {
+        const int32_t l = p.tile_list[t];
+        by += (double)(p.list_off[l + 1] - p.list_off[l]) * 2.0 * hp.n_head_kv * hp.head_dim * kv_es;
+    }
+    const int32_t T = (int32_t)p.tok_list.size();
+    by += (double)T * hp.n_head * hp.head_dim * 8.0;
+    for (int32_t t = 0; t < T; ++t) {
+        const int32_t l = p.tok_list[t];
+        int64_t vis = 0;
+        for (int32_t k = p.list_off[l]; k < p.list_off[l + 1]; ++k) vis += p.list_pos[k] <= pos[t];
+        fl += 4.0 * (double)vis * hp.n_head * hp.head_dim;
+    }
+    c->att_bytes_now = by;
+    c->att_flops_now = fl;
+}
+
+// Attention work items a decode-shaped ubatch of T tokens may use (the captured grid size).
+int32_t attn_cap(llm_ctx* c, int32_t T) {
+    return std::min(c->max_work, std::max(T, 4 * c->n_sm / c->hp.n_head_kv));
+}
+
+// Which decode-GEMV variant serves each op of a T-token ubatch.
+struct OpPaths { bool qkv, wo, gu, down, lm; };
+
+OpPaths op_paths(llm_ctx* c, int32_t T, int32_t O) {
+    OpPaths o{false, false, false, false, false};
+    if (!c->use_bulk || T > gemv_max_tokens()) return o;
+    const llm_hparams& h = c->hp;
+    const Layer& L = c->layers[0];
+    GemvArgs a;
+    a.T = T;
+    a.K = h.n_embd; a.M = c->qkv_width(); o.qkv = gemv_bulk_ok(L.qkv.type, a, GEPI_QKV, c->n_sm);
+    a.K = c->q_width(); a.M = h.n_embd; o.wo = gemv_bulk_ok(L.wo.type, a, GEPI_ADD, c->n_sm);
+    a.K = h.n_embd; a.F = h.n_ff; o.gu = gemv_bulk_ok(L.gu.type, a, GEPI_SWIGLU, c->n_sm);
+    a.K = h.n_ff; a.M = h.n_embd; o.down = gemv_bulk_ok(L.down.type, a, GEPI_ADD, c->n_sm);
+    a.T = std::max(O, 1); a.K = h.n_embd; a.M = h.n_vocab;
+    o.lm = O > 0 && O <= gemv_max_tokens() && gemv_bulk_ok(c->out.type, a, GEPI_LOGITS, c->n_sm);
+    // every layer must share the types of layer 0 for the choice to hold
+    for (int32_t il = 1; il < h.n_layer; ++il) {
+        const Layer& M = c->layers[il];
+        if (M.qkv.type != L.qkv.type || M.wo.type != L.wo.type || M.gu.type != L.gu.type ||
+            M.down.type != L.down.type)
+            return OpPaths{false, false, false, false, false};
+    }
+    return o;
+}
+
 // Enqueue the forward pass of one ubatch ([P2] Example 4 op chain; [P1] Крок 13б layer scheme).
-bool forward_ubatch(llm_ctx* c, int32_t T, int32_t O, int32_t out_row0, const InOffsets& io) {
+// Everything that varies between ubatches of the same shape (tokens, positions, cells, lists,
+// the attention split) is read from the upload buffer, so the sequence can be captured once and
+// replayed.
+bool forward_ubatch(llm_ctx* c, int32_t T, int32_t O, int32_t out_row0, int32_t max_nq) {
     const llm_hparams& hp = c->hp;
     cudaStream_t st = c->st;
+    const InLayout& io = c->io;
     const int32_t d = hp.n_embd, H = hp.n_head, Hkv = hp.n_head_kv, hd = hp.head_dim, F = hp.n_ff;
     const int32_t* din = c->d_in;
     const int32_t *tok = din + io.tok, *pos = din + io.pos, *slot = din + io.slot;
     const size_t kv_es = type_size(c->type_k);
     const bool gemv = T <= gemv_max_tokens();
-    const int32_t lin_cls = gemv ? KC_LINEAR_GEMV : KC_LINEAR_GEMM;
+    const int32_t lin_cls = gemv ? KC_LINEAR_GEMV : (c->tc_ok ? KC_LINEAR_TC : KC_LINEAR_GEMM);
     const double Td = T, Od = O;
     const int qw = c->q_width(), qkvw = c->qkv_width();
-
-    // algorithmic bytes / FLOPs of the attention of this ubatch (only needed when timing)
-    double att_bytes = 0, att_flops = 0;
-    if (c->ktime) {
-        const AttnPlan& p = c->plan;
-        for (int32_t t = 0; t < p.n_tiles(); ++t) {
-            const int32_t l = p.tile_list[t];
-            att_bytes += (double)(p.list_off[l + 1] - p.list_off[l]) * 2.0 * Hkv * hd * kv_es;
-        }
-        att_bytes += Td * qw * 4.0 * 2.0;
-        const SanBatch& b = c->batch;
-        (void)b;
-        for (int32_t t = 0; t < T; ++t) {
-            const int32_t l = p.tok_list[t];
-            int64_t vis = 0;
-            for (int32_t k = p.list_off[l]; k < p.list_off[l + 1]; ++k)
-                vis += p.list_pos[k] <= c->h_in[io.pos + t];
-            att_flops += 4.0 * (double)vis * H * hd;
-        }
-    }
+    const OpPaths bulk = op_paths(c, T, O);
+    const bool pdl = c->use_pdl;
+    unsigned long long* amax = c->d_amax + out_row0;
 
     int k;
     k = kt_begin(c);
-    launch_embed(c->embd, tok, T, c->x, c->d_err, st);
-    kt_end(c, k, KC_EMBED, Td * d * (4.0 + type_size(c->embd.type == LLM_TYPE_Q8_0 ? 1 : c->embd.type)), 0);
-    k = kt_begin(c);
-    launch_rope_table(pos, T, hd, hp.rope_freq_base, c->rope_cs, st);
-    kt_end(c, k, KC_ROPE_TABLE, Td * hd * 4.0, 0);
+    launch_embed_rope(c->embd, tok, pos, T, hd, c->d_theta, c->x, c->rope_cs, amax, O, c->d_err, st);
+    kt_end(c, k, KC_EMBED, Td * d * 8.0 + Td * hd * 4.0, 0);
     if (c->debug) cudaMemcpyAsync(c->dbg_embd, c->x, sizeof(float) * T * d, cudaMemcpyDeviceToDevice, st);
 
     AttnArgs a{};
@@ -358,76 +456,166 @@ bool forward_ubatch(llm_ctx* c, int32_t T, int32_t O, int32_t out_row0, const In
     a.kv_type = c->type_k;
     a.H = H; a.Hkv = Hkv; a.hd = hd;
     a.tok_pos = pos;
-    a.list_off = din + io.list_off; a.list_cells = din + io.list_cells; a.list_pos = din + io.list_pos;
+    a.list_cells = din + io.list_cells; a.list_pos = din + io.list_pos;
     a.perm = din + io.perm;
-    a.tile_list = din + io.tile_list; a.tile_start = din + io.tile_start; a.tile_nq = din + io.tile_nq;
-    a.tile_wi_off = din + io.tile_wi_off;
-    a.wi_tile = din + io.wi_tile; a.wi_c0 = din + io.wi_c0; a.wi_c1 = din + io.wi_c1;
-    a.wi_row_off = din + io.wi_row_off;
+    a.tile_desc = reinterpret_cast<const int4*>(din + io.tile_desc);
+    a.wi_desc = reinterpret_cast<const int4*>(din + io.wi_desc);
+    a.tickets = c->tickets;
     a.part_o = c->part_o; a.part_m = c->part_m; a.part_l = c->part_l;
     a.out = c->attn;
     a.ldo = qw;
-    a.n_work = c->plan.n_work();
-    a.n_tiles = c->plan.n_tiles();
-    a.max_nq = c->plan.max_nq;
+    a.hdr = din + io.hdr;
+    a.n_work = gemv ? attn_cap(c, T) : c->plan.n_work();  // grid bound (the device count decides)
+    a.max_nq = max_nq;
+    a.pdl = c->use_pdl && gemv;
+    a.slot = gemv ? slot : nullptr;                  // decode steps use the staged-row kernel
+    a.n_tok = T;
+
+    GemvArgs g{};
+    g.T = T;
+    g.eps = hp.rms_eps;
+    g.err = c->d_err;
 
     const double norm_bytes = Td * d * 8.0 + d * 4.0;
+    // tensor-core prefill GEMMs; activations as split bf16 (hi + lo) operands, box 128 tokens
+    const bool tc = !gemv && c->tc_ok;
+    const int bi = 0;
+    if (tc) { a.out_b = c->attnb; a.out_b_lo = c->attnb_lo; }
+    auto tc_gemm = [&](const CUtensorMap& wm, const CUtensorMap& xm, int epi, int K, int M, void* Y,
+                       int ldy) {
+        const CUtensorMap* lo = &xm == &c->m_hb[bi] ? &c->m_hb_lo
+                              : &xm == &c->m_attnb[bi] ? &c->m_attnb_lo : &c->m_ub_lo;
+        void* y2 = epi == GEMM_EPI_SWIGLU ? c->ub_lo : nullptr;
+        if (!launch_gemm_tc(wm, xm, epi, K, M, T, F, Y, ldy, c->d_err, st, lo, y2)) {
+            c->err = "tensor-core GEMM launch failed";
+            return false;
+        }
+        return true;
+    };
+    auto bulk_fail = [&]() { c->err = "decode GEMV launch failed"; return false; };
     for (int32_t il = 0; il < hp.n_layer; ++il) {
         Layer& L = c->layers[il];
         void* kc = static_cast<uint8_t*>(c->kv_k) + (size_t)il * c->kv_layer_elems() * kv_es;
         void* vc = static_cast<uint8_t*>(c->kv_v) + (size_t)il * c->kv_layer_elems() * kv_es;
-        k = kt_begin(c);
-        launch_rmsnorm(c->x, nullptr, T, d, L.attn_norm, hp.rms_eps, c->h, st);
-        kt_end(c, k, KC_RMSNORM, norm_bytes, 0);
-        k = kt_begin(c);
-        launch_linear(L.qkv, 0, qkvw, c->h, d, T, c->qkv, qkvw, EPI_STORE, st);
-        kt_end(c, k, lin_cls, wbytes(L.qkv, qkvw) + Td * (d + qkvw) * 4.0, 2.0 * Td * qkvw * d);
-        k = kt_begin(c);
-        launch_rope_kv_append(c->qkv, T, H, Hkv, hd, c->rope_cs, slot, kc, vc, c->n_ctx,
-                              c->type_k, c->d_err, st);
-        kt_end(c, k, KC_ROPE_KV, Td * ((double)qkvw * 4.0 + qw * 4.0 + 2.0 * Hkv * hd * kv_es), 0);
+        // ---- attention norm, Q/K/V, RoPE, K/V append
+        if (bulk.qkv) {
+            k = kt_begin(c);
+            g.W = L.qkv.data; g.S = L.qkv.scales; g.row0 = 0; g.M = qkvw; g.K = d;
+            g.x = c->x; g.ldx = d; g.x_rows = nullptr; g.g = L.attn_norm;
+            g.y = c->qkv; g.ldy = qkvw;
+            g.H = H; g.Hkv = Hkv; g.hd = hd; g.n_ctx = c->n_ctx; g.kv_type = c->type_k;
+            g.cs = c->rope_cs; g.slot = slot; g.kc = kc; g.vc = vc;
+            if (!launch_gemv_bulk(L.qkv.type, g, GEPI_QKV, true, c->n_sm, st, pdl)) return bulk_fail();
+            kt_end(c, k, lin_cls, wbytes(L.qkv, qkvw) + Td * (d * 4.0 + qw * 4.0 + 2.0 * Hkv * hd * kv_es),
+                   2.0 * Td * qkvw * d);
+        } else {
+            k = kt_begin(c);
+            if (tc) launch_rmsnorm_bf16(c->x, nullptr, T, d, L.attn_norm, hp.rms_eps, c->hb, c->hb_lo, st);
+            else launch_rmsnorm(c->x, nullptr, T, d, L.attn_norm, hp.rms_eps, c->h, st);
+            kt_end(c, k, KC_RMSNORM, norm_bytes, 0);
+            k = kt_begin(c);
+            if (tc) { if (!tc_gemm(L.mq, c->m_hb[bi], GEMM_EPI_STORE, d, qkvw, c->qkv, qkvw)) return false; }
+            else launch_linear(L.qkv, 0, qkvw, c->h, d, T, c->qkv, qkvw, EPI_STORE, st);
+            kt_end(c, k, lin_cls, wbytes(L.qkv, qkvw) + Td * (d + qkvw) * 4.0, 2.0 * Td * qkvw * d);
+            k = kt_begin(c);
+            launch_rope_kv_append(c->qkv, T, H, Hkv, hd, c->rope_cs, slot, kc, vc, c->n_ctx,
+                                  c->type_k, c->d_err, st);
+            kt_end(c, k, KC_ROPE_KV, Td * ((double)qkvw * 4.0 + qw * 4.0 + 2.0 * Hkv * hd * kv_es), 0);
+        }
+        // ---- attention over the cache
         a.kc = kc;
         a.vc = vc;
         k = kt_begin(c);
         if (!launch_attention(a, st)) { c->err = "attention shape not supported"; return false; }
-        kt_end(c, k, KC_ATTENTION, att_bytes, att_flops);
+        kt_end(c, k, KC_ATTENTION, -1.0, 0);
         if (c->debug) {
             cudaMemcpy2DAsync(c->dbg_q + (size_t)il * T * qw, sizeof(float) * qw, c->qkv,
                               sizeof(float) * qkvw, sizeof(float) * qw, T, cudaMemcpyDeviceToDevice, st);
-            cudaMemcpyAsync(c->dbg_attn + (size_t)il * T * qw, c->attn, sizeof(float) * T * qw,
-                            cudaMemcpyDeviceToDevice, st);
+            if (!tc)
+                cudaMemcpyAsync(c->dbg_attn + (size_t)il * T * qw, c->attn, sizeof(float) * T * qw,
+                                cudaMemcpyDeviceToDevice, st);
         }
+        // ---- output projection + residual
         k = kt_begin(c);
-        launch_linear(L.wo, 0, d, c->attn, qw, T, c->x, d, EPI_ADD, st);
+        if (bulk.wo) {
+            g.W = L.wo.data; g.S = L.wo.scales; g.row0 = 0; g.M = d; g.K = qw;
+            g.x = c->attn; g.ldx = qw; g.x_rows = nullptr; g.g = nullptr; g.y = c->x; g.ldy = d;
+            if (!launch_gemv_bulk(L.wo.type, g, GEPI_ADD, false, c->n_sm, st, pdl)) return bulk_fail();
+        } else if (tc) {
+            if (!tc_gemm(L.mo, c->m_attnb[bi], GEMM_EPI_ADD, qw, d, c->x, d)) return false;
+        } else {
+            launch_linear(L.wo, 0, d, c->attn, qw, T, c->x, d, EPI_ADD, st);
+        }
         kt_end(c, k, lin_cls, wbytes(L.wo, d) + Td * (qw + 2.0 * d) * 4.0, 2.0 * Td * d * qw);
+        // ---- FFN norm, gate/up, SwiGLU
+        if (bulk.gu) {
+            k = kt_begin(c);
+            g.W = L.gu.data; g.S = L.gu.scales; g.row0 = 0; g.F = F; g.K = d;
+            g.x = c->x; g.ldx = d; g.x_rows = nullptr; g.g = L.ffn_norm; g.y = c->u; g.ldy = F;
+            if (!launch_gemv_bulk(L.gu.type, g, GEPI_SWIGLU, true, c->n_sm, st, pdl)) return bulk_fail();
+            kt_end(c, k, lin_cls, wbytes(L.gu, 2 * (int64_t)F) + Td * (d + F) * 4.0, 4.0 * Td * F * d);
+        } else {
+            k = kt_begin(c);
+            if (tc) launch_rmsnorm_bf16(c->x, nullptr, T, d, L.ffn_norm, hp.rms_eps, c->hb, c->hb_lo, st);
+            else launch_rmsnorm(c->x, nullptr, T, d, L.ffn_norm, hp.rms_eps, c->h, st);
+            kt_end(c, k, KC_RMSNORM, norm_bytes, 0);
+            k = kt_begin(c);
+            if (tc) { if (!tc_gemm(L.mgu, c->m_hb[bi], GEMM_EPI_SWIGLU, d, 0, c->ub, F)) return false; }
+            else launch_linear_swiglu(L.gu, F, c->h, d, T, c->u, F, c->tmp, st);
+            kt_end(c, k, lin_cls, wbytes(L.gu, 2 * (int64_t)F) + Td * (d + F) * 4.0, 4.0 * Td * F * d);
+        }
+        // ---- down projection + residual
         k = kt_begin(c);
-        launch_rmsnorm(c->x, nullptr, T, d, L.ffn_norm, hp.rms_eps, c->h, st);
-        kt_end(c, k, KC_RMSNORM, norm_bytes, 0);
-        k = kt_begin(c);
-        launch_linear_swiglu(L.gu, F, c->h, d, T, c->u, F, c->tmp, st);
-        kt_end(c, k, lin_cls, wbytes(L.gu, 2 * (int64_t)F) + Td * (d + F) * 4.0, 4.0 * Td * F * d);
-        k = kt_begin(c);
-        launch_linear(L.down, 0, d, c->u, F, T, c->x, d, EPI_ADD, st);
+        if (bulk.down) {
+            g.W = L.down.data; g.S = L.down.scales; g.row0 = 0; g.M = d; g.K = F;
+            g.x = c->u; g.ldx = F; g.x_rows = nullptr; g.g = nullptr; g.y = c->x; g.ldy = d;
+            if (!launch_gemv_bulk(L.down.type, g, GEPI_ADD, false, c->n_sm, st, pdl)) return bulk_fail();
+        } else if (tc) {
+            if (!tc_gemm(L.md, c->m_ub[bi], GEMM_EPI_ADD, F, d, c->x, d)) return false;
+        } else {
+            launch_linear(L.down, 0, d, c->u, F, T, c->x, d, EPI_ADD, st);
+        }
         kt_end(c, k, lin_cls, wbytes(L.down, d) + Td * (F + 2.0 * d) * 4.0, 2.0 * Td * d * F);
         if (c->debug)
             cudaMemcpyAsync(c->dbg_lout + (size_t)il * T * d, c->x, sizeof(float) * T * d,
                             cudaMemcpyDeviceToDevice, st);
     }
     if (O > 0) {
-        // keep only the requested rows, final norm, output matrix, greedy pick
-        k = kt_begin(c);
-        launch_rmsnorm(c->x, din + io.out_rows, O, d, c->out_norm, hp.rms_eps, c->hout, st);
-        kt_end(c, k, KC_RMSNORM, Od * d * 8.0 + d * 4.0, 0);
-        if (c->debug)
-            cudaMemcpyAsync(c->dbg_rnorm, c->hout, sizeof(float) * O * d, cudaMemcpyDeviceToDevice, st);
+        // keep only the requested rows, final norm, output matrix, greedy pick ([P1] Крок 13б)
         float* lg = c->d_logits + (size_t)out_row0 * hp.n_vocab;
-        k = kt_begin(c);
-        launch_linear(c->out, 0, hp.n_vocab, c->hout, d, O, lg, hp.n_vocab, EPI_STORE, st);
-        kt_end(c, k, KC_LM_HEAD, wbytes(c->out, hp.n_vocab) + Od * (d + (double)hp.n_vocab) * 4.0,
-               2.0 * Od * hp.n_vocab * d);
-        k = kt_begin(c);
-        launch_argmax(lg, O, hp.n_vocab, c->d_argmax + out_row0, st);
-        kt_end(c, k, KC_ARGMAX, Od * hp.n_vocab * 4.0, 0);
+        const int32_t* orows = din + io.out_rows;
+        const double lm_bytes = wbytes(c->out, hp.n_vocab) + Od * (d + (double)hp.n_vocab) * 4.0;
+        if (bulk.lm && !c->debug) {
+            k = kt_begin(c);
+            g.T = O;
+            g.W = c->out.data; g.S = c->out.scales; g.row0 = 0; g.M = hp.n_vocab; g.K = d;
+            g.x = c->x; g.ldx = d; g.x_rows = orows; g.g = c->out_norm; g.y = lg; g.ldy = hp.n_vocab;
+            g.amax = amax;
+            if (!launch_gemv_bulk(c->out.type, g, GEPI_LOGITS, true, c->n_sm, st, pdl)) return bulk_fail();
+            kt_end(c, k, KC_LM_HEAD, lm_bytes, 2.0 * Od * hp.n_vocab * d);
+        } else {
+            const bool tc_out = tc && O > gemv_max_tokens();
+            k = kt_begin(c);
+            if (tc_out) launch_rmsnorm_bf16(c->x, orows, O, d, c->out_norm, hp.rms_eps, c->hob, c->hob_lo, st);
+            launch_rmsnorm(c->x, orows, O, d, c->out_norm, hp.rms_eps, c->hout, st);
+            kt_end(c, k, KC_RMSNORM, Od * d * 8.0 + d * 4.0, 0);
+            if (c->debug)
+                cudaMemcpyAsync(c->dbg_rnorm, c->hout, sizeof(float) * O * d, cudaMemcpyDeviceToDevice, st);
+            k = kt_begin(c);
+            if (tc_out) {
+                if (!launch_gemm_tc(c->m_lm, c->m_hob[0], GEMM_EPI_STORE, d, hp.n_vocab, O, F, lg,
+                                    hp.n_vocab, c->d_err, st, &c->m_hob_lo)) {
+                    c->err = "tensor-core GEMM launch failed";
+                    return false;
+                }
+            } else {
+                launch_linear(c->out, 0, hp.n_vocab, c->hout, d, O, lg, hp.n_vocab, EPI_STORE, st);
+            }
+            kt_end(c, k, KC_LM_HEAD, lm_bytes, 2.0 * Od * hp.n_vocab * d);
+            k = kt_begin(c);
+            launch_argmax(lg, O, hp.n_vocab, amax, st);
+            kt_end(c, k, KC_ARGMAX, Od * hp.n_vocab * 4.0, 0);
+        }
     }
     c->dbg_T = T;
     c->dbg_O = O;
@@ -522,15 +710,35 @@ llm_ctx* llm_ctx_init(const llm_hparams* hp, const llm_cparams* cp) {
               dalloc(c, &c->qkv, U * c->qkv_width()) && dalloc(c, &c->attn, U * c->q_width()) &&
               dalloc(c, &c->u, U * h.n_ff) && dalloc(c, &c->tmp, U * 2 * (int64_t)h.n_ff) &&
               dalloc(c, &c->hout, U * d) && dalloc(c, &c->rope_cs, U * (h.head_dim / 2)) &&
+              dalloc(c, reinterpret_cast<uint16_t**>(&c->hb), U * d) &&
+              dalloc(c, reinterpret_cast<uint16_t**>(&c->attnb), U * c->q_width()) &&
+              dalloc(c, reinterpret_cast<uint16_t**>(&c->ub), U * (int64_t)h.n_ff) &&
+              dalloc(c, reinterpret_cast<uint16_t**>(&c->hob), U * d) &&
+              dalloc(c, reinterpret_cast<uint16_t**>(&c->hb_lo), U * d) &&
+              dalloc(c, reinterpret_cast<uint16_t**>(&c->attnb_lo), U * c->q_width()) &&
+              dalloc(c, reinterpret_cast<uint16_t**>(&c->ub_lo), U * (int64_t)h.n_ff) &&
+              dalloc(c, reinterpret_cast<uint16_t**>(&c->hob_lo), U * d) &&
               dalloc(c, &c->d_err, 1) &&
               cuda_ok(c, cudaMallocHost(&c->h_err, sizeof(uint32_t)), "cudaMallocHost");
     if (!ok) return die("");
+    {
+        std::vector<double> th(h.head_dim / 2);
+        for (int i = 0; i < h.head_dim / 2; ++i)
+            th[i] = std::pow((double)h.rope_freq_base, -2.0 * i / (double)h.head_dim);
+        ok = dalloc(c, &c->d_theta, th.size()) &&
+             cuda_ok(c, cudaMemcpy(c->d_theta, th.data(), th.size() * sizeof(double),
+                                   cudaMemcpyHostToDevice), "copy");
+        if (!ok) return die("");
+    }
     c->max_rows = (int32_t)std::max<int64_t>(2 * U * G, 8192);
-    ok = dalloc(c, &c->part_o, (size_t)c->max_rows * h.n_head_kv * h.head_dim) &&
+    ok = dalloc(c, &c->tickets, (size_t)U * h.n_head_kv) &&
+         cuda_ok(c, cudaMemset(c->tickets, 0, sizeof(int32_t) * U * h.n_head_kv), "memset") &&
+         dalloc(c, &c->part_o, (size_t)c->max_rows * h.n_head_kv * h.head_dim) &&
          dalloc(c, &c->part_m, (size_t)c->max_rows * h.n_head_kv) &&
          dalloc(c, &c->part_l, (size_t)c->max_rows * h.n_head_kv) &&
          ensure_outputs(c, std::max<int32_t>(c->n_seq_max, (int32_t)std::min<int64_t>(U, 64))) &&
-         ensure_inputs(c, (size_t)8 * U + 2 * (size_t)c->n_ctx + 65536);
+         (c->max_work = std::max<int32_t>((int32_t)U, c->max_rows / G), true) &&
+         ensure_inputs(c, 2 * (size_t)c->n_ctx);
     if (!ok) return die("");
     // KV cells start zeroed so an unwritten cell never holds NaN bit patterns
     ok = cuda_ok(c, cudaMemsetAsync(c->kv_k, 0, kv_elems * type_size(c->type_k), c->st), "memset") &&
@@ -543,6 +751,7 @@ llm_ctx* llm_ctx_init(const llm_hparams* hp, const llm_cparams* cp) {
 void llm_ctx_free(llm_ctx* c) {
     if (!c) return;
     if (c->st) cudaStreamSynchronize(c->st);
+    drop_graphs(c);
     for (void* p : c->allocs) cudaFree(p);
     c->allocs.clear();
     if (c->h_in) cudaFreeHost(c->h_in);
@@ -651,6 +860,37 @@ int llm_weights_ready(llm_ctx* c) {
     }
     if (!c->out_loaded) c->out = c->embd;   // tied output
     c->ready = true;
+    drop_graphs(c);
+    c->tc_ok = false;
+    if (c->host_only) return 0;
+    // tensor-core prefill: every linear weight BF16 with supported shapes
+    const llm_hparams& h = c->hp;
+    const int64_t d = h.n_embd, qw = c->q_width(), qkvw = c->qkv_width(), F = h.n_ff;
+    const int64_t U = c->n_ubatch;
+    bool ok = tc_shape_ok(qkvw, d, GEMM_EPI_STORE, 0) && tc_shape_ok(d, qw, GEMM_EPI_ADD, 0) &&
+              tc_shape_ok(0, d, GEMM_EPI_SWIGLU, F) && tc_shape_ok(d, F, GEMM_EPI_ADD, 0);
+    for (int32_t il = 0; ok && il < h.n_layer; ++il) {
+        Layer& L = c->layers[il];
+        ok = L.qkv.type == LLM_TYPE_BF16 && L.wo.type == LLM_TYPE_BF16 &&
+             L.gu.type == LLM_TYPE_BF16 && L.down.type == LLM_TYPE_BF16 &&
+             tc_make_map(&L.mq, L.qkv.data, qkvw, d, 128) &&
+             tc_make_map(&L.mo, L.wo.data, d, qw, 128) &&
+             tc_make_map(&L.mgu, L.gu.data, 2 * F, d, 64) &&
+             tc_make_map(&L.md, L.down.data, d, F, 128);
+    }
+    const int boxes[2] = {128, 256};
+    for (int i = 0; ok && i < 2; ++i)
+        ok = tc_make_map(&c->m_hb[i], c->hb, U, d, boxes[i]) &&
+             tc_make_map(&c->m_attnb[i], c->attnb, U, qw, boxes[i]) &&
+             tc_make_map(&c->m_ub[i], c->ub, U, F, boxes[i]) &&
+             tc_make_map(&c->m_hob[i], c->hob, U, d, boxes[i]);
+    ok = ok && tc_make_map(&c->m_hb_lo, c->hb_lo, U, d, 128) &&
+         tc_make_map(&c->m_attnb_lo, c->attnb_lo, U, qw, 128) &&
+         tc_make_map(&c->m_ub_lo, c->ub_lo, U, F, 128) &&
+         tc_make_map(&c->m_hob_lo, c->hob_lo, U, d, 128);
+    const bool lm_ok = c->out.type == LLM_TYPE_BF16 && tc_shape_ok(h.n_vocab, d, GEMM_EPI_STORE, 0) &&
+                       tc_make_map(&c->m_lm, c->out.data, h.n_vocab, d, 128);
+    c->tc_ok = ok && lm_ok;
     return 0;
 }
 
@@ -699,8 +939,10 @@ int32_t llm_decode(llm_ctx* c, llm_batch bt) {
             c->err = "aborted";
             return 2;
         }
+        const bool small = T <= gemv_max_tokens();
+        const int32_t cap = small ? attn_cap(c, T) : c->max_work;
         build_attn_plan(c->cells, b, i0, T, kAttnTileQ, c->hp.n_head_kv, G, 4 * c->n_sm,
-                        c->max_rows, c->plan);
+                        c->max_rows, cap, c->plan, small ? 64 : 32);
         if (c->debug) {
             UbDebug u;
             u.n_kv = c->cells.n_kv();
@@ -719,31 +961,80 @@ int32_t llm_decode(llm_ctx* c, llm_batch bt) {
         c->perf.n_tokens += T;
         if (c->host_only) { n_out += O; continue; }
 
-        const InOffsets io = layout_inputs(T, O, c->plan);
-        if (!ensure_inputs(c, io.total)) { rollback(c, i0, T); return -2; }
+        const AttnPlan& p = c->plan;
+        if (!ensure_inputs(c, p.list_cells.size())) { rollback(c, i0, T); return -2; }
+        const InLayout& io = c->io;
         int32_t* hi = c->h_in;
+        hi[io.hdr + 0] = p.n_work();
+        hi[io.hdr + 1] = p.n_tiles();
         std::memcpy(hi + io.tok, b.token.data() + i0, T * sizeof(int32_t));
         std::memcpy(hi + io.pos, b.pos.data() + i0, T * sizeof(int32_t));
         std::memcpy(hi + io.slot, us.data(), T * sizeof(int32_t));
         if (c->fault_kind == 1 && c->fault_ub == ub) hi[io.slot] = c->n_ctx + 7;
         put(hi, io.out_rows, out_rows);
-        const AttnPlan& p = c->plan;
-        put(hi, io.list_off, p.list_off); put(hi, io.list_cells, p.list_cells);
-        put(hi, io.list_pos, p.list_pos); put(hi, io.perm, p.perm);
-        put(hi, io.tile_list, p.tile_list); put(hi, io.tile_start, p.tile_start);
-        put(hi, io.tile_nq, p.tile_nq); put(hi, io.tile_wi_off, p.tile_wi_off);
-        put(hi, io.wi_tile, p.wi_tile); put(hi, io.wi_c0, p.wi_c0); put(hi, io.wi_c1, p.wi_c1);
-        put(hi, io.wi_row_off, p.wi_row_off);
-        bool ok = cuda_ok(c, cudaMemcpyAsync(c->d_in, hi, io.total * sizeof(int32_t),
+        put(hi, io.perm, p.perm);
+        for (int32_t t = 0; t < p.n_tiles(); ++t) {
+            int32_t* d8 = hi + io.tile_desc + 8 * t;
+            const int32_t l = p.tile_list[t];
+            d8[0] = l; d8[1] = p.tile_start[t]; d8[2] = p.tile_nq[t]; d8[3] = p.tile_wi_off[t];
+            d8[4] = p.tile_wi_off[t + 1]; d8[5] = p.list_off[l];
+            d8[6] = p.list_off[l + 1] - p.list_off[l]; d8[7] = 0;
+        }
+        for (int32_t w = 0; w < p.n_work(); ++w) {
+            int32_t* d4 = hi + io.wi_desc + 4 * w;
+            d4[0] = p.wi_tile[w]; d4[1] = p.wi_c0[w]; d4[2] = p.wi_c1[w]; d4[3] = p.wi_row_off[w];
+        }
+        put(hi, io.list_cells, p.list_cells); put(hi, io.list_pos, p.list_pos);
+        const size_t nl = p.list_cells.size();
+        bool ok = cuda_ok(c, cudaMemcpyAsync(c->d_in, hi, io.fixed_end * sizeof(int32_t),
                                              cudaMemcpyHostToDevice, c->st), "inputs upload") &&
+                  (nl == 0 || (cuda_ok(c, cudaMemcpyAsync(c->d_in + io.list_cells, hi + io.list_cells,
+                                                          nl * sizeof(int32_t), cudaMemcpyHostToDevice,
+                                                          c->st), "inputs upload") &&
+                               cuda_ok(c, cudaMemcpyAsync(c->d_in + io.list_pos, hi + io.list_pos,
+                                                          nl * sizeof(int32_t), cudaMemcpyHostToDevice,
+                                                          c->st), "inputs upload"))) &&
                   cuda_ok(c, cudaMemsetAsync(c->d_err, 0, sizeof(uint32_t), c->st), "memset");
-        ok = ok && forward_ubatch(c, T, O, n_out, io);
+        if (c->ktime) attention_work(c, b.pos.data() + i0);
+        const int32_t max_nq = p.max_nq <= 1 ? 1 : kAttnTileQ;
+        const StepGraph* sg = nullptr;
+        if (ok && small && c->use_graphs && !c->debug) {
+            const uint64_t key = (uint64_t)T | ((uint64_t)O << 10) | ((uint64_t)n_out << 20) |
+                                 ((uint64_t)(max_nq > 1) << 52) | ((uint64_t)c->ktime << 53);
+            auto it = c->graphs.find(key);
+            if (it == c->graphs.end()) {
+                StepGraph ng;
+                if (c->ktime) { c->kcap = &ng.timing; c->kcap_events = &ng.events; }
+                cudaGraph_t graph = nullptr;
+                bool cap_ok = cudaStreamBeginCapture(c->st, cudaStreamCaptureModeThreadLocal) == cudaSuccess;
+                const bool fwd_ok = cap_ok && forward_ubatch(c, T, O, n_out, max_nq);
+                if (cap_ok) cap_ok = cudaStreamEndCapture(c->st, &graph) == cudaSuccess && fwd_ok;
+                c->kcap = nullptr;
+                c->kcap_events = nullptr;
+                if (cap_ok) cap_ok = cudaGraphInstantiate(&ng.exec, graph, 0) == cudaSuccess;
+                if (graph) cudaGraphDestroy(graph);
+                cudaGetLastError();
+                if (cap_ok) {
+                    it = c->graphs.emplace(key, std::move(ng)).first;
+                } else {
+                    // capture is an optimisation: fall back to direct launches from now on
+                    for (cudaEvent_t e : ng.events) cudaEventDestroy(e);
+                    c->use_graphs = false;
+                }
+            }
+            if (it != c->graphs.end()) {
+                sg = &it->second;
+                ok = cuda_ok(c, cudaGraphLaunch(sg->exec, c->st), "graph launch");
+                c->perf.n_graph_replays += 1;
+            }
+        }
+        if (ok && !sg) ok = forward_ubatch(c, T, O, n_out, max_nq);
         ok = ok && cuda_ok(c, cudaMemcpyAsync(c->h_err, c->d_err, sizeof(uint32_t),
                                               cudaMemcpyDeviceToHost, c->st), "error word") &&
              cuda_ok(c, cudaStreamSynchronize(c->st), "device computation");
-        kt_collect(c);
+        kt_collect(c, sg);
         if (ok && *c->h_err != 0) {
-            c->err = "device bounds check failed (error word " + std::to_string(*c->h_err) + ")";
+            c->err = "device check failed (error word " + std::to_string(*c->h_err) + ")";
             ok = false;
         }
         if (!ok) {
@@ -792,14 +1083,15 @@ int32_t llm_get_argmax_ith(llm_ctx* c, int32_t i) {
     const int32_t j = resolve_row(c, i);
     if (j < 0) return -1;
     if (!c->h_argmax_valid) {
-        c->h_argmax.resize(c->n_outputs);
-        if (!cuda_ok(c, cudaMemcpyAsync(c->h_argmax.data(), c->d_argmax, c->n_outputs * sizeof(int32_t),
+        c->h_amax.resize(c->n_outputs);
+        if (!cuda_ok(c, cudaMemcpyAsync(c->h_amax.data(), c->d_amax,
+                                        c->n_outputs * sizeof(unsigned long long),
                                         cudaMemcpyDeviceToHost, c->st), "argmax copy") ||
             !cuda_ok(c, cudaStreamSynchronize(c->st), "sync"))
             return -1;
         c->h_argmax_valid = true;
     }
-    return c->h_argmax[j];
+    return unpack_argmax(c->h_amax[j]);
 }
 
 int32_t llm_n_outputs(llm_ctx* c) { return c ? c->n_outputs : 0; }
