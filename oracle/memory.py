@@ -53,33 +53,37 @@ class Batch:
 
 class Cells:
     """KV cells ([P4] KVキャッシュの詳細, llama_kv_cells): per cell a position (-1 = empty) and the
-    set of sequences using it (a cell can be shared)."""
+    set of sequences using it (a cell can be shared), held as a bool row seq[c, s]."""
 
     def __init__(self, n_ctx: int):
         self.pos = np.full(n_ctx, -1, dtype=np.int64)
-        self.seq: List[set] = [set() for _ in range(n_ctx)]
+        self.seq = np.zeros((n_ctx, LLAMA_MAX_SEQ), dtype=bool)
 
     @property
     def size(self) -> int:
         return len(self.pos)
 
     def copy(self) -> "Cells":
-        c = Cells(self.size)
+        c = Cells.__new__(Cells)
         c.pos = self.pos.copy()
-        c.seq = [set(s) for s in self.seq]
+        c.seq = self.seq.copy()
         return c
+
+    def seqs_of(self, c: int) -> set:
+        """The sequence ids cell c holds."""
+        return set(np.nonzero(self.seq[c])[0].tolist())
 
     def is_empty(self, c: int) -> bool:
         return self.pos[c] < 0
 
     def seq_pos_max(self, s: int) -> int:
         """Largest position held for sequence s, -1 if none ([P1] KV-cache section)."""
-        ps = [int(self.pos[c]) for c in range(self.size) if s in self.seq[c]]
-        return max(ps) if ps else -1
+        ps = self.pos[self.seq[:, s]]
+        return int(ps.max()) if len(ps) else -1
 
     def seq_pos_min(self, s: int) -> int:
-        ps = [int(self.pos[c]) for c in range(self.size) if s in self.seq[c]]
-        return min(ps) if ps else -1
+        ps = self.pos[self.seq[:, s]]
+        return int(ps.min()) if len(ps) else -1
 
     def seq_rm(self, s: int, p0: int, p1: int) -> bool:
         """Remove sequence s from the cells with p0 <= pos < p1 ([P4] エラーリカバリ, seq_rm).
@@ -91,22 +95,19 @@ class Cells:
             p0 = 0
         if p1 < 0:
             p1 = np.iinfo(np.int64).max
-        for c in range(self.size):
-            if self.pos[c] < 0 or not (p0 <= self.pos[c] < p1):
-                continue
-            if s < 0:
-                self.seq[c].clear()
-            else:
-                self.seq[c].discard(s)
-            if not self.seq[c]:
-                self.pos[c] = -1
+        sel = (self.pos >= 0) & (self.pos >= p0) & (self.pos < p1)
+        if s < 0:
+            self.seq[sel, :] = False
+        else:
+            self.seq[sel, s] = False
+        self.pos[sel & ~self.seq.any(axis=1)] = -1
         return True
 
     def find_slots(self, n: int) -> Optional[List[int]]:
         """reading ("contiguous, or at least available" cells, [P4] KVキャッシュの詳細): the n
         lowest-index empty cells, in ascending order; None if fewer than n are empty."""
-        free = [c for c in range(self.size) if self.pos[c] < 0]
-        return free[:n] if len(free) >= n else None
+        free = np.nonzero(self.pos < 0)[0]
+        return free[:n].tolist() if len(free) >= n else None
 
     def apply(self, slots: Sequence[int], pos: Sequence[int], seq_ids: Sequence[Sequence[int]]):
         """mctx->apply(): write each token's position and sequence ids into its cell
@@ -114,7 +115,8 @@ class Cells:
         for c, p, ss in zip(slots, pos, seq_ids):
             assert self.pos[c] < 0, "slot must be empty"
             self.pos[c] = int(p)
-            self.seq[c] = set(int(s) for s in ss)
+            self.seq[c, :] = False
+            self.seq[c, [int(s) for s in ss]] = True
 
     def n_kv(self) -> int:
         """Cells the attention reads: highest used cell + 1 (reading of the 'recount' in apply)."""
@@ -133,9 +135,9 @@ class Cells:
         cpos = self.pos[:n_kv]
         shares = {}                      # sequence set -> cells sharing one of its sequences
         for t in range(T):
-            key = frozenset(int(s) for s in seq_ids[t])
+            key = tuple(sorted(int(s) for s in seq_ids[t]))
             if key not in shares:
-                shares[key] = np.array([bool(self.seq[c] & key) for c in range(n_kv)], dtype=bool)
+                shares[key] = self.seq[:n_kv][:, list(key)].any(axis=1)
             m[t] = shares[key] & (cpos >= 0) & (cpos <= pos[t])
         return m
 

@@ -64,7 +64,7 @@ def test_seq_rm_ranges_and_shared_cells():
     c = Cells(6)
     c.apply([0, 1, 2], [0, 1, 2], [[0, 1], [0, 1], [0]])
     c.seq_rm(1, 0, -1)                                           # shared cells keep seq 0
-    assert c.pos.tolist()[:3] == [0, 1, 2] and c.seq[0] == {0}
+    assert c.pos.tolist()[:3] == [0, 1, 2] and c.seqs_of(0) == {0}
     c.seq_rm(0, 1, 2)                                            # [1, 2): only position 1
     assert c.pos.tolist()[:3] == [0, -1, 2]
     c.seq_rm(0, -5, -1)                                          # p0 < 0 -> 0
@@ -88,13 +88,13 @@ def test_mask_brute_force_small_case():
     c = Cells(40)
     for cell in rng.permutation(40)[:30]:
         c.pos[cell] = rng.integers(0, 20)
-        c.seq[cell] = set(rng.choice(NSEQ, size=rng.integers(1, 3), replace=False).tolist())
+        c.seq[cell, rng.choice(NSEQ, size=rng.integers(1, 3), replace=False)] = True
     pos = rng.integers(0, 20, size=7)
     seqs = [[int(rng.integers(0, NSEQ))] for _ in range(7)]
     m = c.mask(pos, seqs, 40)
     for t in range(7):
         for cell in range(40):
-            want = c.pos[cell] >= 0 and seqs[t][0] in c.seq[cell] and c.pos[cell] <= pos[t]
+            want = c.pos[cell] >= 0 and seqs[t][0] in c.seqs_of(cell) and c.pos[cell] <= pos[t]
             assert m[t, cell] == want
 
 
@@ -111,9 +111,9 @@ def test_full_cache_returns_1_and_leaves_state_unchanged():
     assert ctx.decode(list(range(60)), logits=None) == 0
     assert ctx.decode(list(range(60)), logits=None) == 0
     assert ctx.decode(list(range(60)), logits=None) == 0
-    before = (ctx.cells.pos.copy(), [set(s) for s in ctx.cells.seq], [k.copy() for k in ctx.K])
+    before = (ctx.cells.pos.copy(), ctx.cells.seq.copy(), [k.copy() for k in ctx.K])
     assert ctx.decode(list(range(17))) == 1                         # 240 used, 16 free
-    assert np.array_equal(ctx.cells.pos, before[0]) and ctx.cells.seq == before[1]
+    assert np.array_equal(ctx.cells.pos, before[0]) and np.array_equal(ctx.cells.seq, before[1])
     assert all(np.array_equal(a, b) for a, b in zip(ctx.K, before[2]))
     assert ctx.decode(list(range(16))) == 0
 
