@@ -229,10 +229,18 @@ int llm_debug_capture(llm_ctx *ctx, int enable);
 /* Copy a captured intermediate of the last ubatch to host memory as float32, row-major
  * [n_tokens][width]. name: "embd" (layer ignored), "l_out" (residual stream after layer `layer`),
  * "attn_out" (attention output of layer `layer`, before the output projection), "kq_in" (the Q
- * rows after RoPE of layer `layer`), "result_norm" (final-normed output rows). Returns the number
+ * rows after RoPE of layer `layer`), "result_norm" (final-normed output rows; present only when the
+ * output matrix ran unfused, not in the one-token GEMV that normalises in its prologue). Returns the number
  * of floats available (0 if none), writes at most cap. */
 int64_t llm_debug_get_tensor(llm_ctx *ctx, const char *name, int32_t layer, float *out,
                              int64_t cap);
+
+/* Copy layer `layer`'s K cache (which = 0) or V cache (which = 1) to host memory as stored: type_k
+ * / type_v elements laid out [n_head_kv][n_ctx][head_dim] (cell c of KV head g at (g * n_ctx + c)
+ * * head_dim). out may be NULL to query the size. Returns the slab's size in bytes (copies at most
+ * cap_bytes, after the context's stream has finished), 0 for a bad layer/which or a host-only
+ * context. */
+int64_t llm_debug_kv_raw(llm_ctx *ctx, int32_t layer, int32_t which, void *out, int64_t cap_bytes);
 
 /* Per-kernel-class device timing. enable != 0 resets the counters and brackets every later launch
  * with CUDA events on the context's stream (small overhead); 0 stops. */

@@ -100,3 +100,78 @@ def greedy_compare(ctx, ora, n_seq: int, first_rows, n_steps: int, tol: float, r
         assert ora.decode(nxt, seq_id=seqs, n_seq_id=[1] * n_seq, logits=[1] * n_seq) == 0
         rows = list(range(n_seq))
     return report
+
+
+# ---- full-size checks: one layer of the oracle on the library's own inputs ----
+
+def layer_check(ow, hp, il: int, x_in: np.ndarray, x_out: np.ndarray, pos, slots, visible,
+                kc: np.ndarray, vc: np.ndarray, type_kv: int) -> dict:
+    """Layer il of the oracle for a few tokens, fed the library's residual stream before the layer
+    (x_in [n, d]) and the library's layer-il K/V cache (kc, vc [n_head_kv][n_ctx][head_dim], float).
+
+    Checks the K/V rows the library appended for these tokens (at cells `slots`) and the layer's
+    update x_out - x_in, with attention over the cells `visible[t]` (a bool row over the first
+    n_kv cells). At full size this is what the oracle can afford: every layer's input comes from
+    the library, so each layer is checked on its own. Returns the largest relative errors
+    (max |library - oracle| / max |oracle| per token row)."""
+    H, Hkv, hd = hp.n_head, hp.n_head_kv, hp.head_dim
+    n = x_in.shape[0]
+    p = f"blk.{il}."
+    x_in = x_in.astype(np.float64)
+    h = oracle.rms_norm(x_in, ow.vector(p + "attn_norm.weight"), hp.rms_eps)
+    q = oracle.rope(ow.matmul(h, p + "attn_q.weight").reshape(n, H, hd), np.asarray(pos),
+                    hp.rope_freq_base)
+    k = oracle.rope(ow.matmul(h, p + "attn_k.weight").reshape(n, Hkv, hd), np.asarray(pos),
+                    hp.rope_freq_base)
+    v = ow.matmul(h, p + "attn_v.weight").reshape(n, Hkv, hd)
+    k = oracle.round_to_type(k, type_kv)
+    v = oracle.round_to_type(v, type_kv)
+    kc = kc.astype(np.float64)
+    vc = vc.astype(np.float64)
+    err = {"k": 0.0, "v": 0.0, "delta": 0.0}
+    o = np.zeros((n, H * hd))
+    for t in range(n):
+        gk = kc[:, slots[t], :]
+        gv = vc[:, slots[t], :]
+        err["k"] = max(err["k"], rel_err(gk.reshape(-1), k[t].reshape(-1)))
+        err["v"] = max(err["v"], rel_err(gv.reshape(-1), v[t].reshape(-1)))
+        cells = np.nonzero(visible[t])[0]
+        kt = kc[:, cells, :].transpose(1, 0, 2)
+        vt = vc[:, cells, :].transpose(1, 0, 2)
+        o[t] = oracle.attention(q[t:t + 1], kt, vt, np.ones((1, len(cells)), dtype=bool), Hkv)[0]
+    x = x_in + ow.matmul(o, p + "attn_output.weight")
+    h = oracle.rms_norm(x, ow.vector(p + "ffn_norm.weight"), hp.rms_eps)
+    u = oracle.swiglu(ow.matmul(h, p + "ffn_gate.weight"), ow.matmul(h, p + "ffn_up.weight"))
+    x = x + ow.matmul(u, p + "ffn_down.weight")
+    for t in range(n):
+        err["delta"] = max(err["delta"], rel_err(x_out[t] - x_in[t], x[t] - x_in[t]))
+    return err
+
+
+def logits_check(ow, hp, x_last: np.ndarray, g_logits, g_argmax) -> dict:
+    """The oracle's final norm and output matrix on the library's last residual rows [n, d]
+    against the library's logits rows and device argmax picks. Tokens must agree where the
+    oracle's top-2 gap exceeds GAP."""
+    from oracle.context import output_logits
+    o = output_logits(ow, hp, x_last.astype(np.float64))
+    out = {"logits": 0.0, "tokens_checked": 0}
+    for t in range(len(o)):
+        out["logits"] = max(out["logits"], rel_err(g_logits[t], o[t]))
+        top = np.argsort(o[t])[-2:]
+        if o[t][top[1]] - o[t][top[0]] > GAP:
+            assert int(g_argmax[t]) == int(top[1]), (t, int(g_argmax[t]), int(top[1]))
+            out["tokens_checked"] += 1
+    return out
+
+
+def kv_layer(ctx, il: int):
+    return ctx.kv_cache(il, 0), ctx.kv_cache(il, 1)
+
+
+def captured_rows(ctx, il: int, rows):
+    """(x_in, x_out) rows of layer il from the library's capture of its last ubatch."""
+    src = ctx.debug_tensor("embd") if il == 0 else ctx.debug_tensor("l_out", il - 1)
+    d = ctx._hp.n_embd
+    x_in = src.reshape(-1, d)[rows]
+    x_out = ctx.debug_tensor("l_out", il).reshape(-1, d)[rows]
+    return x_in, x_out

@@ -74,6 +74,7 @@ SIGNATURES = {
     "llm_debug_get_tensor": (C.c_int64, [C.c_void_p, C.c_char_p, C.c_int32,
                                          C.POINTER(C.c_float), C.c_int64]),
     "llm_debug_inject_fault": (C.c_int, [C.c_void_p, C.c_int32, C.c_int32]),
+    "llm_debug_kv_raw": (C.c_int64, [C.c_void_p, C.c_int32, C.c_int32, C.c_void_p, C.c_int64]),
     "llm_debug_kernel_timing": (C.c_int, [C.c_void_p, C.c_int]),
     "llm_gemm_bf16_noalloc": (C.c_int, [C.c_int32, C.c_void_p, C.c_int64, C.c_int64, C.c_void_p,
                                         C.c_int32, C.c_void_p, C.c_int32, C.c_int32]),
@@ -293,6 +294,18 @@ class Context:
         out = np.zeros(n, dtype=np.float32)
         lib().llm_debug_get_tensor(self.ptr, name.encode(), layer, _ptr(out, C.c_float), n)
         return out
+
+    def kv_cache(self, layer: int, which: int) -> Optional[np.ndarray]:
+        """Layer `layer`'s K (which 0) or V (which 1) cache as stored, [n_head_kv][n_ctx][head_dim]
+        (float32 or float16 elements)."""
+        n = lib().llm_debug_kv_raw(self.ptr, layer, which, None, 0)
+        if n <= 0:
+            return None
+        out = np.zeros(n, dtype=np.uint8)
+        lib().llm_debug_kv_raw(self.ptr, layer, which, out.ctypes.data_as(C.c_void_p), n)
+        es = 4 if n // (self._hp.n_head_kv * self._hp.head_dim) == 4 * self.n_ctx else 2
+        v = out.view(np.float32 if es == 4 else np.float16)
+        return v.reshape(self._hp.n_head_kv, -1, self._hp.head_dim)
 
     def kernel_timing(self, enable: bool = True) -> int:
         return lib().llm_debug_kernel_timing(self.ptr, int(enable))

@@ -120,8 +120,12 @@ __device__ __forceinline__ unsigned long long pack_argmax(float v, int idx) {
 
 struct Range { int64_t row0, nrows; int local0; };
 
+// Column-stationary one-token variants with at most 32 weights per lane fit three blocks per SM
+// without spilling: two of this kernel and one of the next, which programmatic dependent launch
+// starts early to prefetch its weights.
 template <int WT, int TM, int EPI, bool NORM, int SPW>
-__global__ void __launch_bounds__(kThreads, TM <= 2 ? 2 : 1)
+__global__ void __launch_bounds__(kThreads, TM == 1 && SPW > 0 && SPW * Vec<WT>::N <= 32 ? 3
+                                            : TM <= 2 ? 2 : 1)
 gemv_bulk_kernel(const GemvArgs a) {
     constexpr bool COLS = SPW > 0;
     constexpr int VN = Vec<WT>::N, ES = Vec<WT>::ES;

@@ -150,6 +150,7 @@ struct llm_ctx {
     bool debug = false;
     std::vector<UbDebug> dbg_ub;
     float *dbg_embd = nullptr, *dbg_lout = nullptr, *dbg_attn = nullptr, *dbg_q = nullptr;
+    bool dbg_rnorm_valid = false;   // the final-normed rows exist only on the unfused output path
     float* dbg_rnorm = nullptr;
     int32_t dbg_T = 0, dbg_O = 0;
     int32_t fault_kind = 0, fault_ub = -1;
@@ -585,7 +586,8 @@ bool forward_ubatch(llm_ctx* c, int32_t T, int32_t O, int32_t out_row0, int32_t 
         float* lg = c->d_logits + (size_t)out_row0 * hp.n_vocab;
         const int32_t* orows = din + io.out_rows;
         const double lm_bytes = wbytes(c->out, hp.n_vocab) + Od * (d + (double)hp.n_vocab) * 4.0;
-        if (bulk.lm && !c->debug) {
+        c->dbg_rnorm_valid = false;
+        if (bulk.lm) {
             k = kt_begin(c);
             g.T = O;
             g.W = c->out.data; g.S = c->out.scales; g.row0 = 0; g.M = hp.n_vocab; g.K = d;
@@ -599,8 +601,10 @@ bool forward_ubatch(llm_ctx* c, int32_t T, int32_t O, int32_t out_row0, int32_t 
             if (tc_out) launch_rmsnorm_bf16(c->x, orows, O, d, c->out_norm, hp.rms_eps, c->hob, c->hob_lo, st);
             launch_rmsnorm(c->x, orows, O, d, c->out_norm, hp.rms_eps, c->hout, st);
             kt_end(c, k, KC_RMSNORM, Od * d * 8.0 + d * 4.0, 0);
-            if (c->debug)
+            if (c->debug) {
                 cudaMemcpyAsync(c->dbg_rnorm, c->hout, sizeof(float) * O * d, cudaMemcpyDeviceToDevice, st);
+                c->dbg_rnorm_valid = true;
+            }
             k = kt_begin(c);
             if (tc_out) {
                 if (!launch_gemm_tc(c->m_lm, c->m_hob[0], GEMM_EPI_STORE, d, hp.n_vocab, O, F, lg,
@@ -1164,7 +1168,7 @@ int64_t llm_debug_get_tensor(llm_ctx* c, const char* name, int32_t layer, float*
     const float* src = nullptr;
     int64_t cnt = 0;
     if (n == "embd") { src = c->dbg_embd; cnt = T * d; }
-    else if (n == "result_norm") { src = c->dbg_rnorm; cnt = (int64_t)c->dbg_O * d; }
+    else if (n == "result_norm" && c->dbg_rnorm_valid) { src = c->dbg_rnorm; cnt = (int64_t)c->dbg_O * d; }
     else if (layer >= 0 && layer < c->hp.n_layer) {
         if (n == "l_out") { src = c->dbg_lout + layer * T * d; cnt = T * d; }
         else if (n == "attn_out") { src = c->dbg_attn + layer * T * qw; cnt = T * qw; }
@@ -1176,6 +1180,19 @@ int64_t llm_debug_get_tensor(llm_ctx* c, const char* name, int32_t layer, float*
         cudaMemcpy(out, src, sizeof(float) * std::min(cnt, cap), cudaMemcpyDeviceToHost);
     }
     return cnt;
+}
+
+int64_t llm_debug_kv_raw(llm_ctx* c, int32_t layer, int32_t which, void* out, int64_t cap_bytes) {
+    if (!c || c->host_only || layer < 0 || layer >= c->hp.n_layer || (which != 0 && which != 1))
+        return 0;
+    const size_t es = type_size(which == 0 ? c->type_k : c->type_v);
+    const int64_t n = (int64_t)(c->kv_layer_elems() * es);
+    if (out && cap_bytes > 0) {
+        const uint8_t* src = static_cast<const uint8_t*>(which == 0 ? c->kv_k : c->kv_v) + (size_t)layer * n;
+        cudaStreamSynchronize(c->st);
+        cudaMemcpy(out, src, (size_t)std::min(n, cap_bytes), cudaMemcpyDeviceToHost);
+    }
+    return n;
 }
 
 int llm_debug_kernel_timing(llm_ctx* c, int enable) {
