@@ -68,6 +68,10 @@ enum {
      * memory is allocated and no kernel runs; llm_get_logits_ith returns NULL. Lets the host
      * control plane be tested on a machine without a GPU. */
     LLM_CTX_HOST_ONLY = 1u << 0,
+    /* Run one-token ubatches through the per-op kernel sequence (replayed as a CUDA graph)
+     * instead of the single persistent decode-step kernel. Both compute the same ops in float32
+     * over the stored weights; the flag exists to compare them and to time the difference. */
+    LLM_CTX_PER_OP_KERNELS = 1u << 1,
 };
 
 /* Context parameters ([P1] Крок 9-10 context constructor; [P2] Example 9; [P4] コンテキストの構築).
@@ -205,6 +209,7 @@ typedef struct llm_perf_data {
     int64_t n_ubatches;
     int64_t n_graph_replays;
     double  t_decode_ms;
+    int64_t n_fused_steps;   /* one-token ubatches run as the single persistent kernel */
 } llm_perf_data;
 void llm_perf(llm_ctx *ctx, llm_perf_data *out);
 
@@ -275,6 +280,18 @@ int llm_debug_gemm_bf16(int32_t epi, const void *W, int64_t M, int64_t K, const 
  * reported an error. Synchronous (legacy default stream). */
 int llm_gemm_bf16_noalloc(int32_t epi, const void *W, int64_t M, int64_t K, const void *X,
                           int32_t T, void *Y, int32_t ldy, int32_t F);
+
+/* Timeline of the persistent one-token kernel. enable != 0 makes later one-token steps record, per
+ * block, global-timer stamps (ns) at the start and end of each consumer phase and at the first
+ * and last weight copy the block's producer issues for each matrix; 0 stops. */
+int llm_debug_step_trace_enable(llm_ctx *ctx, int enable);
+/* Copy the last recorded step's stamps to out as [n_blocks][n_slots][2] (start, end) uint64
+ * values: slot 0 the embedding phase, 1 + 5 l + op the phases of layer l (op 0 Q/K/V, 1 attention,
+ * 2 output projection, 3 gate/up, 4 down), 1 + 5 n_layer the output matrix, then
+ * 2 + 5 n_layer + j the producer's matrix j (4 per layer, then the output matrix). Returns the
+ * number of values (0 if nothing was recorded); writes at most cap. */
+int64_t llm_debug_step_trace(llm_ctx *ctx, uint64_t *out, int64_t cap, int32_t *n_blocks,
+                             int32_t *n_slots);
 
 /* Fault injection: kind 1 makes ubatch `ub` of the next llm_decode hand the K/V append kernel a
  * cell index past the cache; the kernel's bounds check skips the write and reports the error

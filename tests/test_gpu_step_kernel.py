@@ -1,0 +1,76 @@
+"""GPU parity of the single persistent decode-step kernel (one-token ubatches) on a 2-layer model
+with the Llama-3-8B layer shape (d 4096, 32/8 heads, head_dim 128, n_ff 14336), a 32000-token
+vocabulary, BF16 weights and an F16 KV cache.
+
+The 300-token prompt splits each KV head's attention of a decode step into several work items,
+so the partial-softmax merge runs. Every step is compared with the oracle (logits max relative
+error; greedy tokens where the oracle's top-2 gap exceeds 1e-3) and with the per-op kernel
+sequence of a second context on the same tokens (both compute in float32 over the stored
+weights, so they agree to float32 summation-order noise). One step requests no logits, which
+runs the kernel without its output-matrix phase."""
+import numpy as np
+import pytest
+
+import synthetic as S
+from synthetic.configs import HParams, Workload
+from tests import gpu_common as G
+
+pytestmark = pytest.mark.gpu
+
+HP = HParams(n_layer=2, n_embd=4096, n_head=32, n_head_kv=8, head_dim=128, n_ff=14336,
+             n_vocab=32000, rope_freq_base=500000.0, rms_eps=1e-5)
+KEY = "llama8b_layers2_bf16"
+N_STEPS = 12
+TOL_ORACLE = 2e-2      # the BF16 bar
+TOL_DECODE = 1e-3      # one-token steps: float32 activations over bf16 weights
+TOL_PATHS = 1e-4       # fused kernel against the per-op kernels
+
+
+def test_step_kernel_matches_oracle_and_per_op_kernels():
+    S.WORKLOADS[KEY] = Workload(KEY, HP, {"embd": S.BF16, "linear": S.BF16}, S.F16, n_ctx=1024,
+                                n_seq=1, n_prompt=300, n_batch=512, n_ubatch=512, n_decode=N_STEPS,
+                                weight_seed=3300, prompt_seed=4300)
+    G.device_model.cache_clear()
+    G.oracle_weights.cache_clear()
+    ctx = G.library_ctx(KEY)
+    ref = G.library_ctx(KEY, per_op_kernels=True)
+    ora = G.oracle_ctx(KEY)
+    toks = G.prompts(KEY)[0]
+    for c in (ctx, ref):
+        assert c.decode(toks) == 0, c.last_error()
+    assert ora.decode(toks) == 0
+    report = {"oracle": 0.0, "decode_vs_oracle": 0.0, "paths": 0.0, "tokens_checked": 0}
+    silent_step = 5
+    for step in range(N_STEPS + 1):
+        if step != silent_step + 1:
+            g, r, o = ctx.get_logits_ith(-1), ref.get_logits_ith(-1), ora.get_logits_ith(-1)
+            e_o = G.rel_err(g, o)
+            e_r = G.rel_err(g, r.astype(np.float64))
+            report["oracle"] = max(report["oracle"], e_o)
+            report["paths"] = max(report["paths"], e_r)
+            assert e_o <= TOL_ORACLE, (step, e_o)
+            if step > 0:
+                report["decode_vs_oracle"] = max(report["decode_vs_oracle"], e_o)
+                assert e_o <= TOL_DECODE, (step, e_o)
+                assert e_r <= TOL_PATHS, (step, e_r)
+            tg = ctx.get_argmax_ith(-1)
+            assert tg == int(np.argmax(g)) and ref.get_argmax_ith(-1) == int(np.argmax(r))
+            top = np.argsort(o)[-2:]
+            if o[top[1]] - o[top[0]] > G.GAP:
+                assert tg == int(top[1]), (step, tg, int(top[1]))
+                report["tokens_checked"] += 1
+            nxt = tg
+        else:
+            nxt = 7                 # the step without logits fed a fixed token
+        if step == N_STEPS:
+            break
+        flag = 0 if step == silent_step else 1
+        for c in (ctx, ref):
+            assert c.decode([nxt], logits=[flag]) == 0, c.last_error()
+        assert ora.decode([nxt], logits=[flag]) == 0
+    print("fused decode-step parity:", report)
+    assert ctx.perf()["n_fused_steps"] == N_STEPS
+    assert ref.perf()["n_fused_steps"] == 0
+    assert report["tokens_checked"] >= N_STEPS // 2
+    ctx.free()
+    ref.free()

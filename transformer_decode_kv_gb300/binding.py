@@ -17,6 +17,7 @@ LIB_PATH = os.path.join(_PKG, "libllm.so")
 
 F32, F16, BF16, Q8_0 = 0, 1, 2, 8
 CTX_HOST_ONLY = 1
+CTX_PER_OP_KERNELS = 2
 
 
 class HParams(C.Structure):
@@ -40,7 +41,8 @@ class Batch(C.Structure):
 
 class PerfData(C.Structure):
     _fields_ = [("n_decode_calls", C.c_int64), ("n_tokens", C.c_int64), ("n_ubatches", C.c_int64),
-                ("n_graph_replays", C.c_int64), ("t_decode_ms", C.c_double)]
+                ("n_graph_replays", C.c_int64), ("t_decode_ms", C.c_double),
+                ("n_fused_steps", C.c_int64)]
 
 
 ABORT_CB = C.CFUNCTYPE(C.c_int, C.c_void_p)
@@ -75,6 +77,9 @@ SIGNATURES = {
                                          C.POINTER(C.c_float), C.c_int64]),
     "llm_debug_inject_fault": (C.c_int, [C.c_void_p, C.c_int32, C.c_int32]),
     "llm_debug_kv_raw": (C.c_int64, [C.c_void_p, C.c_int32, C.c_int32, C.c_void_p, C.c_int64]),
+    "llm_debug_step_trace_enable": (C.c_int, [C.c_void_p, C.c_int]),
+    "llm_debug_step_trace": (C.c_int64, [C.c_void_p, C.POINTER(C.c_uint64), C.c_int64,
+                                         C.POINTER(C.c_int32), C.POINTER(C.c_int32)]),
     "llm_debug_kernel_timing": (C.c_int, [C.c_void_p, C.c_int]),
     "llm_gemm_bf16_noalloc": (C.c_int, [C.c_int32, C.c_void_p, C.c_int64, C.c_int64, C.c_void_p,
                                         C.c_int32, C.c_void_p, C.c_int32, C.c_int32]),
@@ -135,7 +140,7 @@ class Context:
 
     def __init__(self, hp, n_ctx: int, n_seq_max: int = 1, type_k: int = F16, type_v: int = F16,
                  n_batch: int = 2048, n_ubatch: int = 512, stream: Optional[int] = None,
-                 host_only: bool = False):
+                 host_only: bool = False, per_op_kernels: bool = False):
         L = lib()
         self._hp = HParams(hp.n_layer, hp.n_embd, hp.n_head, hp.n_head_kv, hp.head_dim, hp.n_ff,
                            hp.n_vocab, hp.rope_freq_base, hp.rms_eps, getattr(hp, "rope_type", 0))
@@ -143,7 +148,7 @@ class Context:
         cp.n_ctx, cp.n_seq_max, cp.n_batch, cp.n_ubatch = n_ctx, n_seq_max, n_batch, n_ubatch
         cp.type_k, cp.type_v = type_k, type_v
         cp.stream = stream
-        cp.flags = CTX_HOST_ONLY if host_only else 0
+        cp.flags = (CTX_HOST_ONLY if host_only else 0) | (CTX_PER_OP_KERNELS if per_op_kernels else 0)
         self.n_vocab = hp.n_vocab
         self.ptr = L.llm_ctx_init(C.byref(self._hp), C.byref(cp))
         if not self.ptr:
@@ -306,6 +311,19 @@ class Context:
         es = 4 if n // (self._hp.n_head_kv * self._hp.head_dim) == 4 * self.n_ctx else 2
         v = out.view(np.float32 if es == 4 else np.float16)
         return v.reshape(self._hp.n_head_kv, -1, self._hp.head_dim)
+
+    def step_trace_enable(self, enable: bool = True) -> int:
+        return lib().llm_debug_step_trace_enable(self.ptr, int(enable))
+
+    def step_trace(self) -> Optional[np.ndarray]:
+        """The last traced one-token step as uint64 [blocks][slots][2] (start, end) ns stamps."""
+        nb, ns = C.c_int32(0), C.c_int32(0)
+        n = lib().llm_debug_step_trace(self.ptr, None, 0, C.byref(nb), C.byref(ns))
+        if n <= 0:
+            return None
+        out = np.zeros(n, dtype=np.uint64)
+        lib().llm_debug_step_trace(self.ptr, out.ctypes.data_as(C.POINTER(C.c_uint64)), n, None, None)
+        return out.reshape(nb.value, ns.value, 2)
 
     def kernel_timing(self, enable: bool = True) -> int:
         return lib().llm_debug_kernel_timing(self.ptr, int(enable))

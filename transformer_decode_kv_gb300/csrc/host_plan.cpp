@@ -232,7 +232,8 @@ void build_attn_plan(const KvCells& cells, const SanBatch& b, int32_t i0, int32_
             const int32_t l = p.tile_list[t];
             const int32_t L = p.list_off[l + 1] - p.list_off[l];
             int32_t chunk = (L + want - 1) / want;
-            chunk = std::max(min_chunk, (chunk + 31) / 32 * 32);
+            const int32_t gran = std::min<int32_t>(32, min_chunk);
+            chunk = std::max(min_chunk, (chunk + gran - 1) / gran * gran);
             for (int32_t c0 = 0; c0 < std::max(L, 1); c0 += chunk) {
                 p.wi_tile.push_back(t);
                 p.wi_c0.push_back(c0);

@@ -6,24 +6,15 @@
 #include <cfloat>
 #include <climits>
 
+#include "dev_common.cuh"
 #include "kernels.h"
 
 namespace llm {
 
 namespace {
 
-__device__ __forceinline__ float load_elem(const DevMat& m, int64_t row, int64_t col) {
-    const int64_t i = row * m.cols + col;
-    switch (m.type) {
-        case W_F32: return static_cast<const float*>(m.data)[i];
-        case W_F16: return __half2float(static_cast<const __half*>(m.data)[i]);
-        case W_BF16: return __bfloat162float(static_cast<const __nv_bfloat16*>(m.data)[i]);
-        default: {
-            const float d = __half2float(m.scales[row * (m.cols / 32) + col / 32]);
-            return d * (float)static_cast<const int8_t*>(m.data)[i];
-        }
-    }
-}
+using dev::load_elem;
+using dev::rope_cos_sin;
 
 __device__ __forceinline__ float block_sum(float v, float* red) {
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
@@ -141,12 +132,7 @@ __global__ void embed_rope_kernel(DevMat E, const int32_t* __restrict__ tok,
     for (int64_t j = threadIdx.x; j < E.cols; j += blockDim.x)
         x[(int64_t)t * E.cols + j] = ok ? load_elem(E, id, j) : 0.f;
     for (int i = threadIdx.x; i < half; i += blockDim.x) {
-        // the angle pos * theta_i in double, reduced to [-pi, pi] in double, then float sincos
-        const double ang = (double)pos[t] * theta[i];
-        const double r = ang - rint(ang * 0.15915494309189535) * 6.283185307179586;
-        float s, c;
-        sincosf((float)r, &s, &c);
-        cs[(int64_t)t * half + i] = make_float2(c, s);
+        cs[(int64_t)t * half + i] = rope_cos_sin(pos[t], theta[i]);
     }
     if (t == 0)
         for (int i = threadIdx.x; i < n_amax; i += blockDim.x) amax[i] = 0ull;

@@ -18,6 +18,7 @@
 #include <string>
 #include <vector>
 
+#include "decode_step.h"
 #include "gemm_tc.h"
 #include "gemv_bulk.h"
 #include "host_plan.h"
@@ -58,11 +59,11 @@ struct Layer {
 // Kernel classes timed by llm_debug_kernel_timing.
 enum KClass : int32_t {
     KC_EMBED, KC_ROPE_TABLE, KC_RMSNORM, KC_LINEAR_GEMV, KC_LINEAR_GEMM, KC_ROPE_KV, KC_ATTENTION,
-    KC_LM_HEAD, KC_ARGMAX, KC_LINEAR_TC, KC_COUNT
+    KC_LM_HEAD, KC_ARGMAX, KC_LINEAR_TC, KC_DECODE_STEP, KC_COUNT
 };
 const char* const kKClassNames[KC_COUNT] = {"embed", "rope_table", "rmsnorm", "linear_gemv",
                                             "linear_gemm", "rope_kv_append", "attention",
-                                            "lm_head", "argmax", "linear_tcgen05"};
+                                            "lm_head", "argmax", "linear_tcgen05", "decode_step"};
 struct KStat { int64_t launches = 0; double ms = 0, bytes = 0, flops = 0; };
 struct KPending { int32_t cls; cudaEvent_t a, b; double bytes, flops; };
 
@@ -166,6 +167,17 @@ struct llm_ctx {
 
     // decode-step graphs, per (tokens, outputs, output row, tile shape, timing) key
     bool use_graphs = true, use_pdl = true, use_bulk = true;
+    // one-token ubatches as one persistent kernel (decode_step.cu)
+    bool use_step = true, step_ok = false;
+    StepLayer* d_step_layers = nullptr;
+    uint32_t* d_counters = nullptr;     // its grid-wide phase counters [1 + 5 n_layer]
+    int32_t* d_abort = nullptr;
+    uint32_t step_gen = 0;              // launches since the counters were last zeroed
+    bool step_trace = false;
+    uint64_t* d_trace = nullptr;        // timeline of the last traced step
+    int32_t trace_blocks = 0, trace_slots = 0;
+    bool trace_valid = false;
+    double step_weight_bytes = 0;
     std::map<uint64_t, StepGraph> graphs;
 
     SanBatch batch;
@@ -688,6 +700,7 @@ llm_ctx* llm_ctx_init(const llm_hparams* hp, const llm_cparams* cp) {
     c->type_k = cp->type_k;
     c->type_v = cp->type_v;
     c->host_only = (cp->flags & LLM_CTX_HOST_ONLY) != 0;
+    c->use_step = (cp->flags & LLM_CTX_PER_OP_KERNELS) == 0;
     c->cells = KvCells(c->n_ctx, c->n_seq_max);
     c->layers.resize(h.n_layer);
     if (c->host_only) return c;
@@ -723,6 +736,9 @@ llm_ctx* llm_ctx_init(const llm_hparams* hp, const llm_cparams* cp) {
               dalloc(c, reinterpret_cast<uint16_t**>(&c->ub_lo), U * (int64_t)h.n_ff) &&
               dalloc(c, reinterpret_cast<uint16_t**>(&c->hob_lo), U * d) &&
               dalloc(c, &c->d_err, 1) &&
+              dalloc(c, &c->d_counters, 1 + 5 * (size_t)h.n_layer) && dalloc(c, &c->d_abort, 1) &&
+              cuda_ok(c, cudaMemset(c->d_counters, 0, sizeof(uint32_t) * (1 + 5 * (size_t)h.n_layer)), "memset") &&
+              cuda_ok(c, cudaMemset(c->d_abort, 0, sizeof(int32_t)), "memset") &&
               cuda_ok(c, cudaMallocHost(&c->h_err, sizeof(uint32_t)), "cudaMallocHost");
     if (!ok) return die("");
     {
@@ -852,6 +868,93 @@ int llm_load_weights(llm_ctx* c, const char* name, int32_t type, const int64_t n
     return 0;
 }
 
+// The persistent one-token kernel serves the model when every linear weight (and the output
+// matrix) has one 2-byte type and the shapes fit its mapping; its per-layer table is uploaded here.
+static void setup_step(llm_ctx* c) {
+    c->step_ok = false;
+    if (!c->use_step || c->host_only) return;
+    const llm_hparams& h = c->hp;
+    const int32_t wt = c->layers.empty() ? -1 : c->layers[0].qkv.type;
+    bool same = c->out.type == wt;
+    for (const Layer& L : c->layers)
+        same = same && L.qkv.type == wt && L.wo.type == wt && L.gu.type == wt && L.down.type == wt;
+    if (!same || !decode_step_ok(wt, h.n_embd, h.n_head, h.n_head_kv, h.head_dim, h.n_ff, h.n_vocab,
+                                 c->type_k, c->n_sm)) {
+        cudaGetLastError();
+        return;
+    }
+    std::vector<StepLayer> t(h.n_layer);
+    const size_t kv_es = type_size(c->type_k);
+    double wb = wbytes(c->out, h.n_vocab);
+    for (int32_t il = 0; il < h.n_layer; ++il) {
+        const Layer& L = c->layers[il];
+        t[il].qkv = L.qkv.data; t[il].wo = L.wo.data; t[il].gu = L.gu.data; t[il].down = L.down.data;
+        t[il].attn_norm = L.attn_norm; t[il].ffn_norm = L.ffn_norm;
+        t[il].kc = static_cast<uint8_t*>(c->kv_k) + (size_t)il * c->kv_layer_elems() * kv_es;
+        t[il].vc = static_cast<uint8_t*>(c->kv_v) + (size_t)il * c->kv_layer_elems() * kv_es;
+        wb += wbytes(L.qkv, c->qkv_width()) + wbytes(L.wo, h.n_embd) + wbytes(L.gu, 2 * (int64_t)h.n_ff) +
+              wbytes(L.down, h.n_embd);
+    }
+    if (!c->d_step_layers && !dalloc(c, &c->d_step_layers, t.size())) return;
+    if (!cuda_ok(c, cudaMemcpy(c->d_step_layers, t.data(), t.size() * sizeof(StepLayer),
+                               cudaMemcpyHostToDevice), "copy"))
+        return;
+    c->step_weight_bytes = wb;
+    c->step_ok = true;
+}
+
+// After a failed step the phase counters, the abort flag and the attention tickets are reset.
+static bool reset_step_state(llm_ctx* c) {
+    c->step_gen = 0;
+    return cuda_ok(c, cudaMemsetAsync(c->d_counters, 0, sizeof(uint32_t) * (1 + 5 * (size_t)c->hp.n_layer), c->st), "memset") &&
+           cuda_ok(c, cudaMemsetAsync(c->d_abort, 0, sizeof(int32_t), c->st), "memset") &&
+           cuda_ok(c, cudaMemsetAsync(c->tickets, 0, sizeof(int32_t) * c->n_ubatch * c->hp.n_head_kv, c->st), "memset");
+}
+
+// One token through the whole model in one cooperative launch (inputs already uploaded).
+static bool run_step(llm_ctx* c, int32_t O, int32_t out_row0) {
+    const llm_hparams& hp = c->hp;
+    const InLayout& io = c->io;
+    const int32_t* din = c->d_in;
+    StepArgs a;
+    a.layers = c->d_step_layers;
+    a.n_layer = hp.n_layer; a.d = hp.n_embd; a.H = hp.n_head; a.Hkv = hp.n_head_kv; a.hd = hp.head_dim;
+    a.F = hp.n_ff; a.V = hp.n_vocab; a.eps = hp.rms_eps;
+    a.embd = c->embd; a.theta = c->d_theta; a.out = c->out.data; a.out_norm = c->out_norm;
+    a.do_logits = O > 0 ? 1 : 0;
+    a.x = c->x; a.q = c->qkv; a.o = c->attn; a.u = c->u; a.cs = c->rope_cs;
+    a.logits = c->d_logits + (size_t)out_row0 * hp.n_vocab;
+    a.amax = c->d_amax + out_row0;
+    a.tok = din + io.tok; a.pos = din + io.pos; a.slot = din + io.slot; a.hdr = din + io.hdr;
+    a.tile_desc = reinterpret_cast<const int4*>(din + io.tile_desc);
+    a.wi_desc = reinterpret_cast<const int4*>(din + io.wi_desc);
+    a.list_cells = din + io.list_cells; a.list_pos = din + io.list_pos;
+    a.part_o = c->part_o; a.part_m = c->part_m; a.part_l = c->part_l; a.tickets = c->tickets;
+    a.n_ctx = c->n_ctx; a.kv_type = c->type_k;
+    a.counters = c->d_counters; a.gen = c->step_gen; a.abort_flag = c->d_abort; a.err = c->d_err;
+    if (c->step_trace) {
+        const int32_t slots = 3 + 9 * hp.n_layer, blocks = 2 * c->n_sm;
+        if (!c->d_trace) {
+            if (!dalloc(c, &c->d_trace, (size_t)blocks * slots * 2)) return false;
+            cudaMemsetAsync(c->d_trace, 0, sizeof(uint64_t) * blocks * slots * 2, c->st);
+        }
+        a.trace = c->d_trace;
+        a.n_trace = slots;
+        c->trace_blocks = blocks;
+        c->trace_slots = slots;
+        c->trace_valid = true;
+    }
+    const int k = kt_begin(c);
+    if (!launch_decode_step(c->layers[0].qkv.type, a, c->n_sm, c->st)) {
+        c->err = "decode step launch failed";
+        return false;
+    }
+    kt_end(c, k, KC_DECODE_STEP, c->step_weight_bytes + c->att_bytes_now, 0);
+    c->step_gen += 1;
+    c->perf.n_fused_steps += 1;
+    return true;
+}
+
 int llm_weights_ready(llm_ctx* c) {
     if (!c) return -1;
     if (!c->embd_loaded) { c->err = "missing token_embd.weight"; return -1; }
@@ -895,6 +998,7 @@ int llm_weights_ready(llm_ctx* c) {
     const bool lm_ok = c->out.type == LLM_TYPE_BF16 && tc_shape_ok(h.n_vocab, d, GEMM_EPI_STORE, 0) &&
                        tc_make_map(&c->m_lm, c->out.data, h.n_vocab, d, 128);
     c->tc_ok = ok && lm_ok;
+    setup_step(c);
     return 0;
 }
 
@@ -945,8 +1049,10 @@ int32_t llm_decode(llm_ctx* c, llm_batch bt) {
         }
         const bool small = T <= gemv_max_tokens();
         const int32_t cap = small ? attn_cap(c, T) : c->max_work;
+        // the one-token kernel stages one pass of decode_step_cells() cells per work item
+        const bool fused = T == 1 && c->step_ok && !c->debug;
         build_attn_plan(c->cells, b, i0, T, kAttnTileQ, c->hp.n_head_kv, G, 4 * c->n_sm,
-                        c->max_rows, cap, c->plan, small ? 64 : 32);
+                        c->max_rows, cap, c->plan, fused ? decode_step_cells() : small ? 64 : 32);
         if (c->debug) {
             UbDebug u;
             u.n_kv = c->cells.n_kv();
@@ -1002,7 +1108,9 @@ int32_t llm_decode(llm_ctx* c, llm_batch bt) {
         if (c->ktime) attention_work(c, b.pos.data() + i0);
         const int32_t max_nq = p.max_nq <= 1 ? 1 : kAttnTileQ;
         const StepGraph* sg = nullptr;
-        if (ok && small && c->use_graphs && !c->debug) {
+        const bool one_kernel = ok && T == 1 && c->step_ok && !c->debug;
+        if (one_kernel) ok = run_step(c, O, n_out);
+        if (ok && !one_kernel && small && c->use_graphs && !c->debug) {
             const uint64_t key = (uint64_t)T | ((uint64_t)O << 10) | ((uint64_t)n_out << 20) |
                                  ((uint64_t)(max_nq > 1) << 52) | ((uint64_t)c->ktime << 53);
             auto it = c->graphs.find(key);
@@ -1032,7 +1140,7 @@ int32_t llm_decode(llm_ctx* c, llm_batch bt) {
                 c->perf.n_graph_replays += 1;
             }
         }
-        if (ok && !sg) ok = forward_ubatch(c, T, O, n_out, max_nq);
+        if (ok && !sg && !one_kernel) ok = forward_ubatch(c, T, O, n_out, max_nq);
         ok = ok && cuda_ok(c, cudaMemcpyAsync(c->h_err, c->d_err, sizeof(uint32_t),
                                               cudaMemcpyDeviceToHost, c->st), "error word") &&
              cuda_ok(c, cudaStreamSynchronize(c->st), "device computation");
@@ -1044,6 +1152,7 @@ int32_t llm_decode(llm_ctx* c, llm_batch bt) {
         if (!ok) {
             rollback(c, i0, T);
             c->fault_kind = 0;
+            if (one_kernel) reset_step_state(c);
             return -3;
         }
         n_out += O;
@@ -1237,6 +1346,24 @@ int llm_debug_gemm_bf16(int32_t epi, const void* W, int64_t M, int64_t K, const 
          cudaMemcpy(&h, err, sizeof(uint32_t), cudaMemcpyDeviceToHost) == cudaSuccess;
     cudaFree(err);
     return ok && h == 0 ? 0 : -3;
+}
+
+int llm_debug_step_trace_enable(llm_ctx* c, int enable) {
+    if (!c) return -1;
+    c->step_trace = enable != 0 && !c->host_only;
+    return 0;
+}
+
+int64_t llm_debug_step_trace(llm_ctx* c, uint64_t* out, int64_t cap, int32_t* n_blocks, int32_t* n_slots) {
+    if (!c || !c->trace_valid || !c->d_trace) return 0;
+    const int64_t n = (int64_t)c->trace_blocks * c->trace_slots * 2;
+    if (n_blocks) *n_blocks = c->trace_blocks;
+    if (n_slots) *n_slots = c->trace_slots;
+    if (out && cap > 0) {
+        cudaStreamSynchronize(c->st);
+        cudaMemcpy(out, c->d_trace, sizeof(uint64_t) * (size_t)std::min(n, cap), cudaMemcpyDeviceToHost);
+    }
+    return n;
 }
 
 int llm_debug_inject_fault(llm_ctx* c, int32_t kind, int32_t ub) {
