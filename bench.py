@@ -180,7 +180,7 @@ def run_gpu(args, rank, world, local_rank):
     stream = torch.cuda.Stream()
     ctx = Context(hp, n_ctx=w.n_ctx, n_seq_max=1, type_k=w.type_kv, type_v=w.type_kv,
                   n_batch=max(w.n_batch, w.n_prompt), n_ubatch=w.n_ubatch, stream=stream.cuda_stream,
-                  per_op_kernels=args.per_op_kernels)
+                  fused_step=args.fused_step)
     for name, wt, shape, t in S.model_weights(hp, w.weight_seed, w.types, "cuda"):
         if ctx.load_weight(name, wt, shape, t) != 0:
             raise RuntimeError(ctx.last_error())
@@ -271,9 +271,9 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--workload", default="llama8b_bf16_1seq")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--per-op-kernels", action="store_true",
-                    help="one-token steps through the per-op kernel sequence instead of the single "
-                         "persistent step kernel (for comparison)")
+    ap.add_argument("--fused-step", action="store_true",
+                    help="one-token steps as the single persistent step kernel instead of the "
+                         "per-op kernel sequence (for comparison)")
     ap.add_argument("--layers", type=int, default=0,
                     help="profiling aid: run the workload's shape with only this many layers "
                          "(a small case for ncu captures; not a bench number)")
@@ -292,7 +292,7 @@ def main():
               "n_ctx": w.n_ctx, "kv_cache": "f16" if w.type_kv == 1 else "f32",
               "l2": "inputs larger than L2: every decode step streams all weights (no flush)",
               "parallelism": "replicas" if args.gpus > 1 else "single",
-              "decode_path": "per-op kernels" if args.per_op_kernels else "persistent step kernel"}
+              "decode_path": "persistent step kernel" if args.fused_step else "per-op kernels (graph)"}
     if args.layers:
         config["profiling_case_layers"] = args.layers
 

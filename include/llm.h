@@ -68,10 +68,12 @@ enum {
      * memory is allocated and no kernel runs; llm_get_logits_ith returns NULL. Lets the host
      * control plane be tested on a machine without a GPU. */
     LLM_CTX_HOST_ONLY = 1u << 0,
-    /* Run one-token ubatches through the per-op kernel sequence (replayed as a CUDA graph)
-     * instead of the single persistent decode-step kernel. Both compute the same ops in float32
-     * over the stored weights; the flag exists to compare them and to time the difference. */
-    LLM_CTX_PER_OP_KERNELS = 1u << 1,
+    /* Run one-token ubatches as the single persistent decode-step kernel instead of the per-op
+     * kernel sequence (replayed as a CUDA graph). Both compute the same ops in float32 over the
+     * stored weights; the persistent kernel serves 2-byte weights of the 8B layer shape only.
+     * Off by default: on a GB300 the per-op sequence is as fast or faster (3.43 vs 3.47 ms per
+     * 8B BF16 step). */
+    LLM_CTX_FUSED_STEP = 1u << 1,
 };
 
 /* Context parameters ([P1] Крок 9-10 context constructor; [P2] Example 9; [P4] コンテキストの構築).

@@ -5,9 +5,9 @@ vocabulary, BF16 weights and an F16 KV cache.
 The 300-token prompt splits each KV head's attention of a decode step into several work items,
 so the partial-softmax merge runs. Every step is compared with the oracle (logits max relative
 error; greedy tokens where the oracle's top-2 gap exceeds 1e-3) and with the per-op kernel
-sequence of a second context on the same tokens (both compute in float32 over the stored
-weights, so they agree to float32 summation-order noise). One step requests no logits, which
-runs the kernel without its output-matrix phase."""
+sequence (the default path) of a second context on the same tokens (both compute in float32
+over the stored weights, so they agree to float32 summation-order noise). One step requests no
+logits, which runs the kernel without its output-matrix phase."""
 import numpy as np
 import pytest
 
@@ -32,8 +32,8 @@ def test_step_kernel_matches_oracle_and_per_op_kernels():
                                 weight_seed=3300, prompt_seed=4300)
     G.device_model.cache_clear()
     G.oracle_weights.cache_clear()
-    ctx = G.library_ctx(KEY)
-    ref = G.library_ctx(KEY, per_op_kernels=True)
+    ctx = G.library_ctx(KEY, fused_step=True)
+    ref = G.library_ctx(KEY)
     ora = G.oracle_ctx(KEY)
     toks = G.prompts(KEY)[0]
     for c in (ctx, ref):

@@ -17,7 +17,7 @@ LIB_PATH = os.path.join(_PKG, "libllm.so")
 
 F32, F16, BF16, Q8_0 = 0, 1, 2, 8
 CTX_HOST_ONLY = 1
-CTX_PER_OP_KERNELS = 2
+CTX_FUSED_STEP = 2
 
 
 class HParams(C.Structure):
@@ -140,7 +140,7 @@ class Context:
 
     def __init__(self, hp, n_ctx: int, n_seq_max: int = 1, type_k: int = F16, type_v: int = F16,
                  n_batch: int = 2048, n_ubatch: int = 512, stream: Optional[int] = None,
-                 host_only: bool = False, per_op_kernels: bool = False):
+                 host_only: bool = False, fused_step: bool = False):
         L = lib()
         self._hp = HParams(hp.n_layer, hp.n_embd, hp.n_head, hp.n_head_kv, hp.head_dim, hp.n_ff,
                            hp.n_vocab, hp.rope_freq_base, hp.rms_eps, getattr(hp, "rope_type", 0))
@@ -148,7 +148,7 @@ class Context:
         cp.n_ctx, cp.n_seq_max, cp.n_batch, cp.n_ubatch = n_ctx, n_seq_max, n_batch, n_ubatch
         cp.type_k, cp.type_v = type_k, type_v
         cp.stream = stream
-        cp.flags = (CTX_HOST_ONLY if host_only else 0) | (CTX_PER_OP_KERNELS if per_op_kernels else 0)
+        cp.flags = (CTX_HOST_ONLY if host_only else 0) | (CTX_FUSED_STEP if fused_step else 0)
         self.n_vocab = hp.n_vocab
         self.ptr = L.llm_ctx_init(C.byref(self._hp), C.byref(cp))
         if not self.ptr:

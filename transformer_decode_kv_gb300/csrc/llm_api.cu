@@ -168,7 +168,7 @@ struct llm_ctx {
     // decode-step graphs, per (tokens, outputs, output row, tile shape, timing) key
     bool use_graphs = true, use_pdl = true, use_bulk = true;
     // one-token ubatches as one persistent kernel (decode_step.cu)
-    bool use_step = true, step_ok = false;
+    bool use_step = false, step_ok = false;
     StepLayer* d_step_layers = nullptr;
     uint32_t* d_counters = nullptr;     // its grid-wide phase counters [1 + 5 n_layer]
     int32_t* d_abort = nullptr;
@@ -700,7 +700,7 @@ llm_ctx* llm_ctx_init(const llm_hparams* hp, const llm_cparams* cp) {
     c->type_k = cp->type_k;
     c->type_v = cp->type_v;
     c->host_only = (cp->flags & LLM_CTX_HOST_ONLY) != 0;
-    c->use_step = (cp->flags & LLM_CTX_PER_OP_KERNELS) == 0;
+    c->use_step = (cp->flags & LLM_CTX_FUSED_STEP) != 0;
     c->cells = KvCells(c->n_ctx, c->n_seq_max);
     c->layers.resize(h.n_layer);
     if (c->host_only) return c;
