@@ -1,0 +1,356 @@
+// Prefill attention on tensor cores ([P2] "llama.cpp Architecture", Example 4 FLASH_ATTN_EXT;
+// Example 11 for the unfused meaning: scores Q K^T with the KQ mask, softmax, times V).
+//
+// The same work decomposition as the CUDA-core kernel (kernels_attention.cu): a block takes one
+// work item (a query tile of up to 16 tokens of one cell list, and a slice of that list) for one
+// KV head. The tile's 16 tokens x 4 query heads of the group are 64 rows; warp w owns rows
+// 16w .. 16w+15 (row r: token r / 4, head r % 4). Per 64-cell tile of the slice the block gathers
+// the cells' K and V rows (F16, cp.async through L2, double-buffered) and each warp runs
+//   S = Q K^T       mma.m16n8k16 f16 x f16 -> f32 (Q as two f16 terms: hi + lo of the float32)
+//   mask, online softmax in base 2 (log2 e / sqrt(hd) folded into Q)
+//   O += P V        P as two f16 terms, V f16
+// so every product is float32-accurate to about 2^-22 and accumulates in float32. A cell is
+// visible to a row iff cell.pos <= token.pos (the list already holds only the sequence's cells).
+// Partial states (o, m, l) and the ticket merge are shared with the CUDA-core kernel.
+//
+// mma.sync is enough here: a 512-token ubatch of the 8B shape has 2.1 GFLOP of attention per
+// layer, 1% of its matrix work, and this kernel moves it off the CUDA cores.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include <climits>
+#include <cmath>
+#include <cstdint>
+
+#include "attn_common.cuh"
+#include "kernels.h"
+
+namespace llm {
+
+namespace {
+
+using namespace attn;
+
+constexpr int kWarps = 4;
+constexpr int kTC = 64;                    // cells per tile
+constexpr int kG = 4;                      // query heads per KV head
+constexpr int kTQ = 16;                    // tokens per query tile
+constexpr int kRows = kTQ * kG;            // 64 rows: one m16 fragment row block per warp
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
+    const __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&h);
+}
+// x = hi + lo with hi, lo f16 (lo the rounding error of hi)
+__device__ __forceinline__ void split_h2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+    const __half2 h = __floats2half2_rn(x0, x1);
+    const float2 hf = __half22float2(h);
+    hi = *reinterpret_cast<const uint32_t*>(&h);
+    lo = pack_h2(x0 - hf.x, x1 - hf.y);
+}
+__device__ __forceinline__ void mma16816(float* d, const uint32_t* a, uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
+}
+
+template <int HD>
+struct MmaSmem {
+    static constexpr int RS = HD + 8;                       // padded row (halves): no bank conflicts
+    static constexpr size_t tile_bytes = (size_t)kTC * RS * 2;
+    static constexpr size_t q_bytes = (size_t)kRows * RS * 2;      // one f16 term of the Q tile
+    static constexpr size_t bytes = 4 * tile_bytes + 2 * q_bytes + 2 * kTC * 4 + kRows * 4 + 16;
+};
+
+// Issue the gathers of tile [cb, cb + kTC) of the list into buffer b; cell positions to cpos.
+template <int HD>
+__device__ __forceinline__ void gather_tile(const AttnArgs& a, const __half* K, const __half* V, int base,
+                                            int cb, int c1, __half* ks, __half* vs, int* cpos) {
+    constexpr int RS = MmaSmem<HD>::RS, VPR = HD / 8;
+    for (int v = threadIdx.x; v < kTC * VPR; v += kWarps * 32) {
+        const int c = v / VPR, j = v % VPR;
+        int cell = -1;
+        if (cb + c < c1) {
+            cell = a.list_cells[base + cb + c];
+            if (cell >= a.n_ctx) cell = -1;
+        }
+        __half* dk = ks + c * RS + j * 8;
+        __half* dv = vs + c * RS + j * 8;
+        if (cell >= 0) {
+            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dk)),
+                         "l"(K + (int64_t)cell * HD + j * 8) : "memory");
+            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dv)),
+                         "l"(V + (int64_t)cell * HD + j * 8) : "memory");
+        } else {
+            *reinterpret_cast<uint4*>(dk) = make_uint4(0u, 0u, 0u, 0u);
+            *reinterpret_cast<uint4*>(dv) = make_uint4(0u, 0u, 0u, 0u);
+        }
+        if (j == 0) cpos[c] = cell >= 0 ? a.list_pos[base + cb + c] : INT_MAX;
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+}  // namespace
+
+template <int HD>
+__global__ void __launch_bounds__(kWarps * 32, 2) attn_mma_kernel(AttnArgs a, float scale_log2) {
+    using SM = MmaSmem<HD>;
+    constexpr int RS = SM::RS, KC = HD / 16, NC = HD / 8;
+    extern __shared__ __align__(16) uint8_t smem[];
+    __half* kbuf[2] = {reinterpret_cast<__half*>(smem), reinterpret_cast<__half*>(smem + SM::tile_bytes)};
+    __half* vbuf[2] = {reinterpret_cast<__half*>(smem + 2 * SM::tile_bytes),
+                       reinterpret_cast<__half*>(smem + 3 * SM::tile_bytes)};
+    __half* qhs = reinterpret_cast<__half*>(smem + 4 * SM::tile_bytes);  // Q tile, hi term
+    __half* qls = reinterpret_cast<__half*>(smem + 4 * SM::tile_bytes + SM::q_bytes);   // lo term
+    int* cposb = reinterpret_cast<int*>(smem + 4 * SM::tile_bytes + 2 * SM::q_bytes);   // [2][kTC]
+    int* rpos = cposb + 2 * kTC;                                          // [kRows]
+    int* flag = rpos + kRows;
+
+    const int wi = blockIdx.x, kvh = blockIdx.y;
+    if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;");
+    const int n_work = a.hdr[0];
+    const int4 wd = a.wi_desc[wi];
+    if (wi >= n_work) return;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane >> 2, t4 = lane & 3;
+    const int4 td0 = a.tile_desc[2 * wd.x];
+    const int4 td1 = a.tile_desc[2 * wd.x + 1];
+    const int nq = td0.z, s0 = td0.y, c0 = wd.y, c1 = wd.z, base = td1.y;
+    const __half* K = static_cast<const __half*>(a.kc) + (int64_t)kvh * a.n_ctx * HD;
+    const __half* V = static_cast<const __half*>(a.vc) + (int64_t)kvh * a.n_ctx * HD;
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+
+    gather_tile<HD>(a, K, V, base, c0, c1, kbuf[0], vbuf[0], cposb);
+    for (int r = threadIdx.x; r < kRows; r += kWarps * 32) {
+        const int j = r / kG;
+        rpos[r] = j < nq ? a.tok_pos[a.perm[s0 + j]] : -1;
+    }
+
+    // the Q tile as two f16 terms (hi + lo of the float32, log2 e / sqrt(hd) folded in)
+    for (int v = threadIdx.x; v < kRows * HD / 2; v += kWarps * 32) {
+        const int r = v / (HD / 2), col = (v % (HD / 2)) * 2;
+        const int j = r / kG;
+        float2 x = make_float2(0.f, 0.f);
+        if (j < nq) x = *reinterpret_cast<const float2*>(a.q + (int64_t)a.perm[s0 + j] * a.ldq + (kvh * kG + r % kG) * HD + col);
+        uint32_t hi, lo;
+        split_h2(x.x * scale_log2, x.y * scale_log2, hi, lo);
+        *reinterpret_cast<uint32_t*>(qhs + r * RS + col) = hi;
+        *reinterpret_cast<uint32_t*>(qls + r * RS + col) = lo;
+    }
+    const int r0 = warp * 16 + g, r1 = r0 + 8;
+    // A-fragment addresses of this warp's rows: (rows 0-7 | 8-15) x (k 0-7 | 8-15)
+    const int qrow = warp * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
+    const int qcol = (lane >> 4) << 3;
+
+    float o[NC][4];
+#pragma unroll
+    for (int n = 0; n < NC; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+    float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
+
+    int buf = 0;
+    for (int cb = c0; cb < c1; cb += kTC, buf ^= 1) {
+        // the next tile's gathers go out before this tile is used
+        if (cb + kTC < c1) {
+            __syncthreads();       // the other buffer's last readers are done
+            gather_tile<HD>(a, K, V, base, cb + kTC, c1, kbuf[buf ^ 1], vbuf[buf ^ 1], cposb + (buf ^ 1) * kTC);
+            asm volatile("cp.async.wait_group 1;" ::: "memory");
+        } else {
+            asm volatile("cp.async.wait_group 0;" ::: "memory");
+        }
+        __syncthreads();
+        const __half* ks = kbuf[buf];
+        const __half* vs = vbuf[buf];
+        const int* cpos = cposb + buf * kTC;
+
+        // S = Q K^T over the tile's 64 cells: 8 fragments of 8 cells
+        float s[8][4];
+#pragma unroll
+        for (int n = 0; n < 8; ++n) s[n][0] = s[n][1] = s[n][2] = s[n][3] = 0.f;
+#pragma unroll
+        for (int kc = 0; kc < KC; ++kc) {
+            uint32_t qh[4], ql[4];
+            ldsm_x4(smem_addr(qhs + qrow * RS + kc * 16 + qcol), qh[0], qh[1], qh[2], qh[3]);
+            ldsm_x4(smem_addr(qls + qrow * RS + kc * 16 + qcol), ql[0], ql[1], ql[2], ql[3]);
+#pragma unroll
+            for (int n2 = 0; n2 < 4; ++n2) {
+                // matrices: (cells 16 n2 + 0..7, dims 16 kc + 0..7), (same cells, +8 dims),
+                //           (cells 16 n2 + 8..15, dims 16 kc), (cells +8, dims +8)
+                const int cell = 16 * n2 + (lane & 7) + ((lane >> 4) << 3);
+                const int dim = 16 * kc + (((lane >> 3) & 1) << 3);
+                uint32_t b0, b1, b2, b3;
+                ldsm_x4(smem_addr(ks + cell * RS + dim), b0, b1, b2, b3);
+                mma16816(s[2 * n2], qh, b0, b1);
+                mma16816(s[2 * n2], ql, b0, b1);
+                mma16816(s[2 * n2 + 1], qh, b2, b3);
+                mma16816(s[2 * n2 + 1], ql, b2, b3);
+            }
+        }
+        // mask and online softmax (rows r0, r1; this thread's columns 2 t4, 2 t4 + 1 of each
+        // fragment; the row's other columns live in the same quad)
+        const int p0 = rpos[r0], p1 = rpos[r1];
+        float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+        for (int n = 0; n < 8; ++n) {
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int cp = cpos[8 * n + 2 * t4 + e];
+                if (cp > p0) s[n][e] = -INFINITY;
+                if (cp > p1) s[n][2 + e] = -INFINITY;
+                mx0 = fmaxf(mx0, s[n][e]);
+                mx1 = fmaxf(mx1, s[n][2 + e]);
+            }
+        }
+#pragma unroll
+        for (int off = 1; off <= 2; off <<= 1) {
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+        }
+        const float mn0 = fmaxf(m[0], mx0), mn1 = fmaxf(m[1], mx1);
+        const float cr0 = mn0 == -INFINITY ? 1.f : exp2f(m[0] - mn0);
+        const float cr1 = mn1 == -INFINITY ? 1.f : exp2f(m[1] - mn1);
+        m[0] = mn0;
+        m[1] = mn1;
+        float ls0 = 0.f, ls1 = 0.f;
+#pragma unroll
+        for (int n = 0; n < 8; ++n) {
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                s[n][e] = mn0 == -INFINITY ? 0.f : exp2f(s[n][e] - mn0);
+                s[n][2 + e] = mn1 == -INFINITY ? 0.f : exp2f(s[n][2 + e] - mn1);
+                ls0 += s[n][e];
+                ls1 += s[n][2 + e];
+            }
+        }
+        l[0] = l[0] * cr0 + ls0;
+        l[1] = l[1] * cr1 + ls1;
+#pragma unroll
+        for (int n = 0; n < NC; ++n) {
+            o[n][0] *= cr0; o[n][1] *= cr0;
+            o[n][2] *= cr1; o[n][3] *= cr1;
+        }
+        // O += P V: P's accumulator layout is the A layout of the next MMA (16 cells per step)
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+            uint32_t ph[4], pl[4];
+            split_h2(s[2 * kk][0], s[2 * kk][1], ph[0], pl[0]);
+            split_h2(s[2 * kk][2], s[2 * kk][3], ph[1], pl[1]);
+            split_h2(s[2 * kk + 1][0], s[2 * kk + 1][1], ph[2], pl[2]);
+            split_h2(s[2 * kk + 1][2], s[2 * kk + 1][3], ph[3], pl[3]);
+#pragma unroll
+            for (int n2 = 0; n2 < NC / 2; ++n2) {
+                // matrices (transposed): (cells 16 kk + 0..7, dims 16 n2 + 0..7), (cells +8, same
+                // dims), (cells 16 kk, dims +8), (cells +8, dims +8)
+                const int cell = 16 * kk + (lane & 7) + (((lane >> 3) & 1) << 3);
+                const int dim = 16 * n2 + ((lane >> 4) << 3);
+                uint32_t b0, b1, b2, b3;
+                ldsm_x4_t(smem_addr(vs + cell * RS + dim), b0, b1, b2, b3);
+                mma16816(o[2 * n2], ph, b0, b1);
+                mma16816(o[2 * n2], pl, b0, b1);
+                mma16816(o[2 * n2 + 1], ph, b2, b3);
+                mma16816(o[2 * n2 + 1], pl, b2, b3);
+            }
+        }
+    }
+#pragma unroll
+    for (int off = 1; off <= 2; off <<= 1) {
+        l[0] += __shfl_xor_sync(0xffffffffu, l[0], off);
+        l[1] += __shfl_xor_sync(0xffffffffu, l[1], off);
+    }
+
+    const int w0 = td0.w, w1 = td1.x;
+    const int rows[2] = {r0, r1};
+    if (w1 - w0 == 1) {                            // a single work item: normalise directly
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int r = rows[h];
+            if (r / kG >= nq) continue;
+            const float inv = l[h] > 0.f ? 1.f / l[h] : 0.f;
+            const int64_t ob = (int64_t)a.perm[s0 + r / kG] * a.ldo + (kvh * kG + r % kG) * HD;
+#pragma unroll
+            for (int n = 0; n < NC; ++n) {
+                store_out(a, ob + 8 * n + 2 * t4, o[n][2 * h] * inv);
+                store_out(a, ob + 8 * n + 2 * t4 + 1, o[n][2 * h + 1] * inv);
+            }
+        }
+        return;
+    }
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const int r = rows[h];
+        if (r / kG >= nq) continue;
+        const int64_t row = (int64_t)(wd.w + r) * a.Hkv + kvh;
+        if (t4 == 0) {
+            a.part_m[row] = m[h];
+            a.part_l[row] = l[h];
+        }
+#pragma unroll
+        for (int n = 0; n < NC; ++n)
+            *reinterpret_cast<float2*>(a.part_o + row * HD + 8 * n + 2 * t4) = make_float2(o[n][2 * h], o[n][2 * h + 1]);
+    }
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        int* ticket = a.tickets + wd.x * a.Hkv + kvh;
+        const int done = atomicAdd(ticket, 1) + 1;
+        const bool last = done == w1 - w0;
+        if (last) *ticket = 0;
+        *flag = last ? 1 : 0;
+    }
+    __syncthreads();
+    if (!*flag) return;
+    __threadfence();
+    merge_tile<HD, kG>(a, kvh, s0, nq, w0, w1, reinterpret_cast<float*>(smem), 4 * SM::tile_bytes / 4);
+}
+
+template <int HD>
+bool launch_attention_mma_hd(const AttnArgs& a, cudaStream_t st) {
+    const float scale_log2 = (float)(1.4426950408889634 / sqrt((double)HD));
+    constexpr size_t smem = MmaSmem<HD>::bytes;
+    auto k = attn_mma_kernel<HD>;
+    static bool attr = false;
+    if (!attr) {
+        if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+            return false;
+        attr = true;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(a.n_work, a.Hkv);
+    cfg.blockDim = dim3(kWarps * 32);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr_l[1];
+    attr_l[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr_l[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr_l;
+    cfg.numAttrs = a.pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, k, a, scale_log2) == cudaSuccess;
+}
+
+bool attention_mma_ok(const AttnArgs& a) {
+    return a.kv_type == W_F16 && a.H == kG * a.Hkv && (a.hd == 32 || a.hd == 64 || a.hd == 128);
+}
+
+bool launch_attention_mma(const AttnArgs& a, cudaStream_t st) {
+    switch (a.hd) {
+        case 32: return launch_attention_mma_hd<32>(a, st);
+        case 64: return launch_attention_mma_hd<64>(a, st);
+        case 128: return launch_attention_mma_hd<128>(a, st);
+    }
+    return false;
+}
+
+}  // namespace llm

@@ -108,5 +108,9 @@ struct AttnArgs {
 // split-K partial softmax per work item, then a combine per tile ([P2] Example 4 FLASH_ATTN_EXT;
 // Example 11 for the unfused meaning). Scale 1/sqrt(hd).
 bool launch_attention(const AttnArgs& a, cudaStream_t st);
+// The prefill tiles (16 tokens x 4 query heads) on tensor cores (attn_mma.cu): F16 KV, 4 query
+// heads per KV head, head_dim 32, 64 or 128. launch_attention uses it when it applies.
+bool attention_mma_ok(const AttnArgs& a);
+bool launch_attention_mma(const AttnArgs& a, cudaStream_t st);
 
 }  // namespace llm

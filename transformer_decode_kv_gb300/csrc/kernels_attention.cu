@@ -18,11 +18,14 @@
 #include <climits>
 #include <cmath>
 
+#include "attn_common.cuh"
 #include "kernels.h"
 
 namespace llm {
 
 namespace {
+
+using namespace attn;
 
 constexpr int kAttnWarps = 4;
 constexpr int kBC = 32;                  // cells per shared-memory tile (one per lane)
@@ -44,109 +47,6 @@ struct AttnSmem {
     // the merge reuses the q/k/v area
     static constexpr size_t merge_floats = q_floats + k_floats + v_floats;
 };
-
-__device__ __forceinline__ void store_out(const AttnArgs& a, int64_t oi, float v) {
-    if (a.out_b) {
-        const __nv_bfloat16 hi = __float2bfloat16_rn(v);
-        static_cast<__nv_bfloat16*>(a.out_b)[oi] = hi;
-        if (a.out_b_lo)
-            static_cast<__nv_bfloat16*>(a.out_b_lo)[oi] = __float2bfloat16_rn(v - __bfloat162float(hi));
-    } else {
-        a.out[oi] = v;
-    }
-}
-
-// Merge the partials of work items [w0, w1) of one tile and KV head into the output rows.
-template <int HD, int G>
-__device__ void merge_tile(const AttnArgs& a, int kvh, int s0, int nq, int w0, int w1,
-                           float* scratch, size_t scratch_floats) {
-    const int R = nq * G, NW = w1 - w0;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    if ((size_t)R * NW + NW <= scratch_floats) {
-        float* wgt = scratch;                                  // [R][NW]
-        int* roff = reinterpret_cast<int*>(scratch + (size_t)R * NW);
-        __syncthreads();
-        for (int w = threadIdx.x; w < NW; w += blockDim.x) roff[w] = a.wi_desc[w0 + w].w;
-        __syncthreads();
-        for (int r = warp; r < R; r += blockDim.x / 32) {
-            float M = -INFINITY;
-            for (int w = lane; w < NW; w += 32) {
-                const float mw = a.part_m[(int64_t)(roff[w] + r) * a.Hkv + kvh];
-                wgt[r * NW + w] = mw;
-                M = fmaxf(M, mw);
-            }
-            for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-            float L = 0.f;
-            for (int w = lane; w < NW; w += 32) {
-                const float mw = wgt[r * NW + w];
-                const float f = (M == -INFINITY || mw == -INFINITY) ? 0.f : exp2f(mw - M);
-                L += f * a.part_l[(int64_t)(roff[w] + r) * a.Hkv + kvh];
-                wgt[r * NW + w] = f;
-            }
-            for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
-            const float inv = L > 0.f ? 1.f / L : 0.f;
-            for (int w = lane; w < NW; w += 32) wgt[r * NW + w] *= inv;
-        }
-        __syncthreads();
-        // each thread owns outputs idx = threadIdx.x + j * blockDim.x; the partial rows of eight
-        // work items are loaded for all of them before any is used
-        constexpr int kOut = 4;
-        for (int base_idx = 0; base_idx < R * HD; base_idx += kOut * (int)blockDim.x) {
-            float O[kOut];
-            int rr[kOut], dd[kOut];
-            bool live[kOut];
-#pragma unroll
-            for (int j = 0; j < kOut; ++j) {
-                const int idx = base_idx + j * blockDim.x + threadIdx.x;
-                live[j] = idx < R * HD;
-                rr[j] = live[j] ? idx / HD : 0;
-                dd[j] = live[j] ? idx % HD : 0;
-                O[j] = 0.f;
-            }
-            for (int w0b = 0; w0b < NW; w0b += 8) {
-                float pv[8][kOut];
-#pragma unroll
-                for (int u = 0; u < 8; ++u)
-#pragma unroll
-                    for (int j = 0; j < kOut; ++j)
-                        pv[u][j] = (w0b + u < NW && live[j])
-                            ? a.part_o[((int64_t)(roff[w0b + u] + rr[j]) * a.Hkv + kvh) * HD + dd[j]]
-                            : 0.f;
-#pragma unroll
-                for (int u = 0; u < 8; ++u)
-#pragma unroll
-                    for (int j = 0; j < kOut; ++j)
-                        if (w0b + u < NW) O[j] = fmaf(wgt[rr[j] * NW + w0b + u], pv[u][j], O[j]);
-            }
-#pragma unroll
-            for (int j = 0; j < kOut; ++j) {
-                if (!live[j]) continue;
-                const int t = a.perm[s0 + rr[j] / G];
-                store_out(a, (int64_t)t * a.ldo + (kvh * G + rr[j] % G) * HD + dd[j], O[j]);
-            }
-        }
-        return;
-    }
-    for (int idx = threadIdx.x; idx < R * HD; idx += blockDim.x) {
-        const int r = idx / HD, d = idx % HD;
-        float M = -INFINITY;
-        for (int w = w0; w < w1; ++w)
-            M = fmaxf(M, a.part_m[(int64_t)(a.wi_desc[w].w + r) * a.Hkv + kvh]);
-        float L = 0.f, O = 0.f;
-        if (M != -INFINITY) {
-            for (int w = w0; w < w1; ++w) {
-                const int64_t row = (int64_t)(a.wi_desc[w].w + r) * a.Hkv + kvh;
-                const float mw = a.part_m[row];
-                if (mw == -INFINITY) continue;
-                const float f = exp2f(mw - M);
-                L += f * a.part_l[row];
-                O += f * a.part_o[row * HD + d];
-            }
-        }
-        const int t = a.perm[s0 + r / G];
-        store_out(a, (int64_t)t * a.ldo + (kvh * G + r % G) * HD + d, L > 0.f ? O / L : 0.f);
-    }
-}
 
 template <int HD, int TQ, int G, typename KT>
 __global__ void __launch_bounds__(kAttnWarps * 32)
@@ -554,6 +454,7 @@ bool launch_tq(const AttnArgs& a, cudaStream_t st) {
 template <int HD, int G>
 bool launch_hd_g(const AttnArgs& a, cudaStream_t st) {
     if (a.max_nq <= 1) return a.slot ? launch_step<HD, G>(a, st) : launch_tq<HD, 1, G>(a, st);
+    if (attention_mma_ok(a)) return launch_attention_mma(a, st);
     return launch_tq<HD, kAttnTileQ, G>(a, st);
 }
 
