@@ -72,21 +72,18 @@ struct MmaSmem {
     static constexpr int RS = HD + 8;                       // padded row (halves): no bank conflicts
     static constexpr size_t tile_bytes = (size_t)kTC * RS * 2;
     static constexpr size_t q_bytes = (size_t)kRows * RS * 2;      // one f16 term of the Q tile
-    static constexpr size_t bytes = 4 * tile_bytes + 2 * q_bytes + 2 * kTC * 4 + kRows * 4 + 16;
+    static constexpr size_t bytes = 4 * tile_bytes + 2 * q_bytes + 4 * kTC * 4 + 8 * 4 + 2 * kRows * 4 + 16;
 };
 
-// Issue the gathers of tile [cb, cb + kTC) of the list into buffer b; cell positions to cpos.
+// Issue the gathers of one tile into buffer (ks, vs): cell indices from shared memory (ccell,
+// -1 = none), zeros for missing cells.
 template <int HD>
-__device__ __forceinline__ void gather_tile(const AttnArgs& a, const __half* K, const __half* V, int base,
-                                            int cb, int c1, __half* ks, __half* vs, int* cpos) {
+__device__ __forceinline__ void gather_tile(const __half* K, const __half* V, const int* ccell,
+                                            __half* ks, __half* vs) {
     constexpr int RS = MmaSmem<HD>::RS, VPR = HD / 8;
     for (int v = threadIdx.x; v < kTC * VPR; v += kWarps * 32) {
         const int c = v / VPR, j = v % VPR;
-        int cell = -1;
-        if (cb + c < c1) {
-            cell = a.list_cells[base + cb + c];
-            if (cell >= a.n_ctx) cell = -1;
-        }
+        const int cell = ccell[c];
         __half* dk = ks + c * RS + j * 8;
         __half* dv = vs + c * RS + j * 8;
         if (cell >= 0) {
@@ -98,9 +95,30 @@ __device__ __forceinline__ void gather_tile(const AttnArgs& a, const __half* K, 
             *reinterpret_cast<uint4*>(dk) = make_uint4(0u, 0u, 0u, 0u);
             *reinterpret_cast<uint4*>(dv) = make_uint4(0u, 0u, 0u, 0u);
         }
-        if (j == 0) cpos[c] = cell >= 0 ? a.list_pos[base + cb + c] : INT_MAX;
     }
     asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+// Cell index and position of list entry cb + threadIdx.x (threads 0 .. kTC-1; -1 / INT_MAX past
+// the slice's end).
+__device__ __forceinline__ void load_index(const AttnArgs& a, int base, int cb, int c1, int& cell, int& pos) {
+    cell = -1;
+    pos = INT_MAX;
+    const int ci = cb + (int)threadIdx.x;
+    if (threadIdx.x < kTC && ci < c1) {
+        const int cc = a.list_cells[base + ci];
+        if (cc >= 0 && cc < a.n_ctx) { cell = cc; pos = a.list_pos[base + ci]; }
+    }
+}
+// Store a tile's indices (threads 0 .. kTC-1) and each warp's minimum position.
+__device__ __forceinline__ void store_index(int cell, int pos, int* ccell, int* cpos, int* cmin) {
+    if (threadIdx.x < kTC) {
+        ccell[threadIdx.x] = cell;
+        cpos[threadIdx.x] = pos;
+        int mn = pos;
+        for (int off = 16; off > 0; off >>= 1) mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, off));
+        if ((threadIdx.x & 31) == 0) cmin[threadIdx.x >> 5] = mn;
+    }
 }
 
 }  // namespace
@@ -116,8 +134,12 @@ __global__ void __launch_bounds__(kWarps * 32, 2) attn_mma_kernel(AttnArgs a, fl
     __half* qhs = reinterpret_cast<__half*>(smem + 4 * SM::tile_bytes);  // Q tile, hi term
     __half* qls = reinterpret_cast<__half*>(smem + 4 * SM::tile_bytes + SM::q_bytes);   // lo term
     int* cposb = reinterpret_cast<int*>(smem + 4 * SM::tile_bytes + 2 * SM::q_bytes);   // [2][kTC]
-    int* rpos = cposb + 2 * kTC;                                          // [kRows]
-    int* flag = rpos + kRows;
+    int* ccellb = cposb + 2 * kTC;                                        // [2][kTC]
+    int* cminb = ccellb + 2 * kTC;                                        // [2][2] per warp
+    int* rmax = cminb + 4;                                                // largest row position
+    int* rpos = cminb + 8;                                                // [kRows]
+    int* rtok = rpos + kRows;                                             // [kRows] token row of q
+    int* flag = rtok + kRows;
 
     const int wi = blockIdx.x, kvh = blockIdx.y;
     if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;");
@@ -133,22 +155,49 @@ __global__ void __launch_bounds__(kWarps * 32, 2) attn_mma_kernel(AttnArgs a, fl
     const __half* V = static_cast<const __half*>(a.vc) + (int64_t)kvh * a.n_ctx * HD;
     asm volatile("griddepcontrol.wait;" ::: "memory");
 
-    gather_tile<HD>(a, K, V, base, c0, c1, kbuf[0], vbuf[0], cposb);
+    // tile 0: indices, then its gathers; tile 1's indices are loaded while tile 0 is used
+    int ncell, npos;
+    load_index(a, base, c0, c1, ncell, npos);
+    store_index(ncell, npos, ccellb, cposb, cminb);
     for (int r = threadIdx.x; r < kRows; r += kWarps * 32) {
         const int j = r / kG;
-        rpos[r] = j < nq ? a.tok_pos[a.perm[s0 + j]] : -1;
+        const int t = j < nq ? a.perm[s0 + j] : -1;
+        rtok[r] = t;
+        rpos[r] = t >= 0 ? a.tok_pos[t] : -1;
+    }
+    __syncthreads();
+    gather_tile<HD>(K, V, ccellb, kbuf[0], vbuf[0]);
+    load_index(a, base, c0 + kTC, c1, ncell, npos);
+    if (threadIdx.x < 32) {
+        int mx = -1;
+        for (int r = threadIdx.x; r < kRows; r += 32) mx = max(mx, rpos[r]);
+        for (int off = 16; off > 0; off >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+        if (threadIdx.x == 0) *rmax = mx;
     }
 
-    // the Q tile as two f16 terms (hi + lo of the float32, log2 e / sqrt(hd) folded in)
-    for (int v = threadIdx.x; v < kRows * HD / 2; v += kWarps * 32) {
-        const int r = v / (HD / 2), col = (v % (HD / 2)) * 2;
-        const int j = r / kG;
-        float2 x = make_float2(0.f, 0.f);
-        if (j < nq) x = *reinterpret_cast<const float2*>(a.q + (int64_t)a.perm[s0 + j] * a.ldq + (kvh * kG + r % kG) * HD + col);
-        uint32_t hi, lo;
-        split_h2(x.x * scale_log2, x.y * scale_log2, hi, lo);
-        *reinterpret_cast<uint32_t*>(qhs + r * RS + col) = hi;
-        *reinterpret_cast<uint32_t*>(qls + r * RS + col) = lo;
+    // the Q tile as two f16 terms (hi + lo of the float32, log2 e / sqrt(hd) folded in); the
+    // loads of a batch are all issued before any is used
+    constexpr int QV = kRows * HD / 2 / (kWarps * 32);      // float2 per thread
+#pragma unroll
+    for (int b = 0; b < QV; b += 8) {
+        float2 x[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int v = threadIdx.x + (b + i) * kWarps * 32;
+            const int r = v / (HD / 2), col = (v % (HD / 2)) * 2;
+            const int t = rtok[r];
+            x[i] = t >= 0 ? *reinterpret_cast<const float2*>(a.q + (int64_t)t * a.ldq + (kvh * kG + r % kG) * HD + col)
+                          : make_float2(0.f, 0.f);
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int v = threadIdx.x + (b + i) * kWarps * 32;
+            const int r = v / (HD / 2), col = (v % (HD / 2)) * 2;
+            uint32_t hi, lo;
+            split_h2(x[i].x * scale_log2, x[i].y * scale_log2, hi, lo);
+            *reinterpret_cast<uint32_t*>(qhs + r * RS + col) = hi;
+            *reinterpret_cast<uint32_t*>(qls + r * RS + col) = lo;
+        }
     }
     const int r0 = warp * 16 + g, r1 = r0 + 8;
     // A-fragment addresses of this warp's rows: (rows 0-7 | 8-15) x (k 0-7 | 8-15)
@@ -162,10 +211,15 @@ __global__ void __launch_bounds__(kWarps * 32, 2) attn_mma_kernel(AttnArgs a, fl
 
     int buf = 0;
     for (int cb = c0; cb < c1; cb += kTC, buf ^= 1) {
-        // the next tile's gathers go out before this tile is used
-        if (cb + kTC < c1) {
-            __syncthreads();       // the other buffer's last readers are done
-            gather_tile<HD>(a, K, V, base, cb + kTC, c1, kbuf[buf ^ 1], vbuf[buf ^ 1], cposb + (buf ^ 1) * kTC);
+        // the next tile's gathers go out before this tile is used (its indices were loaded during
+        // the previous tile); the indices of the one after are loaded now
+        const bool more = cb + kTC < c1;
+        __syncthreads();           // the other buffer's last readers are done
+        if (more) {
+            store_index(ncell, npos, ccellb + (buf ^ 1) * kTC, cposb + (buf ^ 1) * kTC, cminb + (buf ^ 1) * 2);
+            __syncthreads();
+            gather_tile<HD>(K, V, ccellb + (buf ^ 1) * kTC, kbuf[buf ^ 1], vbuf[buf ^ 1]);
+            load_index(a, base, cb + 2 * kTC, c1, ncell, npos);
             asm volatile("cp.async.wait_group 1;" ::: "memory");
         } else {
             asm volatile("cp.async.wait_group 0;" ::: "memory");
@@ -174,6 +228,8 @@ __global__ void __launch_bounds__(kWarps * 32, 2) attn_mma_kernel(AttnArgs a, fl
         const __half* ks = kbuf[buf];
         const __half* vs = vbuf[buf];
         const int* cpos = cposb + buf * kTC;
+        // a tile no row of this block may see (causal prefill) is skipped
+        if (min(cminb[buf * 2], cminb[buf * 2 + 1]) > *rmax) continue;
 
         // S = Q K^T over the tile's 64 cells: 8 fragments of 8 cells
         float s[8][4];
@@ -184,18 +240,26 @@ __global__ void __launch_bounds__(kWarps * 32, 2) attn_mma_kernel(AttnArgs a, fl
             uint32_t qh[4], ql[4];
             ldsm_x4(smem_addr(qhs + qrow * RS + kc * 16 + qcol), qh[0], qh[1], qh[2], qh[3]);
             ldsm_x4(smem_addr(qls + qrow * RS + kc * 16 + qcol), ql[0], ql[1], ql[2], ql[3]);
+            // K fragments of the 64 cells first, then the hi-term MMAs, then the lo-term ones,
+            // so no two consecutive MMAs share an accumulator
+            uint32_t kb[4][4];
 #pragma unroll
             for (int n2 = 0; n2 < 4; ++n2) {
                 // matrices: (cells 16 n2 + 0..7, dims 16 kc + 0..7), (same cells, +8 dims),
                 //           (cells 16 n2 + 8..15, dims 16 kc), (cells +8, dims +8)
                 const int cell = 16 * n2 + (lane & 7) + ((lane >> 4) << 3);
                 const int dim = 16 * kc + (((lane >> 3) & 1) << 3);
-                uint32_t b0, b1, b2, b3;
-                ldsm_x4(smem_addr(ks + cell * RS + dim), b0, b1, b2, b3);
-                mma16816(s[2 * n2], qh, b0, b1);
-                mma16816(s[2 * n2], ql, b0, b1);
-                mma16816(s[2 * n2 + 1], qh, b2, b3);
-                mma16816(s[2 * n2 + 1], ql, b2, b3);
+                ldsm_x4(smem_addr(ks + cell * RS + dim), kb[n2][0], kb[n2][1], kb[n2][2], kb[n2][3]);
+            }
+#pragma unroll
+            for (int n2 = 0; n2 < 4; ++n2) {
+                mma16816(s[2 * n2], qh, kb[n2][0], kb[n2][1]);
+                mma16816(s[2 * n2 + 1], qh, kb[n2][2], kb[n2][3]);
+            }
+#pragma unroll
+            for (int n2 = 0; n2 < 4; ++n2) {
+                mma16816(s[2 * n2], ql, kb[n2][0], kb[n2][1]);
+                mma16816(s[2 * n2 + 1], ql, kb[n2][2], kb[n2][3]);
             }
         }
         // mask and online softmax (rows r0, r1; this thread's columns 2 t4, 2 t4 + 1 of each
@@ -249,18 +313,29 @@ __global__ void __launch_bounds__(kWarps * 32, 2) attn_mma_kernel(AttnArgs a, fl
             split_h2(s[2 * kk][2], s[2 * kk][3], ph[1], pl[1]);
             split_h2(s[2 * kk + 1][0], s[2 * kk + 1][1], ph[2], pl[2]);
             split_h2(s[2 * kk + 1][2], s[2 * kk + 1][3], ph[3], pl[3]);
+            constexpr int GS = NC / 2 < 4 ? NC / 2 : 4;          // dimension blocks per group
 #pragma unroll
-            for (int n2 = 0; n2 < NC / 2; ++n2) {
-                // matrices (transposed): (cells 16 kk + 0..7, dims 16 n2 + 0..7), (cells +8, same
-                // dims), (cells 16 kk, dims +8), (cells +8, dims +8)
-                const int cell = 16 * kk + (lane & 7) + (((lane >> 3) & 1) << 3);
-                const int dim = 16 * n2 + ((lane >> 4) << 3);
-                uint32_t b0, b1, b2, b3;
-                ldsm_x4_t(smem_addr(vs + cell * RS + dim), b0, b1, b2, b3);
-                mma16816(o[2 * n2], ph, b0, b1);
-                mma16816(o[2 * n2], pl, b0, b1);
-                mma16816(o[2 * n2 + 1], ph, b2, b3);
-                mma16816(o[2 * n2 + 1], pl, b2, b3);
+            for (int h4 = 0; h4 < NC / 2; h4 += GS) {
+                uint32_t vb[GS][4];
+#pragma unroll
+                for (int i = 0; i < GS; ++i) {
+                    // matrices (transposed): (cells 16 kk + 0..7, dims 16 n2 + 0..7), (cells +8,
+                    // same dims), (cells 16 kk, dims +8), (cells +8, dims +8)
+                    const int n2 = h4 + i;
+                    const int cell = 16 * kk + (lane & 7) + (((lane >> 3) & 1) << 3);
+                    const int dim = 16 * n2 + ((lane >> 4) << 3);
+                    ldsm_x4_t(smem_addr(vs + cell * RS + dim), vb[i][0], vb[i][1], vb[i][2], vb[i][3]);
+                }
+#pragma unroll
+                for (int i = 0; i < GS; ++i) {
+                    mma16816(o[2 * (h4 + i)], ph, vb[i][0], vb[i][1]);
+                    mma16816(o[2 * (h4 + i) + 1], ph, vb[i][2], vb[i][3]);
+                }
+#pragma unroll
+                for (int i = 0; i < GS; ++i) {
+                    mma16816(o[2 * (h4 + i)], pl, vb[i][0], vb[i][1]);
+                    mma16816(o[2 * (h4 + i) + 1], pl, vb[i][2], vb[i][3]);
+                }
             }
         }
     }

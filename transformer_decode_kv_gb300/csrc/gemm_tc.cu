@@ -80,6 +80,14 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, u
         : "memory");
 }
 
+// Request a tile of the map into L2 (no shared memory, no completion): the weight tiles a few
+// k-steps ahead, so the copies that follow hit L2 instead of waiting on HBM.
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int x, int y) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y)
+                 : "memory");
+}
+
 __device__ __forceinline__ void tc_fence_before() {
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
 }
@@ -164,8 +172,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nk = K / kBK;
-    const int row0 = blockIdx.x * (EPI == GEMM_EPI_SWIGLU ? 64 : kBM);
-    const int t0 = blockIdx.y * BN;
+    // token tiles run fastest, so the blocks that share a weight tile run together and read it
+    // from HBM once (the rest hit L2)
+    const int row0 = blockIdx.y * (EPI == GEMM_EPI_SWIGLU ? 64 : kBM);
+    const int t0 = blockIdx.x * BN;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
@@ -194,8 +204,17 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     if (threadIdx.x == 0) {
         // ---- TMA producer
         int issued = 0;
+        constexpr int kAhead = 8;                  // weight tiles requested into L2 ahead
+        for (int kb = 0; kb < nk && kb < kAhead; ++kb) {
+            tma_prefetch_2d(&tmA, kb * kBK, row0);
+            if (EPI == GEMM_EPI_SWIGLU) tma_prefetch_2d(&tmA, kb * kBK, F + row0);
+        }
         for (int kb = 0; kb < nk; ++kb) {
             const int s = kb % S;
+            if (kb + kAhead < nk) {
+                tma_prefetch_2d(&tmA, (kb + kAhead) * kBK, row0);
+                if (EPI == GEMM_EPI_SWIGLU) tma_prefetch_2d(&tmA, (kb + kAhead) * kBK, F + row0);
+            }
             const uint32_t ph = (uint32_t)(kb / S) & 1u;
             if (kb >= S && !mbar_wait(&empty[s], ph ^ 1u)) { atomicOr(err, ERR_TIMEOUT); *(volatile int*)abort_flag = 1; break; }
             if (*(volatile int*)abort_flag) break;
@@ -328,7 +347,7 @@ bool launch_tc(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& b2
     }
     const int rows_per_tile = EPI == GEMM_EPI_SWIGLU ? 64 : kBM;
     const int mtiles = (EPI == GEMM_EPI_SWIGLU ? F : M) / rows_per_tile;
-    dim3 grid(mtiles, (T + BN - 1) / BN);
+    dim3 grid((T + BN - 1) / BN, mtiles);
     k<<<grid, 128, C::kSmem, st>>>(a, b, b2, K, M, T, F, Y, Y2, ldy, err);
     return cudaGetLastError() == cudaSuccess;
 }
