@@ -245,31 +245,41 @@ gemv_bulk_kernel(const GemvArgs a) {
                 const int nr = (int)(nrows - row0 < rps ? nrows - row0 : rps);
                 const uint8_t* st0 = stages + (size_t)s * SB + (warp * spw) * kSlice + lane * 16;
                 const __half* ssc = reinterpret_cast<const __half*>(sstages + (size_t)s * (SB / 16));
-                for (int i = 0; i < nr; ++i) {
-                    float part[TM];
+                // all rows of the stage at once (one token in this mapping): two independent
+                // accumulators per row, the row reductions interleaved, then lane i adds row i's
+                // sum to the shared total. A stage holds 16 KB of whole rows: 4 / SPW rows.
+                constexpr int RPS = SPW <= 4 ? 4 / SPW : 1;
+                static_assert(TM == 1, "column-stationary mapping serves one token");
+                float pa[RPS], pb[RPS];
 #pragma unroll
-                    for (int t = 0; t < TM; ++t) part[t] = 0.f;
+                for (int i = 0; i < RPS; ++i) {
+                    pa[i] = 0.f;
+                    pb[i] = 0.f;
+                    if (i < nr) {
 #pragma unroll
-                    for (int k2 = 0; k2 < kMaxSpw; ++k2) {
-                        if (k2 >= spw) break;
-                        const uint4 wv = *reinterpret_cast<const uint4*>(st0 + (size_t)i * row_bytes + k2 * kSlice);
-                        float d = 0.f;
-                        if (Q8)
-                            d = __half2float(ssc[((size_t)i * row_bytes + (warp * spw + k2) * kSlice + lane * 16) / 32]);
-                        float w[VN];
-                        unpack16<WT>(wv, d, w);
+                        for (int k2 = 0; k2 < kMaxSpw; ++k2) {
+                            const uint4 wv = *reinterpret_cast<const uint4*>(st0 + (size_t)i * row_bytes + k2 * kSlice);
+                            float d = 0.f;
+                            if (Q8)
+                                d = __half2float(ssc[((size_t)i * row_bytes + (warp * spw + k2) * kSlice + lane * 16) / 32]);
+                            float w[VN];
+                            unpack16<WT>(wv, d, w);
 #pragma unroll
-                        for (int e = 0; e < VN; ++e)
-#pragma unroll
-                            for (int t = 0; t < TM; ++t) part[t] = fmaf(w[e], xr[k2][e], part[t]);
+                            for (int e = 0; e < VN; e += 2) {
+                                pa[i] = fmaf(w[e], xr[k2][e], pa[i]);
+                                pb[i] = fmaf(w[e + 1], xr[k2][e + 1], pb[i]);
+                            }
+                        }
                     }
-#pragma unroll
-                    for (int t = 0; t < TM; ++t) {
-                        float v = part[t];
-                        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-                        if (lane == 0) atomicAdd(&acc[(rg[r].local0 + (int)(row0 + i)) * TM + t], v);
-                    }
+                    pa[i] += pb[i];
                 }
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+                    for (int i = 0; i < RPS; ++i) pa[i] += __shfl_xor_sync(0xffffffffu, pa[i], o);
+#pragma unroll
+                for (int i = 0; i < RPS; ++i)
+                    if (lane == i && i < nr) atomicAdd(&acc[rg[r].local0 + (int)(row0 + i)], pa[i]);
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&empty[s]);
             }
