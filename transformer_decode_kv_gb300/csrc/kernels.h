@@ -112,5 +112,9 @@ bool launch_attention(const AttnArgs& a, cudaStream_t st);
 // heads per KV head, head_dim 32, 64 or 128. launch_attention uses it when it applies.
 bool attention_mma_ok(const AttnArgs& a);
 bool launch_attention_mma(const AttnArgs& a, cudaStream_t st);
+// Decode steps (one token per query tile) with a 16-block cluster per (token, KV head) merging
+// the split-K partial states through distributed shared memory (attn_decode.cu).
+bool attention_decode_ok(const AttnArgs& a);
+bool launch_attention_decode(const AttnArgs& a, cudaStream_t st);
 
 }  // namespace llm

@@ -453,7 +453,10 @@ bool launch_tq(const AttnArgs& a, cudaStream_t st) {
 
 template <int HD, int G>
 bool launch_hd_g(const AttnArgs& a, cudaStream_t st) {
-    if (a.max_nq <= 1) return a.slot ? launch_step<HD, G>(a, st) : launch_tq<HD, 1, G>(a, st);
+    if (a.max_nq <= 1) {
+        if (a.slot && attention_decode_ok(a)) return launch_attention_decode(a, st);
+        return a.slot ? launch_step<HD, G>(a, st) : launch_tq<HD, 1, G>(a, st);
+    }
     if (attention_mma_ok(a)) return launch_attention_mma(a, st);
     return launch_tq<HD, kAttnTileQ, G>(a, st);
 }
