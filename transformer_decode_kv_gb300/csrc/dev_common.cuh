@@ -15,6 +15,14 @@ namespace dev {
 
 constexpr uint64_t kWaitNs = 2000000000ull;   // every wait gives up after 2 s
 
+// (a0, a1) += (w0 * x0, w1 * x1) as one paired float32 FMA (fma.rn.f32x2): each lane does two
+// independent fused multiply-adds per instruction, each rounded as fmaf.
+__device__ __forceinline__ void fma2(float& a0, float& a1, float w0, float w1, float x0, float x1) {
+    asm("{\n\t.reg .b64 acc, w, x;\n\tmov.b64 acc, {%0, %1};\n\tmov.b64 w, {%2, %3};\n\t"
+        "mov.b64 x, {%4, %5};\n\tfma.rn.f32x2 acc, w, x, acc;\n\tmov.b64 {%0, %1}, acc;\n\t}"
+        : "+f"(a0), "+f"(a1) : "f"(w0), "f"(w1), "f"(x0), "f"(x1));
+}
+
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }

@@ -265,10 +265,8 @@ gemv_bulk_kernel(const GemvArgs a) {
                             float w[VN];
                             unpack16<WT>(wv, d, w);
 #pragma unroll
-                            for (int e = 0; e < VN; e += 2) {
-                                pa[i] = fmaf(w[e], xr[k2][e], pa[i]);
-                                pb[i] = fmaf(w[e + 1], xr[k2][e + 1], pb[i]);
-                            }
+                            for (int e = 0; e < VN; e += 2)
+                                fma2(pa[i], pb[i], w[e], w[e + 1], xr[k2][e], xr[k2][e + 1]);
                         }
                     }
                     pa[i] += pb[i];
