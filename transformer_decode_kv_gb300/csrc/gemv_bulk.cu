@@ -520,8 +520,10 @@ static int plan_grid(int wt, const GemvArgs& a, int epi, int n_sm, size_t* smem,
         const int64_t grid = std::min<int64_t>(units, (int64_t)n_sm * per_sm);
         const int64_t cap = (units + grid - 1) / grid * gran * (epi == GEPI_SWIGLU ? 2 : 1);
         // two blocks per SM leave room for a third: the next kernel's block, started early by
-        // programmatic dependent launch, prefetches its weights while these finish
-        const size_t budget = per_sm == 2 ? 74u * 1024u : 224u * 1024u;
+        // programmatic dependent launch, prefetches its weights while these finish. Rows longer
+        // than 16 KB (one row per stage, 7 slices per warp) need ~92 registers, so no third
+        // block fits beside two of these anyway: they take 108 KB for a third stage instead.
+        const size_t budget = per_sm == 2 ? (cols && rb > 16384 ? 108u : 74u) * 1024u : 224u * 1024u;
         const size_t base = fixed + (size_t)cap * tm * 4;
         const int min_stages = cols && per_stage > 20000 ? 2 : 3;
         if (base + min_stages * per_stage > budget) continue;
