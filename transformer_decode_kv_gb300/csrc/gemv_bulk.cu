@@ -38,6 +38,7 @@ constexpr int kMaxStages = 8;
 constexpr uint32_t kStageBytes = 16384;     // stage size of the general mapping
 constexpr uint32_t kMaxStageBytes = 32768;
 constexpr uint32_t kSlice = 512;                  // bytes per warp pass (16 per lane)
+constexpr uint32_t kColsStage = 24576;            // column-stationary stage: whole rows up to 24 KB
 
 __device__ __forceinline__ void consumer_sync() {
     asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
@@ -247,8 +248,9 @@ gemv_bulk_kernel(const GemvArgs a) {
                 const __half* ssc = reinterpret_cast<const __half*>(sstages + (size_t)s * (SB / 16));
                 // all rows of the stage at once (one token in this mapping): two independent
                 // accumulators per row, the row reductions interleaved, then lane i adds row i's
-                // sum to the shared total. A stage holds 16 KB of whole rows: 4 / SPW rows.
-                constexpr int RPS = SPW <= 4 ? 4 / SPW : 1;
+                // sum to the shared total. A stage holds kColsStage bytes of whole rows.
+                constexpr int RPS = (int)(kColsStage / (SPW * kConsumerWarps * kSlice)) > 0
+                                        ? (int)(kColsStage / (SPW * kConsumerWarps * kSlice)) : 1;
                 static_assert(TM == 1, "column-stationary mapping serves one token");
                 float pa[RPS], pb[RPS];
 #pragma unroll
@@ -509,8 +511,8 @@ static int plan_grid(int wt, const GemvArgs& a, int epi, int n_sm, size_t* smem,
     const bool cols = tm == 1 && (spw == 1 || spw == 2 || spw == 4 || spw == 7) && spw * vn <= 64 &&
                       rb <= kMaxStageBytes;
     (void)vn;
-    const uint32_t sbytes = cols ? (uint32_t)(rb * std::max<int64_t>(1, 16384 / rb) <= kMaxStageBytes
-                                              ? rb * std::max<int64_t>(1, 16384 / rb) : rb)
+    const uint32_t sbytes = cols ? (uint32_t)(rb * std::max<int64_t>(1, kColsStage / rb) <= kMaxStageBytes
+                                              ? rb * std::max<int64_t>(1, kColsStage / rb) : rb)
                                  : kStageBytes;
     *stage_bytes = cols ? (int)sbytes : 0;
     const size_t per_stage = sbytes + (wt == W_Q8_0 ? sbytes / 16 : 0);
