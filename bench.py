@@ -36,6 +36,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "decode tok/s & prefill tok/s on 1×GB300; decode HBM GB/s vs ~8 TB/s peak"
+GEMV_TRAFFIC = {"llama8b_bf16_1seq": 109.16e6}
 
 
 def _env_int(k, d):
@@ -342,6 +343,10 @@ def main():
     # the dominant kernel: the one-token step kernel, or the GEMV class of the per-op sequence
     dom = max((k for k in ks if ks[k]["launches"]), key=lambda k: ks[k]["ms"])
     g = ks[dom]
+    # DRAM bytes (read + written) per launch of the per-layer decode GEMVs of this workload, from
+    # one ncu capture of the current kernel (profiles/gemv_swiglu_llama8b_bf16.md: the mean of the
+    # Q/K/V, output, gate/up and down launches of a layer)
+    traffic = GEMV_TRAFFIC.get(args.workload) if dom == "linear_gemv" and not args.layers else None
     achieved = g["bytes"] / (g["ms"] / 1e3) / 1e9 if g["ms"] > 0 else 0.0
     lm = ks.get("lm_head", {"ms": 0, "bytes": 0})
     line = {
@@ -353,7 +358,8 @@ def main():
         "decode_hbm_gbs": step_bytes * K / res["dec_s"] / 1e9,
         "decode_step_algorithmic_bytes": step_bytes,
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": hbm_peak,
-                     "unit": "GB/s", "frac": achieved / hbm_peak, "traffic": None,
+                     "unit": "GB/s", "frac": achieved / hbm_peak, "traffic": traffic,
+                     "algorithmic_bytes_per_launch": g["bytes"] / max(1, g["launches"]),
                      "peak_source": peak_src,
                      "launches": g["launches"], "avg_launch_us": g["ms"] * 1e3 / max(1, g["launches"])},
         "kernel_share": {k: v["ms"] / max(1e-9, sum(x["ms"] for x in ks.values())) for k, v in ks.items()
