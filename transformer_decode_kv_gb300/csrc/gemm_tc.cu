@@ -321,6 +321,146 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                      "r"((uint32_t)BN));
 }
 
+// Gate/up + SwiGLU with the roles swapped: the MMA's A operand is a 128-token tile of the
+// activations (two bf16 terms, hi and lo) and its B operand 128 gate rows followed by the 128
+// matching up rows (N = 256), so one 64 KB stage feeds twice the MMA work of a 48 KB stage of
+// the weight-major kernel. The accumulator D[128 tokens][256] has one token per TMEM lane: each
+// thread reads its token's gate and up values (columns j and 128 + j) and writes silu(g) * u of
+// 128 consecutive features as bf16 hi and lo terms.
+constexpr int kTnRows = 128;                     // tokens per tile (MMA M)
+constexpr int kTnN = 256;                        // 128 gate + 128 up rows (MMA N)
+constexpr uint32_t kTnA = kTnRows * kBK * 2;     // 16 KB per activation term
+constexpr uint32_t kTnB = kTnN * kBK * 2;        // 32 KB
+constexpr uint32_t kTnStage = 2 * kTnA + kTnB;   // 64 KB
+constexpr int kTnStages = (int)(196608u / kTnStage);
+constexpr size_t kTnSmem = 1024 + (size_t)kTnStages * kTnStage + 256;
+
+__global__ void __launch_bounds__(128, 1)
+gemm_swiglu_tn_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmXlo,
+                      const __grid_constant__ CUtensorMap tmW, int K, int T, int F,
+                      __nv_bfloat16* __restrict__ Y, __nv_bfloat16* __restrict__ Y2, int ldy,
+                      uint32_t* __restrict__ err) {
+    constexpr int S = kTnStages;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * kTnStage);
+    uint64_t* empty = full + S;
+    uint64_t* accf = empty + S;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accf + 1);
+    int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nk = K / kBK;
+    const int t0 = blockIdx.x * kTnRows;             // token tiles run fastest (weight reuse in L2)
+    const int f0 = blockIdx.y * (kTnN / 2);          // first gate/up feature of the tile
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        mbar_init(accf, 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmX)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmXlo)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmW)) : "memory");
+    }
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(tmem_slot)),
+                     "r"((uint32_t)kTnN));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (threadIdx.x == 0) {
+        // ---- TMA producer: per stage the two activation terms and the gate and up rows
+        int issued = 0;
+        for (int kb = 0; kb < nk; ++kb) {
+            const int s = kb % S;
+            const uint32_t ph = (uint32_t)(kb / S) & 1u;
+            if (kb >= S && !mbar_wait(&empty[s], ph ^ 1u)) { atomicOr(err, ERR_TIMEOUT); *(volatile int*)abort_flag = 1; break; }
+            if (*(volatile int*)abort_flag) break;
+            uint8_t* st = smem + (size_t)s * kTnStage;
+            mbar_expect_tx(&full[s], kTnStage);
+            tma_load_2d(st, &tmX, &full[s], kb * kBK, t0);
+            tma_load_2d(st + kTnA, &tmXlo, &full[s], kb * kBK, t0);
+            tma_load_2d(st + 2 * kTnA, &tmW, &full[s], kb * kBK, f0);
+            tma_load_2d(st + 2 * kTnA + kTnB / 2, &tmW, &full[s], kb * kBK, F + f0);
+            issued = kb + 1;
+        }
+        for (int kb = (issued > S ? issued - S : 0); kb < issued; ++kb)
+            mbar_wait(&full[kb % S], (uint32_t)(kb / S) & 1u);
+    } else if (threadIdx.x == 32) {
+        // ---- MMA issuer: D += X_hi W^T + X_lo W^T
+        constexpr uint32_t idesc = idesc_bf16(kTnRows, kTnN);
+        bool ok = true;
+        for (int kb = 0; kb < nk; ++kb) {
+            const int s = kb % S;
+            const uint32_t ph = (uint32_t)(kb / S) & 1u;
+            if (!mbar_wait(&full[s], ph)) { ok = false; break; }
+            tc_fence_after();
+            const uint8_t* st = smem + (size_t)s * kTnStage;
+            const uint64_t ah = sdesc_sw128(smem_u32(st));
+            const uint64_t al = sdesc_sw128(smem_u32(st + kTnA));
+            const uint64_t bd = sdesc_sw128(smem_u32(st + 2 * kTnA));
+#pragma unroll
+            for (int kk = 0; kk < kBK / 16; ++kk)
+                umma_bf16(tmem, ah + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2), idesc, (kb | kk) != 0 ? 1u : 0u);
+#pragma unroll
+            for (int kk = 0; kk < kBK / 16; ++kk)
+                umma_bf16(tmem, al + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2), idesc, 1u);
+            umma_commit(&empty[s]);
+        }
+        if (!ok) { atomicOr(err, ERR_TIMEOUT); *(volatile int*)abort_flag = 1; }
+        umma_commit(accf);
+    }
+    __syncwarp();
+
+    // ---- epilogue: thread = token; gate columns j and up columns 128 + j of its TMEM lane
+    const bool have = mbar_wait(accf, 0);
+    tc_fence_after();
+    if (!have) atomicOr(err, ERR_TIMEOUT);
+    const bool live = have && !*(volatile int*)abort_flag;
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const int t = t0 + warp * 32 + lane;
+#pragma unroll 1
+    for (int j0 = 0; j0 < kTnN / 2; j0 += 16) {
+        float g[16], u[16];
+        tmem_ld16(tmem + lane_base + (uint32_t)j0, g);
+        tmem_ld16(tmem + lane_base + (uint32_t)(kTnN / 2 + j0), u);
+        if (!live || t >= T) continue;
+        uint32_t hi[8], lo[8];
+#pragma unroll
+        for (int j = 0; j < 16; j += 2) {
+            const float o0 = g[j] / (1.0f + expf(-g[j])) * u[j];
+            const float o1 = g[j + 1] / (1.0f + expf(-g[j + 1])) * u[j + 1];
+            const __nv_bfloat162 h = __floats2bfloat162_rn(o0, o1);
+            const float2 hf = __bfloat1622float2(h);
+            const __nv_bfloat162 l2 = __floats2bfloat162_rn(o0 - hf.x, o1 - hf.y);
+            hi[j / 2] = *reinterpret_cast<const uint32_t*>(&h);
+            lo[j / 2] = *reinterpret_cast<const uint32_t*>(&l2);
+        }
+        uint4* dh = reinterpret_cast<uint4*>(Y + (int64_t)t * ldy + f0 + j0);
+        dh[0] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        dh[1] = make_uint4(hi[4], hi[5], hi[6], hi[7]);
+        if (Y2) {
+            uint4* dl = reinterpret_cast<uint4*>(Y2 + (int64_t)t * ldy + f0 + j0);
+            dl[0] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+            dl[1] = make_uint4(lo[4], lo[5], lo[6], lo[7]);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                     "r"((uint32_t)kTnN));
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     if (!fn) {
@@ -381,6 +521,25 @@ bool tc_make_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols,
 }
 
 int tc_token_tile(int T) { return T > 128 ? 256 : 128; }
+
+bool tc_swiglu_tn_ok(int64_t K, int64_t F) { return K % kBK == 0 && K >= kBK && F % (kTnN / 2) == 0 && F > 0; }
+
+bool launch_gemm_swiglu_tn(const CUtensorMap& xmap, const CUtensorMap& xmap_lo, const CUtensorMap& wmap,
+                           int K, int T, int F, void* Y, void* Y2, int ldy, uint32_t* err, cudaStream_t st) {
+    if (T <= 0) return true;
+    static bool attr = false;
+    if (!attr) {
+        if (cudaFuncSetAttribute(gemm_swiglu_tn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)kTnSmem) != cudaSuccess)
+            return false;
+        attr = true;
+    }
+    dim3 grid((T + kTnRows - 1) / kTnRows, F / (kTnN / 2));
+    gemm_swiglu_tn_kernel<<<grid, 128, kTnSmem, st>>>(xmap, xmap_lo, wmap, K, T, F,
+                                                      static_cast<__nv_bfloat16*>(Y),
+                                                      static_cast<__nv_bfloat16*>(Y2), ldy, err);
+    return cudaGetLastError() == cudaSuccess;
+}
 
 bool tc_shape_ok(int64_t M, int64_t K, int epi, int64_t F) {
     if (K % kBK != 0 || K < kBK) return false;

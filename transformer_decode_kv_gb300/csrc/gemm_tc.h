@@ -32,4 +32,11 @@ bool launch_gemm_tc(const CUtensorMap& wmap, const CUtensorMap& xmap, int epi, i
                     int T, int F, void* Y, int ldy, uint32_t* err, cudaStream_t st,
                     const CUtensorMap* xmap_lo = nullptr, void* Y2 = nullptr);
 
+// Gate/up + SwiGLU with the token tile as the MMA's A operand (128 tokens, two bf16 terms: xmap and
+// xmap_lo, box 128 rows) and 128 gate + 128 up rows as B (wmap over the [2F][K] gate|up matrix,
+// box 128 rows): Y, Y2 [>= T][ldy] bf16 hi and lo terms of silu(gate) * up. F % 128 == 0.
+bool tc_swiglu_tn_ok(int64_t K, int64_t F);
+bool launch_gemm_swiglu_tn(const CUtensorMap& xmap, const CUtensorMap& xmap_lo, const CUtensorMap& wmap,
+                           int K, int T, int F, void* Y, void* Y2, int ldy, uint32_t* err, cudaStream_t st);
+
 }  // namespace llm

@@ -54,6 +54,8 @@ struct Layer {
     uint32_t loaded = 0;
     // TMA maps of the BF16 weights for the tensor-core prefill GEMM
     CUtensorMap mq, mo, mgu, md;
+    CUtensorMap mgu128;      // gate|up with 128-row boxes (token-major SwiGLU GEMM)
+    bool gu_tn = false;
 };
 
 // Kernel classes timed by llm_debug_kernel_timing.
@@ -573,7 +575,13 @@ bool forward_ubatch(llm_ctx* c, int32_t T, int32_t O, int32_t out_row0, int32_t 
             else launch_rmsnorm(c->x, nullptr, T, d, L.ffn_norm, hp.rms_eps, c->h, st);
             kt_end(c, k, KC_RMSNORM, norm_bytes, 0);
             k = kt_begin(c);
-            if (tc) { if (!tc_gemm(L.mgu, c->m_hb[bi], GEMM_EPI_SWIGLU, d, 0, c->ub, F)) return false; }
+            if (tc && L.gu_tn) {
+                if (!launch_gemm_swiglu_tn(c->m_hb[bi], c->m_hb_lo, L.mgu128, d, T, F, c->ub, c->ub_lo, F,
+                                           c->d_err, st)) {
+                    c->err = "tensor-core GEMM launch failed";
+                    return false;
+                }
+            } else if (tc) { if (!tc_gemm(L.mgu, c->m_hb[bi], GEMM_EPI_SWIGLU, d, 0, c->ub, F)) return false; }
             else launch_linear_swiglu(L.gu, F, c->h, d, T, c->u, F, c->tmp, st);
             kt_end(c, k, lin_cls, wbytes(L.gu, 2 * (int64_t)F) + Td * (d + F) * 4.0, 4.0 * Td * F * d);
         }
@@ -984,6 +992,7 @@ int llm_weights_ready(llm_ctx* c) {
              tc_make_map(&L.mo, L.wo.data, d, qw, 128) &&
              tc_make_map(&L.mgu, L.gu.data, 2 * F, d, 64) &&
              tc_make_map(&L.md, L.down.data, d, F, 128);
+        L.gu_tn = ok && tc_swiglu_tn_ok(d, F) && tc_make_map(&L.mgu128, L.gu.data, 2 * F, d, 128);
     }
     const int boxes[2] = {128, 256};
     for (int i = 0; ok && i < 2; ++i)
