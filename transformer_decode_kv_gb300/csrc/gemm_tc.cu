@@ -18,6 +18,7 @@
 #include <cuda_bf16.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <cstdint>
 
 #include "gemm_tc.h"
@@ -321,12 +322,13 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                      "r"((uint32_t)BN));
 }
 
-// Gate/up + SwiGLU with the roles swapped: the MMA's A operand is a 128-token tile of the
-// activations (two bf16 terms, hi and lo) and its B operand 128 gate rows followed by the 128
-// matching up rows (N = 256), so one 64 KB stage feeds twice the MMA work of a 48 KB stage of
-// the weight-major kernel. The accumulator D[128 tokens][256] has one token per TMEM lane: each
-// thread reads its token's gate and up values (columns j and 128 + j) and writes silu(g) * u of
-// 128 consecutive features as bf16 hi and lo terms.
+// Token-major GEMM: the MMA's A operand is a 128-token tile of the activations (two bf16 terms,
+// hi and lo) and its B operand 256 weight rows (N = 256; for SwiGLU 128 gate rows followed by the
+// 128 matching up rows), so one 64 KB stage feeds twice the MMA work of a 48 KB stage of the
+// weight-major kernel. The accumulator D[128 tokens][256] has one token per TMEM lane: each thread
+// owns its token's 256 outputs. SwiGLU writes silu(g) * u of 128 consecutive features as bf16
+// hi and lo terms; store / residual add write float32, through vector atomic adds when the K
+// range is split over blockIdx.z (the output then starts zeroed for a store).
 constexpr int kTnRows = 128;                     // tokens per tile (MMA M)
 constexpr int kTnN = 256;                        // 128 gate + 128 up rows (MMA N)
 constexpr uint32_t kTnA = kTnRows * kBK * 2;     // 16 KB per activation term
@@ -335,11 +337,11 @@ constexpr uint32_t kTnStage = 2 * kTnA + kTnB;   // 64 KB
 constexpr int kTnStages = (int)(196608u / kTnStage);
 constexpr size_t kTnSmem = 1024 + (size_t)kTnStages * kTnStage + 256;
 
+template <int EPI>
 __global__ void __launch_bounds__(128, 1)
-gemm_swiglu_tn_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmXlo,
-                      const __grid_constant__ CUtensorMap tmW, int K, int T, int F,
-                      __nv_bfloat16* __restrict__ Y, __nv_bfloat16* __restrict__ Y2, int ldy,
-                      uint32_t* __restrict__ err) {
+gemm_tn_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmXlo,
+               const __grid_constant__ CUtensorMap tmW, int K, int T, int M, int F,
+               void* __restrict__ Y, void* __restrict__ Y2, int ldy, uint32_t* __restrict__ err) {
     constexpr int S = kTnStages;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -350,9 +352,13 @@ gemm_swiglu_tn_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_cons
     int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int nk = K / kBK;
+    const int nk_all = K / kBK;
+    const int per = (nk_all + gridDim.z - 1) / gridDim.z;
+    const int kb0 = min(nk_all, (int)blockIdx.z * per), nk = min(nk_all, kb0 + per) - kb0;
     const int t0 = blockIdx.x * kTnRows;             // token tiles run fastest (weight reuse in L2)
-    const int f0 = blockIdx.y * (kTnN / 2);          // first gate/up feature of the tile
+    // SwiGLU: first gate/up feature of the tile; otherwise the first of its 256 weight rows
+    const int f0 = blockIdx.y * (EPI == GEMM_EPI_SWIGLU ? kTnN / 2 : kTnN);
+    const int w2 = EPI == GEMM_EPI_SWIGLU ? F + f0 : f0 + kTnN / 2;   // second 128-row box
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
@@ -387,10 +393,11 @@ gemm_swiglu_tn_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_cons
             if (*(volatile int*)abort_flag) break;
             uint8_t* st = smem + (size_t)s * kTnStage;
             mbar_expect_tx(&full[s], kTnStage);
-            tma_load_2d(st, &tmX, &full[s], kb * kBK, t0);
-            tma_load_2d(st + kTnA, &tmXlo, &full[s], kb * kBK, t0);
-            tma_load_2d(st + 2 * kTnA, &tmW, &full[s], kb * kBK, f0);
-            tma_load_2d(st + 2 * kTnA + kTnB / 2, &tmW, &full[s], kb * kBK, F + f0);
+            const int kx = (kb0 + kb) * kBK;
+            tma_load_2d(st, &tmX, &full[s], kx, t0);
+            tma_load_2d(st + kTnA, &tmXlo, &full[s], kx, t0);
+            tma_load_2d(st + 2 * kTnA, &tmW, &full[s], kx, f0);
+            tma_load_2d(st + 2 * kTnA + kTnB / 2, &tmW, &full[s], kx, w2);
             issued = kb + 1;
         }
         for (int kb = (issued > S ? issued - S : 0); kb < issued; ++kb)
@@ -425,33 +432,61 @@ gemm_swiglu_tn_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_cons
     const bool have = mbar_wait(accf, 0);
     tc_fence_after();
     if (!have) atomicOr(err, ERR_TIMEOUT);
-    const bool live = have && !*(volatile int*)abort_flag;
+    const bool live = have && !*(volatile int*)abort_flag && nk > 0;
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
     const int t = t0 + warp * 32 + lane;
+    if (EPI == GEMM_EPI_SWIGLU) {
+        __nv_bfloat16* Yb = static_cast<__nv_bfloat16*>(Y);
+        __nv_bfloat16* Yb2 = static_cast<__nv_bfloat16*>(Y2);
 #pragma unroll 1
-    for (int j0 = 0; j0 < kTnN / 2; j0 += 16) {
-        float g[16], u[16];
-        tmem_ld16(tmem + lane_base + (uint32_t)j0, g);
-        tmem_ld16(tmem + lane_base + (uint32_t)(kTnN / 2 + j0), u);
-        if (!live || t >= T) continue;
-        uint32_t hi[8], lo[8];
+        for (int j0 = 0; j0 < kTnN / 2; j0 += 16) {
+            float g[16], u[16];
+            tmem_ld16(tmem + lane_base + (uint32_t)j0, g);
+            tmem_ld16(tmem + lane_base + (uint32_t)(kTnN / 2 + j0), u);
+            if (!live || t >= T) continue;
+            uint32_t hi[8], lo[8];
 #pragma unroll
-        for (int j = 0; j < 16; j += 2) {
-            const float o0 = g[j] / (1.0f + expf(-g[j])) * u[j];
-            const float o1 = g[j + 1] / (1.0f + expf(-g[j + 1])) * u[j + 1];
-            const __nv_bfloat162 h = __floats2bfloat162_rn(o0, o1);
-            const float2 hf = __bfloat1622float2(h);
-            const __nv_bfloat162 l2 = __floats2bfloat162_rn(o0 - hf.x, o1 - hf.y);
-            hi[j / 2] = *reinterpret_cast<const uint32_t*>(&h);
-            lo[j / 2] = *reinterpret_cast<const uint32_t*>(&l2);
+            for (int j = 0; j < 16; j += 2) {
+                const float o0 = g[j] / (1.0f + expf(-g[j])) * u[j];
+                const float o1 = g[j + 1] / (1.0f + expf(-g[j + 1])) * u[j + 1];
+                const __nv_bfloat162 h = __floats2bfloat162_rn(o0, o1);
+                const float2 hf = __bfloat1622float2(h);
+                const __nv_bfloat162 l2 = __floats2bfloat162_rn(o0 - hf.x, o1 - hf.y);
+                hi[j / 2] = *reinterpret_cast<const uint32_t*>(&h);
+                lo[j / 2] = *reinterpret_cast<const uint32_t*>(&l2);
+            }
+            uint4* dh = reinterpret_cast<uint4*>(Yb + (int64_t)t * ldy + f0 + j0);
+            dh[0] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+            dh[1] = make_uint4(hi[4], hi[5], hi[6], hi[7]);
+            if (Yb2) {
+                uint4* dl = reinterpret_cast<uint4*>(Yb2 + (int64_t)t * ldy + f0 + j0);
+                dl[0] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                dl[1] = make_uint4(lo[4], lo[5], lo[6], lo[7]);
+            }
         }
-        uint4* dh = reinterpret_cast<uint4*>(Y + (int64_t)t * ldy + f0 + j0);
-        dh[0] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-        dh[1] = make_uint4(hi[4], hi[5], hi[6], hi[7]);
-        if (Y2) {
-            uint4* dl = reinterpret_cast<uint4*>(Y2 + (int64_t)t * ldy + f0 + j0);
-            dl[0] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-            dl[1] = make_uint4(lo[4], lo[5], lo[6], lo[7]);
+    } else {
+        const bool atomic = gridDim.z > 1;
+        float* Yf = static_cast<float*>(Y);
+#pragma unroll 1
+        for (int j0 = 0; j0 < kTnN; j0 += 16) {
+            float v[16];
+            tmem_ld16(tmem + lane_base + (uint32_t)j0, v);
+            if (!live || t >= T || f0 + j0 >= M) continue;
+            float4* dst = reinterpret_cast<float4*>(Yf + (int64_t)t * ldy + f0 + j0);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                float4 w4 = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+                if (atomic) {
+                    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst + q),
+                                 "f"(w4.x), "f"(w4.y), "f"(w4.z), "f"(w4.w) : "memory");
+                } else {
+                    if (EPI == GEMM_EPI_ADD) {
+                        const float4 o = dst[q];
+                        w4.x += o.x; w4.y += o.y; w4.z += o.z; w4.w += o.w;
+                    }
+                    dst[q] = w4;
+                }
+            }
         }
     }
     tc_fence_before();
@@ -523,22 +558,46 @@ bool tc_make_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols,
 int tc_token_tile(int T) { return T > 128 ? 256 : 128; }
 
 bool tc_swiglu_tn_ok(int64_t K, int64_t F) { return K % kBK == 0 && K >= kBK && F % (kTnN / 2) == 0 && F > 0; }
+bool tc_tn_ok(int64_t M, int64_t K) { return K % kBK == 0 && K >= kBK && M % kTnN == 0 && M > 0; }
+
+template <int EPI>
+bool launch_tn(const CUtensorMap& xmap, const CUtensorMap& xmap_lo, const CUtensorMap& wmap, int K,
+               int T, int M, int F, void* Y, void* Y2, int ldy, int splits, uint32_t* err, cudaStream_t st) {
+    auto k = gemm_tn_kernel<EPI>;
+    static bool attr = false;
+    if (!attr) {
+        if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTnSmem) != cudaSuccess)
+            return false;
+        attr = true;
+    }
+    const int ntile = EPI == GEMM_EPI_SWIGLU ? F / (kTnN / 2) : M / kTnN;
+    dim3 grid((T + kTnRows - 1) / kTnRows, ntile, splits);
+    k<<<grid, 128, kTnSmem, st>>>(xmap, xmap_lo, wmap, K, T, M, F, Y, Y2, ldy, err);
+    return cudaGetLastError() == cudaSuccess;
+}
 
 bool launch_gemm_swiglu_tn(const CUtensorMap& xmap, const CUtensorMap& xmap_lo, const CUtensorMap& wmap,
                            int K, int T, int F, void* Y, void* Y2, int ldy, uint32_t* err, cudaStream_t st) {
     if (T <= 0) return true;
-    static bool attr = false;
-    if (!attr) {
-        if (cudaFuncSetAttribute(gemm_swiglu_tn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)kTnSmem) != cudaSuccess)
-            return false;
-        attr = true;
-    }
-    dim3 grid((T + kTnRows - 1) / kTnRows, F / (kTnN / 2));
-    gemm_swiglu_tn_kernel<<<grid, 128, kTnSmem, st>>>(xmap, xmap_lo, wmap, K, T, F,
-                                                      static_cast<__nv_bfloat16*>(Y),
-                                                      static_cast<__nv_bfloat16*>(Y2), ldy, err);
-    return cudaGetLastError() == cudaSuccess;
+    return launch_tn<GEMM_EPI_SWIGLU>(xmap, xmap_lo, wmap, K, T, 0, F, Y, Y2, ldy, 1, err, st);
+}
+
+int tc_tn_splits(int64_t M, int64_t K, int T, int n_sm) {
+    const int64_t tiles = (T + kTnRows - 1) / kTnRows * (M / kTnN);
+    int s = (int)std::max<int64_t>(1, n_sm / std::max<int64_t>(1, tiles));
+    s = std::min(s, 4);
+    while (s > 1 && K / kBK / s < 8) --s;          // at least 8 k-steps per split
+    return s;
+}
+
+bool launch_gemm_tn(const CUtensorMap& xmap, const CUtensorMap& xmap_lo, const CUtensorMap& wmap, int epi,
+                    int K, int M, int T, float* Y, int ldy, int splits, uint32_t* err, cudaStream_t st) {
+    if (T <= 0) return true;
+    if (epi == GEMM_EPI_STORE)
+        return launch_tn<GEMM_EPI_STORE>(xmap, xmap_lo, wmap, K, T, M, 0, Y, nullptr, ldy, splits, err, st);
+    if (epi == GEMM_EPI_ADD)
+        return launch_tn<GEMM_EPI_ADD>(xmap, xmap_lo, wmap, K, T, M, 0, Y, nullptr, ldy, splits, err, st);
+    return false;
 }
 
 bool tc_shape_ok(int64_t M, int64_t K, int epi, int64_t F) {

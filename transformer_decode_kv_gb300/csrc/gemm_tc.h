@@ -39,4 +39,12 @@ bool tc_swiglu_tn_ok(int64_t K, int64_t F);
 bool launch_gemm_swiglu_tn(const CUtensorMap& xmap, const CUtensorMap& xmap_lo, const CUtensorMap& wmap,
                            int K, int T, int F, void* Y, void* Y2, int ldy, uint32_t* err, cudaStream_t st);
 
+// Store / residual add with the token tile as A (two bf16 terms) and 256 weight rows as B (wmap
+// over W [M][K], box 128 rows): Y [>= T][ldy] float32 (op)= X W^T. M % 256 == 0. splits > 1
+// splits K over blockIdx.z with vector atomic adds into Y (a store then needs Y zeroed first).
+bool tc_tn_ok(int64_t M, int64_t K);
+int tc_tn_splits(int64_t M, int64_t K, int T, int n_sm);
+bool launch_gemm_tn(const CUtensorMap& xmap, const CUtensorMap& xmap_lo, const CUtensorMap& wmap, int epi,
+                    int K, int M, int T, float* Y, int ldy, int splits, uint32_t* err, cudaStream_t st);
+
 }  // namespace llm

@@ -496,8 +496,23 @@ bool forward_ubatch(llm_ctx* c, int32_t T, int32_t O, int32_t out_row0, int32_t 
     const bool tc = !gemv && c->tc_ok;
     const int bi = 0;
     if (tc) { a.out_b = c->attnb; a.out_b_lo = c->attnb_lo; }
+    // store / residual add: the token-major GEMM when the weight rows come in 256-row tiles
+    // (split-K with atomic adds when the tiles alone leave SMs idle), else the weight-major one
     auto tc_gemm = [&](const CUtensorMap& wm, const CUtensorMap& xm, int epi, int K, int M, void* Y,
                        int ldy) {
+        const CUtensorMap* xlo = &xm == &c->m_hb[bi] ? &c->m_hb_lo
+                               : &xm == &c->m_attnb[bi] ? &c->m_attnb_lo : &c->m_ub_lo;
+        if (epi != GEMM_EPI_SWIGLU && tc_tn_ok(M, K)) {
+            const int splits = tc_tn_splits(M, K, T, c->n_sm);
+            if (splits > 1 && epi == GEMM_EPI_STORE &&
+                !cuda_ok(c, cudaMemsetAsync(Y, 0, sizeof(float) * (size_t)T * ldy, st), "memset"))
+                return false;
+            if (!launch_gemm_tn(xm, *xlo, wm, epi, K, M, T, static_cast<float*>(Y), ldy, splits, c->d_err, st)) {
+                c->err = "tensor-core GEMM launch failed";
+                return false;
+            }
+            return true;
+        }
         const CUtensorMap* lo = &xm == &c->m_hb[bi] ? &c->m_hb_lo
                               : &xm == &c->m_attnb[bi] ? &c->m_attnb_lo : &c->m_ub_lo;
         void* y2 = epi == GEMM_EPI_SWIGLU ? c->ub_lo : nullptr;
