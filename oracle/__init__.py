@@ -30,3 +30,4 @@ from .numerics import (rms_norm, rope, attention, silu, swiglu, linear)    # noq
 from .memory import (Cells, sanitize_batch, split_simple, derive_cparams,   # noqa: F401
                      LLAMA_MAX_SEQ, DecodeStatus)
 from .context import OracleContext, OracleWeights                            # noqa: F401
+from .sampling import SamplerParams, sample as sample_chain                   # noqa: F401
