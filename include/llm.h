@@ -215,6 +215,34 @@ typedef struct llm_perf_data {
 } llm_perf_data;
 void llm_perf(llm_ctx *ctx, llm_perf_data *out);
 
+/* ---- sampler chain on the device ([P1] sampler chain after Крок 14: penalties, then the
+ * cut-offs top-k, top-p and min-p, then temperature, then one token is picked; a backend sampler
+ * picks on the device, so the logits row is not copied to the host).
+ * Steps, in order, over logits row i of the last llm_decode (i as in llm_get_logits_ith):
+ *   repeat penalty: each distinct token of penalty_tokens once, l > 0 -> l / repeat_penalty,
+ *     otherwise l * repeat_penalty (1 = off);
+ *   top-k: the top_k largest logits (1 .. 4096; ties at the k-th value: the lower token ids),
+ *     ordered by logit descending then token id ascending;
+ *   top-p: the shortest prefix of that order whose softmax probability (over the candidates,
+ *     before temperature) reaches top_p (1 = off);
+ *   min-p: the candidates with l - l_max >= ln(min_p) (0 = off);
+ *   pick: temperature <= 0 takes the first candidate (greedy); otherwise the first candidate
+ *     whose cumulative weight exp((l - l_max) / temperature) exceeds u times the total.
+ * u in [0, 1) is the caller's uniform random draw (the library draws no random numbers).
+ * penalty_tokens: host array of n_penalty_tokens (<= 4096) token ids, may be NULL if 0.
+ * Returns the token, or -1 for an invalid argument, a row without logits or a device error.
+ * Synchronises the context's stream. */
+typedef struct llm_sampler_params {
+    int32_t top_k;
+    float   top_p;
+    float   min_p;
+    float   temperature;
+    float   repeat_penalty;
+    const int32_t *penalty_tokens;
+    int32_t n_penalty_tokens;
+} llm_sampler_params;
+int32_t llm_sample_ith(llm_ctx *ctx, int32_t i, const llm_sampler_params *params, float u);
+
 /* ---- test and debugging hooks ---------------------------------------------------------------
  * They expose intermediate state so tests can compare it with an independent implementation
  * (the eval-callback idea of [P2] Example 4). */
@@ -294,6 +322,11 @@ int llm_debug_step_trace_enable(llm_ctx *ctx, int enable);
  * number of values (0 if nothing was recorded); writes at most cap. */
 int64_t llm_debug_step_trace(llm_ctx *ctx, uint64_t *out, int64_t cap, int32_t *n_blocks,
                              int32_t *n_slots);
+
+/* Overwrite logits row i of the last llm_decode (i as in llm_get_logits_ith) with n_vocab floats
+ * from the host array row (for tests of llm_sample_ith on chosen rows: ties, NaN, flat rows).
+ * llm_get_argmax_ith keeps the argmax that llm_decode computed. Returns 0, or -1 for a row without logits or a failed copy. Synchronises the stream. */
+int llm_debug_set_logits(llm_ctx *ctx, int32_t i, const float *row);
 
 /* Fault injection: kind 1 makes ubatch `ub` of the next llm_decode hand the K/V append kernel a
  * cell index past the cache; the kernel's bounds check skips the write and reports the error

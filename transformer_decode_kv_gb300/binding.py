@@ -39,6 +39,12 @@ class Batch(C.Structure):
                 ("seq_id", C.POINTER(C.POINTER(C.c_int32))), ("logits", C.POINTER(C.c_int8))]
 
 
+class SamplerParams(C.Structure):
+    _fields_ = [("top_k", C.c_int32), ("top_p", C.c_float), ("min_p", C.c_float),
+                ("temperature", C.c_float), ("repeat_penalty", C.c_float),
+                ("penalty_tokens", C.POINTER(C.c_int32)), ("n_penalty_tokens", C.c_int32)]
+
+
 class PerfData(C.Structure):
     _fields_ = [("n_decode_calls", C.c_int64), ("n_tokens", C.c_int64), ("n_ubatches", C.c_int64),
                 ("n_graph_replays", C.c_int64), ("t_decode_ms", C.c_double),
@@ -77,6 +83,8 @@ SIGNATURES = {
                                          C.POINTER(C.c_float), C.c_int64]),
     "llm_debug_inject_fault": (C.c_int, [C.c_void_p, C.c_int32, C.c_int32]),
     "llm_debug_kv_raw": (C.c_int64, [C.c_void_p, C.c_int32, C.c_int32, C.c_void_p, C.c_int64]),
+    "llm_sample_ith": (C.c_int32, [C.c_void_p, C.c_int32, C.POINTER(SamplerParams), C.c_float]),
+    "llm_debug_set_logits": (C.c_int, [C.c_void_p, C.c_int32, C.POINTER(C.c_float)]),
     "llm_debug_step_trace_enable": (C.c_int, [C.c_void_p, C.c_int]),
     "llm_debug_step_trace": (C.c_int64, [C.c_void_p, C.POINTER(C.c_uint64), C.c_int64,
                                          C.POINTER(C.c_int32), C.POINTER(C.c_int32)]),
@@ -226,6 +234,20 @@ class Context:
         if not p:
             return None
         return np.ctypeslib.as_array(p, shape=(self.n_vocab,)).copy()
+
+    def sample_ith(self, i: int, top_k: int = 40, top_p: float = 1.0, min_p: float = 0.0,
+                   temperature: float = 1.0, repeat_penalty: float = 1.0, penalty_tokens=(),
+                   u: float = 0.0) -> int:
+        """The device sampler chain over logits row i; u in [0, 1) is the uniform draw."""
+        pen = np.asarray(list(penalty_tokens), dtype=np.int32)
+        p = SamplerParams(top_k, top_p, min_p, temperature, repeat_penalty,
+                          pen.ctypes.data_as(C.POINTER(C.c_int32)) if len(pen) else None, len(pen))
+        return lib().llm_sample_ith(self.ptr, i, C.byref(p), u)
+
+    def debug_set_logits(self, i: int, row) -> int:
+        r = np.ascontiguousarray(row, dtype=np.float32)
+        assert r.shape == (self.n_vocab,)
+        return lib().llm_debug_set_logits(self.ptr, i, _ptr(r, C.c_float))
 
     def get_argmax_ith(self, i: int) -> int:
         return lib().llm_get_argmax_ith(self.ptr, i)

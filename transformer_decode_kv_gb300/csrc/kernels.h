@@ -108,6 +108,22 @@ struct AttnArgs {
 // split-K partial softmax per work item, then a combine per tile ([P2] Example 4 FLASH_ATTN_EXT;
 // Example 11 for the unfused meaning). Scale 1/sqrt(hd).
 bool launch_attention(const AttnArgs& a, cudaStream_t st);
+
+// ---- the sampler chain on one logits row (sampler.cu)
+struct SampleArgs {
+    const float* logits = nullptr;   // [V] the row
+    int32_t V = 0;
+    const int32_t* pen_tok = nullptr;  // device: tokens of the repeat penalty
+    int32_t n_pen = 0;
+    float penalty = 1.f;
+    int32_t top_k = 1;               // 1 .. sample_max_k()
+    float top_p = 1.f, min_p = 0.f, temperature = 0.f, u = 0.f;
+    float* scratch = nullptr;        // [V]
+    int32_t* out = nullptr;          // the picked token (device)
+    uint32_t* err = nullptr;
+};
+int sample_max_k();
+bool launch_sample(const SampleArgs& a, cudaStream_t st);
 // The prefill tiles (16 tokens x 4 query heads) on tensor cores (attn_mma.cu): F16 KV, 4 query
 // heads per KV head, head_dim 32, 64 or 128. launch_attention uses it when it applies.
 bool attention_mma_ok(const AttnArgs& a);

@@ -176,6 +176,9 @@ struct llm_ctx {
     int32_t* d_abort = nullptr;
     uint32_t step_gen = 0;              // launches since the counters were last zeroed
     bool step_trace = false;
+    float* d_sample_row = nullptr;      // sampler scratch [V]
+    int32_t* d_sample_tok = nullptr;    // [kMaxPenalty] penalty tokens, then the picked token
+    int32_t* h_sample_tok = nullptr;    // pinned: the picked token
     uint64_t* d_trace = nullptr;        // timeline of the last traced step
     int32_t trace_blocks = 0, trace_slots = 0;
     bool trace_valid = false;
@@ -1373,6 +1376,55 @@ int llm_debug_gemm_bf16(int32_t epi, const void* W, int64_t M, int64_t K, const 
          cudaMemcpy(&h, err, sizeof(uint32_t), cudaMemcpyDeviceToHost) == cudaSuccess;
     cudaFree(err);
     return ok && h == 0 ? 0 : -3;
+}
+
+int32_t llm_sample_ith(llm_ctx* c, int32_t i, const llm_sampler_params* p, float u) {
+    constexpr int32_t kMaxPenalty = 4096;
+    if (!c || !p || c->host_only) return -1;
+    if (p->top_k < 1 || p->top_k > sample_max_k() || !(p->top_p > 0.f && p->top_p <= 1.f) ||
+        !(p->min_p >= 0.f && p->min_p < 1.f) || !(u >= 0.f && u < 1.f) ||
+        p->n_penalty_tokens < 0 || p->n_penalty_tokens > kMaxPenalty ||
+        (p->n_penalty_tokens > 0 && !p->penalty_tokens) || !(p->repeat_penalty > 0.f)) {
+        c->err = "invalid sampler parameters";
+        return -1;
+    }
+    const int32_t j = resolve_row(c, i);
+    if (j < 0) { c->err = "no logits for this output"; return -1; }
+    if (!c->d_sample_row && !(dalloc(c, &c->d_sample_row, (size_t)c->hp.n_vocab) &&
+                              dalloc(c, &c->d_sample_tok, (size_t)kMaxPenalty + 1) &&
+                              cuda_ok(c, cudaMallocHost(&c->h_sample_tok, sizeof(int32_t)), "cudaMallocHost")))
+        return -1;
+    SampleArgs a;
+    a.logits = c->d_logits + (size_t)j * c->hp.n_vocab;
+    a.V = c->hp.n_vocab;
+    a.pen_tok = c->d_sample_tok;
+    a.n_pen = p->n_penalty_tokens;
+    a.penalty = p->repeat_penalty;
+    a.top_k = p->top_k; a.top_p = p->top_p; a.min_p = p->min_p; a.temperature = p->temperature; a.u = u;
+    a.scratch = c->d_sample_row;
+    a.out = c->d_sample_tok + kMaxPenalty;
+    a.err = c->d_err;
+    const bool ok =
+        (a.n_pen == 0 || cuda_ok(c, cudaMemcpyAsync(c->d_sample_tok, p->penalty_tokens, sizeof(int32_t) * a.n_pen,
+                                                    cudaMemcpyHostToDevice, c->st), "copy")) &&
+        cuda_ok(c, cudaMemsetAsync(c->d_err, 0, sizeof(uint32_t), c->st), "memset") &&
+        (launch_sample(a, c->st) || (c->err = "sampler launch failed", false)) &&
+        cuda_ok(c, cudaMemcpyAsync(c->h_sample_tok, a.out, sizeof(int32_t), cudaMemcpyDeviceToHost, c->st), "copy") &&
+        cuda_ok(c, cudaMemcpyAsync(c->h_err, c->d_err, sizeof(uint32_t), cudaMemcpyDeviceToHost, c->st), "copy") &&
+        cuda_ok(c, cudaStreamSynchronize(c->st), "sampler");
+    if (!ok || *c->h_err != 0) return -1;
+    return *c->h_sample_tok;
+}
+
+int llm_debug_set_logits(llm_ctx* c, int32_t i, const float* row) {
+    if (!c || !row || c->host_only) return -1;
+    const int32_t j = resolve_row(c, i);
+    if (j < 0) return -1;
+    c->h_logits_valid = false;
+    return cuda_ok(c, cudaMemcpyAsync(c->d_logits + (size_t)j * c->hp.n_vocab, row, sizeof(float) * c->hp.n_vocab,
+                                      cudaMemcpyHostToDevice, c->st), "copy") &&
+                   cuda_ok(c, cudaStreamSynchronize(c->st), "copy")
+               ? 0 : -1;
 }
 
 int llm_debug_step_trace_enable(llm_ctx* c, int enable) {
