@@ -41,12 +41,46 @@ def decode_weight(raw: np.ndarray, wtype: int, ne0: int) -> np.ndarray:
     raise ValueError(f"unknown weight type {wtype}")
 
 
+def quantize_q8_0(x: np.ndarray) -> np.ndarray:
+    """Rows of values (last axis a whole number of 32-value blocks) -> Q8_0 rows (uint8,
+    [..., ne0/32*34]), the byte layout of [P2] Example 2: per block the fp16 scale d (2 bytes,
+    little-endian) then 32 int8 quants q.
+
+    The pages give the block layout and the way back (value = d * q), not the quantiser. Reading
+    taken: a symmetric absmax scale, so that the block's largest magnitude maps to +-127. The row a
+    cache write receives is float32, and the integer decisions are taken in float32:
+      amax = max |x| (float32), d = amax / 127 (float32 division), id = 1 / d (float32; 0 if d = 0),
+      q = x * id (float32 product) rounded to the nearest integer, halves away from zero,
+      stored d = d rounded to fp16 (nearest even).
+    """
+    x32 = np.asarray(x, dtype=np.float64).astype(np.float32)
+    assert x32.shape[-1] % QK8_0 == 0
+    lead = x32.shape[:-1]
+    b = x32.reshape(-1, x32.shape[-1] // QK8_0, QK8_0)
+    amax = np.max(np.abs(b), axis=2)                                   # float32, exact
+    d = (amax / np.float32(127.0)).astype(np.float32)
+    with np.errstate(divide="ignore"):
+        inv = np.where(d != 0, np.float32(1.0) / d, np.float32(0.0)).astype(np.float32)
+    y = (b * inv[:, :, None]).astype(np.float32).astype(np.float64)   # the float32 product, exactly
+    q = (np.sign(y) * np.floor(np.abs(y) + 0.5)).astype(np.int8)       # halves away from zero
+    out = np.empty(b.shape[:2] + (Q8_0_BYTES,), dtype=np.uint8)
+    out[:, :, 0:2] = d.astype(np.float16).view(np.uint8).reshape(b.shape[0], b.shape[1], 2)
+    out[:, :, 2:] = q.view(np.uint8)
+    return out.reshape(lead + (x32.shape[-1] // QK8_0 * Q8_0_BYTES,))
+
+
 def round_to_type(x: np.ndarray, t: int) -> np.ndarray:
-    """Value a cache row holds after a write of x in type t (round to nearest even), as float64."""
+    """Value a cache row holds after a write of x in type t, as float64: F32/F16 round to nearest
+    even; Q8_0 quantises each 32-value block (quantize_q8_0) and reads back d * q."""
     if t == F32:
         return x.astype(np.float32).astype(np.float64)
     if t == F16:
         return x.astype(np.float16).astype(np.float64)
+    if t == Q8_0:
+        x = np.asarray(x)
+        ne0 = x.shape[-1]
+        raw = quantize_q8_0(x).reshape(-1, ne0 // QK8_0 * Q8_0_BYTES)
+        return q8_0_to_f64(raw, ne0).reshape(x.shape)
     raise ValueError(f"unsupported cache type {t}")
 
 
