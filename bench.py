@@ -275,6 +275,8 @@ def main():
     ap.add_argument("--fused-step", action="store_true",
                     help="one-token steps as the single persistent step kernel instead of the "
                          "per-op kernel sequence (for comparison)")
+    ap.add_argument("--type-kv", default="", choices=["", "f32", "f16", "q8_0"],
+                    help="KV cache type instead of the workload's own (f16 unless it says otherwise)")
     ap.add_argument("--layers", type=int, default=0,
                     help="profiling aid: run the workload's shape with only this many layers "
                          "(a small case for ncu captures; not a bench number)")
@@ -288,9 +290,12 @@ def main():
     if args.layers:
         w = dataclasses.replace(w, hp=dataclasses.replace(w.hp, n_layer=args.layers))
         S.WORKLOADS[args.workload] = w
+    if args.type_kv:
+        w = dataclasses.replace(w, type_kv={"f32": 0, "f16": 1, "q8_0": 8}[args.type_kv])
+        S.WORKLOADS[args.workload] = w
     config = {"workload": args.workload, "description": w.description,
               "prompt_tokens": w.n_prompt, "decode_steps_timed": args.steps,
-              "n_ctx": w.n_ctx, "kv_cache": "f16" if w.type_kv == 1 else "f32",
+              "n_ctx": w.n_ctx, "kv_cache": {0: "f32", 1: "f16", 8: "q8_0"}[w.type_kv],
               "l2": "inputs larger than L2: every decode step streams all weights (no flush)",
               "parallelism": "replicas" if args.gpus > 1 else "single",
               "decode_path": "persistent step kernel" if args.fused_step else "per-op kernels (graph)"}

@@ -78,7 +78,10 @@ enum {
 
 /* Context parameters ([P1] Крок 9-10 context constructor; [P2] Example 9; [P4] コンテキストの構築).
  * n_ctx is rounded up to a multiple of 256; n_batch becomes min(n_ctx, n_batch) and n_ubatch
- * min(n_batch, n_ubatch). type_k / type_v: LLM_TYPE_F32 or LLM_TYPE_F16. stream: a cudaStream_t
+ * min(n_batch, n_ubatch). type_k / type_v: both LLM_TYPE_F32, both LLM_TYPE_F16, or both
+ * LLM_TYPE_Q8_0 ([P2] Memory Math: a q8_0 cache of 34 bytes per 32 values; [P4] type_k/type_v; each
+ * written row is quantised per 32-value block with d = max|x| / 127 and q = round(x / d), the
+ * decisions taken in float32; the fused persistent decode step takes F32/F16 only). stream: a cudaStream_t
  * the library launches all its work on (NULL = the library creates its own non-blocking stream).
  * The KV cache is unified: one set of n_ctx cells shared by all n_seq_max sequences. */
 typedef struct llm_cparams {
@@ -264,7 +267,9 @@ int llm_debug_capture(llm_ctx *ctx, int enable);
 /* Copy a captured intermediate of the last ubatch to host memory as float32, row-major
  * [n_tokens][width]. name: "embd" (layer ignored), "l_out" (residual stream after layer `layer`),
  * "attn_out" (attention output of layer `layer`, before the output projection), "kq_in" (the Q
- * rows after RoPE of layer `layer`), "result_norm" (final-normed output rows; present only when the
+ * rows after RoPE of layer `layer`), "k_in" / "v_in" (Q8_0 caches only: the float32 K rows after
+ * RoPE and the V rows, [n_tokens][n_head_kv * head_dim], that layer `layer` quantised into the
+ * cache), "result_norm" (final-normed output rows; present only when the
  * output matrix ran unfused, not in the one-token GEMV that normalises in its prologue). Returns the number
  * of floats available (0 if none), writes at most cap. */
 int64_t llm_debug_get_tensor(llm_ctx *ctx, const char *name, int32_t layer, float *out,
@@ -272,7 +277,8 @@ int64_t llm_debug_get_tensor(llm_ctx *ctx, const char *name, int32_t layer, floa
 
 /* Copy layer `layer`'s K cache (which = 0) or V cache (which = 1) to host memory as stored: type_k
  * / type_v elements laid out [n_head_kv][n_ctx][head_dim] (cell c of KV head g at (g * n_ctx + c)
- * * head_dim). out may be NULL to query the size. Returns the slab's size in bytes (copies at most
+ * * head_dim). A Q8_0 cache holds the int8 quants in that layout, followed by the fp16 scales
+ * [n_head_kv][n_ctx][head_dim / 32] (one per 32-value block; value = scale * quant). out may be NULL to query the size. Returns the slab's size in bytes (copies at most
  * cap_bytes, after the context's stream has finished), 0 for a bad layer/which or a host-only
  * context. */
 int64_t llm_debug_kv_raw(llm_ctx *ctx, int32_t layer, int32_t which, void *out, int64_t cap_bytes);

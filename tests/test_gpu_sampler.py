@@ -4,9 +4,10 @@ C ABI.
 Rows: the tiny model's own logits rows, and chosen rows written over an output row with the
 debug hook (ties at the top-k threshold, a flat row, NaN and -inf entries, 4096 candidates).
 The bar: the same token as the oracle on the same float32 row. The device works in float32 and
-the oracle in float64, so a case is compared only where no decision lies within 1e-4 of a
+the oracle in float64, so a case is compared only where no decision lies within 2e-5 of a
 boundary (the pick's cumulative weight against u, top-p's cumulative probability against p,
-min-p's log ratio against ln min_p); such near-ties are skipped and counted."""
+min-p's log ratio against ln min_p: float32 sums of up to 4096 terms stay well inside that);
+such near-ties are skipped, counted, and still must pick a candidate of the chain."""
 import math
 
 import numpy as np
@@ -17,7 +18,7 @@ from oracle.sampling import SamplerParams, chain_candidates, pick_margin, sample
 from tests import gpu_common as G
 
 pytestmark = pytest.mark.gpu
-EDGE = 1e-4
+EDGE = 2e-5
 
 PARAMS = [
     SamplerParams(top_k=40, temperature=0.0),
@@ -79,7 +80,7 @@ def test_sampler_matches_oracle_on_model_rows(ctx):
                     continue
                 assert got == want, (i, p, u, got, want)
                 compared += 1
-    assert compared >= 0.9 * (compared + skipped), (compared, skipped)
+    assert compared >= 0.8 * (compared + skipped), (compared, skipped)
 
 
 def test_greedy_equals_decode_argmax(ctx):

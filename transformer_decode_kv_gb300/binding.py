@@ -158,6 +158,7 @@ class Context:
         cp.stream = stream
         cp.flags = (CTX_HOST_ONLY if host_only else 0) | (CTX_FUSED_STEP if fused_step else 0)
         self.n_vocab = hp.n_vocab
+        self.type_k = type_k
         self.ptr = L.llm_ctx_init(C.byref(self._hp), C.byref(cp))
         if not self.ptr:
             raise LlmError("llm_ctx_init failed: " + L.llm_last_error(None).decode())
@@ -324,12 +325,19 @@ class Context:
 
     def kv_cache(self, layer: int, which: int) -> Optional[np.ndarray]:
         """Layer `layer`'s K (which 0) or V (which 1) cache as stored, [n_head_kv][n_ctx][head_dim]
-        (float32 or float16 elements)."""
+        (float32 or float16 elements). A Q8_0 cache comes back as its 34-byte blocks (fp16 scale,
+        then 32 int8 quants), uint8 [n_head_kv][n_ctx][head_dim / 32 * 34]."""
         n = lib().llm_debug_kv_raw(self.ptr, layer, which, None, 0)
         if n <= 0:
             return None
         out = np.zeros(n, dtype=np.uint8)
         lib().llm_debug_kv_raw(self.ptr, layer, which, out.ctypes.data_as(C.c_void_p), n)
+        Hkv, hd = self._hp.n_head_kv, self._hp.head_dim
+        if self.type_k == Q8_0:
+            nq = n // 34 * 32
+            q = out[:nq].reshape(Hkv, -1, hd // 32, 32)
+            s = out[nq:].reshape(Hkv, -1, hd // 32, 2)
+            return np.concatenate([s, q], axis=3).reshape(Hkv, -1, hd // 32 * 34)
         es = 4 if n // (self._hp.n_head_kv * self._hp.head_dim) == 4 * self.n_ctx else 2
         v = out.view(np.float32 if es == 4 else np.float16)
         return v.reshape(self._hp.n_head_kv, -1, self._hp.head_dim)

@@ -1,5 +1,6 @@
-// Device pieces shared by the attention kernels: the output store (float32, or bf16 hi + lo
-// terms for the tensor-core GEMM that follows) and the merge of split-K partial states.
+// Device pieces shared by the attention kernels: Q8_0 cache scales, the output store (float32, or
+// bf16 hi + lo terms for the tensor-core GEMM that follows) and the merge of split-K partial
+// states.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -12,6 +13,18 @@
 
 namespace llm {
 namespace attn {
+
+// A Q8_0 cache scale (fp16), read through L2: it may have been written by the previous kernel.
+__device__ __forceinline__ float ld_scale(const __half* p) {
+    return __half2float(__ushort_as_half(__ldcg(reinterpret_cast<const unsigned short*>(p))));
+}
+
+// The fp16 scales of KV head kvh in a Q8_0 layer cache (quants first, then the scales).
+__device__ __forceinline__ const __half* q8_scales(const void* layer, const AttnArgs& a, int kvh) {
+    return reinterpret_cast<const __half*>(static_cast<const uint8_t*>(layer) +
+                                           kv_q8_scale_offset(a.Hkv, a.n_ctx, a.hd)) +
+           (int64_t)kvh * a.n_ctx * (a.hd / 32);
+}
 
 __device__ __forceinline__ void store_out(const AttnArgs& a, int64_t oi, float v) {
     if (a.out_b) {

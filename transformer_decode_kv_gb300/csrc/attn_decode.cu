@@ -10,6 +10,10 @@
 // keeps each block's shared memory alive until its peers have read it. No global round trip
 // (fence, ticket, partial rows in L2) is on the merge path.
 //
+// A Q8_0 cache (int8 quants per row, one fp16 scale per 32 values in a separate array) is staged
+// as int8 rows plus float scales; a score sums each 32-value block's products, then scales the
+// block sum, and a value row's scale is folded into the probability of its cell.
+//
 // The K/V rows of cells written by earlier steps cannot change while the previous kernel (this
 // step's Q/K/V projection) runs, so the first pass stages them with cp.async before
 // griddepcontrol.wait; Q and this step's own cells are read after it.
@@ -38,6 +42,7 @@ constexpr int kGQ = 4;                   // query heads per KV head: one warp ea
 template <typename KT> __device__ __forceinline__ float kvf(KT v);
 template <> __device__ __forceinline__ float kvf<float>(float v) { return v; }
 template <> __device__ __forceinline__ float kvf<__half>(__half v) { return __half2float(v); }
+template <> __device__ __forceinline__ float kvf<int8_t>(int8_t v) { return (float)v; }
 
 __device__ __forceinline__ uint32_t sm32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -59,13 +64,18 @@ __device__ __forceinline__ float ld_peer(const float* local, uint32_t rank) {
     return v;
 }
 
+// KT = int8_t: a Q8_0 cache (int8 quants per row, one fp16 scale per 32 values kept apart)
 template <int HD, typename KT>
 struct DecSmem {
+    static constexpr bool Q8 = sizeof(KT) == 1;
+    static constexpr int NB = HD / 32;                    // Q8_0 blocks per row
     static constexpr int RB = HD * (int)sizeof(KT);       // bytes of a cached row
     static constexpr int RS = RB + 16;                    // padded stride
     static constexpr size_t bytes = 2 * (size_t)kCH * RS + (size_t)kGQ * HD * 4 /* q */ +
-                                    (size_t)kGQ * (HD + 2) * 4 /* partial */ + 3 * kCH * 4 + 16;
+                                    (size_t)kGQ * (HD + 2) * 4 /* partial */ + 3 * kCH * 4 +
+                                    (Q8 ? 2 * (size_t)kCH * NB * 4 : 0) /* scales */ + 16;
 };
+
 
 }  // namespace
 
@@ -73,7 +83,8 @@ template <int HD, typename KT>
 __global__ void __launch_bounds__(kGQ * 32)
 attn_decode_kernel(AttnArgs a, float scale_log2) {
     using SM = DecSmem<HD, KT>;
-    constexpr int RB = SM::RB, RS = SM::RS, VPR = RB / 16, DPL = HD / 32;
+    constexpr int RB = SM::RB, RS = SM::RS, VPR = RB / 16, DPL = HD / 32, NB = SM::NB;
+    constexpr bool Q8 = SM::Q8;
     extern __shared__ __align__(16) uint8_t sm[];
     uint8_t* kb = sm;                                          // [kCH][RS]
     uint8_t* vb = kb + kCH * RS;                               // [kCH][RS]
@@ -82,6 +93,8 @@ attn_decode_kernel(AttnArgs a, float scale_log2) {
     int* ccell = reinterpret_cast<int*>(pst + kGQ * (HD + 2)); // [kCH]
     int* cvis = ccell + kCH;                                   // [kCH]
     int* cfresh = cvis + kCH;                                  // [kCH]
+    float* ksc = reinterpret_cast<float*>(cfresh + kCH);       // Q8_0: [kCH][NB] K scales
+    float* vsc = ksc + kCH * NB;                               //        [kCH][NB] V scales
 
     const uint32_t rank = cluster_rank();
     const int kvh = blockIdx.y, tile = blockIdx.z;
@@ -98,6 +111,15 @@ attn_decode_kernel(AttnArgs a, float scale_log2) {
     const int c0 = min(len, (int)rank * chunk), c1 = min(len, c0 + chunk);
     const uint8_t* K = static_cast<const uint8_t*>(a.kc) + (int64_t)kvh * a.n_ctx * RB;
     const uint8_t* V = static_cast<const uint8_t*>(a.vc) + (int64_t)kvh * a.n_ctx * RB;
+    const __half* KS = q8_scales(a.kc, a, kvh);
+    const __half* VS = q8_scales(a.vc, a, kvh);
+    auto load_scales = [&](int c, int cell) {
+#pragma unroll
+        for (int b = 0; b < NB; ++b) {
+            ksc[c * NB + b] = ld_scale(KS + (int64_t)cell * NB + b);
+            vsc[c * NB + b] = ld_scale(VS + (int64_t)cell * NB + b);
+        }
+    };
 
     float m = -INFINITY, l = 0.f, o[DPL];
 #pragma unroll
@@ -119,6 +141,9 @@ attn_decode_kernel(AttnArgs a, float scale_log2) {
             ccell[threadIdx.x] = cell;
             cvis[threadIdx.x] = vis && cell >= 0;
             cfresh[threadIdx.x] = fresh;
+            if constexpr (Q8) {
+                if (vis && cell >= 0 && !fresh) load_scales(threadIdx.x, cell);
+            }
         }
         __syncthreads();
         // rows of earlier steps: staged now, possibly before the previous kernel has ended
@@ -137,6 +162,10 @@ attn_decode_kernel(AttnArgs a, float scale_log2) {
                 qs[i] = a.q[(int64_t)t * a.ldq + (kvh * kGQ + i / HD) * HD + i % HD] * scale_log2;
         }
         // rows written by this step's projection kernel: only now
+        if constexpr (Q8) {
+            if (threadIdx.x < kCH && cvis[threadIdx.x] && cfresh[threadIdx.x])
+                load_scales(threadIdx.x, ccell[threadIdx.x]);
+        }
         for (int v = threadIdx.x; v < kCH * VPR; v += blockDim.x) {
             const int c = v / VPR, j = v % VPR;
             if (!cvis[c] || !cfresh[c]) continue;
@@ -154,7 +183,27 @@ attn_decode_kernel(AttnArgs a, float scale_log2) {
         for (int h2 = 0; h2 < 2; ++h2) {
             const int c = lane + 32 * h2;
             s[h2] = -INFINITY;
-            if (cvis[c]) {
+            if (Q8 && cvis[c]) {
+                const uint8_t* kr = kb + c * RS;
+                float acc = 0.f;
+#pragma unroll
+                for (int b = 0; b < NB; ++b) {
+                    float p0 = 0.f, p1 = 0.f;
+#pragma unroll
+                    for (int jj = 0; jj < 2; ++jj) {
+                        const int j = 2 * b + jj;
+                        const uint4 kv = *reinterpret_cast<const uint4*>(kr + j * 16);
+                        const int8_t* ke = reinterpret_cast<const int8_t*>(&kv);
+#pragma unroll
+                        for (int e = 0; e < 16; e += 2) {
+                            p0 = fmaf(q[j * 16 + e], (float)ke[e], p0);
+                            p1 = fmaf(q[j * 16 + e + 1], (float)ke[e + 1], p1);
+                        }
+                    }
+                    acc = fmaf(ksc[c * NB + b], p0 + p1, acc);
+                }
+                s[h2] = acc;
+            } else if (cvis[c]) {
                 const uint8_t* kr = kb + c * RS;
                 float a0 = 0.f, a1 = 0.f;
 #pragma unroll
@@ -191,8 +240,9 @@ attn_decode_kernel(AttnArgs a, float scale_log2) {
             const float pc = __shfl_sync(0xffffffffu, p[c >> 5], c & 31);
             if (pc == 0.f) continue;
             const KT* vr = reinterpret_cast<const KT*>(vb + c * RS) + lane * DPL;
+            const float pd = Q8 ? pc * vsc[c * NB + lane * DPL / 32] : pc;
 #pragma unroll
-            for (int e = 0; e < DPL; ++e) o[e] = fmaf(pc, kvf<KT>(vr[e]), o[e]);
+            for (int e = 0; e < DPL; ++e) o[e] = fmaf(pd, kvf<KT>(vr[e]), o[e]);
         }
         __syncthreads();
     }
@@ -260,6 +310,14 @@ bool attention_decode_ok(const AttnArgs& a) {
 }
 
 bool launch_attention_decode(const AttnArgs& a, cudaStream_t st) {
+    if (a.kv_type == W_Q8_0) {
+        switch (a.hd) {
+            case 32: return launch_dec<32, int8_t>(a, st);
+            case 64: return launch_dec<64, int8_t>(a, st);
+            case 128: return launch_dec<128, int8_t>(a, st);
+        }
+        return false;
+    }
     const bool f32 = a.kv_type == W_F32;
     switch (a.hd) {
         case 32: return f32 ? launch_dec<32, float>(a, st) : launch_dec<32, __half>(a, st);

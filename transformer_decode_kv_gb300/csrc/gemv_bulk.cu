@@ -417,7 +417,7 @@ gemv_bulk_kernel(const GemvArgs a) {
                 dst[0] = y0; dst[1] = y1;
                 continue;
             }
-            const int32_t cell = a.slot[t];
+            const int32_t cell = a.slot ? a.slot[t] : t;
             if (cell < 0 || cell >= a.n_ctx) { atomicOr(a.err, ERR_SLOT_RANGE); continue; }
             const bool is_k = head < a.H + a.Hkv;
             const int g = is_k ? head - a.H : head - a.H - a.Hkv;

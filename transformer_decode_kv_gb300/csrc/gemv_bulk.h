@@ -14,7 +14,7 @@ enum GemvEpi : int32_t {
     GEPI_STORE = 0,    // y[t][m] = acc
     GEPI_ADD = 1,      // y[t][m] += acc (residual)
     GEPI_SWIGLU = 2,   // y[t][j] = silu(acc_gate) * acc_up; W rows [row0, row0+F) gate, +F up
-    GEPI_QKV = 3,      // RoPE on Q/K rows, Q -> y, K/V -> cache cells slot[t]
+    GEPI_QKV = 3,      // RoPE on Q/K rows, Q -> y, K/V -> cache cells slot[t] (cell t if slot is null)
     GEPI_LOGITS = 4,   // y[t][m] = acc and amax[t] = max packed (value, lowest index)
 };
 

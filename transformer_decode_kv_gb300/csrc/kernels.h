@@ -38,6 +38,21 @@ void launch_rmsnorm_bf16(const float* x, const int32_t* rows, int32_t R, int32_t
 void launch_rope_kv_append(float* qkv, int32_t T, int32_t H, int32_t Hkv, int32_t hd,
                            const float2* cs, const int32_t* slot, void* kc, void* vc,
                            int32_t n_ctx, int32_t kv_type, uint32_t* err, cudaStream_t st);
+// With slot == nullptr token t's rows go to cell t (a float32 staging area of n_ctx rows per
+// head, from which launch_kv_quant_q8 fills a Q8_0 cache).
+// Q8_0 cache rows from float32 staging rows sk / sv [Hkv][ld][hd] (token t at row t of each
+// head): per 32-value block d = max|x| / 127, q = x * (1 / d) rounded half away from zero, all in
+// float32, d stored as fp16 ([P2] Example 2 block: fp16 scale and 32 int8 quants, value d * q).
+// The Q8_0 cache of one layer: int8 quants [Hkv][n_ctx][hd], then fp16 scales
+// [Hkv][n_ctx][hd / 32] (kv_q8_scale_offset bytes after the quants). A slot outside [0, n_ctx)
+// skips the write and sets ERR_SLOT_RANGE. With pdl the kernel may start while the previous one
+// runs and waits for it before reading the staging rows.
+void launch_kv_quant_q8(const float* sk, const float* sv, int32_t ld, int32_t T, int32_t Hkv,
+                        int32_t hd, const int32_t* slot, void* kc, void* vc, int32_t n_ctx,
+                        uint32_t* err, cudaStream_t st, bool pdl);
+__host__ __device__ inline size_t kv_q8_scale_offset(int32_t Hkv, int32_t n_ctx, int32_t hd) {
+    return (size_t)Hkv * (size_t)n_ctx * (size_t)hd;
+}
 // u[t][j] = silu(g[t][j]) * up[t][j] with gu = [T][2F] (gate then up) -> u [T][F].
 void launch_swiglu(const float* gu, int32_t T, int32_t F, float* u, cudaStream_t st);
 // amax[r] = the largest logit of row r packed with its index (value in the high word in an

@@ -33,6 +33,7 @@ constexpr int kBC = 32;                  // cells per shared-memory tile (one pe
 template <typename KT> __device__ __forceinline__ float kv_to_f(KT v);
 template <> __device__ __forceinline__ float kv_to_f<float>(float v) { return v; }
 template <> __device__ __forceinline__ float kv_to_f<__half>(__half v) { return __half2float(v); }
+template <> __device__ __forceinline__ float kv_to_f<int8_t>(int8_t v) { return (float)v; }
 
 template <int HD, int TQ, int G>
 struct AttnSmem {
@@ -76,6 +77,9 @@ attn_kernel(AttnArgs a, float scale_log2) {
     const int nq = td0.z, s0 = td0.y, c0 = wd.y, c1 = wd.z, base = td1.y;
     const KT* K = static_cast<const KT*>(a.kc) + (int64_t)kvh * a.n_ctx * HD;
     const KT* V = static_cast<const KT*>(a.vc) + (int64_t)kvh * a.n_ctx * HD;
+    constexpr bool Q8 = sizeof(KT) == 1;           // Q8_0: int8 quants and fp16 scales per 32 values
+    const __half* KS = Q8 ? q8_scales(a.kc, a, kvh) : nullptr;
+    const __half* VS = Q8 ? q8_scales(a.vc, a, kvh) : nullptr;
     asm volatile("griddepcontrol.wait;" ::: "memory");
 
     for (int idx = threadIdx.x; idx < R * HD; idx += blockDim.x) {
@@ -123,16 +127,26 @@ attn_kernel(AttnArgs a, float scale_log2) {
             const int c = v / VPR, j = v % VPR;
             const int cell = ccell[c];
             uint4 kq = make_uint4(0u, 0u, 0u, 0u), vq = kq;
+            float dk = 1.f, dv = 1.f;
             if (cell >= 0) {
                 kq = __ldg(reinterpret_cast<const uint4*>(K + (int64_t)cell * HD) + j);
                 vq = __ldg(reinterpret_cast<const uint4*>(V + (int64_t)cell * HD) + j);
+                if constexpr (Q8) {                  // 16 quants: half of one 32-value block
+                    dk = ld_scale(KS + (int64_t)cell * (HD / 32) + j / 2);
+                    dv = ld_scale(VS + (int64_t)cell * (HD / 32) + j / 2);
+                }
             }
             const KT* ke = reinterpret_cast<const KT*>(&kq);
             const KT* ve = reinterpret_cast<const KT*>(&vq);
 #pragma unroll
             for (int e = 0; e < EPV; ++e) {
-                ks[c * (HD + 1) + j * EPV + e] = kv_to_f<KT>(ke[e]);
-                vs[c * HD + j * EPV + e] = kv_to_f<KT>(ve[e]);
+                if constexpr (Q8) {
+                    ks[c * (HD + 1) + j * EPV + e] = dk * kv_to_f<KT>(ke[e]);
+                    vs[c * HD + j * EPV + e] = dv * kv_to_f<KT>(ve[e]);
+                } else {
+                    ks[c * (HD + 1) + j * EPV + e] = kv_to_f<KT>(ke[e]);
+                    vs[c * HD + j * EPV + e] = kv_to_f<KT>(ve[e]);
+                }
             }
         }
         __syncthreads();
@@ -446,6 +460,11 @@ bool launch_tq(const AttnArgs& a, cudaStream_t st) {
         cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         return cudaLaunchKernelEx(&cfg, k, a, scale_log2) == cudaSuccess;
     }
+    if (a.kv_type == W_Q8_0) {
+        auto k = attn_kernel<HD, TQ, G, int8_t>;
+        cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        return cudaLaunchKernelEx(&cfg, k, a, scale_log2) == cudaSuccess;
+    }
     auto k = attn_kernel<HD, TQ, G, __half>;
     cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     return cudaLaunchKernelEx(&cfg, k, a, scale_log2) == cudaSuccess;
@@ -455,7 +474,7 @@ template <int HD, int G>
 bool launch_hd_g(const AttnArgs& a, cudaStream_t st) {
     if (a.max_nq <= 1) {
         if (a.slot && attention_decode_ok(a)) return launch_attention_decode(a, st);
-        return a.slot ? launch_step<HD, G>(a, st) : launch_tq<HD, 1, G>(a, st);
+        return a.slot && a.kv_type != W_Q8_0 ? launch_step<HD, G>(a, st) : launch_tq<HD, 1, G>(a, st);
     }
     if (attention_mma_ok(a)) return launch_attention_mma(a, st);
     return launch_tq<HD, kAttnTileQ, G>(a, st);

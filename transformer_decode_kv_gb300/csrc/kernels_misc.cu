@@ -75,7 +75,7 @@ __global__ void rope_kv_append_kernel(float* __restrict__ qkv, int H, int Hkv, i
     const int half = hd / 2;
     const int width = (H + 2 * Hkv) * hd;
     float* row = qkv + (int64_t)t * width;
-    const int32_t c = slot[t];
+    const int32_t c = slot ? slot[t] : t;
     const bool ok = c >= 0 && c < n_ctx;
     if (!ok && threadIdx.x == 0) atomicOr(err, ERR_SLOT_RANGE);
     const float2* cst = cs + (int64_t)t * half;
@@ -101,6 +101,39 @@ __global__ void rope_kv_append_kernel(float* __restrict__ qkv, int H, int Hkv, i
     for (int j = threadIdx.x; j < Hkv * hd; j += blockDim.x) {
         const int g = j / hd, d = j % hd;
         vc[((int64_t)g * n_ctx + c) * hd + d] = to_kv<KT>(v[j]);
+    }
+}
+
+// One warp per 32-value block; blockIdx.y = token, blockIdx.z = 0 for K, 1 for V.
+__global__ void kv_quant_q8_kernel(const float* __restrict__ sk, const float* __restrict__ sv, int ld,
+                                   int Hkv, int hd, const int32_t* __restrict__ slot,
+                                   int8_t* __restrict__ kc, int8_t* __restrict__ vc, int n_ctx,
+                                   uint32_t* err) {
+    if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;");
+    const int nb = hd / 32;
+    const int blk = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    const int t = blockIdx.y;
+    const bool is_v = blockIdx.z != 0;
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (blk >= Hkv * nb) return;                                  // whole warp
+    const int g = blk / nb, b = blk % nb;
+    const int32_t cell = slot[t];
+    if (cell < 0 || cell >= n_ctx) {
+        if (lane == 0 && b == 0 && g == 0 && !is_v) atomicOr(err, ERR_SLOT_RANGE);
+        return;
+    }
+    const float x = (is_v ? sv : sk)[((int64_t)g * ld + t) * hd + b * 32 + lane];
+    float amax = fabsf(x);
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    const float d = __fdiv_rn(amax, 127.0f);
+    const float id = d != 0.0f ? __frcp_rn(d) : 0.0f;
+    const float qf = roundf(__fmul_rn(x, id));                    // halves away from zero
+    int8_t* q = is_v ? vc : kc;
+    q[((int64_t)g * n_ctx + cell) * hd + b * 32 + lane] = (int8_t)(int)qf;
+    if (lane == 0) {
+        __half* s = reinterpret_cast<__half*>(q + kv_q8_scale_offset(Hkv, n_ctx, hd));
+        s[((int64_t)g * n_ctx + cell) * nb + b] = __float2half_rn(d);
     }
 }
 
@@ -208,6 +241,25 @@ void launch_rope_kv_append(float* qkv, int32_t T, int32_t H, int32_t Hkv, int32_
     else
         rope_kv_append_kernel<__half><<<T, 256, 0, st>>>(qkv, H, Hkv, hd, cs, slot, (__half*)kc,
                                                         (__half*)vc, n_ctx, err);
+}
+
+void launch_kv_quant_q8(const float* sk, const float* sv, int32_t ld, int32_t T, int32_t Hkv,
+                        int32_t hd, const int32_t* slot, void* kc, void* vc, int32_t n_ctx,
+                        uint32_t* err, cudaStream_t st, bool pdl) {
+    if (T <= 0) return;
+    constexpr int kWarps = 8;
+    const int nblk = Hkv * (hd / 32);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((nblk + kWarps - 1) / kWarps), (unsigned)T, 2);
+    cfg.blockDim = dim3(kWarps * 32);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    cudaLaunchKernelEx(&cfg, kv_quant_q8_kernel, sk, sv, (int)ld, (int)Hkv, (int)hd, slot,
+                       static_cast<int8_t*>(kc), static_cast<int8_t*>(vc), (int)n_ctx, err);
 }
 
 void launch_swiglu(const float* gu, int32_t T, int32_t F, float* u, cudaStream_t st) {

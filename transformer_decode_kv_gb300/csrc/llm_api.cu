@@ -109,9 +109,10 @@ struct llm_ctx {
     bool embd_loaded = false, out_loaded = false, out_norm_loaded = false, ready = false;
     std::vector<void*> allocs;
 
-    // KV cache: K and V each [n_layer][Hkv][n_ctx][hd]
+    // KV cache: K and V each [n_layer][Hkv][n_ctx][hd] (Q8_0: per layer the quants, then the scales)
     void* kv_k = nullptr;
     void* kv_v = nullptr;
+    float* kv_stage = nullptr;                 // Q8_0: this ubatch's K and V rows, [2][Hkv][n_ubatch][hd]
     KvCells cells;
 
     // scratch for one ubatch
@@ -155,6 +156,7 @@ struct llm_ctx {
     float *dbg_embd = nullptr, *dbg_lout = nullptr, *dbg_attn = nullptr, *dbg_q = nullptr;
     bool dbg_rnorm_valid = false;   // the final-normed rows exist only on the unfused output path
     float* dbg_rnorm = nullptr;
+    float *dbg_kin = nullptr, *dbg_vin = nullptr;   // Q8_0 cache: the float32 K/V rows it was given
     int32_t dbg_T = 0, dbg_O = 0;
     int32_t fault_kind = 0, fault_ub = -1;
     llm_perf_data perf{};
@@ -191,6 +193,12 @@ struct llm_ctx {
     int32_t qkv_width() const { return (hp.n_head + 2 * hp.n_head_kv) * hp.head_dim; }
     int32_t q_width() const { return hp.n_head * hp.head_dim; }
     size_t kv_layer_elems() const { return (size_t)hp.n_head_kv * n_ctx * hp.head_dim; }
+    bool kv_q8() const { return type_k == LLM_TYPE_Q8_0; }
+    // bytes of one layer's K (or V) cache: Q8_0 keeps int8 quants, then one fp16 scale per 32 values
+    size_t kv_layer_bytes() const {
+        return kv_q8() ? kv_layer_elems() / 32 * 34 : kv_layer_elems() * type_size(type_k);
+    }
+    double kv_value_bytes() const { return kv_q8() ? 34.0 / 32.0 : (double)type_size(type_k); }
 };
 
 namespace {
@@ -392,7 +400,7 @@ void put(int32_t* base, size_t off, const std::vector<int32_t>& v) {
 void attention_work(llm_ctx* c, const int32_t* pos) {
     const AttnPlan& p = c->plan;
     const llm_hparams& hp = c->hp;
-    const double kv_es = (double)type_size(c->type_k);
+    const double kv_es = c->kv_value_bytes();
     double by = 0, fl = 0;
     for (int32_t t = 0; t < p.n_tiles(); ++t) {
         const int32_t l = p.tile_list[t];
@@ -452,7 +460,11 @@ bool forward_ubatch(llm_ctx* c, int32_t T, int32_t O, int32_t out_row0, int32_t 
     const int32_t d = hp.n_embd, H = hp.n_head, Hkv = hp.n_head_kv, hd = hp.head_dim, F = hp.n_ff;
     const int32_t* din = c->d_in;
     const int32_t *tok = din + io.tok, *pos = din + io.pos, *slot = din + io.slot;
-    const size_t kv_es = type_size(c->type_k);
+    const double kv_es = c->kv_value_bytes();
+    const bool q8 = c->kv_q8();
+    const int32_t U = c->n_ubatch;
+    float* stage_k = c->kv_stage;
+    float* stage_v = q8 ? c->kv_stage + (size_t)Hkv * U * hd : nullptr;
     const bool gemv = T <= gemv_max_tokens();
     const int32_t lin_cls = gemv ? KC_LINEAR_GEMV : (c->tc_ok ? KC_LINEAR_TC : KC_LINEAR_GEMM);
     const double Td = T, Od = O;
@@ -528,8 +540,8 @@ bool forward_ubatch(llm_ctx* c, int32_t T, int32_t O, int32_t out_row0, int32_t 
     auto bulk_fail = [&]() { c->err = "decode GEMV launch failed"; return false; };
     for (int32_t il = 0; il < hp.n_layer; ++il) {
         Layer& L = c->layers[il];
-        void* kc = static_cast<uint8_t*>(c->kv_k) + (size_t)il * c->kv_layer_elems() * kv_es;
-        void* vc = static_cast<uint8_t*>(c->kv_v) + (size_t)il * c->kv_layer_elems() * kv_es;
+        void* kc = static_cast<uint8_t*>(c->kv_k) + (size_t)il * c->kv_layer_bytes();
+        void* vc = static_cast<uint8_t*>(c->kv_v) + (size_t)il * c->kv_layer_bytes();
         // ---- attention norm, Q/K/V, RoPE, K/V append
         if (bulk.qkv) {
             k = kt_begin(c);
@@ -538,9 +550,17 @@ bool forward_ubatch(llm_ctx* c, int32_t T, int32_t O, int32_t out_row0, int32_t 
             g.y = c->qkv; g.ldy = qkvw;
             g.H = H; g.Hkv = Hkv; g.hd = hd; g.n_ctx = c->n_ctx; g.kv_type = c->type_k;
             g.cs = c->rope_cs; g.slot = slot; g.kc = kc; g.vc = vc;
+            if (q8) {                               // float32 rows to the staging area, cell = token
+                g.kv_type = W_F32; g.n_ctx = U; g.slot = nullptr; g.kc = stage_k; g.vc = stage_v;
+            }
             if (!launch_gemv_bulk(L.qkv.type, g, GEPI_QKV, true, c->n_sm, st, pdl)) return bulk_fail();
-            kt_end(c, k, lin_cls, wbytes(L.qkv, qkvw) + Td * (d * 4.0 + qw * 4.0 + 2.0 * Hkv * hd * kv_es),
+            kt_end(c, k, lin_cls, wbytes(L.qkv, qkvw) + Td * (d * 4.0 + qw * 4.0 + 2.0 * Hkv * hd * (q8 ? 4.0 : kv_es)),
                    2.0 * Td * qkvw * d);
+            if (q8) {
+                k = kt_begin(c);
+                launch_kv_quant_q8(stage_k, stage_v, U, T, Hkv, hd, slot, kc, vc, c->n_ctx, c->d_err, st, pdl);
+                kt_end(c, k, KC_ROPE_KV, Td * 2.0 * Hkv * hd * (4.0 + kv_es), 0);
+            }
         } else {
             k = kt_begin(c);
             if (tc) launch_rmsnorm_bf16(c->x, nullptr, T, d, L.attn_norm, hp.rms_eps, c->hb, c->hb_lo, st);
@@ -551,9 +571,26 @@ bool forward_ubatch(llm_ctx* c, int32_t T, int32_t O, int32_t out_row0, int32_t 
             else launch_linear(L.qkv, 0, qkvw, c->h, d, T, c->qkv, qkvw, EPI_STORE, st);
             kt_end(c, k, lin_cls, wbytes(L.qkv, qkvw) + Td * (d + qkvw) * 4.0, 2.0 * Td * qkvw * d);
             k = kt_begin(c);
-            launch_rope_kv_append(c->qkv, T, H, Hkv, hd, c->rope_cs, slot, kc, vc, c->n_ctx,
-                                  c->type_k, c->d_err, st);
+            if (q8) {
+                launch_rope_kv_append(c->qkv, T, H, Hkv, hd, c->rope_cs, nullptr, stage_k, stage_v, U,
+                                      W_F32, c->d_err, st);
+                launch_kv_quant_q8(stage_k, stage_v, U, T, Hkv, hd, slot, kc, vc, c->n_ctx, c->d_err, st, false);
+            } else {
+                launch_rope_kv_append(c->qkv, T, H, Hkv, hd, c->rope_cs, slot, kc, vc, c->n_ctx,
+                                      c->type_k, c->d_err, st);
+            }
             kt_end(c, k, KC_ROPE_KV, Td * ((double)qkvw * 4.0 + qw * 4.0 + 2.0 * Hkv * hd * kv_es), 0);
+        }
+        if (c->debug && q8) {                       // staging [Hkv][U][hd] -> [T][Hkv * hd]
+            const size_t kw = (size_t)Hkv * hd;
+            for (int32_t g2 = 0; g2 < Hkv; ++g2) {
+                cudaMemcpy2DAsync(c->dbg_kin + (size_t)il * T * kw + (size_t)g2 * hd, sizeof(float) * kw,
+                                  stage_k + (size_t)g2 * U * hd, sizeof(float) * hd, sizeof(float) * hd, T,
+                                  cudaMemcpyDeviceToDevice, st);
+                cudaMemcpy2DAsync(c->dbg_vin + (size_t)il * T * kw + (size_t)g2 * hd, sizeof(float) * kw,
+                                  stage_v + (size_t)g2 * U * hd, sizeof(float) * hd, sizeof(float) * hd, T,
+                                  cudaMemcpyDeviceToDevice, st);
+            }
         }
         // ---- attention over the cache
         a.kc = kc;
@@ -713,8 +750,9 @@ llm_ctx* llm_ctx_init(const llm_hparams* hp, const llm_cparams* cp) {
     if (!(h.rms_eps >= 0.f) || !(h.rope_freq_base > 0.f)) return fail("bad rms_eps / rope_freq_base");
     if (cp->n_ctx == 0 || cp->n_batch == 0 || cp->n_ubatch == 0) return fail("zero context size");
     if (cp->n_seq_max < 1 || cp->n_seq_max > (uint32_t)kMaxSeq) return fail("n_seq_max out of range");
-    if ((cp->type_k != LLM_TYPE_F32 && cp->type_k != LLM_TYPE_F16) || cp->type_v != cp->type_k)
-        return fail("type_k/type_v must both be F32 or both F16");
+    if ((cp->type_k != LLM_TYPE_F32 && cp->type_k != LLM_TYPE_F16 && cp->type_k != LLM_TYPE_Q8_0) ||
+        cp->type_v != cp->type_k)
+        return fail("type_k/type_v must both be F32, both F16 or both Q8_0");
     if (cp->n_ctx > (1u << 24)) return fail("n_ctx too large");
 
     auto* c = new llm_ctx();
@@ -746,9 +784,10 @@ llm_ctx* llm_ctx_init(const llm_hparams* hp, const llm_cparams* cp) {
     }
     const int64_t U = c->n_ubatch, d = h.n_embd;
     const int G = h.n_head / h.n_head_kv;
-    const size_t kv_elems = (size_t)h.n_layer * c->kv_layer_elems();
-    bool ok = dalloc(c, reinterpret_cast<uint8_t**>(&c->kv_k), kv_elems * type_size(c->type_k)) &&
-              dalloc(c, reinterpret_cast<uint8_t**>(&c->kv_v), kv_elems * type_size(c->type_v)) &&
+    const size_t kv_bytes = (size_t)h.n_layer * c->kv_layer_bytes();
+    bool ok = dalloc(c, reinterpret_cast<uint8_t**>(&c->kv_k), kv_bytes) &&
+              dalloc(c, reinterpret_cast<uint8_t**>(&c->kv_v), kv_bytes) &&
+              (!c->kv_q8() || dalloc(c, &c->kv_stage, 2 * (size_t)h.n_head_kv * U * h.head_dim)) &&
               dalloc(c, &c->x, U * d) && dalloc(c, &c->h, U * d) &&
               dalloc(c, &c->qkv, U * c->qkv_width()) && dalloc(c, &c->attn, U * c->q_width()) &&
               dalloc(c, &c->u, U * h.n_ff) && dalloc(c, &c->tmp, U * 2 * (int64_t)h.n_ff) &&
@@ -787,8 +826,8 @@ llm_ctx* llm_ctx_init(const llm_hparams* hp, const llm_cparams* cp) {
          ensure_inputs(c, 2 * (size_t)c->n_ctx);
     if (!ok) return die("");
     // KV cells start zeroed so an unwritten cell never holds NaN bit patterns
-    ok = cuda_ok(c, cudaMemsetAsync(c->kv_k, 0, kv_elems * type_size(c->type_k), c->st), "memset") &&
-         cuda_ok(c, cudaMemsetAsync(c->kv_v, 0, kv_elems * type_size(c->type_v), c->st), "memset") &&
+    ok = cuda_ok(c, cudaMemsetAsync(c->kv_k, 0, kv_bytes, c->st), "memset") &&
+         cuda_ok(c, cudaMemsetAsync(c->kv_v, 0, kv_bytes, c->st), "memset") &&
          cuda_ok(c, cudaStreamSynchronize(c->st), "sync");
     if (!ok) return die("");
     return c;
@@ -910,14 +949,13 @@ static void setup_step(llm_ctx* c) {
         return;
     }
     std::vector<StepLayer> t(h.n_layer);
-    const size_t kv_es = type_size(c->type_k);
     double wb = wbytes(c->out, h.n_vocab);
     for (int32_t il = 0; il < h.n_layer; ++il) {
         const Layer& L = c->layers[il];
         t[il].qkv = L.qkv.data; t[il].wo = L.wo.data; t[il].gu = L.gu.data; t[il].down = L.down.data;
         t[il].attn_norm = L.attn_norm; t[il].ffn_norm = L.ffn_norm;
-        t[il].kc = static_cast<uint8_t*>(c->kv_k) + (size_t)il * c->kv_layer_elems() * kv_es;
-        t[il].vc = static_cast<uint8_t*>(c->kv_v) + (size_t)il * c->kv_layer_elems() * kv_es;
+        t[il].kc = static_cast<uint8_t*>(c->kv_k) + (size_t)il * c->kv_layer_bytes();
+        t[il].vc = static_cast<uint8_t*>(c->kv_v) + (size_t)il * c->kv_layer_bytes();
         wb += wbytes(L.qkv, c->qkv_width()) + wbytes(L.wo, h.n_embd) + wbytes(L.gu, 2 * (int64_t)h.n_ff) +
               wbytes(L.down, h.n_embd);
     }
@@ -1296,7 +1334,9 @@ int llm_debug_capture(llm_ctx* c, int enable) {
     const int64_t U = c->n_ubatch, d = c->hp.n_embd, L = c->hp.n_layer, qw = c->q_width();
     const bool ok = dalloc(c, &c->dbg_embd, U * d) && dalloc(c, &c->dbg_lout, L * U * d) &&
                     dalloc(c, &c->dbg_attn, L * U * qw) && dalloc(c, &c->dbg_q, L * U * qw) &&
-                    dalloc(c, &c->dbg_rnorm, U * d);
+                    dalloc(c, &c->dbg_rnorm, U * d) &&
+                    (!c->kv_q8() || (dalloc(c, &c->dbg_kin, L * U * c->hp.n_head_kv * c->hp.head_dim) &&
+                                     dalloc(c, &c->dbg_vin, L * U * c->hp.n_head_kv * c->hp.head_dim)));
     return ok ? 0 : -2;
 }
 
@@ -1312,6 +1352,11 @@ int64_t llm_debug_get_tensor(llm_ctx* c, const char* name, int32_t layer, float*
         if (n == "l_out") { src = c->dbg_lout + layer * T * d; cnt = T * d; }
         else if (n == "attn_out") { src = c->dbg_attn + layer * T * qw; cnt = T * qw; }
         else if (n == "kq_in") { src = c->dbg_q + layer * T * qw; cnt = T * qw; }
+        else if ((n == "k_in" || n == "v_in") && c->dbg_kin) {
+            const int64_t kw = (int64_t)c->hp.n_head_kv * c->hp.head_dim;
+            src = (n == "k_in" ? c->dbg_kin : c->dbg_vin) + layer * T * kw;
+            cnt = T * kw;
+        }
     }
     if (!src) return 0;
     if (out && cap > 0) {
@@ -1324,8 +1369,7 @@ int64_t llm_debug_get_tensor(llm_ctx* c, const char* name, int32_t layer, float*
 int64_t llm_debug_kv_raw(llm_ctx* c, int32_t layer, int32_t which, void* out, int64_t cap_bytes) {
     if (!c || c->host_only || layer < 0 || layer >= c->hp.n_layer || (which != 0 && which != 1))
         return 0;
-    const size_t es = type_size(which == 0 ? c->type_k : c->type_v);
-    const int64_t n = (int64_t)(c->kv_layer_elems() * es);
+    const int64_t n = (int64_t)c->kv_layer_bytes();
     if (out && cap_bytes > 0) {
         const uint8_t* src = static_cast<const uint8_t*>(which == 0 ? c->kv_k : c->kv_v) + (size_t)layer * n;
         cudaStreamSynchronize(c->st);
