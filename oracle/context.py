@@ -140,6 +140,23 @@ class OracleContext:
     def seq_rm(self, s: int, p0: int, p1: int) -> bool:
         return self.cells.seq_rm(s, p0, p1)
 
+    def memory_update(self, optimize: bool) -> bool:
+        """llama_memory_i::update ([P4] KVキャッシュの詳細: with optimize=true the cache is
+        defragmented, cells moved to close the gaps, the K/V rows moving with their cells).
+        Returns True if any cell moved."""
+        if not optimize:
+            return False
+        order = self.cells.defrag_order()
+        if np.array_equal(order, np.arange(len(order))):
+            return False
+        self.cells.move(order)
+        for il in range(len(self.K)):
+            for X in (self.K, self.V):
+                moved = np.zeros_like(X[il])
+                moved[:len(order)] = X[il][order]
+                X[il] = moved
+        return True
+
     # ---- outputs ([P1] Крок 14) ----
     def _reset_outputs(self, n_tokens: int):
         self.output_ids = np.full(n_tokens, -1, dtype=np.int64)
@@ -176,15 +193,13 @@ class OracleContext:
         if b is None:
             return int(DecodeStatus.INVALID_BATCH)
         ubatches = split_simple(b.n_tokens, self.n_ubatch)
-        # find a slot for every ubatch before committing any ([P1] Крок 12)
-        work = self.cells.copy()
-        slots_all = []
-        for ub in ubatches:
-            sl = work.find_slots(len(ub))
-            if sl is None:
-                return int(DecodeStatus.NO_KV_SLOT)
-            work.apply(sl, b.pos[list(ub)], [b.seq_id[i] for i in ub])
-            slots_all.append(sl)
+        # find a slot for every ubatch before committing any ([P1] Крок 12); if that fails, one
+        # defrag and one more try ([P4] KVキャッシュの詳細: FAILED_PREPARE -> defrag -> retry)
+        slots_all = self._prepare(b, ubatches)
+        if slots_all is None and self.memory_update(True):
+            slots_all = self._prepare(b, ubatches)
+        if slots_all is None:
+            return int(DecodeStatus.NO_KV_SLOT)
         self.last_ubatches = []
         rows = []
         for k, ub in enumerate(ubatches):
@@ -207,6 +222,17 @@ class OracleContext:
         self.output_ids = np.full(b.n_tokens, -1, dtype=np.int64)
         self.output_ids[np.nonzero(b.output)[0]] = np.arange(int(b.output.sum()))
         return int(DecodeStatus.OK)
+
+    def _prepare(self, b, ubatches):
+        work = self.cells.copy()
+        slots_all = []
+        for ub in ubatches:
+            sl = work.find_slots(len(ub))
+            if sl is None:
+                return None
+            work.apply(sl, b.pos[list(ub)], [b.seq_id[i] for i in ub])
+            slots_all.append(sl)
+        return slots_all
 
     def _rollback(self, upos, useq):
         """[P4] エラーリカバリ: pos_min per sequence over the ubatch, then seq_rm(s, pos_min, -1)."""

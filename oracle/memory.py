@@ -118,6 +118,27 @@ class Cells:
             self.seq[c, :] = False
             self.seq[c, [int(s) for s in ss]] = True
 
+    def defrag_order(self) -> np.ndarray:
+        """The used cells in their order after a defrag ([P4] KVキャッシュの詳細: memory_update
+        with optimize moves cells to close the gaps; the figure "After Defrag" shows the seven
+        cells S0P0, S0P1, -, S1P0, S0P2, -, S1P1 becoming S0P0, S0P1, S0P2, S1P0, S1P1, -, -).
+
+        reading (the figure's outcome): the used cells packed from cell 0, ordered by sequence then
+        position; a cell shared by several sequences sorts under its lowest sequence id, and equal
+        keys keep their cell order. Returns old cell indices: new cell i takes old cell order[i]."""
+        used = np.nonzero(self.pos >= 0)[0]
+        first_seq = np.array([int(np.argmax(self.seq[c])) for c in used], dtype=np.int64)
+        return used[np.lexsort((used, self.pos[used], first_seq))]
+
+    def move(self, order: Sequence[int]):
+        """Rewrite the cells so that cell i holds what old cell order[i] held; the rest are empty."""
+        order = np.asarray(order, dtype=np.int64)
+        pos = np.full_like(self.pos, -1)
+        seq = np.zeros_like(self.seq)
+        pos[:len(order)] = self.pos[order]
+        seq[:len(order)] = self.seq[order]
+        self.pos, self.seq = pos, seq
+
     def n_kv(self) -> int:
         """Cells the attention reads: highest used cell + 1 (reading of the 'recount' in apply)."""
         used = np.nonzero(self.pos >= 0)[0]

@@ -90,7 +90,7 @@ def test_greedy_equals_decode_argmax(ctx):
 
 def set_row(ctx, i, row):
     assert ctx.debug_set_logits(i, row) == 0, ctx.last_error()
-    assert np.array_equal(ctx.get_logits_ith(i), row.astype(np.float32))
+    assert np.array_equal(ctx.get_logits_ith(i), row.astype(np.float32), equal_nan=True)
 
 
 def test_ties_at_the_top_k_threshold_take_the_lowest_ids(ctx):
