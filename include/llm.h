@@ -186,6 +186,15 @@ int32_t llm_n_outputs(llm_ctx *ctx);
  * Cells left with no sequence become empty and are reused by later batches. Returns 1. */
 int llm_seq_rm(llm_ctx *ctx, int32_t seq, int32_t p0, int32_t p1);
 
+/* Memory update ([P4] KVキャッシュの詳細: memory_update(optimize=true) defragments the cache by
+ * moving cells to close the gaps; the figure "After Defrag" shows the result). With optimize != 0
+ * the used cells are packed from cell 0, ordered by sequence (a shared cell: its lowest sequence
+ * id), then position; every layer's K/V rows move with their cells (device copies, stream
+ * synchronised), so later decodes give the same results up to float summation order.
+ * llm_decode runs the same defrag once, and searches again, when a batch finds no free cells.
+ * Returns 1 if cells moved, 0 if nothing to do (or optimize == 0), -1 on a device error. */
+int llm_memory_update(llm_ctx *ctx, int optimize);
+
 /* Largest / smallest position held for a sequence, -1 if it holds none ([P1] KV-cache section). */
 int32_t llm_seq_pos_max(llm_ctx *ctx, int32_t seq);
 int32_t llm_seq_pos_min(llm_ctx *ctx, int32_t seq);
@@ -215,6 +224,7 @@ typedef struct llm_perf_data {
     int64_t n_graph_replays;
     double  t_decode_ms;
     int64_t n_fused_steps;   /* one-token ubatches run as the single persistent kernel */
+    int64_t n_defrags;       /* cache defrags that moved cells (llm_memory_update or a retry) */
 } llm_perf_data;
 void llm_perf(llm_ctx *ctx, llm_perf_data *out);
 

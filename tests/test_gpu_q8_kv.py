@@ -42,9 +42,9 @@ def test_quantiser_bit_exact_on_the_library_rows():
     key = "tiny_f32_1seq"
     ctx = G.library_ctx(key, type_k=Q8_0, type_v=Q8_0)
     ctx.debug_capture(True)
-    toks = G.prompts(key)[0][:40]
+    toks = G.prompts(key)[0]
     assert ctx.decode(toks) == 0, ctx.last_error()
-    _check_blocks(ctx, 40, ctx.last_slots())
+    _check_blocks(ctx, len(toks), ctx.last_slots())
     assert ctx.decode([int(ctx.get_argmax_ith(-1))]) == 0, ctx.last_error()
     _check_blocks(ctx, 1, ctx.last_slots())
     ctx.free()

@@ -177,3 +177,58 @@ def test_bookkeeping_matches_oracle_randomized(T, seed):
         _same_state(lib, ora, n_seq)
     # the scenario exercises success, full-cache and invalid-batch paths
     assert codes.count(0) >= 20 and (-1 in codes)
+
+
+def _defrag_both(lib, ora):
+    r_lib = lib.memory_update(True)
+    r_ora = ora.memory_update(True)
+    assert r_lib == int(r_ora), (r_lib, r_ora)
+    return r_lib
+
+
+def test_defrag_matches_oracle_figure_and_retry(T):
+    # the pages' figure: S0P0, S0P1, -, S1P0, S0P2, -, S1P1 -> packed by sequence, then position
+    lib, ora = _pair(T, n_ctx=256, n_seq=2, n_batch=64, n_ubatch=64)
+    assert _decode_both(lib, ora, [1, 2, 3, 4, 5, 6, 7], [[0], [0], [0], [1], [0], [1], [1]]) == 0
+    lib.seq_rm(0, 2, 3); ora.seq_rm(0, 2, 3)         # cell 2
+    lib.seq_rm(1, 1, 2); ora.seq_rm(1, 1, 2)         # cell 5
+    assert _defrag_both(lib, ora) == 1
+    assert _defrag_both(lib, ora) == 0
+    _same_state(lib, ora, 2)
+    assert _decode_both(lib, ora, [8, 9], [[0], [1]], logits=[1, 1]) == 0
+    # no free run: one defrag, then the search again (still 1 when the cache is full)
+    lib, ora = _pair(T, n_ctx=256, n_seq=2, n_batch=256, n_ubatch=64)
+    assert _decode_both(lib, ora, [1] * 200, [[i % 2] for i in range(200)]) == 0
+    lib.seq_rm(0, 50, -1); ora.seq_rm(0, 50, -1)
+    assert _decode_both(lib, ora, [1] * 200, [[1]] * 200) == 1
+    assert lib.perf()["n_defrags"] == 1
+    _same_state(lib, ora, 2)
+    assert _decode_both(lib, ora, [1] * 100, [[1]] * 100) == 0
+    _same_state(lib, ora, 2)
+
+
+@pytest.mark.parametrize("seed", [3, 4, 5])
+def test_defrag_matches_oracle_randomized(T, seed):
+    rng = np.random.default_rng(seed)
+    n_seq = 6
+    lib, ora = _pair(T, n_ctx=256, n_seq=n_seq, n_batch=64, n_ubatch=int(rng.integers(1, 33)))
+    moved = 0
+    for step in range(120):
+        r = rng.random()
+        if r < 0.2:
+            s = int(rng.integers(-1, n_seq))
+            p0, p1 = int(rng.integers(-2, 30)), int(rng.integers(-2, 60))
+            lib.seq_rm(s, p0, p1)
+            ora.seq_rm(s, p0, p1)
+        elif r < 0.3:
+            moved += _defrag_both(lib, ora)
+        else:
+            n = int(rng.integers(1, 30))
+            seqs = []
+            for _ in range(n):
+                k = 2 if rng.random() < 0.1 else 1
+                seqs.append(sorted(rng.choice(n_seq, size=k, replace=False).tolist()))
+            toks = rng.integers(0, HP.n_vocab, size=n).tolist()
+            _decode_both(lib, ora, toks, seqs, logits=[1] * n)
+        _same_state(lib, ora, n_seq)
+    assert moved >= 3

@@ -48,7 +48,7 @@ class SamplerParams(C.Structure):
 class PerfData(C.Structure):
     _fields_ = [("n_decode_calls", C.c_int64), ("n_tokens", C.c_int64), ("n_ubatches", C.c_int64),
                 ("n_graph_replays", C.c_int64), ("t_decode_ms", C.c_double),
-                ("n_fused_steps", C.c_int64)]
+                ("n_fused_steps", C.c_int64), ("n_defrags", C.c_int64)]
 
 
 ABORT_CB = C.CFUNCTYPE(C.c_int, C.c_void_p)
@@ -83,6 +83,7 @@ SIGNATURES = {
                                          C.POINTER(C.c_float), C.c_int64]),
     "llm_debug_inject_fault": (C.c_int, [C.c_void_p, C.c_int32, C.c_int32]),
     "llm_debug_kv_raw": (C.c_int64, [C.c_void_p, C.c_int32, C.c_int32, C.c_void_p, C.c_int64]),
+    "llm_memory_update": (C.c_int, [C.c_void_p, C.c_int]),
     "llm_sample_ith": (C.c_int32, [C.c_void_p, C.c_int32, C.POINTER(SamplerParams), C.c_float]),
     "llm_debug_set_logits": (C.c_int, [C.c_void_p, C.c_int32, C.POINTER(C.c_float)]),
     "llm_debug_step_trace_enable": (C.c_int, [C.c_void_p, C.c_int]),
@@ -260,6 +261,9 @@ class Context:
     # ---- memory
     def seq_rm(self, seq: int, p0: int, p1: int) -> int:
         return lib().llm_seq_rm(self.ptr, seq, p0, p1)
+
+    def memory_update(self, optimize: bool = True) -> int:
+        return lib().llm_memory_update(self.ptr, int(optimize))
 
     def seq_pos_max(self, s: int) -> int:
         return lib().llm_seq_pos_max(self.ptr, s)

@@ -153,6 +153,41 @@ void KvCells::seq_rm(int32_t s, int32_t p0, int32_t p1) {
     }
 }
 
+bool KvCells::defrag_order(std::vector<int32_t>& order) const {
+    struct Key { int32_t seq, pos, cell; };
+    std::vector<Key> keys;
+    keys.reserve(used_);
+    for (int32_t cl = 0; cl < size(); ++cl) {
+        if (pos_[cl] < 0) continue;
+        int32_t s = 0;
+        while (s < kMaxSeq && !seq_[cl].test(s)) ++s;
+        keys.push_back({s, pos_[cl], cl});
+    }
+    std::sort(keys.begin(), keys.end(), [](const Key& a, const Key& b) {
+        if (a.seq != b.seq) return a.seq < b.seq;
+        if (a.pos != b.pos) return a.pos < b.pos;
+        return a.cell < b.cell;
+    });
+    order.resize(keys.size());
+    bool moved = false;
+    for (size_t i = 0; i < keys.size(); ++i) {
+        order[i] = keys[i].cell;
+        moved = moved || keys[i].cell != (int32_t)i;
+    }
+    return moved;
+}
+
+void KvCells::move(const std::vector<int32_t>& order) {
+    KvCells fresh(size(), (int32_t)seq_pos_.size());
+    std::vector<int32_t> slot(1), p(1);
+    for (size_t i = 0; i < order.size(); ++i) {
+        slot[0] = (int32_t)i;
+        p[0] = pos_[order[i]];
+        fresh.apply(slot, p.data(), &seq_[order[i]], 1);
+    }
+    *this = std::move(fresh);
+}
+
 // ---------------------------------------------------------------------------------------------
 void build_attn_plan(const KvCells& cells, const SanBatch& b, int32_t i0, int32_t T, int32_t tile_q,
                      int32_t n_head_kv, int32_t n_gqa, int32_t target_items, int32_t max_rows,

@@ -66,6 +66,13 @@ public:
     // p1 < 0 -> no bound). A cell left with no sequence becomes empty.
     void seq_rm(int32_t s, int32_t p0, int32_t p1);
 
+    // Defrag ([P4] KVキャッシュの詳細, memory_update(optimize=true) and its "After Defrag"
+    // figure): the used cells packed from cell 0, ordered by their lowest sequence id, then
+    // position, then cell. order[i] = the old cell that new cell i takes. False if no cell moves.
+    bool defrag_order(std::vector<int32_t>& order) const;
+    // Rewrite the cells so that cell i holds what old cell order[i] held; the rest are empty.
+    void move(const std::vector<int32_t>& order);
+
 private:
     void drop_seq_from_cell(int32_t c, int32_t s);
     void free_cell(int32_t c);

@@ -137,6 +137,16 @@ __global__ void kv_quant_q8_kernel(const float* __restrict__ sk, const float* __
     }
 }
 
+template <typename U>
+__global__ void kv_gather_kernel(const U* __restrict__ src, U* __restrict__ dst,
+                                 const int32_t* __restrict__ order, int n, int n_src, int upr) {
+    const int g = blockIdx.y;
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= (int64_t)n * upr) return;
+    const int r = (int)(i / upr), u = (int)(i % upr);
+    dst[((int64_t)g * n + r) * upr + u] = src[((int64_t)g * n_src + order[r]) * upr + u];
+}
+
 __global__ void swiglu_kernel(const float* __restrict__ gu, int64_t T, int F,
                               float* __restrict__ u) {
     const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -260,6 +270,22 @@ void launch_kv_quant_q8(const float* sk, const float* sv, int32_t ld, int32_t T,
     cfg.numAttrs = pdl ? 1 : 0;
     cudaLaunchKernelEx(&cfg, kv_quant_q8_kernel, sk, sv, (int)ld, (int)Hkv, (int)hd, slot,
                        static_cast<int8_t*>(kc), static_cast<int8_t*>(vc), (int)n_ctx, err);
+}
+
+void launch_kv_gather(const void* src, void* dst, const int32_t* order, int32_t n, int32_t n_head,
+                      int32_t n_src, int32_t row_bytes, cudaStream_t st) {
+    if (n <= 0) return;
+    if (row_bytes % 16 == 0) {
+        const int upr = row_bytes / 16;
+        const dim3 grid((unsigned)(((int64_t)n * upr + 255) / 256), (unsigned)n_head);
+        kv_gather_kernel<uint4><<<grid, 256, 0, st>>>(static_cast<const uint4*>(src), static_cast<uint4*>(dst),
+                                                      order, n, n_src, upr);
+    } else {
+        const int upr = row_bytes / 2;
+        const dim3 grid((unsigned)(((int64_t)n * upr + 255) / 256), (unsigned)n_head);
+        kv_gather_kernel<uint16_t><<<grid, 256, 0, st>>>(static_cast<const uint16_t*>(src),
+                                                         static_cast<uint16_t*>(dst), order, n, n_src, upr);
+    }
 }
 
 void launch_swiglu(const float* gu, int32_t T, int32_t F, float* u, cudaStream_t st) {

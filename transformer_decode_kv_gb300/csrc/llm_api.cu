@@ -113,6 +113,8 @@ struct llm_ctx {
     void* kv_k = nullptr;
     void* kv_v = nullptr;
     float* kv_stage = nullptr;                 // Q8_0: this ubatch's K and V rows, [2][Hkv][n_ubatch][hd]
+    uint8_t* kv_scratch = nullptr;             // defrag: one cache region's moved rows
+    int32_t* d_order = nullptr;                // defrag: old cell of each new cell
     KvCells cells;
 
     // scratch for one ubatch
@@ -1067,6 +1069,8 @@ int llm_weights_ready(llm_ctx* c) {
     return 0;
 }
 
+static int defrag(llm_ctx* c);
+
 int32_t llm_decode(llm_ctx* c, llm_batch bt) {
     if (!c) return -2;
     const auto t0 = std::chrono::steady_clock::now();
@@ -1093,8 +1097,13 @@ int32_t llm_decode(llm_ctx* c, llm_batch bt) {
     // all slots before any commit ([P1] Крок 12): ubatch k takes the next lowest empty cells
     std::vector<int32_t> slots;
     if (!c->cells.find_free(b.n, slots)) {
-        c->err = "no KV slot for the batch";
-        return 1;
+        // one defrag, then one more search ([P4] KVキャッシュの詳細: FAILED_PREPARE -> defrag)
+        const int moved = defrag(c);
+        if (moved < 0) return -2;
+        if (moved == 0 || !c->cells.find_free(b.n, slots)) {
+            c->err = "no KV slot for the batch";
+            return 1;
+        }
     }
     if (!c->host_only && !ensure_outputs(c, b.n_outputs)) return -2;
     c->last_slots = slots;
@@ -1276,6 +1285,54 @@ int32_t llm_get_argmax_ith(llm_ctx* c, int32_t i) {
 }
 
 int32_t llm_n_outputs(llm_ctx* c) { return c ? c->n_outputs : 0; }
+
+// Defrag: move the used cells' K/V rows (every layer) to their new cells, then rewrite the cell
+// metadata. Each cache region (per layer K and V; Q8_0: quants and scales) is gathered into a
+// scratch region in the new order, then copied back as one packed run per KV head.
+static int defrag(llm_ctx* c) {
+    std::vector<int32_t> order;
+    if (!c->cells.defrag_order(order)) return 0;
+    if (!c->host_only) {
+        const int32_t n = (int32_t)order.size(), Hkv = c->hp.n_head_kv, hd = c->hp.head_dim;
+        if (!c->kv_scratch && !dalloc(c, &c->kv_scratch, c->kv_layer_bytes())) return -1;
+        if (!c->d_order && !dalloc(c, &c->d_order, (size_t)c->n_ctx)) return -1;
+        if (!cuda_ok(c, cudaMemcpyAsync(c->d_order, order.data(), sizeof(int32_t) * n, cudaMemcpyHostToDevice,
+                                        c->st), "copy"))
+            return -1;
+        struct Region { size_t off; int32_t rb; };
+        std::vector<Region> regions;
+        if (c->kv_q8()) {
+            regions.push_back({0, hd});
+            regions.push_back({kv_q8_scale_offset(Hkv, c->n_ctx, hd), hd / 32 * 2});
+        } else {
+            regions.push_back({0, hd * (int32_t)type_size(c->type_k)});
+        }
+        for (int32_t il = 0; il < c->hp.n_layer; ++il) {
+            for (void* base : {c->kv_k, c->kv_v}) {
+                uint8_t* layer = static_cast<uint8_t*>(base) + (size_t)il * c->kv_layer_bytes();
+                for (const Region& r : regions) {
+                    launch_kv_gather(layer + r.off, c->kv_scratch, c->d_order, n, Hkv, c->n_ctx, r.rb, c->st);
+                    if (!cuda_ok(c, cudaMemcpy2DAsync(layer + r.off, (size_t)c->n_ctx * r.rb, c->kv_scratch,
+                                                      (size_t)n * r.rb, (size_t)n * r.rb, Hkv,
+                                                      cudaMemcpyDeviceToDevice, c->st), "copy"))
+                        return -1;
+                }
+            }
+        }
+        if (!cuda_ok(c, cudaGetLastError(), "defrag launch") || !cuda_ok(c, cudaStreamSynchronize(c->st), "defrag"))
+            return -1;
+    }
+    c->cells.move(order);
+    c->perf.n_defrags += 1;
+    return 1;
+}
+
+int llm_memory_update(llm_ctx* c, int optimize) {
+    if (!c) return -1;
+    if (!optimize) return 0;
+    if (!c->host_only) cudaSetDevice(c->device);
+    return defrag(c);
+}
 
 int llm_seq_rm(llm_ctx* c, int32_t seq, int32_t p0, int32_t p1) {
     if (!c) return 0;
