@@ -74,6 +74,15 @@ enum {
      * Off by default: on a GB300 the per-op sequence is as fast or faster (3.43 vs 3.47 ms per
      * 8B BF16 step). */
     LLM_CTX_FUSED_STEP = 1u << 1,
+    /* A cache not shared by all sequences (kv_unified = false; [P1] Крок 9-10: n_ctx is divided
+     * among the sequences, n_ctx_seq = n_ctx / n_seq_max cells each; [P2] Example 9): sequence s
+     * writes only cells [s n_ctx_seq, (s + 1) n_ctx_seq), each token must belong to exactly one
+     * sequence (else the batch is invalid, -1), and batches are split with split_equal ([P1]
+     * Крок 12, [P4] llama_ubatch n_seq_tokens / n_seqs): each ubatch takes the sequences with
+     * unused tokens in ascending, consecutive ids (at most n_ubatch of them) and the same number
+     * min(n_ubatch / n_seqs, fewest unused tokens among them) of next tokens from each. Output
+     * rows stay in batch order. */
+    LLM_CTX_KV_SPLIT = 1u << 2,
 };
 
 /* Context parameters ([P1] Крок 9-10 context constructor; [P2] Example 9; [P4] コンテキストの構築).
@@ -205,6 +214,9 @@ void llm_set_abort_callback(llm_ctx *ctx, int (*cb)(void *user), void *user);
 
 /* Effective context sizes after rounding / clamping. */
 uint32_t llm_n_ctx(llm_ctx *ctx);
+/* Cells one sequence can use: n_ctx, or n_ctx / n_seq_max with LLM_CTX_KV_SPLIT ([P2] Example 9
+ * n_ctx_seq). */
+uint32_t llm_n_ctx_seq(llm_ctx *ctx);
 uint32_t llm_n_batch(llm_ctx *ctx);
 uint32_t llm_n_ubatch(llm_ctx *ctx);
 

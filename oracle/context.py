@@ -16,7 +16,7 @@ import numpy as np
 
 from .formats import F16, F32, decode_weight, round_to_type
 from .memory import (Cells, DecodeStatus, LLAMA_MAX_SEQ, derive_cparams, sanitize_batch,
-                     split_simple)
+                     split_simple, split_equal)
 from .numerics import attention, linear, rms_norm, rope, swiglu
 
 
@@ -106,11 +106,15 @@ def output_logits(w: OracleWeights, hp, x_rows: np.ndarray) -> np.ndarray:
 
 
 class OracleContext:
-    """A llama context: a unified KV cache of n_ctx cells, the batch allocator and the outputs."""
+    """A llama context: a KV cache of n_ctx cells, the batch allocator and the outputs.
+
+    kv_unified (default) shares all n_ctx cells among the sequences (one stream); otherwise each
+    sequence has a stream of its own of n_ctx // n_seq_max cells, and batches are split with
+    split_equal instead of split_simple ([P1] Крок 12)."""
 
     def __init__(self, hp, weights: Optional[OracleWeights], n_ctx: int, n_seq_max: int = 1,
                  type_k: int = F16, type_v: int = F16, n_batch: int = 2048, n_ubatch: int = 512,
-                 compute: bool = True):
+                 compute: bool = True, kv_unified: bool = True):
         cp = derive_cparams(n_ctx, n_batch, n_ubatch, n_seq_max)
         if cp is None:
             raise ValueError("invalid context parameters")
@@ -118,7 +122,9 @@ class OracleContext:
         self.hp, self.w = hp, weights
         self.n_seq_max = n_seq_max
         self.type_k, self.type_v = type_k, type_v
-        self.cells = Cells(self.n_ctx)
+        self.kv_unified = kv_unified
+        self.n_stream = 1 if kv_unified else n_seq_max
+        self.cells = Cells(self.n_ctx, self.n_stream)
         self.compute = compute      # False: batch / cell bookkeeping only, no forward pass
         kvd = (hp.n_head_kv, hp.head_dim)
         n_k = hp.n_layer if compute else 0
@@ -146,14 +152,15 @@ class OracleContext:
         Returns True if any cell moved."""
         if not optimize:
             return False
-        order = self.cells.defrag_order()
-        if np.array_equal(order, np.arange(len(order))):
+        if self.cells.is_defragged():
             return False
-        self.cells.move(order)
+        src = self.cells.defrag_order()
+        keep = src >= 0
+        self.cells.move(src)
         for il in range(len(self.K)):
             for X in (self.K, self.V):
                 moved = np.zeros_like(X[il])
-                moved[:len(order)] = X[il][order]
+                moved[keep] = X[il][src[keep]]
                 X[il] = moved
         return True
 
@@ -192,7 +199,13 @@ class OracleContext:
         self._reset_outputs(0)
         if b is None:
             return int(DecodeStatus.INVALID_BATCH)
-        ubatches = split_simple(b.n_tokens, self.n_ubatch)
+        if self.n_stream > 1:
+            # reading: a token of a split cache lives in its sequence's stream, so it has one sequence
+            if any(len(ss) != 1 for ss in b.seq_id):
+                return int(DecodeStatus.INVALID_BATCH)
+            ubatches = split_equal([ss[0] for ss in b.seq_id], self.n_ubatch)
+        else:
+            ubatches = split_simple(b.n_tokens, self.n_ubatch)
         # find a slot for every ubatch before committing any ([P1] Крок 12); if that fails, one
         # defrag and one more try ([P4] KVキャッシュの詳細: FAILED_PREPARE -> defrag -> retry)
         slots_all = self._prepare(b, ubatches)
@@ -201,7 +214,7 @@ class OracleContext:
         if slots_all is None:
             return int(DecodeStatus.NO_KV_SLOT)
         self.last_ubatches = []
-        rows = []
+        rows, row_tok = [], []
         for k, ub in enumerate(ubatches):
             idx = list(ub)
             upos = b.pos[idx]
@@ -218,7 +231,10 @@ class OracleContext:
                 return int(failed)
             out_rows = [t for t, i in enumerate(idx) if b.output[i]]
             rows.append(self._process_ubatch(b.token[idx], upos, useq, slots_all[k], out_rows))
-        self.logits = np.concatenate(rows, axis=0) if rows else np.zeros((0, self.hp.n_vocab))
+            row_tok.extend(idx[t] for t in out_rows)
+        # output rows in batch order, whatever order the ubatches took the tokens in
+        logits = np.concatenate(rows, axis=0) if rows else np.zeros((0, self.hp.n_vocab))
+        self.logits = logits[np.argsort(row_tok, kind="stable")] if row_tok else logits
         self.output_ids = np.full(b.n_tokens, -1, dtype=np.int64)
         self.output_ids[np.nonzero(b.output)[0]] = np.arange(int(b.output.sum()))
         return int(DecodeStatus.OK)
@@ -227,7 +243,19 @@ class OracleContext:
         work = self.cells.copy()
         slots_all = []
         for ub in ubatches:
-            sl = work.find_slots(len(ub))
+            if self.n_stream == 1:
+                sl = work.find_slots(len(ub))
+            else:                            # each token takes the next free cell of its stream
+                sl, need = [None] * len(ub), {}
+                for t, i in enumerate(ub):
+                    need.setdefault(b.seq_id[i][0], []).append(t)
+                for s, ts in need.items():
+                    got = work.find_slots(len(ts), s)
+                    if got is None:
+                        sl = None
+                        break
+                    for t, cell in zip(ts, got):
+                        sl[t] = cell
             if sl is None:
                 return None
             work.apply(sl, b.pos[list(ub)], [b.seq_id[i] for i in ub])

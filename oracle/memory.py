@@ -53,11 +53,24 @@ class Batch:
 
 class Cells:
     """KV cells ([P4] KVキャッシュの詳細, llama_kv_cells): per cell a position (-1 = empty) and the
-    set of sequences using it (a cell can be shared), held as a bool row seq[c, s]."""
+    set of sequences using it (a cell can be shared), held as a bool row seq[c, s].
 
-    def __init__(self, n_ctx: int):
+    n_stream > 1 is a cache that is not shared by all sequences ([P1] Крок 9-10: n_ctx is then
+    divided among the sequences, n_ctx_seq cells each; [P2] Example 9: kv_unified): stream s owns
+    cells [s * n_ctx_seq, (s + 1) * n_ctx_seq), n_ctx_seq = n_ctx // n_stream (reading: the
+    remainder of the division is left unused)."""
+
+    def __init__(self, n_ctx: int, n_stream: int = 1):
         self.pos = np.full(n_ctx, -1, dtype=np.int64)
         self.seq = np.zeros((n_ctx, LLAMA_MAX_SEQ), dtype=bool)
+        self.n_stream = n_stream
+        self.n_ctx_seq = n_ctx // n_stream
+
+    def stream_range(self, s: int):
+        """Cells [lo, hi) of stream s (the whole cache when there is one stream)."""
+        if self.n_stream == 1:
+            return 0, len(self.pos)
+        return s * self.n_ctx_seq, (s + 1) * self.n_ctx_seq
 
     @property
     def size(self) -> int:
@@ -67,6 +80,7 @@ class Cells:
         c = Cells.__new__(Cells)
         c.pos = self.pos.copy()
         c.seq = self.seq.copy()
+        c.n_stream, c.n_ctx_seq = self.n_stream, self.n_ctx_seq
         return c
 
     def seqs_of(self, c: int) -> set:
@@ -103,10 +117,11 @@ class Cells:
         self.pos[sel & ~self.seq.any(axis=1)] = -1
         return True
 
-    def find_slots(self, n: int) -> Optional[List[int]]:
+    def find_slots(self, n: int, stream: int = 0) -> Optional[List[int]]:
         """reading ("contiguous, or at least available" cells, [P4] KVキャッシュの詳細): the n
-        lowest-index empty cells, in ascending order; None if fewer than n are empty."""
-        free = np.nonzero(self.pos < 0)[0]
+        lowest-index empty cells of the stream, in ascending order; None if fewer are empty."""
+        lo, hi = self.stream_range(stream)
+        free = lo + np.nonzero(self.pos[lo:hi] < 0)[0]
         return free[:n].tolist() if len(free) >= n else None
 
     def apply(self, slots: Sequence[int], pos: Sequence[int], seq_ids: Sequence[Sequence[int]]):
@@ -119,24 +134,35 @@ class Cells:
             self.seq[c, [int(s) for s in ss]] = True
 
     def defrag_order(self) -> np.ndarray:
-        """The used cells in their order after a defrag ([P4] KVキャッシュの詳細: memory_update
-        with optimize moves cells to close the gaps; the figure "After Defrag" shows the seven
-        cells S0P0, S0P1, -, S1P0, S0P2, -, S1P1 becoming S0P0, S0P1, S0P2, S1P0, S1P1, -, -).
+        """Where every cell's content comes from after a defrag ([P4] KVキャッシュの詳細:
+        memory_update with optimize moves cells to close the gaps; the figure "After Defrag" shows
+        the seven cells S0P0, S0P1, -, S1P0, S0P2, -, S1P1 becoming S0P0, S0P1, S0P2, S1P0, S1P1,
+        -, -).
 
-        reading (the figure's outcome): the used cells packed from cell 0, ordered by sequence then
-        position; a cell shared by several sequences sorts under its lowest sequence id, and equal
-        keys keep their cell order. Returns old cell indices: new cell i takes old cell order[i]."""
-        used = np.nonzero(self.pos >= 0)[0]
-        first_seq = np.array([int(np.argmax(self.seq[c])) for c in used], dtype=np.int64)
-        return used[np.lexsort((used, self.pos[used], first_seq))]
+        reading (the figure's outcome): in each stream, the used cells packed from the stream's
+        first cell, ordered by sequence then position; a cell shared by several sequences sorts
+        under its lowest sequence id, and equal keys keep their cell order. Returns src [n_ctx]:
+        new cell i takes old cell src[i] (-1: empty)."""
+        src = np.full(len(self.pos), -1, dtype=np.int64)
+        for s in range(self.n_stream):
+            lo, hi = self.stream_range(s)
+            used = lo + np.nonzero(self.pos[lo:hi] >= 0)[0]
+            first_seq = np.array([int(np.argmax(self.seq[c])) for c in used], dtype=np.int64)
+            src[lo:lo + len(used)] = used[np.lexsort((used, self.pos[used], first_seq))]
+        return src
 
-    def move(self, order: Sequence[int]):
-        """Rewrite the cells so that cell i holds what old cell order[i] held; the rest are empty."""
-        order = np.asarray(order, dtype=np.int64)
+    def is_defragged(self) -> bool:
+        src = self.defrag_order()
+        return bool(np.all((src < 0) | (src == np.arange(len(src)))))
+
+    def move(self, src: Sequence[int]):
+        """Rewrite the cells so that cell i holds what old cell src[i] held (-1: empty)."""
+        src = np.asarray(src, dtype=np.int64)
+        keep = src >= 0
         pos = np.full_like(self.pos, -1)
         seq = np.zeros_like(self.seq)
-        pos[:len(order)] = self.pos[order]
-        seq[:len(order)] = self.seq[order]
+        pos[keep] = self.pos[src[keep]]
+        seq[keep] = self.seq[src[keep]]
         self.pos, self.seq = pos, seq
 
     def n_kv(self) -> int:
@@ -232,3 +258,33 @@ def split_simple(n_tokens: int, n_ubatch: int) -> List[range]:
     """split_simple ([P1] Крок 12): the next at most n_ubatch unused tokens of the batch, in batch
     order, until the batch is used up. Returns the token ranges of the ubatches."""
     return [range(i, min(i + n_ubatch, n_tokens)) for i in range(0, n_tokens, n_ubatch)]
+
+
+def split_equal(seq_of_token: Sequence[int], n_ubatch: int) -> List[List[int]]:
+    """split_equal(n_ubatch, sequential = true) ([P1] Крок 12: the splitter of a cache with more
+    than one stream; [P4] llama_ubatch: n_seq_tokens tokens per sequence set, n_seqs sets).
+
+    reading (the pages give the call and the ubatch fields, not the steps): every token belongs
+    to one sequence; a ubatch takes the sequences that still have unused tokens in ascending id,
+    consecutive ids only ("sequential"), at most n_ubatch of them; each of the n_seqs sequences
+    contributes the same number n_seq_tokens = min(n_ubatch // n_seqs, the fewest unused tokens
+    among them) of its next unused tokens in batch order; the ubatch lists them sequence by
+    sequence. Returns the batch indices of each ubatch."""
+    queues = {}
+    for i, s in enumerate(seq_of_token):
+        queues.setdefault(int(s), []).append(i)
+    heads = {s: 0 for s in queues}
+    out = []
+    while True:
+        live = sorted(s for s in queues if heads[s] < len(queues[s]))
+        if not live:
+            return out
+        sets = [live[0]]
+        while len(sets) < n_ubatch and sets[-1] + 1 in live:
+            sets.append(sets[-1] + 1)
+        n_seq_tokens = min(n_ubatch // len(sets), min(len(queues[s]) - heads[s] for s in sets))
+        ub = []
+        for s in sets:
+            ub.extend(queues[s][heads[s]:heads[s] + n_seq_tokens])
+            heads[s] += n_seq_tokens
+        out.append(ub)

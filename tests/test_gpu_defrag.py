@@ -1,7 +1,7 @@
 """GPU parity of the KV defrag (llm_memory_update with optimize), through the C ABI.
 
   - Every layer's K/V rows move with their cells, bit-exact: after the defrag, new cell i holds the
-    bytes old cell order[i] held, order being the oracle's defrag order for the same cell state
+    bytes old cell src[i] held, src being the oracle's defrag map for the same cell state
     (F16 and Q8_0 caches; the Q8_0 blocks move with their scales).
   - Logits of the next step after the defrag: equal to a twin context that was not defragmented
     (up to float summation order, 1e-5) and to the oracle that defragmented too (1e-4, the F32
@@ -20,6 +20,12 @@ KEY = "tiny_f32_8seq"
 N_SEQ, N_PROMPT = 4, 40
 
 
+def _decode(ctx, toks, seqs, logits):
+    if isinstance(ctx, oracle.OracleContext):
+        return ctx.decode(toks, seq_id=seqs, n_seq_id=[len(s) for s in seqs], logits=logits)
+    return ctx.decode(toks, seq_ids=seqs, logits=logits)
+
+
 def _fragment(ctx):
     """Interleaved prompts of N_SEQ sequences, then holes: sequence 1 cut at 10, sequence 3 loses
     positions 5..14, sequence 0 gets 6 more tokens into the first holes."""
@@ -29,11 +35,11 @@ def _fragment(ctx):
     seqs = [[s] for s in range(N_SEQ) for _ in range(N_PROMPT)]
     order = np.argsort(np.tile(np.arange(N_PROMPT), N_SEQ), kind="stable")   # interleave
     toks, seqs = toks[order], [seqs[i] for i in order]
-    assert ctx.decode(toks, seq_ids=seqs, logits=[0] * len(toks)) == 0
+    assert _decode(ctx, toks, seqs, [0] * len(toks)) == 0
     ctx.seq_rm(1, 10, -1)
     ctx.seq_rm(3, 5, 15)
     extra = [int(t) for t in toks[:6]]
-    assert ctx.decode(extra, seq_ids=[[0]] * 6, logits=[0] * 6) == 0
+    assert _decode(ctx, extra, [[0]] * 6, [0] * 6) == 0
 
 
 def _next(ctx):
@@ -52,7 +58,8 @@ def test_defrag_moves_rows_and_keeps_logits(tkv):
     for ctx in (a, b):
         _fragment(ctx)
     _fragment(ora)
-    order = ora.cells.defrag_order()
+    src = ora.cells.defrag_order()
+    keep = src >= 0
     before = [[b.kv_cache(il, which).copy() for which in (0, 1)] for il in range(hp.n_layer)]
     assert b.memory_update(True) == 1
     assert ora.memory_update(True) is True
@@ -60,8 +67,7 @@ def test_defrag_moves_rows_and_keeps_logits(tkv):
     for il in range(hp.n_layer):
         for which in (0, 1):
             after = b.kv_cache(il, which)
-            n = len(order)
-            assert np.array_equal(after[:, :n], before[il][which][:, order]), (il, which)
+            assert np.array_equal(after[:, keep], before[il][which][:, src[keep]]), (il, which)
     la, lb = _next(a), _next(b)
     lo = [None] * N_SEQ
     assert ora.decode([11, 22, 33, 44], seq_id=[[s] for s in range(N_SEQ)], n_seq_id=[1] * N_SEQ,

@@ -49,12 +49,12 @@ def test_context_parameter_derivation(T):
         T.Context(HParams(2, 64, 6, 4, 32, 96, 50, 1e4, 1e-6), n_ctx=256, host_only=True)
 
 
-def _pair(T, n_ctx, n_seq, n_batch, n_ubatch):
+def _pair(T, n_ctx, n_seq, n_batch, n_ubatch, unified=True):
     lib = T.Context(HP, n_ctx=n_ctx, n_seq_max=n_seq, n_batch=n_batch, n_ubatch=n_ubatch,
-                    host_only=True)
+                    host_only=True, kv_unified=unified)
     lib.debug_capture(True)
     ora = oracle.OracleContext(HP, None, n_ctx=n_ctx, n_seq_max=n_seq, n_batch=n_batch,
-                               n_ubatch=n_ubatch, compute=False)
+                               n_ubatch=n_ubatch, compute=False, kv_unified=unified)
     return lib, ora
 
 
@@ -232,3 +232,47 @@ def test_defrag_matches_oracle_randomized(T, seed):
             _decode_both(lib, ora, toks, seqs, logits=[1] * n)
         _same_state(lib, ora, n_seq)
     assert moved >= 3
+
+
+def test_split_cache_scripted(T):
+    lib, ora = _pair(T, n_ctx=256, n_seq=4, n_batch=64, n_ubatch=6, unified=False)
+    assert lib.n_ctx_seq == 64
+    seqs = [[i % 4] for i in range(22)] + [[1]] * 5
+    assert _decode_both(lib, ora, list(range(1, 28)), seqs, logits=[1] * 27) == 0
+    assert [len(u["slots"]) for u in ora.last_ubatches] == [4, 4, 4, 4, 4, 2, 5]
+    _same_state(lib, ora, 4)
+    assert _decode_both(lib, ora, [1], [[0, 1]]) == -1           # one token, two streams
+    assert _decode_both(lib, ora, [1] * 59, [[2]] * 59) == 0       # stream 2: 5 + 59 = 64 cells
+    assert _decode_both(lib, ora, [1], [[2]]) == 1                 # full stream
+    assert _decode_both(lib, ora, [1], [[3]]) == 0
+    lib.seq_rm(2, 3, 10); ora.seq_rm(2, 3, 10)
+    assert _defrag_both(lib, ora) == 1
+    assert _decode_both(lib, ora, [1] * 7, [[2]] * 7) == 0
+    _same_state(lib, ora, 4)
+
+
+@pytest.mark.parametrize("seed", [6, 7, 8])
+def test_split_cache_matches_oracle_randomized(T, seed):
+    rng = np.random.default_rng(seed)
+    n_seq = 5
+    lib, ora = _pair(T, n_ctx=512, n_seq=n_seq, n_batch=64, n_ubatch=int(rng.integers(1, 20)),
+                     unified=False)
+    codes = []
+    for step in range(100):
+        r = rng.random()
+        if r < 0.15:
+            s = int(rng.integers(-1, n_seq))
+            p0, p1 = int(rng.integers(-2, 30)), int(rng.integers(-2, 60))
+            lib.seq_rm(s, p0, p1)
+            ora.seq_rm(s, p0, p1)
+        elif r < 0.22:
+            _defrag_both(lib, ora)
+        else:
+            n = int(rng.integers(1, 40))
+            seqs = [[int(rng.integers(0, n_seq))] for _ in range(n)]
+            if rng.random() < 0.05:
+                seqs[0] = [0, 1]
+            toks = rng.integers(0, HP.n_vocab, size=n).tolist()
+            codes.append(_decode_both(lib, ora, toks, seqs, logits=[1] * n))
+        _same_state(lib, ora, n_seq)
+    assert codes.count(0) >= 20 and 1 in codes

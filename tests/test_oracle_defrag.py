@@ -66,9 +66,10 @@ def test_compaction_invariants(seed):
     c = _random_cells(np.random.default_rng(seed))
     before = sorted((int(c.pos[i]), tuple(sorted(c.seqs_of(i)))) for i in range(c.size) if c.pos[i] >= 0)
     n_used = len(before)
-    order = c.defrag_order()
-    assert sorted(order.tolist()) == [i for i in range(c.size) if c.pos[i] >= 0]
-    c.move(order)
+    src = c.defrag_order()
+    assert np.all(src[:n_used] >= 0) and np.all(src[n_used:] < 0)
+    assert sorted(src[:n_used].tolist()) == [i for i in range(c.size) if c.pos[i] >= 0]
+    c.move(src)
     after = sorted((int(c.pos[i]), tuple(sorted(c.seqs_of(i)))) for i in range(c.size) if c.pos[i] >= 0)
     assert after == before                                   # nothing lost, nothing invented
     assert np.all(c.pos[:n_used] >= 0) and np.all(c.pos[n_used:] < 0)
@@ -76,7 +77,7 @@ def test_compaction_invariants(seed):
     # cells of a sequence's lowest-id group are contiguous and in position order
     key = [(min(c.seqs_of(i)), int(c.pos[i])) for i in range(n_used)]
     assert key == sorted(key)
-    assert np.array_equal(c.defrag_order(), np.arange(n_used))       # idempotent
+    assert c.is_defragged()                                          # idempotent
 
 
 def test_defrag_keeps_logits():
@@ -103,8 +104,16 @@ def test_no_slot_tries_one_defrag():
     ctx = oracle.OracleContext(MICRO, None, n_ctx=256, n_seq_max=2, n_batch=256, compute=False)
     assert ctx.decode([1] * 200, seq_id=[[i % 2] for i in range(200)], n_seq_id=[1] * 200) == 0
     ctx.seq_rm(0, 50, -1)                        # frees the even cells from 100 on
-    order = ctx.cells.defrag_order()
-    assert not np.array_equal(order, np.arange(len(order)))
+    assert not ctx.cells.is_defragged()
     assert ctx.decode([1] * 200, seq_id=[[1]] * 200, n_seq_id=[1] * 200) == 1     # 106 free
-    assert np.array_equal(ctx.cells.defrag_order(), np.arange(len(order)))      # defragged
+    assert ctx.cells.is_defragged()
     assert ctx.decode([1] * 100, seq_id=[[1]] * 100, n_seq_id=[1] * 100) == 0
+
+
+def test_streams_defrag_within_each_stream():
+    c = Cells(16, n_stream=2)                    # cells 0-7 stream 0, 8-15 stream 1
+    c.apply([0, 2, 5, 9, 12, 15], [0, 1, 2, 0, 1, 2], [[0], [0], [0], [1], [1], [1]])
+    src = c.defrag_order()
+    assert src.tolist() == [0, 2, 5, -1, -1, -1, -1, -1, 9, 12, 15, -1, -1, -1, -1, -1]
+    c.move(src)
+    assert c.pos.tolist() == [0, 1, 2, -1, -1, -1, -1, -1, 0, 1, 2, -1, -1, -1, -1, -1]

@@ -18,6 +18,7 @@ LIB_PATH = os.path.join(_PKG, "libllm.so")
 F32, F16, BF16, Q8_0 = 0, 1, 2, 8
 CTX_HOST_ONLY = 1
 CTX_FUSED_STEP = 2
+CTX_KV_SPLIT = 4
 
 
 class HParams(C.Structure):
@@ -70,6 +71,7 @@ SIGNATURES = {
     "llm_seq_pos_min": (C.c_int32, [C.c_void_p, C.c_int32]),
     "llm_set_abort_callback": (None, [C.c_void_p, ABORT_CB, C.c_void_p]),
     "llm_n_ctx": (C.c_uint32, [C.c_void_p]),
+    "llm_n_ctx_seq": (C.c_uint32, [C.c_void_p]),
     "llm_n_batch": (C.c_uint32, [C.c_void_p]),
     "llm_n_ubatch": (C.c_uint32, [C.c_void_p]),
     "llm_kv_used_cells": (C.c_int32, [C.c_void_p]),
@@ -149,7 +151,7 @@ class Context:
 
     def __init__(self, hp, n_ctx: int, n_seq_max: int = 1, type_k: int = F16, type_v: int = F16,
                  n_batch: int = 2048, n_ubatch: int = 512, stream: Optional[int] = None,
-                 host_only: bool = False, fused_step: bool = False):
+                 host_only: bool = False, fused_step: bool = False, kv_unified: bool = True):
         L = lib()
         self._hp = HParams(hp.n_layer, hp.n_embd, hp.n_head, hp.n_head_kv, hp.head_dim, hp.n_ff,
                            hp.n_vocab, hp.rope_freq_base, hp.rms_eps, getattr(hp, "rope_type", 0))
@@ -157,7 +159,8 @@ class Context:
         cp.n_ctx, cp.n_seq_max, cp.n_batch, cp.n_ubatch = n_ctx, n_seq_max, n_batch, n_ubatch
         cp.type_k, cp.type_v = type_k, type_v
         cp.stream = stream
-        cp.flags = (CTX_HOST_ONLY if host_only else 0) | (CTX_FUSED_STEP if fused_step else 0)
+        cp.flags = ((CTX_HOST_ONLY if host_only else 0) | (CTX_FUSED_STEP if fused_step else 0) |
+                    (0 if kv_unified else CTX_KV_SPLIT))
         self.n_vocab = hp.n_vocab
         self.type_k = type_k
         self.ptr = L.llm_ctx_init(C.byref(self._hp), C.byref(cp))
@@ -283,6 +286,10 @@ class Context:
     @property
     def n_ctx(self) -> int:
         return lib().llm_n_ctx(self.ptr)
+
+    @property
+    def n_ctx_seq(self) -> int:
+        return lib().llm_n_ctx_seq(self.ptr)
 
     @property
     def n_batch(self) -> int:

@@ -70,8 +70,12 @@ bool sanitize_batch(int32_t n, const int32_t* token, const int32_t* pos, const i
 }
 
 // ---------------------------------------------------------------------------------------------
-KvCells::KvCells(int32_t n_ctx, int32_t n_seq_max)
-    : pos_(n_ctx, -1), seq_(n_ctx), seq_pos_(n_seq_max), sc_(n_seq_max), sp_(n_seq_max) {}
+KvCells::KvCells(int32_t n_ctx, int32_t n_seq_max, int32_t n_stream)
+    : pos_(n_ctx, -1), seq_(n_ctx), seq_pos_(n_seq_max), sc_(n_seq_max), sp_(n_seq_max),
+      n_stream_(n_stream < 1 ? 1 : n_stream), n_ctx_seq_(n_ctx / (n_stream < 1 ? 1 : n_stream)) {
+    free_lo_.resize(n_stream_);
+    for (int32_t s = 0; s < n_stream_; ++s) free_lo_[s] = stream_lo(s);
+}
 
 int32_t KvCells::seq_pos_max(int32_t s) const {
     if (s < 0 || s >= (int32_t)seq_pos_.size() || seq_pos_[s].empty()) return -1;
@@ -83,9 +87,11 @@ int32_t KvCells::seq_pos_min(int32_t s) const {
     return seq_pos_[s].begin()->first;
 }
 
-bool KvCells::find_free(int32_t n, std::vector<int32_t>& out) const {
+bool KvCells::find_free(int32_t n, std::vector<int32_t>& out, int32_t stream) const {
     out.clear();
-    for (int32_t c = free_lo_; c < size() && (int32_t)out.size() < n; ++c)
+    if (stream < 0 || stream >= n_stream_) return n == 0;
+    const int32_t hi = stream_hi(stream);
+    for (int32_t c = free_lo_[stream]; c < hi && (int32_t)out.size() < n; ++c)
         if (pos_[c] < 0) out.push_back(c);
     return (int32_t)out.size() == n;
 }
@@ -115,13 +121,15 @@ void KvCells::apply(const std::vector<int32_t>& slots, const int32_t* pos, const
         used_ += 1;
         used_max_ = std::max(used_max_, c);
     }
-    while (free_lo_ < size() && pos_[free_lo_] >= 0) ++free_lo_;
+    for (int32_t s = 0; s < n_stream_; ++s)
+        while (free_lo_[s] < stream_hi(s) && pos_[free_lo_[s]] >= 0) ++free_lo_[s];
 }
 
 void KvCells::free_cell(int32_t c) {
     pos_[c] = -1;
     used_ -= 1;
-    free_lo_ = std::min(free_lo_, c);
+    const int32_t s = std::min(stream_of(c), n_stream_ - 1);
+    free_lo_[s] = std::min(free_lo_[s], c);
     while (used_max_ >= 0 && pos_[used_max_] < 0) --used_max_;
 }
 
@@ -153,39 +161,70 @@ void KvCells::seq_rm(int32_t s, int32_t p0, int32_t p1) {
     }
 }
 
-bool KvCells::defrag_order(std::vector<int32_t>& order) const {
+bool KvCells::defrag_order(std::vector<int32_t>& src) const {
     struct Key { int32_t seq, pos, cell; };
-    std::vector<Key> keys;
-    keys.reserve(used_);
-    for (int32_t cl = 0; cl < size(); ++cl) {
-        if (pos_[cl] < 0) continue;
-        int32_t s = 0;
-        while (s < kMaxSeq && !seq_[cl].test(s)) ++s;
-        keys.push_back({s, pos_[cl], cl});
-    }
-    std::sort(keys.begin(), keys.end(), [](const Key& a, const Key& b) {
-        if (a.seq != b.seq) return a.seq < b.seq;
-        if (a.pos != b.pos) return a.pos < b.pos;
-        return a.cell < b.cell;
-    });
-    order.resize(keys.size());
+    src.assign(size(), -1);
     bool moved = false;
-    for (size_t i = 0; i < keys.size(); ++i) {
-        order[i] = keys[i].cell;
-        moved = moved || keys[i].cell != (int32_t)i;
+    std::vector<Key> keys;
+    for (int32_t st = 0; st < n_stream_; ++st) {
+        keys.clear();
+        const int32_t lo = stream_lo(st), hi = stream_hi(st);
+        for (int32_t cl = lo; cl < hi; ++cl) {
+            if (pos_[cl] < 0) continue;
+            int32_t s = 0;
+            while (s < kMaxSeq && !seq_[cl].test(s)) ++s;
+            keys.push_back({s, pos_[cl], cl});
+        }
+        std::sort(keys.begin(), keys.end(), [](const Key& a, const Key& b) {
+            if (a.seq != b.seq) return a.seq < b.seq;
+            if (a.pos != b.pos) return a.pos < b.pos;
+            return a.cell < b.cell;
+        });
+        for (size_t i = 0; i < keys.size(); ++i) {
+            src[lo + i] = keys[i].cell;
+            moved = moved || keys[i].cell != lo + (int32_t)i;
+        }
     }
     return moved;
 }
 
-void KvCells::move(const std::vector<int32_t>& order) {
-    KvCells fresh(size(), (int32_t)seq_pos_.size());
+void KvCells::move(const std::vector<int32_t>& src) {
+    KvCells fresh(size(), (int32_t)seq_pos_.size(), n_stream_);
     std::vector<int32_t> slot(1), p(1);
-    for (size_t i = 0; i < order.size(); ++i) {
-        slot[0] = (int32_t)i;
-        p[0] = pos_[order[i]];
-        fresh.apply(slot, p.data(), &seq_[order[i]], 1);
+    for (int32_t i = 0; i < (int32_t)src.size(); ++i) {
+        if (src[i] < 0) continue;
+        slot[0] = i;
+        p[0] = pos_[src[i]];
+        fresh.apply(slot, p.data(), &seq_[src[i]], 1);
     }
     *this = std::move(fresh);
+}
+
+void split_equal(const std::vector<int32_t>& seq_of, int32_t n_ubatch, std::vector<int32_t>& order,
+                 std::vector<int32_t>& ub_off) {
+    std::map<int32_t, std::vector<int32_t>> queues;           // ascending sequence id
+    for (int32_t i = 0; i < (int32_t)seq_of.size(); ++i) queues[seq_of[i]].push_back(i);
+    std::map<int32_t, size_t> head;
+    order.clear();
+    ub_off.assign(1, 0);
+    std::vector<int32_t> sets;
+    while (true) {
+        sets.clear();
+        for (const auto& q : queues) {
+            if (head[q.first] >= q.second.size()) continue;
+            if (!sets.empty() && (q.first != sets.back() + 1 || (int32_t)sets.size() >= n_ubatch)) break;
+            sets.push_back(q.first);
+        }
+        if (sets.empty()) return;
+        size_t n_seq_tokens = (size_t)(n_ubatch / (int32_t)sets.size());
+        for (int32_t s : sets) n_seq_tokens = std::min(n_seq_tokens, queues[s].size() - head[s]);
+        for (int32_t s : sets) {
+            const auto& q = queues[s];
+            for (size_t k = 0; k < n_seq_tokens; ++k) order.push_back(q[head[s] + k]);
+            head[s] += n_seq_tokens;
+        }
+        ub_off.push_back((int32_t)order.size());
+    }
 }
 
 // ---------------------------------------------------------------------------------------------

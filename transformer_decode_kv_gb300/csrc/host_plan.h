@@ -36,12 +36,17 @@ bool sanitize_batch(int32_t n_tokens, const int32_t* token, const int32_t* pos,
                     int32_t n_vocab, int32_t n_seq_max, int32_t n_batch, const KvCells& cells,
                     SanBatch& out, std::string* why);
 
-// The cells of a unified cache. A cell holds one position (-1 = empty) and the set of sequences
-// that use it. Per sequence the library keeps its cells sorted by index (with their positions),
-// which is what the attention plan reads.
+// The cells of the cache. A cell holds one position (-1 = empty) and the set of sequences that
+// use it. Per sequence the library keeps its cells sorted by index (with their positions), which
+// is what the attention plan reads. n_stream > 1: a cache not shared by all sequences ([P1] Крок
+// 9-10, n_ctx divided among the sequences): stream s owns cells [s n_ctx_seq, (s + 1) n_ctx_seq),
+// n_ctx_seq = n_ctx / n_stream, and a token's cells come from its sequence's stream.
 class KvCells {
 public:
-    explicit KvCells(int32_t n_ctx = 0, int32_t n_seq_max = 1);
+    explicit KvCells(int32_t n_ctx = 0, int32_t n_seq_max = 1, int32_t n_stream = 1);
+
+    int32_t n_stream() const { return n_stream_; }
+    int32_t n_ctx_seq() const { return n_ctx_seq_; }
 
     int32_t size() const { return (int32_t)pos_.size(); }
     int32_t used() const { return used_; }
@@ -56,8 +61,9 @@ public:
     const std::vector<int32_t>& seq_cells(int32_t s) const { return sc_[s]; }
     const std::vector<int32_t>& seq_cell_pos(int32_t s) const { return sp_[s]; }
 
-    // The n lowest-index empty cells, ascending, without claiming them. False if fewer are empty.
-    bool find_free(int32_t n, std::vector<int32_t>& out) const;
+    // The n lowest-index empty cells of a stream, ascending, without claiming them. False if
+    // fewer are empty.
+    bool find_free(int32_t n, std::vector<int32_t>& out, int32_t stream = 0) const;
 
     // Commit tokens to cells (mctx->apply). Cells must be empty.
     void apply(const std::vector<int32_t>& slots, const int32_t* pos, const SeqSet* seqs, int32_t n);
@@ -67,11 +73,12 @@ public:
     void seq_rm(int32_t s, int32_t p0, int32_t p1);
 
     // Defrag ([P4] KVキャッシュの詳細, memory_update(optimize=true) and its "After Defrag"
-    // figure): the used cells packed from cell 0, ordered by their lowest sequence id, then
-    // position, then cell. order[i] = the old cell that new cell i takes. False if no cell moves.
-    bool defrag_order(std::vector<int32_t>& order) const;
-    // Rewrite the cells so that cell i holds what old cell order[i] held; the rest are empty.
-    void move(const std::vector<int32_t>& order);
+    // figure): in each stream the used cells packed from the stream's first cell, ordered by
+    // their lowest sequence id, then position, then cell. src[i] (size n_ctx) = the old cell that
+    // cell i takes, -1 = empty. False if no cell moves.
+    bool defrag_order(std::vector<int32_t>& src) const;
+    // Rewrite the cells so that cell i holds what old cell src[i] held (-1: empty).
+    void move(const std::vector<int32_t>& src);
 
 private:
     void drop_seq_from_cell(int32_t c, int32_t s);
@@ -83,8 +90,21 @@ private:
     std::vector<std::vector<int32_t>> sc_, sp_;         // per sequence: sorted cells, their pos
     int32_t used_ = 0;
     int32_t used_max_ = -1;
-    int32_t free_lo_ = 0;                               // every cell below it is used
+    int32_t n_stream_ = 1, n_ctx_seq_ = 0;
+    std::vector<int32_t> free_lo_;                      // per stream: its cells below are used
+    int32_t stream_lo(int32_t s) const { return n_stream_ == 1 ? 0 : s * n_ctx_seq_; }
+    int32_t stream_hi(int32_t s) const { return n_stream_ == 1 ? size() : (s + 1) * n_ctx_seq_; }
+    int32_t stream_of(int32_t c) const { return n_stream_ == 1 ? 0 : c / n_ctx_seq_; }
 };
+
+// split_equal(n_ubatch, sequential = true) ([P1] Крок 12: the splitter of a cache with more than
+// one stream; [P4] llama_ubatch: n_seq_tokens tokens per sequence set, n_seqs sets). Every token
+// has one sequence (seq_of). A ubatch takes the sequences with unused tokens in ascending id,
+// consecutive ids only, at most n_ubatch of them; each gives n_seq_tokens = min(n_ubatch /
+// n_seqs, fewest unused tokens among them) of its next tokens in batch order, listed sequence by
+// sequence. order = batch indices in ubatch order; ub_off = ubatch boundaries in order (n_ub + 1).
+void split_equal(const std::vector<int32_t>& seq_of, int32_t n_ubatch, std::vector<int32_t>& order,
+                 std::vector<int32_t>& ub_off);
 
 // Attention plan of one ubatch, after its cells are committed.
 //  - A "list" is the ascending set of cells shared with one distinct sequence set of the ubatch's

@@ -53,9 +53,9 @@ void launch_kv_quant_q8(const float* sk, const float* sv, int32_t ld, int32_t T,
 __host__ __device__ inline size_t kv_q8_scale_offset(int32_t Hkv, int32_t n_ctx, int32_t hd) {
     return (size_t)Hkv * (size_t)n_ctx * (size_t)hd;
 }
-// dst[g][i] = src[g][order[i]] for g < n_head (grid y), i < n: rows of row_bytes (a multiple of
-// 2), src rows strided by n_src rows per head, dst rows packed n per head. Used by the defrag to
-// gather the moved cells of one cache region before they are copied back.
+// dst[g][i] = src[g][order[i]] for g < n_head (grid y), i < n (zero where order[i] < 0): rows of
+// row_bytes (a multiple of 2), src rows strided by n_src rows per head, dst rows packed n per
+// head. Used by the defrag to gather one cache region in the new cell order.
 void launch_kv_gather(const void* src, void* dst, const int32_t* order, int32_t n, int32_t n_head,
                       int32_t n_src, int32_t row_bytes, cudaStream_t st);
 // u[t][j] = silu(g[t][j]) * up[t][j] with gu = [T][2F] (gate then up) -> u [T][F].

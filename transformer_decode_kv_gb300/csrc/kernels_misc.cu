@@ -144,7 +144,8 @@ __global__ void kv_gather_kernel(const U* __restrict__ src, U* __restrict__ dst,
     const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= (int64_t)n * upr) return;
     const int r = (int)(i / upr), u = (int)(i % upr);
-    dst[((int64_t)g * n + r) * upr + u] = src[((int64_t)g * n_src + order[r]) * upr + u];
+    const int o = order[r];
+    dst[((int64_t)g * n + r) * upr + u] = o >= 0 ? src[((int64_t)g * n_src + o) * upr + u] : U{};
 }
 
 __global__ void swiglu_kernel(const float* __restrict__ gu, int64_t T, int F,

@@ -147,6 +147,8 @@ struct llm_ctx {
     std::vector<unsigned long long> h_amax;
     bool h_logits_valid = false, h_argmax_valid = false;
     std::vector<int32_t> output_ids;
+    std::vector<int32_t> rows_by_rank;         // output row of the r-th output token in batch order
+    int32_t n_stream = 1;                      // LLM_CTX_KV_SPLIT: one stream per sequence
     int32_t n_outputs = 0;
 
     // control, debug
@@ -767,7 +769,8 @@ llm_ctx* llm_ctx_init(const llm_hparams* hp, const llm_cparams* cp) {
     c->type_v = cp->type_v;
     c->host_only = (cp->flags & LLM_CTX_HOST_ONLY) != 0;
     c->use_step = (cp->flags & LLM_CTX_FUSED_STEP) != 0;
-    c->cells = KvCells(c->n_ctx, c->n_seq_max);
+    c->n_stream = (cp->flags & LLM_CTX_KV_SPLIT) ? c->n_seq_max : 1;
+    c->cells = KvCells(c->n_ctx, c->n_seq_max, c->n_stream);
     c->layers.resize(h.n_layer);
     if (c->host_only) return c;
 
@@ -1084,6 +1087,7 @@ int32_t llm_decode(llm_ctx* c, llm_batch bt) {
     } timer{c, t0};
     c->n_outputs = 0;
     c->output_ids.clear();
+    c->rows_by_rank.clear();
     c->h_logits_valid = c->h_argmax_valid = false;
     if (!c->host_only && !c->ready && llm_weights_ready(c) != 0) return -1;
     if (!c->host_only) cudaSetDevice(c->device);
@@ -1094,13 +1098,49 @@ int32_t llm_decode(llm_ctx* c, llm_batch bt) {
         c->err = "invalid batch: " + why;
         return -1;
     }
-    // all slots before any commit ([P1] Крок 12): ubatch k takes the next lowest empty cells
+    // the ubatches ([P1] Крок 12): split_simple over a unified cache, split_equal over a split
+    // one; a split reorders the batch into ubatch order (orig maps back to batch indices)
+    std::vector<int32_t> ub_off, orig;
+    if (c->n_stream == 1) {
+        for (int32_t i0 = 0; i0 < b.n; i0 += c->n_ubatch) ub_off.push_back(i0);
+        ub_off.push_back(b.n);
+        orig.resize(b.n);
+        for (int32_t i = 0; i < b.n; ++i) orig[i] = i;
+    } else {
+        for (int32_t i = 0; i < b.n; ++i)
+            if (b.seqs[i].count() != 1) {
+                c->err = "invalid batch: a token of a split cache must belong to one sequence";
+                return -1;
+            }
+        split_equal(b.first_seq, c->n_ubatch, orig, ub_off);
+        SanBatch pb = b;
+        for (int32_t j = 0; j < b.n; ++j) {
+            const int32_t i = orig[j];
+            pb.token[j] = b.token[i]; pb.pos[j] = b.pos[i]; pb.seqs[j] = b.seqs[i];
+            pb.first_seq[j] = b.first_seq[i]; pb.output[j] = b.output[i];
+        }
+        b = std::move(pb);
+    }
+    // all slots before any commit: the tokens take the next lowest empty cells (of their stream)
     std::vector<int32_t> slots;
-    if (!c->cells.find_free(b.n, slots)) {
+    auto find_slots = [&]() {
+        if (c->n_stream == 1) return c->cells.find_free(b.n, slots);
+        slots.assign(b.n, -1);
+        std::vector<std::vector<int32_t>> of(c->n_stream);
+        for (int32_t j = 0; j < b.n; ++j) of[b.first_seq[j]].push_back(j);
+        std::vector<int32_t> got;
+        for (int32_t s = 0; s < c->n_stream; ++s) {
+            if (of[s].empty()) continue;
+            if (!c->cells.find_free((int32_t)of[s].size(), got, s)) return false;
+            for (size_t k = 0; k < got.size(); ++k) slots[of[s][k]] = got[k];
+        }
+        return true;
+    };
+    if (!find_slots()) {
         // one defrag, then one more search ([P4] KVキャッシュの詳細: FAILED_PREPARE -> defrag)
         const int moved = defrag(c);
         if (moved < 0) return -2;
-        if (moved == 0 || !c->cells.find_free(b.n, slots)) {
+        if (moved == 0 || !find_slots()) {
             c->err = "no KV slot for the batch";
             return 1;
         }
@@ -1111,9 +1151,8 @@ int32_t llm_decode(llm_ctx* c, llm_batch bt) {
     c->perf.n_decode_calls += 1;
     const int32_t G = c->hp.n_head / c->hp.n_head_kv;
     int32_t n_out = 0;
-    int32_t ub = 0;
-    for (int32_t i0 = 0; i0 < b.n; i0 += c->n_ubatch, ++ub) {
-        const int32_t T = std::min(c->n_ubatch, b.n - i0);
+    for (int32_t ub = 0; ub + 1 < (int32_t)ub_off.size(); ++ub) {
+        const int32_t i0 = ub_off[ub], T = ub_off[ub + 1] - ub_off[ub];
         std::vector<int32_t> us(slots.begin() + i0, slots.begin() + i0 + T);
         c->cells.apply(us, b.pos.data() + i0, b.seqs.data() + i0, T);       // mctx->apply()
         if (c->abort_cb && c->abort_cb(c->abort_ud)) {
@@ -1238,15 +1277,18 @@ int32_t llm_decode(llm_ctx* c, llm_batch bt) {
     c->n_outputs = n_out;
     c->output_ids.assign(b.n, -1);
     int32_t k = 0;
+    for (int32_t j = 0; j < b.n; ++j)                 // rows were written in ubatch order
+        if (b.output[j]) c->output_ids[orig[j]] = k++;
+    c->rows_by_rank.clear();
     for (int32_t i = 0; i < b.n; ++i)
-        if (b.output[i]) c->output_ids[i] = k++;
+        if (c->output_ids[i] >= 0) c->rows_by_rank.push_back(c->output_ids[i]);
     return 0;
 }
 
 static int32_t resolve_row(llm_ctx* c, int32_t i) {
-    if (i < 0) {
+    if (i < 0) {                                        // counted back from the last output
         const int32_t j = c->n_outputs + i;
-        return j >= 0 ? j : -1;
+        return j >= 0 && j < (int32_t)c->rows_by_rank.size() ? c->rows_by_rank[j] : -1;
     }
     if (i >= (int32_t)c->output_ids.size()) return -1;
     return c->output_ids[i];
@@ -1288,12 +1330,12 @@ int32_t llm_n_outputs(llm_ctx* c) { return c ? c->n_outputs : 0; }
 
 // Defrag: move the used cells' K/V rows (every layer) to their new cells, then rewrite the cell
 // metadata. Each cache region (per layer K and V; Q8_0: quants and scales) is gathered into a
-// scratch region in the new order, then copied back as one packed run per KV head.
+// scratch region in the new cell order (empty cells zeroed), then copied back whole.
 static int defrag(llm_ctx* c) {
     std::vector<int32_t> order;
     if (!c->cells.defrag_order(order)) return 0;
     if (!c->host_only) {
-        const int32_t n = (int32_t)order.size(), Hkv = c->hp.n_head_kv, hd = c->hp.head_dim;
+        const int32_t n = c->n_ctx, Hkv = c->hp.n_head_kv, hd = c->hp.head_dim;
         if (!c->kv_scratch && !dalloc(c, &c->kv_scratch, c->kv_layer_bytes())) return -1;
         if (!c->d_order && !dalloc(c, &c->d_order, (size_t)c->n_ctx)) return -1;
         if (!cuda_ok(c, cudaMemcpyAsync(c->d_order, order.data(), sizeof(int32_t) * n, cudaMemcpyHostToDevice,
@@ -1312,9 +1354,8 @@ static int defrag(llm_ctx* c) {
                 uint8_t* layer = static_cast<uint8_t*>(base) + (size_t)il * c->kv_layer_bytes();
                 for (const Region& r : regions) {
                     launch_kv_gather(layer + r.off, c->kv_scratch, c->d_order, n, Hkv, c->n_ctx, r.rb, c->st);
-                    if (!cuda_ok(c, cudaMemcpy2DAsync(layer + r.off, (size_t)c->n_ctx * r.rb, c->kv_scratch,
-                                                      (size_t)n * r.rb, (size_t)n * r.rb, Hkv,
-                                                      cudaMemcpyDeviceToDevice, c->st), "copy"))
+                    if (!cuda_ok(c, cudaMemcpyAsync(layer + r.off, c->kv_scratch, (size_t)Hkv * n * r.rb,
+                                                    cudaMemcpyDeviceToDevice, c->st), "copy"))
                         return -1;
                 }
             }
@@ -1354,6 +1395,7 @@ uint32_t llm_n_ctx(llm_ctx* c) { return c ? (uint32_t)c->n_ctx : 0; }
 uint32_t llm_n_batch(llm_ctx* c) { return c ? (uint32_t)c->n_batch : 0; }
 uint32_t llm_n_ubatch(llm_ctx* c) { return c ? (uint32_t)c->n_ubatch : 0; }
 int32_t llm_kv_used_cells(llm_ctx* c) { return c ? c->cells.used() : 0; }
+uint32_t llm_n_ctx_seq(llm_ctx* c) { return c ? (uint32_t)(c->n_ctx / c->n_stream) : 0; }
 
 const char* llm_last_error(llm_ctx* c) { return c ? c->err.c_str() : g_init_error.c_str(); }
 
