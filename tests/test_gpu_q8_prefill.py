@@ -1,0 +1,45 @@
+"""GPU parity of Q8_0 prefill on the tensor cores (each Q8_0 weight d*q as two bf16 terms, hi + lo,
+in the token-major tcgen05 GEMM) on a 2-layer model of the Llama-3-8B layer shape with Q8_0
+linear weights and F32 embeddings/norms (the 8k workload's types), through the C ABI.
+
+A 512-token prompt (one ubatch: every GEMM on the tensor cores) then greedy steps (Q8_0 GEMVs),
+against the oracle: every flagged logits row within the 2e-2 bar (expected ~1e-4: the terms hold
+the weights to 16 bits and the activations enter as two bf16 terms too)."""
+import numpy as np
+import pytest
+
+import synthetic as S
+from synthetic.configs import HParams, Workload
+from tests import gpu_common as G
+
+pytestmark = pytest.mark.gpu
+
+HP = HParams(n_layer=2, n_embd=4096, n_head=32, n_head_kv=8, head_dim=128, n_ff=14336,
+             n_vocab=32000, rope_freq_base=500000.0, rms_eps=1e-5)
+KEY = "llama8b_layers2_q8_0"
+TOL = 2e-2
+
+
+def test_q8_0_prefill_on_tensor_cores_matches_oracle():
+    S.WORKLOADS[KEY] = Workload(KEY, HP, {"embd": S.F32, "linear": S.Q8_0}, S.F16, n_ctx=1024,
+                                n_seq=1, n_prompt=512, n_batch=512, n_ubatch=512, n_decode=4,
+                                weight_seed=3400, prompt_seed=4400)
+    G.device_model.cache_clear()
+    G.oracle_weights.cache_clear()
+    ctx = G.library_ctx(KEY)
+    ora = G.oracle_ctx(KEY)
+    toks = G.prompts(KEY)[0]
+    flags = np.zeros(512, dtype=np.int8)
+    flags[[0, 100, 300, 511]] = 1
+    assert ctx.decode(toks, logits=flags) == 0, ctx.last_error()
+    assert ora.decode(toks, logits=flags) == 0
+    assert ctx.perf()["n_ubatches"] == 1
+    errs = []
+    for i in (0, 100, 300, 511):
+        errs.append(G.rel_err(ctx.get_logits_ith(i), ora.get_logits_ith(i)))
+    print("Q8_0 prefill rows:", errs)
+    assert max(errs) <= TOL, errs
+    assert max(errs) <= 1e-3, errs              # the two-term weights keep it near float32
+    rep = G.greedy_compare(ctx, ora, 1, [511], 4, TOL, {})
+    print("Q8_0 steps:", rep)
+    ctx.free()

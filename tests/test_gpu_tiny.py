@@ -144,3 +144,19 @@ def test_error_paths_on_gpu():
     assert ref.decode(np.zeros(256 - used + 1, dtype=np.int32)) in (1, -1)
     assert ref.kv_used_cells() == used
     ctx.free(); ref.free()
+
+
+@pytest.mark.parametrize("tkv", [oracle.F16, oracle.Q8_0])
+def test_tiny_long_context_decode(tkv):
+    """A 2000-token prompt (several 64-cell passes per block of the decode attention, both warp
+    groups busy) then greedy steps, against the oracle; F16 and Q8_0 caches."""
+    key = "tiny_f32_1seq"
+    over = dict(n_ctx=4096, n_batch=2048, n_ubatch=512, type_k=tkv, type_v=tkv)
+    ctx, ora = G.library_ctx(key, **over), G.oracle_ctx(key, **over)
+    toks = S.prompt_tokens(4242, 2000, S.WORKLOADS[key].hp.n_vocab).numpy()
+    assert ctx.decode(toks) == 0, ctx.last_error()
+    assert ora.decode(toks) == 0
+    tol = TOL if tkv == oracle.F16 else 1e-3
+    rep = G.greedy_compare(ctx, ora, 1, [len(toks) - 1], 6, tol, {})
+    print("long context", tkv, rep)
+    ctx.free()

@@ -36,8 +36,11 @@ namespace {
 using namespace attn;
 
 constexpr int kCL = 16;                  // blocks per cluster (non-portable size, opted in)
-constexpr int kCH = 64;                  // cells per pass (two per lane)
-constexpr int kGQ = 4;                   // query heads per KV head: one warp each
+constexpr int kCH = 64;                  // cells per pass
+constexpr int kGQ = 4;                   // query heads per KV head: one warp each per group
+constexpr int kGroups = 2;               // warp groups, each taking half of every pass
+constexpr int kCG = kCH / kGroups;       // cells per group and pass: one per lane
+constexpr int kThreads = kGQ * 32 * kGroups;
 
 template <typename KT> __device__ __forceinline__ float kvf(KT v);
 template <> __device__ __forceinline__ float kvf<float>(float v) { return v; }
@@ -71,30 +74,51 @@ struct DecSmem {
     static constexpr int NB = HD / 32;                    // Q8_0 blocks per row
     static constexpr int RB = HD * (int)sizeof(KT);       // bytes of a cached row
     static constexpr int RS = RB + 16;                    // padded stride
-    static constexpr size_t bytes = 2 * (size_t)kCH * RS + (size_t)kGQ * HD * 4 /* q */ +
-                                    (size_t)kGQ * (HD + 2) * 4 /* partial */ + 3 * kCH * 4 +
-                                    (Q8 ? 2 * (size_t)kCH * NB * 4 : 0) /* scales */ + 16;
+    // one pass: K rows, V rows, then per cell: cell, visible, fresh (+ Q8_0: K and V scales)
+    static constexpr size_t rows = 2 * (size_t)kCH * RS;
+    static constexpr size_t stage = rows + 3 * kCH * 4 + (Q8 ? 2 * (size_t)kCH * NB * 4 : 0);
+    static constexpr size_t bytes = 2 * stage + (size_t)kGQ * HD * 4 /* q */ +
+                                    2 * (size_t)kGQ * (HD + 2) * 4 /* block and group partials */ + 16;
 };
 
+template <typename KT>
+struct Stage {
+    uint8_t* kb;
+    uint8_t* vb;
+    int* ccell;
+    int* cvis;
+    int* cfresh;
+    float* ksc;
+    float* vsc;
+};
 
 }  // namespace
 
+// Two warp groups: group g takes cells [32 g, 32 g + 32) of every pass of 64 (one cell per lane
+// for the scores), warp g * 4 + h holds query head h of the KV head's group. Passes are double
+// buffered: the rows of pass i + 1 are in flight while pass i is computed.
 template <int HD, typename KT>
-__global__ void __launch_bounds__(kGQ * 32)
+__global__ void __launch_bounds__(kThreads)
 attn_decode_kernel(AttnArgs a, float scale_log2) {
     using SM = DecSmem<HD, KT>;
     constexpr int RB = SM::RB, RS = SM::RS, VPR = RB / 16, DPL = HD / 32, NB = SM::NB;
     constexpr bool Q8 = SM::Q8;
     extern __shared__ __align__(16) uint8_t sm[];
-    uint8_t* kb = sm;                                          // [kCH][RS]
-    uint8_t* vb = kb + kCH * RS;                               // [kCH][RS]
-    float* qs = reinterpret_cast<float*>(vb + kCH * RS);       // [kGQ][HD]
-    float* pst = qs + kGQ * HD;                                // partial: m[kGQ], l[kGQ], o[kGQ][HD]
-    int* ccell = reinterpret_cast<int*>(pst + kGQ * (HD + 2)); // [kCH]
-    int* cvis = ccell + kCH;                                   // [kCH]
-    int* cfresh = cvis + kCH;                                  // [kCH]
-    float* ksc = reinterpret_cast<float*>(cfresh + kCH);       // Q8_0: [kCH][NB] K scales
-    float* vsc = ksc + kCH * NB;                               //        [kCH][NB] V scales
+    auto stage_of = [&](int s) {
+        uint8_t* b = sm + (size_t)s * SM::stage;
+        Stage<KT> S;
+        S.kb = b;
+        S.vb = b + kCH * RS;
+        S.ccell = reinterpret_cast<int*>(b + SM::rows);
+        S.cvis = S.ccell + kCH;
+        S.cfresh = S.cvis + kCH;
+        S.ksc = reinterpret_cast<float*>(S.cfresh + kCH);
+        S.vsc = S.ksc + kCH * NB;
+        return S;
+    };
+    float* qs = reinterpret_cast<float*>(sm + 2 * SM::stage);          // [kGQ][HD]
+    float* pst = qs + kGQ * HD;                                         // block partial (peers read it)
+    float* gst = pst + kGQ * (HD + 2);                                  // group 1's partial
 
     const uint32_t rank = cluster_rank();
     const int kvh = blockIdx.y, tile = blockIdx.z;
@@ -102,6 +126,7 @@ attn_decode_kernel(AttnArgs a, float scale_log2) {
     // the plan was uploaded before the step's first kernel: readable before griddepcontrol.wait
     if (tile >= a.hdr[1]) return;                               // whole cluster (same tile)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int grp = warp / kGQ, hq = warp % kGQ;
     const int4 td0 = a.tile_desc[2 * tile];
     const int4 td1 = a.tile_desc[2 * tile + 1];
     const int base = td1.y, len = td1.z;
@@ -109,26 +134,22 @@ attn_decode_kernel(AttnArgs a, float scale_log2) {
     const int tpos = a.tok_pos[t];
     const int chunk = (len + kCL - 1) / kCL;
     const int c0 = min(len, (int)rank * chunk), c1 = min(len, c0 + chunk);
+    const int npass = c1 > c0 ? (c1 - c0 + kCH - 1) / kCH : 1;  // at least one: the wait is in it
     const uint8_t* K = static_cast<const uint8_t*>(a.kc) + (int64_t)kvh * a.n_ctx * RB;
     const uint8_t* V = static_cast<const uint8_t*>(a.vc) + (int64_t)kvh * a.n_ctx * RB;
     const __half* KS = q8_scales(a.kc, a, kvh);
     const __half* VS = q8_scales(a.vc, a, kvh);
-    auto load_scales = [&](int c, int cell) {
+    auto load_scales = [&](const Stage<KT>& S, int c, int cell) {
 #pragma unroll
         for (int b = 0; b < NB; ++b) {
-            ksc[c * NB + b] = ld_scale(KS + (int64_t)cell * NB + b);
-            vsc[c * NB + b] = ld_scale(VS + (int64_t)cell * NB + b);
+            S.ksc[c * NB + b] = ld_scale(KS + (int64_t)cell * NB + b);
+            S.vsc[c * NB + b] = ld_scale(VS + (int64_t)cell * NB + b);
         }
     };
-
-    float m = -INFINITY, l = 0.f, o[DPL];
-#pragma unroll
-    for (int e = 0; e < DPL; ++e) o[e] = 0.f;
-    bool waited = false;
-    // at least one (possibly empty) pass, so the first wait always happens inside the loop
-    for (int cb = c0; cb < c1 || (cb == c0 && !waited); cb += kCH) {
+    // cell list of pass i into stage S (threads < kCH); before the wait, fresh cells' scales wait
+    auto setup = [&](int i, const Stage<KT>& S, bool pre_wait) {
         if (threadIdx.x < kCH) {
-            const int ci = cb + threadIdx.x;
+            const int ci = c0 + i * kCH + threadIdx.x;
             int cell = -1, vis = 0, fresh = 0;
             if (ci < c1) {
                 const int cc = a.list_cells[base + ci];
@@ -138,53 +159,72 @@ attn_decode_kernel(AttnArgs a, float scale_log2) {
                     for (int j = 0; j < a.n_tok; ++j) fresh |= a.slot[j] == cc;
                 }
             }
-            ccell[threadIdx.x] = cell;
-            cvis[threadIdx.x] = vis && cell >= 0;
-            cfresh[threadIdx.x] = fresh;
+            S.ccell[threadIdx.x] = cell;
+            S.cvis[threadIdx.x] = vis && cell >= 0;
+            S.cfresh[threadIdx.x] = fresh;
             if constexpr (Q8) {
-                if (vis && cell >= 0 && !fresh) load_scales(threadIdx.x, cell);
+                if (vis && cell >= 0 && !(pre_wait && fresh)) load_scales(S, threadIdx.x, cell);
             }
         }
-        __syncthreads();
-        // rows of earlier steps: staged now, possibly before the previous kernel has ended
-        for (int v = threadIdx.x; v < kCH * VPR; v += blockDim.x) {
+    };
+    auto issue = [&](const Stage<KT>& S, bool pre_wait) {
+        for (int v = threadIdx.x; v < kCH * VPR; v += kThreads) {
             const int c = v / VPR, j = v % VPR;
-            if (!cvis[c] || cfresh[c]) continue;
-            const size_t src = (size_t)ccell[c] * RB + j * 16;
-            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sm32(kb + c * RS + j * 16)), "l"(K + src) : "memory");
-            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sm32(vb + c * RS + j * 16)), "l"(V + src) : "memory");
+            if (!S.cvis[c] || (pre_wait && S.cfresh[c])) continue;
+            const size_t src = (size_t)S.ccell[c] * RB + j * 16;
+            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sm32(S.kb + c * RS + j * 16)), "l"(K + src) : "memory");
+            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sm32(S.vb + c * RS + j * 16)), "l"(V + src) : "memory");
         }
         asm volatile("cp.async.commit_group;" ::: "memory");
-        if (!waited) {
-            asm volatile("griddepcontrol.wait;" ::: "memory");
-            waited = true;
-            for (int i = threadIdx.x; i < kGQ * HD; i += blockDim.x)
-                qs[i] = a.q[(int64_t)t * a.ldq + (kvh * kGQ + i / HD) * HD + i % HD] * scale_log2;
-        }
+    };
+
+    // pass 0: rows of earlier steps staged now, possibly before the previous kernel has ended
+    {
+        const Stage<KT> S0 = stage_of(0);
+        setup(0, S0, true);
+        __syncthreads();
+        issue(S0, true);
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+        for (int i = threadIdx.x; i < kGQ * HD; i += kThreads)
+            qs[i] = a.q[(int64_t)t * a.ldq + (kvh * kGQ + i / HD) * HD + i % HD] * scale_log2;
         // rows written by this step's projection kernel: only now
-        if constexpr (Q8) {
-            if (threadIdx.x < kCH && cvis[threadIdx.x] && cfresh[threadIdx.x])
-                load_scales(threadIdx.x, ccell[threadIdx.x]);
-        }
-        for (int v = threadIdx.x; v < kCH * VPR; v += blockDim.x) {
+        for (int v = threadIdx.x; v < kCH * VPR; v += kThreads) {
             const int c = v / VPR, j = v % VPR;
-            if (!cvis[c] || !cfresh[c]) continue;
-            const size_t src = (size_t)ccell[c] * RB + j * 16;
-            *reinterpret_cast<uint4*>(kb + c * RS + j * 16) = __ldcg(reinterpret_cast<const uint4*>(K + src));
-            *reinterpret_cast<uint4*>(vb + c * RS + j * 16) = __ldcg(reinterpret_cast<const uint4*>(V + src));
+            if (!S0.cvis[c] || !S0.cfresh[c]) continue;
+            const size_t src = (size_t)S0.ccell[c] * RB + j * 16;
+            *reinterpret_cast<uint4*>(S0.kb + c * RS + j * 16) = __ldcg(reinterpret_cast<const uint4*>(K + src));
+            *reinterpret_cast<uint4*>(S0.vb + c * RS + j * 16) = __ldcg(reinterpret_cast<const uint4*>(V + src));
         }
-        asm volatile("cp.async.wait_all;" ::: "memory");
+        if constexpr (Q8) {
+            if (threadIdx.x < kCH && S0.cvis[threadIdx.x] && S0.cfresh[threadIdx.x])
+                load_scales(S0, threadIdx.x, S0.ccell[threadIdx.x]);
+        }
+    }
+
+    float m = -INFINITY, l = 0.f, o[DPL];
+#pragma unroll
+    for (int e = 0; e < DPL; ++e) o[e] = 0.f;
+    const float* q = qs + hq * HD;
+    for (int i = 0; i < npass; ++i) {
+        const Stage<KT> S = stage_of(i & 1);
+        if (i + 1 < npass) {
+            // the other stage was last read by pass i - 1, which ended at the barrier below
+            const Stage<KT> N = stage_of((i + 1) & 1);
+            setup(i + 1, N, false);
+            __syncthreads();
+            issue(N, false);
+            asm volatile("cp.async.wait_group 1;" ::: "memory");
+        } else {
+            asm volatile("cp.async.wait_group 0;" ::: "memory");
+        }
         __syncthreads();
 
-        // scores of query head `warp`: lanes own cells lane and lane + 32
-        const float* q = qs + warp * HD;
-        float s[2];
-#pragma unroll
-        for (int h2 = 0; h2 < 2; ++h2) {
-            const int c = lane + 32 * h2;
-            s[h2] = -INFINITY;
-            if (Q8 && cvis[c]) {
-                const uint8_t* kr = kb + c * RS;
+        // score of this lane's cell for query head hq
+        const int c = grp * kCG + lane;
+        float s = -INFINITY;
+        if (S.cvis[c]) {
+            const uint8_t* kr = S.kb + c * RS;
+            if constexpr (Q8) {
                 float acc = 0.f;
 #pragma unroll
                 for (int b = 0; b < NB; ++b) {
@@ -200,11 +240,10 @@ attn_decode_kernel(AttnArgs a, float scale_log2) {
                             p1 = fmaf(q[j * 16 + e + 1], (float)ke[e + 1], p1);
                         }
                     }
-                    acc = fmaf(ksc[c * NB + b], p0 + p1, acc);
+                    acc = fmaf(S.ksc[c * NB + b], p0 + p1, acc);
                 }
-                s[h2] = acc;
-            } else if (cvis[c]) {
-                const uint8_t* kr = kb + c * RS;
+                s = acc;
+            } else {
                 float a0 = 0.f, a1 = 0.f;
 #pragma unroll
                 for (int j = 0; j < VPR; ++j) {
@@ -217,46 +256,59 @@ attn_decode_kernel(AttnArgs a, float scale_log2) {
                         a1 = fmaf(q[j * EPV + e + 1], kvf<KT>(ke[e + 1]), a1);
                     }
                 }
-                s[h2] = a0 + a1;
+                s = a0 + a1;
             }
         }
-        float mx = fmaxf(s[0], s[1]);
+        float mx = s;
         for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
         const float m_new = fmaxf(m, mx);
-        float p[2] = {0.f, 0.f}, corr = 1.f;
+        float p = 0.f, corr = 1.f;
         if (m_new != -INFINITY) {
             corr = exp2f(m - m_new);
-            p[0] = exp2f(s[0] - m_new);
-            p[1] = exp2f(s[1] - m_new);
+            p = exp2f(s - m_new);
         }
-        float ps = p[0] + p[1];
+        float ps = p;
         for (int off = 16; off > 0; off >>= 1) ps += __shfl_xor_sync(0xffffffffu, ps, off);
         l = l * corr + ps;
         m = m_new;
 #pragma unroll
         for (int e = 0; e < DPL; ++e) o[e] *= corr;
 #pragma unroll 4
-        for (int c = 0; c < kCH; ++c) {
-            const float pc = __shfl_sync(0xffffffffu, p[c >> 5], c & 31);
+        for (int k = 0; k < kCG; ++k) {
+            const float pc = __shfl_sync(0xffffffffu, p, k);
             if (pc == 0.f) continue;
-            const KT* vr = reinterpret_cast<const KT*>(vb + c * RS) + lane * DPL;
-            const float pd = Q8 ? pc * vsc[c * NB + lane * DPL / 32] : pc;
+            const int c2 = grp * kCG + k;
+            const KT* vr = reinterpret_cast<const KT*>(S.vb + c2 * RS) + lane * DPL;
+            const float pd = Q8 ? pc * S.vsc[c2 * NB + lane * DPL / 32] : pc;
 #pragma unroll
             for (int e = 0; e < DPL; ++e) o[e] = fmaf(pd, kvf<KT>(vr[e]), o[e]);
         }
-        __syncthreads();
+        __syncthreads();                                        // stage S free for pass i + 2
     }
 
-    // this block's partial state of its 4 query heads, then the cluster-wide merge
+    // the two groups' states merge into this block's partial, then the cluster-wide merge
     float* pm = pst;
     float* pl = pst + kGQ;
     float* po = pst + 2 * kGQ;
-    if (lane == 0) { pm[warp] = m; pl[warp] = l; }
+    if (grp == 1) {
+        if (lane == 0) { gst[hq] = m; gst[kGQ + hq] = l; }
 #pragma unroll
-    for (int e = 0; e < DPL; ++e) po[warp * HD + lane * DPL + e] = o[e];
+        for (int e = 0; e < DPL; ++e) gst[2 * kGQ + hq * HD + lane * DPL + e] = o[e];
+    }
+    __syncthreads();
+    if (grp == 0) {
+        const float m1 = gst[hq], l1 = gst[kGQ + hq];
+        const float M = fmaxf(m, m1);
+        const float f0 = m == -INFINITY ? 0.f : exp2f(m - M);
+        const float f1 = m1 == -INFINITY ? 0.f : exp2f(m1 - M);
+        if (lane == 0) { pm[hq] = M; pl[hq] = l * f0 + l1 * f1; }
+#pragma unroll
+        for (int e = 0; e < DPL; ++e)
+            po[hq * HD + lane * DPL + e] = o[e] * f0 + gst[2 * kGQ + hq * HD + lane * DPL + e] * f1;
+    }
     cluster_sync_all();
     constexpr int OPB = kGQ * HD / kCL;                        // outputs merged per block
-    for (int i = threadIdx.x; i < OPB; i += blockDim.x) {
+    for (int i = threadIdx.x; i < OPB; i += kThreads) {
         const int idx = (int)rank * OPB + i;
         const int g = idx / HD, dd = idx % HD;
         float M = -INFINITY;
@@ -289,7 +341,7 @@ bool launch_dec(const AttnArgs& a, cudaStream_t st) {
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(kCL, a.Hkv, a.n_tok);
-    cfg.blockDim = dim3(kGQ * 32);
+    cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
     cudaLaunchAttribute attr_l[2];

@@ -23,6 +23,31 @@ __device__ __forceinline__ void fma2(float& a0, float& a1, float w0, float w1, f
         : "+f"(a0), "+f"(a1) : "f"(w0), "f"(w1), "f"(x0), "f"(x1));
 }
 
+// (a0, a1) -= (b, b) as one paired instruction.
+__device__ __forceinline__ void sub2(float& a0, float& a1, float b) {
+    asm("{\n\t.reg .b64 v, s;\n\tmov.b64 v, {%0, %1};\n\tmov.b64 s, {%2, %2};\n\t"
+        "sub.rn.f32x2 v, v, s;\n\tmov.b64 {%0, %1}, v;\n\t}"
+        : "+f"(a0), "+f"(a1) : "f"(b));
+}
+
+// 16 int8 quants -> their values as floats without an int-to-float conversion: each byte, biased
+// by 128, becomes the low mantissa byte of 2^23 (exponent byte 0x4B), and 2^23 + 128 is
+// subtracted exactly.
+__device__ __forceinline__ void unpack_q8_raw(const uint4 v, float* w) {
+    const uint32_t u[4] = {v.x ^ 0x80808080u, v.y ^ 0x80808080u, v.z ^ 0x80808080u, v.w ^ 0x80808080u};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+#pragma unroll
+        for (int b = 0; b < 4; b += 2) {
+            float f0 = __int_as_float((int)__byte_perm(u[i], 0x4B000000u, 0x7540u + b));
+            float f1 = __int_as_float((int)__byte_perm(u[i], 0x4B000000u, 0x7540u + b + 1));
+            sub2(f0, f1, 8388736.0f);
+            w[4 * i + b] = f0;
+            w[4 * i + b + 1] = f1;
+        }
+    }
+}
+
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }

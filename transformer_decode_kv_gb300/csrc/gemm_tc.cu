@@ -328,7 +328,9 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 // weight-major kernel. The accumulator D[128 tokens][256] has one token per TMEM lane: each thread
 // owns its token's 256 outputs. SwiGLU writes silu(g) * u of 128 consecutive features as bf16
 // hi and lo terms; store / residual add write float32, through vector atomic adds when the K
-// range is split over blockIdx.z (the output then starts zeroed for a store).
+// range is split over blockIdx.z (the output then starts zeroed for a store). With a second weight
+// map (tmWlo) the weights are two bf16 terms too (a Q8_0 weight d*q as hi + lo): the K loop runs
+// over both weight terms, each against both activation terms.
 constexpr int kTnRows = 128;                     // tokens per tile (MMA M)
 constexpr int kTnN = 256;                        // 128 gate + 128 up rows (MMA N)
 constexpr uint32_t kTnA = kTnRows * kBK * 2;     // 16 KB per activation term
@@ -340,7 +342,8 @@ constexpr size_t kTnSmem = 1024 + (size_t)kTnStages * kTnStage + 256;
 template <int EPI>
 __global__ void __launch_bounds__(128, 1)
 gemm_tn_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmXlo,
-               const __grid_constant__ CUtensorMap tmW, int K, int T, int M, int F,
+               const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmWlo,
+               int planes, int K, int T, int M, int F,
                void* __restrict__ Y, void* __restrict__ Y2, int ldy, uint32_t* __restrict__ err) {
     constexpr int S = kTnStages;
     extern __shared__ uint8_t smem_raw[];
@@ -354,7 +357,8 @@ gemm_tn_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nk_all = K / kBK;
     const int per = (nk_all + gridDim.z - 1) / gridDim.z;
-    const int kb0 = min(nk_all, (int)blockIdx.z * per), nk = min(nk_all, kb0 + per) - kb0;
+    const int kb0 = min(nk_all, (int)blockIdx.z * per), nkp = min(nk_all, kb0 + per) - kb0;
+    const int nk = nkp * planes;                     // k-steps: this split's K range per weight term
     const int t0 = blockIdx.x * kTnRows;             // token tiles run fastest (weight reuse in L2)
     // SwiGLU: first gate/up feature of the tile; otherwise the first of its 256 weight rows
     const int f0 = blockIdx.y * (EPI == GEMM_EPI_SWIGLU ? kTnN / 2 : kTnN);
@@ -371,6 +375,8 @@ gemm_tn_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmX)) : "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmXlo)) : "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmW)) : "memory");
+        if (planes > 1)
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmWlo)) : "memory");
     }
     if (warp == 0) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -393,11 +399,12 @@ gemm_tn_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
             if (*(volatile int*)abort_flag) break;
             uint8_t* st = smem + (size_t)s * kTnStage;
             mbar_expect_tx(&full[s], kTnStage);
-            const int kx = (kb0 + kb) * kBK;
+            const int kx = (kb0 + kb % nkp) * kBK;
+            const CUtensorMap* wm = kb < nkp ? &tmW : &tmWlo;
             tma_load_2d(st, &tmX, &full[s], kx, t0);
             tma_load_2d(st + kTnA, &tmXlo, &full[s], kx, t0);
-            tma_load_2d(st + 2 * kTnA, &tmW, &full[s], kx, f0);
-            tma_load_2d(st + 2 * kTnA + kTnB / 2, &tmW, &full[s], kx, w2);
+            tma_load_2d(st + 2 * kTnA, wm, &full[s], kx, f0);
+            tma_load_2d(st + 2 * kTnA + kTnB / 2, wm, &full[s], kx, w2);
             issued = kb + 1;
         }
         for (int kb = (issued > S ? issued - S : 0); kb < issued; ++kb)
@@ -561,8 +568,9 @@ bool tc_swiglu_tn_ok(int64_t K, int64_t F) { return K % kBK == 0 && K >= kBK && 
 bool tc_tn_ok(int64_t M, int64_t K) { return K % kBK == 0 && K >= kBK && M % kTnN == 0 && M > 0; }
 
 template <int EPI>
-bool launch_tn(const CUtensorMap& xmap, const CUtensorMap& xmap_lo, const CUtensorMap& wmap, int K,
-               int T, int M, int F, void* Y, void* Y2, int ldy, int splits, uint32_t* err, cudaStream_t st) {
+bool launch_tn(const CUtensorMap& xmap, const CUtensorMap& xmap_lo, const CUtensorMap& wmap,
+               const CUtensorMap* wmap_lo, int K, int T, int M, int F, void* Y, void* Y2, int ldy,
+               int splits, uint32_t* err, cudaStream_t st) {
     auto k = gemm_tn_kernel<EPI>;
     static bool attr = false;
     if (!attr) {
@@ -572,14 +580,16 @@ bool launch_tn(const CUtensorMap& xmap, const CUtensorMap& xmap_lo, const CUtens
     }
     const int ntile = EPI == GEMM_EPI_SWIGLU ? F / (kTnN / 2) : M / kTnN;
     dim3 grid((T + kTnRows - 1) / kTnRows, ntile, splits);
-    k<<<grid, 128, kTnSmem, st>>>(xmap, xmap_lo, wmap, K, T, M, F, Y, Y2, ldy, err);
+    k<<<grid, 128, kTnSmem, st>>>(xmap, xmap_lo, wmap, wmap_lo ? *wmap_lo : wmap, wmap_lo ? 2 : 1, K, T,
+                                  M, F, Y, Y2, ldy, err);
     return cudaGetLastError() == cudaSuccess;
 }
 
 bool launch_gemm_swiglu_tn(const CUtensorMap& xmap, const CUtensorMap& xmap_lo, const CUtensorMap& wmap,
-                           int K, int T, int F, void* Y, void* Y2, int ldy, uint32_t* err, cudaStream_t st) {
+                           int K, int T, int F, void* Y, void* Y2, int ldy, uint32_t* err, cudaStream_t st,
+                           const CUtensorMap* wmap_lo) {
     if (T <= 0) return true;
-    return launch_tn<GEMM_EPI_SWIGLU>(xmap, xmap_lo, wmap, K, T, 0, F, Y, Y2, ldy, 1, err, st);
+    return launch_tn<GEMM_EPI_SWIGLU>(xmap, xmap_lo, wmap, wmap_lo, K, T, 0, F, Y, Y2, ldy, 1, err, st);
 }
 
 int tc_tn_splits(int64_t M, int64_t K, int T, int n_sm) {
@@ -591,12 +601,13 @@ int tc_tn_splits(int64_t M, int64_t K, int T, int n_sm) {
 }
 
 bool launch_gemm_tn(const CUtensorMap& xmap, const CUtensorMap& xmap_lo, const CUtensorMap& wmap, int epi,
-                    int K, int M, int T, float* Y, int ldy, int splits, uint32_t* err, cudaStream_t st) {
+                    int K, int M, int T, float* Y, int ldy, int splits, uint32_t* err, cudaStream_t st,
+                    const CUtensorMap* wmap_lo) {
     if (T <= 0) return true;
     if (epi == GEMM_EPI_STORE)
-        return launch_tn<GEMM_EPI_STORE>(xmap, xmap_lo, wmap, K, T, M, 0, Y, nullptr, ldy, splits, err, st);
+        return launch_tn<GEMM_EPI_STORE>(xmap, xmap_lo, wmap, wmap_lo, K, T, M, 0, Y, nullptr, ldy, splits, err, st);
     if (epi == GEMM_EPI_ADD)
-        return launch_tn<GEMM_EPI_ADD>(xmap, xmap_lo, wmap, K, T, M, 0, Y, nullptr, ldy, splits, err, st);
+        return launch_tn<GEMM_EPI_ADD>(xmap, xmap_lo, wmap, wmap_lo, K, T, M, 0, Y, nullptr, ldy, splits, err, st);
     return false;
 }
 

@@ -261,14 +261,24 @@ gemv_bulk_kernel(const GemvArgs a) {
 #pragma unroll
                         for (int k2 = 0; k2 < kMaxSpw; ++k2) {
                             const uint4 wv = *reinterpret_cast<const uint4*>(st0 + (size_t)i * row_bytes + k2 * kSlice);
-                            float d = 0.f;
-                            if (Q8)
-                                d = __half2float(ssc[((size_t)i * row_bytes + (warp * spw + k2) * kSlice + lane * 16) / 32]);
                             float w[VN];
-                            unpack16<WT>(wv, d, w);
+                            if constexpr (Q8) {
+                                // a lane's 16 quants share one block scale: sum, then scale once
+                                const float d = __half2float(
+                                    ssc[((size_t)i * row_bytes + (warp * spw + k2) * kSlice + lane * 16) / 32]);
+                                unpack_q8_raw(wv, w);
+                                float la = 0.f, lb = 0.f;
 #pragma unroll
-                            for (int e = 0; e < VN; e += 2)
-                                fma2(pa[i], pb[i], w[e], w[e + 1], xr[k2][e], xr[k2][e + 1]);
+                                for (int e = 0; e < VN; e += 2)
+                                    fma2(la, lb, w[e], w[e + 1], xr[k2][e], xr[k2][e + 1]);
+                                pa[i] = fmaf(d, la, pa[i]);
+                                pb[i] = fmaf(d, lb, pb[i]);
+                            } else {
+                                unpack16<WT>(wv, 0.f, w);
+#pragma unroll
+                                for (int e = 0; e < VN; e += 2)
+                                    fma2(pa[i], pb[i], w[e], w[e + 1], xr[k2][e], xr[k2][e + 1]);
+                            }
                         }
                     }
                     pa[i] += pb[i];
@@ -331,19 +341,23 @@ gemv_bulk_kernel(const GemvArgs a) {
                 float d = 0.f;
                 if (Q8) d = __half2float(ssc[((warp * kSlicesPerWarp + j) * kSlice + lane * 16) / 32]);
                 float w[VN];
-                unpack16<WT>(wv, d, w);
+                if constexpr (Q8) unpack_q8_raw(wv, w);
+                else unpack16<WT>(wv, 0.f, w);
                 const uint32_t col = rem / ES + lane * VN;
 #pragma unroll
                 for (int t = 0; t < TM; ++t) {
                     const float* xp = xs + t * K + col;
+                    float ls = 0.f;
 #pragma unroll
                     for (int e2 = 0; e2 < VN; e2 += 4) {
                         const float4 xv = *reinterpret_cast<const float4*>(xp + e2);
-                        part[t] = fmaf(w[e2], xv.x, part[t]);
-                        part[t] = fmaf(w[e2 + 1], xv.y, part[t]);
-                        part[t] = fmaf(w[e2 + 2], xv.z, part[t]);
-                        part[t] = fmaf(w[e2 + 3], xv.w, part[t]);
+                        ls = fmaf(w[e2], xv.x, ls);
+                        ls = fmaf(w[e2 + 1], xv.y, ls);
+                        ls = fmaf(w[e2 + 2], xv.z, ls);
+                        ls = fmaf(w[e2 + 3], xv.w, ls);
                     }
+                    // Q8_0: a lane's 16 quants share one block scale
+                    part[t] = Q8 ? fmaf(d, ls, part[t]) : part[t] + ls;
                 }
                 rem += kSlice;
             }

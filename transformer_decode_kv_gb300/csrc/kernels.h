@@ -58,6 +58,10 @@ __host__ __device__ inline size_t kv_q8_scale_offset(int32_t Hkv, int32_t n_ctx,
 // head. Used by the defrag to gather one cache region in the new cell order.
 void launch_kv_gather(const void* src, void* dst, const int32_t* order, int32_t n, int32_t n_head,
                       int32_t n_src, int32_t row_bytes, cudaStream_t st);
+// Q8_0 weight [rows][cols] (int8 quants q, fp16 scales d per 32 values) -> two bf16 terms:
+// w = d * q (exact in float32), hi = bf16(w), lo = bf16(w - hi); hi + lo holds w to 16 bits.
+void launch_q8_0_to_bf16_terms(const int8_t* q, const __half* d, int64_t rows, int64_t cols, void* hi,
+                               void* lo, cudaStream_t st);
 // u[t][j] = silu(g[t][j]) * up[t][j] with gu = [T][2F] (gate then up) -> u [T][F].
 void launch_swiglu(const float* gu, int32_t T, int32_t F, float* u, cudaStream_t st);
 // amax[r] = the largest logit of row r packed with its index (value in the high word in an

@@ -148,6 +148,16 @@ __global__ void kv_gather_kernel(const U* __restrict__ src, U* __restrict__ dst,
     dst[((int64_t)g * n + r) * upr + u] = o >= 0 ? src[((int64_t)g * n_src + o) * upr + u] : U{};
 }
 
+__global__ void q8_0_terms_kernel(const int8_t* __restrict__ q, const __half* __restrict__ d, int64_t n,
+                                  __nv_bfloat16* __restrict__ hi, __nv_bfloat16* __restrict__ lo) {
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= n) return;
+    const float w = __half2float(d[i / 32]) * (float)q[i];
+    const __nv_bfloat16 h = __float2bfloat16_rn(w);
+    hi[i] = h;
+    lo[i] = __float2bfloat16_rn(w - __bfloat162float(h));
+}
+
 __global__ void swiglu_kernel(const float* __restrict__ gu, int64_t T, int F,
                               float* __restrict__ u) {
     const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -287,6 +297,14 @@ void launch_kv_gather(const void* src, void* dst, const int32_t* order, int32_t 
         kv_gather_kernel<uint16_t><<<grid, 256, 0, st>>>(static_cast<const uint16_t*>(src),
                                                          static_cast<uint16_t*>(dst), order, n, n_src, upr);
     }
+}
+
+void launch_q8_0_to_bf16_terms(const int8_t* q, const __half* d, int64_t rows, int64_t cols, void* hi,
+                               void* lo, cudaStream_t st) {
+    const int64_t n = rows * cols;
+    if (n <= 0) return;
+    q8_0_terms_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(q, d, n, static_cast<__nv_bfloat16*>(hi),
+                                                                    static_cast<__nv_bfloat16*>(lo));
 }
 
 void launch_swiglu(const float* gu, int32_t T, int32_t F, float* u, cudaStream_t st) {

@@ -56,6 +56,10 @@ struct Layer {
     CUtensorMap mq, mo, mgu, md;
     CUtensorMap mgu128;      // gate|up with 128-row boxes (token-major SwiGLU GEMM)
     bool gu_tn = false;
+    // Q8_0 layers: each weight as two bf16 terms (hi + lo) for the token-major GEMM, and the maps
+    // of the low terms (the high terms use mq, mo, mgu128, md)
+    bool q8_tc = false;
+    CUtensorMap mq_lo, mo_lo, mgu128_lo, md_lo;
 };
 
 // Kernel classes timed by llm_debug_kernel_timing.
@@ -127,7 +131,8 @@ struct llm_ctx {
     void *hb_lo = nullptr, *attnb_lo = nullptr, *ub_lo = nullptr, *hob_lo = nullptr;
     CUtensorMap m_hb[2], m_attnb[2], m_ub[2], m_hob[2], m_lm;
     CUtensorMap m_hb_lo, m_attnb_lo, m_ub_lo, m_hob_lo;        // low terms (token box 128)
-    bool tc_ok = false;
+    bool tc_ok = false;                        // tensor-core prefill GEMMs for the layers
+    bool tc_lm = false;                        // ... and for the output matrix
     float *part_o = nullptr, *part_m = nullptr, *part_l = nullptr;
     int32_t* tickets = nullptr;
     int32_t max_rows = 0;
@@ -518,7 +523,7 @@ bool forward_ubatch(llm_ctx* c, int32_t T, int32_t O, int32_t out_row0, int32_t 
     // store / residual add: the token-major GEMM when the weight rows come in 256-row tiles
     // (split-K with atomic adds when the tiles alone leave SMs idle), else the weight-major one
     auto tc_gemm = [&](const CUtensorMap& wm, const CUtensorMap& xm, int epi, int K, int M, void* Y,
-                       int ldy) {
+                       int ldy, const CUtensorMap* wlo) {
         const CUtensorMap* xlo = &xm == &c->m_hb[bi] ? &c->m_hb_lo
                                : &xm == &c->m_attnb[bi] ? &c->m_attnb_lo : &c->m_ub_lo;
         if (epi != GEMM_EPI_SWIGLU && tc_tn_ok(M, K)) {
@@ -526,7 +531,8 @@ bool forward_ubatch(llm_ctx* c, int32_t T, int32_t O, int32_t out_row0, int32_t 
             if (splits > 1 && epi == GEMM_EPI_STORE &&
                 !cuda_ok(c, cudaMemsetAsync(Y, 0, sizeof(float) * (size_t)T * ldy, st), "memset"))
                 return false;
-            if (!launch_gemm_tn(xm, *xlo, wm, epi, K, M, T, static_cast<float*>(Y), ldy, splits, c->d_err, st)) {
+            if (!launch_gemm_tn(xm, *xlo, wm, epi, K, M, T, static_cast<float*>(Y), ldy, splits, c->d_err, st,
+                                wlo)) {
                 c->err = "tensor-core GEMM launch failed";
                 return false;
             }
@@ -571,7 +577,10 @@ bool forward_ubatch(llm_ctx* c, int32_t T, int32_t O, int32_t out_row0, int32_t 
             else launch_rmsnorm(c->x, nullptr, T, d, L.attn_norm, hp.rms_eps, c->h, st);
             kt_end(c, k, KC_RMSNORM, norm_bytes, 0);
             k = kt_begin(c);
-            if (tc) { if (!tc_gemm(L.mq, c->m_hb[bi], GEMM_EPI_STORE, d, qkvw, c->qkv, qkvw)) return false; }
+            if (tc) {
+                if (!tc_gemm(L.mq, c->m_hb[bi], GEMM_EPI_STORE, d, qkvw, c->qkv, qkvw, L.q8_tc ? &L.mq_lo : nullptr))
+                    return false;
+            }
             else launch_linear(L.qkv, 0, qkvw, c->h, d, T, c->qkv, qkvw, EPI_STORE, st);
             kt_end(c, k, lin_cls, wbytes(L.qkv, qkvw) + Td * (d + qkvw) * 4.0, 2.0 * Td * qkvw * d);
             k = kt_begin(c);
@@ -616,7 +625,8 @@ bool forward_ubatch(llm_ctx* c, int32_t T, int32_t O, int32_t out_row0, int32_t 
             g.x = c->attn; g.ldx = qw; g.x_rows = nullptr; g.g = nullptr; g.y = c->x; g.ldy = d;
             if (!launch_gemv_bulk(L.wo.type, g, GEPI_ADD, false, c->n_sm, st, pdl)) return bulk_fail();
         } else if (tc) {
-            if (!tc_gemm(L.mo, c->m_attnb[bi], GEMM_EPI_ADD, qw, d, c->x, d)) return false;
+            if (!tc_gemm(L.mo, c->m_attnb[bi], GEMM_EPI_ADD, qw, d, c->x, d, L.q8_tc ? &L.mo_lo : nullptr))
+                return false;
         } else {
             launch_linear(L.wo, 0, d, c->attn, qw, T, c->x, d, EPI_ADD, st);
         }
@@ -636,11 +646,11 @@ bool forward_ubatch(llm_ctx* c, int32_t T, int32_t O, int32_t out_row0, int32_t 
             k = kt_begin(c);
             if (tc && L.gu_tn) {
                 if (!launch_gemm_swiglu_tn(c->m_hb[bi], c->m_hb_lo, L.mgu128, d, T, F, c->ub, c->ub_lo, F,
-                                           c->d_err, st)) {
+                                           c->d_err, st, L.q8_tc ? &L.mgu128_lo : nullptr)) {
                     c->err = "tensor-core GEMM launch failed";
                     return false;
                 }
-            } else if (tc) { if (!tc_gemm(L.mgu, c->m_hb[bi], GEMM_EPI_SWIGLU, d, 0, c->ub, F)) return false; }
+            } else if (tc) { if (!tc_gemm(L.mgu, c->m_hb[bi], GEMM_EPI_SWIGLU, d, 0, c->ub, F, nullptr)) return false; }
             else launch_linear_swiglu(L.gu, F, c->h, d, T, c->u, F, c->tmp, st);
             kt_end(c, k, lin_cls, wbytes(L.gu, 2 * (int64_t)F) + Td * (d + F) * 4.0, 4.0 * Td * F * d);
         }
@@ -651,7 +661,7 @@ bool forward_ubatch(llm_ctx* c, int32_t T, int32_t O, int32_t out_row0, int32_t 
             g.x = c->u; g.ldx = F; g.x_rows = nullptr; g.g = nullptr; g.y = c->x; g.ldy = d;
             if (!launch_gemv_bulk(L.down.type, g, GEPI_ADD, false, c->n_sm, st, pdl)) return bulk_fail();
         } else if (tc) {
-            if (!tc_gemm(L.md, c->m_ub[bi], GEMM_EPI_ADD, F, d, c->x, d)) return false;
+            if (!tc_gemm(L.md, c->m_ub[bi], GEMM_EPI_ADD, F, d, c->x, d, L.q8_tc ? &L.md_lo : nullptr)) return false;
         } else {
             launch_linear(L.down, 0, d, c->u, F, T, c->x, d, EPI_ADD, st);
         }
@@ -675,7 +685,7 @@ bool forward_ubatch(llm_ctx* c, int32_t T, int32_t O, int32_t out_row0, int32_t 
             if (!launch_gemv_bulk(c->out.type, g, GEPI_LOGITS, true, c->n_sm, st, pdl)) return bulk_fail();
             kt_end(c, k, KC_LM_HEAD, lm_bytes, 2.0 * Od * hp.n_vocab * d);
         } else {
-            const bool tc_out = tc && O > gemv_max_tokens();
+            const bool tc_out = tc && c->tc_lm && O > gemv_max_tokens();
             k = kt_begin(c);
             if (tc_out) launch_rmsnorm_bf16(c->x, orows, O, d, c->out_norm, hp.rms_eps, c->hob, c->hob_lo, st);
             launch_rmsnorm(c->x, orows, O, d, c->out_norm, hp.rms_eps, c->hout, st);
@@ -911,6 +921,7 @@ int llm_load_weights(llm_ctx* c, const char* name, int32_t type, const int64_t n
             if (!cuda_ok(c, cudaMemcpy(g, data, nbytes, cudaMemcpyDefault), "copy")) return -2;
         }
         L.loaded |= sp->bit;
+        L.q8_tc = false;                    // the bf16 terms, if any, are stale
         return 0;
     }
     // fused stores: Q, K, V rows stacked in one matrix; gate rows then up rows in another
@@ -935,6 +946,7 @@ int llm_load_weights(llm_ctx* c, const char* name, int32_t type, const int64_t n
     }
     if (!c->host_only && !fill_rows(c, *m, row0, rows, data, nbytes)) return -2;
     L.loaded |= sp->bit;
+    L.q8_tc = false;
     return 0;
 }
 
@@ -1045,16 +1057,39 @@ int llm_weights_ready(llm_ctx* c) {
     const int64_t U = c->n_ubatch;
     bool ok = tc_shape_ok(qkvw, d, GEMM_EPI_STORE, 0) && tc_shape_ok(d, qw, GEMM_EPI_ADD, 0) &&
               tc_shape_ok(0, d, GEMM_EPI_SWIGLU, F) && tc_shape_ok(d, F, GEMM_EPI_ADD, 0);
+    // Q8_0 layers take the token-major GEMM with the weights as two bf16 terms (4 bytes per weight
+    // of extra device memory, made here once): only when prefill ubatches can occur
+    const bool q8_shapes = U > gemv_max_tokens() && tc_tn_ok(qkvw, d) && tc_tn_ok(d, qw) &&
+                           tc_swiglu_tn_ok(d, F) && tc_tn_ok(d, F);
+    auto terms = [&](const DevMat& W, int64_t rows, int64_t cols, CUtensorMap* hi_map, CUtensorMap* lo_map) {
+        uint16_t *hi = nullptr, *lo = nullptr;
+        if (!dalloc(c, &hi, (size_t)(rows * cols)) || !dalloc(c, &lo, (size_t)(rows * cols))) return false;
+        launch_q8_0_to_bf16_terms(static_cast<const int8_t*>(W.data), W.scales, rows, cols, hi, lo, c->st);
+        return tc_make_map(hi_map, hi, rows, cols, 128) && tc_make_map(lo_map, lo, rows, cols, 128);
+    };
     for (int32_t il = 0; ok && il < h.n_layer; ++il) {
         Layer& L = c->layers[il];
-        ok = L.qkv.type == LLM_TYPE_BF16 && L.wo.type == LLM_TYPE_BF16 &&
-             L.gu.type == LLM_TYPE_BF16 && L.down.type == LLM_TYPE_BF16 &&
-             tc_make_map(&L.mq, L.qkv.data, qkvw, d, 128) &&
-             tc_make_map(&L.mo, L.wo.data, d, qw, 128) &&
-             tc_make_map(&L.mgu, L.gu.data, 2 * F, d, 64) &&
-             tc_make_map(&L.md, L.down.data, d, F, 128);
-        L.gu_tn = ok && tc_swiglu_tn_ok(d, F) && tc_make_map(&L.mgu128, L.gu.data, 2 * F, d, 128);
+        const bool bf16 = L.qkv.type == LLM_TYPE_BF16 && L.wo.type == LLM_TYPE_BF16 &&
+                          L.gu.type == LLM_TYPE_BF16 && L.down.type == LLM_TYPE_BF16;
+        const bool q8 = L.qkv.type == LLM_TYPE_Q8_0 && L.wo.type == LLM_TYPE_Q8_0 &&
+                        L.gu.type == LLM_TYPE_Q8_0 && L.down.type == LLM_TYPE_Q8_0;
+        if (bf16) {
+            ok = tc_make_map(&L.mq, L.qkv.data, qkvw, d, 128) &&
+                 tc_make_map(&L.mo, L.wo.data, d, qw, 128) &&
+                 tc_make_map(&L.mgu, L.gu.data, 2 * F, d, 64) &&
+                 tc_make_map(&L.md, L.down.data, d, F, 128);
+            L.gu_tn = ok && tc_swiglu_tn_ok(d, F) && tc_make_map(&L.mgu128, L.gu.data, 2 * F, d, 128);
+        } else if (q8 && q8_shapes) {
+            L.q8_tc = L.q8_tc || (terms(L.qkv, qkvw, d, &L.mq, &L.mq_lo) && terms(L.wo, d, qw, &L.mo, &L.mo_lo) &&
+                                  terms(L.gu, 2 * F, d, &L.mgu128, &L.mgu128_lo) &&
+                                  terms(L.down, d, F, &L.md, &L.md_lo));
+            ok = L.q8_tc;
+            L.gu_tn = ok;
+        } else {
+            ok = false;
+        }
     }
+    if (ok && !cuda_ok(c, cudaStreamSynchronize(c->st), "weight terms")) return -1;
     const int boxes[2] = {128, 256};
     for (int i = 0; ok && i < 2; ++i)
         ok = tc_make_map(&c->m_hb[i], c->hb, U, d, boxes[i]) &&
@@ -1067,7 +1102,8 @@ int llm_weights_ready(llm_ctx* c) {
          tc_make_map(&c->m_hob_lo, c->hob_lo, U, d, 128);
     const bool lm_ok = c->out.type == LLM_TYPE_BF16 && tc_shape_ok(h.n_vocab, d, GEMM_EPI_STORE, 0) &&
                        tc_make_map(&c->m_lm, c->out.data, h.n_vocab, d, 128);
-    c->tc_ok = ok && lm_ok;
+    c->tc_ok = ok;
+    c->tc_lm = ok && lm_ok;
     setup_step(c);
     return 0;
 }
