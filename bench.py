@@ -258,10 +258,22 @@ def run_gpu(args, rank, world, local_rank):
         t = torch.tensor([e2e_s], dtype=torch.float64)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         e2e_s = float(t[0])
+    # ---- the device sampler chain on the last logits row (top-k 40, top-p 0.95, min-p 0.05,
+    # temperature 0.8, repeat penalty 1.1 over the last 64 tokens): host call to token, per call
+    n_s = 32
+    pen = list(prompt[-64:])
+    ctx.sample_ith(-1, top_k=40, top_p=0.95, min_p=0.05, temperature=0.8, repeat_penalty=1.1,
+                   penalty_tokens=pen, u=0.5)
+    t0 = time.perf_counter()
+    for i in range(n_s):
+        if ctx.sample_ith(-1, top_k=40, top_p=0.95, min_p=0.05, temperature=0.8, repeat_penalty=1.1,
+                          penalty_tokens=pen, u=(i + 0.5) / n_s) < 0:
+            raise RuntimeError(ctx.last_error())
+    sample_us = (time.perf_counter() - t0) / n_s * 1e6
     perf = ctx.perf()
     ctx.free()
     return dict(w=w, dec_s=dec_s, prefill_s=prefill_s, e2e_s=e2e_s, ks=ks, clk=clk.summary(),
-                perf=perf)
+                perf=perf, sample_us=sample_us)
 
 
 def main():
@@ -360,6 +372,7 @@ def main():
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16 weights, f32 activations/accumulation",
         "data": "synthetic (seeded random weights and prompt)", "config": config,
         "prefill_tok_s": pre_tps, "prefill_ms": res["prefill_s"] * 1e3,
+        "sampler_us_per_call": res["sample_us"],
         "decode_hbm_gbs": step_bytes * K / res["dec_s"] / 1e9,
         "decode_step_algorithmic_bytes": step_bytes,
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": hbm_peak,
