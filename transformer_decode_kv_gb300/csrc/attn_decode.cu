@@ -27,6 +27,7 @@
 #include <cstdint>
 
 #include "attn_common.cuh"
+#include "dev_common.cuh"
 #include "kernels.h"
 
 namespace llm {
@@ -146,24 +147,54 @@ attn_decode_kernel(AttnArgs a, float scale_log2) {
             S.vsc[c * NB + b] = ld_scale(VS + (int64_t)cell * NB + b);
         }
     };
-    // cell list of pass i into stage S (threads < kCH); before the wait, fresh cells' scales wait
-    auto setup = [&](int i, const Stage<KT>& S, bool pre_wait) {
+    // The list entry (cell, position; Q8_0 after the wait: its scales) of the next pass to set up
+    // is fetched into registers one pass ahead, so setting up a stage waits on no global load.
+    int pf_cell = -1, pf_pos = 0;
+    float pf_ks[NB], pf_vs[NB];
+    auto fetch = [&](int i, bool with_scales) {
         if (threadIdx.x < kCH) {
             const int ci = c0 + i * kCH + threadIdx.x;
-            int cell = -1, vis = 0, fresh = 0;
+            pf_cell = -1;
+            pf_pos = 0;
             if (ci < c1) {
-                const int cc = a.list_cells[base + ci];
-                if (cc >= 0 && cc < a.n_ctx) {
-                    cell = cc;
-                    vis = a.list_pos[base + ci] <= tpos;
-                    for (int j = 0; j < a.n_tok; ++j) fresh |= a.slot[j] == cc;
+                pf_cell = a.list_cells[base + ci];
+                pf_pos = a.list_pos[base + ci];
+            }
+            if constexpr (Q8) {
+                if (with_scales && pf_cell >= 0 && pf_cell < a.n_ctx && pf_pos <= tpos) {
+#pragma unroll
+                    for (int b = 0; b < NB; ++b) {
+                        pf_ks[b] = ld_scale(KS + (int64_t)pf_cell * NB + b);
+                        pf_vs[b] = ld_scale(VS + (int64_t)pf_cell * NB + b);
+                    }
                 }
+            }
+        }
+    };
+    // stage S takes the fetched entry (threads < kCH); before the wait, fresh cells' scales wait
+    auto setup = [&](const Stage<KT>& S, bool pre_wait) {
+        if (threadIdx.x < kCH) {
+            int cell = -1, vis = 0, fresh = 0;
+            if (pf_cell >= 0 && pf_cell < a.n_ctx) {
+                cell = pf_cell;
+                vis = pf_pos <= tpos;
+                for (int j = 0; j < a.n_tok; ++j) fresh |= a.slot[j] == cell;
             }
             S.ccell[threadIdx.x] = cell;
             S.cvis[threadIdx.x] = vis && cell >= 0;
             S.cfresh[threadIdx.x] = fresh;
             if constexpr (Q8) {
-                if (vis && cell >= 0 && !(pre_wait && fresh)) load_scales(S, threadIdx.x, cell);
+                if (vis && cell >= 0) {
+                    if (pre_wait) {
+                        if (!fresh) load_scales(S, threadIdx.x, cell);
+                    } else {
+#pragma unroll
+                        for (int b = 0; b < NB; ++b) {
+                            S.ksc[threadIdx.x * NB + b] = pf_ks[b];
+                            S.vsc[threadIdx.x * NB + b] = pf_vs[b];
+                        }
+                    }
+                }
             }
         }
     };
@@ -181,10 +212,12 @@ attn_decode_kernel(AttnArgs a, float scale_log2) {
     // pass 0: rows of earlier steps staged now, possibly before the previous kernel has ended
     {
         const Stage<KT> S0 = stage_of(0);
-        setup(0, S0, true);
+        fetch(0, false);
+        setup(S0, true);
         __syncthreads();
         issue(S0, true);
         asm volatile("griddepcontrol.wait;" ::: "memory");
+        if (npass > 1) fetch(1, true);
         for (int i = threadIdx.x; i < kGQ * HD; i += kThreads)
             qs[i] = a.q[(int64_t)t * a.ldq + (kvh * kGQ + i / HD) * HD + i % HD] * scale_log2;
         // rows written by this step's projection kernel: only now
@@ -210,7 +243,8 @@ attn_decode_kernel(AttnArgs a, float scale_log2) {
         if (i + 1 < npass) {
             // the other stage was last read by pass i - 1, which ended at the barrier below
             const Stage<KT> N = stage_of((i + 1) & 1);
-            setup(i + 1, N, false);
+            setup(N, false);
+            if (i + 2 < npass) fetch(i + 2, true);
             __syncthreads();
             issue(N, false);
             asm volatile("cp.async.wait_group 1;" ::: "memory");
@@ -233,11 +267,15 @@ attn_decode_kernel(AttnArgs a, float scale_log2) {
                     for (int jj = 0; jj < 2; ++jj) {
                         const int j = 2 * b + jj;
                         const uint4 kv = *reinterpret_cast<const uint4*>(kr + j * 16);
-                        const int8_t* ke = reinterpret_cast<const int8_t*>(&kv);
+                        float ke[16];
+                        dev::unpack_q8_raw(kv, ke);
 #pragma unroll
-                        for (int e = 0; e < 16; e += 2) {
-                            p0 = fmaf(q[j * 16 + e], (float)ke[e], p0);
-                            p1 = fmaf(q[j * 16 + e + 1], (float)ke[e + 1], p1);
+                        for (int e = 0; e < 16; e += 4) {
+                            const float4 qv = *reinterpret_cast<const float4*>(q + j * 16 + e);
+                            p0 = fmaf(qv.x, ke[e], p0);
+                            p1 = fmaf(qv.y, ke[e + 1], p1);
+                            p0 = fmaf(qv.z, ke[e + 2], p0);
+                            p1 = fmaf(qv.w, ke[e + 3], p1);
                         }
                     }
                     acc = fmaf(S.ksc[c * NB + b], p0 + p1, acc);
@@ -251,9 +289,12 @@ attn_decode_kernel(AttnArgs a, float scale_log2) {
                     const KT* ke = reinterpret_cast<const KT*>(&kv);
                     constexpr int EPV = 16 / (int)sizeof(KT);
 #pragma unroll
-                    for (int e = 0; e < EPV; e += 2) {
-                        a0 = fmaf(q[j * EPV + e], kvf<KT>(ke[e]), a0);
-                        a1 = fmaf(q[j * EPV + e + 1], kvf<KT>(ke[e + 1]), a1);
+                    for (int e = 0; e < EPV; e += 4) {
+                        const float4 qv = *reinterpret_cast<const float4*>(q + j * EPV + e);   // broadcast
+                        a0 = fmaf(qv.x, kvf<KT>(ke[e]), a0);
+                        a1 = fmaf(qv.y, kvf<KT>(ke[e + 1]), a1);
+                        a0 = fmaf(qv.z, kvf<KT>(ke[e + 2]), a0);
+                        a1 = fmaf(qv.w, kvf<KT>(ke[e + 3]), a1);
                     }
                 }
                 s = a0 + a1;
@@ -279,9 +320,20 @@ attn_decode_kernel(AttnArgs a, float scale_log2) {
             if (pc == 0.f) continue;
             const int c2 = grp * kCG + k;
             const KT* vr = reinterpret_cast<const KT*>(S.vb + c2 * RS) + lane * DPL;
-            const float pd = Q8 ? pc * S.vsc[c2 * NB + lane * DPL / 32] : pc;
+            if constexpr (Q8 && DPL % 4 == 0) {
+                const float pd = pc * S.vsc[c2 * NB + lane * DPL / 32];
 #pragma unroll
-            for (int e = 0; e < DPL; ++e) o[e] = fmaf(pd, kvf<KT>(vr[e]), o[e]);
+                for (int e4 = 0; e4 < DPL; e4 += 4) {
+                    float vv[4];
+                    dev::unpack_q8x4_raw(*reinterpret_cast<const uint32_t*>(vr + e4), vv);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) o[e4 + e] = fmaf(pd, vv[e], o[e4 + e]);
+                }
+            } else {
+                const float pd = Q8 ? pc * S.vsc[c2 * NB + lane * DPL / 32] : pc;
+#pragma unroll
+                for (int e = 0; e < DPL; ++e) o[e] = fmaf(pd, kvf<KT>(vr[e]), o[e]);
+            }
         }
         __syncthreads();                                        // stage S free for pass i + 2
     }
