@@ -379,6 +379,308 @@ attn_decode_kernel(AttnArgs a, float scale_log2) {
     cluster_sync_all();                                         // peers are done reading
 }
 
+// ---- F16 caches: the same decomposition with the contractions on tensor cores ----------------
+//
+// S^T = K Q^T and O^T += V^T P^T as mma.sync m16n8k16 (f16 inputs, f32 accumulators), the 16 rows
+// of an A fragment being 16 cells (scores) or 16 output dimensions (values) and the 8 columns of
+// a B fragment the query heads (4 of the group, 4 zero columns). Q and P enter as two f16 terms
+// (hi + lo of the float32), so every product is float32-accurate to about 2^-22, as in the
+// prefill kernel. Warp w takes cells 16w .. 16w+15 of every 64-cell pass and keeps its own
+// online-softmax state; the four warps' states merge in shared memory, then across the cluster.
+constexpr int kMW = 4;                   // warps
+constexpr int kMT = kMW * 32;            // threads
+constexpr int kMC = kCH / kMW;           // cells per warp and pass (one m16 fragment)
+
+template <int HD>
+struct MmaDecSmem {
+    static constexpr int RS = HD + 8;                     // halves per padded row
+    static constexpr int RB = HD * 2;                     // bytes of a cached row
+    static constexpr size_t rows = 2 * (size_t)kCH * RS * 2;
+    static constexpr size_t stage = rows + 3 * kCH * 4;
+    static constexpr size_t bytes = 2 * stage + (size_t)kGQ * HD * 4 /* q */ +
+                                    (size_t)kMW * kMC * 8 * 4 /* P^T per warp */ +
+                                    (size_t)kMW * kGQ * (HD + 2) * 4 /* warp states */ +
+                                    (size_t)kGQ * (HD + 2) * 4 /* block partial */ + 16;
+};
+
+template <int HD>
+__global__ void __launch_bounds__(kMT)
+attn_decode_mma_kernel(AttnArgs a, float scale_log2) {
+    using SM = MmaDecSmem<HD>;
+    constexpr int RS = SM::RS, RB = SM::RB, VPR = RB / 16, NK = HD / 16;
+    extern __shared__ __align__(16) uint8_t sm[];
+    struct St { __half* kb; __half* vb; int* ccell; int* cvis; int* cfresh; };
+    auto stage_of = [&](int s) {
+        uint8_t* b = sm + (size_t)s * SM::stage;
+        St S;
+        S.kb = reinterpret_cast<__half*>(b);
+        S.vb = S.kb + kCH * RS;
+        S.ccell = reinterpret_cast<int*>(b + SM::rows);
+        S.cvis = S.ccell + kCH;
+        S.cfresh = S.cvis + kCH;
+        return S;
+    };
+    float* qs = reinterpret_cast<float*>(sm + 2 * SM::stage);          // [kGQ][HD]
+    float* pT = qs + kGQ * HD;                                          // [warp][16 cells][8]
+    float* ws = pT + kMW * kMC * 8;                                     // [warp][kGQ][HD + 2]
+    float* pst = ws + kMW * kGQ * (HD + 2);                             // block partial (peers read it)
+
+    const uint32_t rank = cluster_rank();
+    const int kvh = blockIdx.y, tile = blockIdx.z;
+    if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;");
+    if (tile >= a.hdr[1]) return;                               // whole cluster (same tile)
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane >> 2, cq = lane & 3;                     // fragment row group, column pair
+    const int4 td0 = a.tile_desc[2 * tile];
+    const int4 td1 = a.tile_desc[2 * tile + 1];
+    const int base = td1.y, len = td1.z;
+    const int t = a.perm[td0.y];
+    const int tpos = a.tok_pos[t];
+    const int chunk = (len + kCL - 1) / kCL;
+    const int c0 = min(len, (int)rank * chunk), c1 = min(len, c0 + chunk);
+    const int npass = c1 > c0 ? (c1 - c0 + kCH - 1) / kCH : 1;
+    const uint8_t* K = static_cast<const uint8_t*>(a.kc) + (int64_t)kvh * a.n_ctx * RB;
+    const uint8_t* V = static_cast<const uint8_t*>(a.vc) + (int64_t)kvh * a.n_ctx * RB;
+
+    int pf_cell = -1, pf_pos = 0;
+    auto fetch = [&](int i) {
+        if (threadIdx.x < kCH) {
+            const int ci = c0 + i * kCH + threadIdx.x;
+            pf_cell = -1;
+            pf_pos = 0;
+            if (ci < c1) {
+                pf_cell = a.list_cells[base + ci];
+                pf_pos = a.list_pos[base + ci];
+            }
+        }
+    };
+    auto setup = [&](const St& S) {
+        if (threadIdx.x < kCH) {
+            int cell = -1, vis = 0, fresh = 0;
+            if (pf_cell >= 0 && pf_cell < a.n_ctx) {
+                cell = pf_cell;
+                vis = pf_pos <= tpos;
+                for (int j = 0; j < a.n_tok; ++j) fresh |= a.slot[j] == cell;
+            }
+            S.ccell[threadIdx.x] = cell;
+            S.cvis[threadIdx.x] = vis && cell >= 0;
+            S.cfresh[threadIdx.x] = fresh;
+        }
+    };
+    auto issue = [&](const St& S, bool pre_wait) {
+        for (int v = threadIdx.x; v < kCH * VPR; v += kMT) {
+            const int c = v / VPR, j = v % VPR;
+            if (!S.cvis[c]) {
+                // the MMA multiplies every row of the tile: a hidden cell's V row must be finite
+                *reinterpret_cast<uint4*>(S.vb + c * RS + j * 8) = make_uint4(0u, 0u, 0u, 0u);
+                continue;
+            }
+            if (pre_wait && S.cfresh[c]) continue;
+            const size_t src = (size_t)S.ccell[c] * RB + j * 16;
+            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sm32(S.kb + c * RS + j * 8)), "l"(K + src) : "memory");
+            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sm32(S.vb + c * RS + j * 8)), "l"(V + src) : "memory");
+        }
+        asm volatile("cp.async.commit_group;" ::: "memory");
+    };
+
+    {
+        const St S0 = stage_of(0);
+        fetch(0);
+        setup(S0);
+        __syncthreads();
+        issue(S0, true);
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+        for (int i = threadIdx.x; i < kGQ * HD; i += kMT)
+            qs[i] = a.q[(int64_t)t * a.ldq + (kvh * kGQ + i / HD) * HD + i % HD] * scale_log2;
+        if (npass > 1) fetch(1);
+        for (int v = threadIdx.x; v < kCH * VPR; v += kMT) {
+            const int c = v / VPR, j = v % VPR;
+            if (!S0.cvis[c] || !S0.cfresh[c]) continue;
+            const size_t src = (size_t)S0.ccell[c] * RB + j * 16;
+            *reinterpret_cast<uint4*>(S0.kb + c * RS + j * 8) = __ldcg(reinterpret_cast<const uint4*>(K + src));
+            *reinterpret_cast<uint4*>(S0.vb + c * RS + j * 8) = __ldcg(reinterpret_cast<const uint4*>(V + src));
+        }
+    }
+    __syncthreads();                                            // qs
+    // B fragments of Q^T (column n = query head g, rows = dims): two f16 terms per k-step
+    uint32_t qh[NK][2], ql[NK][2];
+#pragma unroll
+    for (int kk = 0; kk < NK; ++kk) {
+        const float* qr = qs + (g < kGQ ? g : 0) * HD + kk * 16 + 2 * cq;
+        const float z = g < kGQ ? 1.f : 0.f;
+        split_h2(z * qr[0], z * qr[1], qh[kk][0], ql[kk][0]);
+        split_h2(z * qr[8], z * qr[9], qh[kk][1], ql[kk][1]);
+    }
+
+    float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
+    float o[NK][4];
+#pragma unroll
+    for (int nt = 0; nt < NK; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) o[nt][e] = 0.f;
+    float* pw = pT + warp * kMC * 8;
+    const int cw = warp * kMC;                                  // this warp's cells in a pass
+    for (int i = 0; i < npass; ++i) {
+        const St S = stage_of(i & 1);
+        if (i + 1 < npass) {
+            const St N = stage_of((i + 1) & 1);
+            setup(N);
+            if (i + 2 < npass) fetch(i + 2);
+            __syncthreads();
+            issue(N, false);
+            asm volatile("cp.async.wait_group 1;" ::: "memory");
+        } else {
+            asm volatile("cp.async.wait_group 0;" ::: "memory");
+        }
+        __syncthreads();
+
+        // S^T [16 cells][8 heads] = K Q^T
+        float s[4] = {0.f, 0.f, 0.f, 0.f};
+        {
+            const int mi = lane >> 3, r = lane & 7;
+            const __half* kr = S.kb + (cw + r + (mi & 1) * 8) * RS + (mi >> 1) * 8;
+#pragma unroll
+            for (int kk = 0; kk < NK; ++kk) {
+                uint32_t af[4];
+                ldsm_x4(sm32(kr + kk * 16), af[0], af[1], af[2], af[3]);
+                mma16816(s, af, qh[kk][0], qh[kk][1]);
+                mma16816(s, af, ql[kk][0], ql[kk][1]);
+            }
+        }
+        // this thread: cells cw+g (s[0], s[1]) and cw+g+8 (s[2], s[3]), heads 2cq and 2cq+1
+        const bool live = cq < kGQ / 2;
+        const bool v0 = live && S.cvis[cw + g], v1 = live && S.cvis[cw + g + 8];
+        float sv[4] = {v0 ? s[0] : -INFINITY, v0 ? s[1] : -INFINITY, v1 ? s[2] : -INFINITY, v1 ? s[3] : -INFINITY};
+        float p[4], corr[2];
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            float mx = fmaxf(sv[j], sv[j + 2]);
+#pragma unroll
+            for (int off = 4; off < 32; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+            const float m_new = fmaxf(m[j], mx);
+            corr[j] = m_new == -INFINITY ? 1.f : exp2f(m[j] - m_new);
+            p[j] = sv[j] == -INFINITY ? 0.f : exp2f(sv[j] - m_new);
+            p[j + 2] = sv[j + 2] == -INFINITY ? 0.f : exp2f(sv[j + 2] - m_new);
+            float ps = p[j] + p[j + 2];
+#pragma unroll
+            for (int off = 4; off < 32; off <<= 1) ps += __shfl_xor_sync(0xffffffffu, ps, off);
+            l[j] = l[j] * corr[j] + ps;
+            m[j] = m_new;
+        }
+#pragma unroll
+        for (int nt = 0; nt < NK; ++nt) {
+            o[nt][0] *= corr[0]; o[nt][1] *= corr[1];
+            o[nt][2] *= corr[0]; o[nt][3] *= corr[1];
+        }
+        // P^T [16 cells][8 heads] through shared memory into B fragments (head g, 4 cells)
+        pw[g * 8 + 2 * cq] = p[0];
+        pw[g * 8 + 2 * cq + 1] = p[1];
+        pw[(g + 8) * 8 + 2 * cq] = p[2];
+        pw[(g + 8) * 8 + 2 * cq + 1] = p[3];
+        __syncwarp();
+        uint32_t bh0, bl0, bh1, bl1;
+        split_h2(pw[(2 * cq) * 8 + g], pw[(2 * cq + 1) * 8 + g], bh0, bl0);
+        split_h2(pw[(2 * cq + 8) * 8 + g], pw[(2 * cq + 9) * 8 + g], bh1, bl1);
+        // O^T [16 dims][8 heads] += V^T P^T per 16-dimension tile
+        {
+            const int mi = lane >> 3, r = lane & 7;
+            const __half* vr = S.vb + (cw + r + (mi >> 1) * 8) * RS + (mi & 1) * 8;
+#pragma unroll
+            for (int nt = 0; nt < NK; ++nt) {
+                uint32_t af[4];
+                ldsm_x4_t(sm32(vr + nt * 16), af[0], af[1], af[2], af[3]);
+                mma16816(o[nt], af, bh0, bh1);
+                mma16816(o[nt], af, bl0, bl1);
+            }
+        }
+        __syncwarp();                                           // pw is rewritten next pass
+        __syncthreads();                                        // stage S free for pass i + 2
+    }
+
+    // the warps' states -> this block's partial -> the cluster-wide merge
+    float* my = ws + warp * kGQ * (HD + 2);
+    if (cq < kGQ / 2) {
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            float* hs = my + (2 * cq + j) * (HD + 2);
+            if (g == 0) { hs[0] = m[j]; hs[1] = l[j]; }
+#pragma unroll
+            for (int nt = 0; nt < NK; ++nt) {
+                hs[2 + nt * 16 + g] = o[nt][j];
+                hs[2 + nt * 16 + g + 8] = o[nt][j + 2];
+            }
+        }
+    }
+    __syncthreads();
+    float* pm = pst;
+    float* pl = pst + kGQ;
+    float* po = pst + 2 * kGQ;
+    for (int idx = threadIdx.x; idx < kGQ * HD; idx += kMT) {
+        const int h = idx / HD, dd = idx % HD;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kMW; ++w) M = fmaxf(M, ws[(w * kGQ + h) * (HD + 2)]);
+        float L = 0.f, O = 0.f;
+#pragma unroll
+        for (int w = 0; w < kMW; ++w) {
+            const float* hs = ws + (w * kGQ + h) * (HD + 2);
+            const float f = (M == -INFINITY || hs[0] == -INFINITY) ? 0.f : exp2f(hs[0] - M);
+            L = fmaf(f, hs[1], L);
+            O = fmaf(f, hs[2 + dd], O);
+        }
+        if (dd == 0) { pm[h] = M; pl[h] = L; }
+        po[h * HD + dd] = O;
+    }
+    cluster_sync_all();
+    constexpr int OPB = kGQ * HD / kCL;
+    for (int idx = threadIdx.x; idx < OPB; idx += kMT) {
+        const int oi = (int)rank * OPB + idx;
+        const int h = oi / HD, dd = oi % HD;
+        float M = -INFINITY;
+#pragma unroll
+        for (uint32_t r = 0; r < kCL; ++r) M = fmaxf(M, ld_peer(pm + h, r));
+        float L = 0.f, O = 0.f;
+#pragma unroll
+        for (uint32_t r = 0; r < kCL; ++r) {
+            const float mr = ld_peer(pm + h, r);
+            const float f = (M == -INFINITY || mr == -INFINITY) ? 0.f : exp2f(mr - M);
+            L = fmaf(f, ld_peer(pl + h, r), L);
+            O = fmaf(f, ld_peer(po + h * HD + dd, r), O);
+        }
+        store_out(a, (int64_t)t * a.ldo + (kvh * kGQ + h) * HD + dd, L > 0.f ? O / L : 0.f);
+    }
+    cluster_sync_all();
+}
+
+template <int HD>
+bool launch_dec_mma(const AttnArgs& a, cudaStream_t st) {
+    const float scale_log2 = (float)(1.4426950408889634 / sqrt((double)HD));
+    constexpr size_t smem = MmaDecSmem<HD>::bytes;
+    auto k = attn_decode_mma_kernel<HD>;
+    static bool attr = false;
+    if (!attr) {
+        if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess ||
+            cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
+            return false;
+        attr = true;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(kCL, a.Hkv, a.n_tok);
+    cfg.blockDim = dim3(kMT);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr_l[2];
+    attr_l[0].id = cudaLaunchAttributeClusterDimension;
+    attr_l[0].val.clusterDim.x = kCL;
+    attr_l[0].val.clusterDim.y = 1;
+    attr_l[0].val.clusterDim.z = 1;
+    attr_l[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr_l[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr_l;
+    cfg.numAttrs = a.pdl ? 2 : 1;
+    return cudaLaunchKernelEx(&cfg, k, a, scale_log2) == cudaSuccess;
+}
+
 template <int HD, typename KT>
 bool launch_dec(const AttnArgs& a, cudaStream_t st) {
     const float scale_log2 = (float)(1.4426950408889634 / sqrt((double)HD));
@@ -422,11 +724,18 @@ bool launch_attention_decode(const AttnArgs& a, cudaStream_t st) {
         }
         return false;
     }
-    const bool f32 = a.kv_type == W_F32;
+    if (a.kv_type == W_F16) {                                  // tensor cores
+        switch (a.hd) {
+            case 32: return launch_dec_mma<32>(a, st);
+            case 64: return launch_dec_mma<64>(a, st);
+            case 128: return launch_dec_mma<128>(a, st);
+        }
+        return false;
+    }
     switch (a.hd) {
-        case 32: return f32 ? launch_dec<32, float>(a, st) : launch_dec<32, __half>(a, st);
-        case 64: return f32 ? launch_dec<64, float>(a, st) : launch_dec<64, __half>(a, st);
-        case 128: return f32 ? launch_dec<128, float>(a, st) : launch_dec<128, __half>(a, st);
+        case 32: return launch_dec<32, float>(a, st);
+        case 64: return launch_dec<64, float>(a, st);
+        case 128: return launch_dec<128, float>(a, st);
     }
     return false;
 }
