@@ -188,8 +188,8 @@ struct llm_ctx {
     uint32_t step_gen = 0;              // launches since the counters were last zeroed
     bool step_trace = false;
     float* d_sample_row = nullptr;      // sampler scratch [V]
-    int32_t* d_sample_tok = nullptr;    // [kMaxPenalty] penalty tokens, then the picked token
-    int32_t* h_sample_tok = nullptr;    // pinned: the picked token
+    int32_t* d_sample_tok = nullptr;    // [kMaxPenalty] penalty tokens, the picked token, status
+    int32_t* h_sample_tok = nullptr;    // pinned: the same layout
     uint64_t* d_trace = nullptr;        // timeline of the last traced step
     int32_t trace_blocks = 0, trace_slots = 0;
     bool trace_valid = false;
@@ -1570,8 +1570,9 @@ int32_t llm_sample_ith(llm_ctx* c, int32_t i, const llm_sampler_params* p, float
     const int32_t j = resolve_row(c, i);
     if (j < 0) { c->err = "no logits for this output"; return -1; }
     if (!c->d_sample_row && !(dalloc(c, &c->d_sample_row, (size_t)c->hp.n_vocab) &&
-                              dalloc(c, &c->d_sample_tok, (size_t)kMaxPenalty + 1) &&
-                              cuda_ok(c, cudaMallocHost(&c->h_sample_tok, sizeof(int32_t)), "cudaMallocHost")))
+                              dalloc(c, &c->d_sample_tok, (size_t)kMaxPenalty + 2) &&
+                              cuda_ok(c, cudaMallocHost(&c->h_sample_tok, sizeof(int32_t) * (kMaxPenalty + 2)),
+                                      "cudaMallocHost")))
         return -1;
     SampleArgs a;
     a.logits = c->d_logits + (size_t)j * c->hp.n_vocab;
@@ -1581,18 +1582,19 @@ int32_t llm_sample_ith(llm_ctx* c, int32_t i, const llm_sampler_params* p, float
     a.penalty = p->repeat_penalty;
     a.top_k = p->top_k; a.top_p = p->top_p; a.min_p = p->min_p; a.temperature = p->temperature; a.u = u;
     a.scratch = c->d_sample_row;
-    a.out = c->d_sample_tok + kMaxPenalty;
-    a.err = c->d_err;
+    a.out = c->d_sample_tok + kMaxPenalty;              // then the status word
+    a.err = reinterpret_cast<uint32_t*>(c->d_sample_tok + kMaxPenalty + 1);
+    if (a.n_pen > 0) std::memcpy(c->h_sample_tok, p->penalty_tokens, sizeof(int32_t) * a.n_pen);
     const bool ok =
-        (a.n_pen == 0 || cuda_ok(c, cudaMemcpyAsync(c->d_sample_tok, p->penalty_tokens, sizeof(int32_t) * a.n_pen,
+        (a.n_pen == 0 || cuda_ok(c, cudaMemcpyAsync(c->d_sample_tok, c->h_sample_tok, sizeof(int32_t) * a.n_pen,
                                                     cudaMemcpyHostToDevice, c->st), "copy")) &&
-        cuda_ok(c, cudaMemsetAsync(c->d_err, 0, sizeof(uint32_t), c->st), "memset") &&
         (launch_sample(a, c->st) || (c->err = "sampler launch failed", false)) &&
-        cuda_ok(c, cudaMemcpyAsync(c->h_sample_tok, a.out, sizeof(int32_t), cudaMemcpyDeviceToHost, c->st), "copy") &&
-        cuda_ok(c, cudaMemcpyAsync(c->h_err, c->d_err, sizeof(uint32_t), cudaMemcpyDeviceToHost, c->st), "copy") &&
+        cuda_ok(c, cudaMemcpyAsync(c->h_sample_tok + kMaxPenalty, a.out, 2 * sizeof(int32_t),
+                                   cudaMemcpyDeviceToHost, c->st), "copy") &&
         cuda_ok(c, cudaStreamSynchronize(c->st), "sampler");
-    if (!ok || *c->h_err != 0) return -1;
-    return *c->h_sample_tok;
+    if (!ok) return -1;
+    if (c->h_sample_tok[kMaxPenalty + 1] != 0) { c->err = "sampler found no candidate"; return -1; }
+    return c->h_sample_tok[kMaxPenalty];
 }
 
 int llm_debug_set_logits(llm_ctx* c, int32_t i, const float* row) {

@@ -3,17 +3,18 @@
 // greedily or at random; a backend sampler picks on the device so the logits need not be copied
 // to the host).
 //
-// One block over one logits row (V floats):
+// One block of 1024 threads over one logits row (V floats):
 //   1. the row into a scratch row, the repeat penalty applied to each distinct listed token
 //      (l > 0 -> l / r, else l * r);
-//   2. the k-th largest value by a 4-pass radix select (8-bit digits) over an order-preserving
-//      integer key; candidates = every value above it, plus the lowest token ids among those equal
-//      to it (a block-wide prefix count over contiguous chunks keeps that deterministic);
+//   2. the k-th largest value by a 3-pass radix select (11, 11, 10 bits) over an order-preserving
+//      integer key (histograms aggregated per warp, the digit found by a block scan);
+//      candidates = every value above it, plus the lowest token ids among those equal to it
+//      (when more are equal than needed, a block scan over contiguous chunks ranks them);
 //   3. a bitonic sort of the candidates by (value descending, token id ascending);
-//   4. one thread walks the sorted list: top-p on the untempered probabilities (the shortest
-//      prefix reaching p), min-p (l - l_max >= ln min_p), then temperature and the pick: the first
-//      candidate whose cumulative weight exp((l - l_max) / t) exceeds u times the total, u being
-//      the caller's uniform draw in [0, 1); t <= 0 picks the first candidate.
+//   4. over the sorted list, with block scans: top-p on the untempered probabilities (the
+//      shortest prefix reaching p), min-p (l - l_max >= ln min_p), then temperature and the pick:
+//      the first candidate whose cumulative weight exp((l - l_max) / t) exceeds u times the
+//      total, u being the caller's uniform draw in [0, 1); t <= 0 picks the first candidate.
 #include <cuda_runtime.h>
 
 #include <climits>
@@ -27,7 +28,10 @@ namespace llm {
 namespace {
 
 constexpr int kThreadsS = 1024;
+constexpr int kWarpsS = kThreadsS / 32;
 constexpr int kMaxK = 4096;
+constexpr int kPer = kMaxK / kThreadsS;                  // sorted candidates per thread
+constexpr int kBins = 2048;
 
 __device__ __forceinline__ uint32_t fkey(float v) {
     if (v != v) return 0u;                                  // NaN sorts below everything
@@ -35,12 +39,40 @@ __device__ __forceinline__ uint32_t fkey(float v) {
     return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
 }
 
+// Inclusive sum over the block's threads (every thread calls it; wsum holds 32 words).
+template <typename T>
+__device__ T block_scan(T v, T* wsum, T* total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const T n = __shfl_up_sync(0xffffffffu, v, off);
+        if (lane >= off) v += n;
+    }
+    if (lane == 31) wsum[warp] = v;
+    __syncthreads();
+    if (warp == 0) {
+        T w = wsum[lane];
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const T n = __shfl_up_sync(0xffffffffu, w, off);
+            if (lane >= off) w += n;
+        }
+        wsum[lane] = w;
+    }
+    __syncthreads();
+    if (warp > 0) v += wsum[warp - 1];
+    if (total) *total = wsum[kWarpsS - 1];
+    __syncthreads();                                        // wsum free for the next scan
+    return v;
+}
+
 __global__ void __launch_bounds__(kThreadsS) sample_kernel(SampleArgs a) {
-    __shared__ uint32_t hist[256];
+    __shared__ uint32_t hist[kBins];
     __shared__ unsigned long long cand[kMaxK];              // (~key << 32) | token id
-    __shared__ uint32_t chunk_eq[kThreadsS];
-    __shared__ uint32_t s_prefix, s_mask, s_remaining, n_cand;
-    const int tid = threadIdx.x;
+    __shared__ uint32_t wsum_u[32];
+    __shared__ float wsum_f[32];
+    __shared__ uint32_t s_prefix, s_remaining, n_cand, s_first;
+    const int tid = threadIdx.x, lane = tid & 31;
     const int V = a.V;
     float* row = a.scratch;
 
@@ -48,68 +80,96 @@ __global__ void __launch_bounds__(kThreadsS) sample_kernel(SampleArgs a) {
     for (int v = tid; v < V; v += kThreadsS) row[v] = a.logits[v];
     __syncthreads();
     if (a.penalty != 1.0f) {
-        for (int j = tid; j < a.n_pen; j += kThreadsS) {
-            const int t = a.pen_tok[j];
+        // the listed tokens in shared memory (the candidate buffer is free until step 2)
+        int* pen = reinterpret_cast<int*>(cand);
+        const int np = min(a.n_pen, 2 * kMaxK);
+        for (int j = tid; j < np; j += kThreadsS) pen[j] = a.pen_tok[j];
+        __syncthreads();
+        for (int j = tid; j < np; j += kThreadsS) {
+            const int t = pen[j];
             bool first = t >= 0 && t < V;
-            for (int i = 0; i < j && first; ++i) first = a.pen_tok[i] != t;
+            for (int i = 0; i < j && first; ++i) first = pen[i] != t;
             if (first) row[t] = row[t] > 0.f ? row[t] / a.penalty : row[t] * a.penalty;
         }
+        __syncthreads();
     }
+    if (tid == 0) { s_prefix = 0u; s_remaining = (uint32_t)min(a.top_k, V); n_cand = 0u; }
     __syncthreads();
 
-    // 2. radix select of the k-th largest key
-    const uint32_t k = (uint32_t)min(a.top_k, V);
-    if (tid == 0) { s_prefix = 0u; s_mask = 0u; s_remaining = k; n_cand = 0u; }
-    for (int shift = 24; shift >= 0; shift -= 8) {
-        for (int i = tid; i < 256; i += kThreadsS) hist[i] = 0u;
+    // 2. radix select of the k-th largest key: digits of 11, 11 and 10 bits from the top
+    uint32_t mask = 0u;
+    for (int pass = 0; pass < 3; ++pass) {
+        const int shift = pass == 0 ? 21 : pass == 1 ? 10 : 0;
+        const uint32_t dmask = pass == 2 ? 0x3FFu : 0x7FFu;
+        for (int i = tid; i < kBins; i += kThreadsS) hist[i] = 0u;
         __syncthreads();
-        const uint32_t prefix = s_prefix, mask = s_mask;
-        for (int v = tid; v < V; v += kThreadsS) {
-            const uint32_t key = fkey(row[v]);
-            if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 0xFFu], 1u);
-        }
-        __syncthreads();
-        if (tid == 0) {
-            uint32_t rem = s_remaining, acc = 0u;
-            int d = 255;
-            for (; d > 0; --d) {
-                if (acc + hist[d] >= rem) break;
-                acc += hist[d];
+        const uint32_t prefix = s_prefix;
+        for (int v0 = 0; v0 < V; v0 += kThreadsS) {
+            const int v = v0 + tid;
+            uint32_t bin = 0xFFFFFFFFu;
+            if (v < V) {
+                const uint32_t key = fkey(row[v]);
+                if ((key & mask) == prefix) bin = (key >> shift) & dmask;
             }
-            s_prefix = prefix | ((uint32_t)d << shift);
-            s_mask = mask | (0xFFu << shift);
-            s_remaining = rem - acc;
+            const unsigned same = __match_any_sync(0xffffffffu, bin);
+            if (bin != 0xFFFFFFFFu && lane == __ffs(same) - 1) atomicAdd(&hist[bin], (uint32_t)__popc(same));
         }
         __syncthreads();
+        // thread i holds bins 2047 - 2i and 2046 - 2i (descending): the digit where the count
+        // from the top reaches the remaining rank
+        const uint32_t rem = s_remaining;
+        const int b_hi = kBins - 1 - 2 * tid, b_lo = b_hi - 1;
+        const uint32_t c = hist[b_hi] + hist[b_lo];
+        const uint32_t incl = block_scan<uint32_t>(c, wsum_u, nullptr);
+        const uint32_t excl = incl - c;
+        if (excl < rem && incl >= rem) {
+            const bool in_hi = excl + hist[b_hi] >= rem;
+            const uint32_t d = (uint32_t)(in_hi ? b_hi : b_lo);
+            s_prefix = prefix | (d << shift);
+            s_remaining = rem - (in_hi ? excl : excl + hist[b_hi]);
+        }
+        mask |= dmask << shift;
+        __syncthreads();
     }
-    const uint32_t thr = s_prefix, need_eq = s_remaining;    // take need_eq of the keys == thr
+    const uint32_t thr = s_prefix, need_eq = s_remaining;  // take need_eq of the keys == thr
+    const uint32_t n_eq = hist[thr & 0x3FFu];                // keys equal to thr (last histogram)
 
-    // candidates above the threshold
-    for (int v = tid; v < V; v += kThreadsS) {
-        const uint32_t key = fkey(row[v]);
-        if (key > thr) {
-            const uint32_t j = atomicAdd(&n_cand, 1u);
-            if (j < (uint32_t)kMaxK) cand[j] = ((unsigned long long)(~key) << 32) | (uint32_t)v;
+    // candidates above the threshold (and all the equal ones when exactly enough are equal)
+    const bool take_all_eq = n_eq == need_eq;
+    for (int v0 = 0; v0 < V; v0 += kThreadsS) {
+        const int v = v0 + tid;
+        uint32_t key = 0u;
+        bool take = false;
+        if (v < V) {
+            key = fkey(row[v]);
+            take = key > thr || (take_all_eq && key == thr);
+        }
+        const unsigned ball = __ballot_sync(0xffffffffu, take);
+        if (ball) {
+            uint32_t base = 0u;
+            if (lane == 0) base = atomicAdd(&n_cand, (uint32_t)__popc(ball));
+            base = __shfl_sync(0xffffffffu, base, 0);
+            if (take) {
+                const uint32_t j = base + __popc(ball & ((1u << lane) - 1u));
+                if (j < (uint32_t)kMaxK) cand[j] = ((unsigned long long)(~key) << 32) | (uint32_t)v;
+            }
         }
     }
-    // ties at the threshold: the lowest token ids, by a prefix count over contiguous chunks
-    const int chunk = (V + kThreadsS - 1) / kThreadsS;
-    const int v0 = tid * chunk, v1 = min(V, v0 + chunk);
-    uint32_t cnt = 0u;
-    for (int v = v0; v < v1; ++v) cnt += fkey(row[v]) == thr;
-    chunk_eq[tid] = cnt;
-    __syncthreads();
-    if (tid == 0) {
-        uint32_t run = 0u;
-        for (int i = 0; i < kThreadsS; ++i) { const uint32_t c = chunk_eq[i]; chunk_eq[i] = run; run += c; }
-    }
-    __syncthreads();
-    uint32_t rank = chunk_eq[tid];
-    for (int v = v0; v < v1 && rank < need_eq; ++v) {
-        if (fkey(row[v]) != thr) continue;
-        const uint32_t j = atomicAdd(&n_cand, 1u);
-        if (j < (uint32_t)kMaxK) cand[j] = ((unsigned long long)(~thr) << 32) | (uint32_t)v;
-        ++rank;
+    if (!take_all_eq) {
+        // more keys equal the threshold than needed: the lowest token ids, ranked by a block
+        // scan of per-thread counts over contiguous chunks
+        __syncthreads();
+        const int chunk = (V + kThreadsS - 1) / kThreadsS;
+        const int v0 = tid * chunk, v1 = min(V, v0 + chunk);
+        uint32_t cnt = 0u;
+        for (int v = v0; v < v1; ++v) cnt += fkey(row[v]) == thr;
+        uint32_t rank = block_scan<uint32_t>(cnt, wsum_u, nullptr) - cnt;
+        for (int v = v0; v < v1 && rank < need_eq; ++v) {
+            if (fkey(row[v]) != thr) continue;
+            const uint32_t j = atomicAdd(&n_cand, 1u);
+            if (j < (uint32_t)kMaxK) cand[j] = ((unsigned long long)(~thr) << 32) | (uint32_t)v;
+            ++rank;
+        }
     }
     __syncthreads();
 
@@ -132,43 +192,82 @@ __global__ void __launch_bounds__(kThreadsS) sample_kernel(SampleArgs a) {
             __syncthreads();
         }
     }
-
-    // 4. cut-offs, temperature and the pick, in the sorted order
-    if (tid == 0) {
-        if (n == 0u) { atomicOr(a.err, ERR_ROW_RANGE); *a.out = -1; return; }
-        const float l0 = row[(uint32_t)cand[0]];
-        uint32_t m = n;
-        if (a.top_p < 1.0f) {
-            float z = 0.f;
-            for (uint32_t i = 0; i < m; ++i) z += expf(row[(uint32_t)cand[i]] - l0);
-            float c = 0.f;
-            uint32_t keep = m;
-            for (uint32_t i = 0; i < m; ++i) {
-                c += expf(row[(uint32_t)cand[i]] - l0);
-                if (c / z >= a.top_p) { keep = i + 1; break; }
-            }
-            m = keep;
-        }
-        if (a.min_p > 0.0f) {
-            const float lm = logf(a.min_p);
-            uint32_t keep = 1;
-            while (keep < m && row[(uint32_t)cand[keep]] - l0 >= lm) ++keep;
-            m = keep;
-        }
-        int token = (int)(uint32_t)cand[0];
-        if (a.temperature > 0.0f) {
-            float z = 0.f;
-            for (uint32_t i = 0; i < m; ++i) z += expf((row[(uint32_t)cand[i]] - l0) / a.temperature);
-            const float target = a.u * z;
-            float c = 0.f;
-            token = (int)(uint32_t)cand[m - 1];
-            for (uint32_t i = 0; i < m; ++i) {
-                c += expf((row[(uint32_t)cand[i]] - l0) / a.temperature);
-                if (c > target) { token = (int)(uint32_t)cand[i]; break; }
-            }
-        }
-        *a.out = token;
+    if (n == 0u) {
+        if (tid == 0) { *a.out = -1; *a.err = ERR_ROW_RANGE; }
+        return;
     }
+
+    // 4. cut-offs, temperature and the pick over the sorted list; thread t holds candidates
+    // kPer t .. kPer t + kPer - 1
+    const float l0 = row[(uint32_t)cand[0]];
+    float lv[kPer];
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+        const uint32_t i = (uint32_t)(tid * kPer + j);
+        lv[j] = i < n ? row[(uint32_t)cand[i]] : -INFINITY;
+    }
+    uint32_t m = n;
+    auto first_index = [&](bool hit, uint32_t i) {          // block-wide smallest i with hit
+        if (tid == 0) s_first = 0xFFFFFFFFu;
+        __syncthreads();
+        if (hit) atomicMin(&s_first, i);
+        __syncthreads();
+        const uint32_t f = s_first;
+        __syncthreads();
+        return f;
+    };
+    if (a.top_p < 1.0f) {
+        float e[kPer], loc = 0.f;
+#pragma unroll
+        for (int j = 0; j < kPer; ++j) {
+            e[j] = (uint32_t)(tid * kPer + j) < m ? expf(lv[j] - l0) : 0.f;
+            loc += e[j];
+        }
+        float z = 0.f;
+        float c = block_scan<float>(loc, wsum_f, &z) - loc;
+        uint32_t hit = 0xFFFFFFFFu;
+#pragma unroll
+        for (int j = 0; j < kPer; ++j) {
+            c += e[j];
+            const uint32_t i = (uint32_t)(tid * kPer + j);
+            if (i < m && hit == 0xFFFFFFFFu && c / z >= a.top_p) hit = i;
+        }
+        const uint32_t f = first_index(hit != 0xFFFFFFFFu, hit);
+        if (f != 0xFFFFFFFFu) m = f + 1;
+    }
+    if (a.min_p > 0.0f) {
+        const float lm = logf(a.min_p);
+        uint32_t miss = 0xFFFFFFFFu;
+#pragma unroll
+        for (int j = 0; j < kPer; ++j) {
+            const uint32_t i = (uint32_t)(tid * kPer + j);
+            if (i >= 1 && i < m && miss == 0xFFFFFFFFu && !(lv[j] - l0 >= lm)) miss = i;
+        }
+        const uint32_t f = first_index(miss != 0xFFFFFFFFu, miss);
+        if (f != 0xFFFFFFFFu) m = f;
+    }
+    int token = (int)(uint32_t)cand[0];
+    if (a.temperature > 0.0f) {
+        float w[kPer], loc = 0.f;
+#pragma unroll
+        for (int j = 0; j < kPer; ++j) {
+            w[j] = (uint32_t)(tid * kPer + j) < m ? expf((lv[j] - l0) / a.temperature) : 0.f;
+            loc += w[j];
+        }
+        float z = 0.f;
+        float c = block_scan<float>(loc, wsum_f, &z) - loc;
+        const float target = a.u * z;
+        uint32_t hit = 0xFFFFFFFFu;
+#pragma unroll
+        for (int j = 0; j < kPer; ++j) {
+            c += w[j];
+            const uint32_t i = (uint32_t)(tid * kPer + j);
+            if (i < m && hit == 0xFFFFFFFFu && c > target) hit = i;
+        }
+        const uint32_t f = first_index(hit != 0xFFFFFFFFu, hit);
+        token = (int)(uint32_t)cand[f != 0xFFFFFFFFu ? f : m - 1];
+    }
+    if (tid == 0) { *a.out = token; *a.err = 0u; }
 }
 
 }  // namespace
