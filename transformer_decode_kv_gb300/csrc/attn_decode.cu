@@ -391,36 +391,57 @@ constexpr int kMW = 4;                   // warps
 constexpr int kMT = kMW * 32;            // threads
 constexpr int kMC = kCH / kMW;           // cells per warp and pass (one m16 fragment)
 
-template <int HD>
+// KT = int8_t: a Q8_0 cache. Its int8 rows are staged as they are, expanded to exact f16 values
+// in a shared tile per pass, and the block scales enter outside the MMAs: a score sums each
+// 32-dimension block's fragment times the cell's K scale; the P^T fragment is multiplied by the
+// cells' V scales for each 32-dimension output block.
+template <int HD, typename KT>
 struct MmaDecSmem {
-    static constexpr int RS = HD + 8;                     // halves per padded row
-    static constexpr int RB = HD * 2;                     // bytes of a cached row
-    static constexpr size_t rows = 2 * (size_t)kCH * RS * 2;
-    static constexpr size_t stage = rows + 3 * kCH * 4;
-    static constexpr size_t bytes = 2 * stage + (size_t)kGQ * HD * 4 /* q */ +
+    static constexpr bool Q8 = sizeof(KT) == 1;
+    static constexpr int NB = HD / 32;
+    static constexpr int RS = HD + 8;                     // halves per padded f16 row
+    static constexpr int RB = HD * (int)sizeof(KT);       // bytes of a cached row
+    static constexpr int RSS = Q8 ? RB + 16 : RS * 2;     // bytes per staged row
+    static constexpr size_t rows = 2 * (size_t)kCH * RSS;
+    static constexpr size_t stage = rows + 3 * kCH * 4 + (Q8 ? 2 * (size_t)kCH * NB * 4 : 0);
+    static constexpr size_t tile = Q8 ? 2 * (size_t)kCH * RS * 2 : 0;   // expanded K and V
+    static constexpr size_t bytes = 2 * stage + tile + (size_t)kGQ * HD * 4 /* q */ +
                                     (size_t)kMW * kMC * 8 * 4 /* P^T per warp */ +
                                     (size_t)kMW * kGQ * (HD + 2) * 4 /* warp states */ +
                                     (size_t)kGQ * (HD + 2) * 4 /* block partial */ + 16;
 };
 
-template <int HD>
+// two int8 (low bytes of v, selected by sel) -> an exact half2: the biased byte as the low
+// mantissa bits of 1024, minus 1024 + 128
+__device__ __forceinline__ uint32_t q8x2_to_h2(uint32_t biased, uint32_t sel) {
+    const uint32_t h = __byte_perm(biased, 0x64646464u, sel);
+    const __half2 v = __hsub2(*reinterpret_cast<const __half2*>(&h), __half2half2(__ushort_as_half(0x6480u)));
+    return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+template <int HD, typename KT>
 __global__ void __launch_bounds__(kMT)
 attn_decode_mma_kernel(AttnArgs a, float scale_log2) {
-    using SM = MmaDecSmem<HD>;
-    constexpr int RS = SM::RS, RB = SM::RB, VPR = RB / 16, NK = HD / 16;
+    using SM = MmaDecSmem<HD, KT>;
+    constexpr bool Q8 = SM::Q8;
+    constexpr int RS = SM::RS, RB = SM::RB, RSS = SM::RSS, VPR = RB / 16, NK = HD / 16, NB = SM::NB;
     extern __shared__ __align__(16) uint8_t sm[];
-    struct St { __half* kb; __half* vb; int* ccell; int* cvis; int* cfresh; };
+    struct St { uint8_t* kraw; uint8_t* vraw; int* ccell; int* cvis; int* cfresh; float* ksc; float* vsc; };
     auto stage_of = [&](int s) {
         uint8_t* b = sm + (size_t)s * SM::stage;
         St S;
-        S.kb = reinterpret_cast<__half*>(b);
-        S.vb = S.kb + kCH * RS;
+        S.kraw = b;
+        S.vraw = b + kCH * RSS;
         S.ccell = reinterpret_cast<int*>(b + SM::rows);
         S.cvis = S.ccell + kCH;
         S.cfresh = S.cvis + kCH;
+        S.ksc = reinterpret_cast<float*>(S.cfresh + kCH);
+        S.vsc = S.ksc + kCH * NB;
         return S;
     };
-    float* qs = reinterpret_cast<float*>(sm + 2 * SM::stage);          // [kGQ][HD]
+    __half* tk = reinterpret_cast<__half*>(sm + 2 * SM::stage);       // Q8_0: expanded K tile
+    __half* tv = tk + kCH * RS;                                         //        and V tile
+    float* qs = reinterpret_cast<float*>(sm + 2 * SM::stage + SM::tile);  // [kGQ][HD]
     float* pT = qs + kGQ * HD;                                          // [warp][16 cells][8]
     float* ws = pT + kMW * kMC * 8;                                     // [warp][kGQ][HD + 2]
     float* pst = ws + kMW * kGQ * (HD + 2);                             // block partial (peers read it)
@@ -441,9 +462,12 @@ attn_decode_mma_kernel(AttnArgs a, float scale_log2) {
     const int npass = c1 > c0 ? (c1 - c0 + kCH - 1) / kCH : 1;
     const uint8_t* K = static_cast<const uint8_t*>(a.kc) + (int64_t)kvh * a.n_ctx * RB;
     const uint8_t* V = static_cast<const uint8_t*>(a.vc) + (int64_t)kvh * a.n_ctx * RB;
+    const __half* KS = q8_scales(a.kc, a, kvh);
+    const __half* VS = q8_scales(a.vc, a, kvh);
 
     int pf_cell = -1, pf_pos = 0;
-    auto fetch = [&](int i) {
+    float pf_ks[NB], pf_vs[NB];
+    auto fetch = [&](int i, bool with_scales) {
         if (threadIdx.x < kCH) {
             const int ci = c0 + i * kCH + threadIdx.x;
             pf_cell = -1;
@@ -452,9 +476,20 @@ attn_decode_mma_kernel(AttnArgs a, float scale_log2) {
                 pf_cell = a.list_cells[base + ci];
                 pf_pos = a.list_pos[base + ci];
             }
+            if constexpr (Q8) {
+                if (with_scales && pf_cell >= 0 && pf_cell < a.n_ctx && pf_pos <= tpos) {
+#pragma unroll
+                    for (int b = 0; b < NB; ++b) {
+                        pf_ks[b] = ld_scale(KS + (int64_t)pf_cell * NB + b);
+                        pf_vs[b] = ld_scale(VS + (int64_t)pf_cell * NB + b);
+                    }
+                }
+            }
         }
     };
-    auto setup = [&](const St& S) {
+    // stage S takes the fetched entry; Q8_0: hidden cells get zero scales (their rows stay stale
+    // but finite), cells of this step get theirs after the wait
+    auto setup = [&](const St& S, bool pre_wait) {
         if (threadIdx.x < kCH) {
             int cell = -1, vis = 0, fresh = 0;
             if (pf_cell >= 0 && pf_cell < a.n_ctx) {
@@ -465,6 +500,20 @@ attn_decode_mma_kernel(AttnArgs a, float scale_log2) {
             S.ccell[threadIdx.x] = cell;
             S.cvis[threadIdx.x] = vis && cell >= 0;
             S.cfresh[threadIdx.x] = fresh;
+            if constexpr (Q8) {
+                const bool v = vis && cell >= 0;
+#pragma unroll
+                for (int b = 0; b < NB; ++b) {
+                    float ks = 0.f, vs = 0.f;
+                    if (v && !pre_wait) { ks = pf_ks[b]; vs = pf_vs[b]; }
+                    if (v && pre_wait && !fresh) {
+                        ks = ld_scale(KS + (int64_t)cell * NB + b);
+                        vs = ld_scale(VS + (int64_t)cell * NB + b);
+                    }
+                    S.ksc[threadIdx.x * NB + b] = ks;
+                    S.vsc[threadIdx.x * NB + b] = vs;
+                }
+            }
         }
     };
     auto issue = [&](const St& S, bool pre_wait) {
@@ -472,33 +521,43 @@ attn_decode_mma_kernel(AttnArgs a, float scale_log2) {
             const int c = v / VPR, j = v % VPR;
             if (!S.cvis[c]) {
                 // the MMA multiplies every row of the tile: a hidden cell's V row must be finite
-                *reinterpret_cast<uint4*>(S.vb + c * RS + j * 8) = make_uint4(0u, 0u, 0u, 0u);
+                if constexpr (!Q8) *reinterpret_cast<uint4*>(S.vraw + c * RSS + j * 16) = make_uint4(0u, 0u, 0u, 0u);
                 continue;
             }
             if (pre_wait && S.cfresh[c]) continue;
             const size_t src = (size_t)S.ccell[c] * RB + j * 16;
-            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sm32(S.kb + c * RS + j * 8)), "l"(K + src) : "memory");
-            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sm32(S.vb + c * RS + j * 8)), "l"(V + src) : "memory");
+            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sm32(S.kraw + c * RSS + j * 16)), "l"(K + src) : "memory");
+            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sm32(S.vraw + c * RSS + j * 16)), "l"(V + src) : "memory");
         }
         asm volatile("cp.async.commit_group;" ::: "memory");
     };
 
     {
         const St S0 = stage_of(0);
-        fetch(0);
-        setup(S0);
+        fetch(0, false);
+        setup(S0, true);
         __syncthreads();
         issue(S0, true);
         asm volatile("griddepcontrol.wait;" ::: "memory");
         for (int i = threadIdx.x; i < kGQ * HD; i += kMT)
             qs[i] = a.q[(int64_t)t * a.ldq + (kvh * kGQ + i / HD) * HD + i % HD] * scale_log2;
-        if (npass > 1) fetch(1);
+        if (npass > 1) fetch(1, true);
         for (int v = threadIdx.x; v < kCH * VPR; v += kMT) {
             const int c = v / VPR, j = v % VPR;
             if (!S0.cvis[c] || !S0.cfresh[c]) continue;
             const size_t src = (size_t)S0.ccell[c] * RB + j * 16;
-            *reinterpret_cast<uint4*>(S0.kb + c * RS + j * 8) = __ldcg(reinterpret_cast<const uint4*>(K + src));
-            *reinterpret_cast<uint4*>(S0.vb + c * RS + j * 8) = __ldcg(reinterpret_cast<const uint4*>(V + src));
+            *reinterpret_cast<uint4*>(S0.kraw + c * RSS + j * 16) = __ldcg(reinterpret_cast<const uint4*>(K + src));
+            *reinterpret_cast<uint4*>(S0.vraw + c * RSS + j * 16) = __ldcg(reinterpret_cast<const uint4*>(V + src));
+        }
+        if constexpr (Q8) {
+            if (threadIdx.x < kCH && S0.cvis[threadIdx.x] && S0.cfresh[threadIdx.x]) {
+                const int cell = S0.ccell[threadIdx.x];
+#pragma unroll
+                for (int b = 0; b < NB; ++b) {
+                    S0.ksc[threadIdx.x * NB + b] = ld_scale(KS + (int64_t)cell * NB + b);
+                    S0.vsc[threadIdx.x * NB + b] = ld_scale(VS + (int64_t)cell * NB + b);
+                }
+            }
         }
     }
     __syncthreads();                                            // qs
@@ -524,8 +583,8 @@ attn_decode_mma_kernel(AttnArgs a, float scale_log2) {
         const St S = stage_of(i & 1);
         if (i + 1 < npass) {
             const St N = stage_of((i + 1) & 1);
-            setup(N);
-            if (i + 2 < npass) fetch(i + 2);
+            setup(N, false);
+            if (i + 2 < npass) fetch(i + 2, true);
             __syncthreads();
             issue(N, false);
             asm volatile("cp.async.wait_group 1;" ::: "memory");
@@ -533,18 +592,53 @@ attn_decode_mma_kernel(AttnArgs a, float scale_log2) {
             asm volatile("cp.async.wait_group 0;" ::: "memory");
         }
         __syncthreads();
+        const __half* kb;
+        const __half* vb;
+        if constexpr (Q8) {
+            // int8 rows -> exact f16 tiles (the previous pass's MMAs ended at the last barrier)
+            for (int idx = threadIdx.x; idx < kCH * (HD / 4); idx += kMT) {
+                const int c = idx / (HD / 4), w4 = idx % (HD / 4);
+                const uint32_t kq = *reinterpret_cast<const uint32_t*>(S.kraw + c * RSS + w4 * 4) ^ 0x80808080u;
+                const uint32_t vq = *reinterpret_cast<const uint32_t*>(S.vraw + c * RSS + w4 * 4) ^ 0x80808080u;
+                *reinterpret_cast<uint2*>(tk + c * RS + w4 * 4) = make_uint2(q8x2_to_h2(kq, 0x7170u), q8x2_to_h2(kq, 0x7372u));
+                *reinterpret_cast<uint2*>(tv + c * RS + w4 * 4) = make_uint2(q8x2_to_h2(vq, 0x7170u), q8x2_to_h2(vq, 0x7372u));
+            }
+            __syncthreads();
+            kb = tk;
+            vb = tv;
+        } else {
+            kb = reinterpret_cast<const __half*>(S.kraw);
+            vb = reinterpret_cast<const __half*>(S.vraw);
+        }
 
-        // S^T [16 cells][8 heads] = K Q^T
+        // S^T [16 cells][8 heads] = K Q^T (Q8_0: per 32-dimension block, times the cells' K scales)
         float s[4] = {0.f, 0.f, 0.f, 0.f};
         {
             const int mi = lane >> 3, r = lane & 7;
-            const __half* kr = S.kb + (cw + r + (mi & 1) * 8) * RS + (mi >> 1) * 8;
+            const __half* kr = kb + (cw + r + (mi & 1) * 8) * RS + (mi >> 1) * 8;
+            if constexpr (Q8) {
 #pragma unroll
-            for (int kk = 0; kk < NK; ++kk) {
-                uint32_t af[4];
-                ldsm_x4(sm32(kr + kk * 16), af[0], af[1], af[2], af[3]);
-                mma16816(s, af, qh[kk][0], qh[kk][1]);
-                mma16816(s, af, ql[kk][0], ql[kk][1]);
+                for (int b = 0; b < NB; ++b) {
+                    float sb[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                    for (int kk = 2 * b; kk < 2 * b + 2; ++kk) {
+                        uint32_t af[4];
+                        ldsm_x4(sm32(kr + kk * 16), af[0], af[1], af[2], af[3]);
+                        mma16816(sb, af, qh[kk][0], qh[kk][1]);
+                        mma16816(sb, af, ql[kk][0], ql[kk][1]);
+                    }
+                    const float d0 = S.ksc[(cw + g) * NB + b], d1 = S.ksc[(cw + g + 8) * NB + b];
+                    s[0] = fmaf(d0, sb[0], s[0]); s[1] = fmaf(d0, sb[1], s[1]);
+                    s[2] = fmaf(d1, sb[2], s[2]); s[3] = fmaf(d1, sb[3], s[3]);
+                }
+            } else {
+#pragma unroll
+                for (int kk = 0; kk < NK; ++kk) {
+                    uint32_t af[4];
+                    ldsm_x4(sm32(kr + kk * 16), af[0], af[1], af[2], af[3]);
+                    mma16816(s, af, qh[kk][0], qh[kk][1]);
+                    mma16816(s, af, ql[kk][0], ql[kk][1]);
+                }
             }
         }
         // this thread: cells cw+g (s[0], s[1]) and cw+g+8 (s[2], s[3]), heads 2cq and 2cq+1
@@ -578,15 +672,28 @@ attn_decode_mma_kernel(AttnArgs a, float scale_log2) {
         pw[(g + 8) * 8 + 2 * cq] = p[2];
         pw[(g + 8) * 8 + 2 * cq + 1] = p[3];
         __syncwarp();
-        uint32_t bh0, bl0, bh1, bl1;
-        split_h2(pw[(2 * cq) * 8 + g], pw[(2 * cq + 1) * 8 + g], bh0, bl0);
-        split_h2(pw[(2 * cq + 8) * 8 + g], pw[(2 * cq + 9) * 8 + g], bh1, bl1);
-        // O^T [16 dims][8 heads] += V^T P^T per 16-dimension tile
+        const float pq[4] = {pw[(2 * cq) * 8 + g], pw[(2 * cq + 1) * 8 + g], pw[(2 * cq + 8) * 8 + g],
+                             pw[(2 * cq + 9) * 8 + g]};
+        // O^T [16 dims][8 heads] += V^T P^T per 16-dimension tile (Q8_0: P^T times the cells' V
+        // scales of each 32-dimension block)
         {
             const int mi = lane >> 3, r = lane & 7;
-            const __half* vr = S.vb + (cw + r + (mi >> 1) * 8) * RS + (mi & 1) * 8;
+            const __half* vr = vb + (cw + r + (mi >> 1) * 8) * RS + (mi & 1) * 8;
+            uint32_t bh0, bl0, bh1, bl1;
+            if constexpr (!Q8) {
+                split_h2(pq[0], pq[1], bh0, bl0);
+                split_h2(pq[2], pq[3], bh1, bl1);
+            }
 #pragma unroll
             for (int nt = 0; nt < NK; ++nt) {
+                if constexpr (Q8) {
+                    if ((nt & 1) == 0) {
+                        const int b = nt / 2;
+                        const float* vs = S.vsc + (cw + 2 * cq) * NB + b;
+                        split_h2(pq[0] * vs[0], pq[1] * vs[NB], bh0, bl0);
+                        split_h2(pq[2] * vs[8 * NB], pq[3] * vs[9 * NB], bh1, bl1);
+                    }
+                }
                 uint32_t af[4];
                 ldsm_x4_t(sm32(vr + nt * 16), af[0], af[1], af[2], af[3]);
                 mma16816(o[nt], af, bh0, bh1);
@@ -652,11 +759,11 @@ attn_decode_mma_kernel(AttnArgs a, float scale_log2) {
     cluster_sync_all();
 }
 
-template <int HD>
+template <int HD, typename KT>
 bool launch_dec_mma(const AttnArgs& a, cudaStream_t st) {
     const float scale_log2 = (float)(1.4426950408889634 / sqrt((double)HD));
-    constexpr size_t smem = MmaDecSmem<HD>::bytes;
-    auto k = attn_decode_mma_kernel<HD>;
+    constexpr size_t smem = MmaDecSmem<HD, KT>::bytes;
+    auto k = attn_decode_mma_kernel<HD, KT>;
     static bool attr = false;
     if (!attr) {
         if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess ||
@@ -716,19 +823,19 @@ bool attention_decode_ok(const AttnArgs& a) {
 }
 
 bool launch_attention_decode(const AttnArgs& a, cudaStream_t st) {
-    if (a.kv_type == W_Q8_0) {
+    if (a.kv_type == W_Q8_0) {                                 // tensor cores
         switch (a.hd) {
-            case 32: return launch_dec<32, int8_t>(a, st);
-            case 64: return launch_dec<64, int8_t>(a, st);
-            case 128: return launch_dec<128, int8_t>(a, st);
+            case 32: return launch_dec_mma<32, int8_t>(a, st);
+            case 64: return launch_dec_mma<64, int8_t>(a, st);
+            case 128: return launch_dec_mma<128, int8_t>(a, st);
         }
         return false;
     }
     if (a.kv_type == W_F16) {                                  // tensor cores
         switch (a.hd) {
-            case 32: return launch_dec_mma<32>(a, st);
-            case 64: return launch_dec_mma<64>(a, st);
-            case 128: return launch_dec_mma<128>(a, st);
+            case 32: return launch_dec_mma<32, __half>(a, st);
+            case 64: return launch_dec_mma<64, __half>(a, st);
+            case 128: return launch_dec_mma<128, __half>(a, st);
         }
         return false;
     }

@@ -142,7 +142,7 @@ struct SampleArgs {
     float penalty = 1.f;
     int32_t top_k = 1;               // 1 .. sample_max_k()
     float top_p = 1.f, min_p = 0.f, temperature = 0.f, u = 0.f;
-    float* scratch = nullptr;        // [V]
+    float* scratch = nullptr;        // [V + 4], 16-byte aligned
     int32_t* out = nullptr;          // the picked token (device)
     uint32_t* err = nullptr;
 };

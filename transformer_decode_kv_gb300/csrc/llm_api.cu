@@ -1569,7 +1569,7 @@ int32_t llm_sample_ith(llm_ctx* c, int32_t i, const llm_sampler_params* p, float
     }
     const int32_t j = resolve_row(c, i);
     if (j < 0) { c->err = "no logits for this output"; return -1; }
-    if (!c->d_sample_row && !(dalloc(c, &c->d_sample_row, (size_t)c->hp.n_vocab) &&
+    if (!c->d_sample_row && !(dalloc(c, &c->d_sample_row, (size_t)c->hp.n_vocab + 4) &&
                               dalloc(c, &c->d_sample_tok, (size_t)kMaxPenalty + 2) &&
                               cuda_ok(c, cudaMallocHost(&c->h_sample_tok, sizeof(int32_t) * (kMaxPenalty + 2)),
                                       "cudaMallocHost")))

@@ -39,6 +39,34 @@ __device__ __forceinline__ uint32_t fkey(float v) {
     return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
 }
 
+// Calls f(v, x, ok) for every value x = row[v] of the scratch row (16-byte aligned, V % 4 == 0),
+// 16 values per thread and step loaded as four float4 before any is used, so each thread keeps
+// four loads in flight. Every thread makes the same number of calls (ok = false past the end):
+// f may use warp-wide intrinsics.
+template <typename F>
+__device__ __forceinline__ void for_each_value(const float* row, int V, F&& f) {
+    constexpr int kU = 4;
+    const float4* r4 = reinterpret_cast<const float4*>(row);
+    const int V4 = V / 4;
+    for (int i0 = 0; i0 < V4; i0 += kThreadsS * kU) {
+        float4 x[kU];
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+            const int i = i0 + u * kThreadsS + (int)threadIdx.x;
+            x[u] = i < V4 ? r4[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+            const int i = i0 + u * kThreadsS + (int)threadIdx.x;
+            const bool ok = i < V4;
+            f(4 * i, x[u].x, ok);
+            f(4 * i + 1, x[u].y, ok);
+            f(4 * i + 2, x[u].z, ok);
+            f(4 * i + 3, x[u].w, ok);
+        }
+    }
+}
+
 // Inclusive sum over the block's threads (every thread calls it; wsum holds 32 words).
 template <typename T>
 __device__ T block_scan(T v, T* wsum, T* total) {
@@ -76,8 +104,22 @@ __global__ void __launch_bounds__(kThreadsS) sample_kernel(SampleArgs a) {
     const int V = a.V;
     float* row = a.scratch;
 
-    // 1. penalised copy of the row
-    for (int v = tid; v < V; v += kThreadsS) row[v] = a.logits[v];
+    // 1. penalised copy of the row (padded with -inf to a multiple of 4 values; the padding is
+    // never a candidate because k <= V); eight independent loads per thread in flight
+    const int Vp = (V + 3) & ~3;
+    for (int v0 = 0; v0 < Vp; v0 += 8 * kThreadsS) {
+        float x[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int v = v0 + u * kThreadsS + tid;
+            x[u] = v < V ? a.logits[v] : -INFINITY;
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int v = v0 + u * kThreadsS + tid;
+            if (v < Vp) row[v] = x[u];
+        }
+    }
     __syncthreads();
     if (a.penalty != 1.0f) {
         // the listed tokens in shared memory (the candidate buffer is free until step 2)
@@ -104,16 +146,15 @@ __global__ void __launch_bounds__(kThreadsS) sample_kernel(SampleArgs a) {
         for (int i = tid; i < kBins; i += kThreadsS) hist[i] = 0u;
         __syncthreads();
         const uint32_t prefix = s_prefix;
-        for (int v0 = 0; v0 < V; v0 += kThreadsS) {
-            const int v = v0 + tid;
+        for_each_value(row, Vp, [&](int v, float x, bool ok) {
             uint32_t bin = 0xFFFFFFFFu;
-            if (v < V) {
-                const uint32_t key = fkey(row[v]);
+            if (ok && v < V) {
+                const uint32_t key = fkey(x);
                 if ((key & mask) == prefix) bin = (key >> shift) & dmask;
             }
             const unsigned same = __match_any_sync(0xffffffffu, bin);
             if (bin != 0xFFFFFFFFu && lane == __ffs(same) - 1) atomicAdd(&hist[bin], (uint32_t)__popc(same));
-        }
+        });
         __syncthreads();
         // thread i holds bins 2047 - 2i and 2046 - 2i (descending): the digit where the count
         // from the top reaches the remaining rank
@@ -136,12 +177,11 @@ __global__ void __launch_bounds__(kThreadsS) sample_kernel(SampleArgs a) {
 
     // candidates above the threshold (and all the equal ones when exactly enough are equal)
     const bool take_all_eq = n_eq == need_eq;
-    for (int v0 = 0; v0 < V; v0 += kThreadsS) {
-        const int v = v0 + tid;
+    for_each_value(row, Vp, [&](int v, float x, bool ok) {
         uint32_t key = 0u;
         bool take = false;
-        if (v < V) {
-            key = fkey(row[v]);
+        if (ok && v < V) {
+            key = fkey(x);
             take = key > thr || (take_all_eq && key == thr);
         }
         const unsigned ball = __ballot_sync(0xffffffffu, take);
@@ -154,7 +194,7 @@ __global__ void __launch_bounds__(kThreadsS) sample_kernel(SampleArgs a) {
                 if (j < (uint32_t)kMaxK) cand[j] = ((unsigned long long)(~key) << 32) | (uint32_t)v;
             }
         }
-    }
+    });
     if (!take_all_eq) {
         // more keys equal the threshold than needed: the lowest token ids, ranked by a block
         // scan of per-thread counts over contiguous chunks
