@@ -2,17 +2,14 @@
 // Architecture", Example 4 FLASH_ATTN_EXT; Example 11 for the unfused meaning).
 //
 // Every query tile of a decode ubatch holds one token. The kCL blocks of a cluster split the
-// token's cell list into equal slices; each block runs the online softmax of the 4 query heads of
-// its KV head over its slice (warp g = query head g, one cell per lane per 32 cells, hd/32 output
-// dimensions per lane), leaves its partial state (m, l, o) in its own shared memory, and after a
-// cluster barrier every block merges a kCL-th of the output dimensions by reading all partial
-// states through distributed shared memory (mapa + ld.shared::cluster). A second cluster barrier
-// keeps each block's shared memory alive until its peers have read it. No global round trip
-// (fence, ticket, partial rows in L2) is on the merge path.
-//
-// A Q8_0 cache (int8 quants per row, one fp16 scale per 32 values in a separate array) is staged
-// as int8 rows plus float scales; a score sums each 32-value block's products, then scales the
-// block sum, and a value row's scale is folded into the probability of its cell.
+// token's cell list into equal slices and walk them in passes of 64 cells; each block runs the
+// online softmax of the 4 query heads of its KV head over its slice, leaves its partial state
+// (m, l, o) in its own shared memory, and after a cluster barrier every block merges a kCL-th of
+// the output dimensions by reading all partial states through distributed shared memory (mapa +
+// ld.shared::cluster). A second cluster barrier keeps each block's shared memory alive until its
+// peers have read it. No global round trip (fence, ticket, partial rows in L2) is on the merge
+// path. F16 and Q8_0 caches run the contractions on tensor cores (attn_decode_mma_kernel); F32
+// caches on CUDA cores (attn_decode_kernel).
 //
 // The K/V rows of cells written by earlier steps cannot change while the previous kernel (this
 // step's Q/K/V projection) runs, so the first pass stages them with cp.async before
@@ -27,7 +24,6 @@
 #include <cstdint>
 
 #include "attn_common.cuh"
-#include "dev_common.cuh"
 #include "kernels.h"
 
 namespace llm {
@@ -42,11 +38,6 @@ constexpr int kGQ = 4;                   // query heads per KV head: one warp ea
 constexpr int kGroups = 2;               // warp groups, each taking half of every pass
 constexpr int kCG = kCH / kGroups;       // cells per group and pass: one per lane
 constexpr int kThreads = kGQ * 32 * kGroups;
-
-template <typename KT> __device__ __forceinline__ float kvf(KT v);
-template <> __device__ __forceinline__ float kvf<float>(float v) { return v; }
-template <> __device__ __forceinline__ float kvf<__half>(__half v) { return __half2float(v); }
-template <> __device__ __forceinline__ float kvf<int8_t>(int8_t v) { return (float)v; }
 
 __device__ __forceinline__ uint32_t sm32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -68,53 +59,46 @@ __device__ __forceinline__ float ld_peer(const float* local, uint32_t rank) {
     return v;
 }
 
-// KT = int8_t: a Q8_0 cache (int8 quants per row, one fp16 scale per 32 values kept apart)
-template <int HD, typename KT>
+// The F32-cache kernel's shared memory: two stages of one pass (K rows, V rows, then per cell:
+// cell, visible, fresh), Q, and the block and group partial states.
+template <int HD>
 struct DecSmem {
-    static constexpr bool Q8 = sizeof(KT) == 1;
-    static constexpr int NB = HD / 32;                    // Q8_0 blocks per row
-    static constexpr int RB = HD * (int)sizeof(KT);       // bytes of a cached row
+    static constexpr int RB = HD * 4;                     // bytes of a cached row
     static constexpr int RS = RB + 16;                    // padded stride
-    // one pass: K rows, V rows, then per cell: cell, visible, fresh (+ Q8_0: K and V scales)
     static constexpr size_t rows = 2 * (size_t)kCH * RS;
-    static constexpr size_t stage = rows + 3 * kCH * 4 + (Q8 ? 2 * (size_t)kCH * NB * 4 : 0);
+    static constexpr size_t stage = rows + 3 * kCH * 4;
     static constexpr size_t bytes = 2 * stage + (size_t)kGQ * HD * 4 /* q */ +
                                     2 * (size_t)kGQ * (HD + 2) * 4 /* block and group partials */ + 16;
 };
 
-template <typename KT>
 struct Stage {
     uint8_t* kb;
     uint8_t* vb;
     int* ccell;
     int* cvis;
     int* cfresh;
-    float* ksc;
-    float* vsc;
 };
 
 }  // namespace
 
-// Two warp groups: group g takes cells [32 g, 32 g + 32) of every pass of 64 (one cell per lane
-// for the scores), warp g * 4 + h holds query head h of the KV head's group. Passes are double
-// buffered: the rows of pass i + 1 are in flight while pass i is computed.
-template <int HD, typename KT>
+// F32 caches, on CUDA cores. Two warp groups: group g takes cells [32 g, 32 g + 32) of every
+// pass of 64 (one cell per lane for the scores), warp g * 4 + h holds query head h of the KV
+// head's group. Passes are double buffered: the rows of pass i + 1 are in flight while pass i is
+// computed.
+template <int HD>
 __global__ void __launch_bounds__(kThreads)
 attn_decode_kernel(AttnArgs a, float scale_log2) {
-    using SM = DecSmem<HD, KT>;
-    constexpr int RB = SM::RB, RS = SM::RS, VPR = RB / 16, DPL = HD / 32, NB = SM::NB;
-    constexpr bool Q8 = SM::Q8;
+    using SM = DecSmem<HD>;
+    constexpr int RB = SM::RB, RS = SM::RS, VPR = RB / 16, DPL = HD / 32;
     extern __shared__ __align__(16) uint8_t sm[];
     auto stage_of = [&](int s) {
         uint8_t* b = sm + (size_t)s * SM::stage;
-        Stage<KT> S;
+        Stage S;
         S.kb = b;
         S.vb = b + kCH * RS;
         S.ccell = reinterpret_cast<int*>(b + SM::rows);
         S.cvis = S.ccell + kCH;
         S.cfresh = S.cvis + kCH;
-        S.ksc = reinterpret_cast<float*>(S.cfresh + kCH);
-        S.vsc = S.ksc + kCH * NB;
         return S;
     };
     float* qs = reinterpret_cast<float*>(sm + 2 * SM::stage);          // [kGQ][HD]
@@ -138,20 +122,10 @@ attn_decode_kernel(AttnArgs a, float scale_log2) {
     const int npass = c1 > c0 ? (c1 - c0 + kCH - 1) / kCH : 1;  // at least one: the wait is in it
     const uint8_t* K = static_cast<const uint8_t*>(a.kc) + (int64_t)kvh * a.n_ctx * RB;
     const uint8_t* V = static_cast<const uint8_t*>(a.vc) + (int64_t)kvh * a.n_ctx * RB;
-    const __half* KS = q8_scales(a.kc, a, kvh);
-    const __half* VS = q8_scales(a.vc, a, kvh);
-    auto load_scales = [&](const Stage<KT>& S, int c, int cell) {
-#pragma unroll
-        for (int b = 0; b < NB; ++b) {
-            S.ksc[c * NB + b] = ld_scale(KS + (int64_t)cell * NB + b);
-            S.vsc[c * NB + b] = ld_scale(VS + (int64_t)cell * NB + b);
-        }
-    };
-    // The list entry (cell, position; Q8_0 after the wait: its scales) of the next pass to set up
-    // is fetched into registers one pass ahead, so setting up a stage waits on no global load.
+    // The list entry (cell, position) of the next pass to set up is fetched into registers one
+    // pass ahead, so setting up a stage waits on no global load.
     int pf_cell = -1, pf_pos = 0;
-    float pf_ks[NB], pf_vs[NB];
-    auto fetch = [&](int i, bool with_scales) {
+    auto fetch = [&](int i) {
         if (threadIdx.x < kCH) {
             const int ci = c0 + i * kCH + threadIdx.x;
             pf_cell = -1;
@@ -160,19 +134,9 @@ attn_decode_kernel(AttnArgs a, float scale_log2) {
                 pf_cell = a.list_cells[base + ci];
                 pf_pos = a.list_pos[base + ci];
             }
-            if constexpr (Q8) {
-                if (with_scales && pf_cell >= 0 && pf_cell < a.n_ctx && pf_pos <= tpos) {
-#pragma unroll
-                    for (int b = 0; b < NB; ++b) {
-                        pf_ks[b] = ld_scale(KS + (int64_t)pf_cell * NB + b);
-                        pf_vs[b] = ld_scale(VS + (int64_t)pf_cell * NB + b);
-                    }
-                }
-            }
         }
     };
-    // stage S takes the fetched entry (threads < kCH); before the wait, fresh cells' scales wait
-    auto setup = [&](const Stage<KT>& S, bool pre_wait) {
+    auto setup = [&](const Stage& S) {
         if (threadIdx.x < kCH) {
             int cell = -1, vis = 0, fresh = 0;
             if (pf_cell >= 0 && pf_cell < a.n_ctx) {
@@ -183,22 +147,9 @@ attn_decode_kernel(AttnArgs a, float scale_log2) {
             S.ccell[threadIdx.x] = cell;
             S.cvis[threadIdx.x] = vis && cell >= 0;
             S.cfresh[threadIdx.x] = fresh;
-            if constexpr (Q8) {
-                if (vis && cell >= 0) {
-                    if (pre_wait) {
-                        if (!fresh) load_scales(S, threadIdx.x, cell);
-                    } else {
-#pragma unroll
-                        for (int b = 0; b < NB; ++b) {
-                            S.ksc[threadIdx.x * NB + b] = pf_ks[b];
-                            S.vsc[threadIdx.x * NB + b] = pf_vs[b];
-                        }
-                    }
-                }
-            }
         }
     };
-    auto issue = [&](const Stage<KT>& S, bool pre_wait) {
+    auto issue = [&](const Stage& S, bool pre_wait) {
         for (int v = threadIdx.x; v < kCH * VPR; v += kThreads) {
             const int c = v / VPR, j = v % VPR;
             if (!S.cvis[c] || (pre_wait && S.cfresh[c])) continue;
@@ -211,13 +162,13 @@ attn_decode_kernel(AttnArgs a, float scale_log2) {
 
     // pass 0: rows of earlier steps staged now, possibly before the previous kernel has ended
     {
-        const Stage<KT> S0 = stage_of(0);
-        fetch(0, false);
-        setup(S0, true);
+        const Stage S0 = stage_of(0);
+        fetch(0);
+        setup(S0);
         __syncthreads();
         issue(S0, true);
         asm volatile("griddepcontrol.wait;" ::: "memory");
-        if (npass > 1) fetch(1, true);
+        if (npass > 1) fetch(1);
         for (int i = threadIdx.x; i < kGQ * HD; i += kThreads)
             qs[i] = a.q[(int64_t)t * a.ldq + (kvh * kGQ + i / HD) * HD + i % HD] * scale_log2;
         // rows written by this step's projection kernel: only now
@@ -228,10 +179,6 @@ attn_decode_kernel(AttnArgs a, float scale_log2) {
             *reinterpret_cast<uint4*>(S0.kb + c * RS + j * 16) = __ldcg(reinterpret_cast<const uint4*>(K + src));
             *reinterpret_cast<uint4*>(S0.vb + c * RS + j * 16) = __ldcg(reinterpret_cast<const uint4*>(V + src));
         }
-        if constexpr (Q8) {
-            if (threadIdx.x < kCH && S0.cvis[threadIdx.x] && S0.cfresh[threadIdx.x])
-                load_scales(S0, threadIdx.x, S0.ccell[threadIdx.x]);
-        }
     }
 
     float m = -INFINITY, l = 0.f, o[DPL];
@@ -239,12 +186,12 @@ attn_decode_kernel(AttnArgs a, float scale_log2) {
     for (int e = 0; e < DPL; ++e) o[e] = 0.f;
     const float* q = qs + hq * HD;
     for (int i = 0; i < npass; ++i) {
-        const Stage<KT> S = stage_of(i & 1);
+        const Stage S = stage_of(i & 1);
         if (i + 1 < npass) {
             // the other stage was last read by pass i - 1, which ended at the barrier below
-            const Stage<KT> N = stage_of((i + 1) & 1);
-            setup(N, false);
-            if (i + 2 < npass) fetch(i + 2, true);
+            const Stage N = stage_of((i + 1) & 1);
+            setup(N);
+            if (i + 2 < npass) fetch(i + 2);
             __syncthreads();
             issue(N, false);
             asm volatile("cp.async.wait_group 1;" ::: "memory");
@@ -258,44 +205,16 @@ attn_decode_kernel(AttnArgs a, float scale_log2) {
         float s = -INFINITY;
         if (S.cvis[c]) {
             const uint8_t* kr = S.kb + c * RS;
-            if constexpr (Q8) {
-                float acc = 0.f;
-#pragma unroll
-                for (int b = 0; b < NB; ++b) {
-                    float p0 = 0.f, p1 = 0.f;
-#pragma unroll
-                    for (int jj = 0; jj < 2; ++jj) {
-                        const int j = 2 * b + jj;
-                        const uint4 kv = *reinterpret_cast<const uint4*>(kr + j * 16);
-                        float ke[16];
-                        dev::unpack_q8_raw(kv, ke);
-#pragma unroll
-                        for (int e = 0; e < 16; e += 4) {
-                            const float4 qv = *reinterpret_cast<const float4*>(q + j * 16 + e);
-                            p0 = fmaf(qv.x, ke[e], p0);
-                            p1 = fmaf(qv.y, ke[e + 1], p1);
-                            p0 = fmaf(qv.z, ke[e + 2], p0);
-                            p1 = fmaf(qv.w, ke[e + 3], p1);
-                        }
-                    }
-                    acc = fmaf(S.ksc[c * NB + b], p0 + p1, acc);
-                }
-                s = acc;
-            } else {
+            {
                 float a0 = 0.f, a1 = 0.f;
 #pragma unroll
                 for (int j = 0; j < VPR; ++j) {
-                    const uint4 kv = *reinterpret_cast<const uint4*>(kr + j * 16);
-                    const KT* ke = reinterpret_cast<const KT*>(&kv);
-                    constexpr int EPV = 16 / (int)sizeof(KT);
-#pragma unroll
-                    for (int e = 0; e < EPV; e += 4) {
-                        const float4 qv = *reinterpret_cast<const float4*>(q + j * EPV + e);   // broadcast
-                        a0 = fmaf(qv.x, kvf<KT>(ke[e]), a0);
-                        a1 = fmaf(qv.y, kvf<KT>(ke[e + 1]), a1);
-                        a0 = fmaf(qv.z, kvf<KT>(ke[e + 2]), a0);
-                        a1 = fmaf(qv.w, kvf<KT>(ke[e + 3]), a1);
-                    }
+                    const float4 kv = *reinterpret_cast<const float4*>(kr + j * 16);
+                    const float4 qv = *reinterpret_cast<const float4*>(q + j * 4);   // broadcast
+                    a0 = fmaf(qv.x, kv.x, a0);
+                    a1 = fmaf(qv.y, kv.y, a1);
+                    a0 = fmaf(qv.z, kv.z, a0);
+                    a1 = fmaf(qv.w, kv.w, a1);
                 }
                 s = a0 + a1;
             }
@@ -319,21 +238,9 @@ attn_decode_kernel(AttnArgs a, float scale_log2) {
             const float pc = __shfl_sync(0xffffffffu, p, k);
             if (pc == 0.f) continue;
             const int c2 = grp * kCG + k;
-            const KT* vr = reinterpret_cast<const KT*>(S.vb + c2 * RS) + lane * DPL;
-            if constexpr (Q8 && DPL % 4 == 0) {
-                const float pd = pc * S.vsc[c2 * NB + lane * DPL / 32];
+            const float* vr = reinterpret_cast<const float*>(S.vb + c2 * RS) + lane * DPL;
 #pragma unroll
-                for (int e4 = 0; e4 < DPL; e4 += 4) {
-                    float vv[4];
-                    dev::unpack_q8x4_raw(*reinterpret_cast<const uint32_t*>(vr + e4), vv);
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) o[e4 + e] = fmaf(pd, vv[e], o[e4 + e]);
-                }
-            } else {
-                const float pd = Q8 ? pc * S.vsc[c2 * NB + lane * DPL / 32] : pc;
-#pragma unroll
-                for (int e = 0; e < DPL; ++e) o[e] = fmaf(pd, kvf<KT>(vr[e]), o[e]);
-            }
+            for (int e = 0; e < DPL; ++e) o[e] = fmaf(pc, vr[e], o[e]);
         }
         __syncthreads();                                        // stage S free for pass i + 2
     }
@@ -788,11 +695,11 @@ bool launch_dec_mma(const AttnArgs& a, cudaStream_t st) {
     return cudaLaunchKernelEx(&cfg, k, a, scale_log2) == cudaSuccess;
 }
 
-template <int HD, typename KT>
+template <int HD>
 bool launch_dec(const AttnArgs& a, cudaStream_t st) {
     const float scale_log2 = (float)(1.4426950408889634 / sqrt((double)HD));
-    constexpr size_t smem = DecSmem<HD, KT>::bytes;
-    auto k = attn_decode_kernel<HD, KT>;
+    constexpr size_t smem = DecSmem<HD>::bytes;
+    auto k = attn_decode_kernel<HD>;
     static bool attr = false;
     if (!attr) {
         if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess ||
@@ -839,10 +746,10 @@ bool launch_attention_decode(const AttnArgs& a, cudaStream_t st) {
         }
         return false;
     }
-    switch (a.hd) {
-        case 32: return launch_dec<32, float>(a, st);
-        case 64: return launch_dec<64, float>(a, st);
-        case 128: return launch_dec<128, float>(a, st);
+    switch (a.hd) {                                            // F32: CUDA cores
+        case 32: return launch_dec<32>(a, st);
+        case 64: return launch_dec<64>(a, st);
+        case 128: return launch_dec<128>(a, st);
     }
     return false;
 }
