@@ -30,6 +30,22 @@ __device__ __forceinline__ void sub2(float& a0, float& a1, float b) {
         : "+f"(a0), "+f"(a1) : "f"(b));
 }
 
+// 8 int8 quants -> floats (see unpack_q8_raw).
+__device__ __forceinline__ void unpack_q8x8_raw(const uint2 v, float* w) {
+    const uint32_t u[2] = {v.x ^ 0x80808080u, v.y ^ 0x80808080u};
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+#pragma unroll
+        for (int b = 0; b < 4; b += 2) {
+            float f0 = __int_as_float((int)__byte_perm(u[i], 0x4B000000u, 0x7540u + b));
+            float f1 = __int_as_float((int)__byte_perm(u[i], 0x4B000000u, 0x7540u + b + 1));
+            sub2(f0, f1, 8388736.0f);
+            w[4 * i + b] = f0;
+            w[4 * i + b + 1] = f1;
+        }
+    }
+}
+
 // 16 int8 quants -> their values as floats without an int-to-float conversion: each byte, biased
 // by 128, becomes the low mantissa byte of 2^23 (exponent byte 0x4B), and 2^23 + 128 is
 // subtracted exactly.

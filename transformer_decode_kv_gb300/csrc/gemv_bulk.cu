@@ -38,6 +38,13 @@ constexpr int kMaxStages = 8;
 constexpr uint32_t kStageBytes = 16384;     // stage size of the general mapping
 constexpr uint32_t kMaxStageBytes = 32768;
 constexpr uint32_t kSlice = 512;                  // bytes per warp pass (16 per lane)
+// Column-stationary Q8_0 rows use 8-byte lane chunks (256-byte slices): 8 quants per lane keep the
+// activations of a 14336-wide row (7 slices per warp) in registers, and a chunk stays inside one
+// 32-value block.
+template <int WT> struct ColsGeom {
+    static constexpr int CH = WT == W_Q8_0 ? 8 : 16;      // bytes per lane and slice
+    static constexpr int SL = 32 * CH;                      // slice bytes
+};
 constexpr uint32_t kColsStage = 24576;            // column-stationary stage: whole rows up to 24 KB
 
 __device__ __forceinline__ void consumer_sync() {
@@ -50,7 +57,7 @@ struct Range { int64_t row0, nrows; int local0; };
 // without spilling: two of this kernel and one of the next, which programmatic dependent launch
 // starts early to prefetch its weights.
 template <int WT, int TM, int EPI, bool NORM, int SPW>
-__global__ void __launch_bounds__(kThreads, TM == 1 && SPW > 0 && SPW * Vec<WT>::N <= 32 ? 3
+__global__ void __launch_bounds__(kThreads, TM == 1 && SPW > 0 && SPW * ColsGeom<WT>::CH / Vec<WT>::ES <= 32 ? 3
                                             : TM <= 2 ? 2 : 1)
 gemv_bulk_kernel(const GemvArgs a) {
     constexpr bool COLS = SPW > 0;
@@ -146,16 +153,18 @@ gemv_bulk_kernel(const GemvArgs a) {
     // column-stationary mapping: each warp loads only its own columns of the (single) activation
     // row into registers; the RMS is reduced across the warps
     constexpr int kSpw = SPW > 0 ? SPW : 1;
-    float xr[kSpw][VN];
+    constexpr int CH = ColsGeom<WT>::CH, SL = ColsGeom<WT>::SL;
+    constexpr int VC = COLS ? CH / ES : VN;               // values per lane chunk
+    float xr[kSpw][VC];
     if constexpr (COLS) {
         const int src = a.x_rows ? a.x_rows[0] : 0;
         const float* xg = a.x + (int64_t)src * a.ldx;
         float ss = 0.f;
 #pragma unroll
         for (int k2 = 0; k2 < kSpw; ++k2) {
-            const int col = (warp * kSpw + k2) * (kSlice / ES) + lane * VN;
+            const int col = (warp * kSpw + k2) * (SL / ES) + lane * VC;
 #pragma unroll
-            for (int e = 0; e < VN; e += 4) {
+            for (int e = 0; e < VC; e += 4) {
                 const float4 v = *reinterpret_cast<const float4*>(xg + col + e);
                 xr[k2][e] = v.x; xr[k2][e + 1] = v.y; xr[k2][e + 2] = v.z; xr[k2][e + 3] = v.w;
                 ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
@@ -171,9 +180,9 @@ gemv_bulk_kernel(const GemvArgs a) {
             const float sc = 1.0f / sqrtf(s / (float)K + a.eps);
 #pragma unroll
             for (int k2 = 0; k2 < kSpw; ++k2) {
-                const int col = (warp * kSpw + k2) * (kSlice / ES) + lane * VN;
+                const int col = (warp * kSpw + k2) * (SL / ES) + lane * VC;
 #pragma unroll
-                for (int e = 0; e < VN; e += 4) {
+                for (int e = 0; e < VC; e += 4) {
                     const float4 g = *reinterpret_cast<const float4*>(a.g + col + e);
                     xr[k2][e] *= sc * g.x; xr[k2][e + 1] *= sc * g.y;
                     xr[k2][e + 2] *= sc * g.z; xr[k2][e + 3] *= sc * g.w;
@@ -244,13 +253,13 @@ gemv_bulk_kernel(const GemvArgs a) {
                     break;
                 }
                 const int nr = (int)(nrows - row0 < rps ? nrows - row0 : rps);
-                const uint8_t* st0 = stages + (size_t)s * SB + (warp * spw) * kSlice + lane * 16;
+                const uint8_t* st0 = stages + (size_t)s * SB + (warp * spw) * SL + lane * CH;
                 const __half* ssc = reinterpret_cast<const __half*>(sstages + (size_t)s * (SB / 16));
                 // all rows of the stage at once (one token in this mapping): two independent
                 // accumulators per row, the row reductions interleaved, then lane i adds row i's
                 // sum to the shared total. A stage holds kColsStage bytes of whole rows.
-                constexpr int RPS = (int)(kColsStage / (SPW * kConsumerWarps * kSlice)) > 0
-                                        ? (int)(kColsStage / (SPW * kConsumerWarps * kSlice)) : 1;
+                constexpr int RPS = (int)(kColsStage / (SPW * kConsumerWarps * SL)) > 0
+                                        ? (int)(kColsStage / (SPW * kConsumerWarps * SL)) : 1;
                 static_assert(TM == 1, "column-stationary mapping serves one token");
                 float pa[RPS], pb[RPS];
 #pragma unroll
@@ -260,20 +269,22 @@ gemv_bulk_kernel(const GemvArgs a) {
                     if (i < nr) {
 #pragma unroll
                         for (int k2 = 0; k2 < kMaxSpw; ++k2) {
-                            const uint4 wv = *reinterpret_cast<const uint4*>(st0 + (size_t)i * row_bytes + k2 * kSlice);
-                            float w[VN];
                             if constexpr (Q8) {
-                                // a lane's 16 quants share one block scale: sum, then scale once
+                                // a lane's 8 quants share one block scale: sum, then scale once
+                                const uint2 wv = *reinterpret_cast<const uint2*>(st0 + (size_t)i * row_bytes + k2 * SL);
                                 const float d = __half2float(
-                                    ssc[((size_t)i * row_bytes + (warp * spw + k2) * kSlice + lane * 16) / 32]);
-                                unpack_q8_raw(wv, w);
+                                    ssc[((size_t)i * row_bytes + (warp * spw + k2) * SL + lane * CH) / 32]);
+                                float w[8];
+                                unpack_q8x8_raw(wv, w);
                                 float la = 0.f, lb = 0.f;
 #pragma unroll
-                                for (int e = 0; e < VN; e += 2)
+                                for (int e = 0; e < 8; e += 2)
                                     fma2(la, lb, w[e], w[e + 1], xr[k2][e], xr[k2][e + 1]);
                                 pa[i] = fmaf(d, la, pa[i]);
                                 pb[i] = fmaf(d, lb, pb[i]);
                             } else {
+                                const uint4 wv = *reinterpret_cast<const uint4*>(st0 + (size_t)i * row_bytes + k2 * SL);
+                                float w[VN];
                                 unpack16<WT>(wv, 0.f, w);
 #pragma unroll
                                 for (int e = 0; e < VN; e += 2)
@@ -519,8 +530,9 @@ static int plan_grid(int wt, const GemvArgs& a, int epi, int n_sm, size_t* smem,
     const int64_t units = (epi == GEPI_SWIGLU ? a.F : a.M) / gran;
     if (units <= 0) return 0;
     // column-stationary mapping: whole rows per stage, each warp owns a fixed eighth of a row
-    const int64_t spr = rb / kSlice;
-    const int vn = wt == W_F32 ? 4 : wt == W_Q8_0 ? 16 : 8;
+    const int64_t cols_slice = wt == W_Q8_0 ? 256 : kSlice;      // ColsGeom<WT>::SL
+    const int64_t spr = rb / cols_slice;
+    const int vn = wt == W_F32 ? 4 : 8;                           // values per lane chunk
     const int64_t spw = spr % kConsumerWarps == 0 ? spr / kConsumerWarps : 0;
     const bool cols = tm == 1 && (spw == 1 || spw == 2 || spw == 4 || spw == 7) && spw * vn <= 64 &&
                       rb <= kMaxStageBytes;
@@ -566,7 +578,7 @@ bool launch_gemv_bulk(int wt, GemvArgs a, int epi, bool norm, int n_sm, cudaStre
     a.rows_cap = cap;
     a.n_stages = ns;
     a.stage_bytes = sb;
-    const int spw = sb > 0 ? (int)(wrow_bytes(wt, a.K) / kSlice / kConsumerWarps) : 0;
+    const int spw = sb > 0 ? (int)(wrow_bytes(wt, a.K) / (wt == W_Q8_0 ? 256 : kSlice) / kConsumerWarps) : 0;
     // the (epilogue, norm) pairs the decode path uses
     switch (epi) {
         case GEPI_STORE: if (!norm) return launch_wt<GEPI_STORE, false>(wt, a, spw, grid, smem, st, pdl); break;
