@@ -1,10 +1,11 @@
-"""GPU parity of Q8_0 prefill on the tensor cores (each Q8_0 weight d*q as two bf16 terms, hi + lo,
-in the token-major tcgen05 GEMM) on a 2-layer model of the Llama-3-8B layer shape with Q8_0
-linear weights and F32 embeddings/norms (the 8k workload's types), through the C ABI.
+"""GPU parity of Q8_0 prefill on the tensor cores (each Q8_0 weight d*q as two f16 terms, hi + lo,
+which hold it exactly, in the token-major tcgen05 GEMM; activations one f16 term) on a 2-layer
+model of the Llama-3-8B layer shape with Q8_0 linear weights and F32 embeddings/norms (the 8k
+workload's types), through the C ABI.
 
 A 512-token prompt (one ubatch: every GEMM on the tensor cores) then greedy steps (Q8_0 GEMVs),
-against the oracle: every flagged logits row within the 2e-2 bar (expected ~1e-4: the terms hold
-the weights to 16 bits and the activations enter as two bf16 terms too)."""
+against the oracle: every flagged logits row within the 2e-2 bar (expected ~1e-3: the f16
+activations carry 11 significant bits)."""
 import numpy as np
 import pytest
 
@@ -39,7 +40,7 @@ def test_q8_0_prefill_on_tensor_cores_matches_oracle():
         errs.append(G.rel_err(ctx.get_logits_ith(i), ora.get_logits_ith(i)))
     print("Q8_0 prefill rows:", errs)
     assert max(errs) <= TOL, errs
-    assert max(errs) <= 1e-3, errs              # the two-term weights keep it near float32
+    assert max(errs) <= 5e-3, errs              # well inside the bar: exact weights, f16 activations
     rep = G.greedy_compare(ctx, ora, 1, [511], 4, TOL, {})
     print("Q8_0 steps:", rep)
     ctx.free()

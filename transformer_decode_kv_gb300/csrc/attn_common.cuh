@@ -59,7 +59,9 @@ __device__ __forceinline__ const __half* q8_scales(const void* layer, const Attn
 }
 
 __device__ __forceinline__ void store_out(const AttnArgs& a, int64_t oi, float v) {
-    if (a.out_b) {
+    if (a.out_b && a.out_f16) {
+        static_cast<__half*>(a.out_b)[oi] = __float2half_rn(v);
+    } else if (a.out_b) {
         const __nv_bfloat16 hi = __float2bfloat16_rn(v);
         static_cast<__nv_bfloat16*>(a.out_b)[oi] = hi;
         if (a.out_b_lo)

@@ -113,6 +113,10 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int m, int n) {
     return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) |
            ((uint32_t)(m >> 4) << 24);
 }
+// the same with f16 A and B (kind::f16 takes one type for both operands)
+__host__ __device__ constexpr uint32_t idesc_f16(int m, int n) {
+    return (1u << 4) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
+}
 
 __device__ __forceinline__ void umma_bf16(uint32_t dtmem, uint64_t a, uint64_t b, uint32_t idesc,
                                           uint32_t accumulate) {
@@ -331,21 +335,31 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 // range is split over blockIdx.z (the output then starts zeroed for a store). With a second weight
 // map (tmWlo) the weights are two bf16 terms too (a Q8_0 weight d*q as hi + lo): the K loop runs
 // over both weight terms, each against both activation terms.
+//
+// A2 = false: one f16 activation term and f16 weights (a BF16 weight converted exactly, or a
+// Q8_0 weight as two f16 terms that hold d*q exactly): one MMA per k-step and weight term, and
+// SwiGLU writes a single f16 output.
 constexpr int kTnRows = 128;                     // tokens per tile (MMA M)
 constexpr int kTnN = 256;                        // 128 gate + 128 up rows (MMA N)
 constexpr uint32_t kTnA = kTnRows * kBK * 2;     // 16 KB per activation term
 constexpr uint32_t kTnB = kTnN * kBK * 2;        // 32 KB
-constexpr uint32_t kTnStage = 2 * kTnA + kTnB;   // 64 KB
-constexpr int kTnStages = (int)(196608u / kTnStage);
-constexpr size_t kTnSmem = 1024 + (size_t)kTnStages * kTnStage + 256;
+template <bool A2>
+struct TnCfg {
+    static constexpr uint32_t kStage = (A2 ? 2 : 1) * kTnA + kTnB;    // 64 KB or 48 KB
+    static constexpr int kStages = (int)(196608u / kStage);             // 3 or 4
+    static constexpr size_t kSmem = 1024 + (size_t)kStages * kStage + 256;
+};
 
-template <int EPI>
+template <int EPI, bool A2>
 __global__ void __launch_bounds__(128, 1)
 gemm_tn_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmXlo,
                const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmWlo,
                int planes, int K, int T, int M, int F,
                void* __restrict__ Y, void* __restrict__ Y2, int ldy, uint32_t* __restrict__ err) {
-    constexpr int S = kTnStages;
+    using C = TnCfg<A2>;
+    constexpr int S = C::kStages;
+    constexpr uint32_t kTnStage = C::kStage;
+    constexpr uint32_t kBOff = (A2 ? 2 : 1) * kTnA;              // weights after the activation terms
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * kTnStage);
@@ -373,7 +387,7 @@ gemm_tn_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmX)) : "memory");
-        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmXlo)) : "memory");
+        if (A2) asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmXlo)) : "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmW)) : "memory");
         if (planes > 1)
             asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmWlo)) : "memory");
@@ -402,16 +416,16 @@ gemm_tn_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
             const int kx = (kb0 + kb % nkp) * kBK;
             const CUtensorMap* wm = kb < nkp ? &tmW : &tmWlo;
             tma_load_2d(st, &tmX, &full[s], kx, t0);
-            tma_load_2d(st + kTnA, &tmXlo, &full[s], kx, t0);
-            tma_load_2d(st + 2 * kTnA, wm, &full[s], kx, f0);
-            tma_load_2d(st + 2 * kTnA + kTnB / 2, wm, &full[s], kx, w2);
+            if (A2) tma_load_2d(st + kTnA, &tmXlo, &full[s], kx, t0);
+            tma_load_2d(st + kBOff, wm, &full[s], kx, f0);
+            tma_load_2d(st + kBOff + kTnB / 2, wm, &full[s], kx, w2);
             issued = kb + 1;
         }
         for (int kb = (issued > S ? issued - S : 0); kb < issued; ++kb)
             mbar_wait(&full[kb % S], (uint32_t)(kb / S) & 1u);
     } else if (threadIdx.x == 32) {
-        // ---- MMA issuer: D += X_hi W^T + X_lo W^T
-        constexpr uint32_t idesc = idesc_bf16(kTnRows, kTnN);
+        // ---- MMA issuer: D += X_hi W^T + X_lo W^T (A2), or D += X W^T
+        constexpr uint32_t idesc = A2 ? idesc_bf16(kTnRows, kTnN) : idesc_f16(kTnRows, kTnN);
         bool ok = true;
         for (int kb = 0; kb < nk; ++kb) {
             const int s = kb % S;
@@ -420,14 +434,16 @@ gemm_tn_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
             tc_fence_after();
             const uint8_t* st = smem + (size_t)s * kTnStage;
             const uint64_t ah = sdesc_sw128(smem_u32(st));
-            const uint64_t al = sdesc_sw128(smem_u32(st + kTnA));
-            const uint64_t bd = sdesc_sw128(smem_u32(st + 2 * kTnA));
+            const uint64_t bd = sdesc_sw128(smem_u32(st + kBOff));
 #pragma unroll
             for (int kk = 0; kk < kBK / 16; ++kk)
                 umma_bf16(tmem, ah + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2), idesc, (kb | kk) != 0 ? 1u : 0u);
+            if (A2) {
+                const uint64_t al = sdesc_sw128(smem_u32(st + kTnA));
 #pragma unroll
-            for (int kk = 0; kk < kBK / 16; ++kk)
-                umma_bf16(tmem, al + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2), idesc, 1u);
+                for (int kk = 0; kk < kBK / 16; ++kk)
+                    umma_bf16(tmem, al + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2), idesc, 1u);
+            }
             umma_commit(&empty[s]);
         }
         if (!ok) { atomicOr(err, ERR_TIMEOUT); *(volatile int*)abort_flag = 1; }
@@ -442,7 +458,26 @@ gemm_tn_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
     const bool live = have && !*(volatile int*)abort_flag && nk > 0;
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
     const int t = t0 + warp * 32 + lane;
-    if (EPI == GEMM_EPI_SWIGLU) {
+    if (EPI == GEMM_EPI_SWIGLU && !A2) {
+#pragma unroll 1
+        for (int j0 = 0; j0 < kTnN / 2; j0 += 16) {
+            float g[16], u[16];
+            tmem_ld16(tmem + lane_base + (uint32_t)j0, g);
+            tmem_ld16(tmem + lane_base + (uint32_t)(kTnN / 2 + j0), u);
+            if (!live || t >= T) continue;
+            uint32_t h[8];
+#pragma unroll
+            for (int j = 0; j < 16; j += 2) {
+                const float o0 = g[j] / (1.0f + expf(-g[j])) * u[j];
+                const float o1 = g[j + 1] / (1.0f + expf(-g[j + 1])) * u[j + 1];
+                const __half2 hv = __floats2half2_rn(o0, o1);
+                h[j / 2] = *reinterpret_cast<const uint32_t*>(&hv);
+            }
+            uint4* dh = reinterpret_cast<uint4*>(static_cast<__half*>(Y) + (int64_t)t * ldy + f0 + j0);
+            dh[0] = make_uint4(h[0], h[1], h[2], h[3]);
+            dh[1] = make_uint4(h[4], h[5], h[6], h[7]);
+        }
+    } else if (EPI == GEMM_EPI_SWIGLU) {
         __nv_bfloat16* Yb = static_cast<__nv_bfloat16*>(Y);
         __nv_bfloat16* Yb2 = static_cast<__nv_bfloat16*>(Y2);
 #pragma unroll 1
@@ -547,7 +582,7 @@ bool launch_epi(const CUtensorMap& wmap, const CUtensorMap& xmap, const CUtensor
 
 }  // namespace
 
-bool tc_make_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int box_rows) {
+bool tc_make_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int box_rows, bool f16) {
     auto fn = encode_fn();
     if (!fn) return false;
     if (cols % kBK != 0 || (reinterpret_cast<uintptr_t>(base) & 15) != 0) return false;
@@ -555,7 +590,8 @@ bool tc_make_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols,
     const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
     const cuuint32_t box[2] = {(cuuint32_t)kBK, (cuuint32_t)box_rows};
     const cuuint32_t estr[2] = {1, 1};
-    const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
+    const CUresult r = fn(map, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                          const_cast<void*>(base), dims,
                           strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -567,29 +603,32 @@ int tc_token_tile(int T) { return T > 128 ? 256 : 128; }
 bool tc_swiglu_tn_ok(int64_t K, int64_t F) { return K % kBK == 0 && K >= kBK && F % (kTnN / 2) == 0 && F > 0; }
 bool tc_tn_ok(int64_t M, int64_t K) { return K % kBK == 0 && K >= kBK && M % kTnN == 0 && M > 0; }
 
-template <int EPI>
-bool launch_tn(const CUtensorMap& xmap, const CUtensorMap& xmap_lo, const CUtensorMap& wmap,
+template <int EPI, bool A2>
+bool launch_tn(const CUtensorMap& xmap, const CUtensorMap* xmap_lo, const CUtensorMap& wmap,
                const CUtensorMap* wmap_lo, int K, int T, int M, int F, void* Y, void* Y2, int ldy,
                int splits, uint32_t* err, cudaStream_t st) {
-    auto k = gemm_tn_kernel<EPI>;
+    using C = TnCfg<A2>;
+    auto k = gemm_tn_kernel<EPI, A2>;
     static bool attr = false;
     if (!attr) {
-        if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTnSmem) != cudaSuccess)
+        if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem) != cudaSuccess)
             return false;
         attr = true;
     }
     const int ntile = EPI == GEMM_EPI_SWIGLU ? F / (kTnN / 2) : M / kTnN;
     dim3 grid((T + kTnRows - 1) / kTnRows, ntile, splits);
-    k<<<grid, 128, kTnSmem, st>>>(xmap, xmap_lo, wmap, wmap_lo ? *wmap_lo : wmap, wmap_lo ? 2 : 1, K, T,
-                                  M, F, Y, Y2, ldy, err);
+    k<<<grid, 128, C::kSmem, st>>>(xmap, xmap_lo ? *xmap_lo : xmap, wmap, wmap_lo ? *wmap_lo : wmap,
+                                   wmap_lo ? 2 : 1, K, T, M, F, Y, Y2, ldy, err);
     return cudaGetLastError() == cudaSuccess;
 }
 
-bool launch_gemm_swiglu_tn(const CUtensorMap& xmap, const CUtensorMap& xmap_lo, const CUtensorMap& wmap,
+bool launch_gemm_swiglu_tn(const CUtensorMap& xmap, const CUtensorMap* xmap_lo, const CUtensorMap& wmap,
                            int K, int T, int F, void* Y, void* Y2, int ldy, uint32_t* err, cudaStream_t st,
                            const CUtensorMap* wmap_lo) {
     if (T <= 0) return true;
-    return launch_tn<GEMM_EPI_SWIGLU>(xmap, xmap_lo, wmap, wmap_lo, K, T, 0, F, Y, Y2, ldy, 1, err, st);
+    if (xmap_lo)
+        return launch_tn<GEMM_EPI_SWIGLU, true>(xmap, xmap_lo, wmap, wmap_lo, K, T, 0, F, Y, Y2, ldy, 1, err, st);
+    return launch_tn<GEMM_EPI_SWIGLU, false>(xmap, nullptr, wmap, wmap_lo, K, T, 0, F, Y, nullptr, ldy, 1, err, st);
 }
 
 int tc_tn_splits(int64_t M, int64_t K, int T, int n_sm) {
@@ -600,14 +639,20 @@ int tc_tn_splits(int64_t M, int64_t K, int T, int n_sm) {
     return s;
 }
 
-bool launch_gemm_tn(const CUtensorMap& xmap, const CUtensorMap& xmap_lo, const CUtensorMap& wmap, int epi,
+bool launch_gemm_tn(const CUtensorMap& xmap, const CUtensorMap* xmap_lo, const CUtensorMap& wmap, int epi,
                     int K, int M, int T, float* Y, int ldy, int splits, uint32_t* err, cudaStream_t st,
                     const CUtensorMap* wmap_lo) {
     if (T <= 0) return true;
     if (epi == GEMM_EPI_STORE)
-        return launch_tn<GEMM_EPI_STORE>(xmap, xmap_lo, wmap, wmap_lo, K, T, M, 0, Y, nullptr, ldy, splits, err, st);
+        return xmap_lo ? launch_tn<GEMM_EPI_STORE, true>(xmap, xmap_lo, wmap, wmap_lo, K, T, M, 0, Y, nullptr, ldy,
+                                                         splits, err, st)
+                       : launch_tn<GEMM_EPI_STORE, false>(xmap, nullptr, wmap, wmap_lo, K, T, M, 0, Y, nullptr, ldy,
+                                                          splits, err, st);
     if (epi == GEMM_EPI_ADD)
-        return launch_tn<GEMM_EPI_ADD>(xmap, xmap_lo, wmap, wmap_lo, K, T, M, 0, Y, nullptr, ldy, splits, err, st);
+        return xmap_lo ? launch_tn<GEMM_EPI_ADD, true>(xmap, xmap_lo, wmap, wmap_lo, K, T, M, 0, Y, nullptr, ldy,
+                                                       splits, err, st)
+                       : launch_tn<GEMM_EPI_ADD, false>(xmap, nullptr, wmap, wmap_lo, K, T, M, 0, Y, nullptr, ldy,
+                                                        splits, err, st);
     return false;
 }
 

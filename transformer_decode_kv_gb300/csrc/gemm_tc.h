@@ -14,9 +14,10 @@ enum GemmEpi : int32_t {
     GEMM_EPI_SWIGLU = 2,   // Y[t][j] = silu(gate_j) * up_j (bf16); W rows [0,F) gate, [F,2F) up
 };
 
-// TMA map of a row-major bf16 matrix [rows][cols] (cols % 64 == 0, base 16-byte aligned), loaded
-// in boxes of 64 columns x box_rows rows with the 128-byte swizzle.
-bool tc_make_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int box_rows);
+// TMA map of a row-major bf16 (or, with f16, float16) matrix [rows][cols] (cols % 64 == 0, base
+// 16-byte aligned), loaded in boxes of 64 columns x box_rows rows with the 128-byte swizzle.
+bool tc_make_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int box_rows,
+                 bool f16 = false);
 
 // Token tile the launcher uses for T tokens (the activation map's box height must match).
 int tc_token_tile(int T);
@@ -35,19 +36,22 @@ bool launch_gemm_tc(const CUtensorMap& wmap, const CUtensorMap& xmap, int epi, i
 // Gate/up + SwiGLU with the token tile as the MMA's A operand (128 tokens, two bf16 terms: xmap and
 // xmap_lo, box 128 rows) and 128 gate + 128 up rows as B (wmap over the [2F][K] gate|up matrix,
 // box 128 rows): Y, Y2 [>= T][ldy] bf16 hi and lo terms of silu(gate) * up. F % 128 == 0.
+// Without xmap_lo, activations and weights are f16 (one term each; maps made with f16) and Y
+// receives a single f16 output.
 bool tc_swiglu_tn_ok(int64_t K, int64_t F);
 // With wmap_lo the weights are two bf16 terms as well (hi in wmap, lo in wmap_lo; a Q8_0 weight
 // d*q split so that hi + lo holds it to 16 bits): four products per k-step instead of two.
-bool launch_gemm_swiglu_tn(const CUtensorMap& xmap, const CUtensorMap& xmap_lo, const CUtensorMap& wmap,
+bool launch_gemm_swiglu_tn(const CUtensorMap& xmap, const CUtensorMap* xmap_lo, const CUtensorMap& wmap,
                            int K, int T, int F, void* Y, void* Y2, int ldy, uint32_t* err, cudaStream_t st,
                            const CUtensorMap* wmap_lo = nullptr);
 
 // Store / residual add with the token tile as A (two bf16 terms) and 256 weight rows as B (wmap
 // over W [M][K], box 128 rows): Y [>= T][ldy] float32 (op)= X W^T. M % 256 == 0. splits > 1
 // splits K over blockIdx.z with vector atomic adds into Y (a store then needs Y zeroed first).
+// Without xmap_lo: f16 activations and weights, one term each.
 bool tc_tn_ok(int64_t M, int64_t K);
 int tc_tn_splits(int64_t M, int64_t K, int T, int n_sm);
-bool launch_gemm_tn(const CUtensorMap& xmap, const CUtensorMap& xmap_lo, const CUtensorMap& wmap, int epi,
+bool launch_gemm_tn(const CUtensorMap& xmap, const CUtensorMap* xmap_lo, const CUtensorMap& wmap, int epi,
                     int K, int M, int T, float* Y, int ldy, int splits, uint32_t* err, cudaStream_t st,
                     const CUtensorMap* wmap_lo = nullptr);
 

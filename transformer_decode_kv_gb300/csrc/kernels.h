@@ -58,6 +58,15 @@ __host__ __device__ inline size_t kv_q8_scale_offset(int32_t Hkv, int32_t n_ctx,
 // head. Used by the defrag to gather one cache region in the new cell order.
 void launch_kv_gather(const void* src, void* dst, const int32_t* order, int32_t n, int32_t n_head,
                       int32_t n_src, int32_t row_bytes, cudaStream_t st);
+// The same with a single f16 output (the prefill GEMMs' f16 operand).
+void launch_rmsnorm_f16(const float* x, const int32_t* rows, int32_t R, int32_t d, const float* g,
+                        float eps, void* yh, cudaStream_t st);
+// Q8_0 weight -> two f16 terms hi = f16(d * q), lo = f16(d * q - hi): exact, since d * q has at
+// most 18 significant bits (fp16 scale x 8-bit integer) and hi + lo hold 22 (within f16 range).
+void launch_q8_0_to_f16_terms(const int8_t* q, const __half* d, int64_t rows, int64_t cols, void* hi, void* lo,
+                              cudaStream_t st);
+// y[i] = f16(x[i]) for n bf16 values: exact for |x| in the f16 normal range [2^-14, 65504].
+void launch_bf16_to_f16(const void* x, int64_t n, void* y, cudaStream_t st);
 // Q8_0 weight [rows][cols] (int8 quants q, fp16 scales d per 32 values) -> two bf16 terms:
 // w = d * q (exact in float32), hi = bf16(w), lo = bf16(w - hi); hi + lo holds w to 16 bits.
 void launch_q8_0_to_bf16_terms(const int8_t* q, const __half* d, int64_t rows, int64_t cols, void* hi,
@@ -121,6 +130,7 @@ struct AttnArgs {
     float* out;              // [T][H * hd]
     void* out_b;             // if set: bf16 output [T][H * hd] instead of out
     void* out_b_lo;          // with out_b: the low bf16 term of the output
+    bool out_f16;            // with out_b: a single f16 output instead of bf16 terms
     int32_t ldo;
     const int32_t* hdr;      // device: [0] work items of this ubatch
     int32_t n_work, max_nq;  // grid size (an upper bound of the device count), tile shape

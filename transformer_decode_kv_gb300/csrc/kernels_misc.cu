@@ -36,6 +36,7 @@ __device__ __forceinline__ void store_out(float* y, int64_t i, float v) { y[i] =
 __device__ __forceinline__ void store_out(__nv_bfloat16* y, int64_t i, float v) {
     y[i] = __float2bfloat16_rn(v);
 }
+__device__ __forceinline__ void store_out(__half* y, int64_t i, float v) { y[i] = __float2half_rn(v); }
 
 template <typename OT>
 __global__ void rmsnorm_kernel(const float* __restrict__ x, const int32_t* __restrict__ rows,
@@ -156,6 +157,21 @@ __global__ void q8_0_terms_kernel(const int8_t* __restrict__ q, const __half* __
     const __nv_bfloat16 h = __float2bfloat16_rn(w);
     hi[i] = h;
     lo[i] = __float2bfloat16_rn(w - __bfloat162float(h));
+}
+
+__global__ void q8_0_f16_terms_kernel(const int8_t* __restrict__ q, const __half* __restrict__ d, int64_t n,
+                                      __half* __restrict__ hi, __half* __restrict__ lo) {
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= n) return;
+    const float w = __half2float(d[i / 32]) * (float)q[i];
+    const __half h = __float2half_rn(w);
+    hi[i] = h;
+    lo[i] = __float2half_rn(w - __half2float(h));
+}
+
+__global__ void bf16_to_f16_kernel(const __nv_bfloat16* __restrict__ x, int64_t n, __half* __restrict__ y) {
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i < n) y[i] = __float2half_rn(__bfloat162float(x[i]));
 }
 
 __global__ void swiglu_kernel(const float* __restrict__ gu, int64_t T, int F,
@@ -297,6 +313,27 @@ void launch_kv_gather(const void* src, void* dst, const int32_t* order, int32_t 
         kv_gather_kernel<uint16_t><<<grid, 256, 0, st>>>(static_cast<const uint16_t*>(src),
                                                          static_cast<uint16_t*>(dst), order, n, n_src, upr);
     }
+}
+
+void launch_rmsnorm_f16(const float* x, const int32_t* rows, int32_t R, int32_t d, const float* g,
+                        float eps, void* yh, cudaStream_t st) {
+    if (R <= 0) return;
+    rmsnorm_kernel<__half><<<R, d >= 1024 ? 512 : 256, 0, st>>>(x, rows, d, g, eps, static_cast<__half*>(yh),
+                                                               nullptr);
+}
+
+void launch_q8_0_to_f16_terms(const int8_t* q, const __half* d, int64_t rows, int64_t cols, void* hi, void* lo,
+                              cudaStream_t st) {
+    const int64_t n = rows * cols;
+    if (n <= 0) return;
+    q8_0_f16_terms_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(q, d, n, static_cast<__half*>(hi),
+                                                                        static_cast<__half*>(lo));
+}
+
+void launch_bf16_to_f16(const void* x, int64_t n, void* y, cudaStream_t st) {
+    if (n <= 0) return;
+    bf16_to_f16_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(static_cast<const __nv_bfloat16*>(x), n,
+                                                                     static_cast<__half*>(y));
 }
 
 void launch_q8_0_to_bf16_terms(const int8_t* q, const __half* d, int64_t rows, int64_t cols, void* hi,

@@ -56,9 +56,9 @@ struct Layer {
     CUtensorMap mq, mo, mgu, md;
     CUtensorMap mgu128;      // gate|up with 128-row boxes (token-major SwiGLU GEMM)
     bool gu_tn = false;
-    // Q8_0 layers: each weight as two bf16 terms (hi + lo) for the token-major GEMM, and the maps
-    // of the low terms (the high terms use mq, mo, mgu128, md)
-    bool q8_tc = false;
+    // f16 prefill operands: a BF16 layer's weights converted to f16 (mq, mo, mgu128, md over the
+    // copies), a Q8_0 layer's as two f16 terms (hi in those maps, lo in the *_lo maps)
+    bool f16_ready = false, q8_tc = false;
     CUtensorMap mq_lo, mo_lo, mgu128_lo, md_lo;
 };
 
@@ -132,6 +132,8 @@ struct llm_ctx {
     CUtensorMap m_hb[2], m_attnb[2], m_ub[2], m_hob[2], m_lm;
     CUtensorMap m_hb_lo, m_attnb_lo, m_ub_lo, m_hob_lo;        // low terms (token box 128)
     bool tc_ok = false;                        // tensor-core prefill GEMMs for the layers
+    bool tc_f16 = false;                       // ... with f16 operands (one term each, token-major)
+    CUtensorMap m_hh, m_ah, m_uh;              // f16 views of hb, attnb, ub (token box 128)
     bool tc_lm = false;                        // ... and for the output matrix
     float *part_o = nullptr, *part_m = nullptr, *part_l = nullptr;
     int32_t* tickets = nullptr;
@@ -516,22 +518,25 @@ bool forward_ubatch(llm_ctx* c, int32_t T, int32_t O, int32_t out_row0, int32_t 
     g.err = c->d_err;
 
     const double norm_bytes = Td * d * 8.0 + d * 4.0;
-    // tensor-core prefill GEMMs; activations as split bf16 (hi + lo) operands, box 128 tokens
+    // tensor-core prefill GEMMs: f16 operands (one term each), or activations as split bf16 (hi +
+    // lo) operands; box 128 tokens
     const bool tc = !gemv && c->tc_ok;
+    const bool f16 = tc && c->tc_f16;
     const int bi = 0;
-    if (tc) { a.out_b = c->attnb; a.out_b_lo = c->attnb_lo; }
+    if (tc) { a.out_b = c->attnb; a.out_b_lo = f16 ? nullptr : c->attnb_lo; a.out_f16 = f16; }
     // store / residual add: the token-major GEMM when the weight rows come in 256-row tiles
     // (split-K with atomic adds when the tiles alone leave SMs idle), else the weight-major one
     auto tc_gemm = [&](const CUtensorMap& wm, const CUtensorMap& xm, int epi, int K, int M, void* Y,
                        int ldy, const CUtensorMap* wlo) {
-        const CUtensorMap* xlo = &xm == &c->m_hb[bi] ? &c->m_hb_lo
+        const CUtensorMap* xlo = f16 ? nullptr
+                               : &xm == &c->m_hb[bi] ? &c->m_hb_lo
                                : &xm == &c->m_attnb[bi] ? &c->m_attnb_lo : &c->m_ub_lo;
         if (epi != GEMM_EPI_SWIGLU && tc_tn_ok(M, K)) {
             const int splits = tc_tn_splits(M, K, T, c->n_sm);
             if (splits > 1 && epi == GEMM_EPI_STORE &&
                 !cuda_ok(c, cudaMemsetAsync(Y, 0, sizeof(float) * (size_t)T * ldy, st), "memset"))
                 return false;
-            if (!launch_gemm_tn(xm, *xlo, wm, epi, K, M, T, static_cast<float*>(Y), ldy, splits, c->d_err, st,
+            if (!launch_gemm_tn(xm, xlo, wm, epi, K, M, T, static_cast<float*>(Y), ldy, splits, c->d_err, st,
                                 wlo)) {
                 c->err = "tensor-core GEMM launch failed";
                 return false;
@@ -573,12 +578,14 @@ bool forward_ubatch(llm_ctx* c, int32_t T, int32_t O, int32_t out_row0, int32_t 
             }
         } else {
             k = kt_begin(c);
-            if (tc) launch_rmsnorm_bf16(c->x, nullptr, T, d, L.attn_norm, hp.rms_eps, c->hb, c->hb_lo, st);
+            if (f16) launch_rmsnorm_f16(c->x, nullptr, T, d, L.attn_norm, hp.rms_eps, c->hb, st);
+            else if (tc) launch_rmsnorm_bf16(c->x, nullptr, T, d, L.attn_norm, hp.rms_eps, c->hb, c->hb_lo, st);
             else launch_rmsnorm(c->x, nullptr, T, d, L.attn_norm, hp.rms_eps, c->h, st);
             kt_end(c, k, KC_RMSNORM, norm_bytes, 0);
             k = kt_begin(c);
             if (tc) {
-                if (!tc_gemm(L.mq, c->m_hb[bi], GEMM_EPI_STORE, d, qkvw, c->qkv, qkvw, L.q8_tc ? &L.mq_lo : nullptr))
+                if (!tc_gemm(L.mq, f16 ? c->m_hh : c->m_hb[bi], GEMM_EPI_STORE, d, qkvw, c->qkv, qkvw,
+                             L.q8_tc ? &L.mq_lo : nullptr))
                     return false;
             }
             else launch_linear(L.qkv, 0, qkvw, c->h, d, T, c->qkv, qkvw, EPI_STORE, st);
@@ -625,7 +632,8 @@ bool forward_ubatch(llm_ctx* c, int32_t T, int32_t O, int32_t out_row0, int32_t 
             g.x = c->attn; g.ldx = qw; g.x_rows = nullptr; g.g = nullptr; g.y = c->x; g.ldy = d;
             if (!launch_gemv_bulk(L.wo.type, g, GEPI_ADD, false, c->n_sm, st, pdl)) return bulk_fail();
         } else if (tc) {
-            if (!tc_gemm(L.mo, c->m_attnb[bi], GEMM_EPI_ADD, qw, d, c->x, d, L.q8_tc ? &L.mo_lo : nullptr))
+            if (!tc_gemm(L.mo, f16 ? c->m_ah : c->m_attnb[bi], GEMM_EPI_ADD, qw, d, c->x, d,
+                         L.q8_tc ? &L.mo_lo : nullptr))
                 return false;
         } else {
             launch_linear(L.wo, 0, d, c->attn, qw, T, c->x, d, EPI_ADD, st);
@@ -640,13 +648,15 @@ bool forward_ubatch(llm_ctx* c, int32_t T, int32_t O, int32_t out_row0, int32_t 
             kt_end(c, k, lin_cls, wbytes(L.gu, 2 * (int64_t)F) + Td * (d + F) * 4.0, 4.0 * Td * F * d);
         } else {
             k = kt_begin(c);
-            if (tc) launch_rmsnorm_bf16(c->x, nullptr, T, d, L.ffn_norm, hp.rms_eps, c->hb, c->hb_lo, st);
+            if (f16) launch_rmsnorm_f16(c->x, nullptr, T, d, L.ffn_norm, hp.rms_eps, c->hb, st);
+            else if (tc) launch_rmsnorm_bf16(c->x, nullptr, T, d, L.ffn_norm, hp.rms_eps, c->hb, c->hb_lo, st);
             else launch_rmsnorm(c->x, nullptr, T, d, L.ffn_norm, hp.rms_eps, c->h, st);
             kt_end(c, k, KC_RMSNORM, norm_bytes, 0);
             k = kt_begin(c);
             if (tc && L.gu_tn) {
-                if (!launch_gemm_swiglu_tn(c->m_hb[bi], c->m_hb_lo, L.mgu128, d, T, F, c->ub, c->ub_lo, F,
-                                           c->d_err, st, L.q8_tc ? &L.mgu128_lo : nullptr)) {
+                if (!launch_gemm_swiglu_tn(f16 ? c->m_hh : c->m_hb[bi], f16 ? nullptr : &c->m_hb_lo, L.mgu128, d, T,
+                                           F, c->ub, f16 ? nullptr : c->ub_lo, F, c->d_err, st,
+                                           L.q8_tc ? &L.mgu128_lo : nullptr)) {
                     c->err = "tensor-core GEMM launch failed";
                     return false;
                 }
@@ -661,7 +671,9 @@ bool forward_ubatch(llm_ctx* c, int32_t T, int32_t O, int32_t out_row0, int32_t 
             g.x = c->u; g.ldx = F; g.x_rows = nullptr; g.g = nullptr; g.y = c->x; g.ldy = d;
             if (!launch_gemv_bulk(L.down.type, g, GEPI_ADD, false, c->n_sm, st, pdl)) return bulk_fail();
         } else if (tc) {
-            if (!tc_gemm(L.md, c->m_ub[bi], GEMM_EPI_ADD, F, d, c->x, d, L.q8_tc ? &L.md_lo : nullptr)) return false;
+            if (!tc_gemm(L.md, f16 ? c->m_uh : c->m_ub[bi], GEMM_EPI_ADD, F, d, c->x, d,
+                         L.q8_tc ? &L.md_lo : nullptr))
+                return false;
         } else {
             launch_linear(L.down, 0, d, c->u, F, T, c->x, d, EPI_ADD, st);
         }
@@ -921,7 +933,7 @@ int llm_load_weights(llm_ctx* c, const char* name, int32_t type, const int64_t n
             if (!cuda_ok(c, cudaMemcpy(g, data, nbytes, cudaMemcpyDefault), "copy")) return -2;
         }
         L.loaded |= sp->bit;
-        L.q8_tc = false;                    // the bf16 terms, if any, are stale
+        L.q8_tc = L.f16_ready = false;      // the f16 operands, if any, are stale
         return 0;
     }
     // fused stores: Q, K, V rows stacked in one matrix; gate rows then up rows in another
@@ -946,7 +958,7 @@ int llm_load_weights(llm_ctx* c, const char* name, int32_t type, const int64_t n
     }
     if (!c->host_only && !fill_rows(c, *m, row0, rows, data, nbytes)) return -2;
     L.loaded |= sp->bit;
-    L.q8_tc = false;
+    L.q8_tc = L.f16_ready = false;
     return 0;
 }
 
@@ -1049,7 +1061,7 @@ int llm_weights_ready(llm_ctx* c) {
     if (!c->out_loaded) c->out = c->embd;   // tied output
     c->ready = true;
     drop_graphs(c);
-    c->tc_ok = false;
+    c->tc_ok = c->tc_f16 = false;
     if (c->host_only) return 0;
     // tensor-core prefill: every linear weight BF16 with supported shapes
     const llm_hparams& h = c->hp;
@@ -1057,39 +1069,59 @@ int llm_weights_ready(llm_ctx* c) {
     const int64_t U = c->n_ubatch;
     bool ok = tc_shape_ok(qkvw, d, GEMM_EPI_STORE, 0) && tc_shape_ok(d, qw, GEMM_EPI_ADD, 0) &&
               tc_shape_ok(0, d, GEMM_EPI_SWIGLU, F) && tc_shape_ok(d, F, GEMM_EPI_ADD, 0);
-    // Q8_0 layers take the token-major GEMM with the weights as two bf16 terms (4 bytes per weight
-    // of extra device memory, made here once): only when prefill ubatches can occur
-    const bool q8_shapes = U > gemv_max_tokens() && tc_tn_ok(qkvw, d) && tc_tn_ok(d, qw) &&
+    // Prefill GEMMs on the token-major kernel with f16 operands when every layer's shapes allow it
+    // and prefill ubatches can occur: a BF16 weight converted to f16 (exact in the f16 normal
+    // range; 2 bytes per weight of extra device memory), a Q8_0 weight as two f16 terms that hold
+    // d * q exactly (4 bytes per weight), made here once. Otherwise BF16 layers use the bf16
+    // operands (activations as two terms) on the kernels their shapes allow.
+    const bool tn_shapes = U > gemv_max_tokens() && tc_tn_ok(qkvw, d) && tc_tn_ok(d, qw) &&
                            tc_swiglu_tn_ok(d, F) && tc_tn_ok(d, F);
-    auto terms = [&](const DevMat& W, int64_t rows, int64_t cols, CUtensorMap* hi_map, CUtensorMap* lo_map) {
+    auto f16_copy = [&](const DevMat& W, int64_t rows, int64_t cols, CUtensorMap* map) {
+        uint16_t* y = nullptr;
+        if (!dalloc(c, &y, (size_t)(rows * cols))) return false;
+        launch_bf16_to_f16(W.data, rows * cols, y, c->st);
+        return tc_make_map(map, y, rows, cols, 128, true);
+    };
+    auto f16_terms = [&](const DevMat& W, int64_t rows, int64_t cols, CUtensorMap* hi_map, CUtensorMap* lo_map) {
         uint16_t *hi = nullptr, *lo = nullptr;
         if (!dalloc(c, &hi, (size_t)(rows * cols)) || !dalloc(c, &lo, (size_t)(rows * cols))) return false;
-        launch_q8_0_to_bf16_terms(static_cast<const int8_t*>(W.data), W.scales, rows, cols, hi, lo, c->st);
-        return tc_make_map(hi_map, hi, rows, cols, 128) && tc_make_map(lo_map, lo, rows, cols, 128);
+        launch_q8_0_to_f16_terms(static_cast<const int8_t*>(W.data), W.scales, rows, cols, hi, lo, c->st);
+        return tc_make_map(hi_map, hi, rows, cols, 128, true) && tc_make_map(lo_map, lo, rows, cols, 128, true);
     };
+    bool f16 = tn_shapes;
     for (int32_t il = 0; ok && il < h.n_layer; ++il) {
         Layer& L = c->layers[il];
         const bool bf16 = L.qkv.type == LLM_TYPE_BF16 && L.wo.type == LLM_TYPE_BF16 &&
                           L.gu.type == LLM_TYPE_BF16 && L.down.type == LLM_TYPE_BF16;
         const bool q8 = L.qkv.type == LLM_TYPE_Q8_0 && L.wo.type == LLM_TYPE_Q8_0 &&
                         L.gu.type == LLM_TYPE_Q8_0 && L.down.type == LLM_TYPE_Q8_0;
-        if (bf16) {
+        if (bf16 && tn_shapes) {
+            L.f16_ready = L.f16_ready || (f16_copy(L.qkv, qkvw, d, &L.mq) && f16_copy(L.wo, d, qw, &L.mo) &&
+                                          f16_copy(L.gu, 2 * F, d, &L.mgu128) && f16_copy(L.down, d, F, &L.md));
+            ok = L.f16_ready;
+            L.gu_tn = ok;
+        } else if (bf16) {
+            f16 = false;
             ok = tc_make_map(&L.mq, L.qkv.data, qkvw, d, 128) &&
                  tc_make_map(&L.mo, L.wo.data, d, qw, 128) &&
                  tc_make_map(&L.mgu, L.gu.data, 2 * F, d, 64) &&
                  tc_make_map(&L.md, L.down.data, d, F, 128);
             L.gu_tn = ok && tc_swiglu_tn_ok(d, F) && tc_make_map(&L.mgu128, L.gu.data, 2 * F, d, 128);
-        } else if (q8 && q8_shapes) {
-            L.q8_tc = L.q8_tc || (terms(L.qkv, qkvw, d, &L.mq, &L.mq_lo) && terms(L.wo, d, qw, &L.mo, &L.mo_lo) &&
-                                  terms(L.gu, 2 * F, d, &L.mgu128, &L.mgu128_lo) &&
-                                  terms(L.down, d, F, &L.md, &L.md_lo));
+        } else if (q8 && tn_shapes) {
+            L.q8_tc = L.q8_tc || (f16_terms(L.qkv, qkvw, d, &L.mq, &L.mq_lo) &&
+                                  f16_terms(L.wo, d, qw, &L.mo, &L.mo_lo) &&
+                                  f16_terms(L.gu, 2 * F, d, &L.mgu128, &L.mgu128_lo) &&
+                                  f16_terms(L.down, d, F, &L.md, &L.md_lo));
             ok = L.q8_tc;
             L.gu_tn = ok;
         } else {
             ok = false;
         }
     }
-    if (ok && !cuda_ok(c, cudaStreamSynchronize(c->st), "weight terms")) return -1;
+    if (ok && !cuda_ok(c, cudaStreamSynchronize(c->st), "f16 weights")) return -1;
+    ok = ok && (!f16 || (tc_make_map(&c->m_hh, c->hb, U, d, 128, true) &&
+                         tc_make_map(&c->m_ah, c->attnb, U, qw, 128, true) &&
+                         tc_make_map(&c->m_uh, c->ub, U, F, 128, true)));
     const int boxes[2] = {128, 256};
     for (int i = 0; ok && i < 2; ++i)
         ok = tc_make_map(&c->m_hb[i], c->hb, U, d, boxes[i]) &&
@@ -1103,6 +1135,7 @@ int llm_weights_ready(llm_ctx* c) {
     const bool lm_ok = c->out.type == LLM_TYPE_BF16 && tc_shape_ok(h.n_vocab, d, GEMM_EPI_STORE, 0) &&
                        tc_make_map(&c->m_lm, c->out.data, h.n_vocab, d, 128);
     c->tc_ok = ok;
+    c->tc_f16 = ok && f16;
     c->tc_lm = ok && lm_ok;
     setup_step(c);
     return 0;
