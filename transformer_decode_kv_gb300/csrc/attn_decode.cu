@@ -502,15 +502,16 @@ attn_decode_mma_kernel(AttnArgs a, float scale_log2) {
         const __half* kb;
         const __half* vb;
         if constexpr (Q8) {
-            // int8 rows -> exact f16 tiles (the previous pass's MMAs ended at the last barrier)
-            for (int idx = threadIdx.x; idx < kCH * (HD / 4); idx += kMT) {
-                const int c = idx / (HD / 4), w4 = idx % (HD / 4);
-                const uint32_t kq = *reinterpret_cast<const uint32_t*>(S.kraw + c * RSS + w4 * 4) ^ 0x80808080u;
-                const uint32_t vq = *reinterpret_cast<const uint32_t*>(S.vraw + c * RSS + w4 * 4) ^ 0x80808080u;
-                *reinterpret_cast<uint2*>(tk + c * RS + w4 * 4) = make_uint2(q8x2_to_h2(kq, 0x7170u), q8x2_to_h2(kq, 0x7372u));
-                *reinterpret_cast<uint2*>(tv + c * RS + w4 * 4) = make_uint2(q8x2_to_h2(vq, 0x7170u), q8x2_to_h2(vq, 0x7372u));
+            // this warp's 16 int8 rows -> exact f16 rows of the tiles (only this warp's MMAs read
+            // them, and its previous pass's MMAs are done)
+            for (int idx = lane; idx < kMC * (HD / 4); idx += 32) {
+                const int cc = cw + idx / (HD / 4), w4 = idx % (HD / 4);
+                const uint32_t kq = *reinterpret_cast<const uint32_t*>(S.kraw + cc * RSS + w4 * 4) ^ 0x80808080u;
+                const uint32_t vq = *reinterpret_cast<const uint32_t*>(S.vraw + cc * RSS + w4 * 4) ^ 0x80808080u;
+                *reinterpret_cast<uint2*>(tk + cc * RS + w4 * 4) = make_uint2(q8x2_to_h2(kq, 0x7170u), q8x2_to_h2(kq, 0x7372u));
+                *reinterpret_cast<uint2*>(tv + cc * RS + w4 * 4) = make_uint2(q8x2_to_h2(vq, 0x7170u), q8x2_to_h2(vq, 0x7372u));
             }
-            __syncthreads();
+            __syncwarp();
             kb = tk;
             vb = tv;
         } else {
