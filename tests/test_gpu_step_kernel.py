@@ -22,7 +22,8 @@ HP = HParams(n_layer=2, n_embd=4096, n_head=32, n_head_kv=8, head_dim=128, n_ff=
 KEY = "llama8b_layers2_bf16"
 N_STEPS = 12
 TOL_ORACLE = 2e-2      # the BF16 bar
-TOL_DECODE = 1e-3      # one-token steps: float32 activations over bf16 weights
+TOL_DECODE = 5e-3      # one-token steps: float32 activations over bf16 weights, attending to the
+                       # prompt's K/V rows from the prefill (f16 GEMM operands)
 TOL_PATHS = 1e-4       # fused kernel against the per-op kernels
 
 
