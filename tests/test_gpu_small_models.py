@@ -1,7 +1,8 @@
 """GPU parity on small BF16 and Q8_0 models whose shapes take every fast path of the library:
 the tensor-core prefill GEMMs (BF16), the bulk-staged decode GEMVs with fused RMSNorm, RoPE + K/V
 append, SwiGLU and logits/argmax epilogues (BF16 and Q8_0), and decode-step graph replay.
-Against the oracle: logits within the bar of the weight type, greedy tokens gap-checked."""
+Against the oracle: logits within the 2e-2 bar of BF16 and Q8_0 weights (the prefill GEMMs take
+f16 operands), greedy tokens gap-checked."""
 import dataclasses
 
 import numpy as np
@@ -25,7 +26,7 @@ def _workload(key, types, n_prompt, n_ubatch):
 
 @pytest.mark.parametrize("key,types,tol", [
     ("small_bf16", {"embd": S.BF16, "linear": S.BF16}, 2e-2),
-    ("small_q8_0", {"embd": S.F32, "linear": S.Q8_0}, 1e-4),
+    ("small_q8_0", {"embd": S.F32, "linear": S.Q8_0}, 2e-2),     # prefill GEMMs take f16 operands
 ])
 @pytest.mark.parametrize("n_prompt,n_ubatch", [(300, 512), (77, 32)])
 def test_small_model_prefill_and_decode(key, types, tol, n_prompt, n_ubatch):

@@ -152,12 +152,16 @@ struct SampleArgs {
     float penalty = 1.f;
     int32_t top_k = 1;               // 1 .. sample_max_k()
     float top_p = 1.f, min_p = 0.f, temperature = 0.f, u = 0.f;
-    float* scratch = nullptr;        // [V + 4], 16-byte aligned
     int32_t* out = nullptr;          // the picked token (device)
-    uint32_t* err = nullptr;
+    uint32_t* err = nullptr;         // written 0 on success, ERR_ROW_RANGE without a candidate
 };
 int sample_max_k();
-bool launch_sample(const SampleArgs& a, cudaStream_t st);
+// Device state one sampler call uses (barrier, histograms, candidates): sample_state_bytes()
+// bytes, zeroed once at allocation and again after a call that did not finish (err not written).
+size_t sample_state_bytes();
+// One cooperative launch over up to 64 blocks (more for rows above 64 x 4096 values); false if
+// the row is too long for the SM count or the launch failed.
+bool launch_sample(const SampleArgs& a, void* state, int n_sm, cudaStream_t st);
 // The prefill tiles (16 tokens x 4 query heads) on tensor cores (attn_mma.cu): F16 KV, 4 query
 // heads per KV head, head_dim 32, 64 or 128. launch_attention uses it when it applies.
 bool attention_mma_ok(const AttnArgs& a);

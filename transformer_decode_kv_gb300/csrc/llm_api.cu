@@ -189,7 +189,7 @@ struct llm_ctx {
     int32_t* d_abort = nullptr;
     uint32_t step_gen = 0;              // launches since the counters were last zeroed
     bool step_trace = false;
-    float* d_sample_row = nullptr;      // sampler scratch [V]
+    uint8_t* d_sample_state = nullptr;  // sampler barrier, histograms and candidates
     int32_t* d_sample_tok = nullptr;    // [kMaxPenalty] penalty tokens, the picked token, status
     int32_t* h_sample_tok = nullptr;    // pinned: the same layout
     uint64_t* d_trace = nullptr;        // timeline of the last traced step
@@ -1602,10 +1602,11 @@ int32_t llm_sample_ith(llm_ctx* c, int32_t i, const llm_sampler_params* p, float
     }
     const int32_t j = resolve_row(c, i);
     if (j < 0) { c->err = "no logits for this output"; return -1; }
-    if (!c->d_sample_row && !(dalloc(c, &c->d_sample_row, (size_t)c->hp.n_vocab + 4) &&
-                              dalloc(c, &c->d_sample_tok, (size_t)kMaxPenalty + 2) &&
-                              cuda_ok(c, cudaMallocHost(&c->h_sample_tok, sizeof(int32_t) * (kMaxPenalty + 2)),
-                                      "cudaMallocHost")))
+    if (!c->d_sample_state &&
+        !(dalloc(c, &c->d_sample_state, sample_state_bytes()) &&
+          cuda_ok(c, cudaMemset(c->d_sample_state, 0, sample_state_bytes()), "memset") &&
+          dalloc(c, &c->d_sample_tok, (size_t)kMaxPenalty + 2) &&
+          cuda_ok(c, cudaMallocHost(&c->h_sample_tok, sizeof(int32_t) * (kMaxPenalty + 2)), "cudaMallocHost")))
         return -1;
     SampleArgs a;
     a.logits = c->d_logits + (size_t)j * c->hp.n_vocab;
@@ -1614,19 +1615,26 @@ int32_t llm_sample_ith(llm_ctx* c, int32_t i, const llm_sampler_params* p, float
     a.n_pen = p->n_penalty_tokens;
     a.penalty = p->repeat_penalty;
     a.top_k = p->top_k; a.top_p = p->top_p; a.min_p = p->min_p; a.temperature = p->temperature; a.u = u;
-    a.scratch = c->d_sample_row;
     a.out = c->d_sample_tok + kMaxPenalty;              // then the status word
     a.err = reinterpret_cast<uint32_t*>(c->d_sample_tok + kMaxPenalty + 1);
     if (a.n_pen > 0) std::memcpy(c->h_sample_tok, p->penalty_tokens, sizeof(int32_t) * a.n_pen);
     const bool ok =
         (a.n_pen == 0 || cuda_ok(c, cudaMemcpyAsync(c->d_sample_tok, c->h_sample_tok, sizeof(int32_t) * a.n_pen,
                                                     cudaMemcpyHostToDevice, c->st), "copy")) &&
-        (launch_sample(a, c->st) || (c->err = "sampler launch failed", false)) &&
+        cuda_ok(c, cudaMemsetAsync(a.out, 0xFF, 2 * sizeof(int32_t), c->st), "memset") &&
+        (launch_sample(a, c->d_sample_state, c->n_sm, c->st) || (c->err = "sampler launch failed", false)) &&
         cuda_ok(c, cudaMemcpyAsync(c->h_sample_tok + kMaxPenalty, a.out, 2 * sizeof(int32_t),
                                    cudaMemcpyDeviceToHost, c->st), "copy") &&
         cuda_ok(c, cudaStreamSynchronize(c->st), "sampler");
     if (!ok) return -1;
-    if (c->h_sample_tok[kMaxPenalty + 1] != 0) { c->err = "sampler found no candidate"; return -1; }
+    const uint32_t st = static_cast<uint32_t>(c->h_sample_tok[kMaxPenalty + 1]);
+    if (st == 0xFFFFFFFFu) {                            // a barrier gave up: reset the state
+        cudaMemsetAsync(c->d_sample_state, 0, sample_state_bytes(), c->st);
+        cudaStreamSynchronize(c->st);
+        c->err = "sampler did not finish";
+        return -1;
+    }
+    if (st != 0) { c->err = "sampler found no candidate"; return -1; }
     return c->h_sample_tok[kMaxPenalty];
 }
 
