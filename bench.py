@@ -369,7 +369,7 @@ def main():
     line = {
         "metric": METRIC, "value": dec_tps, "unit": "tok/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": res["dec_s"] / K * 1e3, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16 weights, f32 activations/accumulation",
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16 weights; decode f32 activations, prefill f16 GEMM operands; f32 accumulation",
         "data": "synthetic (seeded random weights and prompt)", "config": config,
         "prefill_tok_s": pre_tps, "prefill_ms": res["prefill_s"] * 1e3,
         "sampler_us_per_call": res["sample_us"],
