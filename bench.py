@@ -179,9 +179,10 @@ def run_gpu(args, rank, world, local_rank):
     w = S.WORKLOADS[args.workload]
     hp = w.hp
     stream = torch.cuda.Stream()
-    ctx = Context(hp, n_ctx=w.n_ctx, n_seq_max=1, type_k=w.type_kv, type_v=w.type_kv,
-                  n_batch=max(w.n_batch, w.n_prompt), n_ubatch=w.n_ubatch, stream=stream.cuda_stream,
-                  fused_step=args.fused_step)
+    NS = w.n_seq                                        # sequences decoded together
+    ctx = Context(hp, n_ctx=w.n_ctx, n_seq_max=NS, type_k=w.type_kv, type_v=w.type_kv,
+                  n_batch=max(w.n_batch, w.n_prompt) if NS == 1 else w.n_batch, n_ubatch=w.n_ubatch,
+                  stream=stream.cuda_stream, fused_step=args.fused_step)
     for name, wt, shape, t in S.model_weights(hp, w.weight_seed, w.types, "cuda"):
         if ctx.load_weight(name, wt, shape, t) != 0:
             raise RuntimeError(ctx.last_error())
@@ -189,8 +190,25 @@ def run_gpu(args, rank, world, local_rank):
     if ctx.weights_ready() != 0:
         raise RuntimeError(ctx.last_error())
     torch.cuda.empty_cache()
-    prompt = S.prompt_tokens(w.prompt_seed_of(rank) if w.n_seq > 1 else w.prompt_seed + 97 * rank,
-                             w.n_prompt, hp.n_vocab).numpy()
+    prompts = [S.prompt_tokens(w.prompt_seed_of(s) + 977 * rank if NS > 1 else w.prompt_seed + 97 * rank,
+                               w.n_prompt, hp.n_vocab).numpy() for s in range(NS)]
+    prompt = prompts[0]
+
+    def prefill():
+        """Every sequence's prompt, in calls of at most n_batch tokens; the last token of each
+        sequence is the only output."""
+        if NS == 1:
+            return ctx.decode(prompt)
+        for s in range(NS):
+            for i0 in range(0, w.n_prompt, ctx.n_batch):
+                chunk = prompts[s][i0:i0 + ctx.n_batch]
+                flags = [0] * len(chunk)
+                if i0 + len(chunk) == w.n_prompt:
+                    flags[-1] = 1
+                r = ctx.decode(chunk, seq_ids=[[s]] * len(chunk), logits=flags)
+                if r != 0:
+                    return r
+        return 0
 
     def barrier():
         if world > 1:
@@ -198,12 +216,12 @@ def run_gpu(args, rank, world, local_rank):
 
     # ---- prefill: the prompt as one batch (split into n_ubatch ubatches), timed with events
     pre_times = []
-    for rep in range(3):
+    for rep in range(3 if NS == 1 else 2):
         ctx.seq_rm(-1, -1, -1)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         torch.cuda.synchronize()
         e0.record(stream)
-        r = ctx.decode(prompt)
+        r = prefill()
         e1.record(stream)
         torch.cuda.synchronize()
         if r != 0:
@@ -211,20 +229,28 @@ def run_gpu(args, rank, world, local_rank):
         if rep > 0:
             pre_times.append(e0.elapsed_time(e1) / 1e3)
     prefill_s = float(np.median(pre_times))
-    tok0 = ctx.get_argmax_ith(-1)
+    tok0 = ctx.get_argmax_ith(-1) if NS == 1 else [ctx.get_argmax_ith(-1)] * NS
+
+    seq_rows = [[s] for s in range(NS)]
 
     def decode_steps(n, tok):
+        """n greedy steps: one token per sequence each, device argmax read back each step."""
         for _ in range(n):
-            if ctx.decode([tok]) != 0:
-                raise RuntimeError(ctx.last_error())
-            tok = ctx.get_argmax_ith(-1)
+            if NS == 1:
+                if ctx.decode([tok]) != 0:
+                    raise RuntimeError(ctx.last_error())
+                tok = ctx.get_argmax_ith(-1)
+            else:
+                if ctx.decode(tok, seq_ids=seq_rows, logits=[1] * NS) != 0:
+                    raise RuntimeError(ctx.last_error())
+                tok = [ctx.get_argmax_ith(i) for i in range(NS)]
         return tok
 
     K, W = args.steps, args.warmup
-    if w.n_prompt + max(K, W) >= ctx.n_ctx:
+    if NS * (w.n_prompt + max(K, W)) > ctx.n_ctx:
         raise SystemExit(f"--steps/--warmup exceed the cache ({ctx.n_ctx} cells)")
     decode_steps(W, tok0)
-    ctx.seq_rm(0, w.n_prompt, -1)                       # back to the prompt context
+    ctx.seq_rm(-1, w.n_prompt, -1)                      # back to the prompt context
     barrier()
     torch.cuda.synchronize()
     with ClockSampler(local_rank) as clk:
@@ -241,14 +267,14 @@ def run_gpu(args, rank, world, local_rank):
         dec_s, prefill_s = float(t[0]), float(t[1])
 
     # ---- per-kernel timing over the same steps (roofline of the dominant kernel)
-    ctx.seq_rm(0, w.n_prompt, -1)
+    ctx.seq_rm(-1, w.n_prompt, -1)
     ctx.kernel_timing(True)
     decode_steps(K, tok0)
     ctx.kernel_timing(False)
     ks = ctx.kernel_stats()
 
     # ---- end to end: host token in, host argmax out, wall clock around K steps
-    ctx.seq_rm(0, w.n_prompt, -1)
+    ctx.seq_rm(-1, w.n_prompt, -1)
     barrier()
     torch.cuda.synchronize()
     t0 = time.perf_counter()
@@ -305,7 +331,7 @@ def main():
     if args.type_kv:
         w = dataclasses.replace(w, type_kv={"f32": 0, "f16": 1, "q8_0": 8}[args.type_kv])
         S.WORKLOADS[args.workload] = w
-    config = {"workload": args.workload, "description": w.description,
+    config = {"workload": args.workload, "description": w.description, "sequences": w.n_seq,
               "prompt_tokens": w.n_prompt, "decode_steps_timed": args.steps,
               "n_ctx": w.n_ctx, "kv_cache": {0: "f32", 1: "f16", 8: "q8_0"}[w.type_kv],
               "l2": "inputs larger than L2: every decode step streams all weights (no flush)",
@@ -351,8 +377,8 @@ def main():
         return
     hp = w.hp
     K = args.steps
-    dec_tps = world * K / res["dec_s"]
-    pre_tps = world * w.n_prompt / res["prefill_s"]
+    dec_tps = world * w.n_seq * K / res["dec_s"]
+    pre_tps = world * w.n_seq * w.n_prompt / res["prefill_s"]
     hbm_peak, bf16_peak, peak_src = measured_peaks()
     ks = res["ks"]
     # decode step algorithmic bytes: every class's bytes over the K steps
@@ -383,8 +409,8 @@ def main():
         "kernel_share": {k: v["ms"] / max(1e-9, sum(x["ms"] for x in ks.values())) for k, v in ks.items()
                          if v["launches"]},
         "clocks": res["clk"],
-        "e2e": {"value": world * K / res["e2e_s"], "unit": "tok/s", "h2d_bytes_per_step": 4,
-                "d2h_bytes_per_step": 4},
+        "e2e": {"value": world * w.n_seq * K / res["e2e_s"], "unit": "tok/s",
+                "h2d_bytes_per_step": 4 * w.n_seq, "d2h_bytes_per_step": 8 * w.n_seq},
         "gpu_launches": int(sum(v["launches"] for v in ks.values()) / max(1, K)) * K,
     }
     if not args.no_cpu_baseline:

@@ -60,6 +60,38 @@ __global__ void rmsnorm_kernel(const float* __restrict__ x, const int32_t* __res
     }
 }
 
+// The same for rows of d = 1024 * NV values and an f16 output: 256 threads, each holding NV float4
+// of the row in registers, so the row is read once.
+template <int NV>
+__global__ void __launch_bounds__(256) rmsnorm_f16_vec_kernel(const float* __restrict__ x,
+                                                             const int32_t* __restrict__ rows, int d,
+                                                             const float* __restrict__ g, float eps,
+                                                             __half* __restrict__ y) {
+    __shared__ float red[32];
+    const int r = blockIdx.x;
+    const int src = rows ? rows[r] : r;
+    const float4* xr = reinterpret_cast<const float4*>(x + (int64_t)src * d);
+    float4 v[NV];
+    float ss = 0.f;
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+        v[i] = xr[i * 256 + threadIdx.x];
+        ss += v[i].x * v[i].x + v[i].y * v[i].y + v[i].z * v[i].z + v[i].w * v[i].w;
+    }
+    ss = block_sum(ss, red);
+    const float inv = 1.0f / sqrtf(ss / (float)d + eps);
+    const float4* g4 = reinterpret_cast<const float4*>(g);
+    uint2* yr = reinterpret_cast<uint2*>(y + (int64_t)r * d);
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+        const float4 gg = g4[i * 256 + threadIdx.x];
+        const __half2 a = __floats2half2_rn(v[i].x * inv * gg.x, v[i].y * inv * gg.y);
+        const __half2 b = __floats2half2_rn(v[i].z * inv * gg.z, v[i].w * inv * gg.w);
+        yr[i * 256 + threadIdx.x] = make_uint2(*reinterpret_cast<const uint32_t*>(&a),
+                                               *reinterpret_cast<const uint32_t*>(&b));
+    }
+}
+
 template <typename KT>
 __device__ __forceinline__ KT to_kv(float v);
 template <>
@@ -83,14 +115,13 @@ __global__ void rope_kv_append_kernel(float* __restrict__ qkv, int H, int Hkv, i
     const int npairs = (H + Hkv) * half;
     for (int j = threadIdx.x; j < npairs; j += blockDim.x) {
         const int head = j / half, i = j % half;
-        float* p = row + head * hd + 2 * i;
-        const float x0 = p[0], x1 = p[1];
+        float2* p = reinterpret_cast<float2*>(row + head * hd + 2 * i);
+        const float2 xv = *p;
         const float2 e = cst[i];
-        const float y0 = x0 * e.x - x1 * e.y;
-        const float y1 = x0 * e.y + x1 * e.x;
+        const float y0 = xv.x * e.x - xv.y * e.y;
+        const float y1 = xv.x * e.y + xv.y * e.x;
         if (head < H) {
-            p[0] = y0;
-            p[1] = y1;
+            *p = make_float2(y0, y1);
         } else if (ok) {
             KT* dst = kc + ((int64_t)(head - H) * n_ctx + c) * hd + 2 * i;
             dst[0] = to_kv<KT>(y0);
@@ -98,10 +129,13 @@ __global__ void rope_kv_append_kernel(float* __restrict__ qkv, int H, int Hkv, i
         }
     }
     if (!ok) return;
-    const float* v = row + (H + Hkv) * hd;
-    for (int j = threadIdx.x; j < Hkv * hd; j += blockDim.x) {
-        const int g = j / hd, d = j % hd;
-        vc[((int64_t)g * n_ctx + c) * hd + d] = to_kv<KT>(v[j]);
+    const float2* v = reinterpret_cast<const float2*>(row + (H + Hkv) * hd);
+    for (int j = threadIdx.x; j < Hkv * hd / 2; j += blockDim.x) {
+        const int g = (2 * j) / hd, d = (2 * j) % hd;
+        const float2 vv = v[j];
+        KT* dst = vc + ((int64_t)g * n_ctx + c) * hd + d;
+        dst[0] = to_kv<KT>(vv.x);
+        dst[1] = to_kv<KT>(vv.y);
     }
 }
 
@@ -318,8 +352,14 @@ void launch_kv_gather(const void* src, void* dst, const int32_t* order, int32_t 
 void launch_rmsnorm_f16(const float* x, const int32_t* rows, int32_t R, int32_t d, const float* g,
                         float eps, void* yh, cudaStream_t st) {
     if (R <= 0) return;
-    rmsnorm_kernel<__half><<<R, d >= 1024 ? 512 : 256, 0, st>>>(x, rows, d, g, eps, static_cast<__half*>(yh),
-                                                               nullptr);
+    __half* y = static_cast<__half*>(yh);
+    switch (d) {
+        case 1024: rmsnorm_f16_vec_kernel<1><<<R, 256, 0, st>>>(x, rows, d, g, eps, y); return;
+        case 2048: rmsnorm_f16_vec_kernel<2><<<R, 256, 0, st>>>(x, rows, d, g, eps, y); return;
+        case 4096: rmsnorm_f16_vec_kernel<4><<<R, 256, 0, st>>>(x, rows, d, g, eps, y); return;
+        case 8192: rmsnorm_f16_vec_kernel<8><<<R, 256, 0, st>>>(x, rows, d, g, eps, y); return;
+    }
+    rmsnorm_kernel<__half><<<R, d >= 1024 ? 512 : 256, 0, st>>>(x, rows, d, g, eps, y, nullptr);
 }
 
 void launch_q8_0_to_f16_terms(const int8_t* q, const __half* d, int64_t rows, int64_t cols, void* hi, void* lo,
