@@ -509,7 +509,7 @@ bool forward_ubatch(llm_ctx* c, int32_t T, int32_t O, int32_t out_row0, int32_t 
     a.n_work = gemv ? attn_cap(c, T) : c->plan.n_work();  // grid bound (the device count decides)
     a.max_nq = max_nq;
     a.pdl = c->use_pdl && gemv;
-    a.slot = gemv ? slot : nullptr;                  // decode steps use the staged-row kernel
+    a.slot = slot;                                   // tiles of one token use the cluster decode kernel
     a.n_tok = T;
 
     GemvArgs g{};
