@@ -160,3 +160,24 @@ def test_tiny_long_context_decode(tkv):
     rep = G.greedy_compare(ctx, ora, 1, [len(toks) - 1], 6, tol, {})
     print("long context", tkv, rep)
     ctx.free()
+
+
+@pytest.mark.parametrize("n_seq", [16, 48])
+def test_tiny_many_sequence_decode_steps(n_seq):
+    """Decode steps with one token for each of 16 or 48 sequences in one ubatch: the tensor-core
+    decode attention runs with clusters of 4 and of 1 block per (token, KV head)."""
+    key = "tiny_f32_8seq"
+    w = S.WORKLOADS[key]
+    over = dict(n_seq_max=n_seq, n_ctx=4096, n_batch=1024, n_ubatch=512)
+    ctx, ora = G.library_ctx(key, **over), G.oracle_ctx(key, **over)
+    n_p = 20
+    toks = np.concatenate([S.prompt_tokens(900 + s, n_p, w.hp.n_vocab).numpy() for s in range(n_seq)])
+    seqs = [[s] for s in range(n_seq) for _ in range(n_p)]
+    flags = np.zeros(len(toks), dtype=np.int8)
+    flags[[(s + 1) * n_p - 1 for s in range(n_seq)]] = 1
+    assert ctx.decode(toks, seq_ids=seqs, logits=flags) == 0, ctx.last_error()
+    assert ora.decode(toks, seq_id=seqs, n_seq_id=[1] * len(toks), logits=flags) == 0
+    rows = [(s + 1) * n_p - 1 for s in range(n_seq)]
+    rep = G.greedy_compare(ctx, ora, n_seq, rows, 3, TOL, {})
+    assert rep["tokens_checked"] >= n_seq
+    ctx.free()

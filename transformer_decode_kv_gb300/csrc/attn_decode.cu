@@ -326,7 +326,9 @@ __device__ __forceinline__ uint32_t q8x2_to_h2(uint32_t biased, uint32_t sel) {
     return *reinterpret_cast<const uint32_t*>(&v);
 }
 
-template <int HD, typename KT>
+// CL blocks per cluster: 16 for a few tokens; fewer (down to 1, no peers) when many tokens already
+// fill the GPU, so each block walks a longer slice and pays the fixed costs less often.
+template <int HD, typename KT, int CL>
 __global__ void __launch_bounds__(kMT)
 attn_decode_mma_kernel(AttnArgs a, float scale_log2) {
     using SM = MmaDecSmem<HD, KT>;
@@ -364,7 +366,7 @@ attn_decode_mma_kernel(AttnArgs a, float scale_log2) {
     const int base = td1.y, len = td1.z;
     const int t = a.perm[td0.y];
     const int tpos = a.tok_pos[t];
-    const int chunk = (len + kCL - 1) / kCL;
+    const int chunk = (len + CL - 1) / CL;
     const int c0 = min(len, (int)rank * chunk), c1 = min(len, c0 + chunk);
     const int npass = c1 > c0 ? (c1 - c0 + kCH - 1) / kCH : 1;
     const uint8_t* K = static_cast<const uint8_t*>(a.kc) + (int64_t)kvh * a.n_ctx * RB;
@@ -647,16 +649,16 @@ attn_decode_mma_kernel(AttnArgs a, float scale_log2) {
         po[h * HD + dd] = O;
     }
     cluster_sync_all();
-    constexpr int OPB = kGQ * HD / kCL;
+    constexpr int OPB = kGQ * HD / CL;
     for (int idx = threadIdx.x; idx < OPB; idx += kMT) {
         const int oi = (int)rank * OPB + idx;
         const int h = oi / HD, dd = oi % HD;
         float M = -INFINITY;
 #pragma unroll
-        for (uint32_t r = 0; r < kCL; ++r) M = fmaxf(M, ld_peer(pm + h, r));
+        for (uint32_t r = 0; r < CL; ++r) M = fmaxf(M, ld_peer(pm + h, r));
         float L = 0.f, O = 0.f;
 #pragma unroll
-        for (uint32_t r = 0; r < kCL; ++r) {
+        for (uint32_t r = 0; r < CL; ++r) {
             const float mr = ld_peer(pm + h, r);
             const float f = (M == -INFINITY || mr == -INFINITY) ? 0.f : exp2f(mr - M);
             L = fmaf(f, ld_peer(pl + h, r), L);
@@ -667,11 +669,11 @@ attn_decode_mma_kernel(AttnArgs a, float scale_log2) {
     cluster_sync_all();
 }
 
-template <int HD, typename KT>
-bool launch_dec_mma(const AttnArgs& a, cudaStream_t st) {
+template <int HD, typename KT, int CL>
+bool launch_dec_mma_cl(const AttnArgs& a, cudaStream_t st) {
     const float scale_log2 = (float)(1.4426950408889634 / sqrt((double)HD));
     constexpr size_t smem = MmaDecSmem<HD, KT>::bytes;
-    auto k = attn_decode_mma_kernel<HD, KT>;
+    auto k = attn_decode_mma_kernel<HD, KT, CL>;
     static bool attr = false;
     if (!attr) {
         if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess ||
@@ -680,13 +682,13 @@ bool launch_dec_mma(const AttnArgs& a, cudaStream_t st) {
         attr = true;
     }
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(kCL, a.Hkv, a.n_tok);
+    cfg.gridDim = dim3(CL, a.Hkv, a.n_tok);
     cfg.blockDim = dim3(kMT);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
     cudaLaunchAttribute attr_l[2];
     attr_l[0].id = cudaLaunchAttributeClusterDimension;
-    attr_l[0].val.clusterDim.x = kCL;
+    attr_l[0].val.clusterDim.x = CL;
     attr_l[0].val.clusterDim.y = 1;
     attr_l[0].val.clusterDim.z = 1;
     attr_l[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -694,6 +696,22 @@ bool launch_dec_mma(const AttnArgs& a, cudaStream_t st) {
     cfg.attrs = attr_l;
     cfg.numAttrs = a.pdl ? 2 : 1;
     return cudaLaunchKernelEx(&cfg, k, a, scale_log2) == cudaSuccess;
+}
+
+// The cluster size: 16 unless 16 blocks per (token, KV head) would exceed two blocks per SM.
+template <int HD, typename KT>
+bool launch_dec_mma(const AttnArgs& a, cudaStream_t st) {
+    static int n_sm = 0;
+    if (n_sm == 0) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
+        if (n_sm <= 0) n_sm = 148;
+    }
+    const int64_t units = (int64_t)a.Hkv * a.n_tok;
+    if (16 * units <= 2 * n_sm) return launch_dec_mma_cl<HD, KT, 16>(a, st);
+    if (4 * units <= 2 * n_sm) return launch_dec_mma_cl<HD, KT, 4>(a, st);
+    return launch_dec_mma_cl<HD, KT, 1>(a, st);
 }
 
 template <int HD>
