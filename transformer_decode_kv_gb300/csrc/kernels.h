@@ -67,10 +67,6 @@ void launch_q8_0_to_f16_terms(const int8_t* q, const __half* d, int64_t rows, in
                               cudaStream_t st);
 // y[i] = f16(x[i]) for n bf16 values: exact for |x| in the f16 normal range [2^-14, 65504].
 void launch_bf16_to_f16(const void* x, int64_t n, void* y, cudaStream_t st);
-// Q8_0 weight [rows][cols] (int8 quants q, fp16 scales d per 32 values) -> two bf16 terms:
-// w = d * q (exact in float32), hi = bf16(w), lo = bf16(w - hi); hi + lo holds w to 16 bits.
-void launch_q8_0_to_bf16_terms(const int8_t* q, const __half* d, int64_t rows, int64_t cols, void* hi,
-                               void* lo, cudaStream_t st);
 // u[t][j] = silu(g[t][j]) * up[t][j] with gu = [T][2F] (gate then up) -> u [T][F].
 void launch_swiglu(const float* gu, int32_t T, int32_t F, float* u, cudaStream_t st);
 // amax[r] = the largest logit of row r packed with its index (value in the high word in an

@@ -183,16 +183,6 @@ __global__ void kv_gather_kernel(const U* __restrict__ src, U* __restrict__ dst,
     dst[((int64_t)g * n + r) * upr + u] = o >= 0 ? src[((int64_t)g * n_src + o) * upr + u] : U{};
 }
 
-__global__ void q8_0_terms_kernel(const int8_t* __restrict__ q, const __half* __restrict__ d, int64_t n,
-                                  __nv_bfloat16* __restrict__ hi, __nv_bfloat16* __restrict__ lo) {
-    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (i >= n) return;
-    const float w = __half2float(d[i / 32]) * (float)q[i];
-    const __nv_bfloat16 h = __float2bfloat16_rn(w);
-    hi[i] = h;
-    lo[i] = __float2bfloat16_rn(w - __bfloat162float(h));
-}
-
 __global__ void q8_0_f16_terms_kernel(const int8_t* __restrict__ q, const __half* __restrict__ d, int64_t n,
                                       __half* __restrict__ hi, __half* __restrict__ lo) {
     const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -374,14 +364,6 @@ void launch_bf16_to_f16(const void* x, int64_t n, void* y, cudaStream_t st) {
     if (n <= 0) return;
     bf16_to_f16_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(static_cast<const __nv_bfloat16*>(x), n,
                                                                      static_cast<__half*>(y));
-}
-
-void launch_q8_0_to_bf16_terms(const int8_t* q, const __half* d, int64_t rows, int64_t cols, void* hi,
-                               void* lo, cudaStream_t st) {
-    const int64_t n = rows * cols;
-    if (n <= 0) return;
-    q8_0_terms_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(q, d, n, static_cast<__nv_bfloat16*>(hi),
-                                                                    static_cast<__nv_bfloat16*>(lo));
 }
 
 void launch_swiglu(const float* gu, int32_t T, int32_t F, float* u, cudaStream_t st) {
