@@ -634,7 +634,7 @@ bool launch_gemm_swiglu_tn(const CUtensorMap& xmap, const CUtensorMap* xmap_lo, 
 int tc_tn_splits(int64_t M, int64_t K, int T, int n_sm) {
     const int64_t tiles = (T + kTnRows - 1) / kTnRows * (M / kTnN);
     int s = (int)std::max<int64_t>(1, n_sm / std::max<int64_t>(1, tiles));
-    s = std::min(s, 16);                           // one token tile (a multi-sequence step): many
+    s = std::min(s, 16);                           // a single token tile needs many to fill the SMs
     while (s > 1 && K / kBK / s < 8) --s;          // at least 8 k-steps per split
     return s;
 }
