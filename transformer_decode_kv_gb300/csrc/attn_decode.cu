@@ -312,10 +312,12 @@ struct MmaDecSmem {
     static constexpr size_t rows = 2 * (size_t)kCH * RSS;
     static constexpr size_t stage = rows + 3 * kCH * 4 + (Q8 ? 2 * (size_t)kCH * NB * 4 : 0);
     static constexpr size_t tile = Q8 ? 2 * (size_t)kCH * RS * 2 : 0;   // expanded K and V
+    // the warp states and the block partial reuse the stages once the passes are done, which
+    // keeps the block small enough for two blocks of the next GEMV beside it on an SM
+    static constexpr size_t states = (size_t)kMW * kGQ * (HD + 2) * 4 + (size_t)kGQ * (HD + 2) * 4;
+    static_assert(states <= 2 * stage, "states fit in the stage area");
     static constexpr size_t bytes = 2 * stage + tile + (size_t)kGQ * HD * 4 /* q */ +
-                                    (size_t)kMW * kMC * 8 * 4 /* P^T per warp */ +
-                                    (size_t)kMW * kGQ * (HD + 2) * 4 /* warp states */ +
-                                    (size_t)kGQ * (HD + 2) * 4 /* block partial */ + 16;
+                                    (size_t)kMW * kMC * 8 * 4 /* P^T per warp */ + 16;
 };
 
 // two int8 (low bytes of v, selected by sel) -> an exact half2: the biased byte as the low
@@ -352,7 +354,7 @@ attn_decode_mma_kernel(AttnArgs a, float scale_log2) {
     __half* tv = tk + kCH * RS;                                         //        and V tile
     float* qs = reinterpret_cast<float*>(sm + 2 * SM::stage + SM::tile);  // [kGQ][HD]
     float* pT = qs + kGQ * HD;                                          // [warp][16 cells][8]
-    float* ws = pT + kMW * kMC * 8;                                     // [warp][kGQ][HD + 2]
+    float* ws = reinterpret_cast<float*>(sm);                           // after the passes: [warp][kGQ][HD + 2]
     float* pst = ws + kMW * kGQ * (HD + 2);                             // block partial (peers read it)
 
     const uint32_t rank = cluster_rank();
