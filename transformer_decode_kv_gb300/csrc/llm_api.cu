@@ -439,17 +439,19 @@ struct OpPaths { bool qkv, wo, gu, down, lm; };
 
 OpPaths op_paths(llm_ctx* c, int32_t T, int32_t O) {
     OpPaths o{false, false, false, false, false};
-    if (!c->use_bulk || T > gemv_max_tokens()) return o;
+    if (!c->use_bulk) return o;
     const llm_hparams& h = c->hp;
     const Layer& L = c->layers[0];
     GemvArgs a;
+    // the output matrix sees only the O flagged rows: the GEMV serves it after a prefill too
+    a.T = std::max(O, 1); a.K = h.n_embd; a.M = h.n_vocab;
+    o.lm = O > 0 && O <= gemv_max_tokens() && gemv_bulk_ok(c->out.type, a, GEPI_LOGITS, c->n_sm);
+    if (T > gemv_max_tokens()) return o;
     a.T = T;
     a.K = h.n_embd; a.M = c->qkv_width(); o.qkv = gemv_bulk_ok(L.qkv.type, a, GEPI_QKV, c->n_sm);
     a.K = c->q_width(); a.M = h.n_embd; o.wo = gemv_bulk_ok(L.wo.type, a, GEPI_ADD, c->n_sm);
     a.K = h.n_embd; a.F = h.n_ff; o.gu = gemv_bulk_ok(L.gu.type, a, GEPI_SWIGLU, c->n_sm);
     a.K = h.n_ff; a.M = h.n_embd; o.down = gemv_bulk_ok(L.down.type, a, GEPI_ADD, c->n_sm);
-    a.T = std::max(O, 1); a.K = h.n_embd; a.M = h.n_vocab;
-    o.lm = O > 0 && O <= gemv_max_tokens() && gemv_bulk_ok(c->out.type, a, GEPI_LOGITS, c->n_sm);
     // every layer must share the types of layer 0 for the choice to hold
     for (int32_t il = 1; il < h.n_layer; ++il) {
         const Layer& M = c->layers[il];
