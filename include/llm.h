@@ -300,9 +300,12 @@ int64_t llm_debug_get_tensor(llm_ctx *ctx, const char *name, int32_t layer, floa
 /* Copy layer `layer`'s K cache (which = 0) or V cache (which = 1) to host memory as stored: type_k
  * / type_v elements laid out [n_head_kv][n_ctx][head_dim] (cell c of KV head g at (g * n_ctx + c)
  * * head_dim). A Q8_0 cache holds the int8 quants in that layout, followed by the fp16 scales
- * [n_head_kv][n_ctx][head_dim / 32] (one per 32-value block; value = scale * quant). out may be NULL to query the size. Returns the slab's size in bytes (copies at most
- * cap_bytes, after the context's stream has finished), 0 for a bad layer/which or a host-only
- * context. */
+ * [n_head_kv][n_ctx][head_dim / 32] (one per 32-value block; value = scale * quant). which = 2 / 3
+ * (Q8_0 caches only; layer ignored beyond its range check): the f16 copy of the K / V quants, same
+ * layout, that the last attention over query tiles of several tokens read (the last layer of the
+ * last such ubatch), valid for the cells below that ubatch's n_kv. out may be NULL to query the size.
+ * Returns the slab's size in bytes (copies at most cap_bytes, after the context's stream has
+ * finished), 0 for a bad layer/which or a host-only context. */
 int64_t llm_debug_kv_raw(llm_ctx *ctx, int32_t layer, int32_t which, void *out, int64_t cap_bytes);
 
 /* Per-kernel-class device timing. enable != 0 resets the counters and brackets every later launch

@@ -9,6 +9,8 @@
     in different precisions (float32 here, float64 in the oracle): a value whose product lies
     within rounding of a half-integer lands one quantisation step (max|x| / 127 of its block)
     apart, which moves a logit by far more than float32 rounding does.
+  - The f16 copy of the quants the tensor-core prefill tiles read (they apply the scales): every
+    used cell's int8 quants, bit-exact.
   - The Llama-3-8B shape (head_dim 128) at full size: layers checked one by one on the library's
     own inputs and dequantised cache (the F16 path's 2e-2 bar).
 """
@@ -76,6 +78,22 @@ def test_tiny_8seq_q8_0_cache_batched():
     rep = G.greedy_compare(ctx, ora, w.n_seq, rows, 16, TOL, {})
     print("tiny 8-seq Q8_0 cache:", rep)
     assert rep["tokens_checked"] >= 50
+    ctx.free()
+
+
+def test_prefill_tiles_read_the_exact_quants():
+    key = "tiny_f32_8seq"
+    ctx = G.library_ctx(key, type_k=Q8_0, type_v=Q8_0)
+    hp = ctx._hp
+    Hkv, hd = hp.n_head_kv, hp.head_dim
+    toks, seqs, flags = G.prompt_batch(key)
+    assert ctx.decode(toks, seq_ids=seqs, logits=flags) == 0, ctx.last_error()
+    used = np.unique(ctx.last_slots())
+    for which in (0, 1):
+        blocks = ctx.kv_cache(hp.n_layer - 1, which)            # the copy holds the last layer
+        q = blocks.reshape(Hkv, -1, hd // 32, 34)[:, :, :, 2:].view(np.int8).reshape(Hkv, -1, hd)
+        got = ctx.kv_f16_copy(which)[:, used]
+        assert np.array_equal(got.astype(np.float64), q[:, used].astype(np.float64)), which
     ctx.free()
 
 

@@ -353,6 +353,17 @@ class Context:
         v = out.view(np.float32 if es == 4 else np.float16)
         return v.reshape(self._hp.n_head_kv, -1, self._hp.head_dim)
 
+    def kv_f16_copy(self, which: int) -> Optional[np.ndarray]:
+        """Q8_0 caches: the f16 copy of the K (which 0) or V (which 1) quants that the last
+        attention over query tiles of several tokens read, float16 [n_head_kv][n_ctx][head_dim]
+        (cells below that ubatch's n_kv are valid)."""
+        n = lib().llm_debug_kv_raw(self.ptr, 0, which + 2, None, 0)
+        if n <= 0:
+            return None
+        out = np.zeros(n, dtype=np.uint8)
+        lib().llm_debug_kv_raw(self.ptr, 0, which + 2, out.ctypes.data_as(C.c_void_p), n)
+        return out.view(np.float16).reshape(self._hp.n_head_kv, -1, self._hp.head_dim)
+
     def step_trace_enable(self, enable: bool = True) -> int:
         return lib().llm_debug_step_trace_enable(self.ptr, int(enable))
 

@@ -13,6 +13,12 @@
 // visible to a row iff cell.pos <= token.pos (the list already holds only the sequence's cells).
 // Partial states (o, m, l) and the ticket merge are shared with the CUDA-core kernel.
 //
+// A Q8_0 cache ([P2] Example 2 blocks: value d * q per 32 values) comes as f16 copies of its
+// int8 quants (exact) plus the cache's fp16 scales, gathered with the rows. K: each 32-dim block's
+// Q . q products accumulate apart and join S times that block's d of the cell. V: the scale
+// varies along the contracted cells, so each 32-dim block of the output takes P times the cells'
+// d of that block, split into two f16 terms as P is. The values d * q are never rounded.
+//
 // mma.sync is enough here: a 512-token ubatch of the 8B shape has 2.1 GFLOP of attention per
 // layer, 1% of its matrix work, and this kernel moves it off the CUDA cores.
 #include <cuda_bf16.h>
@@ -38,20 +44,46 @@ constexpr int kTQ = 16;                    // tokens per query tile
 constexpr int kRows = kTQ * kG;            // 64 rows: one m16 fragment row block per warp
 
 
-template <int HD>
+template <int HD, bool Q8>
 struct MmaSmem {
     static constexpr int RS = HD + 8;                       // padded row (halves): no bank conflicts
+    static constexpr int NB = HD / 32;                      // Q8_0 blocks per row
     static constexpr size_t tile_bytes = (size_t)kTC * RS * 2;
     static constexpr size_t q_bytes = (size_t)kRows * RS * 2;      // one f16 term of the Q tile
-    static constexpr size_t bytes = 4 * tile_bytes + 2 * q_bytes + 4 * kTC * 4 + 8 * 4 + 2 * kRows * 4 + 16;
+    static constexpr size_t base_bytes = 4 * tile_bytes + 2 * q_bytes + 4 * kTC * 4 + 8 * 4 + 2 * kRows * 4 + 16;
+    static constexpr size_t sc_off = (base_bytes + 15) / 16 * 16;
+    static constexpr size_t sc_tile = (size_t)kTC * NB;    // halves: one tile's K (or V) scales
+    static constexpr size_t bytes = Q8 ? sc_off + 4 * sc_tile * 2 : base_bytes;
 };
 
 // Issue the gathers of one tile into buffer (ks, vs): cell indices from shared memory (ccell,
-// -1 = none), zeros for missing cells.
-template <int HD>
+// -1 = none), zeros for missing cells. Q8: also the cells' scales (KS, VS) into (kd, vd).
+template <int HD, bool Q8>
 __device__ __forceinline__ void gather_tile(const __half* K, const __half* V, const int* ccell,
-                                            __half* ks, __half* vs) {
-    constexpr int RS = MmaSmem<HD>::RS, VPR = HD / 8;
+                                            __half* ks, __half* vs, const __half* KS = nullptr,
+                                            const __half* VS = nullptr, __half* kd = nullptr,
+                                            __half* vd = nullptr) {
+    constexpr int RS = MmaSmem<HD, Q8>::RS, VPR = HD / 8, NB = HD / 32;
+    if constexpr (Q8) {
+        if (threadIdx.x < 2 * kTC) {
+            const int c = threadIdx.x % kTC;
+            const bool isv = threadIdx.x >= kTC;
+            const int cell = ccell[c];
+            __half* dst = (isv ? vd : kd) + c * NB;
+            if (cell >= 0) {
+                const __half* src = (isv ? VS : KS) + (int64_t)cell * NB;
+                if constexpr (NB >= 2) {
+                    asm volatile("cp.async.ca.shared.global [%0], [%1], %2;" ::"r"(smem_addr(dst)), "l"(src),
+                                 "n"(NB * 2) : "memory");
+                } else {
+                    *dst = *src;
+                }
+            } else {
+#pragma unroll
+                for (int b = 0; b < NB; ++b) dst[b] = __float2half(0.f);
+            }
+        }
+    }
     for (int v = threadIdx.x; v < kTC * VPR; v += kWarps * 32) {
         const int c = v / VPR, j = v % VPR;
         const int cell = ccell[c];
@@ -94,10 +126,10 @@ __device__ __forceinline__ void store_index(int cell, int pos, int* ccell, int* 
 
 }  // namespace
 
-template <int HD>
+template <int HD, bool Q8>
 __global__ void __launch_bounds__(kWarps * 32, 2) attn_mma_kernel(AttnArgs a, float scale_log2) {
-    using SM = MmaSmem<HD>;
-    constexpr int RS = SM::RS, KC = HD / 16, NC = HD / 8;
+    using SM = MmaSmem<HD, Q8>;
+    constexpr int RS = SM::RS, KC = HD / 16, NC = HD / 8, NB = SM::NB;
     extern __shared__ __align__(16) uint8_t smem[];
     __half* kbuf[2] = {reinterpret_cast<__half*>(smem), reinterpret_cast<__half*>(smem + SM::tile_bytes)};
     __half* vbuf[2] = {reinterpret_cast<__half*>(smem + 2 * SM::tile_bytes),
@@ -111,6 +143,8 @@ __global__ void __launch_bounds__(kWarps * 32, 2) attn_mma_kernel(AttnArgs a, fl
     int* rpos = cminb + 8;                                                // [kRows]
     int* rtok = rpos + kRows;                                             // [kRows] token row of q
     int* flag = rtok + kRows;
+    // Q8: [2 buffers][K, V][kTC][NB] scales
+    __half* scb = reinterpret_cast<__half*>(smem + SM::sc_off);
 
     const int wi = blockIdx.x, kvh = blockIdx.y;
     if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;");
@@ -124,6 +158,10 @@ __global__ void __launch_bounds__(kWarps * 32, 2) attn_mma_kernel(AttnArgs a, fl
     const int nq = td0.z, s0 = td0.y, c0 = wd.y, c1 = wd.z, base = td1.y;
     const __half* K = static_cast<const __half*>(a.kc) + (int64_t)kvh * a.n_ctx * HD;
     const __half* V = static_cast<const __half*>(a.vc) + (int64_t)kvh * a.n_ctx * HD;
+    const __half* KS = Q8 ? static_cast<const __half*>(a.k_scale) + (int64_t)kvh * a.n_ctx * NB : nullptr;
+    const __half* VS = Q8 ? static_cast<const __half*>(a.v_scale) + (int64_t)kvh * a.n_ctx * NB : nullptr;
+    auto ksc = [&](int b) { return scb + (2 * b) * SM::sc_tile; };       // buffer b's K scales
+    auto vsc = [&](int b) { return scb + (2 * b + 1) * SM::sc_tile; };
     asm volatile("griddepcontrol.wait;" ::: "memory");
 
     // tile 0: indices, then its gathers; tile 1's indices are loaded while tile 0 is used
@@ -137,7 +175,7 @@ __global__ void __launch_bounds__(kWarps * 32, 2) attn_mma_kernel(AttnArgs a, fl
         rpos[r] = t >= 0 ? a.tok_pos[t] : -1;
     }
     __syncthreads();
-    gather_tile<HD>(K, V, ccellb, kbuf[0], vbuf[0]);
+    gather_tile<HD, Q8>(K, V, ccellb, kbuf[0], vbuf[0], KS, VS, ksc(0), vsc(0));
     load_index(a, base, c0 + kTC, c1, ncell, npos);
     if (threadIdx.x < 32) {
         int mx = -1;
@@ -189,7 +227,8 @@ __global__ void __launch_bounds__(kWarps * 32, 2) attn_mma_kernel(AttnArgs a, fl
         if (more) {
             store_index(ncell, npos, ccellb + (buf ^ 1) * kTC, cposb + (buf ^ 1) * kTC, cminb + (buf ^ 1) * 2);
             __syncthreads();
-            gather_tile<HD>(K, V, ccellb + (buf ^ 1) * kTC, kbuf[buf ^ 1], vbuf[buf ^ 1]);
+            gather_tile<HD, Q8>(K, V, ccellb + (buf ^ 1) * kTC, kbuf[buf ^ 1], vbuf[buf ^ 1], KS, VS,
+                                ksc(buf ^ 1), vsc(buf ^ 1));
             load_index(a, base, cb + 2 * kTC, c1, ncell, npos);
             asm volatile("cp.async.wait_group 1;" ::: "memory");
         } else {
@@ -206,8 +245,7 @@ __global__ void __launch_bounds__(kWarps * 32, 2) attn_mma_kernel(AttnArgs a, fl
         float s[8][4];
 #pragma unroll
         for (int n = 0; n < 8; ++n) s[n][0] = s[n][1] = s[n][2] = s[n][3] = 0.f;
-#pragma unroll
-        for (int kc = 0; kc < KC; ++kc) {
+        auto qk = [&](float (&acc)[8][4], int kc) {
             uint32_t qh[4], ql[4];
             ldsm_x4(smem_addr(qhs + qrow * RS + kc * 16 + qcol), qh[0], qh[1], qh[2], qh[3]);
             ldsm_x4(smem_addr(qls + qrow * RS + kc * 16 + qcol), ql[0], ql[1], ql[2], ql[3]);
@@ -224,14 +262,38 @@ __global__ void __launch_bounds__(kWarps * 32, 2) attn_mma_kernel(AttnArgs a, fl
             }
 #pragma unroll
             for (int n2 = 0; n2 < 4; ++n2) {
-                mma16816(s[2 * n2], qh, kb[n2][0], kb[n2][1]);
-                mma16816(s[2 * n2 + 1], qh, kb[n2][2], kb[n2][3]);
+                mma16816(acc[2 * n2], qh, kb[n2][0], kb[n2][1]);
+                mma16816(acc[2 * n2 + 1], qh, kb[n2][2], kb[n2][3]);
             }
 #pragma unroll
             for (int n2 = 0; n2 < 4; ++n2) {
-                mma16816(s[2 * n2], ql, kb[n2][0], kb[n2][1]);
-                mma16816(s[2 * n2 + 1], ql, kb[n2][2], kb[n2][3]);
+                mma16816(acc[2 * n2], ql, kb[n2][0], kb[n2][1]);
+                mma16816(acc[2 * n2 + 1], ql, kb[n2][2], kb[n2][3]);
             }
+        };
+        if constexpr (Q8) {
+            // per 32-dim block: the quants' products, then times the block's d of each cell
+            const __half* kd = ksc(buf);
+#pragma unroll
+            for (int b = 0; b < NB; ++b) {
+                float t[8][4];
+#pragma unroll
+                for (int n = 0; n < 8; ++n) t[n][0] = t[n][1] = t[n][2] = t[n][3] = 0.f;
+                qk(t, 2 * b);
+                qk(t, 2 * b + 1);
+#pragma unroll
+                for (int n = 0; n < 8; ++n) {
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const float dk = __half2float(kd[(8 * n + 2 * t4 + e) * NB + b]);
+                        s[n][e] = fmaf(t[n][e], dk, s[n][e]);
+                        s[n][2 + e] = fmaf(t[n][2 + e], dk, s[n][2 + e]);
+                    }
+                }
+            }
+        } else {
+#pragma unroll
+            for (int kc = 0; kc < KC; ++kc) qk(s, kc);
         }
         // mask and online softmax (rows r0, r1; this thread's columns 2 t4, 2 t4 + 1 of each
         // fragment; the row's other columns live in the same quad)
@@ -277,35 +339,73 @@ __global__ void __launch_bounds__(kWarps * 32, 2) attn_mma_kernel(AttnArgs a, fl
             o[n][2] *= cr1; o[n][3] *= cr1;
         }
         // O += P V: P's accumulator layout is the A layout of the next MMA (16 cells per step)
+        if constexpr (Q8) {
+            // this thread's cells of step kk: 16 kk + 2 t4 + {0, 1} (A registers 0, 1) and
+            // 16 kk + 8 + 2 t4 + {0, 1} (registers 2, 3)
+            const __half* vd = vsc(buf);
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-            uint32_t ph[4], pl[4];
-            split_h2(s[2 * kk][0], s[2 * kk][1], ph[0], pl[0]);
-            split_h2(s[2 * kk][2], s[2 * kk][3], ph[1], pl[1]);
-            split_h2(s[2 * kk + 1][0], s[2 * kk + 1][1], ph[2], pl[2]);
-            split_h2(s[2 * kk + 1][2], s[2 * kk + 1][3], ph[3], pl[3]);
-            constexpr int GS = NC / 2 < 4 ? NC / 2 : 4;          // dimension blocks per group
+            for (int kk = 0; kk < 4; ++kk) {
+                const int ca = 16 * kk + 2 * t4;
 #pragma unroll
-            for (int h4 = 0; h4 < NC / 2; h4 += GS) {
-                uint32_t vb[GS][4];
+                for (int b = 0; b < NB; ++b) {
+                    const float d0 = __half2float(vd[ca * NB + b]), d1 = __half2float(vd[(ca + 1) * NB + b]);
+                    const float d2 = __half2float(vd[(ca + 8) * NB + b]), d3 = __half2float(vd[(ca + 9) * NB + b]);
+                    uint32_t ph[4], pl[4];
+                    split_h2(s[2 * kk][0] * d0, s[2 * kk][1] * d1, ph[0], pl[0]);
+                    split_h2(s[2 * kk][2] * d0, s[2 * kk][3] * d1, ph[1], pl[1]);
+                    split_h2(s[2 * kk + 1][0] * d2, s[2 * kk + 1][1] * d3, ph[2], pl[2]);
+                    split_h2(s[2 * kk + 1][2] * d2, s[2 * kk + 1][3] * d3, ph[3], pl[3]);
+                    uint32_t vb[2][4];
 #pragma unroll
-                for (int i = 0; i < GS; ++i) {
-                    // matrices (transposed): (cells 16 kk + 0..7, dims 16 n2 + 0..7), (cells +8,
-                    // same dims), (cells 16 kk, dims +8), (cells +8, dims +8)
-                    const int n2 = h4 + i;
-                    const int cell = 16 * kk + (lane & 7) + (((lane >> 3) & 1) << 3);
-                    const int dim = 16 * n2 + ((lane >> 4) << 3);
-                    ldsm_x4_t(smem_addr(vs + cell * RS + dim), vb[i][0], vb[i][1], vb[i][2], vb[i][3]);
+                    for (int i = 0; i < 2; ++i) {
+                        const int n2 = 2 * b + i;                 // 16-dim groups of block b
+                        const int cell = 16 * kk + (lane & 7) + (((lane >> 3) & 1) << 3);
+                        const int dim = 16 * n2 + ((lane >> 4) << 3);
+                        ldsm_x4_t(smem_addr(vs + cell * RS + dim), vb[i][0], vb[i][1], vb[i][2], vb[i][3]);
+                    }
+#pragma unroll
+                    for (int i = 0; i < 2; ++i) {
+                        mma16816(o[2 * (2 * b + i)], ph, vb[i][0], vb[i][1]);
+                        mma16816(o[2 * (2 * b + i) + 1], ph, vb[i][2], vb[i][3]);
+                    }
+#pragma unroll
+                    for (int i = 0; i < 2; ++i) {
+                        mma16816(o[2 * (2 * b + i)], pl, vb[i][0], vb[i][1]);
+                        mma16816(o[2 * (2 * b + i) + 1], pl, vb[i][2], vb[i][3]);
+                    }
                 }
+            }
+        } else {
 #pragma unroll
-                for (int i = 0; i < GS; ++i) {
-                    mma16816(o[2 * (h4 + i)], ph, vb[i][0], vb[i][1]);
-                    mma16816(o[2 * (h4 + i) + 1], ph, vb[i][2], vb[i][3]);
-                }
+            for (int kk = 0; kk < 4; ++kk) {
+                uint32_t ph[4], pl[4];
+                split_h2(s[2 * kk][0], s[2 * kk][1], ph[0], pl[0]);
+                split_h2(s[2 * kk][2], s[2 * kk][3], ph[1], pl[1]);
+                split_h2(s[2 * kk + 1][0], s[2 * kk + 1][1], ph[2], pl[2]);
+                split_h2(s[2 * kk + 1][2], s[2 * kk + 1][3], ph[3], pl[3]);
+                constexpr int GS = NC / 2 < 4 ? NC / 2 : 4;          // dimension blocks per group
 #pragma unroll
-                for (int i = 0; i < GS; ++i) {
-                    mma16816(o[2 * (h4 + i)], pl, vb[i][0], vb[i][1]);
-                    mma16816(o[2 * (h4 + i) + 1], pl, vb[i][2], vb[i][3]);
+                for (int h4 = 0; h4 < NC / 2; h4 += GS) {
+                    uint32_t vb[GS][4];
+#pragma unroll
+                    for (int i = 0; i < GS; ++i) {
+                        // matrices (transposed): (cells 16 kk + 0..7, dims 16 n2 + 0..7), (cells +8,
+                        // same dims), (cells 16 kk, dims +8), (cells +8, dims +8)
+                        const int n2 = h4 + i;
+                        const int cell = 16 * kk + (lane & 7) + (((lane >> 3) & 1) << 3);
+                        const int dim = 16 * n2 + ((lane >> 4) << 3);
+                        ldsm_x4_t(smem_addr(vs + cell * RS + dim), vb[i][0], vb[i][1], vb[i][2], vb[i][3]);
+                    }
+#pragma unroll
+                    for (int i = 0; i < GS; ++i) {
+                        mma16816(o[2 * (h4 + i)], ph, vb[i][0], vb[i][1]);
+                        mma16816(o[2 * (h4 + i) + 1], ph, vb[i][2], vb[i][3]);
+                    }
+#pragma unroll
+                    for (int i = 0; i < GS; ++i) {
+                        mma16816(o[2 * (h4 + i)], pl, vb[i][0], vb[i][1]);
+                        mma16816(o[2 * (h4 + i) + 1], pl, vb[i][2], vb[i][3]);
+                    }
                 }
             }
         }
@@ -362,11 +462,11 @@ __global__ void __launch_bounds__(kWarps * 32, 2) attn_mma_kernel(AttnArgs a, fl
     merge_tile<HD, kG>(a, kvh, s0, nq, w0, w1, reinterpret_cast<float*>(smem), 4 * SM::tile_bytes / 4);
 }
 
-template <int HD>
+template <int HD, bool Q8>
 bool launch_attention_mma_hd(const AttnArgs& a, cudaStream_t st) {
     const float scale_log2 = (float)(1.4426950408889634 / sqrt((double)HD));
-    constexpr size_t smem = MmaSmem<HD>::bytes;
-    auto k = attn_mma_kernel<HD>;
+    constexpr size_t smem = MmaSmem<HD, Q8>::bytes;
+    auto k = attn_mma_kernel<HD, Q8>;
     static bool attr = false;
     if (!attr) {
         if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
@@ -387,14 +487,23 @@ bool launch_attention_mma_hd(const AttnArgs& a, cudaStream_t st) {
 }
 
 bool attention_mma_ok(const AttnArgs& a) {
-    return a.kv_type == W_F16 && a.H == kG * a.Hkv && (a.hd == 32 || a.hd == 64 || a.hd == 128);
+    const bool kv = a.kv_type == W_F16 || (a.kv_type == W_Q8_0 && a.k_scale && a.v_scale);
+    return kv && a.H == kG * a.Hkv && (a.hd == 32 || a.hd == 64 || a.hd == 128);
 }
 
 bool launch_attention_mma(const AttnArgs& a, cudaStream_t st) {
+    if (a.kv_type == W_Q8_0) {
+        switch (a.hd) {
+            case 32: return launch_attention_mma_hd<32, true>(a, st);
+            case 64: return launch_attention_mma_hd<64, true>(a, st);
+            case 128: return launch_attention_mma_hd<128, true>(a, st);
+        }
+        return false;
+    }
     switch (a.hd) {
-        case 32: return launch_attention_mma_hd<32>(a, st);
-        case 64: return launch_attention_mma_hd<64>(a, st);
-        case 128: return launch_attention_mma_hd<128>(a, st);
+        case 32: return launch_attention_mma_hd<32, false>(a, st);
+        case 64: return launch_attention_mma_hd<64, false>(a, st);
+        case 128: return launch_attention_mma_hd<128, false>(a, st);
     }
     return false;
 }

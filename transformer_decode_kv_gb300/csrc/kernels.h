@@ -53,6 +53,12 @@ void launch_kv_quant_q8(const float* sk, const float* sv, int32_t ld, int32_t T,
 __host__ __device__ inline size_t kv_q8_scale_offset(int32_t Hkv, int32_t n_ctx, int32_t hd) {
     return (size_t)Hkv * (size_t)n_ctx * (size_t)hd;
 }
+// The int8 quants of every cell below *n_kv (a device word) of one layer's Q8_0 K and V caches as
+// f16 (exact) into out = [2][Hkv][n_ctx][hd] (K then V, the F16 cache layout): the tensor-core
+// prefill tiles read a Q8_0 cache through this copy and apply the fp16 scales of the cache
+// themselves. Cells at or above *n_kv are not written.
+void launch_kv_q8_to_f16(const void* kc, const void* vc, void* out, int32_t Hkv, int32_t n_ctx,
+                         int32_t hd, const int32_t* n_kv, cudaStream_t st);
 // dst[g][i] = src[g][order[i]] for g < n_head (grid y), i < n (zero where order[i] < 0): rows of
 // row_bytes (a multiple of 2), src rows strided by n_src rows per head, dst rows packed n per
 // head. Used by the defrag to gather one cache region in the new cell order.
@@ -112,6 +118,10 @@ struct AttnArgs {
     int32_t ldq;
     const void* kc;          // this layer's K cache [Hkv][n_ctx][hd]
     const void* vc;
+    // Q8_0 caches, query tiles of several tokens: kc / vc are f16 copies of the quants and these
+    // the cache's fp16 scales [Hkv][n_ctx][hd / 32] (null otherwise)
+    const void* k_scale = nullptr;
+    const void* v_scale = nullptr;
     int32_t n_ctx, kv_type, H, Hkv, hd;
     const int32_t* tok_pos;  // [T]
     const int32_t* list_cells; const int32_t* list_pos;   // concatenated cell lists
@@ -158,8 +168,9 @@ size_t sample_state_bytes();
 // One cooperative launch over up to 64 blocks (more for rows above 64 x 4096 values); false if
 // the row is too long for the SM count or the launch failed.
 bool launch_sample(const SampleArgs& a, void* state, int n_sm, cudaStream_t st);
-// The prefill tiles (16 tokens x 4 query heads) on tensor cores (attn_mma.cu): F16 KV, 4 query
-// heads per KV head, head_dim 32, 64 or 128. launch_attention uses it when it applies.
+// The prefill tiles (16 tokens x 4 query heads) on tensor cores (attn_mma.cu): F16 KV, or a Q8_0
+// cache through its f16 quant copy and scales (k_scale / v_scale), 4 query heads per KV head,
+// head_dim 32, 64 or 128. launch_attention uses it when it applies.
 bool attention_mma_ok(const AttnArgs& a);
 bool launch_attention_mma(const AttnArgs& a, cudaStream_t st);
 // Decode steps (one token per query tile) with a 16-block cluster per (token, KV head) merging

@@ -477,6 +477,7 @@ bool launch_hd_g(const AttnArgs& a, cudaStream_t st) {
         return a.slot && a.kv_type != W_Q8_0 ? launch_step<HD, G>(a, st) : launch_tq<HD, 1, G>(a, st);
     }
     if (attention_mma_ok(a)) return launch_attention_mma(a, st);
+    if (a.k_scale) return false;                   // the quant copies are for the tensor-core tiles
     return launch_tq<HD, kAttnTileQ, G>(a, st);
 }
 

@@ -172,6 +172,33 @@ __global__ void kv_quant_q8_kernel(const float* __restrict__ sk, const float* __
     }
 }
 
+// One thread per 8 values of a cell row: an 8-byte load of quants, one 16-byte store of f16.
+__global__ void kv_q8_to_f16_kernel(const int8_t* __restrict__ kc, const int8_t* __restrict__ vc,
+                                    __half* __restrict__ out, int Hkv, int n_ctx, int hd,
+                                    const int32_t* __restrict__ n_kv) {
+    const int upr = hd / 8;
+    const int64_t n = (int64_t)Hkv * n_ctx * upr;
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= n) return;
+    const int64_t row = i / upr;                                  // g * n_ctx + cell
+    if ((int)(row % n_ctx) >= __ldg(n_kv)) return;
+    const int j = (int)(i % upr);
+    const bool is_v = blockIdx.y != 0;
+    const int8_t* q = is_v ? vc : kc;
+    const uint2 raw = __ldg(reinterpret_cast<const uint2*>(q + row * hd + j * 8));
+    uint32_t w[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const uint32_t src = k < 2 ? raw.x : raw.y;
+        const int sh = (k & 1) * 16;
+        const float a = (float)(int8_t)((src >> sh) & 0xffu), b = (float)(int8_t)((src >> (sh + 8)) & 0xffu);
+        const __half2 h = __floats2half2_rn(a, b);
+        w[k] = *reinterpret_cast<const uint32_t*>(&h);
+    }
+    __half* o = out + (is_v ? (int64_t)Hkv * n_ctx * hd : 0) + row * hd + j * 8;
+    *reinterpret_cast<uint4*>(o) = make_uint4(w[0], w[1], w[2], w[3]);
+}
+
 template <typename U>
 __global__ void kv_gather_kernel(const U* __restrict__ src, U* __restrict__ dst,
                                  const int32_t* __restrict__ order, int n, int n_src, int upr) {
@@ -321,6 +348,15 @@ void launch_kv_quant_q8(const float* sk, const float* sv, int32_t ld, int32_t T,
     cfg.numAttrs = pdl ? 1 : 0;
     cudaLaunchKernelEx(&cfg, kv_quant_q8_kernel, sk, sv, (int)ld, (int)Hkv, (int)hd, slot,
                        static_cast<int8_t*>(kc), static_cast<int8_t*>(vc), (int)n_ctx, err);
+}
+
+void launch_kv_q8_to_f16(const void* kc, const void* vc, void* out, int32_t Hkv, int32_t n_ctx,
+                         int32_t hd, const int32_t* n_kv, cudaStream_t st) {
+    const int64_t n = (int64_t)Hkv * n_ctx * (hd / 8);
+    if (n <= 0) return;
+    const dim3 grid((unsigned)((n + 255) / 256), 2);
+    kv_q8_to_f16_kernel<<<grid, 256, 0, st>>>(static_cast<const int8_t*>(kc), static_cast<const int8_t*>(vc),
+                                              static_cast<__half*>(out), (int)Hkv, (int)n_ctx, (int)hd, n_kv);
 }
 
 void launch_kv_gather(const void* src, void* dst, const int32_t* order, int32_t n, int32_t n_head,

@@ -117,6 +117,7 @@ struct llm_ctx {
     void* kv_k = nullptr;
     void* kv_v = nullptr;
     float* kv_stage = nullptr;                 // Q8_0: this ubatch's K and V rows, [2][Hkv][n_ubatch][hd]
+    uint16_t* kv_f16 = nullptr;                // Q8_0: one layer's cache as f16 values, [2][Hkv][n_ctx][hd]
     uint8_t* kv_scratch = nullptr;             // defrag: one cache region's moved rows
     int32_t* d_order = nullptr;                // defrag: old cell of each new cell
     KvCells cells;
@@ -411,7 +412,8 @@ void put(int32_t* base, size_t off, const std::vector<int32_t>& v) {
 void attention_work(llm_ctx* c, const int32_t* pos) {
     const AttnPlan& p = c->plan;
     const llm_hparams& hp = c->hp;
-    const double kv_es = c->kv_value_bytes();
+    // multi-token tiles over a Q8_0 cache read the f16 copy of its quants and its scales
+    const double kv_es = c->kv_q8() && p.max_nq > 1 ? 2.0 + 2.0 / 32.0 : c->kv_value_bytes();
     double by = 0, fl = 0;
     for (int32_t t = 0; t < p.n_tiles(); ++t) {
         const int32_t l = p.tile_list[t];
@@ -617,6 +619,19 @@ bool forward_ubatch(llm_ctx* c, int32_t T, int32_t O, int32_t out_row0, int32_t 
         // ---- attention over the cache
         a.kc = kc;
         a.vc = vc;
+        a.k_scale = a.v_scale = nullptr;
+        if (q8 && max_nq > 1) {
+            // query tiles of several tokens run on tensor cores over f16 copies of the quants of
+            // the cells in use and the cache's own scales; one-token tiles read the blocks directly
+            const double nkv = c->cells.n_kv();
+            k = kt_begin(c);
+            launch_kv_q8_to_f16(kc, vc, c->kv_f16, Hkv, c->n_ctx, hd, din + io.hdr + 2, st);
+            kt_end(c, k, KC_ROPE_KV, nkv * 2.0 * Hkv * hd * 3.0, 0);
+            a.kc = c->kv_f16;
+            a.vc = c->kv_f16 + (size_t)Hkv * c->n_ctx * hd;
+            a.k_scale = static_cast<const uint8_t*>(kc) + kv_q8_scale_offset(Hkv, c->n_ctx, hd);
+            a.v_scale = static_cast<const uint8_t*>(vc) + kv_q8_scale_offset(Hkv, c->n_ctx, hd);
+        }
         k = kt_begin(c);
         if (!launch_attention(a, st)) { c->err = "attention shape not supported"; return false; }
         kt_end(c, k, KC_ATTENTION, -1.0, 0);
@@ -817,6 +832,7 @@ llm_ctx* llm_ctx_init(const llm_hparams* hp, const llm_cparams* cp) {
     bool ok = dalloc(c, reinterpret_cast<uint8_t**>(&c->kv_k), kv_bytes) &&
               dalloc(c, reinterpret_cast<uint8_t**>(&c->kv_v), kv_bytes) &&
               (!c->kv_q8() || dalloc(c, &c->kv_stage, 2 * (size_t)h.n_head_kv * U * h.head_dim)) &&
+              (!c->kv_q8() || dalloc(c, &c->kv_f16, 2 * (size_t)h.n_head_kv * c->n_ctx * h.head_dim)) &&
               dalloc(c, &c->x, U * d) && dalloc(c, &c->h, U * d) &&
               dalloc(c, &c->qkv, U * c->qkv_width()) && dalloc(c, &c->attn, U * c->q_width()) &&
               dalloc(c, &c->u, U * h.n_ff) && dalloc(c, &c->tmp, U * 2 * (int64_t)h.n_ff) &&
@@ -1264,6 +1280,7 @@ int32_t llm_decode(llm_ctx* c, llm_batch bt) {
         int32_t* hi = c->h_in;
         hi[io.hdr + 0] = p.n_work();
         hi[io.hdr + 1] = p.n_tiles();
+        hi[io.hdr + 2] = c->cells.n_kv();
         std::memcpy(hi + io.tok, b.token.data() + i0, T * sizeof(int32_t));
         std::memcpy(hi + io.pos, b.pos.data() + i0, T * sizeof(int32_t));
         std::memcpy(hi + io.slot, us.data(), T * sizeof(int32_t));
@@ -1537,11 +1554,13 @@ int64_t llm_debug_get_tensor(llm_ctx* c, const char* name, int32_t layer, float*
 }
 
 int64_t llm_debug_kv_raw(llm_ctx* c, int32_t layer, int32_t which, void* out, int64_t cap_bytes) {
-    if (!c || c->host_only || layer < 0 || layer >= c->hp.n_layer || (which != 0 && which != 1))
-        return 0;
-    const int64_t n = (int64_t)c->kv_layer_bytes();
+    if (!c || c->host_only || layer < 0 || layer >= c->hp.n_layer || which < 0 || which > 3) return 0;
+    if (which >= 2 && !c->kv_f16) return 0;
+    const int64_t n = which >= 2 ? (int64_t)c->hp.n_head_kv * c->n_ctx * c->hp.head_dim * 2
+                                 : (int64_t)c->kv_layer_bytes();
     if (out && cap_bytes > 0) {
-        const uint8_t* src = static_cast<const uint8_t*>(which == 0 ? c->kv_k : c->kv_v) + (size_t)layer * n;
+        const uint8_t* src = which >= 2 ? reinterpret_cast<const uint8_t*>(c->kv_f16) + (size_t)(which - 2) * n
+                           : static_cast<const uint8_t*>(which == 0 ? c->kv_k : c->kv_v) + (size_t)layer * n;
         cudaStreamSynchronize(c->st);
         cudaMemcpy(out, src, (size_t)std::min(n, cap_bytes), cudaMemcpyDeviceToHost);
     }
