@@ -146,14 +146,16 @@ def test_error_paths_on_gpu():
     ctx.free(); ref.free()
 
 
+@pytest.mark.parametrize("n_prompt", [1000, 2000, 3500])
 @pytest.mark.parametrize("tkv", [oracle.F16, oracle.Q8_0])
-def test_tiny_long_context_decode(tkv):
-    """A 2000-token prompt (several 64-cell passes per block of the decode attention, both warp
-    groups busy) then greedy steps, against the oracle; F16 and Q8_0 caches."""
+def test_tiny_long_context_decode(tkv, n_prompt):
+    """A long prompt then greedy steps, against the oracle; F16 and Q8_0 caches. The decode
+    attention's 16 blocks per KV head take slices of about 63, 125 and 219 cells: one, two and
+    four passes of 64 cells."""
     key = "tiny_f32_1seq"
-    over = dict(n_ctx=4096, n_batch=2048, n_ubatch=512, type_k=tkv, type_v=tkv)
+    over = dict(n_ctx=4096, n_batch=4096, n_ubatch=512, type_k=tkv, type_v=tkv)
     ctx, ora = G.library_ctx(key, **over), G.oracle_ctx(key, **over)
-    toks = S.prompt_tokens(4242, 2000, S.WORKLOADS[key].hp.n_vocab).numpy()
+    toks = S.prompt_tokens(4242, n_prompt, S.WORKLOADS[key].hp.n_vocab).numpy()
     assert ctx.decode(toks) == 0, ctx.last_error()
     assert ora.decode(toks) == 0
     tol = TOL if tkv == oracle.F16 else 1e-3
@@ -179,5 +181,29 @@ def test_tiny_many_sequence_decode_steps(n_seq):
     assert ora.decode(toks, seq_id=seqs, n_seq_id=[1] * len(toks), logits=flags) == 0
     rows = [(s + 1) * n_p - 1 for s in range(n_seq)]
     rep = G.greedy_compare(ctx, ora, n_seq, rows, 3, TOL, {})
+    assert rep["tokens_checked"] >= n_seq
+    ctx.free()
+
+
+def test_tiny_many_long_sequences_decode_steps():
+    """16 sequences of 520 cells: clusters of 4 blocks per (token, KV head), each block walking 3
+    passes of 64 cells."""
+    key = "tiny_f32_8seq"
+    w = S.WORKLOADS[key]
+    n_seq, n_p = 16, 520
+    over = dict(n_seq_max=n_seq, n_ctx=8448, n_batch=1024, n_ubatch=512)
+    ctx, ora = G.library_ctx(key, **over), G.oracle_ctx(key, **over)
+    for s in range(n_seq):
+        toks = S.prompt_tokens(700 + s, n_p, w.hp.n_vocab).numpy()
+        flags = np.zeros(n_p, dtype=np.int8)
+        flags[-1] = 1
+        assert ctx.decode(toks, seq_ids=[[s]] * n_p, logits=flags) == 0, ctx.last_error()
+        assert ora.decode(toks, seq_id=[[s]] * n_p, n_seq_id=[1] * n_p, logits=flags) == 0
+    # the last call's output row is sequence 15's; run one step of all sequences to compare
+    nxt = [int(ctx.get_argmax_ith(-1))] * n_seq
+    seqs = [[s] for s in range(n_seq)]
+    assert ctx.decode(nxt, seq_ids=seqs, logits=[1] * n_seq) == 0, ctx.last_error()
+    assert ora.decode(nxt, seq_id=seqs, n_seq_id=[1] * n_seq, logits=[1] * n_seq) == 0
+    rep = G.greedy_compare(ctx, ora, n_seq, list(range(n_seq)), 2, TOL, {})
     assert rep["tokens_checked"] >= n_seq
     ctx.free()

@@ -292,32 +292,42 @@ attn_decode_kernel(AttnArgs a, float scale_log2) {
 // of an A fragment being 16 cells (scores) or 16 output dimensions (values) and the 8 columns of
 // a B fragment the query heads (4 of the group, 4 zero columns). Q and P enter as two f16 terms
 // (hi + lo of the float32), so every product is float32-accurate to about 2^-22, as in the
-// prefill kernel. Warp w takes cells 16w .. 16w+15 of every 64-cell pass and keeps its own
-// online-softmax state; the four warps' states merge in shared memory, then across the cluster.
-constexpr int kMW = 4;                   // warps
-constexpr int kMT = kMW * 32;            // threads
-constexpr int kMC = kCH / kMW;           // cells per warp and pass (one m16 fragment)
+// prefill kernel. A block of MW warps walks its slice in passes of 16 MW cells; warp w takes cells
+// 16w .. 16w+15 of every pass and keeps its own online-softmax state; the warps' states merge in
+// shared memory, then across the cluster.
+//
+// Each pass is a chain of dependent steps per warp (MMAs, shuffles of the softmax, the P^T
+// exchange); at 8192 cells over 16-block clusters the kernel is latency-bound (9% issue-active,
+// DRAM at 16% of peak, stalls spread over fixed-latency waits, L1/shared loads and barriers). The
+// K Q^T chain runs in four independent accumulators. Blocks stay at 4 warps (MW): 8-warp blocks
+// and deeper pipelines (three or four stages) measured slower at that length, since a block above
+// ~113 KB of shared memory takes an SM alone and leaves no room for the next GEMV's blocks that
+// start early under programmatic dependent launch.
+constexpr int kMC = 16;                  // cells per warp and pass (one m16 fragment)
 
-// KT = int8_t: a Q8_0 cache. Its int8 rows are staged as they are, expanded to exact f16 values
-// in a shared tile per pass, and the block scales enter outside the MMAs: a score sums each
-// 32-dimension block's fragment times the cell's K scale; the P^T fragment is multiplied by the
-// cells' V scales for each 32-dimension output block.
-template <int HD, typename KT>
+// KT = int8_t: a Q8_0 cache. Its int8 rows and fp16 scales are staged as they are, the rows
+// expanded to exact f16 values in a shared tile per pass, and the block scales enter outside the
+// MMAs: a score sums each 32-dimension block's fragment times the cell's K scale; the P^T fragment
+// is multiplied by the cells' V scales for each 32-dimension output block.
+//
+// NS stages: NS - 1 passes are in flight while one is computed (two are used).
+template <int HD, typename KT, int NS, int MW>
 struct MmaDecSmem {
+    static constexpr int CH = kMC * MW;                  // cells per pass
     static constexpr bool Q8 = sizeof(KT) == 1;
     static constexpr int NB = HD / 32;
     static constexpr int RS = HD + 8;                     // halves per padded f16 row
     static constexpr int RB = HD * (int)sizeof(KT);       // bytes of a cached row
     static constexpr int RSS = Q8 ? RB + 16 : RS * 2;     // bytes per staged row
-    static constexpr size_t rows = 2 * (size_t)kCH * RSS;
-    static constexpr size_t stage = rows + 3 * kCH * 4 + (Q8 ? 2 * (size_t)kCH * NB * 4 : 0);
-    static constexpr size_t tile = Q8 ? 2 * (size_t)kCH * RS * 2 : 0;   // expanded K and V
-    // the warp states and the block partial reuse the stages once the passes are done, which
-    // keeps the block small enough for two blocks of the next GEMV beside it on an SM
-    static constexpr size_t states = (size_t)kMW * kGQ * (HD + 2) * 4 + (size_t)kGQ * (HD + 2) * 4;
+    static constexpr size_t rows = 2 * (size_t)CH * RSS;
+    static constexpr size_t stage = rows + 3 * CH * 4 + (Q8 ? 2 * (size_t)CH * NB * 2 : 0);
+    static_assert(stage % 16 == 0, "stages stay 16-byte aligned");
+    static constexpr size_t tile = Q8 ? 2 * (size_t)CH * RS * 2 : 0;   // expanded K and V
+    // the warp states and the block partial reuse the stages once the passes are done
+    static constexpr size_t states = (size_t)MW * kGQ * (HD + 2) * 4 + (size_t)kGQ * (HD + 2) * 4;
     static_assert(states <= 2 * stage, "states fit in the stage area");
-    static constexpr size_t bytes = 2 * stage + tile + (size_t)kGQ * HD * 4 /* q */ +
-                                    (size_t)kMW * kMC * 8 * 4 /* P^T per warp */ + 16;
+    static constexpr size_t bytes = NS * stage + tile + (size_t)kGQ * HD * 4 /* q */ +
+                                    (size_t)MW * kMC * 8 * 4 /* P^T per warp */ + 16;
 };
 
 // two int8 (low bytes of v, selected by sel) -> an exact half2: the biased byte as the low
@@ -330,32 +340,33 @@ __device__ __forceinline__ uint32_t q8x2_to_h2(uint32_t biased, uint32_t sel) {
 
 // CL blocks per cluster: 16 for a few tokens; fewer (down to 1, no peers) when many tokens already
 // fill the GPU, so each block walks a longer slice and pays the fixed costs less often.
-template <int HD, typename KT, int CL>
-__global__ void __launch_bounds__(kMT)
+template <int HD, typename KT, int CL, int NS, int MW>
+__global__ void __launch_bounds__(MW * 32)
 attn_decode_mma_kernel(AttnArgs a, float scale_log2) {
-    using SM = MmaDecSmem<HD, KT>;
+    using SM = MmaDecSmem<HD, KT, NS, MW>;
+    constexpr int CH = SM::CH, MT = MW * 32;
     constexpr bool Q8 = SM::Q8;
     constexpr int RS = SM::RS, RB = SM::RB, RSS = SM::RSS, VPR = RB / 16, NK = HD / 16, NB = SM::NB;
     extern __shared__ __align__(16) uint8_t sm[];
-    struct St { uint8_t* kraw; uint8_t* vraw; int* ccell; int* cvis; int* cfresh; float* ksc; float* vsc; };
+    struct St { uint8_t* kraw; uint8_t* vraw; int* ccell; int* cvis; int* cfresh; __half* ksc; __half* vsc; };
     auto stage_of = [&](int s) {
         uint8_t* b = sm + (size_t)s * SM::stage;
         St S;
         S.kraw = b;
-        S.vraw = b + kCH * RSS;
+        S.vraw = b + CH * RSS;
         S.ccell = reinterpret_cast<int*>(b + SM::rows);
-        S.cvis = S.ccell + kCH;
-        S.cfresh = S.cvis + kCH;
-        S.ksc = reinterpret_cast<float*>(S.cfresh + kCH);
-        S.vsc = S.ksc + kCH * NB;
+        S.cvis = S.ccell + CH;
+        S.cfresh = S.cvis + CH;
+        S.ksc = reinterpret_cast<__half*>(S.cfresh + CH);
+        S.vsc = S.ksc + CH * NB;
         return S;
     };
-    __half* tk = reinterpret_cast<__half*>(sm + 2 * SM::stage);       // Q8_0: expanded K tile
-    __half* tv = tk + kCH * RS;                                         //        and V tile
-    float* qs = reinterpret_cast<float*>(sm + 2 * SM::stage + SM::tile);  // [kGQ][HD]
+    __half* tk = reinterpret_cast<__half*>(sm + NS * SM::stage);      // Q8_0: expanded K tile
+    __half* tv = tk + CH * RS;                                         //        and V tile
+    float* qs = reinterpret_cast<float*>(sm + NS * SM::stage + SM::tile);  // [kGQ][HD]
     float* pT = qs + kGQ * HD;                                          // [warp][16 cells][8]
     float* ws = reinterpret_cast<float*>(sm);                           // after the passes: [warp][kGQ][HD + 2]
-    float* pst = ws + kMW * kGQ * (HD + 2);                             // block partial (peers read it)
+    float* pst = ws + MW * kGQ * (HD + 2);                             // block partial (peers read it)
 
     const uint32_t rank = cluster_rank();
     const int kvh = blockIdx.y, tile = blockIdx.z;
@@ -370,38 +381,27 @@ attn_decode_mma_kernel(AttnArgs a, float scale_log2) {
     const int tpos = a.tok_pos[t];
     const int chunk = (len + CL - 1) / CL;
     const int c0 = min(len, (int)rank * chunk), c1 = min(len, c0 + chunk);
-    const int npass = c1 > c0 ? (c1 - c0 + kCH - 1) / kCH : 1;
+    const int npass = c1 > c0 ? (c1 - c0 + CH - 1) / CH : 1;
     const uint8_t* K = static_cast<const uint8_t*>(a.kc) + (int64_t)kvh * a.n_ctx * RB;
     const uint8_t* V = static_cast<const uint8_t*>(a.vc) + (int64_t)kvh * a.n_ctx * RB;
     const __half* KS = q8_scales(a.kc, a, kvh);
     const __half* VS = q8_scales(a.vc, a, kvh);
 
+    // list entries of a pass, loaded one pass before its stage is set up
     int pf_cell = -1, pf_pos = 0;
-    float pf_ks[NB], pf_vs[NB];
-    auto fetch = [&](int i, bool with_scales) {
-        if (threadIdx.x < kCH) {
-            const int ci = c0 + i * kCH + threadIdx.x;
+    auto fetch = [&](int i) {
+        if (threadIdx.x < CH) {
+            const int ci = c0 + i * CH + threadIdx.x;
             pf_cell = -1;
             pf_pos = 0;
             if (ci < c1) {
                 pf_cell = a.list_cells[base + ci];
                 pf_pos = a.list_pos[base + ci];
             }
-            if constexpr (Q8) {
-                if (with_scales && pf_cell >= 0 && pf_cell < a.n_ctx && pf_pos <= tpos) {
-#pragma unroll
-                    for (int b = 0; b < NB; ++b) {
-                        pf_ks[b] = ld_scale(KS + (int64_t)pf_cell * NB + b);
-                        pf_vs[b] = ld_scale(VS + (int64_t)pf_cell * NB + b);
-                    }
-                }
-            }
         }
     };
-    // stage S takes the fetched entry; Q8_0: hidden cells get zero scales (their rows stay stale
-    // but finite), cells of this step get theirs after the wait
-    auto setup = [&](const St& S, bool pre_wait) {
-        if (threadIdx.x < kCH) {
+    auto setup = [&](const St& S) {
+        if (threadIdx.x < CH) {
             int cell = -1, vis = 0, fresh = 0;
             if (pf_cell >= 0 && pf_cell < a.n_ctx) {
                 cell = pf_cell;
@@ -411,24 +411,30 @@ attn_decode_mma_kernel(AttnArgs a, float scale_log2) {
             S.ccell[threadIdx.x] = cell;
             S.cvis[threadIdx.x] = vis && cell >= 0;
             S.cfresh[threadIdx.x] = fresh;
-            if constexpr (Q8) {
-                const bool v = vis && cell >= 0;
+        }
+    };
+    // the stage's rows (and Q8_0 scales) as one cp.async group; before the wait on the previous
+    // kernel the rows of this step's cells are left out (loaded after it). Q8_0: hidden cells get
+    // zero scales (their int8 rows stay stale but finite).
+    auto issue = [&](const St& S, bool pre_wait) {
+        if constexpr (Q8) {
+            const int c = threadIdx.x % CH;
+            const bool isv = threadIdx.x >= CH;                 // MT == 2 CH
+            __half* dst = (isv ? S.vsc : S.ksc) + c * NB;
+            if (!S.cvis[c]) {
 #pragma unroll
-                for (int b = 0; b < NB; ++b) {
-                    float ks = 0.f, vs = 0.f;
-                    if (v && !pre_wait) { ks = pf_ks[b]; vs = pf_vs[b]; }
-                    if (v && pre_wait && !fresh) {
-                        ks = ld_scale(KS + (int64_t)cell * NB + b);
-                        vs = ld_scale(VS + (int64_t)cell * NB + b);
-                    }
-                    S.ksc[threadIdx.x * NB + b] = ks;
-                    S.vsc[threadIdx.x * NB + b] = vs;
+                for (int b = 0; b < NB; ++b) dst[b] = __ushort_as_half(0);
+            } else if (!(pre_wait && S.cfresh[c])) {
+                const __half* src = (isv ? VS : KS) + (int64_t)S.ccell[c] * NB;
+                if constexpr (NB >= 2) {
+                    asm volatile("cp.async.ca.shared.global [%0], [%1], %2;" ::"r"(sm32(dst)), "l"(src),
+                                 "n"(NB * 2) : "memory");
+                } else {
+                    dst[0] = __ushort_as_half(__ldcg(reinterpret_cast<const unsigned short*>(src)));
                 }
             }
         }
-    };
-    auto issue = [&](const St& S, bool pre_wait) {
-        for (int v = threadIdx.x; v < kCH * VPR; v += kMT) {
+        for (int v = threadIdx.x; v < CH * VPR; v += MT) {
             const int c = v / VPR, j = v % VPR;
             if (!S.cvis[c]) {
                 // the MMA multiplies every row of the tile: a hidden cell's V row must be finite
@@ -445,15 +451,15 @@ attn_decode_mma_kernel(AttnArgs a, float scale_log2) {
 
     {
         const St S0 = stage_of(0);
-        fetch(0, false);
-        setup(S0, true);
+        fetch(0);
+        setup(S0);
         __syncthreads();
         issue(S0, true);
         asm volatile("griddepcontrol.wait;" ::: "memory");
-        for (int i = threadIdx.x; i < kGQ * HD; i += kMT)
+        for (int i = threadIdx.x; i < kGQ * HD; i += MT)
             qs[i] = a.q[(int64_t)t * a.ldq + (kvh * kGQ + i / HD) * HD + i % HD] * scale_log2;
-        if (npass > 1) fetch(1, true);
-        for (int v = threadIdx.x; v < kCH * VPR; v += kMT) {
+        if (npass > 1) fetch(1);
+        for (int v = threadIdx.x; v < CH * VPR; v += MT) {
             const int c = v / VPR, j = v % VPR;
             if (!S0.cvis[c] || !S0.cfresh[c]) continue;
             const size_t src = (size_t)S0.ccell[c] * RB + j * 16;
@@ -461,14 +467,26 @@ attn_decode_mma_kernel(AttnArgs a, float scale_log2) {
             *reinterpret_cast<uint4*>(S0.vraw + c * RSS + j * 16) = __ldcg(reinterpret_cast<const uint4*>(V + src));
         }
         if constexpr (Q8) {
-            if (threadIdx.x < kCH && S0.cvis[threadIdx.x] && S0.cfresh[threadIdx.x]) {
+            if (threadIdx.x < CH && S0.cvis[threadIdx.x] && S0.cfresh[threadIdx.x]) {
                 const int cell = S0.ccell[threadIdx.x];
 #pragma unroll
                 for (int b = 0; b < NB; ++b) {
-                    S0.ksc[threadIdx.x * NB + b] = ld_scale(KS + (int64_t)cell * NB + b);
-                    S0.vsc[threadIdx.x * NB + b] = ld_scale(VS + (int64_t)cell * NB + b);
+                    S0.ksc[threadIdx.x * NB + b] = __float2half_rn(ld_scale(KS + (int64_t)cell * NB + b));
+                    S0.vsc[threadIdx.x * NB + b] = __float2half_rn(ld_scale(VS + (int64_t)cell * NB + b));
                 }
             }
+        }
+    }
+    // passes 1 .. NS - 2 (empty groups past the last pass): NS - 1 groups committed
+    for (int j = 1; j < NS - 1; ++j) {
+        if (j < npass) {
+            const St N = stage_of(j);
+            setup(N);
+            if (j + 1 < npass) fetch(j + 1);
+            __syncthreads();
+            issue(N, false);
+        } else {
+            asm volatile("cp.async.commit_group;" ::: "memory");
         }
     }
     __syncthreads();                                            // qs
@@ -491,17 +509,18 @@ attn_decode_mma_kernel(AttnArgs a, float scale_log2) {
     float* pw = pT + warp * kMC * 8;
     const int cw = warp * kMC;                                  // this warp's cells in a pass
     for (int i = 0; i < npass; ++i) {
-        const St S = stage_of(i & 1);
-        if (i + 1 < npass) {
-            const St N = stage_of((i + 1) & 1);
-            setup(N, false);
-            if (i + 2 < npass) fetch(i + 2, true);
+        const St S = stage_of(i % NS);
+        const int nx = i + NS - 1;                              // the pass issued now
+        if (nx < npass) {
+            const St N = stage_of(nx % NS);
+            setup(N);
+            if (nx + 1 < npass) fetch(nx + 1);
             __syncthreads();
             issue(N, false);
-            asm volatile("cp.async.wait_group 1;" ::: "memory");
         } else {
-            asm volatile("cp.async.wait_group 0;" ::: "memory");
+            asm volatile("cp.async.commit_group;" ::: "memory");
         }
+        asm volatile("cp.async.wait_group %0;" ::"n"(NS - 1) : "memory");   // pass i has landed
         __syncthreads();
         const __half* kb;
         const __half* vb;
@@ -539,18 +558,22 @@ attn_decode_mma_kernel(AttnArgs a, float scale_log2) {
                         mma16816(sb, af, qh[kk][0], qh[kk][1]);
                         mma16816(sb, af, ql[kk][0], ql[kk][1]);
                     }
-                    const float d0 = S.ksc[(cw + g) * NB + b], d1 = S.ksc[(cw + g + 8) * NB + b];
+                    const float d0 = __half2float(S.ksc[(cw + g) * NB + b]);
+                    const float d1 = __half2float(S.ksc[(cw + g + 8) * NB + b]);
                     s[0] = fmaf(d0, sb[0], s[0]); s[1] = fmaf(d0, sb[1], s[1]);
                     s[2] = fmaf(d1, sb[2], s[2]); s[3] = fmaf(d1, sb[3], s[3]);
                 }
             } else {
+                float acc[4][4] = {};
 #pragma unroll
                 for (int kk = 0; kk < NK; ++kk) {
                     uint32_t af[4];
                     ldsm_x4(sm32(kr + kk * 16), af[0], af[1], af[2], af[3]);
-                    mma16816(s, af, qh[kk][0], qh[kk][1]);
-                    mma16816(s, af, ql[kk][0], ql[kk][1]);
+                    mma16816(acc[kk & 1], af, qh[kk][0], qh[kk][1]);
+                    mma16816(acc[2 + (kk & 1)], af, ql[kk][0], ql[kk][1]);
                 }
+#pragma unroll
+                for (int e = 0; e < 4; ++e) s[e] = (acc[0][e] + acc[1][e]) + (acc[2][e] + acc[3][e]);
             }
         }
         // this thread: cells cw+g (s[0], s[1]) and cw+g+8 (s[2], s[3]), heads 2cq and 2cq+1
@@ -601,9 +624,9 @@ attn_decode_mma_kernel(AttnArgs a, float scale_log2) {
                 if constexpr (Q8) {
                     if ((nt & 1) == 0) {
                         const int b = nt / 2;
-                        const float* vs = S.vsc + (cw + 2 * cq) * NB + b;
-                        split_h2(pq[0] * vs[0], pq[1] * vs[NB], bh0, bl0);
-                        split_h2(pq[2] * vs[8 * NB], pq[3] * vs[9 * NB], bh1, bl1);
+                        const __half* vs = S.vsc + (cw + 2 * cq) * NB + b;
+                        split_h2(pq[0] * __half2float(vs[0]), pq[1] * __half2float(vs[NB]), bh0, bl0);
+                        split_h2(pq[2] * __half2float(vs[8 * NB]), pq[3] * __half2float(vs[9 * NB]), bh1, bl1);
                     }
                 }
                 uint32_t af[4];
@@ -613,7 +636,7 @@ attn_decode_mma_kernel(AttnArgs a, float scale_log2) {
             }
         }
         __syncwarp();                                           // pw is rewritten next pass
-        __syncthreads();                                        // stage S free for pass i + 2
+        __syncthreads();                                        // stage S free for pass i + NS
     }
 
     // the warps' states -> this block's partial -> the cluster-wide merge
@@ -634,14 +657,14 @@ attn_decode_mma_kernel(AttnArgs a, float scale_log2) {
     float* pm = pst;
     float* pl = pst + kGQ;
     float* po = pst + 2 * kGQ;
-    for (int idx = threadIdx.x; idx < kGQ * HD; idx += kMT) {
+    for (int idx = threadIdx.x; idx < kGQ * HD; idx += MT) {
         const int h = idx / HD, dd = idx % HD;
         float M = -INFINITY;
 #pragma unroll
-        for (int w = 0; w < kMW; ++w) M = fmaxf(M, ws[(w * kGQ + h) * (HD + 2)]);
+        for (int w = 0; w < MW; ++w) M = fmaxf(M, ws[(w * kGQ + h) * (HD + 2)]);
         float L = 0.f, O = 0.f;
 #pragma unroll
-        for (int w = 0; w < kMW; ++w) {
+        for (int w = 0; w < MW; ++w) {
             const float* hs = ws + (w * kGQ + h) * (HD + 2);
             const float f = (M == -INFINITY || hs[0] == -INFINITY) ? 0.f : exp2f(hs[0] - M);
             L = fmaf(f, hs[1], L);
@@ -652,7 +675,7 @@ attn_decode_mma_kernel(AttnArgs a, float scale_log2) {
     }
     cluster_sync_all();
     constexpr int OPB = kGQ * HD / CL;
-    for (int idx = threadIdx.x; idx < OPB; idx += kMT) {
+    for (int idx = threadIdx.x; idx < OPB; idx += MT) {
         const int oi = (int)rank * OPB + idx;
         const int h = oi / HD, dd = oi % HD;
         float M = -INFINITY;
@@ -671,11 +694,11 @@ attn_decode_mma_kernel(AttnArgs a, float scale_log2) {
     cluster_sync_all();
 }
 
-template <int HD, typename KT, int CL>
+template <int HD, typename KT, int CL, int NS, int MW>
 bool launch_dec_mma_cl(const AttnArgs& a, cudaStream_t st) {
     const float scale_log2 = (float)(1.4426950408889634 / sqrt((double)HD));
-    constexpr size_t smem = MmaDecSmem<HD, KT>::bytes;
-    auto k = attn_decode_mma_kernel<HD, KT, CL>;
+    constexpr size_t smem = MmaDecSmem<HD, KT, NS, MW>::bytes;
+    auto k = attn_decode_mma_kernel<HD, KT, CL, NS, MW>;
     static bool attr = false;
     if (!attr) {
         if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess ||
@@ -685,7 +708,7 @@ bool launch_dec_mma_cl(const AttnArgs& a, cudaStream_t st) {
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(CL, a.Hkv, a.n_tok);
-    cfg.blockDim = dim3(kMT);
+    cfg.blockDim = dim3(MW * 32);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
     cudaLaunchAttribute attr_l[2];
@@ -700,9 +723,7 @@ bool launch_dec_mma_cl(const AttnArgs& a, cudaStream_t st) {
     return cudaLaunchKernelEx(&cfg, k, a, scale_log2) == cudaSuccess;
 }
 
-// The cluster size: 16 unless 16 blocks per (token, KV head) would exceed two blocks per SM.
-template <int HD, typename KT>
-bool launch_dec_mma(const AttnArgs& a, cudaStream_t st) {
+int sm_count() {
     static int n_sm = 0;
     if (n_sm == 0) {
         int dev = 0;
@@ -710,10 +731,22 @@ bool launch_dec_mma(const AttnArgs& a, cudaStream_t st) {
         cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
         if (n_sm <= 0) n_sm = 148;
     }
-    const int64_t units = (int64_t)a.Hkv * a.n_tok;
-    if (16 * units <= 2 * n_sm) return launch_dec_mma_cl<HD, KT, 16>(a, st);
-    if (4 * units <= 2 * n_sm) return launch_dec_mma_cl<HD, KT, 4>(a, st);
-    return launch_dec_mma_cl<HD, KT, 1>(a, st);
+    return n_sm;
+}
+
+// The cluster size: 16 unless 16 blocks per (token, KV head) would exceed two blocks per SM.
+int dec_cluster(int n_tok, int Hkv) {
+    const int64_t units = (int64_t)Hkv * n_tok, n_sm = sm_count();
+    return 16 * units <= 2 * n_sm ? 16 : 4 * units <= 2 * n_sm ? 4 : 1;
+}
+
+template <int HD, typename KT>
+bool launch_dec_mma(const AttnArgs& a, cudaStream_t st) {
+    switch (dec_cluster(a.n_tok, a.Hkv)) {
+        case 16: return launch_dec_mma_cl<HD, KT, 16, 2, 4>(a, st);
+        case 4: return launch_dec_mma_cl<HD, KT, 4, 2, 4>(a, st);
+    }
+    return launch_dec_mma_cl<HD, KT, 1, 2, 4>(a, st);
 }
 
 template <int HD>
