@@ -11,6 +11,9 @@
 // base-2 exponent with log2(e)/sqrt(hd) folded into Q); a cell is visible to a row iff
 // cell.pos <= token.pos. Each block writes its partial (o, m, l); the last block of a
 // (tile, KV head) to finish (a self-resetting ticket) merges the partials and writes the output.
+//
+// These CUDA-core tiles serve F32 caches; F16 and Q8_0 caches take the tensor-core tiles
+// (attn_mma.cu), and tiles of one token the cluster decode kernels (attn_decode.cu).
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -30,11 +33,6 @@ using namespace attn;
 constexpr int kAttnWarps = 4;
 constexpr int kBC = 32;                  // cells per shared-memory tile (one per lane)
 
-template <typename KT> __device__ __forceinline__ float kv_to_f(KT v);
-template <> __device__ __forceinline__ float kv_to_f<float>(float v) { return v; }
-template <> __device__ __forceinline__ float kv_to_f<__half>(__half v) { return __half2float(v); }
-template <> __device__ __forceinline__ float kv_to_f<int8_t>(int8_t v) { return (float)v; }
-
 template <int HD, int TQ, int G>
 struct AttnSmem {
     static constexpr int R = TQ * G;
@@ -49,7 +47,7 @@ struct AttnSmem {
     static constexpr size_t merge_floats = q_floats + k_floats + v_floats;
 };
 
-template <int HD, int TQ, int G, typename KT>
+template <int HD, int TQ, int G>
 __global__ void __launch_bounds__(kAttnWarps * 32)
 attn_kernel(AttnArgs a, float scale_log2) {
     using SM = AttnSmem<HD, TQ, G>;
@@ -75,11 +73,8 @@ attn_kernel(AttnArgs a, float scale_log2) {
     const int4 td0 = a.tile_desc[2 * wd.x];        // list, first token, tokens, first item
     const int4 td1 = a.tile_desc[2 * wd.x + 1];    // end item, list start, list length, -
     const int nq = td0.z, s0 = td0.y, c0 = wd.y, c1 = wd.z, base = td1.y;
-    const KT* K = static_cast<const KT*>(a.kc) + (int64_t)kvh * a.n_ctx * HD;
-    const KT* V = static_cast<const KT*>(a.vc) + (int64_t)kvh * a.n_ctx * HD;
-    constexpr bool Q8 = sizeof(KT) == 1;           // Q8_0: int8 quants and fp16 scales per 32 values
-    const __half* KS = Q8 ? q8_scales(a.kc, a, kvh) : nullptr;
-    const __half* VS = Q8 ? q8_scales(a.vc, a, kvh) : nullptr;
+    const float* K = static_cast<const float*>(a.kc) + (int64_t)kvh * a.n_ctx * HD;
+    const float* V = static_cast<const float*>(a.vc) + (int64_t)kvh * a.n_ctx * HD;
     asm volatile("griddepcontrol.wait;" ::: "memory");
 
     for (int idx = threadIdx.x; idx < R * HD; idx += blockDim.x) {
@@ -106,7 +101,7 @@ attn_kernel(AttnArgs a, float scale_log2) {
         for (int e = 0; e < DPL; ++e) o[i][e] = 0.f;
     }
 
-    constexpr int EPV = 16 / (int)sizeof(KT);          // elements per 16-byte vector
+    constexpr int EPV = 4;                               // floats per 16-byte vector
     constexpr int VPR = HD / EPV;                        // vectors per cached row
     for (int cb = c0; cb < c1; cb += kBC) {
         __syncthreads();
@@ -127,26 +122,16 @@ attn_kernel(AttnArgs a, float scale_log2) {
             const int c = v / VPR, j = v % VPR;
             const int cell = ccell[c];
             uint4 kq = make_uint4(0u, 0u, 0u, 0u), vq = kq;
-            float dk = 1.f, dv = 1.f;
             if (cell >= 0) {
                 kq = __ldg(reinterpret_cast<const uint4*>(K + (int64_t)cell * HD) + j);
                 vq = __ldg(reinterpret_cast<const uint4*>(V + (int64_t)cell * HD) + j);
-                if constexpr (Q8) {                  // 16 quants: half of one 32-value block
-                    dk = ld_scale(KS + (int64_t)cell * (HD / 32) + j / 2);
-                    dv = ld_scale(VS + (int64_t)cell * (HD / 32) + j / 2);
-                }
             }
-            const KT* ke = reinterpret_cast<const KT*>(&kq);
-            const KT* ve = reinterpret_cast<const KT*>(&vq);
+            const float* ke = reinterpret_cast<const float*>(&kq);
+            const float* ve = reinterpret_cast<const float*>(&vq);
 #pragma unroll
             for (int e = 0; e < EPV; ++e) {
-                if constexpr (Q8) {
-                    ks[c * (HD + 1) + j * EPV + e] = dk * kv_to_f<KT>(ke[e]);
-                    vs[c * HD + j * EPV + e] = dv * kv_to_f<KT>(ve[e]);
-                } else {
-                    ks[c * (HD + 1) + j * EPV + e] = kv_to_f<KT>(ke[e]);
-                    vs[c * HD + j * EPV + e] = kv_to_f<KT>(ve[e]);
-                }
+                ks[c * (HD + 1) + j * EPV + e] = ke[e];
+                vs[c * HD + j * EPV + e] = ve[e];
             }
         }
         __syncthreads();
@@ -245,202 +230,6 @@ attn_kernel(AttnArgs a, float scale_log2) {
     merge_tile<HD, G>(a, kvh, s0, nq, w0, w1, qs, SM::merge_floats);
 }
 
-// Decode-step attention (every query tile holds one token). The K/V rows of cells written by
-// earlier steps cannot change while the previous kernel (this step's Q/K/V projection) runs, so
-// the block stages them (cp.async, padded rows) before griddepcontrol.wait; only Q and the cells
-// written by this step are read after it. Grid (KV head, work item): the active blocks come first.
-// Warp g handles query head g of the group: scores with one cell per lane, softmax, then V with
-// each lane owning HD/32 output dimensions.
-template <int HD, int G, typename KT>
-__global__ void __launch_bounds__(128)
-attn_step_kernel(AttnArgs a, float scale_log2) {
-    constexpr int CH = 64;                                  // cells staged per pass
-    constexpr int RB = HD * (int)sizeof(KT);                // bytes of a cached row
-    constexpr int RS = RB + 16;                             // padded row stride
-    constexpr int VPR = RB / 16;                            // 16-byte chunks per row
-    constexpr int DPL = HD / 32;
-    static_assert(G == 4, "one warp per query head of the group");
-    extern __shared__ __align__(16) uint8_t sm[];
-    uint8_t* kb = sm;                                       // [CH][RS]
-    uint8_t* vb = kb + CH * RS;                             // [CH][RS]
-    float* qs = reinterpret_cast<float*>(vb + CH * RS);     // [G][HD]
-    int* ccell = reinterpret_cast<int*>(qs + G * HD);       // [CH]
-    int* cvis = ccell + CH;                                 // [CH] visible
-    int* cfresh = cvis + CH;                                // [CH] written by this step
-    int* flag = cfresh + CH;
-
-    const int kvh = blockIdx.x, wi = blockIdx.y;
-    if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;");
-    const int n_work = a.hdr[0];
-    const int4 wd = a.wi_desc[wi];
-    if (wi >= n_work) return;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int4 td0 = a.tile_desc[2 * wd.x];
-    const int4 td1 = a.tile_desc[2 * wd.x + 1];
-    const int s0 = td0.y, base = td1.y, c0 = wd.y, c1 = wd.z;
-    const int t = a.perm[s0];
-    const int tpos = a.tok_pos[t];
-    const uint8_t* K = static_cast<const uint8_t*>(a.kc) + (int64_t)kvh * a.n_ctx * RB;
-    const uint8_t* V = static_cast<const uint8_t*>(a.vc) + (int64_t)kvh * a.n_ctx * RB;
-
-    float m = -INFINITY, l = 0.f, o[DPL];
-#pragma unroll
-    for (int e = 0; e < DPL; ++e) o[e] = 0.f;
-    bool waited = false;
-    for (int cb = c0; cb < c1; cb += CH) {
-        if (threadIdx.x < CH) {
-            const int ci = cb + threadIdx.x;
-            int cell = -1, vis = 0, fresh = 0;
-            if (ci < c1) {
-                const int cc = a.list_cells[base + ci];
-                if (cc >= 0 && cc < a.n_ctx) {
-                    cell = cc;
-                    vis = a.list_pos[base + ci] <= tpos;
-                    for (int j = 0; j < a.n_tok; ++j) fresh |= a.slot[j] == cc;
-                }
-            }
-            ccell[threadIdx.x] = cell;
-            cvis[threadIdx.x] = vis && cell >= 0;
-            cfresh[threadIdx.x] = fresh;
-        }
-        __syncthreads();
-        // rows of earlier steps: staged now, possibly before the previous kernel has ended
-        for (int v = threadIdx.x; v < CH * VPR; v += blockDim.x) {
-            const int c = v / VPR, j = v % VPR;
-            if (!cvis[c] || cfresh[c]) continue;
-            const size_t src = (size_t)ccell[c] * RB + j * 16;
-            const uint32_t dk = (uint32_t)__cvta_generic_to_shared(kb + c * RS + j * 16);
-            const uint32_t dv = (uint32_t)__cvta_generic_to_shared(vb + c * RS + j * 16);
-            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dk), "l"(K + src) : "memory");
-            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dv), "l"(V + src) : "memory");
-        }
-        asm volatile("cp.async.commit_group;" ::: "memory");
-        if (!waited) {
-            asm volatile("griddepcontrol.wait;" ::: "memory");
-            waited = true;
-            for (int i = threadIdx.x; i < G * HD; i += blockDim.x)
-                qs[i] = a.q[(int64_t)t * a.ldq + (kvh * G + i / HD) * HD + i % HD] * scale_log2;
-        }
-        // rows written by this step's projection kernel: only now
-        for (int v = threadIdx.x; v < CH * VPR; v += blockDim.x) {
-            const int c = v / VPR, j = v % VPR;
-            if (!cvis[c] || !cfresh[c]) continue;
-            const size_t src = (size_t)ccell[c] * RB + j * 16;
-            *reinterpret_cast<uint4*>(kb + c * RS + j * 16) = *reinterpret_cast<const uint4*>(K + src);
-            *reinterpret_cast<uint4*>(vb + c * RS + j * 16) = *reinterpret_cast<const uint4*>(V + src);
-        }
-        asm volatile("cp.async.wait_all;" ::: "memory");
-        __syncthreads();
-
-        // scores of query head `warp`: lanes own cells lane and lane + 32
-        const float* q = qs + warp * HD;
-        float s[2];
-#pragma unroll
-        for (int h2 = 0; h2 < 2; ++h2) {
-            const int c = lane + 32 * h2;
-            s[h2] = -INFINITY;
-            if (cvis[c]) {
-                const uint8_t* kr = kb + c * RS;
-                float a0 = 0.f, a1 = 0.f;
-#pragma unroll
-                for (int j = 0; j < VPR; ++j) {
-                    const uint4 kv = *reinterpret_cast<const uint4*>(kr + j * 16);
-                    const KT* ke = reinterpret_cast<const KT*>(&kv);
-                    constexpr int EPV = 16 / (int)sizeof(KT);
-#pragma unroll
-                    for (int e = 0; e < EPV; e += 2) {
-                        a0 = fmaf(q[j * EPV + e], kv_to_f<KT>(ke[e]), a0);
-                        a1 = fmaf(q[j * EPV + e + 1], kv_to_f<KT>(ke[e + 1]), a1);
-                    }
-                }
-                s[h2] = a0 + a1;
-            }
-        }
-        float mx = fmaxf(s[0], s[1]);
-        for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-        const float m_new = fmaxf(m, mx);
-        float p[2] = {0.f, 0.f}, corr = 1.f;
-        if (m_new != -INFINITY) {
-            corr = exp2f(m - m_new);
-            p[0] = exp2f(s[0] - m_new);
-            p[1] = exp2f(s[1] - m_new);
-        }
-        float ps = p[0] + p[1];
-        for (int off = 16; off > 0; off >>= 1) ps += __shfl_xor_sync(0xffffffffu, ps, off);
-        l = l * corr + ps;
-        m = m_new;
-#pragma unroll
-        for (int e = 0; e < DPL; ++e) o[e] *= corr;
-#pragma unroll 4
-        for (int c = 0; c < CH; ++c) {
-            const float pc = __shfl_sync(0xffffffffu, p[c >> 5], c & 31);
-            if (pc == 0.f) continue;
-            const KT* vr = reinterpret_cast<const KT*>(vb + c * RS) + lane * DPL;
-#pragma unroll
-            for (int e = 0; e < DPL; ++e) o[e] = fmaf(pc, kv_to_f<KT>(vr[e]), o[e]);
-        }
-        __syncthreads();
-    }
-    if (!waited) asm volatile("griddepcontrol.wait;" ::: "memory");
-
-    const int w0 = td0.w, w1 = td1.x;
-    const int g = warp;
-    if (w1 - w0 == 1) {
-        const float inv = l > 0.f ? 1.f / l : 0.f;
-#pragma unroll
-        for (int e = 0; e < DPL; ++e)
-            store_out(a, (int64_t)t * a.ldo + (kvh * G + g) * HD + lane * DPL + e, o[e] * inv);
-        return;
-    }
-    const int64_t row = (int64_t)(wd.w + g) * a.Hkv + kvh;
-    if (lane == 0) {
-        a.part_m[row] = m;
-        a.part_l[row] = l;
-    }
-#pragma unroll
-    for (int e = 0; e < DPL; ++e) a.part_o[row * HD + lane * DPL + e] = o[e];
-    __threadfence();
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        __threadfence();
-        int* ticket = a.tickets + wd.x * a.Hkv + kvh;
-        const int done = atomicAdd(ticket, 1) + 1;
-        const bool last = done == w1 - w0;
-        if (last) *ticket = 0;
-        *flag = last ? 1 : 0;
-    }
-    __syncthreads();
-    if (!*flag) return;
-    __threadfence();
-    merge_tile<HD, G>(a, kvh, s0, 1, w0, w1, reinterpret_cast<float*>(sm), (size_t)(2 * CH * RS) / 4);
-}
-
-template <int HD, int G>
-bool launch_step(const AttnArgs& a, cudaStream_t st) {
-    const float scale_log2 = (float)(1.4426950408889634 / sqrt((double)HD));
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(a.Hkv, a.n_work);
-    cfg.blockDim = dim3(128);
-    cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = a.pdl ? 1 : 0;
-    if (a.kv_type == W_F32) {
-        constexpr size_t smem = 2 * 64 * (HD * 4 + 16) + G * HD * 4 + 4 * 64 * 4 + 16;
-        auto k = attn_step_kernel<HD, G, float>;
-        cfg.dynamicSmemBytes = smem;
-        cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        return cudaLaunchKernelEx(&cfg, k, a, scale_log2) == cudaSuccess;
-    }
-    constexpr size_t smem = 2 * 64 * (HD * 2 + 16) + G * HD * 4 + 4 * 64 * 4 + 16;
-    auto k = attn_step_kernel<HD, G, __half>;
-    cfg.dynamicSmemBytes = smem;
-    cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    return cudaLaunchKernelEx(&cfg, k, a, scale_log2) == cudaSuccess;
-}
-
 template <int HD, int TQ, int G>
 bool launch_tq(const AttnArgs& a, cudaStream_t st) {
     const float scale_log2 = (float)(1.4426950408889634 / sqrt((double)HD));
@@ -455,27 +244,17 @@ bool launch_tq(const AttnArgs& a, cudaStream_t st) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = a.pdl ? 1 : 0;
-    if (a.kv_type == W_F32) {
-        auto k = attn_kernel<HD, TQ, G, float>;
-        cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        return cudaLaunchKernelEx(&cfg, k, a, scale_log2) == cudaSuccess;
-    }
-    if (a.kv_type == W_Q8_0) {
-        auto k = attn_kernel<HD, TQ, G, int8_t>;
-        cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        return cudaLaunchKernelEx(&cfg, k, a, scale_log2) == cudaSuccess;
-    }
-    auto k = attn_kernel<HD, TQ, G, __half>;
+    if (a.kv_type != W_F32) return false;          // F16 and Q8_0 caches take the tensor-core tiles
+    auto k = attn_kernel<HD, TQ, G>;
     cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     return cudaLaunchKernelEx(&cfg, k, a, scale_log2) == cudaSuccess;
 }
 
 template <int HD, int G>
 bool launch_hd_g(const AttnArgs& a, cudaStream_t st) {
-    if (a.max_nq <= 1) {
-        if (a.slot && attention_decode_ok(a)) return launch_attention_decode(a, st);
-        return a.slot && a.kv_type != W_Q8_0 ? launch_step<HD, G>(a, st) : launch_tq<HD, 1, G>(a, st);
-    }
+    // tiles of one token: the cluster decode kernels; of several: the tensor-core tiles (F16, Q8_0)
+    // or the CUDA-core tiles (F32)
+    if (a.max_nq <= 1) return attention_decode_ok(a) && launch_attention_decode(a, st);
     if (attention_mma_ok(a)) return launch_attention_mma(a, st);
     if (a.k_scale) return false;                   // the quant copies are for the tensor-core tiles
     return launch_tq<HD, kAttnTileQ, G>(a, st);
