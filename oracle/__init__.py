@@ -20,8 +20,7 @@ Sources, cited by page title and section:
   [P4] "デコードループ：バッチ処理、KVキャッシュ、メモリ管理" (readoss.com): バッチパイプライン,
        KVキャッシュの詳細, エラーリカバリとステートロールバック.
 
-Readings where the pages are silent are listed in DESIGN.md ("Readings of the pages") and marked
-"reading:" in the docstrings. Whole-forward logits are "parity unpinned" by the pages (they print
+Readings taken where the pages are silent are marked "reading:" in the docstrings. Whole-forward logits are "parity unpinned" by the pages (they print
 no logits for a reproducible input); the forward pass is pinned by closed forms, analytic models
 and invariants in tests/test_oracle_*.py.
 """

@@ -15,7 +15,7 @@ def pytest_configure(config):
 
 def pytest_collection_modifyitems(config, items):
     # tests that need a GPU skip cleanly when none is present, so a CPU run of the whole suite
-    # stays green; `-m gpu` on a GPU machine runs them
+    # stays green; `-m gpu` on a machine with a GPU runs them
     try:
         import torch
         has_gpu = torch.cuda.is_available()
