@@ -222,13 +222,18 @@ class Context:
         if pos is not None:
             p = _i32(pos); keep.append(p); b.pos = _ptr(p, C.c_int32)
         if seq_ids is not None:
-            rows = [_i32(s if hasattr(s, "__len__") else [s]) for s in seq_ids]
-            keep += rows
-            nsid = _i32([len(r) for r in rows]); keep.append(nsid)
-            arr = (C.POINTER(C.c_int32) * n)(*[_ptr(r, C.c_int32) for r in rows])
-            keep.append(arr)
+            # one flat id array; row i's pointer is its start inside it
+            if len(seq_ids) != n:
+                raise ValueError("seq_ids needs one row per token")
+            rows = [r if hasattr(r, "__len__") else (r,) for r in seq_ids]
+            nsid = np.fromiter((len(r) for r in rows), dtype=np.int32, count=n)
+            flat = np.fromiter((x for r in rows for x in r), dtype=np.int32, count=int(nsid.sum()))
+            start = np.zeros(n, dtype=np.uint64)
+            np.cumsum(nsid[:-1], out=start[1:])
+            ptrs = np.ascontiguousarray(np.uint64(flat.ctypes.data) + np.uint64(4) * start)
+            keep += [nsid, flat, ptrs]
             b.n_seq_id = _ptr(nsid, C.c_int32)
-            b.seq_id = C.cast(arr, C.POINTER(C.POINTER(C.c_int32)))
+            b.seq_id = ptrs.ctypes.data_as(C.POINTER(C.POINTER(C.c_int32)))
         if logits is not None:
             lg = np.ascontiguousarray(np.asarray(logits, dtype=np.int8)); keep.append(lg)
             b.logits = _ptr(lg, C.c_int8)
