@@ -299,10 +299,10 @@ attn_decode_kernel(AttnArgs a, float scale_log2) {
 // Each pass is a chain of dependent steps per warp (MMAs, shuffles of the softmax, the P^T
 // exchange); at 8192 cells over 16-block clusters the kernel is latency-bound (9% issue-active,
 // DRAM at 16% of peak, stalls spread over fixed-latency waits, L1/shared loads and barriers). The
-// K Q^T chain runs in four independent accumulators. Blocks stay at 4 warps (MW): 8-warp blocks
-// and deeper pipelines (three or four stages) measured slower at that length, since a block above
-// ~113 KB of shared memory takes an SM alone and leaves no room for the next GEMV's blocks that
-// start early under programmatic dependent launch.
+// K Q^T chain runs in four independent accumulators. Blocks stay at 4 warps (MW) and two stages:
+// 8-warp blocks and four stages measured slower at that length (a block above ~113 KB of shared
+// memory takes an SM alone and leaves no room for the next GEMV's blocks that start early under
+// programmatic dependent launch), three stages within 1%.
 constexpr int kMC = 16;                  // cells per warp and pass (one m16 fragment)
 
 // KT = int8_t: a Q8_0 cache. Its int8 rows and fp16 scales are staged as they are, the rows
