@@ -28,6 +28,9 @@ def test_block_layout_and_printed_sizes():
     x = np.random.default_rng(1).normal(size=(3, 256))
     raw = OF.quantize_q8_0(x)
     assert raw.shape == (3, 272) and raw.dtype == np.uint8         # ffn_gate row: nb[1] = 272
+    # the whole ffn_gate {256, 704} of the tiny model: nb[2] = bytes = 191488
+    assert OF.quantize_q8_0(np.zeros((704, 256))).nbytes == 191488
+    assert OF.type_row_bytes(OF.Q8_0, 256) * 704 == 191488
     # tiny model: 4 layers x 64 values x 4096 cells -> "K (q8_0): 1.06 MiB"
     per_layer = OF.quantize_q8_0(np.zeros((4096, 64))).nbytes
     assert per_layer == 4096 * 64 // 32 * 34
