@@ -335,12 +335,20 @@ int llm_debug_gemm_bf16(int32_t epi, const void *W, int64_t M, int64_t K, const 
  * kernel's error word) is a fixed 256-byte array inside the library that every GPU which loads
  * the library holds until the process exits. The first call on a device looks that array's
  * device address up (cudaGetSymbolAddress) with the device current; make that first call before
- * starting any stream capture. Every call shares the array, so calls whose GPU work overlaps
- * (from several host threads or streams) race on it. Arguments, limits and results are those of
+ * starting any stream capture. The address is kept for the life of the process: a device reset
+ * (cudaDeviceReset, or anything else that destroys the device's primary context) unloads the
+ * array, so do not call this entry point on a device after resetting it. Every call shares the
+ * array, so calls whose GPU work overlaps (from several host threads or streams) race on it; each
+ * call clears the error word before its launch. Arguments, limits and results are those of
  * llm_debug_gemm_bf16: -1 for an unsupported shape, -3 if the launch failed or the kernel
  * reported an error. Synchronous (legacy default stream). */
 int llm_gemm_bf16_noalloc(int32_t epi, const void *W, int64_t M, int64_t K, const void *X,
                           int32_t T, void *Y, int32_t ldy, int32_t F);
+
+/* Test hook of llm_gemm_bf16_noalloc: write `value` into its error word on the current device
+ * (synchronous), as a previous call that failed would leave it, so a test can check that the
+ * next call starts from a cleared word. Returns 0, or -3 if the copy failed. */
+int llm_debug_noalloc_scratch_poke(uint32_t value);
 
 /* Timeline of the persistent one-token kernel. enable != 0 makes later one-token steps record, per
  * block, global-timer stamps (ns) at the start and end of each consumer phase and at the first

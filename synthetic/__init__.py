@@ -119,6 +119,30 @@ def weight_bytes(seed: int, name: str, shape: tuple, wtype: int, device="cpu",
     raise ValueError(f"unsupported weight type {wtype}")
 
 
+def weight_rows(seed: int, name: str, shape: tuple, wtype: int, rows, device="cpu",
+                sigma: float = 0.02, q8_scale_sigma: float = 2e-4) -> torch.Tensor:
+    """Rows `rows` (indices into ne1) of the tensor weight_bytes would make, without making the
+    rest: the same counters, so the bytes equal weight_bytes(...)[rows]."""
+    ne0 = int(shape[0])
+    key = name_key(seed, name)
+    out = []
+    for r in (int(x) for x in rows):
+        if wtype in (F32, F16, BF16):
+            dt = {F32: torch.float32, F16: torch.float16, BF16: torch.bfloat16}[wtype]
+            out.append(normal_f32(key, ne0, sigma, device, start=r * ne0).to(dt))
+        elif wtype == Q8_0:
+            nb, b0 = ne0 // QK8_0, r * (ne0 // QK8_0)
+            blk = torch.empty((nb, Q8_0_BLOCK_BYTES), dtype=torch.uint8, device=device)
+            d = normal_f32(key ^ 0x5A5A5A5A, nb, q8_scale_sigma, device, start=b0).abs().to(torch.float16)
+            q = uniform_int(key, nb * QK8_0, -127, 127, device, start=b0 * QK8_0).to(torch.int8)
+            blk[:, 0:2] = d.view(torch.uint8).view(nb, 2)
+            blk[:, 2:] = q.view(torch.uint8).view(nb, QK8_0)
+            out.append(blk.view(-1))
+        else:
+            raise ValueError(f"unsupported weight type {wtype}")
+    return torch.stack(out)
+
+
 def prompt_tokens(seed: int, n: int, n_vocab: int, device="cpu") -> torch.Tensor:
     """n token ids uniform over [0, n_vocab) (int32)."""
     key = name_key(seed, "prompt")

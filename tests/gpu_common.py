@@ -175,3 +175,28 @@ def captured_rows(ctx, il: int, rows):
     x_in = src.reshape(-1, d)[rows]
     x_out = ctx.debug_tensor("l_out", il).reshape(-1, d)[rows]
     return x_in, x_out
+
+
+def mirror_ctx(w, **over):
+    """The oracle's batch and cell bookkeeping alone (no forward pass), run beside the library."""
+    kw = dict(n_ctx=w.n_ctx, n_seq_max=w.n_seq, type_k=w.type_kv, type_v=w.type_kv,
+              n_batch=w.n_batch, n_ubatch=w.n_ubatch)
+    kw.update(over)
+    return oracle.OracleContext(w.hp, None, compute=False, **kw)
+
+
+def mirror_slots(m):
+    return np.concatenate([np.asarray(u["slots"], dtype=np.int32) for u in m.last_ubatches])
+
+
+def check_layers(ctx, ow, w, layers, rows, bidx, pos, seqs, mirror, report, tag, tol):
+    """layer_check for the captured rows `rows` of the library's last ubatch (batch indices bidx,
+    positions pos, sequence ids seqs), with the mirror's visibility of the cells."""
+    slots = ctx.last_slots()
+    vis = mirror.cells.mask(pos, seqs, mirror.cells.n_kv())
+    for il in layers:
+        x_in, x_out = captured_rows(ctx, il, rows)
+        kc, vc = kv_layer(ctx, il)
+        e = layer_check(ow, w.hp, il, x_in, x_out, pos, slots[bidx], vis, kc, vc, w.type_kv)
+        report[f"{tag}_layer{il}"] = e
+        assert max(e.values()) <= tol, (tag, il, e)

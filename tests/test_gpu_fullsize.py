@@ -26,24 +26,14 @@ TOL = 2e-2
 
 
 def _mirror(w):
-    return oracle.OracleContext(w.hp, None, n_ctx=w.n_ctx, n_seq_max=w.n_seq, type_k=w.type_kv,
-                                type_v=w.type_kv, n_batch=w.n_batch, n_ubatch=w.n_ubatch,
-                                compute=False)
+    return G.mirror_ctx(w)
 
 
-def _mirror_slots(m):
-    return np.concatenate([np.asarray(u["slots"], dtype=np.int32) for u in m.last_ubatches])
+_mirror_slots = G.mirror_slots
 
 
 def _check_layers(ctx, ow, w, layers, rows, bidx, pos, seqs, mirror, report, tag):
-    slots = ctx.last_slots()
-    vis = mirror.cells.mask(pos, seqs, mirror.cells.n_kv())
-    for il in layers:
-        x_in, x_out = G.captured_rows(ctx, il, rows)
-        kc, vc = G.kv_layer(ctx, il)
-        e = G.layer_check(ow, w.hp, il, x_in, x_out, pos, slots[bidx], vis, kc, vc, w.type_kv)
-        report[f"{tag}_layer{il}"] = e
-        assert max(e.values()) <= TOL, (tag, il, e)
+    G.check_layers(ctx, ow, w, layers, rows, bidx, pos, seqs, mirror, report, tag, TOL)
 
 
 def test_llama8b_q8_0_8k_prompt_and_decode_layerwise():
@@ -185,3 +175,54 @@ def test_llama8b_bf16_32seq_batched_layerwise_isolation_and_seq_rm():
         assert e <= TOL, (s, e)
         one.free()
     print("bf16 32-seq layerwise parity:", report)
+
+
+def test_llama8b_bf16_32seq_literal_65536_cells_error_path():
+    """The 32-sequence workload with the cache size it names (65536 cells): the prompts fill every
+    cell, so the first decode step returns 1 and leaves each sequence's positions and the K/V
+    rows as they were; after seq_rm of the upper half of sequence 0, 32 steps of 32 tokens run
+    (slots bit-exact against the oracle's bookkeeping) and the next step returns 1 again.
+    ("Як це працює", Крок 11-12; "デコードループ", エラーリカバリとステートロールバック.)"""
+    key = "llama8b_bf16_32seq"
+    w = S.WORKLOADS[key]
+    n_seq, n_p = w.n_seq, w.n_prompt
+    ctx = G.library_ctx(key, n_ctx=65536)
+    mirror = G.mirror_ctx(w, n_ctx=65536)
+    prompts = G.prompts(key)
+    for s in range(n_seq):
+        flags = np.zeros(n_p, dtype=np.int8)
+        flags[-1] = 1
+        assert ctx.decode(prompts[s], seq_ids=[[s]] * n_p, logits=flags) == 0, ctx.last_error()
+        assert mirror.decode(prompts[s], seq_id=[[s]] * n_p, n_seq_id=[1] * n_p, logits=flags) == 0
+    assert ctx.kv_used_cells() == 65536
+    nxt = [ctx.get_argmax_ith(-1)] * n_seq
+    seqs = [[s] for s in range(n_seq)]
+
+    def state():
+        return [(ctx.seq_pos_min(s), ctx.seq_pos_max(s)) for s in range(n_seq)] + [ctx.kv_used_cells()]
+
+    def kv_digest():
+        return [hash(ctx.kv_cache(il, j).tobytes()) for il in (0, w.hp.n_layer - 1) for j in (0, 1)]
+
+    st0, kv0 = state(), kv_digest()
+    assert ctx.decode(nxt, seq_ids=seqs, logits=[1] * n_seq) == 1
+    assert mirror.decode(nxt, seq_id=seqs, n_seq_id=[1] * n_seq, logits=[1] * n_seq) == 1
+    assert state() == st0
+    # the retry's defrag finds the cache already packed: no row moves
+    assert kv_digest() == kv0
+    assert ctx.get_logits_ith(-1) is None
+    half = (ctx.seq_pos_max(0) + 1) // 2
+    assert ctx.seq_rm(0, half, -1) == 1 and mirror.seq_rm(0, half, -1)
+    assert ctx.kv_used_cells() == 65536 - 1024
+    for i in range(32):
+        assert ctx.decode(nxt, seq_ids=seqs, logits=[1] * n_seq) == 0, (i, ctx.last_error())
+        assert mirror.decode(nxt, seq_id=seqs, n_seq_id=[1] * n_seq, logits=[1] * n_seq) == 0
+        assert np.array_equal(ctx.last_slots(), G.mirror_slots(mirror)), i
+        nxt = [ctx.get_argmax_ith(j) for j in range(n_seq)]
+        assert all(0 <= t < w.hp.n_vocab for t in nxt)
+    assert ctx.kv_used_cells() == 65536
+    st1 = state()
+    assert ctx.decode(nxt, seq_ids=seqs, logits=[1] * n_seq) == 1
+    assert mirror.decode(nxt, seq_id=seqs, n_seq_id=[1] * n_seq, logits=[1] * n_seq) == 1
+    assert state() == st1
+    ctx.free()

@@ -55,8 +55,10 @@ def test_tiny_8seq_batched_prompt_and_greedy_steps():
     for k, u in enumerate(ora.last_ubatches):
         assert np.array_equal(ctx.ubatch_mask(k), u["mask"]), k
     rows = [(s + 1) * w.n_prompt - 1 for s in range(w.n_seq)]
-    rep = G.greedy_compare(ctx, ora, w.n_seq, rows, 32, TOL, {})
-    assert rep["tokens_checked"] >= 100
+    # the workload's whole run: 128 greedy steps of one token per sequence
+    rep = G.greedy_compare(ctx, ora, w.n_seq, rows, w.n_decode, TOL, {})
+    assert rep["tokens_checked"] >= 400
+    assert all(ctx.seq_pos_max(s) == w.n_prompt + w.n_decode - 1 for s in range(w.n_seq))
     ctx.free()
 
 
@@ -139,10 +141,13 @@ def test_error_paths_on_gpu():
     assert ref.decode(toks[:20]) == 2
     assert ref.seq_pos_max(0) == 31 + 16
     ref.set_abort_callback(None)
-    # a full cache returns 1 and changes nothing
+    # a batch within n_batch that the cache cannot hold returns 1 and changes nothing
     used = ref.kv_used_cells()
-    assert ref.decode(np.zeros(256 - used + 1, dtype=np.int32)) in (1, -1)
-    assert ref.kv_used_cells() == used
+    pmax = ref.seq_pos_max(0)
+    assert ref.decode(np.zeros(256 - used + 1, dtype=np.int32)) == 1, ref.last_error()
+    assert ref.kv_used_cells() == used and ref.seq_pos_max(0) == pmax
+    assert ref.get_logits_ith(-1) is None
+    assert ref.decode(np.zeros(256 - used, dtype=np.int32)) == 0      # exactly the free cells fit
     ctx.free(); ref.free()
 
 

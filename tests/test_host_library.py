@@ -276,3 +276,51 @@ def test_split_cache_matches_oracle_randomized(T, seed):
             codes.append(_decode_both(lib, ora, toks, seqs, logits=[1] * n))
         _same_state(lib, ora, n_seq)
     assert codes.count(0) >= 20 and 1 in codes
+
+
+def test_literal_65536_cell_cache_of_the_32_sequence_workload(T):
+    """The 32-sequence workload read literally: 32 prompts of 2048 tokens fill all 65536 cells, so
+    the first decode step (one token per sequence) finds no cell and returns 1 with every cell
+    holding what it held; seq_rm of the upper half of sequence 0 frees 1024 cells, which 32 steps
+    of 32 tokens use up (lowest cells first), and the 33rd step returns 1 again, changing no
+    sequence's positions. The failed search is retried once after a defrag, which may move cells
+    (the second failure does: the freed cells sit between used ones), so what must stay is each
+    sequence's set of positions, and the library's cells must equal the oracle's.
+    ("Як це працює", Крок 11-12: no slot for a ubatch -> 1 before any ubatch is committed;
+    "デコードループ", KVキャッシュの詳細 (FAILED_PREPARE -> defrag -> retry) and
+    エラーリカバリとステートロールバック.)"""
+
+    def content(o):
+        return sorted((s, int(o.cells.pos[c])) for c in np.nonzero(o.cells.pos >= 0)[0]
+                      for s in np.nonzero(o.cells.seq[c])[0])
+
+    n_seq, n_p = 32, 2048
+    lib, ora = _pair(T, n_ctx=65536, n_seq=n_seq, n_batch=2048, n_ubatch=512)
+    for s in range(n_seq):
+        flags = [0] * (n_p - 1) + [1]
+        assert _decode_both(lib, ora, [s + 1] * n_p, [[s]] * n_p, logits=flags) == 0
+    assert lib.kv_used_cells() == 65536
+    seqs = [[s] for s in range(n_seq)]
+    step = [5] * n_seq
+    before = content(ora)
+    assert _decode_both(lib, ora, step, seqs, logits=[1] * n_seq) == 1
+    _same_state(lib, ora, n_seq)
+    assert content(ora) == before
+    assert all(lib.seq_pos_max(s) == n_p - 1 for s in range(n_seq))
+    half = (lib.seq_pos_max(0) + 1) // 2
+    assert lib.seq_rm(0, half, -1) == 1 and ora.seq_rm(0, half, -1)
+    _same_state(lib, ora, n_seq)
+    assert lib.kv_used_cells() == 65536 - 1024
+    for i in range(32):
+        assert _decode_both(lib, ora, step, seqs, logits=[1] * n_seq) == 0, i
+        assert lib.last_slots().min() >= half      # the freed cells of sequence 0, lowest first
+    assert lib.kv_used_cells() == 65536
+    assert lib.seq_pos_max(0) == half + 31 and lib.seq_pos_max(1) == n_p + 31
+    before = content(ora)
+    assert _decode_both(lib, ora, step, seqs, logits=[1] * n_seq) == 1
+    _same_state(lib, ora, n_seq)
+    assert content(ora) == before
+    # the library's cells after its defrag are the oracle's, cell by cell: the next batch that
+    # fits takes the same slots on both sides
+    lib.seq_rm(5, n_p, -1); ora.seq_rm(5, n_p, -1)
+    assert _decode_both(lib, ora, [9] * 8, [[5]] * 8) == 0

@@ -94,6 +94,7 @@ SIGNATURES = {
     "llm_debug_kernel_timing": (C.c_int, [C.c_void_p, C.c_int]),
     "llm_gemm_bf16_noalloc": (C.c_int, [C.c_int32, C.c_void_p, C.c_int64, C.c_int64, C.c_void_p,
                                         C.c_int32, C.c_void_p, C.c_int32, C.c_int32]),
+    "llm_debug_noalloc_scratch_poke": (C.c_int, [C.c_uint32]),
     "llm_debug_gemm_bf16": (C.c_int, [C.c_int32, C.c_void_p, C.c_int64, C.c_int64, C.c_void_p,
                                       C.c_int32, C.c_void_p, C.c_int32, C.c_int32]),
     "llm_debug_kernel_stats": (C.c_int32, [C.c_void_p, C.c_int32, C.c_char_p, C.c_int32,
@@ -144,6 +145,11 @@ def gemm_bf16_noalloc(epi: int, W, X, Y, F: int = 0) -> int:
     return lib().llm_gemm_bf16_noalloc(epi, C.c_void_p(W.data_ptr()), W.shape[0], W.shape[1],
                                        C.c_void_p(X.data_ptr()), X.shape[0],
                                        C.c_void_p(Y.data_ptr()), Y.stride(0), F)
+
+
+def debug_noalloc_scratch_poke(value: int) -> int:
+    """Plant a value in the allocation-free GEMM's error word on the current device."""
+    return lib().llm_debug_noalloc_scratch_poke(value)
 
 
 class Context:

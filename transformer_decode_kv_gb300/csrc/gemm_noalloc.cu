@@ -67,3 +67,9 @@ extern "C" int llm_gemm_bf16_noalloc(int32_t epi, const void* W, int64_t M, int6
          cudaMemcpy(&h, err, sizeof(uint32_t), cudaMemcpyDeviceToHost) == cudaSuccess;
     return ok && h == 0 ? 0 : -3;
 }
+
+extern "C" int llm_debug_noalloc_scratch_poke(uint32_t value) {
+    uint32_t* err = scratch_on_current_device();
+    if (!err) return -3;
+    return cudaMemcpy(err, &value, sizeof(uint32_t), cudaMemcpyHostToDevice) == cudaSuccess ? 0 : -3;
+}
