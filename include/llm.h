@@ -328,6 +328,21 @@ int32_t llm_debug_kernel_stats(llm_ctx *ctx, int32_t i, char *name, int32_t name
 int llm_debug_gemm_bf16(int32_t epi, const void *W, int64_t M, int64_t K, const void *X, int32_t T,
                         void *Y, int32_t ldy, int32_t F);
 
+/* One launch of the token-major tensor-core GEMM the prefill ubatches use, on device buffers,
+ * synchronous ([P2] "llama.cpp Architecture", Example 4: MUL_MAT of a {K, M} weight by the
+ * ubatch's activations, ADD, SWIGLU). W f16 row-major [rows][K] (W_lo optional: a second f16 term
+ * of the same weights, both multiplied into the sums, as a Q8_0 weight's d*q is held), X f16
+ * row-major [T][K], K % 64 == 0. epi 0: Y[t][m] = sum_k W[m][k] X[t][k] as float32 (rows = M,
+ * M % 256 == 0; with splits > 1 the K range is split over `splits` CTAs whose partial sums are
+ * added atomically, so Y must start zeroed); epi 1: the same added into Y; epi 2: Y[t][j] (f16,
+ * ldy in f16 elements) = silu(gate_j) * up_j with gate rows [0, F) and up rows [F, 2F) of W
+ * (F % 128 == 0, splits 1). one_cta != 0 keeps the one-CTA kernel for T > 128 (the two-CTA
+ * cta_group::2 kernel otherwise). Returns 0, -1 for an unsupported shape, -3 if the launch
+ * failed or the kernel reported an error. */
+int llm_debug_gemm_tn_f16(int32_t epi, const void *W, const void *W_lo, int64_t M, int64_t K,
+                          const void *X, int32_t T, float *Y, int32_t ldy, int32_t F, int32_t splits,
+                          int32_t one_cta);
+
 /* The same GEMM as llm_debug_gemm_bf16, for callers that cannot allocate device memory (for
  * example engines that reserve all GPU memory up front for their own pools, or code that must
  * not trigger the device-wide synchronisation cudaFree performs). The pages have no counterpart:

@@ -95,6 +95,8 @@ SIGNATURES = {
     "llm_gemm_bf16_noalloc": (C.c_int, [C.c_int32, C.c_void_p, C.c_int64, C.c_int64, C.c_void_p,
                                         C.c_int32, C.c_void_p, C.c_int32, C.c_int32]),
     "llm_debug_noalloc_scratch_poke": (C.c_int, [C.c_uint32]),
+    "llm_debug_gemm_tn_f16": (C.c_int, [C.c_int32, C.c_void_p, C.c_void_p, C.c_int64, C.c_int64, C.c_void_p,
+                                        C.c_int32, C.c_void_p, C.c_int32, C.c_int32, C.c_int32, C.c_int32]),
     "llm_debug_gemm_bf16": (C.c_int, [C.c_int32, C.c_void_p, C.c_int64, C.c_int64, C.c_void_p,
                                       C.c_int32, C.c_void_p, C.c_int32, C.c_int32]),
     "llm_debug_kernel_stats": (C.c_int32, [C.c_void_p, C.c_int32, C.c_char_p, C.c_int32,
@@ -145,6 +147,15 @@ def gemm_bf16_noalloc(epi: int, W, X, Y, F: int = 0) -> int:
     return lib().llm_gemm_bf16_noalloc(epi, C.c_void_p(W.data_ptr()), W.shape[0], W.shape[1],
                                        C.c_void_p(X.data_ptr()), X.shape[0],
                                        C.c_void_p(Y.data_ptr()), Y.stride(0), F)
+
+
+def debug_gemm_tn_f16(epi: int, W, X, Y, F: int = 0, W_lo=None, splits: int = 1, one_cta: bool = False) -> int:
+    """One token-major tensor-core GEMM launch on torch CUDA tensors (W [rows][K] f16, X [T][K] f16)."""
+    M = W.shape[0] if epi != 2 else 0
+    return lib().llm_debug_gemm_tn_f16(epi, C.c_void_p(W.data_ptr()),
+                                       C.c_void_p(W_lo.data_ptr()) if W_lo is not None else None,
+                                       M, W.shape[1], C.c_void_p(X.data_ptr()), X.shape[0],
+                                       C.c_void_p(Y.data_ptr()), Y.stride(0), F, splits, int(one_cta))
 
 
 def debug_noalloc_scratch_poke(value: int) -> int:

@@ -350,6 +350,89 @@ struct TnCfg {
     static constexpr size_t kSmem = 1024 + (size_t)kStages * kStage + 256;
 };
 
+// Epilogue of the token-major GEMM: thread (warp, lane) drains TMEM lane 32 warp + lane, the
+// accumulator row of token t, and writes its outputs: SwiGLU silu(gate_j) * up_j of the 128
+// features from f0 (gate in columns j, up in 128 + j) as f16 (one term) or bf16 hi + lo, or the
+// 256 store / residual-add columns from f0 as float32 (vector atomic adds when K is split).
+template <int EPI, bool A2>
+__device__ __forceinline__ void tn_epilogue(uint32_t tmem, int warp, int t, int T, int M, int f0, bool live,
+                                            bool atomic, void* __restrict__ Y, void* __restrict__ Y2,
+                                            int ldy) {
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    if (EPI == GEMM_EPI_SWIGLU && !A2) {
+#pragma unroll 1
+        for (int j0 = 0; j0 < kTnN / 2; j0 += 16) {
+            float g[16], u[16];
+            tmem_ld16(tmem + lane_base + (uint32_t)j0, g);
+            tmem_ld16(tmem + lane_base + (uint32_t)(kTnN / 2 + j0), u);
+            if (!live || t >= T) continue;
+            uint32_t h[8];
+#pragma unroll
+            for (int j = 0; j < 16; j += 2) {
+                const float o0 = g[j] / (1.0f + expf(-g[j])) * u[j];
+                const float o1 = g[j + 1] / (1.0f + expf(-g[j + 1])) * u[j + 1];
+                const __half2 hv = __floats2half2_rn(o0, o1);
+                h[j / 2] = *reinterpret_cast<const uint32_t*>(&hv);
+            }
+            uint4* dh = reinterpret_cast<uint4*>(static_cast<__half*>(Y) + (int64_t)t * ldy + f0 + j0);
+            dh[0] = make_uint4(h[0], h[1], h[2], h[3]);
+            dh[1] = make_uint4(h[4], h[5], h[6], h[7]);
+        }
+    } else if (EPI == GEMM_EPI_SWIGLU) {
+        __nv_bfloat16* Yb = static_cast<__nv_bfloat16*>(Y);
+        __nv_bfloat16* Yb2 = static_cast<__nv_bfloat16*>(Y2);
+#pragma unroll 1
+        for (int j0 = 0; j0 < kTnN / 2; j0 += 16) {
+            float g[16], u[16];
+            tmem_ld16(tmem + lane_base + (uint32_t)j0, g);
+            tmem_ld16(tmem + lane_base + (uint32_t)(kTnN / 2 + j0), u);
+            if (!live || t >= T) continue;
+            uint32_t hi[8], lo[8];
+#pragma unroll
+            for (int j = 0; j < 16; j += 2) {
+                const float o0 = g[j] / (1.0f + expf(-g[j])) * u[j];
+                const float o1 = g[j + 1] / (1.0f + expf(-g[j + 1])) * u[j + 1];
+                const __nv_bfloat162 h = __floats2bfloat162_rn(o0, o1);
+                const float2 hf = __bfloat1622float2(h);
+                const __nv_bfloat162 l2 = __floats2bfloat162_rn(o0 - hf.x, o1 - hf.y);
+                hi[j / 2] = *reinterpret_cast<const uint32_t*>(&h);
+                lo[j / 2] = *reinterpret_cast<const uint32_t*>(&l2);
+            }
+            uint4* dh = reinterpret_cast<uint4*>(Yb + (int64_t)t * ldy + f0 + j0);
+            dh[0] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+            dh[1] = make_uint4(hi[4], hi[5], hi[6], hi[7]);
+            if (Yb2) {
+                uint4* dl = reinterpret_cast<uint4*>(Yb2 + (int64_t)t * ldy + f0 + j0);
+                dl[0] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                dl[1] = make_uint4(lo[4], lo[5], lo[6], lo[7]);
+            }
+        }
+    } else {
+        float* Yf = static_cast<float*>(Y);
+#pragma unroll 1
+        for (int j0 = 0; j0 < kTnN; j0 += 16) {
+            float v[16];
+            tmem_ld16(tmem + lane_base + (uint32_t)j0, v);
+            if (!live || t >= T || f0 + j0 >= M) continue;
+            float4* dst = reinterpret_cast<float4*>(Yf + (int64_t)t * ldy + f0 + j0);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                float4 w4 = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+                if (atomic) {
+                    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst + q),
+                                 "f"(w4.x), "f"(w4.y), "f"(w4.z), "f"(w4.w) : "memory");
+                } else {
+                    if (EPI == GEMM_EPI_ADD) {
+                        const float4 o = dst[q];
+                        w4.x += o.x; w4.y += o.y; w4.z += o.z; w4.w += o.w;
+                    }
+                    dst[q] = w4;
+                }
+            }
+        }
+    }
+}
+
 template <int EPI, bool A2>
 __global__ void __launch_bounds__(128, 1)
 gemm_tn_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmXlo,
@@ -456,85 +539,179 @@ gemm_tn_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
     tc_fence_after();
     if (!have) atomicOr(err, ERR_TIMEOUT);
     const bool live = have && !*(volatile int*)abort_flag && nk > 0;
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-    const int t = t0 + warp * 32 + lane;
-    if (EPI == GEMM_EPI_SWIGLU && !A2) {
-#pragma unroll 1
-        for (int j0 = 0; j0 < kTnN / 2; j0 += 16) {
-            float g[16], u[16];
-            tmem_ld16(tmem + lane_base + (uint32_t)j0, g);
-            tmem_ld16(tmem + lane_base + (uint32_t)(kTnN / 2 + j0), u);
-            if (!live || t >= T) continue;
-            uint32_t h[8];
-#pragma unroll
-            for (int j = 0; j < 16; j += 2) {
-                const float o0 = g[j] / (1.0f + expf(-g[j])) * u[j];
-                const float o1 = g[j + 1] / (1.0f + expf(-g[j + 1])) * u[j + 1];
-                const __half2 hv = __floats2half2_rn(o0, o1);
-                h[j / 2] = *reinterpret_cast<const uint32_t*>(&hv);
-            }
-            uint4* dh = reinterpret_cast<uint4*>(static_cast<__half*>(Y) + (int64_t)t * ldy + f0 + j0);
-            dh[0] = make_uint4(h[0], h[1], h[2], h[3]);
-            dh[1] = make_uint4(h[4], h[5], h[6], h[7]);
-        }
-    } else if (EPI == GEMM_EPI_SWIGLU) {
-        __nv_bfloat16* Yb = static_cast<__nv_bfloat16*>(Y);
-        __nv_bfloat16* Yb2 = static_cast<__nv_bfloat16*>(Y2);
-#pragma unroll 1
-        for (int j0 = 0; j0 < kTnN / 2; j0 += 16) {
-            float g[16], u[16];
-            tmem_ld16(tmem + lane_base + (uint32_t)j0, g);
-            tmem_ld16(tmem + lane_base + (uint32_t)(kTnN / 2 + j0), u);
-            if (!live || t >= T) continue;
-            uint32_t hi[8], lo[8];
-#pragma unroll
-            for (int j = 0; j < 16; j += 2) {
-                const float o0 = g[j] / (1.0f + expf(-g[j])) * u[j];
-                const float o1 = g[j + 1] / (1.0f + expf(-g[j + 1])) * u[j + 1];
-                const __nv_bfloat162 h = __floats2bfloat162_rn(o0, o1);
-                const float2 hf = __bfloat1622float2(h);
-                const __nv_bfloat162 l2 = __floats2bfloat162_rn(o0 - hf.x, o1 - hf.y);
-                hi[j / 2] = *reinterpret_cast<const uint32_t*>(&h);
-                lo[j / 2] = *reinterpret_cast<const uint32_t*>(&l2);
-            }
-            uint4* dh = reinterpret_cast<uint4*>(Yb + (int64_t)t * ldy + f0 + j0);
-            dh[0] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-            dh[1] = make_uint4(hi[4], hi[5], hi[6], hi[7]);
-            if (Yb2) {
-                uint4* dl = reinterpret_cast<uint4*>(Yb2 + (int64_t)t * ldy + f0 + j0);
-                dl[0] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-                dl[1] = make_uint4(lo[4], lo[5], lo[6], lo[7]);
-            }
-        }
-    } else {
-        const bool atomic = gridDim.z > 1;
-        float* Yf = static_cast<float*>(Y);
-#pragma unroll 1
-        for (int j0 = 0; j0 < kTnN; j0 += 16) {
-            float v[16];
-            tmem_ld16(tmem + lane_base + (uint32_t)j0, v);
-            if (!live || t >= T || f0 + j0 >= M) continue;
-            float4* dst = reinterpret_cast<float4*>(Yf + (int64_t)t * ldy + f0 + j0);
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                float4 w4 = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-                if (atomic) {
-                    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst + q),
-                                 "f"(w4.x), "f"(w4.y), "f"(w4.z), "f"(w4.w) : "memory");
-                } else {
-                    if (EPI == GEMM_EPI_ADD) {
-                        const float4 o = dst[q];
-                        w4.x += o.x; w4.y += o.y; w4.z += o.z; w4.w += o.w;
-                    }
-                    dst[q] = w4;
-                }
-            }
-        }
-    }
+    tn_epilogue<EPI, A2>(tmem, warp, t0 + warp * 32 + lane, T, M, f0, live, gridDim.z > 1, Y, Y2, ldy);
     tc_fence_before();
     __syncthreads();
     if (warp == 0)
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                     "r"((uint32_t)kTnN));
+}
+
+// Two-CTA token-major GEMM (tcgen05.mma.cta_group::2), f16 operands: a cluster of two CTAs
+// computes a 256-token x 256-row tile. The MMA's A operand is the 256 tokens, 128 in each CTA's
+// shared memory, and its B operand the 256 weight rows (for SwiGLU 128 gate + 128 up rows), 128 in
+// each CTA; the leader CTA (cluster rank 0) issues every MMA and each CTA's TMEM receives the
+// accumulator rows of its own 128 tokens, all 256 columns, so the epilogue is the one-CTA
+// kernel's. A stage holds 32 KB per CTA against 48 KB for the same MMA work per SM in the one-CTA
+// tile, so six stages fit and each SM pulls two thirds of the bytes through its L2 port.
+// Both CTAs' copies of a stage complete on the leader's full barrier (the leader arms it for both
+// halves); the leader's commits arrive on the empty and accumulator barriers of both CTAs.
+constexpr uint32_t kTn2Half = 128 * kBK * 2;           // 16 KB: 128 rows x 64 f16
+constexpr uint32_t kTn2Stage = 2 * kTn2Half;           // this CTA's A half + B half
+constexpr int kTn2Stages = 6;
+constexpr size_t kTn2Smem = 1024 + (size_t)kTn2Stages * kTn2Stage + 256;
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// every thread of both CTAs arrives; shared-memory writes before it are visible after it
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// shared::cluster address of the same shared variable in CTA `rank` of the cluster
+__device__ __forceinline__ uint32_t cluster_addr(uint32_t saddr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+    return r;
+}
+
+// TMA tile into this CTA's shared memory whose completion is counted on an mbarrier of either CTA
+// of the pair (bar: a shared::cluster address)
+__device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* map, uint32_t bar, int x, int y) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y)
+        : "memory");
+}
+
+__device__ __forceinline__ void umma_f16_pair(uint32_t dtmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                              uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(dtmem),
+        "l"(a), "l"(b), "r"(idesc), "r"(accumulate));
+}
+
+// arrive (once) on the mbarrier at this shared offset in both CTAs when the MMAs issued so far end
+__device__ __forceinline__ void umma_commit_pair(uint64_t* bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+            smem_u32(bar)), "h"((uint16_t)3)
+        : "memory");
+}
+
+template <int EPI>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(128, 1)
+gemm_tn2_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
+                const __grid_constant__ CUtensorMap tmWlo, int planes, int K, int T, int M, int F,
+                void* __restrict__ Y, int ldy, uint32_t* __restrict__ err) {
+    constexpr int S = kTn2Stages;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * kTn2Stage);
+    uint64_t* empty = full + S;
+    uint64_t* accf = empty + S;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accf + 1);
+    int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
+
+    const uint32_t rank = cluster_rank();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nk_all = K / kBK;
+    const int per = (nk_all + gridDim.z - 1) / gridDim.z;
+    const int kb0 = min(nk_all, (int)blockIdx.z * per), nkp = min(nk_all, kb0 + per) - kb0;
+    const int nk = nkp * planes;
+    const int tm = (int)(blockIdx.x >> 1) * 2 * kTnRows + (int)rank * kTnRows;   // this CTA's tokens
+    const int f0 = blockIdx.y * (EPI == GEMM_EPI_SWIGLU ? kTnN / 2 : kTnN);
+    // this CTA's 128 weight rows: the gate (rank 0) or up (rank 1) rows of the features from f0,
+    // or rows f0 + 128 rank
+    const int wrow = EPI == GEMM_EPI_SWIGLU ? (rank ? F + f0 : f0) : f0 + (int)rank * (kTnN / 2);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        mbar_init(accf, 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmX)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmW)) : "memory");
+        if (planes > 1)
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmWlo)) : "memory");
+    }
+    if (warp == 0) {
+        // the pair allocates the same TMEM columns in both SMs (issued by one warp of each CTA)
+        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(tmem_slot)),
+                     "r"((uint32_t)kTnN));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;");
+    }
+    tc_fence_before();
+    cluster_sync_all();                 // barriers of both CTAs initialised, TMEM address written
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (threadIdx.x == 0) {
+        // ---- TMA producer (both CTAs): this CTA's 128 tokens and 128 weight rows per stage
+        int issued = 0;
+        for (int kb = 0; kb < nk; ++kb) {
+            const int s = kb % S;
+            const uint32_t ph = (uint32_t)(kb / S) & 1u;
+            if (kb >= S && !mbar_wait(&empty[s], ph ^ 1u)) { atomicOr(err, ERR_TIMEOUT); *(volatile int*)abort_flag = 1; break; }
+            if (*(volatile int*)abort_flag) break;
+            uint8_t* st = smem + (size_t)s * kTn2Stage;
+            const uint32_t fb = cluster_addr(smem_u32(&full[s]), 0);
+            if (rank == 0) mbar_expect_tx(&full[s], 2 * kTn2Stage);
+            const int kx = (kb0 + kb % nkp) * kBK;
+            const CUtensorMap* wm = kb < nkp ? &tmW : &tmWlo;
+            tma_load_2d_pair(st, &tmX, fb, kx, tm);
+            tma_load_2d_pair(st + kTn2Half, wm, fb, kx, wrow);
+            issued = kb + 1;
+        }
+        // drain: the copies issued have landed before the CTA can exit (the leader's full barrier
+        // counts both CTAs' bytes; the peer sees its last stage consumed)
+        if (rank == 0) {
+            for (int kb = (issued > S ? issued - S : 0); kb < issued; ++kb)
+                mbar_wait(&full[kb % S], (uint32_t)(kb / S) & 1u);
+        } else if (issued > 0) {
+            mbar_wait(&empty[(issued - 1) % S], (uint32_t)((issued - 1) / S) & 1u);
+        }
+    } else if (threadIdx.x == 32 && rank == 0) {
+        // ---- MMA issuer (leader): D[256 tokens][256] += X W^T, one MMA per 16-wide k-step
+        constexpr uint32_t idesc = idesc_f16(2 * kTnRows, kTnN);
+        bool ok = true;
+        for (int kb = 0; kb < nk; ++kb) {
+            const int s = kb % S;
+            const uint32_t ph = (uint32_t)(kb / S) & 1u;
+            if (!mbar_wait(&full[s], ph)) { ok = false; break; }
+            tc_fence_after();
+            const uint8_t* st = smem + (size_t)s * kTn2Stage;
+            const uint64_t ad = sdesc_sw128(smem_u32(st));
+            const uint64_t bd = sdesc_sw128(smem_u32(st + kTn2Half));
+#pragma unroll
+            for (int kk = 0; kk < kBK / 16; ++kk)
+                umma_f16_pair(tmem, ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2), idesc, (kb | kk) != 0 ? 1u : 0u);
+            umma_commit_pair(&empty[s]);
+        }
+        if (!ok) { atomicOr(err, ERR_TIMEOUT); *(volatile int*)abort_flag = 1; }
+        umma_commit_pair(accf);
+    }
+    __syncwarp();
+
+    const bool have = mbar_wait(accf, 0);
+    tc_fence_after();
+    if (!have) atomicOr(err, ERR_TIMEOUT);
+    const bool live = have && !*(volatile int*)abort_flag && nk > 0;
+    tn_epilogue<EPI, false>(tmem, warp, tm + warp * 32 + lane, T, M, f0, live, gridDim.z > 1, Y, nullptr, ldy);
+    tc_fence_before();
+    cluster_sync_all();                 // both CTAs done with the pair's TMEM and shared memory
+    if (warp == 0)
+        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem),
                      "r"((uint32_t)kTnN));
 }
 
@@ -603,10 +780,30 @@ int tc_token_tile(int T) { return T > 128 ? 256 : 128; }
 bool tc_swiglu_tn_ok(int64_t K, int64_t F) { return K % kBK == 0 && K >= kBK && F % (kTnN / 2) == 0 && F > 0; }
 bool tc_tn_ok(int64_t M, int64_t K) { return K % kBK == 0 && K >= kBK && M % kTnN == 0 && M > 0; }
 
+// The two-CTA kernel serves f16 operands when the ubatch fills more than one 128-token tile.
+template <int EPI>
+bool launch_tn2(const CUtensorMap& xmap, const CUtensorMap& wmap, const CUtensorMap* wmap_lo, int K, int T,
+                int M, int F, void* Y, int ldy, int splits, uint32_t* err, cudaStream_t st) {
+    auto k = gemm_tn2_kernel<EPI>;
+    static bool attr = false;
+    if (!attr) {
+        if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTn2Smem) != cudaSuccess)
+            return false;
+        attr = true;
+    }
+    const int ntile = EPI == GEMM_EPI_SWIGLU ? F / (kTnN / 2) : M / kTnN;
+    dim3 grid(2 * ((T + 2 * kTnRows - 1) / (2 * kTnRows)), ntile, splits);
+    k<<<grid, 128, kTn2Smem, st>>>(xmap, wmap, wmap_lo ? *wmap_lo : wmap, wmap_lo ? 2 : 1, K, T, M, F, Y,
+                                   ldy, err);
+    return cudaGetLastError() == cudaSuccess;
+}
+
 template <int EPI, bool A2>
 bool launch_tn(const CUtensorMap& xmap, const CUtensorMap* xmap_lo, const CUtensorMap& wmap,
                const CUtensorMap* wmap_lo, int K, int T, int M, int F, void* Y, void* Y2, int ldy,
-               int splits, uint32_t* err, cudaStream_t st) {
+               int splits, uint32_t* err, cudaStream_t st, bool one_cta) {
+    if (!A2 && T > kTnRows && !one_cta)
+        return launch_tn2<EPI>(xmap, wmap, wmap_lo, K, T, M, F, Y, ldy, splits, err, st);
     using C = TnCfg<A2>;
     auto k = gemm_tn_kernel<EPI, A2>;
     static bool attr = false;
@@ -624,11 +821,13 @@ bool launch_tn(const CUtensorMap& xmap, const CUtensorMap* xmap_lo, const CUtens
 
 bool launch_gemm_swiglu_tn(const CUtensorMap& xmap, const CUtensorMap* xmap_lo, const CUtensorMap& wmap,
                            int K, int T, int F, void* Y, void* Y2, int ldy, uint32_t* err, cudaStream_t st,
-                           const CUtensorMap* wmap_lo) {
+                           const CUtensorMap* wmap_lo, bool one_cta) {
     if (T <= 0) return true;
     if (xmap_lo)
-        return launch_tn<GEMM_EPI_SWIGLU, true>(xmap, xmap_lo, wmap, wmap_lo, K, T, 0, F, Y, Y2, ldy, 1, err, st);
-    return launch_tn<GEMM_EPI_SWIGLU, false>(xmap, nullptr, wmap, wmap_lo, K, T, 0, F, Y, nullptr, ldy, 1, err, st);
+        return launch_tn<GEMM_EPI_SWIGLU, true>(xmap, xmap_lo, wmap, wmap_lo, K, T, 0, F, Y, Y2, ldy, 1, err, st,
+                                                one_cta);
+    return launch_tn<GEMM_EPI_SWIGLU, false>(xmap, nullptr, wmap, wmap_lo, K, T, 0, F, Y, nullptr, ldy, 1, err, st,
+                                             one_cta);
 }
 
 int tc_tn_splits(int64_t M, int64_t K, int T, int n_sm) {
@@ -641,18 +840,18 @@ int tc_tn_splits(int64_t M, int64_t K, int T, int n_sm) {
 
 bool launch_gemm_tn(const CUtensorMap& xmap, const CUtensorMap* xmap_lo, const CUtensorMap& wmap, int epi,
                     int K, int M, int T, float* Y, int ldy, int splits, uint32_t* err, cudaStream_t st,
-                    const CUtensorMap* wmap_lo) {
+                    const CUtensorMap* wmap_lo, bool one_cta) {
     if (T <= 0) return true;
     if (epi == GEMM_EPI_STORE)
         return xmap_lo ? launch_tn<GEMM_EPI_STORE, true>(xmap, xmap_lo, wmap, wmap_lo, K, T, M, 0, Y, nullptr, ldy,
-                                                         splits, err, st)
+                                                         splits, err, st, one_cta)
                        : launch_tn<GEMM_EPI_STORE, false>(xmap, nullptr, wmap, wmap_lo, K, T, M, 0, Y, nullptr, ldy,
-                                                          splits, err, st);
+                                                          splits, err, st, one_cta);
     if (epi == GEMM_EPI_ADD)
         return xmap_lo ? launch_tn<GEMM_EPI_ADD, true>(xmap, xmap_lo, wmap, wmap_lo, K, T, M, 0, Y, nullptr, ldy,
-                                                       splits, err, st)
+                                                       splits, err, st, one_cta)
                        : launch_tn<GEMM_EPI_ADD, false>(xmap, nullptr, wmap, wmap_lo, K, T, M, 0, Y, nullptr, ldy,
-                                                        splits, err, st);
+                                                        splits, err, st, one_cta);
     return false;
 }
 

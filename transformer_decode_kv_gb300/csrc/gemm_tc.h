@@ -41,9 +41,11 @@ bool launch_gemm_tc(const CUtensorMap& wmap, const CUtensorMap& xmap, int epi, i
 bool tc_swiglu_tn_ok(int64_t K, int64_t F);
 // With wmap_lo the weights are two bf16 terms as well (hi in wmap, lo in wmap_lo; a Q8_0 weight
 // d*q split so that hi + lo holds it to 16 bits): four products per k-step instead of two.
+// With f16 operands and more than 128 tokens the two-CTA kernel (tcgen05 cta_group::2, 256-token
+// tiles) runs unless one_cta is set.
 bool launch_gemm_swiglu_tn(const CUtensorMap& xmap, const CUtensorMap* xmap_lo, const CUtensorMap& wmap,
                            int K, int T, int F, void* Y, void* Y2, int ldy, uint32_t* err, cudaStream_t st,
-                           const CUtensorMap* wmap_lo = nullptr);
+                           const CUtensorMap* wmap_lo = nullptr, bool one_cta = false);
 
 // Store / residual add with the token tile as A (two bf16 terms) and 256 weight rows as B (wmap
 // over W [M][K], box 128 rows): Y [>= T][ldy] float32 (op)= X W^T. M % 256 == 0. splits > 1
@@ -53,6 +55,6 @@ bool tc_tn_ok(int64_t M, int64_t K);
 int tc_tn_splits(int64_t M, int64_t K, int T, int n_sm);
 bool launch_gemm_tn(const CUtensorMap& xmap, const CUtensorMap* xmap_lo, const CUtensorMap& wmap, int epi,
                     int K, int M, int T, float* Y, int ldy, int splits, uint32_t* err, cudaStream_t st,
-                    const CUtensorMap* wmap_lo = nullptr);
+                    const CUtensorMap* wmap_lo = nullptr, bool one_cta = false);
 
 }  // namespace llm

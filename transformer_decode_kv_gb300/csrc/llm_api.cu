@@ -1611,6 +1611,31 @@ int llm_debug_gemm_bf16(int32_t epi, const void* W, int64_t M, int64_t K, const 
     return ok && h == 0 ? 0 : -3;
 }
 
+int llm_debug_gemm_tn_f16(int32_t epi, const void* W, const void* W_lo, int64_t M, int64_t K, const void* X,
+                          int32_t T, float* Y, int32_t ldy, int32_t F, int32_t splits, int32_t one_cta) {
+    if (!W || !X || !Y || T <= 0 || epi < 0 || epi > 2 || splits < 1) return -1;
+    const bool swiglu = epi == GEMM_EPI_SWIGLU;
+    if (swiglu ? !tc_swiglu_tn_ok(K, F) : !tc_tn_ok(M, K)) return -1;
+    if (swiglu && splits != 1) return -1;
+    const int64_t wrows = swiglu ? 2 * (int64_t)F : M;
+    CUtensorMap wm, wl, xm;
+    if (!tc_make_map(&wm, W, wrows, K, 128, true) || !tc_make_map(&xm, X, T, K, 128, true) ||
+        (W_lo && !tc_make_map(&wl, W_lo, wrows, K, 128, true)))
+        return -1;
+    uint32_t* err = nullptr;
+    if (cudaMalloc(&err, sizeof(uint32_t)) != cudaSuccess) return -3;
+    cudaMemset(err, 0, sizeof(uint32_t));
+    bool ok = swiglu ? launch_gemm_swiglu_tn(xm, nullptr, wm, (int)K, T, F, Y, nullptr, ldy, err, 0,
+                                             W_lo ? &wl : nullptr, one_cta != 0)
+                     : launch_gemm_tn(xm, nullptr, wm, epi, (int)K, (int)M, T, Y, ldy, splits, err, 0,
+                                      W_lo ? &wl : nullptr, one_cta != 0);
+    uint32_t h = 0;
+    ok = ok && cudaDeviceSynchronize() == cudaSuccess &&
+         cudaMemcpy(&h, err, sizeof(uint32_t), cudaMemcpyDeviceToHost) == cudaSuccess;
+    cudaFree(err);
+    return ok && h == 0 ? 0 : -3;
+}
+
 int32_t llm_sample_ith(llm_ctx* c, int32_t i, const llm_sampler_params* p, float u) {
     constexpr int32_t kMaxPenalty = 4096;
     if (!c || !p || c->host_only) return -1;
