@@ -673,6 +673,7 @@ def main():
             "launches": gemm["launches"], "share_of_prompt": gemm["ms"] / pre_tot if pre_tot else None,
             "method": "CUDA events around each launch of one prompt (eager launches)"},
         "kernel_share": {k: v["ms"] / pre_tot for k, v in kp.items() if v["launches"]} if pre_tot else {},
+        "kernel_ms": {k: v["ms"] for k, v in kp.items() if v["launches"]},
     }
     line = {
         "metric": METRIC, "value": dec_tps, "unit": "tok/s", "n_gpus": world, "steps": K,

@@ -343,6 +343,15 @@ int llm_debug_gemm_tn_f16(int32_t epi, const void *W, const void *W_lo, int64_t 
                           const void *X, int32_t T, float *Y, int32_t ldy, int32_t F, int32_t splits,
                           int32_t one_cta);
 
+/* The two-CTA token-major GEMM of llm_debug_gemm_tn_f16 (T > 128, one weight term) with a
+ * timeline: per CTA 8 uint64 values in trace, global-timer stamps in ns (start, set-up done, first
+ * stage ready, last MMA issued, accumulator ready, epilogue done, end) and the SM id, CTAs in
+ * launch order (x fastest, then y, then z). Returns the number of values written (cap must hold
+ * them), -1 for an unsupported shape or a short buffer, -3 on a failure. */
+int64_t llm_debug_gemm_tn_f16_trace(int32_t epi, const void *W, int64_t M, int64_t K, const void *X,
+                                    int32_t T, float *Y, int32_t ldy, int32_t F, int32_t splits,
+                                    uint64_t *trace, int64_t cap);
+
 /* The same GEMM as llm_debug_gemm_bf16, for callers that cannot allocate device memory (for
  * example engines that reserve all GPU memory up front for their own pools, or code that must
  * not trigger the device-wide synchronisation cudaFree performs). The pages have no counterpart:

@@ -95,6 +95,9 @@ SIGNATURES = {
     "llm_gemm_bf16_noalloc": (C.c_int, [C.c_int32, C.c_void_p, C.c_int64, C.c_int64, C.c_void_p,
                                         C.c_int32, C.c_void_p, C.c_int32, C.c_int32]),
     "llm_debug_noalloc_scratch_poke": (C.c_int, [C.c_uint32]),
+    "llm_debug_gemm_tn_f16_trace": (C.c_int64, [C.c_int32, C.c_void_p, C.c_int64, C.c_int64, C.c_void_p, C.c_int32,
+                                              C.c_void_p, C.c_int32, C.c_int32, C.c_int32,
+                                              C.POINTER(C.c_uint64), C.c_int64]),
     "llm_debug_gemm_tn_f16": (C.c_int, [C.c_int32, C.c_void_p, C.c_void_p, C.c_int64, C.c_int64, C.c_void_p,
                                         C.c_int32, C.c_void_p, C.c_int32, C.c_int32, C.c_int32, C.c_int32]),
     "llm_debug_gemm_bf16": (C.c_int, [C.c_int32, C.c_void_p, C.c_int64, C.c_int64, C.c_void_p,
@@ -156,6 +159,17 @@ def debug_gemm_tn_f16(epi: int, W, X, Y, F: int = 0, W_lo=None, splits: int = 1,
                                        C.c_void_p(W_lo.data_ptr()) if W_lo is not None else None,
                                        M, W.shape[1], C.c_void_p(X.data_ptr()), X.shape[0],
                                        C.c_void_p(Y.data_ptr()), Y.stride(0), F, splits, int(one_cta))
+
+
+def debug_gemm_tn_f16_trace(epi: int, W, X, Y, F: int = 0, splits: int = 1):
+    """The two-CTA token-major GEMM with its per-CTA timeline: returns (status, [n_cta, 8] uint64)."""
+    M = W.shape[0] if epi != 2 else 0
+    cap = 8 * 4096
+    out = np.zeros(cap, dtype=np.uint64)
+    n = lib().llm_debug_gemm_tn_f16_trace(epi, C.c_void_p(W.data_ptr()), M, W.shape[1], C.c_void_p(X.data_ptr()),
+                                          X.shape[0], C.c_void_p(Y.data_ptr()), Y.stride(0), F, splits,
+                                          out.ctypes.data_as(C.POINTER(C.c_uint64)), cap)
+    return (0, out[:n].reshape(-1, 8)) if n > 0 else (int(n), None)
 
 
 def debug_noalloc_scratch_poke(value: int) -> int:

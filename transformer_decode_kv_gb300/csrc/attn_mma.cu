@@ -11,6 +11,8 @@
 //   O += P V        P as two f16 terms, V f16
 // so every product is float32-accurate to about 2^-22 and accumulates in float32. A cell is
 // visible to a row iff cell.pos <= token.pos (the list already holds only the sequence's cells).
+// ONE: Q and P as one f16 term each (half the MMAs), for a forward pass whose matrix products
+// already take f16 activations (the attention output is rounded to f16 for them anyway).
 // Partial states (o, m, l) and the ticket merge are shared with the CUDA-core kernel.
 //
 // A Q8_0 cache ([P2] Example 2 blocks: value d * q per 32 values) comes as f16 copies of its
@@ -126,7 +128,7 @@ __device__ __forceinline__ void store_index(int cell, int pos, int* ccell, int* 
 
 }  // namespace
 
-template <int HD, bool Q8>
+template <int HD, bool Q8, bool ONE>
 __global__ void __launch_bounds__(kWarps * 32, 2) attn_mma_kernel(AttnArgs a, float scale_log2) {
     using SM = MmaSmem<HD, Q8>;
     constexpr int RS = SM::RS, KC = HD / 16, NC = HD / 8, NB = SM::NB;
@@ -205,7 +207,7 @@ __global__ void __launch_bounds__(kWarps * 32, 2) attn_mma_kernel(AttnArgs a, fl
             uint32_t hi, lo;
             split_h2(x[i].x * scale_log2, x[i].y * scale_log2, hi, lo);
             *reinterpret_cast<uint32_t*>(qhs + r * RS + col) = hi;
-            *reinterpret_cast<uint32_t*>(qls + r * RS + col) = lo;
+            if (!ONE) *reinterpret_cast<uint32_t*>(qls + r * RS + col) = lo;
         }
     }
     const int r0 = warp * 16 + g, r1 = r0 + 8;
@@ -248,7 +250,7 @@ __global__ void __launch_bounds__(kWarps * 32, 2) attn_mma_kernel(AttnArgs a, fl
         auto qk = [&](float (&acc)[8][4], int kc) {
             uint32_t qh[4], ql[4];
             ldsm_x4(smem_addr(qhs + qrow * RS + kc * 16 + qcol), qh[0], qh[1], qh[2], qh[3]);
-            ldsm_x4(smem_addr(qls + qrow * RS + kc * 16 + qcol), ql[0], ql[1], ql[2], ql[3]);
+            if (!ONE) ldsm_x4(smem_addr(qls + qrow * RS + kc * 16 + qcol), ql[0], ql[1], ql[2], ql[3]);
             // K fragments of the 64 cells first, then the hi-term MMAs, then the lo-term ones,
             // so no two consecutive MMAs share an accumulator
             uint32_t kb[4][4];
@@ -265,10 +267,12 @@ __global__ void __launch_bounds__(kWarps * 32, 2) attn_mma_kernel(AttnArgs a, fl
                 mma16816(acc[2 * n2], qh, kb[n2][0], kb[n2][1]);
                 mma16816(acc[2 * n2 + 1], qh, kb[n2][2], kb[n2][3]);
             }
+            if (!ONE) {
 #pragma unroll
-            for (int n2 = 0; n2 < 4; ++n2) {
-                mma16816(acc[2 * n2], ql, kb[n2][0], kb[n2][1]);
-                mma16816(acc[2 * n2 + 1], ql, kb[n2][2], kb[n2][3]);
+                for (int n2 = 0; n2 < 4; ++n2) {
+                    mma16816(acc[2 * n2], ql, kb[n2][0], kb[n2][1]);
+                    mma16816(acc[2 * n2 + 1], ql, kb[n2][2], kb[n2][3]);
+                }
             }
         };
         if constexpr (Q8) {
@@ -368,10 +372,12 @@ __global__ void __launch_bounds__(kWarps * 32, 2) attn_mma_kernel(AttnArgs a, fl
                         mma16816(o[2 * (2 * b + i)], ph, vb[i][0], vb[i][1]);
                         mma16816(o[2 * (2 * b + i) + 1], ph, vb[i][2], vb[i][3]);
                     }
+                    if (!ONE) {
 #pragma unroll
-                    for (int i = 0; i < 2; ++i) {
-                        mma16816(o[2 * (2 * b + i)], pl, vb[i][0], vb[i][1]);
-                        mma16816(o[2 * (2 * b + i) + 1], pl, vb[i][2], vb[i][3]);
+                        for (int i = 0; i < 2; ++i) {
+                            mma16816(o[2 * (2 * b + i)], pl, vb[i][0], vb[i][1]);
+                            mma16816(o[2 * (2 * b + i) + 1], pl, vb[i][2], vb[i][3]);
+                        }
                     }
                 }
             }
@@ -401,10 +407,12 @@ __global__ void __launch_bounds__(kWarps * 32, 2) attn_mma_kernel(AttnArgs a, fl
                         mma16816(o[2 * (h4 + i)], ph, vb[i][0], vb[i][1]);
                         mma16816(o[2 * (h4 + i) + 1], ph, vb[i][2], vb[i][3]);
                     }
+                    if (!ONE) {
 #pragma unroll
-                    for (int i = 0; i < GS; ++i) {
-                        mma16816(o[2 * (h4 + i)], pl, vb[i][0], vb[i][1]);
-                        mma16816(o[2 * (h4 + i) + 1], pl, vb[i][2], vb[i][3]);
+                        for (int i = 0; i < GS; ++i) {
+                            mma16816(o[2 * (h4 + i)], pl, vb[i][0], vb[i][1]);
+                            mma16816(o[2 * (h4 + i) + 1], pl, vb[i][2], vb[i][3]);
+                        }
                     }
                 }
             }
@@ -462,11 +470,11 @@ __global__ void __launch_bounds__(kWarps * 32, 2) attn_mma_kernel(AttnArgs a, fl
     merge_tile<HD, kG>(a, kvh, s0, nq, w0, w1, reinterpret_cast<float*>(smem), 4 * SM::tile_bytes / 4);
 }
 
-template <int HD, bool Q8>
-bool launch_attention_mma_hd(const AttnArgs& a, cudaStream_t st) {
+template <int HD, bool Q8, bool ONE>
+bool launch_attention_mma_hd1(const AttnArgs& a, cudaStream_t st) {
     const float scale_log2 = (float)(1.4426950408889634 / sqrt((double)HD));
     constexpr size_t smem = MmaSmem<HD, Q8>::bytes;
-    auto k = attn_mma_kernel<HD, Q8>;
+    auto k = attn_mma_kernel<HD, Q8, ONE>;
     static bool attr = false;
     if (!attr) {
         if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
@@ -484,6 +492,13 @@ bool launch_attention_mma_hd(const AttnArgs& a, cudaStream_t st) {
     cfg.attrs = attr_l;
     cfg.numAttrs = a.pdl ? 1 : 0;
     return cudaLaunchKernelEx(&cfg, k, a, scale_log2) == cudaSuccess;
+}
+
+// one f16 term for Q and P when the output goes to f16 GEMM operands (a single f16 output)
+template <int HD, bool Q8>
+bool launch_attention_mma_hd(const AttnArgs& a, cudaStream_t st) {
+    return a.out_b && a.out_f16 ? launch_attention_mma_hd1<HD, Q8, true>(a, st)
+                                : launch_attention_mma_hd1<HD, Q8, false>(a, st);
 }
 
 bool attention_mma_ok(const AttnArgs& a) {

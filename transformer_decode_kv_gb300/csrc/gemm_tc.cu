@@ -147,6 +147,43 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+          "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
+          "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
+          "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// silu(g) * u with the fast exponential and divide (a few ulp; the result is then rounded to f16)
+__device__ __forceinline__ float silu_mul_fast(float g, float u) {
+    return __fdividef(g, 1.0f + __expf(-g)) * u;
+}
+
+// TMA tile store / reduce-add of a shared-memory box into the map's tensor (bulk-group completion)
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void* src, int x, int y) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)), "r"(smem_u32(src)), "r"(x), "r"(y)
+                 : "memory");
+}
+__device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* map, const void* src, int x, int y) {
+    asm volatile("cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)), "r"(smem_u32(src)), "r"(x), "r"(y)
+                 : "memory");
+}
+__device__ __forceinline__ void st_shared_v4(uint8_t* p, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(smem_u32(p)), "r"(a), "r"(b), "r"(c), "r"(d)
+                 : "memory");
+}
+
 // SPLIT: the activations come as two bf16 terms (hi + lo, about 16 significant bits); both are
 // multiplied into the same accumulator, so the product keeps float32-like activation precision.
 template <int BN, bool SPLIT = false>
@@ -433,10 +470,125 @@ __device__ __forceinline__ void tn_epilogue(uint32_t tmem, int warp, int t, int 
     }
 }
 
+// Epilogue through shared memory and TMA stores (f16 operands): warp w stages the accumulator rows
+// of its 32 tokens in 128-byte-swizzled boxes of 32 rows (store / add: 8 boxes of 32 float32
+// columns, 32 KB per warp; SwiGLU: 2 boxes of 64 f16 features, 8 KB per warp) in the pipeline's
+// shared memory, which the MMAs no longer read, and lane 0 writes them with bulk tensor copies:
+// a store, or an element-wise reduce-add in L2 for the residual add and for K splits (the partial
+// sums of several CTAs then add without atomics). Rows past T are written as zeros (a store) or
+// add nothing; a warp whose rows all lie past T writes nothing. The Q/K/V epilogue stores a Q
+// tile like a store after the rotation and writes K and V tiles straight to their cache rows.
+template <int EPI>
+__device__ __forceinline__ void tn_epilogue_tma(uint32_t tmem, int warp, int lane, int trow0, int T, int f0,
+                                                bool live, bool reduce, const CUtensorMap* ymap, uint8_t* smem,
+                                                const TnQkv& qe, uint32_t* err) {
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const int t = trow0 + lane;
+    const bool row_ok = t < T;
+    const uint32_t sw = (uint32_t)(lane & 7);
+    uint8_t* wbuf = smem + (size_t)warp * (EPI == GEMM_EPI_SWIGLU ? 8192 : 32768);
+    bool boxes = true;                               // whether this tile goes out through the boxes
+    if (EPI == GEMM_EPI_SWIGLU) {
+#pragma unroll 1
+        for (int j0 = 0; j0 < kTnN / 2; j0 += 32) {
+            float g[32], u[32];
+            tmem_ld32(tmem + lane_base + (uint32_t)j0, g);
+            tmem_ld32(tmem + lane_base + (uint32_t)(kTnN / 2 + j0), u);
+            uint32_t h[16];
+#pragma unroll
+            for (int j = 0; j < 32; j += 2) {
+                const __half2 hv = __floats2half2_rn(row_ok ? silu_mul_fast(g[j], u[j]) : 0.0f,
+                                                     row_ok ? silu_mul_fast(g[j + 1], u[j + 1]) : 0.0f);
+                h[j / 2] = *reinterpret_cast<const uint32_t*>(&hv);
+            }
+            uint8_t* row = wbuf + (j0 / 64) * 4096 + lane * 128;
+            const uint32_t c0 = (uint32_t)((j0 % 64) / 8);
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+                st_shared_v4(row + (((c0 + c) ^ sw) << 4), h[4 * c], h[4 * c + 1], h[4 * c + 2], h[4 * c + 3]);
+        }
+    } else {
+        // Q/K/V: which part the tile holds, and this token's cache cell for a K or V tile
+        const int qcols = qe.H * qe.hd, kcols = qe.Hkv * qe.hd;
+        const bool rot = EPI == GEMM_EPI_QKV && f0 < qcols + kcols;
+        const bool kv = EPI == GEMM_EPI_QKV && f0 >= qcols;
+        int32_t cell = 0;
+        if (kv) {
+            cell = row_ok ? qe.slot[t] : 0;
+            const bool ok = cell >= 0 && cell < qe.n_ctx;
+            if (row_ok && !ok && live) atomicOr(err, ERR_SLOT_RANGE);
+            boxes = false;
+            live = live && row_ok && ok;
+        }
+#pragma unroll 1
+        for (int b = 0; b < kTnN / 32; ++b) {
+            float v[32];
+            tmem_ld32(tmem + lane_base + (uint32_t)(32 * b), v);
+            const int col = f0 + 32 * b;
+            if (rot && row_ok) {
+                // adjacent pairs (2i, 2i + 1) of a head turn by the token's angle for pair i
+                const int e0 = col % qe.hd;
+                const float4* cs4 = reinterpret_cast<const float4*>(qe.cs + (int64_t)t * (qe.hd / 2) + e0 / 2);
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    const float4 e = cs4[q];            // (cos, sin) of pairs 2q and 2q + 1
+                    const float x0 = v[4 * q], x1 = v[4 * q + 1], x2 = v[4 * q + 2], x3 = v[4 * q + 3];
+                    v[4 * q] = x0 * e.x - x1 * e.y;
+                    v[4 * q + 1] = x0 * e.y + x1 * e.x;
+                    v[4 * q + 2] = x2 * e.z - x3 * e.w;
+                    v[4 * q + 3] = x2 * e.w + x3 * e.z;
+                }
+            }
+            if (kv) {
+                if (live) {
+                    const bool isk = col < qcols + kcols;
+                    const int kcol = col - (isk ? qcols : qcols + kcols);
+                    const int g = kcol / qe.hd, e0 = kcol % qe.hd;
+                    __half* dst = static_cast<__half*>(isk ? qe.kc : qe.vc) + ((int64_t)g * qe.n_ctx + cell) * qe.hd + e0;
+                    uint32_t h[16];
+#pragma unroll
+                    for (int j = 0; j < 32; j += 2) {
+                        const __half2 hv = __floats2half2_rn(v[j], v[j + 1]);
+                        h[j / 2] = *reinterpret_cast<const uint32_t*>(&hv);
+                    }
+                    uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) d4[c] = make_uint4(h[4 * c], h[4 * c + 1], h[4 * c + 2], h[4 * c + 3]);
+                }
+                continue;
+            }
+            uint8_t* row = wbuf + b * 4096 + lane * 128;
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                const float* q = v + 4 * c;
+                st_shared_v4(row + (((uint32_t)c ^ sw) << 4), row_ok ? __float_as_uint(q[0]) : 0u,
+                             row_ok ? __float_as_uint(q[1]) : 0u, row_ok ? __float_as_uint(q[2]) : 0u,
+                             row_ok ? __float_as_uint(q[3]) : 0u);
+            }
+        }
+    }
+    if (!boxes) return;
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    __syncwarp();
+    if (lane == 0 && live && trow0 < T) {
+        constexpr int nbox = EPI == GEMM_EPI_SWIGLU ? 2 : kTnN / 32;
+        constexpr int bw = EPI == GEMM_EPI_SWIGLU ? 64 : 32;
+#pragma unroll 1
+        for (int b = 0; b < nbox; ++b) {
+            if (reduce) tma_reduce_add_2d(ymap, wbuf + b * 4096, f0 + b * bw, trow0);
+            else tma_store_2d(ymap, wbuf + b * 4096, f0 + b * bw, trow0);
+        }
+        asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+        asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+    }
+    __syncwarp();
+}
+
 template <int EPI, bool A2>
 __global__ void __launch_bounds__(128, 1)
 gemm_tn_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmXlo,
                const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmWlo,
+               const __grid_constant__ CUtensorMap tmY, int use_ymap, const TnQkv qe,
                int planes, int K, int T, int M, int F,
                void* __restrict__ Y, void* __restrict__ Y2, int ldy, uint32_t* __restrict__ err) {
     using C = TnCfg<A2>;
@@ -488,6 +640,18 @@ gemm_tn_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
 
     if (threadIdx.x == 0) {
         // ---- TMA producer: per stage the two activation terms and the gate and up rows
+        // the weights of the first stages go out before the grid dependency wait (they do not
+        // depend on the kernel before), the activations after it
+        const int pre = min(nk, S);
+        for (int kb = 0; kb < pre; ++kb) {
+            uint8_t* st = smem + (size_t)kb * kTnStage;
+            const int kx = (kb0 + kb % nkp) * kBK;
+            const CUtensorMap* wm = kb < nkp ? &tmW : &tmWlo;
+            mbar_expect_tx(&full[kb], kTnStage);
+            tma_load_2d(st + kBOff, wm, &full[kb], kx, f0);
+            tma_load_2d(st + kBOff + kTnB / 2, wm, &full[kb], kx, w2);
+        }
+        asm volatile("griddepcontrol.wait;" ::: "memory");
         int issued = 0;
         for (int kb = 0; kb < nk; ++kb) {
             const int s = kb % S;
@@ -495,15 +659,18 @@ gemm_tn_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
             if (kb >= S && !mbar_wait(&empty[s], ph ^ 1u)) { atomicOr(err, ERR_TIMEOUT); *(volatile int*)abort_flag = 1; break; }
             if (*(volatile int*)abort_flag) break;
             uint8_t* st = smem + (size_t)s * kTnStage;
-            mbar_expect_tx(&full[s], kTnStage);
             const int kx = (kb0 + kb % nkp) * kBK;
             const CUtensorMap* wm = kb < nkp ? &tmW : &tmWlo;
+            if (kb >= S) {
+                mbar_expect_tx(&full[s], kTnStage);
+                tma_load_2d(st + kBOff, wm, &full[s], kx, f0);
+                tma_load_2d(st + kBOff + kTnB / 2, wm, &full[s], kx, w2);
+            }
             tma_load_2d(st, &tmX, &full[s], kx, t0);
             if (A2) tma_load_2d(st + kTnA, &tmXlo, &full[s], kx, t0);
-            tma_load_2d(st + kBOff, wm, &full[s], kx, f0);
-            tma_load_2d(st + kBOff + kTnB / 2, wm, &full[s], kx, w2);
             issued = kb + 1;
         }
+        if (issued < pre) issued = pre;
         for (int kb = (issued > S ? issued - S : 0); kb < issued; ++kb)
             mbar_wait(&full[kb % S], (uint32_t)(kb / S) & 1u);
     } else if (threadIdx.x == 32) {
@@ -537,9 +704,15 @@ gemm_tn_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
     // ---- epilogue: thread = token; gate columns j and up columns 128 + j of its TMEM lane
     const bool have = mbar_wait(accf, 0);
     tc_fence_after();
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;");
     if (!have) atomicOr(err, ERR_TIMEOUT);
     const bool live = have && !*(volatile int*)abort_flag && nk > 0;
-    tn_epilogue<EPI, A2>(tmem, warp, t0 + warp * 32 + lane, T, M, f0, live, gridDim.z > 1, Y, Y2, ldy);
+    if (!A2 && use_ymap)
+        tn_epilogue_tma<EPI>(tmem, warp, lane, t0 + warp * 32, T, f0, live,
+                             EPI == GEMM_EPI_ADD || gridDim.z > 1, &tmY, smem, qe, err);
+    else if (EPI != GEMM_EPI_QKV)
+        tn_epilogue<EPI, A2>(tmem, warp, t0 + warp * 32 + lane, T, M, f0, live, gridDim.z > 1, Y, Y2, ldy);
     tc_fence_before();
     __syncthreads();
     if (warp == 0)
@@ -558,7 +731,7 @@ gemm_tn_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
 // halves); the leader's commits arrive on the empty and accumulator barriers of both CTAs.
 constexpr uint32_t kTn2Half = 128 * kBK * 2;           // 16 KB: 128 rows x 64 f16
 constexpr uint32_t kTn2Stage = 2 * kTn2Half;           // this CTA's A half + B half
-constexpr int kTn2Stages = 6;
+constexpr int kTn2Stages = 7;
 constexpr size_t kTn2Smem = 1024 + (size_t)kTn2Stages * kTn2Stage + 256;
 
 __device__ __forceinline__ uint32_t cluster_rank() {
@@ -605,11 +778,25 @@ __device__ __forceinline__ void umma_commit_pair(uint64_t* bar) {
         : "memory");
 }
 
-template <int EPI>
+// TRACE: each CTA writes global-timer stamps (ns) to trace[8 * block + i]: 0 start, 1 set-up done,
+// 2 first stage ready (leader's MMA thread), 3 last MMA issued, 4 accumulator ready, 5 epilogue
+// done, 6 end, 7 the SM id.
+template <int EPI, bool TRACE>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(128, 1)
 gemm_tn2_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
-                const __grid_constant__ CUtensorMap tmWlo, int planes, int K, int T, int M, int F,
-                void* __restrict__ Y, int ldy, uint32_t* __restrict__ err) {
+                const __grid_constant__ CUtensorMap tmWlo, const __grid_constant__ CUtensorMap tmY, int use_ymap,
+                const TnQkv qe, int planes, int K, int T, int M, int F,
+                void* __restrict__ Y, int ldy, uint32_t* __restrict__ err, uint64_t* __restrict__ trace) {
+    uint64_t* tr = nullptr;
+    if (TRACE) {
+        tr = trace + 8 * (size_t)(blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z));
+        if (threadIdx.x == 0) {
+            tr[0] = global_ns();
+            uint32_t sm;
+            asm volatile("mov.u32 %0, %%smid;" : "=r"(sm));
+            tr[7] = sm;
+        }
+    }
     constexpr int S = kTn2Stages;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -655,9 +842,21 @@ gemm_tn2_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
     cluster_sync_all();                 // barriers of both CTAs initialised, TMEM address written
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    if (TRACE && threadIdx.x == 0) tr[1] = global_ns();
 
     if (threadIdx.x == 0) {
-        // ---- TMA producer (both CTAs): this CTA's 128 tokens and 128 weight rows per stage
+        // ---- TMA producer (both CTAs): this CTA's 128 tokens and 128 weight rows per stage. The
+        // weights of the first stages do not depend on the kernel before (launched with
+        // programmatic dependent launch, this one may start while that one ends): they are
+        // requested before the grid dependency wait, the activations after it.
+        const int pre = min(nk, S);
+        for (int kb = 0; kb < pre; ++kb) {
+            const uint32_t fb = cluster_addr(smem_u32(&full[kb]), 0);
+            if (rank == 0) mbar_expect_tx(&full[kb], 2 * kTn2Stage);
+            tma_load_2d_pair(smem + (size_t)kb * kTn2Stage + kTn2Half, kb < nkp ? &tmW : &tmWlo, fb,
+                             (kb0 + kb % nkp) * kBK, wrow);
+        }
+        asm volatile("griddepcontrol.wait;" ::: "memory");
         int issued = 0;
         for (int kb = 0; kb < nk; ++kb) {
             const int s = kb % S;
@@ -666,13 +865,15 @@ gemm_tn2_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
             if (*(volatile int*)abort_flag) break;
             uint8_t* st = smem + (size_t)s * kTn2Stage;
             const uint32_t fb = cluster_addr(smem_u32(&full[s]), 0);
-            if (rank == 0) mbar_expect_tx(&full[s], 2 * kTn2Stage);
             const int kx = (kb0 + kb % nkp) * kBK;
-            const CUtensorMap* wm = kb < nkp ? &tmW : &tmWlo;
+            if (kb >= S) {
+                if (rank == 0) mbar_expect_tx(&full[s], 2 * kTn2Stage);
+                tma_load_2d_pair(st + kTn2Half, kb < nkp ? &tmW : &tmWlo, fb, kx, wrow);
+            }
             tma_load_2d_pair(st, &tmX, fb, kx, tm);
-            tma_load_2d_pair(st + kTn2Half, wm, fb, kx, wrow);
             issued = kb + 1;
         }
+        if (issued < pre) issued = pre;                // the early weight copies are in flight too
         // drain: the copies issued have landed before the CTA can exit (the leader's full barrier
         // counts both CTAs' bytes; the peer sees its last stage consumed)
         if (rank == 0) {
@@ -690,6 +891,7 @@ gemm_tn2_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
             const uint32_t ph = (uint32_t)(kb / S) & 1u;
             if (!mbar_wait(&full[s], ph)) { ok = false; break; }
             tc_fence_after();
+            if (TRACE && kb == 0) tr[2] = global_ns();
             const uint8_t* st = smem + (size_t)s * kTn2Stage;
             const uint64_t ad = sdesc_sw128(smem_u32(st));
             const uint64_t bd = sdesc_sw128(smem_u32(st + kTn2Half));
@@ -700,19 +902,34 @@ gemm_tn2_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
         }
         if (!ok) { atomicOr(err, ERR_TIMEOUT); *(volatile int*)abort_flag = 1; }
         umma_commit_pair(accf);
+        if (TRACE) tr[3] = global_ns();
     }
     __syncwarp();
 
     const bool have = mbar_wait(accf, 0);
     tc_fence_after();
+    if (TRACE && threadIdx.x == 0) tr[4] = global_ns();
+    // the output may be read or written by the kernel before until it has ended; the kernel after
+    // may be scheduled now (it waits for this one's end before touching its data)
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;");
     if (!have) atomicOr(err, ERR_TIMEOUT);
     const bool live = have && !*(volatile int*)abort_flag && nk > 0;
-    tn_epilogue<EPI, false>(tmem, warp, tm + warp * 32 + lane, T, M, f0, live, gridDim.z > 1, Y, nullptr, ldy);
+    if (use_ymap)
+        tn_epilogue_tma<EPI>(tmem, warp, lane, tm + warp * 32, T, f0, live, EPI == GEMM_EPI_ADD || gridDim.z > 1,
+                             &tmY, smem, qe, err);
+    else if (EPI != GEMM_EPI_QKV)
+        tn_epilogue<EPI, false>(tmem, warp, tm + warp * 32 + lane, T, M, f0, live, gridDim.z > 1, Y, nullptr, ldy);
+    if (TRACE) {
+        __syncthreads();
+        if (threadIdx.x == 0) tr[5] = global_ns();
+    }
     tc_fence_before();
     cluster_sync_all();                 // both CTAs done with the pair's TMEM and shared memory
     if (warp == 0)
         asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem),
                      "r"((uint32_t)kTnN));
+    if (TRACE && threadIdx.x == 0) tr[6] = global_ns();
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -781,10 +998,13 @@ bool tc_swiglu_tn_ok(int64_t K, int64_t F) { return K % kBK == 0 && K >= kBK && 
 bool tc_tn_ok(int64_t M, int64_t K) { return K % kBK == 0 && K >= kBK && M % kTnN == 0 && M > 0; }
 
 // The two-CTA kernel serves f16 operands when the ubatch fills more than one 128-token tile.
-template <int EPI>
+// ymap (f16 operands only): the output's tensor map for the TMA-store epilogue (float32 boxes of
+// 32 columns x 32 rows, or f16 boxes of 64 x 32 for SwiGLU, 128-byte swizzle), else direct stores.
+template <int EPI, bool TRACE = false>
 bool launch_tn2(const CUtensorMap& xmap, const CUtensorMap& wmap, const CUtensorMap* wmap_lo, int K, int T,
-                int M, int F, void* Y, int ldy, int splits, uint32_t* err, cudaStream_t st) {
-    auto k = gemm_tn2_kernel<EPI>;
+                int M, int F, void* Y, int ldy, int splits, uint32_t* err, cudaStream_t st,
+                const CUtensorMap* ymap, const TnQkv& qe, uint64_t* trace = nullptr, bool pdl = false) {
+    auto k = gemm_tn2_kernel<EPI, TRACE>;
     static bool attr = false;
     if (!attr) {
         if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTn2Smem) != cudaSuccess)
@@ -792,18 +1012,28 @@ bool launch_tn2(const CUtensorMap& xmap, const CUtensorMap& wmap, const CUtensor
         attr = true;
     }
     const int ntile = EPI == GEMM_EPI_SWIGLU ? F / (kTnN / 2) : M / kTnN;
-    dim3 grid(2 * ((T + 2 * kTnRows - 1) / (2 * kTnRows)), ntile, splits);
-    k<<<grid, 128, kTn2Smem, st>>>(xmap, wmap, wmap_lo ? *wmap_lo : wmap, wmap_lo ? 2 : 1, K, T, M, F, Y,
-                                   ldy, err);
-    return cudaGetLastError() == cudaSuccess;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * ((T + 2 * kTnRows - 1) / (2 * kTnRows)), ntile, splits);
+    cfg.blockDim = dim3(128);
+    cfg.dynamicSmemBytes = kTn2Smem;
+    cfg.stream = st;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, k, xmap, wmap, wmap_lo ? *wmap_lo : wmap, ymap ? *ymap : xmap, ymap ? 1 : 0, qe,
+                              wmap_lo ? 2 : 1, K, T, M, F, Y, ldy, err, trace) == cudaSuccess;
 }
 
 template <int EPI, bool A2>
 bool launch_tn(const CUtensorMap& xmap, const CUtensorMap* xmap_lo, const CUtensorMap& wmap,
                const CUtensorMap* wmap_lo, int K, int T, int M, int F, void* Y, void* Y2, int ldy,
-               int splits, uint32_t* err, cudaStream_t st, bool one_cta) {
+               int splits, uint32_t* err, cudaStream_t st, bool one_cta, const CUtensorMap* ymap,
+               const TnQkv& qe = TnQkv{}, bool pdl = false) {
+    if (A2) ymap = nullptr;
     if (!A2 && T > kTnRows && !one_cta)
-        return launch_tn2<EPI>(xmap, wmap, wmap_lo, K, T, M, F, Y, ldy, splits, err, st);
+        return launch_tn2<EPI>(xmap, wmap, wmap_lo, K, T, M, F, Y, ldy, splits, err, st, ymap, qe, nullptr, pdl);
     using C = TnCfg<A2>;
     auto k = gemm_tn_kernel<EPI, A2>;
     static bool attr = false;
@@ -813,21 +1043,30 @@ bool launch_tn(const CUtensorMap& xmap, const CUtensorMap* xmap_lo, const CUtens
         attr = true;
     }
     const int ntile = EPI == GEMM_EPI_SWIGLU ? F / (kTnN / 2) : M / kTnN;
-    dim3 grid((T + kTnRows - 1) / kTnRows, ntile, splits);
-    k<<<grid, 128, C::kSmem, st>>>(xmap, xmap_lo ? *xmap_lo : xmap, wmap, wmap_lo ? *wmap_lo : wmap,
-                                   wmap_lo ? 2 : 1, K, T, M, F, Y, Y2, ldy, err);
-    return cudaGetLastError() == cudaSuccess;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((T + kTnRows - 1) / kTnRows, ntile, splits);
+    cfg.blockDim = dim3(128);
+    cfg.dynamicSmemBytes = C::kSmem;
+    cfg.stream = st;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, k, xmap, xmap_lo ? *xmap_lo : xmap, wmap, wmap_lo ? *wmap_lo : wmap,
+                              ymap ? *ymap : xmap, ymap ? 1 : 0, qe, wmap_lo ? 2 : 1, K, T, M, F, Y, Y2, ldy,
+                              err) == cudaSuccess;
 }
 
 bool launch_gemm_swiglu_tn(const CUtensorMap& xmap, const CUtensorMap* xmap_lo, const CUtensorMap& wmap,
                            int K, int T, int F, void* Y, void* Y2, int ldy, uint32_t* err, cudaStream_t st,
-                           const CUtensorMap* wmap_lo, bool one_cta) {
+                           const CUtensorMap* wmap_lo, bool one_cta, const CUtensorMap* ymap, bool pdl) {
     if (T <= 0) return true;
     if (xmap_lo)
         return launch_tn<GEMM_EPI_SWIGLU, true>(xmap, xmap_lo, wmap, wmap_lo, K, T, 0, F, Y, Y2, ldy, 1, err, st,
-                                                one_cta);
+                                                one_cta, nullptr, TnQkv{}, pdl);
     return launch_tn<GEMM_EPI_SWIGLU, false>(xmap, nullptr, wmap, wmap_lo, K, T, 0, F, Y, nullptr, ldy, 1, err, st,
-                                             one_cta);
+                                             one_cta, ymap, TnQkv{}, pdl);
 }
 
 int tc_tn_splits(int64_t M, int64_t K, int T, int n_sm) {
@@ -840,19 +1079,67 @@ int tc_tn_splits(int64_t M, int64_t K, int T, int n_sm) {
 
 bool launch_gemm_tn(const CUtensorMap& xmap, const CUtensorMap* xmap_lo, const CUtensorMap& wmap, int epi,
                     int K, int M, int T, float* Y, int ldy, int splits, uint32_t* err, cudaStream_t st,
-                    const CUtensorMap* wmap_lo, bool one_cta) {
+                    const CUtensorMap* wmap_lo, bool one_cta, const CUtensorMap* ymap, const TnQkv* qkv, bool pdl) {
     if (T <= 0) return true;
+    if (epi == GEMM_EPI_QKV) {
+        if (xmap_lo || !ymap || !qkv || splits != 1 || !tc_tn_qkv_ok(qkv->H, qkv->Hkv, qkv->hd)) return false;
+        return launch_tn<GEMM_EPI_QKV, false>(xmap, nullptr, wmap, wmap_lo, K, T, M, 0, Y, nullptr, ldy, 1, err, st,
+                                              one_cta, ymap, *qkv, pdl);
+    }
     if (epi == GEMM_EPI_STORE)
         return xmap_lo ? launch_tn<GEMM_EPI_STORE, true>(xmap, xmap_lo, wmap, wmap_lo, K, T, M, 0, Y, nullptr, ldy,
-                                                         splits, err, st, one_cta)
+                                                         splits, err, st, one_cta, nullptr, TnQkv{}, pdl)
                        : launch_tn<GEMM_EPI_STORE, false>(xmap, nullptr, wmap, wmap_lo, K, T, M, 0, Y, nullptr, ldy,
-                                                          splits, err, st, one_cta);
+                                                          splits, err, st, one_cta, ymap, TnQkv{}, pdl);
     if (epi == GEMM_EPI_ADD)
         return xmap_lo ? launch_tn<GEMM_EPI_ADD, true>(xmap, xmap_lo, wmap, wmap_lo, K, T, M, 0, Y, nullptr, ldy,
-                                                       splits, err, st, one_cta)
+                                                       splits, err, st, one_cta, nullptr, TnQkv{}, pdl)
                        : launch_tn<GEMM_EPI_ADD, false>(xmap, nullptr, wmap, wmap_lo, K, T, M, 0, Y, nullptr, ldy,
-                                                        splits, err, st, one_cta);
+                                                        splits, err, st, one_cta, ymap, TnQkv{}, pdl);
     return false;
+}
+
+bool launch_gemm_tn2_traced(const CUtensorMap& xmap, const CUtensorMap& wmap, int epi, int K, int M, int T,
+                            int F, void* Y, int ldy, int splits, uint32_t* err, cudaStream_t st,
+                            const CUtensorMap* ymap, uint64_t* trace) {
+    if (T <= kTnRows) return false;
+    switch (epi) {
+        case GEMM_EPI_STORE:
+            return launch_tn2<GEMM_EPI_STORE, true>(xmap, wmap, nullptr, K, T, M, F, Y, ldy, splits, err, st, ymap,
+                                                    TnQkv{}, trace);
+        case GEMM_EPI_ADD:
+            return launch_tn2<GEMM_EPI_ADD, true>(xmap, wmap, nullptr, K, T, M, F, Y, ldy, splits, err, st, ymap,
+                                                  TnQkv{}, trace);
+        case GEMM_EPI_SWIGLU:
+            return launch_tn2<GEMM_EPI_SWIGLU, true>(xmap, wmap, nullptr, K, T, M, F, Y, ldy, 1, err, st, ymap,
+                                                     TnQkv{}, trace);
+    }
+    return false;
+}
+
+bool tc_tn_qkv_ok(int H, int Hkv, int hd) {
+    return hd > 0 && kTnN % hd == 0 && hd % 32 == 0 && (H * hd) % kTnN == 0 && (Hkv * hd) % kTnN == 0;
+}
+
+bool tc_make_out_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, bool f16) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const int64_t es = f16 ? 2 : 4;
+    if ((reinterpret_cast<uintptr_t>(base) & 15) != 0 || (cols * es) % 16 != 0) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)(cols * es)};
+    const cuuint32_t box[2] = {(cuuint32_t)(128 / es), 32u};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = fn(map, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
+                          const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+int tc_tn2_blocks(int epi, int M, int T, int F, int splits) {
+    const int ntile = epi == GEMM_EPI_SWIGLU ? F / (kTnN / 2) : M / kTnN;
+    return 2 * ((T + 2 * kTnRows - 1) / (2 * kTnRows)) * ntile * splits;
 }
 
 bool tc_shape_ok(int64_t M, int64_t K, int epi, int64_t F) {

@@ -12,6 +12,19 @@ enum GemmEpi : int32_t {
     GEMM_EPI_STORE = 0,    // Y[t][m] = acc (float32)
     GEMM_EPI_ADD = 1,      // Y[t][m] += acc (float32, the residual add)
     GEMM_EPI_SWIGLU = 2,   // Y[t][j] = silu(gate_j) * up_j (bf16); W rows [0,F) gate, [F,2F) up
+    GEMM_EPI_QKV = 3,      // the fused Q/K/V projection's outputs: RoPE, K/V rows to the cache (TnQkv)
+};
+
+// The Q/K/V epilogue of the token-major GEMM with f16 operands ([P2] "llama.cpp Architecture",
+// Example 4: ROPE of Q and K, SET_ROWS of K and V into the layer's cache): columns [0, H hd) are
+// Q, stored rotated (float32) into Y; [H hd, (H + Hkv) hd) are K and the rest V, rotated (K) and
+// rounded to f16 into their cache rows. Needs 256 % hd == 0 and H hd, Hkv hd multiples of 256.
+struct TnQkv {
+    const float2* cs = nullptr;      // [T][hd / 2] cos, sin of each token's angle per pair
+    const int32_t* slot = nullptr;   // [T] cache cell of each token (checked against n_ctx)
+    void* kc = nullptr;              // f16 [Hkv][n_ctx][hd]
+    void* vc = nullptr;
+    int n_ctx = 0, H = 0, Hkv = 0, hd = 0;
 };
 
 // TMA map of a row-major bf16 (or, with f16, float16) matrix [rows][cols] (cols % 64 == 0, base
@@ -45,16 +58,36 @@ bool tc_swiglu_tn_ok(int64_t K, int64_t F);
 // tiles) runs unless one_cta is set.
 bool launch_gemm_swiglu_tn(const CUtensorMap& xmap, const CUtensorMap* xmap_lo, const CUtensorMap& wmap,
                            int K, int T, int F, void* Y, void* Y2, int ldy, uint32_t* err, cudaStream_t st,
-                           const CUtensorMap* wmap_lo = nullptr, bool one_cta = false);
+                           const CUtensorMap* wmap_lo = nullptr, bool one_cta = false,
+                           const CUtensorMap* ymap = nullptr, bool pdl = false);
 
 // Store / residual add with the token tile as A (two bf16 terms) and 256 weight rows as B (wmap
 // over W [M][K], box 128 rows): Y [>= T][ldy] float32 (op)= X W^T. M % 256 == 0. splits > 1
-// splits K over blockIdx.z with vector atomic adds into Y (a store then needs Y zeroed first).
+// splits K over blockIdx.z with vector atomic adds (or, with ymap, bulk reduce-adds) into Y (a
+// store then needs Y zeroed first).
 // Without xmap_lo: f16 activations and weights, one term each.
 bool tc_tn_ok(int64_t M, int64_t K);
 int tc_tn_splits(int64_t M, int64_t K, int T, int n_sm);
 bool launch_gemm_tn(const CUtensorMap& xmap, const CUtensorMap* xmap_lo, const CUtensorMap& wmap, int epi,
                     int K, int M, int T, float* Y, int ldy, int splits, uint32_t* err, cudaStream_t st,
-                    const CUtensorMap* wmap_lo = nullptr, bool one_cta = false);
+                    const CUtensorMap* wmap_lo = nullptr, bool one_cta = false,
+                    const CUtensorMap* ymap = nullptr, const TnQkv* qkv = nullptr, bool pdl = false);
+// pdl: launched with programmatic dependent launch (the kernel requests its first weight tiles
+// before it waits for the kernel before it to end).
+// Whether the Q/K/V epilogue serves these head counts (f16 operands, ymap given, one K split).
+bool tc_tn_qkv_ok(int H, int Hkv, int hd);
+
+// Tensor map of a kernel's output [rows][cols] (float32, or f16 with f16) for the TMA-store
+// epilogue of the token-major GEMM with f16 operands: boxes of 128 bytes x 32 rows, 128-byte
+// swizzle. Pass it as ymap: the epilogue then stages each warp's rows in shared memory and
+// writes them with bulk tensor stores (the residual add and K splits as reduce-adds).
+bool tc_make_out_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, bool f16);
+
+// The two-CTA kernel with a timeline: 8 global-timer stamps per CTA in trace (see gemm_tc.cu), for
+// tc_tn2_blocks(...) CTAs. Returns false for T <= 128 or a launch failure.
+bool launch_gemm_tn2_traced(const CUtensorMap& xmap, const CUtensorMap& wmap, int epi, int K, int M, int T,
+                            int F, void* Y, int ldy, int splits, uint32_t* err, cudaStream_t st,
+                            const CUtensorMap* ymap, uint64_t* trace);
+int tc_tn2_blocks(int epi, int M, int T, int F, int splits);
 
 }  // namespace llm

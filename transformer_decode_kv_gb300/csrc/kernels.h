@@ -64,9 +64,10 @@ void launch_kv_q8_to_f16(const void* kc, const void* vc, void* out, int32_t Hkv,
 // head. Used by the defrag to gather one cache region in the new cell order.
 void launch_kv_gather(const void* src, void* dst, const int32_t* order, int32_t n, int32_t n_head,
                       int32_t n_src, int32_t row_bytes, cudaStream_t st);
-// The same with a single f16 output (the prefill GEMMs' f16 operand).
+// The same with a single f16 output (the prefill GEMMs' f16 operand); pdl: launched with
+// programmatic dependent launch after the kernel that writes x (d of 1024 to 8192).
 void launch_rmsnorm_f16(const float* x, const int32_t* rows, int32_t R, int32_t d, const float* g,
-                        float eps, void* yh, cudaStream_t st);
+                        float eps, void* yh, cudaStream_t st, bool pdl = false);
 // Q8_0 weight -> two f16 terms hi = f16(d * q), lo = f16(d * q - hi): exact, since d * q has at
 // most 18 significant bits (fp16 scale x 8-bit integer) and hi + lo hold 22 (within f16 range).
 void launch_q8_0_to_f16_terms(const int8_t* q, const __half* d, int64_t rows, int64_t cols, void* hi, void* lo,

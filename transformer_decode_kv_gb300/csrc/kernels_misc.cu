@@ -68,6 +68,9 @@ __global__ void __launch_bounds__(256) rmsnorm_f16_vec_kernel(const float* __res
                                                              const float* __restrict__ g, float eps,
                                                              __half* __restrict__ y) {
     __shared__ float red[32];
+    // launched with programmatic dependent launch: x comes from the kernel before
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;");
     const int r = blockIdx.x;
     const int src = rows ? rows[r] : r;
     const float4* xr = reinterpret_cast<const float4*>(x + (int64_t)src * d);
@@ -376,14 +379,23 @@ void launch_kv_gather(const void* src, void* dst, const int32_t* order, int32_t 
 }
 
 void launch_rmsnorm_f16(const float* x, const int32_t* rows, int32_t R, int32_t d, const float* g,
-                        float eps, void* yh, cudaStream_t st) {
+                        float eps, void* yh, cudaStream_t st, bool pdl) {
     if (R <= 0) return;
     __half* y = static_cast<__half*>(yh);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(R);
+    cfg.blockDim = dim3(256);
+    cfg.stream = st;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = pdl ? 1 : 0;
     switch (d) {
-        case 1024: rmsnorm_f16_vec_kernel<1><<<R, 256, 0, st>>>(x, rows, d, g, eps, y); return;
-        case 2048: rmsnorm_f16_vec_kernel<2><<<R, 256, 0, st>>>(x, rows, d, g, eps, y); return;
-        case 4096: rmsnorm_f16_vec_kernel<4><<<R, 256, 0, st>>>(x, rows, d, g, eps, y); return;
-        case 8192: rmsnorm_f16_vec_kernel<8><<<R, 256, 0, st>>>(x, rows, d, g, eps, y); return;
+        case 1024: cudaLaunchKernelEx(&cfg, rmsnorm_f16_vec_kernel<1>, x, rows, d, g, eps, y); return;
+        case 2048: cudaLaunchKernelEx(&cfg, rmsnorm_f16_vec_kernel<2>, x, rows, d, g, eps, y); return;
+        case 4096: cudaLaunchKernelEx(&cfg, rmsnorm_f16_vec_kernel<4>, x, rows, d, g, eps, y); return;
+        case 8192: cudaLaunchKernelEx(&cfg, rmsnorm_f16_vec_kernel<8>, x, rows, d, g, eps, y); return;
     }
     rmsnorm_kernel<__half><<<R, d >= 1024 ? 512 : 256, 0, st>>>(x, rows, d, g, eps, y, nullptr);
 }

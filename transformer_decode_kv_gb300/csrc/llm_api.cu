@@ -135,6 +135,7 @@ struct llm_ctx {
     bool tc_ok = false;                        // tensor-core prefill GEMMs for the layers
     bool tc_f16 = false;                       // ... with f16 operands (one term each, token-major)
     CUtensorMap m_hh, m_ah, m_uh;              // f16 views of hb, attnb, ub (token box 128)
+    CUtensorMap m_y_qkv, m_y_x, m_y_ub;        // outputs of the f16 token-major GEMMs (TMA-store epilogue)
     bool tc_lm = false;                        // ... and for the output matrix
     float *part_o = nullptr, *part_m = nullptr, *part_l = nullptr;
     int32_t* tickets = nullptr;
@@ -512,7 +513,9 @@ bool forward_ubatch(llm_ctx* c, int32_t T, int32_t O, int32_t out_row0, int32_t 
     a.hdr = din + io.hdr;
     a.n_work = gemv ? attn_cap(c, T) : c->plan.n_work();  // grid bound (the device count decides)
     a.max_nq = max_nq;
-    a.pdl = c->use_pdl && gemv;
+    // prefill with f16 GEMM operands chains its kernels with programmatic dependent launch too
+    const bool pdl_pre = c->use_pdl && !gemv && c->tc_ok && c->tc_f16 && !c->ktime;
+    a.pdl = (c->use_pdl && gemv) || pdl_pre;
     a.slot = slot;                                   // tiles of one token use the cluster decode kernel
     a.n_tok = T;
 
@@ -540,8 +543,9 @@ bool forward_ubatch(llm_ctx* c, int32_t T, int32_t O, int32_t out_row0, int32_t 
             if (splits > 1 && epi == GEMM_EPI_STORE &&
                 !cuda_ok(c, cudaMemsetAsync(Y, 0, sizeof(float) * (size_t)T * ldy, st), "memset"))
                 return false;
+            const CUtensorMap* ym = !f16 ? nullptr : Y == c->qkv ? &c->m_y_qkv : Y == c->x ? &c->m_y_x : nullptr;
             if (!launch_gemm_tn(xm, xlo, wm, epi, K, M, T, static_cast<float*>(Y), ldy, splits, c->d_err, st,
-                                wlo)) {
+                                wlo, false, ym, nullptr, pdl_pre && !(splits > 1 && epi == GEMM_EPI_STORE))) {
                 c->err = "tensor-core GEMM launch failed";
                 return false;
             }
@@ -582,28 +586,42 @@ bool forward_ubatch(llm_ctx* c, int32_t T, int32_t O, int32_t out_row0, int32_t 
             }
         } else {
             k = kt_begin(c);
-            if (f16) launch_rmsnorm_f16(c->x, nullptr, T, d, L.attn_norm, hp.rms_eps, c->hb, st);
+            if (f16) launch_rmsnorm_f16(c->x, nullptr, T, d, L.attn_norm, hp.rms_eps, c->hb, st, pdl_pre && il > 0);
             else if (tc) launch_rmsnorm_bf16(c->x, nullptr, T, d, L.attn_norm, hp.rms_eps, c->hb, c->hb_lo, st);
             else launch_rmsnorm(c->x, nullptr, T, d, L.attn_norm, hp.rms_eps, c->h, st);
             kt_end(c, k, KC_RMSNORM, norm_bytes, 0);
+            // F16 cache, f16 GEMM operands: RoPE and the K/V append run in the GEMM's epilogue
+            const bool fused_qkv = f16 && !q8 && c->type_k == LLM_TYPE_F16 && c->type_v == LLM_TYPE_F16 &&
+                                   tc_tn_qkv_ok(H, Hkv, hd) && tc_tn_ok(qkvw, d);
             k = kt_begin(c);
-            if (tc) {
+            if (fused_qkv) {
+                TnQkv qe;
+                qe.cs = c->rope_cs; qe.slot = slot; qe.kc = kc; qe.vc = vc;
+                qe.n_ctx = c->n_ctx; qe.H = H; qe.Hkv = Hkv; qe.hd = hd;
+                if (!launch_gemm_tn(c->m_hh, nullptr, L.mq, GEMM_EPI_QKV, d, qkvw, T, c->qkv, qkvw, 1, c->d_err, st,
+                                    L.q8_tc ? &L.mq_lo : nullptr, false, &c->m_y_qkv, &qe, pdl_pre)) {
+                    c->err = "tensor-core GEMM launch failed";
+                    return false;
+                }
+            } else if (tc) {
                 if (!tc_gemm(L.mq, f16 ? c->m_hh : c->m_hb[bi], GEMM_EPI_STORE, d, qkvw, c->qkv, qkvw,
                              L.q8_tc ? &L.mq_lo : nullptr))
                     return false;
             }
             else launch_linear(L.qkv, 0, qkvw, c->h, d, T, c->qkv, qkvw, EPI_STORE, st);
             kt_end(c, k, lin_cls, wbytes(L.qkv, qkvw) + Td * (d + qkvw) * 4.0, 2.0 * Td * qkvw * d);
-            k = kt_begin(c);
-            if (q8) {
-                launch_rope_kv_append(c->qkv, T, H, Hkv, hd, c->rope_cs, nullptr, stage_k, stage_v, U,
-                                      W_F32, c->d_err, st);
-                launch_kv_quant_q8(stage_k, stage_v, U, T, Hkv, hd, slot, kc, vc, c->n_ctx, c->d_err, st, false);
-            } else {
-                launch_rope_kv_append(c->qkv, T, H, Hkv, hd, c->rope_cs, slot, kc, vc, c->n_ctx,
-                                      c->type_k, c->d_err, st);
+            if (!fused_qkv) {
+                k = kt_begin(c);
+                if (q8) {
+                    launch_rope_kv_append(c->qkv, T, H, Hkv, hd, c->rope_cs, nullptr, stage_k, stage_v, U,
+                                          W_F32, c->d_err, st);
+                    launch_kv_quant_q8(stage_k, stage_v, U, T, Hkv, hd, slot, kc, vc, c->n_ctx, c->d_err, st, false);
+                } else {
+                    launch_rope_kv_append(c->qkv, T, H, Hkv, hd, c->rope_cs, slot, kc, vc, c->n_ctx,
+                                          c->type_k, c->d_err, st);
+                }
+                kt_end(c, k, KC_ROPE_KV, Td * ((double)qkvw * 4.0 + qw * 4.0 + 2.0 * Hkv * hd * kv_es), 0);
             }
-            kt_end(c, k, KC_ROPE_KV, Td * ((double)qkvw * 4.0 + qw * 4.0 + 2.0 * Hkv * hd * kv_es), 0);
         }
         if (c->debug && q8) {                       // staging [Hkv][U][hd] -> [T][Hkv * hd]
             const size_t kw = (size_t)Hkv * hd;
@@ -665,7 +683,7 @@ bool forward_ubatch(llm_ctx* c, int32_t T, int32_t O, int32_t out_row0, int32_t 
             kt_end(c, k, lin_cls, wbytes(L.gu, 2 * (int64_t)F) + Td * (d + F) * 4.0, 4.0 * Td * F * d);
         } else {
             k = kt_begin(c);
-            if (f16) launch_rmsnorm_f16(c->x, nullptr, T, d, L.ffn_norm, hp.rms_eps, c->hb, st);
+            if (f16) launch_rmsnorm_f16(c->x, nullptr, T, d, L.ffn_norm, hp.rms_eps, c->hb, st, pdl_pre);
             else if (tc) launch_rmsnorm_bf16(c->x, nullptr, T, d, L.ffn_norm, hp.rms_eps, c->hb, c->hb_lo, st);
             else launch_rmsnorm(c->x, nullptr, T, d, L.ffn_norm, hp.rms_eps, c->h, st);
             kt_end(c, k, KC_RMSNORM, norm_bytes, 0);
@@ -673,7 +691,8 @@ bool forward_ubatch(llm_ctx* c, int32_t T, int32_t O, int32_t out_row0, int32_t 
             if (tc && L.gu_tn) {
                 if (!launch_gemm_swiglu_tn(f16 ? c->m_hh : c->m_hb[bi], f16 ? nullptr : &c->m_hb_lo, L.mgu128, d, T,
                                            F, c->ub, f16 ? nullptr : c->ub_lo, F, c->d_err, st,
-                                           L.q8_tc ? &L.mgu128_lo : nullptr)) {
+                                           L.q8_tc ? &L.mgu128_lo : nullptr, false, f16 ? &c->m_y_ub : nullptr,
+                                           pdl_pre)) {
                     c->err = "tensor-core GEMM launch failed";
                     return false;
                 }
@@ -1139,7 +1158,10 @@ int llm_weights_ready(llm_ctx* c) {
     if (ok && !cuda_ok(c, cudaStreamSynchronize(c->st), "f16 weights")) return -1;
     ok = ok && (!f16 || (tc_make_map(&c->m_hh, c->hb, U, d, 128, true) &&
                          tc_make_map(&c->m_ah, c->attnb, U, qw, 128, true) &&
-                         tc_make_map(&c->m_uh, c->ub, U, F, 128, true)));
+                         tc_make_map(&c->m_uh, c->ub, U, F, 128, true) &&
+                         tc_make_out_map(&c->m_y_qkv, c->qkv, U, qkvw, false) &&
+                         tc_make_out_map(&c->m_y_x, c->x, U, d, false) &&
+                         tc_make_out_map(&c->m_y_ub, c->ub, U, F, true)));
     const int boxes[2] = {128, 256};
     for (int i = 0; ok && i < 2; ++i)
         ok = tc_make_map(&c->m_hb[i], c->hb, U, d, boxes[i]) &&
@@ -1625,15 +1647,46 @@ int llm_debug_gemm_tn_f16(int32_t epi, const void* W, const void* W_lo, int64_t 
     uint32_t* err = nullptr;
     if (cudaMalloc(&err, sizeof(uint32_t)) != cudaSuccess) return -3;
     cudaMemset(err, 0, sizeof(uint32_t));
+    // the output through the TMA-store epilogue when its rows are whole 16-byte multiples
+    CUtensorMap ym;
+    const bool use_y = tc_make_out_map(&ym, Y, T, ldy, swiglu);
     bool ok = swiglu ? launch_gemm_swiglu_tn(xm, nullptr, wm, (int)K, T, F, Y, nullptr, ldy, err, 0,
-                                             W_lo ? &wl : nullptr, one_cta != 0)
+                                             W_lo ? &wl : nullptr, one_cta != 0, use_y ? &ym : nullptr)
                      : launch_gemm_tn(xm, nullptr, wm, epi, (int)K, (int)M, T, Y, ldy, splits, err, 0,
-                                      W_lo ? &wl : nullptr, one_cta != 0);
+                                      W_lo ? &wl : nullptr, one_cta != 0, use_y ? &ym : nullptr);
     uint32_t h = 0;
     ok = ok && cudaDeviceSynchronize() == cudaSuccess &&
          cudaMemcpy(&h, err, sizeof(uint32_t), cudaMemcpyDeviceToHost) == cudaSuccess;
     cudaFree(err);
     return ok && h == 0 ? 0 : -3;
+}
+
+int64_t llm_debug_gemm_tn_f16_trace(int32_t epi, const void* W, int64_t M, int64_t K, const void* X, int32_t T,
+                                    float* Y, int32_t ldy, int32_t F, int32_t splits, uint64_t* trace,
+                                    int64_t cap) {
+    if (!W || !X || !Y || T <= 128 || epi < 0 || epi > 2 || splits < 1) return -1;
+    const bool swiglu = epi == GEMM_EPI_SWIGLU;
+    if (swiglu ? (!tc_swiglu_tn_ok(K, F) || splits != 1) : !tc_tn_ok(M, K)) return -1;
+    const int64_t n = 8 * (int64_t)tc_tn2_blocks(epi, (int)M, T, F, splits);
+    if (!trace || cap < n) return -1;
+    const int64_t wrows = swiglu ? 2 * (int64_t)F : M;
+    CUtensorMap wm, xm, ym;
+    if (!tc_make_map(&wm, W, wrows, K, 128, true) || !tc_make_map(&xm, X, T, K, 128, true)) return -1;
+    const bool use_y = tc_make_out_map(&ym, Y, T, ldy, swiglu);
+    uint32_t* err = nullptr;
+    uint64_t* dtr = nullptr;
+    if (cudaMalloc(&err, sizeof(uint32_t)) != cudaSuccess) return -3;
+    if (cudaMalloc(&dtr, sizeof(uint64_t) * n) != cudaSuccess) { cudaFree(err); return -3; }
+    cudaMemset(err, 0, sizeof(uint32_t));
+    bool ok = launch_gemm_tn2_traced(xm, wm, epi, (int)K, (int)M, T, F, Y, ldy, splits, err, 0,
+                                     use_y ? &ym : nullptr, dtr);
+    uint32_t h = 0;
+    ok = ok && cudaDeviceSynchronize() == cudaSuccess &&
+         cudaMemcpy(&h, err, sizeof(uint32_t), cudaMemcpyDeviceToHost) == cudaSuccess &&
+         cudaMemcpy(trace, dtr, sizeof(uint64_t) * n, cudaMemcpyDeviceToHost) == cudaSuccess;
+    cudaFree(err);
+    cudaFree(dtr);
+    return ok && h == 0 ? n : -3;
 }
 
 int32_t llm_sample_ith(llm_ctx* c, int32_t i, const llm_sampler_params* p, float u) {
