@@ -144,11 +144,20 @@ struct AttnArgs {
     bool pdl;                // programmatic dependent launch after the previous kernel
     const int32_t* slot;     // decode steps: the cells this ubatch writes (n_tok of them)
     int32_t n_tok;
+    int32_t tile_q = kAttnTileQ;   // query tokens per tile of the plan (attention_tc_tile_q() for
+                                   // the tcgen05 tiles)
+    uint32_t* err = nullptr;       // error word (ERR_TIMEOUT from a bounded wait that ran out)
 };
 // Grouped-query attention of every token over the cells of its list with cell.pos <= token.pos:
 // split-K partial softmax per work item, then a combine per tile ([P2] Example 4 FLASH_ATTN_EXT;
 // Example 11 for the unfused meaning). Scale 1/sqrt(hd).
 bool launch_attention(const AttnArgs& a, cudaStream_t st);
+// The tcgen05 prefill tiles (attn_tc.cu): F16 cache, head_dim 128, 4 query heads per KV head, a
+// single f16 output (forward passes whose matrix products take f16 activations), plans of
+// attention_tc_tile_q() tokens per tile.
+int attention_tc_tile_q();
+bool attention_tc_ok(const AttnArgs& a);
+bool launch_attention_tc(const AttnArgs& a, cudaStream_t st);
 
 // ---- the sampler chain on one logits row (sampler.cu)
 struct SampleArgs {

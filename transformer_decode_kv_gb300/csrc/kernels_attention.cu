@@ -255,6 +255,7 @@ bool launch_hd_g(const AttnArgs& a, cudaStream_t st) {
     // tiles of one token: the cluster decode kernels; of several: the tensor-core tiles (F16, Q8_0)
     // or the CUDA-core tiles (F32)
     if (a.max_nq <= 1) return attention_decode_ok(a) && launch_attention_decode(a, st);
+    if (a.tile_q == attention_tc_tile_q()) return attention_tc_ok(a) && launch_attention_tc(a, st);
     if (attention_mma_ok(a)) return launch_attention_mma(a, st);
     if (a.k_scale) return false;                   // the quant copies are for the tensor-core tiles
     return launch_tq<HD, kAttnTileQ, G>(a, st);

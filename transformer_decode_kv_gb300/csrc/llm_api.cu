@@ -513,6 +513,8 @@ bool forward_ubatch(llm_ctx* c, int32_t T, int32_t O, int32_t out_row0, int32_t 
     a.hdr = din + io.hdr;
     a.n_work = gemv ? attn_cap(c, T) : c->plan.n_work();  // grid bound (the device count decides)
     a.max_nq = max_nq;
+    a.tile_q = max_nq > 1 ? max_nq : kAttnTileQ;
+    a.err = c->d_err;
     // prefill with f16 GEMM operands chains its kernels with programmatic dependent launch too
     const bool pdl_pre = c->use_pdl && !gemv && c->tc_ok && c->tc_f16 && !c->ktime;
     a.pdl = (c->use_pdl && gemv) || pdl_pre;
@@ -1276,8 +1278,13 @@ int32_t llm_decode(llm_ctx* c, llm_batch bt) {
         // prefill tiles: a work item per (tile, KV head) unless that leaves SMs idle; splitting a
         // tile's list costs a merge (measured at 512 tokens: 48 us per layer unsplit, 101 us in
         // 256-cell items, 126 us in 128-cell items)
-        build_attn_plan(c->cells, b, i0, T, kAttnTileQ, c->hp.n_head_kv, G, (small ? 4 : 1) * c->n_sm,
-                        c->max_rows, cap, c->plan, fused ? decode_step_cells() : small ? 64 : 32);
+        // prefill ubatches of a forward pass with f16 GEMM operands over an F16 cache take the
+        // tcgen05 attention tiles, whose plan has 32 tokens per tile
+        const bool tc_attn = !small && c->tc_ok && c->tc_f16 && c->type_k == LLM_TYPE_F16 &&
+                             c->type_v == LLM_TYPE_F16 && c->hp.head_dim == 128 && G == 4;
+        const int32_t tile_q = tc_attn ? attention_tc_tile_q() : kAttnTileQ;
+        build_attn_plan(c->cells, b, i0, T, tile_q, c->hp.n_head_kv, G, (small ? 4 : 1) * c->n_sm,
+                        c->max_rows, cap, c->plan, fused ? decode_step_cells() : small ? 64 : tc_attn ? 128 : 32);
         if (c->debug) {
             UbDebug u;
             u.n_kv = c->cells.n_kv();
@@ -1332,7 +1339,7 @@ int32_t llm_decode(llm_ctx* c, llm_batch bt) {
                                                           c->st), "inputs upload"))) &&
                   cuda_ok(c, cudaMemsetAsync(c->d_err, 0, sizeof(uint32_t), c->st), "memset");
         if (c->ktime) attention_work(c, b.pos.data() + i0);
-        const int32_t max_nq = p.max_nq <= 1 ? 1 : kAttnTileQ;
+        const int32_t max_nq = p.max_nq <= 1 ? 1 : tile_q;
         const StepGraph* sg = nullptr;
         const bool one_kernel = ok && T == 1 && c->step_ok && !c->debug;
         if (one_kernel) ok = run_step(c, O, n_out);
