@@ -17,14 +17,15 @@
 // a row's maximum grows by more than 8 (P stays below 2^8 otherwise), and the final division
 // uses the same maximum for both, so the result does not depend on when rescaling happened.
 //
-// Roles (224 threads): warps 0-1 gather the K and V rows of each step by cell index (cp.async,
-// 16 bytes per copy, into 128-byte-swizzled tiles; warp p fills stage p, the steps of its parity)
-// with the cells' positions, warp 2 allocates
+// Roles (224 threads): warp 0 brings the K and V rows of each step with the cells' positions into
+// 128-byte-swizzled tiles (bulk tensor copies when the step's cells are consecutive, else a gather
+// by cell index, cp.async 16 bytes per copy), warps 1 and 3-6 write the Q tile, warp 2 allocates
 // TMEM and one of its threads issues the MMAs, warps 3-6 run the softmax and the epilogue (warp w
 // reads TMEM lanes 32 (w % 4) .. 32 (w % 4) + 31; TMEM loads and stores are warp-wide, so every
-// one runs with the whole warp converged, whatever its rows need). Cells past the last one any row may see are
-// not visited. Every wait is bounded by a wall-clock limit; a timeout sets ERR_TIMEOUT and the
-// CTA drains what it issued and frees TMEM.
+// one runs with the whole warp converged, whatever its rows need). Cells past the last one any row
+// may see are not visited (the plan ends each work item at the last entry a row may see). Every
+// wait is bounded by a wall-clock limit; a timeout sets ERR_TIMEOUT and the CTA drains what it
+// issued and frees TMEM.
 #include <cuda_fp16.h>
 
 #include <climits>
@@ -46,7 +47,7 @@ constexpr int kTok = 32;                         // tokens per query tile
 constexpr int kRows = kTok * kG;                 // 128 MMA rows
 constexpr int kCells = 128;                      // cells per step
 constexpr int kThreads = 224;
-constexpr int kProdWarps = 2;
+constexpr int kQThreads = 160;                   // warps 1 and 3-6 write the Q tile
 constexpr uint32_t kBlk = 128 * 64 * 2;          // [128 rows][64 f16], 128-byte swizzle: 16 KB
 constexpr uint32_t kTileB = 2 * kBlk;            // [128 rows][128 f16]: 32 KB
 constexpr uint64_t kWaitNs = 2000000000ull;
@@ -58,8 +59,8 @@ struct TcSmem {
     static constexpr uint32_t v0 = k0 + 2 * kTileB;
     static constexpr uint32_t p = v0 + 2 * kTileB;
     static constexpr uint32_t cpos = p + kTileB;                 // int [2][kCells]
-    static constexpr uint32_t rpos = cpos + 2 * kCells * 4;      // int [kRows]
-    static constexpr uint32_t misc = rpos + kRows * 4;           // ints: rmax, end, flag, tmem
+    static constexpr uint32_t rpos = cpos + 2 * kCells * 4;      // int [kRows], then [kTok] tokens
+    static constexpr uint32_t misc = rpos + (kRows + kTok) * 4;  // ints: flag, abort, tmem
     static constexpr uint32_t bars = misc + 64;                  // mbarriers
     static constexpr uint32_t bytes = bars + 16 * 8;
     static constexpr size_t alloc = 1024 + (size_t)bytes;
@@ -150,6 +151,24 @@ __device__ __forceinline__ void ld32(uint32_t taddr, float* v) {
 #pragma unroll
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
+// warp-wide TMEM load of 64 columns; the caller waits (tcgen05.wait::ld) before using v
+__device__ __forceinline__ void ld64_nowait(uint32_t taddr, uint32_t* r) {
+    __syncwarp();
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,"
+        "%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%64];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]),
+          "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]),
+          "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]),
+          "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]),
+          "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
+        : "r"(taddr));
+}
+
 __device__ __forceinline__ void st32(uint32_t taddr, const float* v) {
     __syncwarp();
     asm volatile(
@@ -174,21 +193,25 @@ __device__ __forceinline__ uint32_t swz(int r, int ch) {
     return (uint32_t)((ch >> 3) * kBlk + r * 128 + ((((uint32_t)ch & 7u) ^ ((uint32_t)r & 7u)) << 4));
 }
 
-__global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnArgs a, float scale_log2) {
+// use_tma: tmK / tmV map this context's K and V caches as [layers x heads x cells][128] f16 rows
+// (boxes of 64 dims x 128 rows, 128-byte swizzle): a step whose cells are consecutive comes in four
+// bulk tensor copies; other steps are gathered row by row.
+__global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnArgs a, float scale_log2,
+                                                              const __grid_constant__ CUtensorMap tmK,
+                                                              const __grid_constant__ CUtensorMap tmV, int use_tma) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     int* cposb = reinterpret_cast<int*>(sm + TcSmem::cpos);
     int* rpos = reinterpret_cast<int*>(sm + TcSmem::rpos);
     int* misc = reinterpret_cast<int*>(sm + TcSmem::misc);
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + TcSmem::bars);
-    uint64_t* kv_full = bars;          // [2] count 32: the gathering warp of the stage
+    uint64_t* kv_full = bars;          // [2] count 1: lane 0 of the gathering warp (+ bulk copy bytes)
     uint64_t* kv_empty = bars + 2;     // [2] count 1: MMA commit after O += P V
     uint64_t* s_full = bars + 4;       // [2] count 1: MMA commit after S = Q K^T
     uint64_t* s_free = bars + 6;       // [2] count 128: the softmax threads read S
     uint64_t* p_full = bars + 8;       // count 128: P written (and O rescaled)
     uint64_t* o_done = bars + 9;       // count 1: O += P V of a step ended
-    int* rmax_s = misc;                // largest position of a row of the tile
-    int* end_s = misc + 1;             // one past the last list entry any row may see
+    uint64_t* q_full = bars + 10;      // count kQThreads: the Q tile written
     int* flag = misc + 2;
     int* abort_f = misc + 3;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc + 4);
@@ -207,14 +230,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnArgs a, float 
     asm volatile("griddepcontrol.wait;" ::: "memory");
 
     if (threadIdx.x == 0) {
-        mb_init(&kv_full[0], 32); mb_init(&kv_full[1], 32);
+        mb_init(&kv_full[0], 1); mb_init(&kv_full[1], 1);
+        mb_init(q_full, kQThreads);
         mb_init(&kv_empty[0], 1); mb_init(&kv_empty[1], 1);
         mb_init(&s_full[0], 1); mb_init(&s_full[1], 1);
         mb_init(&s_free[0], kRows); mb_init(&s_free[1], kRows);
         mb_init(p_full, kRows);
         mb_init(o_done, 1);
-        *rmax_s = -1;
-        *end_s = c0;
         *abort_f = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -223,30 +245,34 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnArgs a, float 
                      "r"(512u));
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
     }
-    for (int r = threadIdx.x; r < kRows; r += kThreads) {
-        const int j = r / kG;
-        rpos[r] = j < nq ? a.tok_pos[a.perm[s0 + j]] : INT_MIN;
+    int* rtok = rpos + kRows;            // [kTok] token index of each tile row group
+    if (threadIdx.x < kTok) {
+        const int t = threadIdx.x < nq ? a.perm[s0 + threadIdx.x] : -1;
+        rtok[threadIdx.x] = t;
+        const int p = t >= 0 ? a.tok_pos[t] : INT_MIN;
+#pragma unroll
+        for (int h = 0; h < kG; ++h) rpos[threadIdx.x * kG + h] = p;
     }
+    tc_before();
     __syncthreads();
-    if (threadIdx.x < kRows) atomicMax(rmax_s, rpos[threadIdx.x]);
-    __syncthreads();
-    // the last list entry of [c0, c1) any row may see (later ones are masked for every row)
-    {
-        const int rmax = *rmax_s;
-        int last = c0 - 1;
-        for (int i = c1 - 1 - (int)threadIdx.x; i >= c0; i -= kThreads) {
-            const int cc = a.list_cells[base + i];
-            if (cc >= 0 && cc < a.n_ctx && a.list_pos[base + i] <= rmax) { last = i; break; }
-        }
-        if (last >= c0) atomicMax(end_s, last + 1);
-    }
-    // the Q tile: f16 of q times log2(e) / sqrt(hd), 128-byte-swizzled [128 rows][128 dims]
-    for (int v = threadIdx.x; v < kRows * 16; v += kThreads) {
+    tc_after();
+    const uint32_t tmem = *tmem_slot;
+    const int cend = c1;                  // the plan leaves out entries no row of the tile may see
+    const int nt = (cend - c0 + kCells - 1) / kCells;     // steps of 128 cells
+    const uint32_t sbuf[2] = {tmem, tmem + 128};
+    const uint32_t obuf = tmem + 256;
+
+    // the Q tile: f16 of q times log2(e) / sqrt(hd), 128-byte-swizzled [128 rows][128 dims],
+    // written by warps 1 and 3-6 while warp 0 fetches the first keys and values
+    const int qt = warp == 1 ? lane : warp >= 3 ? 32 + 32 * (warp - 3) + lane : -1;
+    if (qt >= 0) {
+#pragma unroll 4
+    for (int v = qt; v < kRows * 16; v += kQThreads) {
         const int r = v >> 4, ch = v & 15;
-        const int j = r / kG;
+        const int t = rtok[r / kG];
         uint32_t h[4] = {0u, 0u, 0u, 0u};
-        if (j < nq) {
-            const float* qp = a.q + (int64_t)a.perm[s0 + j] * a.ldq + (kvh * kG + r % kG) * kHD + ch * 8;
+        if (t >= 0) {
+            const float* qp = a.q + (int64_t)t * a.ldq + (kvh * kG + r % kG) * kHD + ch * 8;
             const float4 x0 = *reinterpret_cast<const float4*>(qp);
             const float4 x1 = *reinterpret_cast<const float4*>(qp + 4);
             h[0] = pack_h2(x0.x * scale_log2, x0.y * scale_log2);
@@ -256,60 +282,100 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnArgs a, float 
         }
         *reinterpret_cast<uint4*>(sm + TcSmem::q + swz(r, ch)) = make_uint4(h[0], h[1], h[2], h[3]);
     }
-    proxy_fence();
-    tc_before();
-    __syncthreads();
-    tc_after();
-    const uint32_t tmem = *tmem_slot;
-    const int cend = *end_s;
-    const int nt = (cend - c0 + kCells - 1) / kCells;     // steps of 128 cells
-    const uint32_t sbuf[2] = {tmem, tmem + 128};
-    const uint32_t obuf = tmem + 256;
+        proxy_fence();
+        mb_arrive(q_full);
+    }
 
-    if (warp < kProdWarps) {
-        // ---- gather: warp p fills stage p with the steps j = p, p + 2, ..., each thread 4 cells
-        // (K and V rows, 16 chunks each); a step is published as soon as its copies have landed,
-        // so publishing never waits on the consumers of another step
-        const int p = warp;
-        for (int j = p; j < nt; j += kProdWarps) {
-            if (j >= kProdWarps && !mb_wait(&kv_empty[p], (uint32_t)(j / kProdWarps - 1) & 1u)) {
+    if (warp == 0) {
+        // ---- keys and values: every step of 128 list entries into stage j % 2 (after the
+        // step that used it two steps earlier has been multiplied into O), with the cells'
+        // positions for the mask. Consecutive cells: four bulk tensor copies (K and V, 64 dims
+        // each) counted on the stage's barrier; otherwise rows gathered by cell index.
+        const int64_t row0 = (int64_t)a.kv_row0 + (int64_t)kvh * a.n_ctx;
+        for (int j = 0; j < nt; ++j) {
+            const int s = j & 1;
+            if (j >= 2 && !mb_wait(&kv_empty[s], (uint32_t)((j >> 1) - 1) & 1u)) {
                 if (a.err) atomicOr(a.err, ERR_TIMEOUT);
                 *(volatile int*)abort_f = 1;
-                break;
             }
-            if (*(volatile int*)abort_f) break;
-            uint8_t* kt = sm + TcSmem::k0 + p * kTileB;
-            uint8_t* vt = sm + TcSmem::v0 + p * kTileB;
-            int* cpos = cposb + p * kCells;
-#pragma unroll 1
-            for (int u = 0; u < kCells / 32; ++u) {
-                const int i = lane + 32 * u;                     // cell row of the step
-                const int li = c0 + j * kCells + i;
-                int cell = -1, pos = INT_MAX;
-                if (li < cend) {
-                    const int cc = a.list_cells[base + li];
-                    if (cc >= 0 && cc < a.n_ctx) { cell = cc; pos = a.list_pos[base + li]; }
-                }
-                cpos[i] = pos;
+            if (__any_sync(0xffffffffu, *(volatile int*)abort_f != 0)) break;
+            uint8_t* kt = sm + TcSmem::k0 + s * kTileB;
+            uint8_t* vt = sm + TcSmem::v0 + s * kTileB;
+            int* cpos = cposb + s * kCells;
+            const int n = min(kCells, cend - (c0 + j * kCells));      // list entries of the step
+            int cell[kCells / 32];
+            bool valid = true;
 #pragma unroll
-                for (int ch = 0; ch < 16; ++ch) {
-                    const uint32_t o = swz(i, ch);
-                    if (cell >= 0) {
-                        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(kt + o)),
-                                     "l"(K + (int64_t)cell * kHD + ch * 8) : "memory");
-                        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(vt + o)),
-                                     "l"(V + (int64_t)cell * kHD + ch * 8) : "memory");
-                    } else {
-                        *reinterpret_cast<uint4*>(kt + o) = make_uint4(0u, 0u, 0u, 0u);
-                        *reinterpret_cast<uint4*>(vt + o) = make_uint4(0u, 0u, 0u, 0u);
+            for (int u = 0; u < kCells / 32; ++u) {
+                const int i = lane + 32 * u;
+                int cc = -1, pos = INT_MAX;
+                if (i < n) {
+                    cc = a.list_cells[base + c0 + j * kCells + i];
+                    pos = a.list_pos[base + c0 + j * kCells + i];
+                    if (cc < 0 || cc >= a.n_ctx) { valid = false; pos = INT_MAX; }
+                }
+                cell[u] = cc;
+                cpos[i] = pos;
+            }
+            const int first = __shfl_sync(0xffffffffu, cell[0], 0);
+            int lastv = cell[0];
+#pragma unroll
+            for (int u = 1; u < kCells / 32; ++u)
+                if (u == (n - 1) / 32) lastv = cell[u];
+            const int last = __shfl_sync(0xffffffffu, lastv, (n - 1) & 31);
+            // a list is ascending: its entries are consecutive cells iff last - first = n - 1
+            const bool contig = use_tma && __all_sync(0xffffffffu, valid) && last - first == n - 1;
+            if (contig) {
+                __syncwarp();
+                if (lane == 0) {
+                    const uint32_t fb = smem_addr(&kv_full[s]);
+                    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(fb), "r"(4 * kBlk)
+                                 : "memory");
+                    const int y = (int)(row0 + first);
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        asm volatile(
+                            "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+                            " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_addr(kt + h * kBlk)),
+                            "l"(reinterpret_cast<uint64_t>(&tmK)), "r"(fb), "r"(64 * h), "r"(y)
+                            : "memory");
+                        asm volatile(
+                            "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+                            " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_addr(vt + h * kBlk)),
+                            "l"(reinterpret_cast<uint64_t>(&tmV)), "r"(fb), "r"(64 * h), "r"(y)
+                            : "memory");
                     }
                 }
+            } else {
+#pragma unroll 1
+                for (int u = 0; u < kCells / 32; ++u) {
+                    const int i = lane + 32 * u;
+                    const bool ok = cpos[i] != INT_MAX;
+#pragma unroll
+                    for (int ch = 0; ch < 16; ++ch) {
+                        const uint32_t o = swz(i, ch);
+                        if (ok) {
+                            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(kt + o)),
+                                         "l"(K + (int64_t)cell[u] * kHD + ch * 8) : "memory");
+                            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(vt + o)),
+                                         "l"(V + (int64_t)cell[u] * kHD + ch * 8) : "memory");
+                        } else {
+                            *reinterpret_cast<uint4*>(kt + o) = make_uint4(0u, 0u, 0u, 0u);
+                            *reinterpret_cast<uint4*>(vt + o) = make_uint4(0u, 0u, 0u, 0u);
+                        }
+                    }
+                }
+                asm volatile("cp.async.commit_group;" ::: "memory");
+                asm volatile("cp.async.wait_group 0;" ::: "memory");
+                proxy_fence();
+                __syncwarp();
+                if (lane == 0) mb_arrive(&kv_full[s]);
             }
-            asm volatile("cp.async.commit_group;" ::: "memory");
-            asm volatile("cp.async.wait_group 0;" ::: "memory");
-            proxy_fence();
-            mb_arrive(&kv_full[p]);
         }
+        // the bulk copies issued have landed before the CTA can leave
+        __syncwarp();
+        if (lane == 0)
+            for (int j = nt > 2 ? nt - 2 : 0; j < nt; ++j) mb_wait(&kv_full[j & 1], (uint32_t)(j >> 1) & 1u);
     } else if (warp == 2) {
         if (lane == 0) {
             // ---- MMA issuer
@@ -329,6 +395,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnArgs a, float 
                 commit(o_done);
                 commit(&kv_empty[i & 1]);
             };
+            ok = nt == 0 || mb_wait(q_full, 0);
             int j = 0;
             for (; j < nt && ok; ++j) {
                 const int s = j & 1;
@@ -367,16 +434,25 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnArgs a, float 
             bool ok = mb_wait(&s_full[s], (uint32_t)(j >> 1) & 1u) && mb_wait(&kv_full[s], (uint32_t)(j >> 1) & 1u);
             if (!__all_sync(0xffffffffu, ok)) { live = false; break; }
             tc_after();
-            const int* cpos = cposb + s * kCells;
-            // pass 1: the row's largest visible score
+            const int4* cpos4 = reinterpret_cast<const int4*>(cposb + s * kCells);
+            // the row's 128 scores: two 64-column loads, one wait
+            uint32_t v[kCells];
+            ld64_nowait(sbuf[s] + lane_base, v);
+            ld64_nowait(sbuf[s] + lane_base + 64, v + 64);
+            asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+            tc_before();
+            mb_arrive(&s_free[s]);
+            // masked cells (position > the token's) become -inf; the largest visible score
             float mx = -INFINITY;
-#pragma unroll 1
-            for (int q = 0; q < kCells / 32; ++q) {
-                float v[32];
-                ld32(sbuf[s] + lane_base + 32 * q, v);
 #pragma unroll
-                for (int c = 0; c < 32; ++c)
-                    if (cpos[32 * q + c] <= rp) mx = fmaxf(mx, v[c]);
+            for (int c4 = 0; c4 < kCells / 4; ++c4) {
+                const int4 cp = cpos4[c4];
+                if (cp.x > rp) v[4 * c4] = __float_as_uint(-INFINITY);
+                if (cp.y > rp) v[4 * c4 + 1] = __float_as_uint(-INFINITY);
+                if (cp.z > rp) v[4 * c4 + 2] = __float_as_uint(-INFINITY);
+                if (cp.w > rp) v[4 * c4 + 3] = __float_as_uint(-INFINITY);
+                mx = fmaxf(mx, fmaxf(fmaxf(__uint_as_float(v[4 * c4]), __uint_as_float(v[4 * c4 + 1])),
+                                     fmaxf(__uint_as_float(v[4 * c4 + 2]), __uint_as_float(v[4 * c4 + 3]))));
             }
             const float mn = fmaxf(m, mx);
             float mu = m;
@@ -385,23 +461,15 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnArgs a, float 
                 rescale = m != -INFINITY && l > 0.f;
                 mu = mn;
             }
-            // pass 2: P = 2^(s - mu) of the visible cells (0 elsewhere), packed f16
-            uint32_t ph[kCells / 2];
+            // P = 2^(s - mu), packed f16 in place of the scores (a masked cell gives 0)
             float sum = 0.f;
 #pragma unroll
-            for (int q = 0; q < kCells / 32; ++q) {
-                float v[32];
-                ld32(sbuf[s] + lane_base + 32 * q, v);
-#pragma unroll
-                for (int c = 0; c < 32; c += 2) {
-                    const float p0 = (mu == -INFINITY || cpos[32 * q + c] > rp) ? 0.f : exp2f(v[c] - mu);
-                    const float p1 = (mu == -INFINITY || cpos[32 * q + c + 1] > rp) ? 0.f : exp2f(v[c + 1] - mu);
-                    sum += p0 + p1;
-                    ph[(32 * q + c) / 2] = pack_h2(p0, p1);
-                }
+            for (int c = 0; c < kCells; c += 2) {
+                const float p0 = mu == -INFINITY ? 0.f : exp2f(__uint_as_float(v[c]) - mu);
+                const float p1 = mu == -INFINITY ? 0.f : exp2f(__uint_as_float(v[c + 1]) - mu);
+                sum += p0 + p1;
+                v[c / 2] = pack_h2(p0, p1);
             }
-            tc_before();
-            mb_arrive(&s_free[s]);
             const float f = rescale ? exp2f(m - mu) : 1.f;
             l = l * f + sum;
             m = mu;
@@ -409,6 +477,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnArgs a, float 
             ok = j == 0 || mb_wait(o_done, (uint32_t)(j - 1) & 1u);
             if (!__all_sync(0xffffffffu, ok)) { live = false; break; }
             tc_after();
+#pragma unroll
+            for (int ch = 0; ch < kCells / 8; ++ch)
+                *reinterpret_cast<uint4*>(prow + swz(r, ch)) = make_uint4(v[4 * ch], v[4 * ch + 1], v[4 * ch + 2], v[4 * ch + 3]);
             // TMEM loads and stores are warp-wide: the whole warp rescales when any of its rows
             // needs it (f = 1 for the others)
             if (__any_sync(0xffffffffu, rescale)) {
@@ -422,10 +493,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnArgs a, float 
                 }
                 asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
             }
-#pragma unroll
-            for (int ch = 0; ch < kCells / 8; ++ch)
-                *reinterpret_cast<uint4*>(prow + swz(r, ch)) =
-                    make_uint4(ph[4 * ch], ph[4 * ch + 1], ph[4 * ch + 2], ph[4 * ch + 3]);
             proxy_fence();
             tc_before();
             mb_arrive(p_full);
@@ -530,7 +597,9 @@ bool launch_attention_tc(const AttnArgs& a, cudaStream_t st) {
     at[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = at;
     cfg.numAttrs = a.pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, attn_tc_kernel, a, scale_log2) == cudaSuccess;
+    const bool tma = a.kmap && a.vmap;
+    return cudaLaunchKernelEx(&cfg, attn_tc_kernel, a, scale_log2, tma ? *a.kmap : CUtensorMap{},
+                              tma ? *a.vmap : CUtensorMap{}, tma ? 1 : 0) == cudaSuccess;
 }
 
 }  // namespace llm

@@ -295,16 +295,25 @@ void build_attn_plan(const KvCells& cells, const SanBatch& b, int32_t i0, int32_
             }
         }
     }
-    // split each tile's list into work items
+    // split each tile's list into work items; list entries past the last one any token of the
+    // tile may see (position <= the tile's largest position) are left out
     const int32_t nt = (int32_t)p.tile_list.size();
+    std::vector<int32_t> tile_len(nt);
+    for (int32_t t = 0; t < nt; ++t) {
+        const int32_t l = p.tile_list[t];
+        int32_t pmax = INT32_MIN;
+        for (int32_t j = 0; j < p.tile_nq[t]; ++j) pmax = std::max(pmax, b.pos[i0 + p.perm[p.tile_start[t] + j]]);
+        int32_t L = p.list_off[l + 1] - p.list_off[l];
+        while (L > 1 && p.list_pos[p.list_off[l] + L - 1] > pmax) --L;
+        tile_len[t] = L;
+    }
     int32_t want = std::max(1, target_items / std::max(1, nt * n_head_kv));
     for (;;) {
         p.wi_tile.clear(); p.wi_c0.clear(); p.wi_c1.clear();
         p.wi_row_off.assign(1, 0);
         p.tile_wi_off.assign(1, 0);
         for (int32_t t = 0; t < nt; ++t) {
-            const int32_t l = p.tile_list[t];
-            const int32_t L = p.list_off[l + 1] - p.list_off[l];
+            const int32_t L = tile_len[t];
             int32_t chunk = (L + want - 1) / want;
             const int32_t gran = std::min<int32_t>(32, min_chunk);
             chunk = std::max(min_chunk, (chunk + gran - 1) / gran * gran);

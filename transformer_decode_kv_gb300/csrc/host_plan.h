@@ -110,7 +110,9 @@ void split_equal(const std::vector<int32_t>& seq_of, int32_t n_ubatch, std::vect
 //  - A "list" is the ascending set of cells shared with one distinct sequence set of the ubatch's
 //    tokens; a token may read a cell of its list iff cell.pos <= token.pos (causal).
 //  - Tokens are grouped by list (perm) and cut into query tiles of at most tile_q tokens.
-//  - Each tile's list is cut into work items of at most chunk cells (split-K over the cache).
+//  - Each tile's list is cut into work items of at most chunk cells (split-K over the cache); list
+//    entries after the last one with a position <= the tile's largest token position are left out
+//    (no token of the tile may see them).
 struct AttnPlan {
     std::vector<int32_t> list_off;      // [n_lists + 1]
     std::vector<int32_t> list_cells;    // concatenated cell indices

@@ -4,6 +4,7 @@
 
 #include <cstdint>
 #include <cuda_fp16.h>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 namespace llm {
@@ -147,6 +148,11 @@ struct AttnArgs {
     int32_t tile_q = kAttnTileQ;   // query tokens per tile of the plan (attention_tc_tile_q() for
                                    // the tcgen05 tiles)
     uint32_t* err = nullptr;       // error word (ERR_TIMEOUT from a bounded wait that ran out)
+    // tcgen05 tiles, F16 caches: TMA maps of the whole K and V caches as [layers x Hkv x n_ctx]
+    // rows of hd f16 (null: gather every row), and this layer's first row
+    const CUtensorMap* kmap = nullptr;
+    const CUtensorMap* vmap = nullptr;
+    int32_t kv_row0 = 0;
 };
 // Grouped-query attention of every token over the cells of its list with cell.pos <= token.pos:
 // split-K partial softmax per work item, then a combine per tile ([P2] Example 4 FLASH_ATTN_EXT;

@@ -136,6 +136,8 @@ struct llm_ctx {
     bool tc_f16 = false;                       // ... with f16 operands (one term each, token-major)
     CUtensorMap m_hh, m_ah, m_uh;              // f16 views of hb, attnb, ub (token box 128)
     CUtensorMap m_y_qkv, m_y_x, m_y_ub;        // outputs of the f16 token-major GEMMs (TMA-store epilogue)
+    CUtensorMap m_kc, m_vc;                    // F16 K and V caches as [layers x Hkv x n_ctx][hd] rows
+    bool kv_maps = false;
     bool tc_lm = false;                        // ... and for the output matrix
     float *part_o = nullptr, *part_m = nullptr, *part_l = nullptr;
     int32_t* tickets = nullptr;
@@ -639,6 +641,9 @@ bool forward_ubatch(llm_ctx* c, int32_t T, int32_t O, int32_t out_row0, int32_t 
         // ---- attention over the cache
         a.kc = kc;
         a.vc = vc;
+        a.kmap = c->kv_maps ? &c->m_kc : nullptr;
+        a.vmap = c->kv_maps ? &c->m_vc : nullptr;
+        a.kv_row0 = il * Hkv * c->n_ctx;
         a.k_scale = a.v_scale = nullptr;
         if (q8 && max_nq > 1) {
             // query tiles of several tokens run on tensor cores over f16 copies of the quants of
@@ -896,6 +901,12 @@ llm_ctx* llm_ctx_init(const llm_hparams* hp, const llm_cparams* cp) {
          cuda_ok(c, cudaMemsetAsync(c->kv_v, 0, kv_bytes, c->st), "memset") &&
          cuda_ok(c, cudaStreamSynchronize(c->st), "sync");
     if (!ok) return die("");
+    // bulk tensor copies of consecutive cells for the tcgen05 prefill attention (F16, hd 128)
+    if (c->type_k == LLM_TYPE_F16 && c->type_v == LLM_TYPE_F16 && h.head_dim == 128) {
+        const int64_t rows = (int64_t)h.n_layer * h.n_head_kv * c->n_ctx;
+        c->kv_maps = rows < INT32_MAX && tc_make_map(&c->m_kc, c->kv_k, rows, h.head_dim, 128, true) &&
+                     tc_make_map(&c->m_vc, c->kv_v, rows, h.head_dim, 128, true);
+    }
     return c;
 }
 
