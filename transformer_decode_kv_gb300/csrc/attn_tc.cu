@@ -13,7 +13,7 @@
 //                    stored (cells x dims: a B operand in MN-major layout)
 // Q and P are one f16 term each and accumulation is float32: the precision of a forward pass
 // whose matrix products take f16 activations. Scores are in the log2 domain (log2 e / sqrt(hd)
-// folded into Q). The running maximum is raised lazily: O and the row sum are rescaled only when
+// folded into Q; the powers of two by the hardware ex2 approximation). The running maximum is raised lazily: O and the row sum are rescaled only when
 // a row's maximum grows by more than 8 (P stays below 2^8 otherwise), and the final division
 // uses the same maximum for both, so the result does not depend on when rescaling happened.
 //
@@ -187,6 +187,14 @@ __device__ __forceinline__ void st32(uint32_t taddr, const float* v) {
         "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
         : "memory");
 }
+// 2^x by the hardware approximation (PTX ex2.approx.ftz: a few ulp of float32; -inf gives 0),
+// for P, which is rounded to f16 (11 significant bits) right after
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 // byte offset of 16-byte chunk `ch` (0..15) of row `r` in a [128 rows][128 f16] tile made of two
 // 128-byte-swizzled [128][64] blocks
 __device__ __forceinline__ uint32_t swz(int r, int ch) {
@@ -465,12 +473,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnArgs a, float 
             float sum = 0.f;
 #pragma unroll
             for (int c = 0; c < kCells; c += 2) {
-                const float p0 = mu == -INFINITY ? 0.f : exp2f(__uint_as_float(v[c]) - mu);
-                const float p1 = mu == -INFINITY ? 0.f : exp2f(__uint_as_float(v[c + 1]) - mu);
+                const float p0 = mu == -INFINITY ? 0.f : ex2(__uint_as_float(v[c]) - mu);
+                const float p1 = mu == -INFINITY ? 0.f : ex2(__uint_as_float(v[c + 1]) - mu);
                 sum += p0 + p1;
                 v[c / 2] = pack_h2(p0, p1);
             }
-            const float f = rescale ? exp2f(m - mu) : 1.f;
+            const float f = rescale ? ex2(m - mu) : 1.f;
             l = l * f + sum;
             m = mu;
             // O += P V of the previous step has ended: P's buffer is free and O is stable
