@@ -151,12 +151,14 @@ def test_error_paths_on_gpu():
     ctx.free(); ref.free()
 
 
-@pytest.mark.parametrize("n_prompt", [1000, 2000, 3500])
+@pytest.mark.parametrize("n_prompt", [1000, 2000, 2044, 3500])
 @pytest.mark.parametrize("tkv", [oracle.F16, oracle.Q8_0])
 def test_tiny_long_context_decode(tkv, n_prompt):
     """A long prompt then greedy steps, against the oracle; F16 and Q8_0 caches. The decode
-    attention's 16 blocks per KV head take slices of about 63, 125 and 219 cells: one, two and
-    four passes of 64 cells."""
+    attention's 16 blocks per KV head take slices of about 63 and 125 cells (one and two passes
+    of 64 cells); from 2048 cells on, two clusters of 16 share each KV head's list and merge
+    through global partial rows: 2044 crosses that bound between the third and fourth step,
+    3500 takes slices of about 110 cells."""
     key = "tiny_f32_1seq"
     over = dict(n_ctx=4096, n_batch=4096, n_ubatch=512, type_k=tkv, type_v=tkv)
     ctx, ora = G.library_ctx(key, **over), G.oracle_ctx(key, **over)

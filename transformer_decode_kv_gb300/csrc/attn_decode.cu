@@ -340,7 +340,12 @@ __device__ __forceinline__ uint32_t q8x2_to_h2(uint32_t biased, uint32_t sel) {
 
 // CL blocks per cluster: 16 for a few tokens; fewer (down to 1, no peers) when many tokens already
 // fill the GPU, so each block walks a longer slice and pays the fixed costs less often.
-template <int HD, typename KT, int CL, int NS, int MW>
+// NCL clusters per (token, KV head): with 2 (long lists) the list is cut into 2 CL slices and
+// twice as many blocks stream it (two per SM); each cluster merges its slices through
+// distributed shared memory as before, then block r of the one cluster and block r of the other
+// meet through global partial rows: each writes its (max, sum, outputs) and takes a ticket, and
+// the second to arrive combines both and stores the output (no block waits for another).
+template <int HD, typename KT, int CL, int NS, int MW, int NCL>
 __global__ void __launch_bounds__(MW * 32)
 attn_decode_mma_kernel(AttnArgs a, float scale_log2) {
     using SM = MmaDecSmem<HD, KT, NS, MW>;
@@ -379,8 +384,9 @@ attn_decode_mma_kernel(AttnArgs a, float scale_log2) {
     const int base = td1.y, len = td1.z;
     const int t = a.perm[td0.y];
     const int tpos = a.tok_pos[t];
-    const int chunk = (len + CL - 1) / CL;
-    const int c0 = min(len, (int)rank * chunk), c1 = min(len, c0 + chunk);
+    const int clq = NCL > 1 ? (int)(blockIdx.x / CL) : 0;        // which of the NCL clusters
+    const int chunk = (len + CL * NCL - 1) / (CL * NCL);
+    const int c0 = min(len, (clq * CL + (int)rank) * chunk), c1 = min(len, c0 + chunk);
     const int npass = c1 > c0 ? (c1 - c0 + CH - 1) / CH : 1;
     const uint8_t* K = static_cast<const uint8_t*>(a.kc) + (int64_t)kvh * a.n_ctx * RB;
     const uint8_t* V = static_cast<const uint8_t*>(a.vc) + (int64_t)kvh * a.n_ctx * RB;
@@ -675,13 +681,15 @@ attn_decode_mma_kernel(AttnArgs a, float scale_log2) {
     }
     cluster_sync_all();
     constexpr int OPB = kGQ * HD / CL;
-    for (int idx = threadIdx.x; idx < OPB; idx += MT) {
+    // the cluster's (max, sum, unnormalised output) of output oi = rank * OPB + idx
+    auto merge = [&](int idx, float& M, float& L, float& O) {
         const int oi = (int)rank * OPB + idx;
         const int h = oi / HD, dd = oi % HD;
-        float M = -INFINITY;
+        M = -INFINITY;
 #pragma unroll
         for (uint32_t r = 0; r < CL; ++r) M = fmaxf(M, ld_peer(pm + h, r));
-        float L = 0.f, O = 0.f;
+        L = 0.f;
+        O = 0.f;
 #pragma unroll
         for (uint32_t r = 0; r < CL; ++r) {
             const float mr = ld_peer(pm + h, r);
@@ -689,16 +697,65 @@ attn_decode_mma_kernel(AttnArgs a, float scale_log2) {
             L = fmaf(f, ld_peer(pl + h, r), L);
             O = fmaf(f, ld_peer(po + h * HD + dd, r), O);
         }
-        store_out(a, (int64_t)t * a.ldo + (kvh * kGQ + h) * HD + dd, L > 0.f ? O / L : 0.f);
+    };
+    if constexpr (NCL == 1) {
+        for (int idx = threadIdx.x; idx < OPB; idx += MT) {
+            float M, L, O;
+            merge(idx, M, L, O);
+            const int oi = (int)rank * OPB + idx;
+            store_out(a, (int64_t)t * a.ldo + (kvh * kGQ + oi / HD) * HD + oi % HD, L > 0.f ? O / L : 0.f);
+        }
+    } else {
+        // this cluster's share of block `rank`'s outputs (all of one head) goes to global partial
+        // rows [tile][cluster][head][KV head]; the ticket [tile][KV head][rank] counts the blocks
+        // with this rank that are done, and the last of the NCL combines the shares and stores
+        static_assert(OPB <= MT && HD % OPB == 0, "one output per thread, one head per block");
+        __shared__ int last_s;
+        const int h = (int)rank * OPB / HD, dd = (int)rank * OPB % HD + (int)threadIdx.x;
+        float M = -INFINITY, L = 0.f, O = 0.f;
+        if (threadIdx.x < OPB) {
+            merge(threadIdx.x, M, L, O);
+            const int64_t row = ((int64_t)(tile * NCL + clq) * kGQ + h) * a.Hkv + kvh;
+            if (threadIdx.x == 0) { a.part_m[row] = M; a.part_l[row] = L; }
+            a.part_o[row * HD + dd] = O;
+        }
+        __threadfence();
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            int* tkt = a.tickets + ((int64_t)tile * a.Hkv + kvh) * CL + rank;
+            const int done = atomicAdd(tkt, 1) + 1;
+            last_s = done == NCL;
+            if (done == NCL) *tkt = 0;                 // zero again for the next launch
+        }
+        __syncthreads();
+        if (last_s && threadIdx.x < OPB) {
+            __threadfence();
+            float Mx = M;
+            for (int q = 0; q < NCL; ++q) {
+                if (q == clq) continue;
+                Mx = fmaxf(Mx, __ldcg(a.part_m + ((int64_t)(tile * NCL + q) * kGQ + h) * a.Hkv + kvh));
+            }
+            float Lt = 0.f, Ot = 0.f;
+            for (int q = 0; q < NCL; ++q) {
+                const int64_t row = ((int64_t)(tile * NCL + q) * kGQ + h) * a.Hkv + kvh;
+                const float mq = q == clq ? M : __ldcg(a.part_m + row);
+                const float lq = q == clq ? L : __ldcg(a.part_l + row);
+                const float oq = q == clq ? O : __ldcg(a.part_o + row * HD + dd);
+                const float f = (Mx == -INFINITY || mq == -INFINITY) ? 0.f : exp2f(mq - Mx);
+                Lt = fmaf(f, lq, Lt);
+                Ot = fmaf(f, oq, Ot);
+            }
+            store_out(a, (int64_t)t * a.ldo + (kvh * kGQ + h) * HD + dd, Lt > 0.f ? Ot / Lt : 0.f);
+        }
     }
     cluster_sync_all();
 }
 
-template <int HD, typename KT, int CL, int NS, int MW>
+template <int HD, typename KT, int CL, int NS, int MW, int NCL = 1>
 bool launch_dec_mma_cl(const AttnArgs& a, cudaStream_t st) {
     const float scale_log2 = (float)(1.4426950408889634 / sqrt((double)HD));
     constexpr size_t smem = MmaDecSmem<HD, KT, NS, MW>::bytes;
-    auto k = attn_decode_mma_kernel<HD, KT, CL, NS, MW>;
+    auto k = attn_decode_mma_kernel<HD, KT, CL, NS, MW, NCL>;
     static bool attr = false;
     if (!attr) {
         if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess ||
@@ -707,7 +764,7 @@ bool launch_dec_mma_cl(const AttnArgs& a, cudaStream_t st) {
         attr = true;
     }
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(CL, a.Hkv, a.n_tok);
+    cfg.gridDim = dim3(CL * NCL, a.Hkv, a.n_tok);
     cfg.blockDim = dim3(MW * 32);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
@@ -740,10 +797,19 @@ int dec_cluster(int n_tok, int Hkv) {
     return 16 * units <= 2 * n_sm ? 16 : 4 * units <= 2 * n_sm ? 4 : 1;
 }
 
+// Two clusters per (token, KV head) when the lists are long (the caller's plan decides; its
+// choice is part of a captured step's key) and 2 x 16 blocks per unit still fit two per SM.
+bool dec_two_clusters(const AttnArgs& a) {
+    const int64_t units = (int64_t)a.Hkv * a.n_tok;
+    return a.long_lists && 2 * 16 * units <= 2 * (int64_t)sm_count();
+}
+
 template <int HD, typename KT>
 bool launch_dec_mma(const AttnArgs& a, cudaStream_t st) {
     switch (dec_cluster(a.n_tok, a.Hkv)) {
-        case 16: return launch_dec_mma_cl<HD, KT, 16, 2, 4>(a, st);
+        case 16:
+            if (dec_two_clusters(a)) return launch_dec_mma_cl<HD, KT, 16, 2, 4, 2>(a, st);
+            return launch_dec_mma_cl<HD, KT, 16, 2, 4>(a, st);
         case 4: return launch_dec_mma_cl<HD, KT, 4, 2, 4>(a, st);
     }
     return launch_dec_mma_cl<HD, KT, 1, 2, 4>(a, st);

@@ -131,7 +131,8 @@ struct AttnArgs {
     const int4* tile_desc;   // per tile, 2 x int4: {list, first token, tokens, first item},
                              //                     {end item, list start, list length, 0}
     const int4* wi_desc;     // per work item: {tile, first cell, end cell, first partial row}
-    int32_t* tickets;        // [tiles][Hkv] zero between launches (blocks done per tile)
+    int32_t* tickets;        // [tiles][Hkv] zero between launches (blocks done per tile); holds
+                             // kDecTicketsPerHead times as many
     float* part_o;           // [rows][Hkv][hd] unnormalised partial outputs
     float* part_m;           // [rows][Hkv] running max (log2 domain)
     float* part_l;           // [rows][Hkv] running sum
@@ -153,7 +154,13 @@ struct AttnArgs {
     const CUtensorMap* kmap = nullptr;
     const CUtensorMap* vmap = nullptr;
     int32_t kv_row0 = 0;
+    // decode steps: the ubatch's longest cell list reaches kDecLongList cells (the decode kernel
+    // may then split each (token, KV head) over two clusters; tickets then holds
+    // [tiles][Hkv][kDecTicketsPerHead])
+    bool long_lists = false;
 };
+constexpr int kDecTicketsPerHead = 16;
+constexpr int kDecLongList = 2048;
 // Grouped-query attention of every token over the cells of its list with cell.pos <= token.pos:
 // split-K partial softmax per work item, then a combine per tile ([P2] Example 4 FLASH_ATTN_EXT;
 // Example 11 for the unfused meaning). Scale 1/sqrt(hd).

@@ -184,10 +184,11 @@ struct llm_ctx {
     KStat kstat[KC_COUNT];
     double att_bytes_now = 0, att_flops_now = 0;
 
-    // decode-step graphs, per (tokens, outputs, output row, tile shape, timing) key
+    // decode-step graphs, per (tokens, outputs, output row, tile shape, timing, long lists) key
     bool use_graphs = true, use_pdl = true, use_bulk = true;
     // one-token ubatches as one persistent kernel (decode_step.cu)
     bool use_step = false, step_ok = false;
+    bool dec_long = false;                     // this decode ubatch's longest list >= kDecLongList
     StepLayer* d_step_layers = nullptr;
     uint32_t* d_counters = nullptr;     // its grid-wide phase counters [1 + 5 n_layer]
     int32_t* d_abort = nullptr;
@@ -522,6 +523,7 @@ bool forward_ubatch(llm_ctx* c, int32_t T, int32_t O, int32_t out_row0, int32_t 
     a.pdl = (c->use_pdl && gemv) || pdl_pre;
     a.slot = slot;                                   // tiles of one token use the cluster decode kernel
     a.n_tok = T;
+    a.long_lists = gemv && c->dec_long;
 
     GemvArgs g{};
     g.T = T;
@@ -887,8 +889,8 @@ llm_ctx* llm_ctx_init(const llm_hparams* hp, const llm_cparams* cp) {
         if (!ok) return die("");
     }
     c->max_rows = (int32_t)std::max<int64_t>(2 * U * G, 8192);
-    ok = dalloc(c, &c->tickets, (size_t)U * h.n_head_kv) &&
-         cuda_ok(c, cudaMemset(c->tickets, 0, sizeof(int32_t) * U * h.n_head_kv), "memset") &&
+    ok = dalloc(c, &c->tickets, (size_t)U * h.n_head_kv * kDecTicketsPerHead) &&
+         cuda_ok(c, cudaMemset(c->tickets, 0, sizeof(int32_t) * U * h.n_head_kv * kDecTicketsPerHead), "memset") &&
          dalloc(c, &c->part_o, (size_t)c->max_rows * h.n_head_kv * h.head_dim) &&
          dalloc(c, &c->part_m, (size_t)c->max_rows * h.n_head_kv) &&
          dalloc(c, &c->part_l, (size_t)c->max_rows * h.n_head_kv) &&
@@ -1051,7 +1053,8 @@ static bool reset_step_state(llm_ctx* c) {
     c->step_gen = 0;
     return cuda_ok(c, cudaMemsetAsync(c->d_counters, 0, sizeof(uint32_t) * (1 + 5 * (size_t)c->hp.n_layer), c->st), "memset") &&
            cuda_ok(c, cudaMemsetAsync(c->d_abort, 0, sizeof(int32_t), c->st), "memset") &&
-           cuda_ok(c, cudaMemsetAsync(c->tickets, 0, sizeof(int32_t) * c->n_ubatch * c->hp.n_head_kv, c->st), "memset");
+           cuda_ok(c, cudaMemsetAsync(c->tickets, 0, sizeof(int32_t) * c->n_ubatch * c->hp.n_head_kv * kDecTicketsPerHead,
+                                      c->st), "memset");
 }
 
 // One token through the whole model in one cooperative launch (inputs already uploaded).
@@ -1351,12 +1354,16 @@ int32_t llm_decode(llm_ctx* c, llm_batch bt) {
                   cuda_ok(c, cudaMemsetAsync(c->d_err, 0, sizeof(uint32_t), c->st), "memset");
         if (c->ktime) attention_work(c, b.pos.data() + i0);
         const int32_t max_nq = p.max_nq <= 1 ? 1 : tile_q;
+        int32_t max_len = 0;
+        for (size_t l = 0; l + 1 < p.list_off.size(); ++l) max_len = std::max(max_len, p.list_off[l + 1] - p.list_off[l]);
+        c->dec_long = max_len >= kDecLongList;
         const StepGraph* sg = nullptr;
         const bool one_kernel = ok && T == 1 && c->step_ok && !c->debug;
         if (one_kernel) ok = run_step(c, O, n_out);
         if (ok && !one_kernel && small && c->use_graphs && !c->debug) {
             const uint64_t key = (uint64_t)T | ((uint64_t)O << 10) | ((uint64_t)n_out << 20) |
-                                 ((uint64_t)(max_nq > 1) << 52) | ((uint64_t)c->ktime << 53);
+                                 ((uint64_t)(max_nq > 1) << 52) | ((uint64_t)c->ktime << 53) |
+                                 ((uint64_t)c->dec_long << 54);
             auto it = c->graphs.find(key);
             if (it == c->graphs.end()) {
                 StepGraph ng;
