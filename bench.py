@@ -504,6 +504,7 @@ def run_extra(key, stream, peaks):
     e1.record(stream)
     torch.cuda.synchronize()
     dec_s = e0.elapsed_time(e1) / 1e3
+    wdev = ctx.perf()["weight_device_bytes"]
     ctx.free()
     torch.cuda.empty_cache()
     step_bytes = float(np.mean([decode_step_bytes(w, v, w.n_seq) for v in visible_cells(w, w.n_decode)]))
@@ -518,7 +519,8 @@ def run_extra(key, stream, peaks):
             "prefill_tok_s": w.n_seq * w.n_prompt / prefill_s, "prefill_ms": prefill_s * 1e3,
             "prefill_flops": pre_fl, "prefill_tflops": pre_tf,
             "prefill_tensor_frac": pre_tf / peaks["bf16_tflops"],
-            "seq_rm_after_step": w.seq_rm_at if w.seq_rm_at > 0 else None}
+            "seq_rm_after_step": w.seq_rm_at if w.seq_rm_at > 0 else None,
+            "weight_device_bytes": wdev}
 
 
 def main():

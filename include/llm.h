@@ -237,6 +237,9 @@ typedef struct llm_perf_data {
     double  t_decode_ms;
     int64_t n_fused_steps;   /* one-token ubatches run as the single persistent kernel */
     int64_t n_defrags;       /* cache defrags that moved cells (llm_memory_update or a retry) */
+    int64_t weight_device_bytes;  /* device memory holding the weights as stored plus the operand
+                                     copies made for the prefill matrix products (a BF16 weight's
+                                     f16 copy; Q8_0 weights get none) */
 } llm_perf_data;
 void llm_perf(llm_ctx *ctx, llm_perf_data *out);
 
@@ -342,6 +345,25 @@ int llm_debug_gemm_bf16(int32_t epi, const void *W, int64_t M, int64_t K, const 
 int llm_debug_gemm_tn_f16(int32_t epi, const void *W, const void *W_lo, int64_t M, int64_t K,
                           const void *X, int32_t T, float *Y, int32_t ldy, int32_t F, int32_t splits,
                           int32_t one_cta);
+
+/* llm_debug_gemm_tn_f16 over a Q8_0 weight held as the library stores it ([P2] "llama.cpp
+ * Architecture", Example 2 block: an fp16 scale d and 32 int8 quants q, value d * q): Wq int8
+ * row-major [rows][K], Ws fp16 scales [rows][K / 32] (device memory, 16-byte aligned), X f16
+ * [T][K]. The two-CTA kernel dequantises each 64-wide k-step into the exact f16 terms of d * q in
+ * shared memory; any T >= 1. epi and the remaining arguments as for llm_debug_gemm_tn_f16.
+ * Returns 0, -1 for an unsupported shape, -3 on a failure. */
+int llm_debug_gemm_tn_q8(int32_t epi, const void *Wq, const void *Ws, int64_t M, int64_t K, const void *X,
+                         int32_t T, float *Y, int32_t ldy, int32_t F, int32_t splits);
+
+/* llm_debug_gemm_tn_q8 with per-CTA counters: 8 uint64 values per CTA in trace (start and end
+ * global-timer stamps in ns at 0 and 7, the accumulator-ready stamp at 6; SM cycles the first
+ * converter thread waited for quant tiles (1), for free stages (2) and spent converting (3); SM
+ * cycles the MMA thread of the pair's leader waited for activation tiles (4) and for converted
+ * terms (5)), CTAs in launch order. Returns the number of values written (cap must hold them), -1
+ * for an unsupported shape or a short buffer, -3 on a failure. */
+int64_t llm_debug_gemm_tn_q8_trace(int32_t epi, const void *Wq, const void *Ws, int64_t M, int64_t K,
+                                   const void *X, int32_t T, float *Y, int32_t ldy, int32_t F,
+                                   int32_t splits, uint64_t *trace, int64_t cap);
 
 /* The two-CTA token-major GEMM of llm_debug_gemm_tn_f16 (T > 128, one weight term) with a
  * timeline: per CTA 8 uint64 values in trace, global-timer stamps in ns (start, set-up done, first

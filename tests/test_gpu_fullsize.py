@@ -46,6 +46,9 @@ def test_llama8b_q8_0_8k_prompt_and_decode_layerwise():
     toks = G.prompts(key)[0]
     report = {}
 
+    # Q8_0 linear weights as stored (no f16 copies for the prefill GEMMs): below 12 GB with the
+    # float32 embeddings
+    assert ctx.perf()["weight_device_bytes"] < 12e9, ctx.perf()
     ctx.debug_capture(True)
     assert ctx.decode(toks) == 0, ctx.last_error()
     assert mirror.decode(toks) == 0

@@ -1,5 +1,6 @@
-"""GPU parity of Q8_0 prefill on the tensor cores (each Q8_0 weight d*q as two f16 terms, hi + lo,
-which hold it exactly, in the token-major tcgen05 GEMM; activations one f16 term) on a 2-layer
+"""GPU parity of Q8_0 prefill on the tensor cores (the token-major tcgen05 GEMM reads each Q8_0
+weight as stored and dequantises every k-step into two f16 terms, hi + lo, which hold d*q exactly;
+activations one f16 term) on a 2-layer
 model of the Llama-3-8B layer shape with Q8_0 linear weights and F32 embeddings/norms (the 8k
 workload's types), through the C ABI.
 
@@ -35,6 +36,14 @@ def test_q8_0_prefill_on_tensor_cores_matches_oracle():
     assert ctx.decode(toks, logits=flags) == 0, ctx.last_error()
     assert ora.decode(toks, logits=flags) == 0
     assert ctx.perf()["n_ubatches"] == 1
+    # the weights stay as stored (Q8_0: 34 bytes per 32 values), plus, for the prefill GEMMs, a
+    # second copy of the linear layers' block scales in the per-k-step layout (2 bytes per 32)
+    q8 = lambda rows, cols: rows * cols // 32 * (34 + 2)
+    qkvw = (HP.n_head + 2 * HP.n_head_kv) * HP.head_dim
+    per_layer = (q8(qkvw, HP.n_embd) + q8(HP.n_embd, HP.n_head * HP.head_dim) + q8(2 * HP.n_ff, HP.n_embd) +
+                 q8(HP.n_embd, HP.n_ff))
+    stored = HP.n_layer * per_layer + HP.n_vocab * HP.n_embd * 4 + HP.n_vocab * HP.n_embd // 32 * 34
+    assert ctx.perf()["weight_device_bytes"] == stored
     errs = []
     for i in (0, 100, 300, 511):
         errs.append(G.rel_err(ctx.get_logits_ith(i), ora.get_logits_ith(i)))

@@ -49,7 +49,8 @@ class SamplerParams(C.Structure):
 class PerfData(C.Structure):
     _fields_ = [("n_decode_calls", C.c_int64), ("n_tokens", C.c_int64), ("n_ubatches", C.c_int64),
                 ("n_graph_replays", C.c_int64), ("t_decode_ms", C.c_double),
-                ("n_fused_steps", C.c_int64), ("n_defrags", C.c_int64)]
+                ("n_fused_steps", C.c_int64), ("n_defrags", C.c_int64),
+                ("weight_device_bytes", C.c_int64)]
 
 
 ABORT_CB = C.CFUNCTYPE(C.c_int, C.c_void_p)
@@ -98,6 +99,11 @@ SIGNATURES = {
     "llm_debug_gemm_tn_f16_trace": (C.c_int64, [C.c_int32, C.c_void_p, C.c_int64, C.c_int64, C.c_void_p, C.c_int32,
                                               C.c_void_p, C.c_int32, C.c_int32, C.c_int32,
                                               C.POINTER(C.c_uint64), C.c_int64]),
+    "llm_debug_gemm_tn_q8": (C.c_int, [C.c_int32, C.c_void_p, C.c_void_p, C.c_int64, C.c_int64, C.c_void_p,
+                                       C.c_int32, C.c_void_p, C.c_int32, C.c_int32, C.c_int32]),
+    "llm_debug_gemm_tn_q8_trace": (C.c_int64, [C.c_int32, C.c_void_p, C.c_void_p, C.c_int64, C.c_int64,
+                                             C.c_void_p, C.c_int32, C.c_void_p, C.c_int32, C.c_int32, C.c_int32,
+                                             C.POINTER(C.c_uint64), C.c_int64]),
     "llm_debug_gemm_tn_f16": (C.c_int, [C.c_int32, C.c_void_p, C.c_void_p, C.c_int64, C.c_int64, C.c_void_p,
                                         C.c_int32, C.c_void_p, C.c_int32, C.c_int32, C.c_int32, C.c_int32]),
     "llm_debug_gemm_bf16": (C.c_int, [C.c_int32, C.c_void_p, C.c_int64, C.c_int64, C.c_void_p,
@@ -159,6 +165,26 @@ def debug_gemm_tn_f16(epi: int, W, X, Y, F: int = 0, W_lo=None, splits: int = 1,
                                        C.c_void_p(W_lo.data_ptr()) if W_lo is not None else None,
                                        M, W.shape[1], C.c_void_p(X.data_ptr()), X.shape[0],
                                        C.c_void_p(Y.data_ptr()), Y.stride(0), F, splits, int(one_cta))
+
+
+def debug_gemm_tn_q8(epi: int, Wq, Ws, X, Y, F: int = 0, splits: int = 1) -> int:
+    """The token-major GEMM over a Q8_0 weight (Wq int8 [rows][K], Ws f16 scales [rows][K / 32], X f16
+    [T][K]) dequantised inside the kernel."""
+    M = Wq.shape[0] if epi != 2 else 0
+    return lib().llm_debug_gemm_tn_q8(epi, C.c_void_p(Wq.data_ptr()), C.c_void_p(Ws.data_ptr()), M, Wq.shape[1],
+                                      C.c_void_p(X.data_ptr()), X.shape[0], C.c_void_p(Y.data_ptr()), Y.stride(0),
+                                      F, splits)
+
+
+def debug_gemm_tn_q8_trace(epi: int, Wq, Ws, X, Y, F: int = 0, splits: int = 1):
+    """The Q8_0 token-major GEMM with its per-CTA counters: returns (status, [n_cta, 8] uint64)."""
+    M = Wq.shape[0] if epi != 2 else 0
+    cap = 8 * 8192
+    out = np.zeros(cap, dtype=np.uint64)
+    n = lib().llm_debug_gemm_tn_q8_trace(epi, C.c_void_p(Wq.data_ptr()), C.c_void_p(Ws.data_ptr()), M, Wq.shape[1],
+                                         C.c_void_p(X.data_ptr()), X.shape[0], C.c_void_p(Y.data_ptr()), Y.stride(0),
+                                         F, splits, out.ctypes.data_as(C.POINTER(C.c_uint64)), cap)
+    return (0, out[:n].reshape(-1, 8)) if n > 0 else (int(n), None)
 
 
 def debug_gemm_tn_f16_trace(epi: int, W, X, Y, F: int = 0, splits: int = 1):

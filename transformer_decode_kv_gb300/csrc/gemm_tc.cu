@@ -935,6 +935,463 @@ gemm_tn2_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
     if (TRACE && threadIdx.x == 0) tr[6] = global_ns();
 }
 
+// ---- Q8_0 weights dequantised inside the two-CTA kernel
+//
+// The weight operand is read from HBM as stored (int8 quants, one fp16 scale per 32 values: 34
+// bytes per 32 weights) instead of as precomputed f16 terms (4 bytes per weight). The product is
+// computed transposed, D[weight row][token] = (hi + lo) X^T: the weight terms are the MMA's A
+// operand, held in tensor memory, and the token tile is B in shared memory. Per k-step of 64
+// values a producer thread copies this CTA's 128 x 64 quant tile and the rows' block scales into a
+// raw ring (64-byte swizzle), and sixteen converter warps (four threads per weight row, 16 quants
+// each) turn it into the two f16 terms hi = rn(d q) and lo = rn(d q - hi) (hi + lo = d q exactly)
+// and store them into a ring of tensor-memory stages with tcgen05.st. Compared with terms in
+// shared memory this keeps the converters' stores off shared memory, whose bandwidth the MMA's
+// operand reads (the token tile is read by both CTAs of the pair, once per term) already fill.
+// ([P2] "llama.cpp Architecture", Example 4 MUL_MAT over a q8_0 weight; the block format of the
+// GGUF quant types.)
+// Warps 0-3: token-tile producer (thread 0), MMA issuer (thread 32, leader CTA), quant-tile
+// producer (thread 64), then the epilogue (each warp 32 weight rows, the tensor-memory lanes it may
+// access); warps 4 and up: converters. SwiGLU: a CTA's 128 weight rows are the gate rows of 64
+// features and then their up rows, so a product's two factors are in the same CTA.
+constexpr uint32_t kQ8Tok = kTn2Half;                     // 128 tokens x 64 f16: 16 KB
+constexpr int kQ8TokStages = 6;
+constexpr uint32_t kQ8Quants = 128 * kBK;                // 128 rows x 64 quants: 8 KB
+constexpr uint32_t kQ8Raw = kQ8Quants + 128 * 4;          // + the rows' two block scales each
+constexpr int kQ8RawStages = 6;
+constexpr int kQ8AStages = 4;                             // tensor-memory stages of 64 columns (hi, lo)
+constexpr uint32_t kQ8ACol0 = kTnN;                       // the accumulator takes columns [0, 256)
+constexpr int kQ8ConvWarps = 16;
+constexpr int kQ8Threads = 128 + 32 * kQ8ConvWarps;
+constexpr size_t kQ8Smem = 1024 + (size_t)kQ8TokStages * kQ8Tok + (size_t)kQ8RawStages * kQ8Raw + 512;
+static_assert(kQ8Smem <= 232448, "the Q8_0 rings fit one CTA's shared memory");
+static_assert(kQ8ACol0 + 64 * kQ8AStages <= 512, "accumulator and weight stages fit tensor memory");
+
+__device__ __forceinline__ bool mbar_try_cluster(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// the same bounded wait, acquiring at cluster scope (arrivals that release from the peer CTA)
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity) {
+    if (mbar_try_cluster(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    while (!mbar_try_cluster(bar, parity))
+        if (global_ns() - t0 > kWaitNs) return false;
+    return true;
+}
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_bar) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_local(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+// four int8 quants (one 32-bit word) times the block scale d as f16 terms: (hi01, hi23, lo01, lo23)
+__device__ __forceinline__ void q8x4_terms(uint32_t w, __half2 d, uint32_t& h01, uint32_t& h23, uint32_t& l01,
+                                           uint32_t& l23) {
+    const uint32_t u = w ^ 0x80808080u;                  // q + 128 as unsigned bytes
+    const uint32_t b01 = __byte_perm(u, 0x64646464u, 0x4140u), b23 = __byte_perm(u, 0x64646464u, 0x4342u);
+    const __half2 off = __halves2half2(__ushort_as_half(0x6480u), __ushort_as_half(0x6480u));   // 1152
+    // 1024 + (q + 128) - 1152 = q, exact in f16
+    const __half2 q01 = __hsub2(*reinterpret_cast<const __half2*>(&b01), off);
+    const __half2 q23 = __hsub2(*reinterpret_cast<const __half2*>(&b23), off);
+    const __half2 x01 = __hmul2(q01, d), x23 = __hmul2(q23, d);
+    const __half2 y01 = __hfma2(q01, d, __hneg2(x01)), y23 = __hfma2(q23, d, __hneg2(x23));
+    h01 = *reinterpret_cast<const uint32_t*>(&x01);
+    h23 = *reinterpret_cast<const uint32_t*>(&x23);
+    l01 = *reinterpret_cast<const uint32_t*>(&y01);
+    l23 = *reinterpret_cast<const uint32_t*>(&y23);
+}
+
+// A from tensor memory, B from shared memory, D in tensor memory (the pair's MMA)
+__device__ __forceinline__ void umma_ts_pair(uint32_t dtmem, uint32_t atmem, uint64_t b, uint32_t idesc,
+                                             uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(dtmem),
+        "r"(atmem), "l"(b), "r"(idesc), "r"(accumulate));
+}
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t* v) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"(v[0]),
+                 "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+                 : "memory");
+}
+
+// The transposed epilogue: warp w (< 4) holds D rows 32 w .. 32 w + 31 of this CTA (weight rows, one
+// per lane) for the pair's 256 tokens (tensor-memory columns), read 32 tokens at a time. With an
+// output map the values go through shared-memory boxes of 32 tokens x 128 bytes (128-byte
+// swizzle, written transposed: one lane per column) and bulk tensor stores, or element-wise
+// reduce-adds in L2 for the residual add and K splits; without one, direct stores.
+template <int EPI>
+__device__ __forceinline__ void q8t_epilogue(uint32_t tmem, int warp, int lane, int tok0, int T, int mrow0,
+                                             bool live, bool split, const CUtensorMap* ymap, void* Y, int ldy,
+                                             const TnQkv& qe, uint8_t* stage, uint32_t* err) {
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const int m = mrow0 + warp * 32 + lane;                 // this lane's weight row (not SwiGLU)
+    const int qcols = qe.H * qe.hd, kcols = qe.Hkv * qe.hd;
+    const bool rot = EPI == GEMM_EPI_QKV && mrow0 < qcols + kcols;
+    const bool isq = EPI == GEMM_EPI_QKV && mrow0 < qcols;
+    const bool isk = EPI == GEMM_EPI_QKV && !isq && mrow0 < qcols + kcols;
+    const bool boxes = ymap != nullptr && (EPI != GEMM_EPI_QKV || isq);
+    const bool reduce = EPI == GEMM_EPI_ADD || split;
+    // boxes: warp w's two 4 KB buffers (f32 outputs); SwiGLU: one 4 KB f16 box per chunk shared by
+    // warps 0 and 1, two buffers, and the exchange area for the up values
+    uint8_t* wbuf = stage + warp * 8192;
+    float* exf = reinterpret_cast<float*>(stage + 32768);
+    uint8_t* hbuf = stage + 32768 + 9216;                   // 1024-aligned, after the exchange area
+    static_assert(2 * 64 * 17 * 4 <= 9216, "exchange area");
+#pragma unroll 1
+    for (int b = 0; b < kTnN / 32; ++b) {
+        float v[32];
+        tmem_ld32(tmem + lane_base + (uint32_t)(32 * b), v);
+        const int t0 = tok0 + 32 * b;
+        if (EPI == GEMM_EPI_SWIGLU) {
+            // warps 0, 1 hold the gate rows of the CTA's 64 features, warps 2, 3 their up rows; the
+            // gate warps take tokens 0-15 of the chunk and the up warps tokens 16-31, each handing
+            // the other half of its values over through shared memory (ex [2][64 features][17])
+            const int f = (warp & 1) * 32 + lane;                    // feature within the CTA's 64
+            const bool gate = warp < 2;
+            float* mine = exf + (gate ? 0 : 64 * 17);                // what this warp hands over
+            float* theirs = exf + (gate ? 64 * 17 : 0);
+            if (b >= 2 && threadIdx.x == 0 && boxes) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+#pragma unroll
+            for (int j = 0; j < 16; ++j) mine[f * 17 + j] = v[gate ? 16 + j : j];
+            asm volatile("bar.sync 1, 128;" ::: "memory");
+            uint8_t* box = hbuf + (b & 1) * 4096;
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                const int jj = gate ? j : 16 + j;                    // token within the chunk
+                const float g = gate ? v[j] : theirs[f * 17 + j];
+                const float u = gate ? theirs[f * 17 + j] : v[16 + j];
+                const __half h = __float2half_rn(silu_mul_fast(g, u));
+                if (boxes) {
+                    *reinterpret_cast<__half*>(box + jj * 128 + ((((uint32_t)f >> 3) ^ (uint32_t)(jj & 7)) << 4) +
+                                               (f & 7) * 2) = h;
+                } else if (live && t0 + jj < T) {
+                    static_cast<__half*>(Y)[(int64_t)(t0 + jj) * ldy + mrow0 + f] = h;
+                }
+            }
+            if (boxes) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            asm volatile("bar.sync 1, 128;" ::: "memory");
+            if (boxes && threadIdx.x == 0 && live && t0 < T) {
+                tma_store_2d(ymap, box, mrow0, t0);
+                asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+            }
+            continue;
+        }
+        if (EPI == GEMM_EPI_QKV && rot) {
+            // adjacent pairs (2i, 2i + 1) of a head turn by the token's angle for pair i; the pair's
+            // two values are in neighbouring lanes
+            const int e = m % qe.hd;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                const int t = min(t0 + j, T - 1);
+                const float2 cs = qe.cs[(int64_t)t * (qe.hd / 2) + e / 2];
+                const float o = __shfl_xor_sync(0xffffffffu, v[j], 1);
+                v[j] = (e & 1) ? fmaf(o, cs.y, v[j] * cs.x) : fmaf(-o, cs.y, v[j] * cs.x);
+            }
+        }
+        if (EPI == GEMM_EPI_QKV && !isq) {
+            if (!live) continue;
+            const int e = m % qe.hd;
+            const int kvh = (m - qcols - (isk ? 0 : kcols)) / qe.hd;
+            __half* cache = static_cast<__half*>(isk ? qe.kc : qe.vc);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                const int t = t0 + j;
+                if (t >= T) continue;
+                const int32_t cell = qe.slot[t];
+                if (cell < 0 || cell >= qe.n_ctx) {
+                    if (e == 0) atomicOr(err, ERR_SLOT_RANGE);
+                    continue;
+                }
+                cache[((int64_t)kvh * qe.n_ctx + cell) * qe.hd + e] = __float2half_rn(v[j]);
+            }
+            continue;
+        }
+        if (boxes) {
+            uint8_t* box = wbuf + (b & 1) * 4096;
+            if (b >= 2 && lane == 0) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+            __syncwarp();
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+                *reinterpret_cast<float*>(box + j * 128 + ((((uint32_t)lane >> 2) ^ (uint32_t)(j & 7)) << 4) +
+                                          (lane & 3) * 4) = v[j];
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            __syncwarp();
+            if (lane == 0 && live && t0 < T) {
+                if (reduce) tma_reduce_add_2d(ymap, box, mrow0 + warp * 32, t0);
+                else tma_store_2d(ymap, box, mrow0 + warp * 32, t0);
+                asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+            }
+            continue;
+        }
+        if (!live) continue;
+        float* y = static_cast<float*>(Y);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            const int t = t0 + j;
+            if (t >= T) continue;
+            float* dst = y + (int64_t)t * ldy + m;
+            if (reduce) atomicAdd(dst, v[j]);
+            else *dst = v[j];
+        }
+    }
+    // the boxes have been read before the shared memory is given up
+    if (lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+    __syncwarp();
+}
+
+// TRACE: per CTA 8 values in trace: 0 start (global timer, ns), SM cycles the first converter
+// thread spent 1 waiting for quant tiles, 2 waiting for free weight stages, 3 converting; SM cycles
+// the MMA thread (leader) spent 4 waiting for token tiles, 5 waiting for converted terms; 6 the
+// accumulator ready, 7 the end (global timer, ns).
+template <int EPI, bool TRACE>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kQ8Threads, 1)
+gemm_tn2q8_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmQ,
+                  const uint32_t* __restrict__ kscales, int wrows, const __grid_constant__ CUtensorMap tmY,
+                  int use_ymap, const TnQkv qe, int K, int T, int M, int F, void* __restrict__ Y, int ldy,
+                  uint32_t* __restrict__ err, uint64_t* __restrict__ trace) {
+    constexpr int ST = kQ8TokStages, R = kQ8RawStages, SA = kQ8AStages;
+    uint64_t* tr = TRACE ? trace + 8 * (size_t)(blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z))
+                         : nullptr;
+    if (TRACE && threadIdx.x == 0) tr[0] = global_ns();
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    uint8_t* raw = smem + ST * kQ8Tok;
+    uint64_t* tfull = reinterpret_cast<uint64_t*>(raw + R * kQ8Raw);   // token tiles (leader: both CTAs)
+    uint64_t* tempty = tfull + ST;                                       // token stage read (both CTAs)
+    uint64_t* afull = tempty + ST;                                       // weight terms (leader: its 16
+                                                                         // warps + the peer's forward)
+    uint64_t* aempty = afull + SA;                                       // weight stage read (both CTAs)
+    uint64_t* cfull = aempty + SA;                                       // peer: its 16 warps' terms
+    uint64_t* rfull = cfull + SA;                                        // quant tile landed (local)
+    uint64_t* rempty = rfull + R;                                        // quant tile converted (local)
+    uint64_t* accf = rempty + R;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accf + 1);
+    int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
+
+    const uint32_t rank = cluster_rank();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nk_all = K / kBK;
+    const int per = (nk_all + gridDim.z - 1) / gridDim.z;
+    const int kb0 = min(nk_all, (int)blockIdx.z * per), nk = min(nk_all, kb0 + per) - kb0;
+    const int tok0 = (int)(blockIdx.x >> 1) * 2 * kTnRows;               // the pair's first token
+    const int tm = tok0 + (int)rank * kTnRows;                           // this CTA's B rows
+    // this CTA's 128 weight rows: SwiGLU gate rows of features [fg, fg + 64) then their up rows;
+    // otherwise rows [mrow0, mrow0 + 128)
+    const int fg = blockIdx.y * (kTnN / 2) + (int)rank * 64;
+    const int mrow0 = EPI == GEMM_EPI_SWIGLU ? fg : blockIdx.y * kTnN + (int)rank * kTnRows;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < ST; ++s) {
+            mbar_init(&tfull[s], 1);
+            mbar_init(&tempty[s], 1);
+        }
+        for (int a = 0; a < SA; ++a) {
+            mbar_init(&afull[a], kQ8ConvWarps + 1);
+            mbar_init(&aempty[a], 1);
+            mbar_init(&cfull[a], kQ8ConvWarps);
+        }
+        for (int r = 0; r < R; ++r) {
+            mbar_init(&rfull[r], 1);
+            mbar_init(&rempty[r], kQ8ConvWarps);
+        }
+        mbar_init(accf, 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmX)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmQ)) : "memory");
+    }
+    if (warp == 0) {
+        // the accumulator (256 columns) and the weight stages (4 x 64 columns), in both SMs
+        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(tmem_slot)),
+                     "r"(512u));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;");
+    }
+    tc_fence_before();
+    cluster_sync_all();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (threadIdx.x == 64) {
+        // ---- quant-tile producer: the quants of k-step kb by tensor copy, the rows' scales of
+        // that k-step (contiguous in the per-k-step scale layout) by bulk copies, into raw slot
+        // kb % R once the converters are done with it. Not written by the kernel before: no grid
+        // dependency wait.
+        int rissued = 0;
+        for (int kb = 0; kb < nk; ++kb) {
+            const int r = kb % R;
+            if (kb >= R && !mbar_wait(&rempty[r], ((uint32_t)(kb / R) & 1u) ^ 1u)) {
+                atomicOr(err, ERR_TIMEOUT); *(volatile int*)abort_flag = 1; break;
+            }
+            if (*(volatile int*)abort_flag) break;
+            uint8_t* dst = raw + (size_t)r * kQ8Raw;
+            const int kx = (kb0 + kb) * kBK;
+            const uint32_t* ks = kscales + (int64_t)(kb0 + kb) * wrows;
+            mbar_expect_tx(&rfull[r], kQ8Raw);
+            if (EPI == GEMM_EPI_SWIGLU) {
+                tma_load_2d(dst, &tmQ, &rfull[r], kx, fg);
+                tma_load_2d(dst + 64 * kBK, &tmQ, &rfull[r], kx, F + fg);
+            } else {
+                tma_load_2d(dst, &tmQ, &rfull[r], kx, mrow0);
+            }
+            const int nseg = EPI == GEMM_EPI_SWIGLU ? 2 : 1;
+            for (int g = 0; g < nseg; ++g) {
+                const int row = EPI == GEMM_EPI_SWIGLU ? (g ? F + fg : fg) : mrow0;
+                asm volatile(
+                    "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                        smem_u32(dst + kQ8Quants + g * (128 / nseg) * 4)),
+                    "l"(ks + row), "r"((uint32_t)(128 / nseg) * 4u), "r"(smem_u32(&rfull[r]))
+                    : "memory");
+            }
+            rissued = kb + 1;
+        }
+        for (int kb = (rissued > R ? rissued - R : 0); kb < rissued; ++kb)
+            mbar_wait(&rfull[kb % R], (uint32_t)(kb / R) & 1u);
+    } else if (threadIdx.x == 0) {
+        // ---- token-tile producer (both CTAs: this CTA's 128 tokens, half of the pair's B)
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+        int issued = 0;
+        for (int kb = 0; kb < nk; ++kb) {
+            const int s = kb % ST;
+            if (kb >= ST && !mbar_wait(&tempty[s], ((uint32_t)(kb / ST) & 1u) ^ 1u)) {
+                atomicOr(err, ERR_TIMEOUT); *(volatile int*)abort_flag = 1; break;
+            }
+            if (*(volatile int*)abort_flag) break;
+            if (rank == 0) mbar_expect_tx(&tfull[s], 2 * kQ8Tok);
+            tma_load_2d_pair(smem + (size_t)s * kQ8Tok, &tmX, cluster_addr(smem_u32(&tfull[s]), 0), (kb0 + kb) * kBK,
+                             tm);
+            issued = kb + 1;
+        }
+        if (rank == 0) {
+            for (int kb = (issued > ST ? issued - ST : 0); kb < issued; ++kb)
+                mbar_wait(&tfull[kb % ST], (uint32_t)(kb / ST) & 1u);
+        } else if (issued > 0) {
+            mbar_wait(&tempty[(issued - 1) % ST], (uint32_t)((issued - 1) / ST) & 1u);
+        }
+    } else if (rank == 1 && (threadIdx.x == 96 || threadIdx.x == 32)) {
+        // ---- forwarders (peer CTA, even and odd k-steps): once the peer's 16 converter warps have
+        // stored a stage, one arrival on the leader's barrier. An arrival that releases at cluster
+        // scope stalls its thread for a long time; here it holds up no converter, and two
+        // forwarders take alternate k-steps.
+        const uint32_t afull0 = cluster_addr(smem_u32(&afull[0]), 0);
+        for (int kb = threadIdx.x == 96 ? 0 : 1; kb < nk; kb += 2) {
+            const int a = kb % SA;
+            if (!mbar_wait(&cfull[a], (uint32_t)(kb / SA) & 1u)) {
+                atomicOr(err, ERR_TIMEOUT); *(volatile int*)abort_flag = 1; break;
+            }
+            mbar_arrive_cluster(afull0 + (uint32_t)(a * 8));
+        }
+    } else if (threadIdx.x == 32 && rank == 0) {
+        // ---- MMA issuer (leader): D[256 weight rows][256 tokens] += (hi + lo) X^T
+        constexpr uint32_t idesc = idesc_f16(2 * kTnRows, kTnN);
+        bool ok = true;
+        long long wa = 0, wb = 0;
+        for (int kb = 0; kb < nk; ++kb) {
+            const int s = kb % ST, a = kb % SA;
+            const long long c0 = TRACE ? clock64() : 0;
+            if (!mbar_wait(&tfull[s], (uint32_t)(kb / ST) & 1u)) { ok = false; break; }
+            const long long c1 = TRACE ? clock64() : 0;
+            if (!mbar_wait_cluster(&afull[a], (uint32_t)(kb / SA) & 1u)) { ok = false; break; }
+            if (TRACE) { wa += c1 - c0; wb += clock64() - c1; }
+            tc_fence_after();
+            const uint64_t bd = sdesc_sw128(smem_u32(smem + (size_t)s * kQ8Tok));
+            const uint32_t ahi = tmem + kQ8ACol0 + 64u * (uint32_t)a, alo = ahi + 32u;
+#pragma unroll
+            for (int kk = 0; kk < kBK / 16; ++kk) {
+                umma_ts_pair(tmem, ahi + 8u * kk, bd + (uint64_t)(kk * 2), idesc, (kb | kk) != 0 ? 1u : 0u);
+                umma_ts_pair(tmem, alo + 8u * kk, bd + (uint64_t)(kk * 2), idesc, 1u);
+            }
+            umma_commit_pair(&tempty[s]);
+            umma_commit_pair(&aempty[a]);
+        }
+        if (!ok) { atomicOr(err, ERR_TIMEOUT); *(volatile int*)abort_flag = 1; }
+        umma_commit_pair(accf);
+        if (TRACE) { tr[4] = (uint64_t)wa; tr[5] = (uint64_t)wb; }
+    } else if (warp >= 4) {
+        // ---- converters: warp w holds tensor-memory lanes 32 (w % 4) .. + 31 (weight rows) and
+        // quant chunk part = (w - 4) / 4 (values 16 part .. 16 part + 15 of the k-step), which is
+        // the MMA's k-slice `part` (8 columns of each term's 32)
+        const int q = warp & 3, part = (warp - 4) >> 2;
+        const int cr = q * 32 + lane;                             // weight row of this CTA's tile
+        const uint32_t rs = (uint32_t)((cr >> 1) & 3);
+        const uint32_t roff = (uint32_t)cr * kBK + (((uint32_t)part ^ rs) << 4);            // 64-byte swizzle
+        const uint32_t soff = kQ8Quants + (uint32_t)cr * 4 + (uint32_t)(part >> 1) * 2;    // its block scale
+        const uint32_t tl = tmem + ((uint32_t)(q * 32) << 16) + kQ8ACol0 + 8u * (uint32_t)part;
+        long long w_raw = 0, w_empty = 0, t_conv = 0;
+        bool ok = true;
+        for (int kb = 0; kb < nk && ok; ++kb) {
+            const int r = kb % R, a = kb % SA;
+            const long long t0 = TRACE ? clock64() : 0;
+            ok = mbar_wait(&rfull[r], (uint32_t)(kb / R) & 1u);
+            if (!ok) break;
+            const uint8_t* slot = raw + (size_t)r * kQ8Raw;
+            const uint4 v = *reinterpret_cast<const uint4*>(slot + roff);
+            const __half2 d = __half2half2(__ushort_as_half(*reinterpret_cast<const unsigned short*>(slot + soff)));
+            const long long t1 = TRACE ? clock64() : 0;
+            if (kb >= SA) ok = mbar_wait(&aempty[a], ((uint32_t)(kb / SA) & 1u) ^ 1u);
+            const long long t2 = TRACE ? clock64() : 0;
+            if (TRACE) { w_raw += t1 - t0; w_empty += t2 - t1; }
+            if (!ok) break;
+            uint32_t h[8], l[8];
+            q8x4_terms(v.x, d, h[0], h[1], l[0], l[1]);
+            q8x4_terms(v.y, d, h[2], h[3], l[2], l[3]);
+            q8x4_terms(v.z, d, h[4], h[5], l[4], l[5]);
+            q8x4_terms(v.w, d, h[6], h[7], l[6], l[7]);
+            tc_fence_after();                                  // after the wait for the stage to be free
+            tmem_st8(tl + 64u * (uint32_t)a, h);
+            tmem_st8(tl + 64u * (uint32_t)a + 32u, l);
+            asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive_local(&rempty[r]);
+                mbar_arrive_local(rank == 0 ? &afull[a] : &cfull[a]);   // the leader's own MMA barrier
+            }
+            if (TRACE) t_conv += clock64() - t2;
+        }
+        if (!ok) {
+            atomicOr(err, ERR_TIMEOUT);
+            *(volatile int*)abort_flag = 1;
+        }
+        if (TRACE && warp == 4 && lane == 0) { tr[1] = (uint64_t)w_raw; tr[2] = (uint64_t)w_empty; tr[3] = (uint64_t)t_conv; }
+    }
+    __syncwarp();
+
+    if (warp < 4) {
+        const bool have = mbar_wait(accf, 0);
+        tc_fence_after();
+        if (TRACE && threadIdx.x == 0) tr[6] = global_ns();
+        // the outputs may be read or written by the kernel before until it has ended
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+        if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;");
+        if (!have) atomicOr(err, ERR_TIMEOUT);
+        const bool live = have && !*(volatile int*)abort_flag && nk > 0;
+        q8t_epilogue<EPI>(tmem, warp, lane, tok0, T, mrow0, live, gridDim.z > 1, use_ymap ? &tmY : nullptr, Y, ldy,
+                          qe, smem, err);
+    }
+    tc_fence_before();
+    cluster_sync_all();
+    if (warp == 0)
+        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(512u));
+    if (TRACE && threadIdx.x == 0) tr[7] = global_ns();
+}
+
+__global__ void q8_scales_by_kstep_kernel(const uint32_t* __restrict__ s, int64_t rows, int64_t nk,
+                                          uint32_t* __restrict__ out) {
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;      // [row][kb] order of the source
+    if (i >= rows * nk) return;
+    const int64_t row = i / nk, kb = i % nk;
+    out[kb * rows + row] = s[i];                      // the row's scales 2 kb and 2 kb + 1 as one word
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     if (!fn) {
@@ -995,6 +1452,27 @@ bool tc_make_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols,
     return r == CUDA_SUCCESS;
 }
 
+void q8_scales_by_kstep(const __half* s, int64_t rows, int64_t K, uint32_t* out, cudaStream_t st) {
+    const int64_t n = rows * (K / kBK);
+    if (n <= 0) return;
+    q8_scales_by_kstep_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(reinterpret_cast<const uint32_t*>(s), rows,
+                                                                           K / kBK, out);
+}
+
+bool tc_make_map_q8(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int box_rows) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    if (cols % kBK != 0 || (reinterpret_cast<uintptr_t>(base) & 15) != 0) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)cols};
+    const cuuint32_t box[2] = {(cuuint32_t)kBK, (cuuint32_t)box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 int tc_token_tile(int T) { return T > 128 ? 256 : 128; }
 
 bool tc_swiglu_tn_ok(int64_t K, int64_t F) { return K % kBK == 0 && K >= kBK && F % (kTnN / 2) == 0 && F > 0; }
@@ -1027,6 +1505,36 @@ bool launch_tn2(const CUtensorMap& xmap, const CUtensorMap& wmap, const CUtensor
     cfg.numAttrs = pdl ? 1 : 0;
     return cudaLaunchKernelEx(&cfg, k, xmap, wmap, wmap_lo ? *wmap_lo : wmap, ymap ? *ymap : xmap, ymap ? 1 : 0, qe,
                               wmap_lo ? 2 : 1, K, T, M, F, Y, ldy, err, trace) == cudaSuccess;
+}
+
+// The Q8_0 pair kernel serves any token count (a ubatch of at most 128 tokens leaves the peer's
+// token rows empty: its tile reads past the ubatch and those outputs are not written). ymap: the
+// output's tensor map (tc_make_out_map) for the bulk-store epilogue, else direct stores.
+template <int EPI, bool TRACE = false>
+bool launch_tn2q8(const CUtensorMap& xmap, const CUtensorMap& qmap, const uint32_t* kscales, int K, int T, int M,
+                  int F, void* Y, int ldy, int splits, uint32_t* err, cudaStream_t st, const CUtensorMap* ymap,
+                  const TnQkv& qe, bool pdl, uint64_t* trace = nullptr) {
+    auto k = gemm_tn2q8_kernel<EPI, TRACE>;
+    static bool attr = false;
+    if (!attr) {
+        if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kQ8Smem) != cudaSuccess)
+            return false;
+        attr = true;
+    }
+    const int ntile = EPI == GEMM_EPI_SWIGLU ? F / (kTnN / 2) : M / kTnN;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * ((T + 2 * kTnRows - 1) / (2 * kTnRows)), ntile, splits);
+    cfg.blockDim = dim3(kQ8Threads);
+    cfg.dynamicSmemBytes = kQ8Smem;
+    cfg.stream = st;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = pdl ? 1 : 0;
+    const int wrows = EPI == GEMM_EPI_SWIGLU ? 2 * F : M;
+    return cudaLaunchKernelEx(&cfg, k, xmap, qmap, kscales, wrows, ymap ? *ymap : xmap, ymap ? 1 : 0, qe, K, T, M, F,
+                              Y, ldy, err, trace) == cudaSuccess;
 }
 
 template <int EPI, bool A2>
@@ -1063,8 +1571,13 @@ bool launch_tn(const CUtensorMap& xmap, const CUtensorMap* xmap_lo, const CUtens
 
 bool launch_gemm_swiglu_tn(const CUtensorMap& xmap, const CUtensorMap* xmap_lo, const CUtensorMap& wmap,
                            int K, int T, int F, void* Y, void* Y2, int ldy, uint32_t* err, cudaStream_t st,
-                           const CUtensorMap* wmap_lo, bool one_cta, const CUtensorMap* ymap, bool pdl) {
+                           const CUtensorMap* wmap_lo, bool one_cta, const CUtensorMap* ymap, bool pdl,
+                           const uint32_t* q8_scales) {
     if (T <= 0) return true;
+    if (q8_scales) {
+        if (xmap_lo || wmap_lo) return false;
+        return launch_tn2q8<GEMM_EPI_SWIGLU>(xmap, wmap, q8_scales, K, T, 0, F, Y, ldy, 1, err, st, ymap, TnQkv{}, pdl);
+    }
     if (xmap_lo)
         return launch_tn<GEMM_EPI_SWIGLU, true>(xmap, xmap_lo, wmap, wmap_lo, K, T, 0, F, Y, Y2, ldy, 1, err, st,
                                                 one_cta, nullptr, TnQkv{}, pdl);
@@ -1082,8 +1595,25 @@ int tc_tn_splits(int64_t M, int64_t K, int T, int n_sm) {
 
 bool launch_gemm_tn(const CUtensorMap& xmap, const CUtensorMap* xmap_lo, const CUtensorMap& wmap, int epi,
                     int K, int M, int T, float* Y, int ldy, int splits, uint32_t* err, cudaStream_t st,
-                    const CUtensorMap* wmap_lo, bool one_cta, const CUtensorMap* ymap, const TnQkv* qkv, bool pdl) {
+                    const CUtensorMap* wmap_lo, bool one_cta, const CUtensorMap* ymap, const TnQkv* qkv, bool pdl,
+                    const uint32_t* q8_scales) {
     if (T <= 0) return true;
+    if (q8_scales) {
+        if (xmap_lo || wmap_lo) return false;
+        switch (epi) {
+            case GEMM_EPI_QKV:
+                if (!qkv || splits != 1 || !tc_tn_qkv_ok(qkv->H, qkv->Hkv, qkv->hd)) return false;
+                return launch_tn2q8<GEMM_EPI_QKV>(xmap, wmap, q8_scales, K, T, M, 0, Y, ldy, 1, err, st, ymap, *qkv,
+                                                  pdl);
+            case GEMM_EPI_STORE:
+                return launch_tn2q8<GEMM_EPI_STORE>(xmap, wmap, q8_scales, K, T, M, 0, Y, ldy, splits, err, st, ymap,
+                                                    TnQkv{}, pdl);
+            case GEMM_EPI_ADD:
+                return launch_tn2q8<GEMM_EPI_ADD>(xmap, wmap, q8_scales, K, T, M, 0, Y, ldy, splits, err, st, ymap,
+                                                  TnQkv{}, pdl);
+        }
+        return false;
+    }
     if (epi == GEMM_EPI_QKV) {
         if (xmap_lo || !ymap || !qkv || splits != 1 || !tc_tn_qkv_ok(qkv->H, qkv->Hkv, qkv->hd)) return false;
         return launch_tn<GEMM_EPI_QKV, false>(xmap, nullptr, wmap, wmap_lo, K, T, M, 0, Y, nullptr, ldy, 1, err, st,
@@ -1116,6 +1646,23 @@ bool launch_gemm_tn2_traced(const CUtensorMap& xmap, const CUtensorMap& wmap, in
         case GEMM_EPI_SWIGLU:
             return launch_tn2<GEMM_EPI_SWIGLU, true>(xmap, wmap, nullptr, K, T, M, F, Y, ldy, 1, err, st, ymap,
                                                      TnQkv{}, trace);
+    }
+    return false;
+}
+
+bool launch_gemm_tn2q8_traced(const CUtensorMap& xmap, const CUtensorMap& qmap, const uint32_t* scales, int epi,
+                              int K, int M, int T, int F, void* Y, int ldy, int splits, uint32_t* err,
+                              cudaStream_t st, const CUtensorMap* ymap, uint64_t* trace) {
+    switch (epi) {
+        case GEMM_EPI_STORE:
+            return launch_tn2q8<GEMM_EPI_STORE, true>(xmap, qmap, scales, K, T, M, F, Y, ldy, splits, err, st, ymap,
+                                                      TnQkv{}, false, trace);
+        case GEMM_EPI_ADD:
+            return launch_tn2q8<GEMM_EPI_ADD, true>(xmap, qmap, scales, K, T, M, F, Y, ldy, splits, err, st, ymap,
+                                                    TnQkv{}, false, trace);
+        case GEMM_EPI_SWIGLU:
+            return launch_tn2q8<GEMM_EPI_SWIGLU, true>(xmap, qmap, scales, K, T, M, F, Y, ldy, 1, err, st, ymap,
+                                                       TnQkv{}, false, trace);
     }
     return false;
 }

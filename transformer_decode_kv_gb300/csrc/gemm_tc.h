@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cuda.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -59,7 +60,7 @@ bool tc_swiglu_tn_ok(int64_t K, int64_t F);
 bool launch_gemm_swiglu_tn(const CUtensorMap& xmap, const CUtensorMap* xmap_lo, const CUtensorMap& wmap,
                            int K, int T, int F, void* Y, void* Y2, int ldy, uint32_t* err, cudaStream_t st,
                            const CUtensorMap* wmap_lo = nullptr, bool one_cta = false,
-                           const CUtensorMap* ymap = nullptr, bool pdl = false);
+                           const CUtensorMap* ymap = nullptr, bool pdl = false, const uint32_t* q8_scales = nullptr);
 
 // Store / residual add with the token tile as A (two bf16 terms) and 256 weight rows as B (wmap
 // over W [M][K], box 128 rows): Y [>= T][ldy] float32 (op)= X W^T. M % 256 == 0. splits > 1
@@ -71,9 +72,21 @@ int tc_tn_splits(int64_t M, int64_t K, int T, int n_sm);
 bool launch_gemm_tn(const CUtensorMap& xmap, const CUtensorMap* xmap_lo, const CUtensorMap& wmap, int epi,
                     int K, int M, int T, float* Y, int ldy, int splits, uint32_t* err, cudaStream_t st,
                     const CUtensorMap* wmap_lo = nullptr, bool one_cta = false,
-                    const CUtensorMap* ymap = nullptr, const TnQkv* qkv = nullptr, bool pdl = false);
+                    const CUtensorMap* ymap = nullptr, const TnQkv* qkv = nullptr, bool pdl = false,
+                    const uint32_t* q8_scales = nullptr);
 // pdl: launched with programmatic dependent launch (the kernel requests its first weight tiles
 // before it waits for the kernel before it to end).
+// q8_scales: the weight is Q8_0, wmap its quants (tc_make_map_q8) and q8_scales its fp16 block
+// scales in the per-k-step layout of q8_scales_by_kstep; the two-CTA kernel dequantises each
+// k-step into exact f16 terms in shared memory (f16 activations, no wmap_lo; any token count).
+// The quant map of a Q8_0 weight [rows][cols] int8: boxes of 64 quants x box_rows rows (128; 64 for
+// the gate|up matrix of the SwiGLU epilogue), 64-byte swizzle.
+bool tc_make_map_q8(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int box_rows);
+// The fp16 block scales of a Q8_0 weight, s [rows][K / 32], in the layout the Q8_0 GEMM copies per
+// k-step: out[kb][row] = the row's two scales of values 64 kb .. 64 kb + 63 (low half first), so
+// the scales of 128 consecutive rows of one k-step are 512 contiguous bytes. K % 64 == 0; rows a
+// multiple of 4.
+void q8_scales_by_kstep(const __half* s, int64_t rows, int64_t K, uint32_t* out, cudaStream_t st);
 // Whether the Q/K/V epilogue serves these head counts (f16 operands, ymap given, one K split).
 bool tc_tn_qkv_ok(int H, int Hkv, int hd);
 
@@ -89,5 +102,10 @@ bool launch_gemm_tn2_traced(const CUtensorMap& xmap, const CUtensorMap& wmap, in
                             int F, void* Y, int ldy, int splits, uint32_t* err, cudaStream_t st,
                             const CUtensorMap* ymap, uint64_t* trace);
 int tc_tn2_blocks(int epi, int M, int T, int F, int splits);
+// The Q8_0 two-CTA kernel with per-CTA wait and conversion counters (8 values per CTA in trace,
+// see gemm_tc.cu), for tc_tn2_blocks(...) CTAs.
+bool launch_gemm_tn2q8_traced(const CUtensorMap& xmap, const CUtensorMap& qmap, const uint32_t* scales, int epi,
+                              int K, int M, int T, int F, void* Y, int ldy, int splits, uint32_t* err,
+                              cudaStream_t st, const CUtensorMap* ymap, uint64_t* trace);
 
 }  // namespace llm

@@ -69,10 +69,6 @@ void launch_kv_gather(const void* src, void* dst, const int32_t* order, int32_t 
 // programmatic dependent launch after the kernel that writes x (d of 1024 to 8192).
 void launch_rmsnorm_f16(const float* x, const int32_t* rows, int32_t R, int32_t d, const float* g,
                         float eps, void* yh, cudaStream_t st, bool pdl = false);
-// Q8_0 weight -> two f16 terms hi = f16(d * q), lo = f16(d * q - hi): exact, since d * q has at
-// most 18 significant bits (fp16 scale x 8-bit integer) and hi + lo hold 22 (within f16 range).
-void launch_q8_0_to_f16_terms(const int8_t* q, const __half* d, int64_t rows, int64_t cols, void* hi, void* lo,
-                              cudaStream_t st);
 // y[i] = f16(x[i]) for n bf16 values: exact for |x| in the f16 normal range [2^-14, 65504].
 void launch_bf16_to_f16(const void* x, int64_t n, void* y, cudaStream_t st);
 // u[t][j] = silu(g[t][j]) * up[t][j] with gu = [T][2F] (gate then up) -> u [T][F].

@@ -213,16 +213,6 @@ __global__ void kv_gather_kernel(const U* __restrict__ src, U* __restrict__ dst,
     dst[((int64_t)g * n + r) * upr + u] = o >= 0 ? src[((int64_t)g * n_src + o) * upr + u] : U{};
 }
 
-__global__ void q8_0_f16_terms_kernel(const int8_t* __restrict__ q, const __half* __restrict__ d, int64_t n,
-                                      __half* __restrict__ hi, __half* __restrict__ lo) {
-    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (i >= n) return;
-    const float w = __half2float(d[i / 32]) * (float)q[i];
-    const __half h = __float2half_rn(w);
-    hi[i] = h;
-    lo[i] = __float2half_rn(w - __half2float(h));
-}
-
 __global__ void bf16_to_f16_kernel(const __nv_bfloat16* __restrict__ x, int64_t n, __half* __restrict__ y) {
     const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (i < n) y[i] = __float2half_rn(__bfloat162float(x[i]));
@@ -398,14 +388,6 @@ void launch_rmsnorm_f16(const float* x, const int32_t* rows, int32_t R, int32_t 
         case 8192: cudaLaunchKernelEx(&cfg, rmsnorm_f16_vec_kernel<8>, x, rows, d, g, eps, y); return;
     }
     rmsnorm_kernel<__half><<<R, d >= 1024 ? 512 : 256, 0, st>>>(x, rows, d, g, eps, y, nullptr);
-}
-
-void launch_q8_0_to_f16_terms(const int8_t* q, const __half* d, int64_t rows, int64_t cols, void* hi, void* lo,
-                              cudaStream_t st) {
-    const int64_t n = rows * cols;
-    if (n <= 0) return;
-    q8_0_f16_terms_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(q, d, n, static_cast<__half*>(hi),
-                                                                        static_cast<__half*>(lo));
 }
 
 void launch_bf16_to_f16(const void* x, int64_t n, void* y, cudaStream_t st) {

@@ -57,9 +57,10 @@ struct Layer {
     CUtensorMap mgu128;      // gate|up with 128-row boxes (token-major SwiGLU GEMM)
     bool gu_tn = false;
     // f16 prefill operands: a BF16 layer's weights converted to f16 (mq, mo, mgu128, md over the
-    // copies), a Q8_0 layer's as two f16 terms (hi in those maps, lo in the *_lo maps)
+    // copies); a Q8_0 layer's quants as stored (the same maps, int8 tiles dequantised by the GEMM)
     bool f16_ready = false, q8_tc = false;
-    CUtensorMap mq_lo, mo_lo, mgu128_lo, md_lo;
+    // Q8_0: the block scales in the per-k-step layout the prefill GEMM copies
+    uint32_t *qkv_ks = nullptr, *wo_ks = nullptr, *gu_ks = nullptr, *down_ks = nullptr;
 };
 
 // Kernel classes timed by llm_debug_kernel_timing.
@@ -251,11 +252,13 @@ bool alloc_mat(llm_ctx* c, DevMat& m, int32_t type, int64_t rows, int64_t cols) 
         if (!dalloc(c, &q, (size_t)(rows * cols))) return false;
         if (!dalloc(c, &m.scales, (size_t)(rows * cols / 32))) return false;
         m.data = q;
+        c->perf.weight_device_bytes += rows * cols + rows * cols / 32 * 2;
         return true;
     }
     uint8_t* p = nullptr;
     if (!dalloc(c, &p, (size_t)(rows * cols) * type_size(type))) return false;
     m.data = p;
+    c->perf.weight_device_bytes += rows * cols * (int64_t)type_size(type);
     return true;
 }
 
@@ -540,7 +543,7 @@ bool forward_ubatch(llm_ctx* c, int32_t T, int32_t O, int32_t out_row0, int32_t 
     // store / residual add: the token-major GEMM when the weight rows come in 256-row tiles
     // (split-K with atomic adds when the tiles alone leave SMs idle), else the weight-major one
     auto tc_gemm = [&](const CUtensorMap& wm, const CUtensorMap& xm, int epi, int K, int M, void* Y,
-                       int ldy, const CUtensorMap* wlo) {
+                       int ldy, const uint32_t* q8s) {
         const CUtensorMap* xlo = f16 ? nullptr
                                : &xm == &c->m_hb[bi] ? &c->m_hb_lo
                                : &xm == &c->m_attnb[bi] ? &c->m_attnb_lo : &c->m_ub_lo;
@@ -551,7 +554,8 @@ bool forward_ubatch(llm_ctx* c, int32_t T, int32_t O, int32_t out_row0, int32_t 
                 return false;
             const CUtensorMap* ym = !f16 ? nullptr : Y == c->qkv ? &c->m_y_qkv : Y == c->x ? &c->m_y_x : nullptr;
             if (!launch_gemm_tn(xm, xlo, wm, epi, K, M, T, static_cast<float*>(Y), ldy, splits, c->d_err, st,
-                                wlo, false, ym, nullptr, pdl_pre && !(splits > 1 && epi == GEMM_EPI_STORE))) {
+                                nullptr, false, ym, nullptr, pdl_pre && !(splits > 1 && epi == GEMM_EPI_STORE),
+                                q8s)) {
                 c->err = "tensor-core GEMM launch failed";
                 return false;
             }
@@ -605,13 +609,13 @@ bool forward_ubatch(llm_ctx* c, int32_t T, int32_t O, int32_t out_row0, int32_t 
                 qe.cs = c->rope_cs; qe.slot = slot; qe.kc = kc; qe.vc = vc;
                 qe.n_ctx = c->n_ctx; qe.H = H; qe.Hkv = Hkv; qe.hd = hd;
                 if (!launch_gemm_tn(c->m_hh, nullptr, L.mq, GEMM_EPI_QKV, d, qkvw, T, c->qkv, qkvw, 1, c->d_err, st,
-                                    L.q8_tc ? &L.mq_lo : nullptr, false, &c->m_y_qkv, &qe, pdl_pre)) {
+                                    nullptr, false, &c->m_y_qkv, &qe, pdl_pre, L.q8_tc ? L.qkv_ks : nullptr)) {
                     c->err = "tensor-core GEMM launch failed";
                     return false;
                 }
             } else if (tc) {
                 if (!tc_gemm(L.mq, f16 ? c->m_hh : c->m_hb[bi], GEMM_EPI_STORE, d, qkvw, c->qkv, qkvw,
-                             L.q8_tc ? &L.mq_lo : nullptr))
+                             L.q8_tc ? L.qkv_ks : nullptr))
                     return false;
             }
             else launch_linear(L.qkv, 0, qkvw, c->h, d, T, c->qkv, qkvw, EPI_STORE, st);
@@ -677,7 +681,7 @@ bool forward_ubatch(llm_ctx* c, int32_t T, int32_t O, int32_t out_row0, int32_t 
             if (!launch_gemv_bulk(L.wo.type, g, GEPI_ADD, false, c->n_sm, st, pdl)) return bulk_fail();
         } else if (tc) {
             if (!tc_gemm(L.mo, f16 ? c->m_ah : c->m_attnb[bi], GEMM_EPI_ADD, qw, d, c->x, d,
-                         L.q8_tc ? &L.mo_lo : nullptr))
+                         L.q8_tc ? L.wo_ks : nullptr))
                 return false;
         } else {
             launch_linear(L.wo, 0, d, c->attn, qw, T, c->x, d, EPI_ADD, st);
@@ -700,8 +704,8 @@ bool forward_ubatch(llm_ctx* c, int32_t T, int32_t O, int32_t out_row0, int32_t 
             if (tc && L.gu_tn) {
                 if (!launch_gemm_swiglu_tn(f16 ? c->m_hh : c->m_hb[bi], f16 ? nullptr : &c->m_hb_lo, L.mgu128, d, T,
                                            F, c->ub, f16 ? nullptr : c->ub_lo, F, c->d_err, st,
-                                           L.q8_tc ? &L.mgu128_lo : nullptr, false, f16 ? &c->m_y_ub : nullptr,
-                                           pdl_pre)) {
+                                           nullptr, false, f16 ? &c->m_y_ub : nullptr, pdl_pre,
+                                           L.q8_tc ? L.gu_ks : nullptr)) {
                     c->err = "tensor-core GEMM launch failed";
                     return false;
                 }
@@ -717,7 +721,7 @@ bool forward_ubatch(llm_ctx* c, int32_t T, int32_t O, int32_t out_row0, int32_t 
             if (!launch_gemv_bulk(L.down.type, g, GEPI_ADD, false, c->n_sm, st, pdl)) return bulk_fail();
         } else if (tc) {
             if (!tc_gemm(L.md, f16 ? c->m_uh : c->m_ub[bi], GEMM_EPI_ADD, F, d, c->x, d,
-                         L.q8_tc ? &L.md_lo : nullptr))
+                         L.q8_tc ? L.down_ks : nullptr))
                 return false;
         } else {
             launch_linear(L.down, 0, d, c->u, F, T, c->x, d, EPI_ADD, st);
@@ -1124,22 +1128,26 @@ int llm_weights_ready(llm_ctx* c) {
               tc_shape_ok(0, d, GEMM_EPI_SWIGLU, F) && tc_shape_ok(d, F, GEMM_EPI_ADD, 0);
     // Prefill GEMMs on the token-major kernel with f16 operands when every layer's shapes allow it
     // and prefill ubatches can occur: a BF16 weight converted to f16 (exact in the f16 normal
-    // range; 2 bytes per weight of extra device memory), a Q8_0 weight as two f16 terms that hold
-    // d * q exactly (4 bytes per weight), made here once. Otherwise BF16 layers use the bf16
-    // operands (activations as two terms) on the kernels their shapes allow.
+    // range; 2 bytes per weight of extra device memory), made here once; a Q8_0 weight as stored,
+    // dequantised by the GEMM into two f16 terms that hold d * q exactly (no extra memory).
+    // Otherwise BF16 layers use the bf16 operands (activations as two terms) on the kernels their
+    // shapes allow.
     const bool tn_shapes = U > gemv_max_tokens() && tc_tn_ok(qkvw, d) && tc_tn_ok(d, qw) &&
                            tc_swiglu_tn_ok(d, F) && tc_tn_ok(d, F);
     auto f16_copy = [&](const DevMat& W, int64_t rows, int64_t cols, CUtensorMap* map) {
         uint16_t* y = nullptr;
         if (!dalloc(c, &y, (size_t)(rows * cols))) return false;
+        c->perf.weight_device_bytes += rows * cols * 2;
         launch_bf16_to_f16(W.data, rows * cols, y, c->st);
         return tc_make_map(map, y, rows, cols, 128, true);
     };
-    auto f16_terms = [&](const DevMat& W, int64_t rows, int64_t cols, CUtensorMap* hi_map, CUtensorMap* lo_map) {
-        uint16_t *hi = nullptr, *lo = nullptr;
-        if (!dalloc(c, &hi, (size_t)(rows * cols)) || !dalloc(c, &lo, (size_t)(rows * cols))) return false;
-        launch_q8_0_to_f16_terms(static_cast<const int8_t*>(W.data), W.scales, rows, cols, hi, lo, c->st);
-        return tc_make_map(hi_map, hi, rows, cols, 128, true) && tc_make_map(lo_map, lo, rows, cols, 128, true);
+    // a Q8_0 weight: the quants' tensor map, and its scales in the per-k-step layout (1/32 of a
+    // byte per weight more)
+    auto q8_ks = [&](const DevMat& W, int64_t rows, int64_t cols, CUtensorMap* map, uint32_t** ks, int box_rows) {
+        if (!dalloc(c, ks, (size_t)(rows * (cols / 64)))) return false;
+        c->perf.weight_device_bytes += rows * (cols / 64) * 4;
+        q8_scales_by_kstep(W.scales, rows, cols, *ks, c->st);
+        return tc_make_map_q8(map, W.data, rows, cols, box_rows);
     };
     bool f16 = tn_shapes;
     for (int32_t il = 0; ok && il < h.n_layer; ++il) {
@@ -1161,10 +1169,10 @@ int llm_weights_ready(llm_ctx* c) {
                  tc_make_map(&L.md, L.down.data, d, F, 128);
             L.gu_tn = ok && tc_swiglu_tn_ok(d, F) && tc_make_map(&L.mgu128, L.gu.data, 2 * F, d, 128);
         } else if (q8 && tn_shapes) {
-            L.q8_tc = L.q8_tc || (f16_terms(L.qkv, qkvw, d, &L.mq, &L.mq_lo) &&
-                                  f16_terms(L.wo, d, qw, &L.mo, &L.mo_lo) &&
-                                  f16_terms(L.gu, 2 * F, d, &L.mgu128, &L.mgu128_lo) &&
-                                  f16_terms(L.down, d, F, &L.md, &L.md_lo));
+            L.q8_tc = L.q8_tc || (q8_ks(L.qkv, qkvw, d, &L.mq, &L.qkv_ks, 128) &&
+                                  q8_ks(L.wo, d, qw, &L.mo, &L.wo_ks, 128) &&
+                                  q8_ks(L.gu, 2 * F, d, &L.mgu128, &L.gu_ks, 64) &&
+                                  q8_ks(L.down, d, F, &L.md, &L.down_ks, 128));
             ok = L.q8_tc;
             L.gu_tn = ok;
         } else {
@@ -1684,6 +1692,70 @@ int llm_debug_gemm_tn_f16(int32_t epi, const void* W, const void* W_lo, int64_t 
          cudaMemcpy(&h, err, sizeof(uint32_t), cudaMemcpyDeviceToHost) == cudaSuccess;
     cudaFree(err);
     return ok && h == 0 ? 0 : -3;
+}
+
+int llm_debug_gemm_tn_q8(int32_t epi, const void* Wq, const void* Ws, int64_t M, int64_t K, const void* X,
+                         int32_t T, float* Y, int32_t ldy, int32_t F, int32_t splits) {
+    if (!Wq || !Ws || !X || !Y || T <= 0 || epi < 0 || epi > 2 || splits < 1) return -1;
+    if ((reinterpret_cast<uintptr_t>(Ws) & 15) != 0) return -1;
+    const bool swiglu = epi == GEMM_EPI_SWIGLU;
+    if (swiglu ? (!tc_swiglu_tn_ok(K, F) || splits != 1) : !tc_tn_ok(M, K)) return -1;
+    const int64_t wrows = swiglu ? 2 * (int64_t)F : M;
+    CUtensorMap qm, xm, ym;
+    if (!tc_make_map_q8(&qm, Wq, wrows, K, swiglu ? 64 : 128) || !tc_make_map(&xm, X, T, K, 128, true)) return -1;
+    const bool use_y = tc_make_out_map(&ym, Y, T, ldy, swiglu);
+    uint32_t* err = nullptr;
+    if (cudaMalloc(&err, sizeof(uint32_t)) != cudaSuccess) return -3;
+    cudaMemset(err, 0, sizeof(uint32_t));
+    uint32_t* ks = nullptr;
+    if (cudaMalloc(&ks, sizeof(uint32_t) * (size_t)(wrows * (K / 64))) != cudaSuccess) { cudaFree(err); return -3; }
+    q8_scales_by_kstep(static_cast<const __half*>(Ws), wrows, K, ks, 0);
+    bool ok = swiglu ? launch_gemm_swiglu_tn(xm, nullptr, qm, (int)K, T, F, Y, nullptr, ldy, err, 0, nullptr, false,
+                                             use_y ? &ym : nullptr, false, ks)
+                     : launch_gemm_tn(xm, nullptr, qm, epi, (int)K, (int)M, T, Y, ldy, splits, err, 0, nullptr, false,
+                                      use_y ? &ym : nullptr, nullptr, false, ks);
+    uint32_t h = 0;
+    ok = ok && cudaDeviceSynchronize() == cudaSuccess &&
+         cudaMemcpy(&h, err, sizeof(uint32_t), cudaMemcpyDeviceToHost) == cudaSuccess;
+    cudaFree(ks);
+    cudaFree(err);
+    return ok && h == 0 ? 0 : -3;
+}
+
+int64_t llm_debug_gemm_tn_q8_trace(int32_t epi, const void* Wq, const void* Ws, int64_t M, int64_t K,
+                                   const void* X, int32_t T, float* Y, int32_t ldy, int32_t F, int32_t splits,
+                                   uint64_t* trace, int64_t cap) {
+    if (!Wq || !Ws || !X || !Y || T <= 0 || epi < 0 || epi > 2 || splits < 1) return -1;
+    if ((reinterpret_cast<uintptr_t>(Ws) & 15) != 0) return -1;
+    const bool swiglu = epi == GEMM_EPI_SWIGLU;
+    if (swiglu ? (!tc_swiglu_tn_ok(K, F) || splits != 1) : !tc_tn_ok(M, K)) return -1;
+    const int64_t n = 8 * (int64_t)tc_tn2_blocks(epi, (int)M, T, F, splits);
+    if (!trace || cap < n) return -1;
+    const int64_t wrows = swiglu ? 2 * (int64_t)F : M;
+    CUtensorMap qm, xm, ym;
+    if (!tc_make_map_q8(&qm, Wq, wrows, K, swiglu ? 64 : 128) || !tc_make_map(&xm, X, T, K, 128, true)) return -1;
+    const bool use_y = tc_make_out_map(&ym, Y, T, ldy, swiglu);
+    uint32_t* err = nullptr;
+    uint64_t* dtr = nullptr;
+    if (cudaMalloc(&err, sizeof(uint32_t)) != cudaSuccess) return -3;
+    if (cudaMalloc(&dtr, sizeof(uint64_t) * n) != cudaSuccess) { cudaFree(err); return -3; }
+    cudaMemset(err, 0, sizeof(uint32_t));
+    cudaMemset(dtr, 0, sizeof(uint64_t) * n);
+    uint32_t* ks = nullptr;
+    if (cudaMalloc(&ks, sizeof(uint32_t) * (size_t)(wrows * (K / 64))) != cudaSuccess) {
+        cudaFree(dtr); cudaFree(err); return -3;
+    }
+    q8_scales_by_kstep(static_cast<const __half*>(Ws), wrows, K, ks, 0);
+    bool ok = launch_gemm_tn2q8_traced(xm, qm, ks, epi, (int)K, (int)M, T, F, Y, ldy, splits, err, 0,
+                                       use_y ? &ym : nullptr, dtr);
+    uint32_t h = 0;
+    ok = ok && cudaDeviceSynchronize() == cudaSuccess &&
+         cudaMemcpy(&h, err, sizeof(uint32_t), cudaMemcpyDeviceToHost) == cudaSuccess &&
+         cudaMemcpy(trace, dtr, sizeof(uint64_t) * n, cudaMemcpyDeviceToHost) == cudaSuccess;
+    cudaFree(ks);
+    cudaFree(dtr);
+    cudaFree(err);
+    return ok && h == 0 ? n : -3;
 }
 
 int64_t llm_debug_gemm_tn_f16_trace(int32_t epi, const void* W, int64_t M, int64_t K, const void* X, int32_t T,
