@@ -475,9 +475,10 @@ def run_headline(args, rank, world, local_rank, stream):
                           penalty_tokens=pen, u=(i + 0.5) / n_s) < 0:
             raise RuntimeError(ctx.last_error())
     sample_us = (time.perf_counter() - t0) / n_s * 1e6
+    wdev = ctx.perf()["weight_device_bytes"]
     ctx.free()
     return dict(dec_s=dec_s, prefill_s=prefill_s, e2e_s=e2e_s, ks=ks, ks_pre=ks_pre,
-                clk=clk.summary((tw0, tw1)), sample_us=sample_us, visible=visible_cells(w, K))
+                clk=clk.summary((tw0, tw1)), sample_us=sample_us, visible=visible_cells(w, K), wdev=wdev)
 
 
 def run_extra(key, stream, peaks):
@@ -684,6 +685,7 @@ def main():
         "dtype": "bf16 weights; decode f32 activations, prefill f16 GEMM operands; f32 accumulation",
         "data": "synthetic (seeded random weights and prompt)", "config": config,
         "prefill_tok_s": pre_tps, "prefill_ms": res["prefill_s"] * 1e3,
+        "weight_device_bytes": res["wdev"],
         "sampler_us_per_call": res["sample_us"],
         "decode_step_algorithmic_bytes": step_bytes,
         "decode_hbm_gbs": step_bytes / (ms_step / 1e3) / 1e9,
