@@ -1022,31 +1022,36 @@ __device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t* v) {
                  : "memory");
 }
 
-// The transposed epilogue: warp w (< 4) holds D rows 32 w .. 32 w + 31 of this CTA (weight rows, one
-// per lane) for the pair's 256 tokens (tensor-memory columns), read 32 tokens at a time. With an
-// output map the values go through shared-memory boxes of 32 tokens x 128 bytes (128-byte
-// swizzle, written transposed: one lane per column) and bulk tensor stores, or element-wise
-// reduce-adds in L2 for the residual add and K splits; without one, direct stores.
+// The transposed epilogue, on four groups of four warps (warps 0-15: the converters are idle by
+// then): warp w holds D rows 32 (w % 4) .. + 31 of this CTA (weight rows, one per lane, the
+// tensor-memory lanes it may read), and group g = w / 4 takes the 32-token chunks g and g + 4 of the
+// pair's 256 tokens (tensor-memory columns). With an output map the values go through shared-memory
+// boxes of 32 tokens x 128 bytes (128-byte swizzle, written transposed: one lane per column) and
+// bulk tensor stores, or element-wise reduce-adds in L2 for the residual add and K splits;
+// without one, direct stores.
 template <int EPI>
 __device__ __forceinline__ void q8t_epilogue(uint32_t tmem, int warp, int lane, int tok0, int T, int mrow0,
                                              bool live, bool split, const CUtensorMap* ymap, void* Y, int ldy,
                                              const TnQkv& qe, uint8_t* stage, uint32_t* err) {
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-    const int m = mrow0 + warp * 32 + lane;                 // this lane's weight row (not SwiGLU)
+    const int q = warp & 3, grp = warp >> 2;
+    const uint32_t lane_base = (uint32_t)(q * 32) << 16;
+    const int m = mrow0 + q * 32 + lane;                    // this lane's weight row (not SwiGLU)
     const int qcols = qe.H * qe.hd, kcols = qe.Hkv * qe.hd;
     const bool rot = EPI == GEMM_EPI_QKV && mrow0 < qcols + kcols;
     const bool isq = EPI == GEMM_EPI_QKV && mrow0 < qcols;
     const bool isk = EPI == GEMM_EPI_QKV && !isq && mrow0 < qcols + kcols;
     const bool boxes = ymap != nullptr && (EPI != GEMM_EPI_QKV || isq);
     const bool reduce = EPI == GEMM_EPI_ADD || split;
-    // boxes: warp w's two 4 KB buffers (f32 outputs); SwiGLU: one 4 KB f16 box per chunk shared by
-    // warps 0 and 1, two buffers, and the exchange area for the up values
+    // boxes: warp w's two 4 KB buffers (f32 outputs); SwiGLU: per group an exchange area for the
+    // handed-over values and two 4 KB f16 boxes (one per chunk, shared by the group's warps)
     uint8_t* wbuf = stage + warp * 8192;
-    float* exf = reinterpret_cast<float*>(stage + 32768);
-    uint8_t* hbuf = stage + 32768 + 9216;                   // 1024-aligned, after the exchange area
+    float* exf = reinterpret_cast<float*>(stage + grp * 17408);
+    uint8_t* hbuf = stage + grp * 17408 + 9216;             // 1024-aligned, after the exchange area
     static_assert(2 * 64 * 17 * 4 <= 9216, "exchange area");
+    const uint32_t bar_id = 1u + (uint32_t)grp;
+    const bool leader = q == 0 && lane == 0;                // issues the group's SwiGLU box stores
 #pragma unroll 1
-    for (int b = 0; b < kTnN / 32; ++b) {
+    for (int it = 0, b = grp; b < kTnN / 32; ++it, b += 4) {
         float v[32];
         tmem_ld32(tmem + lane_base + (uint32_t)(32 * b), v);
         const int t0 = tok0 + 32 * b;
@@ -1054,15 +1059,15 @@ __device__ __forceinline__ void q8t_epilogue(uint32_t tmem, int warp, int lane, 
             // warps 0, 1 hold the gate rows of the CTA's 64 features, warps 2, 3 their up rows; the
             // gate warps take tokens 0-15 of the chunk and the up warps tokens 16-31, each handing
             // the other half of its values over through shared memory (ex [2][64 features][17])
-            const int f = (warp & 1) * 32 + lane;                    // feature within the CTA's 64
-            const bool gate = warp < 2;
+            const int f = (q & 1) * 32 + lane;                       // feature within the CTA's 64
+            const bool gate = q < 2;
             float* mine = exf + (gate ? 0 : 64 * 17);                // what this warp hands over
             float* theirs = exf + (gate ? 64 * 17 : 0);
-            if (b >= 2 && threadIdx.x == 0 && boxes) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+            if (it >= 2 && leader && boxes) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
 #pragma unroll
             for (int j = 0; j < 16; ++j) mine[f * 17 + j] = v[gate ? 16 + j : j];
-            asm volatile("bar.sync 1, 128;" ::: "memory");
-            uint8_t* box = hbuf + (b & 1) * 4096;
+            asm volatile("bar.sync %0, 128;" ::"r"(bar_id) : "memory");
+            uint8_t* box = hbuf + (it & 1) * 4096;
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
                 const int jj = gate ? j : 16 + j;                    // token within the chunk
@@ -1077,8 +1082,8 @@ __device__ __forceinline__ void q8t_epilogue(uint32_t tmem, int warp, int lane, 
                 }
             }
             if (boxes) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            asm volatile("bar.sync 1, 128;" ::: "memory");
-            if (boxes && threadIdx.x == 0 && live && t0 < T) {
+            asm volatile("bar.sync %0, 128;" ::"r"(bar_id) : "memory");
+            if (boxes && leader && live && t0 < T) {
                 tma_store_2d(ymap, box, mrow0, t0);
                 asm volatile("cp.async.bulk.commit_group;" ::: "memory");
             }
@@ -1115,8 +1120,8 @@ __device__ __forceinline__ void q8t_epilogue(uint32_t tmem, int warp, int lane, 
             continue;
         }
         if (boxes) {
-            uint8_t* box = wbuf + (b & 1) * 4096;
-            if (b >= 2 && lane == 0) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+            uint8_t* box = wbuf + (it & 1) * 4096;
+            if (it >= 2 && lane == 0) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
             __syncwarp();
 #pragma unroll
             for (int j = 0; j < 32; ++j)
@@ -1125,8 +1130,8 @@ __device__ __forceinline__ void q8t_epilogue(uint32_t tmem, int warp, int lane, 
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             __syncwarp();
             if (lane == 0 && live && t0 < T) {
-                if (reduce) tma_reduce_add_2d(ymap, box, mrow0 + warp * 32, t0);
-                else tma_store_2d(ymap, box, mrow0 + warp * 32, t0);
+                if (reduce) tma_reduce_add_2d(ymap, box, mrow0 + q * 32, t0);
+                else tma_store_2d(ymap, box, mrow0 + q * 32, t0);
                 asm volatile("cp.async.bulk.commit_group;" ::: "memory");
             }
             continue;
@@ -1365,7 +1370,7 @@ gemm_tn2q8_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
     }
     __syncwarp();
 
-    if (warp < 4) {
+    if (warp < 16) {
         const bool have = mbar_wait(accf, 0);
         tc_fence_after();
         if (TRACE && threadIdx.x == 0) tr[6] = global_ns();
