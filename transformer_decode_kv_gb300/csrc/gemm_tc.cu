@@ -481,19 +481,26 @@ __device__ __forceinline__ void tn_epilogue(uint32_t tmem, int warp, int t, int 
 // sums of several CTAs then add without atomics). Rows past T are written as zeros (a store) or
 // add nothing; a warp whose rows all lie past T writes nothing. The Q/K/V epilogue stores a Q
 // tile like a store after the rotation and writes K and V tiles straight to their cache rows.
+// half: -1 for all of the tile's columns (warp w of four), or 0 / 1 for the first or second half
+// of them (two groups of four warps; warp w reads TMEM lanes of w % 4 and stages its boxes in its
+// own shared-memory slice).
 template <int EPI>
 __device__ __forceinline__ void tn_epilogue_tma(uint32_t tmem, int warp, int lane, int trow0, int T, int f0,
                                                 bool live, bool reduce, const CUtensorMap* ymap, uint8_t* smem,
-                                                const TnQkv& qe, uint32_t* err) {
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+                                                const TnQkv& qe, uint32_t* err, int half = -1) {
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const int t = trow0 + lane;
     const bool row_ok = t < T;
     const uint32_t sw = (uint32_t)(lane & 7);
-    uint8_t* wbuf = smem + (size_t)warp * (EPI == GEMM_EPI_SWIGLU ? 8192 : 32768);
+    // column blocks [cb0, cb1) of 32 (non-SwiGLU) or gate column offsets [j0a, j0b) (SwiGLU)
+    const int cb0 = half < 0 ? 0 : half * (kTnN / 64), cb1 = half < 0 ? kTnN / 32 : cb0 + kTnN / 64;
+    const int j0a = half < 0 ? 0 : half * (kTnN / 4), j0b = half < 0 ? kTnN / 2 : j0a + kTnN / 4;
+    uint8_t* wbuf = smem + (size_t)warp * (EPI == GEMM_EPI_SWIGLU ? 8192 : (half < 0 ? 32768 : 16384)) -
+                    (EPI == GEMM_EPI_SWIGLU ? 0 : (size_t)cb0 * 4096);
     bool boxes = true;                               // whether this tile goes out through the boxes
     if (EPI == GEMM_EPI_SWIGLU) {
 #pragma unroll 1
-        for (int j0 = 0; j0 < kTnN / 2; j0 += 32) {
+        for (int j0 = j0a; j0 < j0b; j0 += 32) {
             float g[32], u[32];
             tmem_ld32(tmem + lane_base + (uint32_t)j0, g);
             tmem_ld32(tmem + lane_base + (uint32_t)(kTnN / 2 + j0), u);
@@ -524,7 +531,7 @@ __device__ __forceinline__ void tn_epilogue_tma(uint32_t tmem, int warp, int lan
             live = live && row_ok && ok;
         }
 #pragma unroll 1
-        for (int b = 0; b < kTnN / 32; ++b) {
+        for (int b = cb0; b < cb1; ++b) {
             float v[32];
             tmem_ld32(tmem + lane_base + (uint32_t)(32 * b), v);
             const int col = f0 + 32 * b;
@@ -574,10 +581,11 @@ __device__ __forceinline__ void tn_epilogue_tma(uint32_t tmem, int warp, int lan
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     __syncwarp();
     if (lane == 0 && live && trow0 < T) {
-        constexpr int nbox = EPI == GEMM_EPI_SWIGLU ? 2 : kTnN / 32;
         constexpr int bw = EPI == GEMM_EPI_SWIGLU ? 64 : 32;
+        const int bb0 = EPI == GEMM_EPI_SWIGLU ? j0a / 64 : cb0;
+        const int bb1 = EPI == GEMM_EPI_SWIGLU ? (j0b + 63) / 64 : cb1;
 #pragma unroll 1
-        for (int b = 0; b < nbox; ++b) {
+        for (int b = bb0; b < bb1; ++b) {
             if (reduce) tma_reduce_add_2d(ymap, wbuf + b * 4096, f0 + b * bw, trow0);
             else tma_store_2d(ymap, wbuf + b * 4096, f0 + b * bw, trow0);
         }
@@ -781,11 +789,13 @@ __device__ __forceinline__ void umma_commit_pair(uint64_t* bar) {
         : "memory");
 }
 
+// 256 threads: thread 0 issues TMA loads, thread 32 (leader) the MMAs; all eight warps run the
+// epilogue, warps 0-3 and 4-7 each half of the tile's columns.
 // TRACE: each CTA writes global-timer stamps (ns) to trace[8 * block + i]: 0 start, 1 set-up done,
 // 2 first stage ready (leader's MMA thread), 3 last MMA issued, 4 accumulator ready, 5 epilogue
 // done, 6 end, 7 the SM id.
 template <int EPI, bool TRACE>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(128, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
 gemm_tn2_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                 const __grid_constant__ CUtensorMap tmWlo, const __grid_constant__ CUtensorMap tmY, int use_ymap,
                 const TnQkv qe, int planes, int K, int T, int M, int F,
@@ -918,10 +928,11 @@ gemm_tn2_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
     if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;");
     if (!have) atomicOr(err, ERR_TIMEOUT);
     const bool live = have && !*(volatile int*)abort_flag && nk > 0;
+    // the epilogue on both groups of four warps, each group half of the columns
     if (use_ymap)
-        tn_epilogue_tma<EPI>(tmem, warp, lane, tm + warp * 32, T, f0, live, EPI == GEMM_EPI_ADD || gridDim.z > 1,
-                             &tmY, smem, qe, err);
-    else if (EPI != GEMM_EPI_QKV)
+        tn_epilogue_tma<EPI>(tmem, warp, lane, tm + (warp & 3) * 32, T, f0, live,
+                             EPI == GEMM_EPI_ADD || gridDim.z > 1, &tmY, smem, qe, err, warp >> 2);
+    else if (EPI != GEMM_EPI_QKV && warp < 4)
         tn_epilogue<EPI, false>(tmem, warp, tm + warp * 32 + lane, T, M, f0, live, gridDim.z > 1, Y, nullptr, ldy);
     if (TRACE) {
         __syncthreads();
@@ -1500,7 +1511,7 @@ bool launch_tn2(const CUtensorMap& xmap, const CUtensorMap& wmap, const CUtensor
     const int ntile = EPI == GEMM_EPI_SWIGLU ? F / (kTnN / 2) : M / kTnN;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * ((T + 2 * kTnRows - 1) / (2 * kTnRows)), ntile, splits);
-    cfg.blockDim = dim3(128);
+    cfg.blockDim = dim3(256);
     cfg.dynamicSmemBytes = kTn2Smem;
     cfg.stream = st;
     cudaLaunchAttribute at[1];
