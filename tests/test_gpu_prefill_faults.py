@@ -1,5 +1,6 @@
-"""The prefill path of the Llama-3-8B layer shape (2 layers, BF16, F16 cache) over a prompt of two
-512-token ubatches, where the Q/K/V GEMM's epilogue applies RoPE and writes K and V to their cache
+"""The prefill path of the Llama-3-8B layer shape (2 layers, BF16 or Q8_0 linear weights, F16
+cache) over a prompt of two 512-token ubatches, where the Q/K/V GEMM's epilogue (the two-CTA
+kernel's, or the Q8_0 kernel's transposed one) applies RoPE and writes K and V to their cache
 cells: a cell index planted past the cache for the second ubatch is caught by that epilogue's
 bounds check, llm_decode returns -3 and rolls the second ubatch back ("デコードループ",
 エラーリカバリとステートロールバック), and decoding the rest afterwards gives the logits of a run that
@@ -18,12 +19,14 @@ pytestmark = pytest.mark.gpu
 
 HP = HParams(n_layer=2, n_embd=4096, n_head=32, n_head_kv=8, head_dim=128, n_ff=14336,
              n_vocab=32000, rope_freq_base=500000.0, rms_eps=1e-5)
-KEY = "llama8b_layers2_bf16"
 RUN_TOL = 2e-3
 
 
-def test_bad_cell_in_the_fused_qkv_epilogue_rolls_back_and_resumes():
-    S.WORKLOADS[KEY] = Workload(KEY, HP, {"embd": S.BF16, "linear": S.BF16}, S.F16, n_ctx=2048,
+@pytest.mark.parametrize("wtype", ["bf16", "q8_0"])
+def test_bad_cell_in_the_fused_qkv_epilogue_rolls_back_and_resumes(wtype):
+    KEY = "llama8b_layers2_" + wtype
+    lin = S.BF16 if wtype == "bf16" else S.Q8_0
+    S.WORKLOADS[KEY] = Workload(KEY, HP, {"embd": S.BF16, "linear": lin}, S.F16, n_ctx=2048,
                                 n_seq=1, n_prompt=1024, n_batch=1024, n_ubatch=512, n_decode=2,
                                 weight_seed=3500, prompt_seed=4500)
     G.device_model.cache_clear()
