@@ -1368,7 +1368,10 @@ int32_t llm_decode(llm_ctx* c, llm_batch bt) {
         const StepGraph* sg = nullptr;
         const bool one_kernel = ok && T == 1 && c->step_ok && !c->debug;
         if (one_kernel) ok = run_step(c, O, n_out);
-        if (ok && !one_kernel && small && c->use_graphs && !c->debug) {
+        // decode ubatches (one token per attention tile: the cluster kernels, whose grid follows T)
+        // replay a captured graph per key; prefill ubatches size their attention grids from the
+        // host plan and launch directly
+        if (ok && !one_kernel && (small || max_nq <= 1) && c->use_graphs && !c->debug) {
             const uint64_t key = (uint64_t)T | ((uint64_t)O << 10) | ((uint64_t)n_out << 20) |
                                  ((uint64_t)(max_nq > 1) << 52) | ((uint64_t)c->ktime << 53) |
                                  ((uint64_t)c->dec_long << 54);
