@@ -403,6 +403,24 @@ def time_prefill(drv, stream, reps):
     return float(np.median(times))
 
 
+def max_over_ranks(times, world):
+    """Each timing's maximum over the replicas (the job's time is its slowest replica's); every rank
+    receives the same values. A single process returns its own."""
+    if world <= 1:
+        return [float(x) for x in times]
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x) for x in times], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t]
+
+
+def job_rate(units_per_replica, world, seconds):
+    """Whole-job throughput of N replicas that each processed units_per_replica in at most seconds
+    (weak scaling: the work per GPU is fixed)."""
+    return world * units_per_replica / seconds
+
+
 def run_headline(args, rank, world, local_rank, stream):
     import torch
     import torch.distributed as dist
@@ -458,10 +476,7 @@ def run_headline(args, rank, world, local_rank, stream):
         t0 = time.perf_counter()
         drv.steps(K, tok0)
         e2e_s = time.perf_counter() - t0
-    if world > 1:
-        t = torch.tensor([dec_s, prefill_s, e2e_s], dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        dec_s, prefill_s, e2e_s = float(t[0]), float(t[1]), float(t[2])
+    dec_s, prefill_s, e2e_s = max_over_ranks([dec_s, prefill_s, e2e_s], world)
 
     # ---- the device sampler chain on the last logits row (top-k 40, top-p 0.95, min-p 0.05,
     # temperature 0.8, repeat penalty 1.1 over the last 64 tokens): host call to token, per call
@@ -623,8 +638,8 @@ def main():
         return
     K = args.steps
     dec_s, ms_step = res["dec_s"], res["dec_s"] / K * 1e3
-    dec_tps = world * w.n_seq * K / dec_s
-    pre_tps = world * w.n_seq * w.n_prompt / res["prefill_s"]
+    dec_tps = job_rate(w.n_seq * K, world, dec_s)
+    pre_tps = job_rate(w.n_seq * w.n_prompt, world, res["prefill_s"])
     hbm = peaks["hbm_gbs"]
 
     # ---- decode roofline: the GEMV class's share of the graph-replayed step
@@ -694,7 +709,7 @@ def main():
         "roofline_prefill": roofline_prefill,
         "kernel_share": share,
         "clocks": res["clk"],
-        "e2e": {"value": world * w.n_seq * K / res["e2e_s"], "unit": "tok/s",
+        "e2e": {"value": job_rate(w.n_seq * K, world, res["e2e_s"]), "unit": "tok/s",
                 "h2d_bytes_per_step": 4 * w.n_seq, "d2h_bytes_per_step": 8 * w.n_seq},
         "gpu_launches": int(round(sum(v["launches"] for v in ks.values()) / K)) * K,
     }
