@@ -961,9 +961,11 @@ gemm_tn2_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
 // ([P2] "llama.cpp Architecture", Example 4 MUL_MAT over a q8_0 weight; the block format of the
 // GGUF quant types.)
 // Warps 0-3: token-tile producer (thread 0), MMA issuer (thread 32, leader CTA), quant-tile
-// producer (thread 64), then the epilogue (each warp 32 weight rows, the tensor-memory lanes it may
-// access); warps 4 and up: converters. SwiGLU: a CTA's 128 weight rows are the gate rows of 64
-// features and then their up rows, so a product's two factors are in the same CTA.
+// producer (thread 64); in the peer CTA threads 32 and 96 forward its converters' completion to
+// the leader (alternate k-steps). Warps 4-19: converters. Warps 0-15 then run the epilogue (warp w
+// holds the 32 weight rows of the tensor-memory lanes it may access, w % 4). SwiGLU: a CTA's 128
+// weight rows are the gate rows of 64 features and then their up rows, so a product's two factors
+// are in the same CTA.
 constexpr uint32_t kQ8Tok = kTn2Half;                     // 128 tokens x 64 f16: 16 KB
 constexpr int kQ8TokStages = 6;
 constexpr uint32_t kQ8Quants = 128 * kBK;                // 128 rows x 64 quants: 8 KB
